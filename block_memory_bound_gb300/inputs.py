@@ -1,0 +1,93 @@
+"""Seeded synthetic inputs for RMSNorm and RoPE.
+
+This module holds no arithmetic of either operator. It draws the inputs that the CUDA
+path and the CPU oracle both consume, so that the two are compared on identical data:
+
+* RMSNorm: ``x[rows, cols] ~ N(0, 1)``, ``w[cols] ~ N(1, 0.1)``; in the stress recipe
+  1% of the rows (chosen by a seeded permutation) are scaled by 1e3 and another,
+  disjoint 1% by 1e-4. Values are drawn in fp32 and rounded once to the storage type
+  (bf16 rounding is torch's, round to nearest even).
+* RoPE: ``x[B, S, H, D] ~ N(0, 1)`` rounded to the storage type, and fp32 tables
+  ``sin, cos [S, D/2]`` at ``angle = s * theta^(-2i/D)``, ``i = 0 .. D/2-1``, computed in
+  fp64 and rounded once to fp32 (Llama-3.2-1B uses theta = 500000).
+
+Sub-seeds: x uses ``seed*16 + 0``, w ``seed*16 + 1``, the stress-row permutation
+``seed*16 + 2`` and the RoPE input ``seed*16 + 3``. ``device`` selects where the numbers
+are drawn (torch's CPU and CUDA generators give different streams for one seed; the
+recipe is the distribution, and every comparison uses one draw for both sides).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+STORAGE = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def _gen(seed: int, k: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 16 + k)
+    return g
+
+
+def rmsnorm_inputs(rows: int, cols: int, dtype: str = "bf16", seed: int = 0,
+                   stress: bool = False, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+    """Return ``(x[rows, cols], w[cols])`` of storage type ``dtype`` on ``device``."""
+    st = STORAGE[dtype]
+    x = torch.randn(rows, cols, generator=_gen(seed, 0, device), dtype=torch.float32,
+                    device=device)
+    w = torch.randn(cols, generator=_gen(seed, 1, device), dtype=torch.float32,
+                    device=device)
+    w = w.mul_(0.1).add_(1.0)
+    if stress and rows > 0:
+        n1 = rows // 100
+        perm = torch.randperm(rows, generator=_gen(seed, 2, "cpu")).to(device)
+        if n1 > 0:
+            x[perm[:n1]] *= 1e3
+            x[perm[n1:2 * n1]] *= 1e-4
+    return x.to(st), w.to(st)
+
+
+def rope_tables(S: int, D: int, theta: float = 500000.0) -> tuple[np.ndarray, np.ndarray]:
+    """fp32 ``(sin, cos)`` tables ``[S, D/2]``: angle = s * theta^(-2i/D), drawn in fp64."""
+    half = D // 2
+    inv_freq = theta ** (-2.0 * np.arange(half, dtype=np.float64) / D)
+    angle = np.arange(S, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.sin(angle).astype(np.float32), np.cos(angle).astype(np.float32)
+
+
+def rope_inputs(B: int, S: int, H: int, D: int, dtype: str = "bf16", seed: int = 0,
+                theta: float = 500000.0, device="cpu"
+                ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Return ``(x[B, S, H, D], sin[S, D/2], cos[S, D/2])``; x of ``dtype``, tables fp32."""
+    st = STORAGE[dtype]
+    x = torch.randn(B, S, H, D, generator=_gen(seed, 3, device), dtype=torch.float32,
+                    device=device).to(st)
+    sin_t, cos_t = rope_tables(S, D, theta)
+    return x, torch.from_numpy(sin_t).to(device), torch.from_numpy(cos_t).to(device)
+
+
+def p3_style_rmsnorm_inputs(rows: int, cols: int, dtype: str = "bf16"
+                            ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Deterministic RMSNorm case in the style of the xserv unit tests:
+    ``x_i = ((i mod 17) - 8) * 0.1`` over the flattened matrix, ``w_j = 0.5 + (j mod 3) * 0.2``."""
+    i = torch.arange(rows * cols, dtype=torch.float32)
+    x = (((i % 17) - 8.0) * 0.1).reshape(rows, cols)
+    w = 0.5 + (torch.arange(cols, dtype=torch.float32) % 3) * 0.2
+    return x.to(STORAGE[dtype]), w.to(STORAGE[dtype])
+
+
+def to_numpy(t: torch.Tensor) -> np.ndarray:
+    """CPU copy as numpy: bf16 as ``uint16`` bit patterns, fp32 as ``float32``."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def from_numpy(a: np.ndarray) -> torch.Tensor:
+    """Inverse of :func:`to_numpy` (``uint16`` is read as bf16 bit patterns)."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a))

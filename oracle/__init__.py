@@ -1,0 +1,177 @@
+"""CPU oracle for RMSNorm forward and rotate-half RoPE (fp64, plain C++).
+
+TEST INFRASTRUCTURE ONLY: the tests, the package entry point's smoke check and the
+benchmark's CPU-baseline leg are the only callers. The product path (the CUDA library
+and its Python binding) never imports this module, and this module never imports the
+product package.
+
+The arithmetic lives in ``camp_oracle.cpp`` (see its header for the definitions and the
+passages they follow). This file only compiles that source with the host C++ compiler
+and marshals numpy arrays through ctypes. bf16 arrays are passed as ``numpy.uint16`` bit
+patterns, fp32 arrays as ``numpy.float32``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "camp_oracle.cpp")
+LIBRARY = os.path.join(_HERE, "libcamp_oracle.so")
+
+# Storage-type codes understood by the oracle's C entry points.
+F32 = 1
+BF16 = 3
+
+# -ffp-contract=off: no fused multiply-add may change a result between x86-64 and aarch64.
+CXXFLAGS = ["-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", "-ffp-contract=off",
+            "-fno-fast-math", "-Wall", "-Wextra"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(source: str = SOURCE, output: str = LIBRARY, force: bool = False) -> str:
+    """Compile the oracle into a shared library (skipped when it is up to date)."""
+    if (not force and os.path.exists(output)
+            and os.path.getmtime(output) >= os.path.getmtime(source)):
+        return output
+    cxx = os.environ.get("CXX", "g++")
+    tmp = output + f".tmp{os.getpid()}"
+    subprocess.run([cxx, *CXXFLAGS, source, "-o", tmp], check=True)
+    os.replace(tmp, output)
+    return output
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    i64, vp, dbl, c_int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double, ctypes.c_int
+    lib.oracle_bf16_round.argtypes = [dbl]
+    lib.oracle_bf16_round.restype = ctypes.c_uint16
+    lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_value.restype = dbl
+    lib.oracle_threads_available.argtypes = []
+    lib.oracle_threads_available.restype = c_int
+    lib.oracle_rmsnorm_f64.argtypes = [vp, vp, vp, i64, i64, dbl]
+    lib.oracle_rmsnorm_f64.restype = c_int
+    lib.oracle_rmsnorm.argtypes = [vp, vp, vp, i64, i64, dbl, c_int, c_int]
+    lib.oracle_rmsnorm.restype = c_int
+    lib.oracle_rope_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64]
+    lib.oracle_rope_f64.restype = c_int
+    lib.oracle_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, c_int]
+    lib.oracle_rope.restype = c_int
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Build (if needed) and load the oracle library. ``path`` loads another build."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _storage(dtype: str) -> tuple[int, type]:
+    if dtype == "bf16":
+        return BF16, np.uint16
+    if dtype == "f32":
+        return F32, np.float32
+    raise ValueError(f"unknown storage type {dtype!r}")
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"{what}: oracle returned status {rc}")
+
+
+def threads_available(lib: ctypes.CDLL | None = None) -> int:
+    return (lib or load()).oracle_threads_available()
+
+
+def bf16_round(values, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """fp64 values -> bf16 bit patterns, rounded once to nearest, ties to even."""
+    lib = lib or load()
+    v = np.asarray(values, dtype=np.float64).ravel()
+    out = np.fromiter((lib.oracle_bf16_round(float(t)) for t in v), dtype=np.uint16,
+                      count=v.size)
+    return out.reshape(np.shape(values))
+
+
+def bf16_value(bits, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """bf16 bit patterns -> their exact values as fp64."""
+    lib = lib or load()
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    out = np.fromiter((lib.oracle_bf16_value(int(t)) for t in b), dtype=np.float64,
+                      count=b.size)
+    return out.reshape(np.shape(bits))
+
+
+def rmsnorm_f64(x, w, eps: float, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Unrounded fp64 RMSNorm of fp64 ``x[rows, cols]`` with weight ``w[cols]``."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    rows, cols = x.shape
+    assert w.shape == (cols,)
+    y = np.empty_like(x)
+    _check(lib.oracle_rmsnorm_f64(_ptr(x), _ptr(w), _ptr(y), rows, cols, float(eps)),
+           "rmsnorm_f64")
+    return y
+
+
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float, dtype: str, nthreads: int = 0,
+            lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """RMSNorm of storage-typed ``x[rows, cols]``, ``w[cols]``: fp64 inside, one rounding."""
+    lib = lib or load()
+    code, npt = _storage(dtype)
+    x = np.ascontiguousarray(x)
+    w = np.ascontiguousarray(w)
+    assert x.dtype == npt and w.dtype == npt, (x.dtype, w.dtype, dtype)
+    rows, cols = x.shape
+    assert w.shape == (cols,)
+    y = np.empty_like(x)
+    _check(lib.oracle_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, cols, float(eps), code,
+                              int(nthreads)), "rmsnorm")
+    return y
+
+
+def rope_f64(x, sin_t, cos_t, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Unrounded fp64 rotate-half RoPE of ``x[B, S, H, D]`` with tables ``[S, D/2]``."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    sin_t = np.ascontiguousarray(sin_t, dtype=np.float64)
+    cos_t = np.ascontiguousarray(cos_t, dtype=np.float64)
+    B, S, H, D = x.shape
+    assert sin_t.shape == (S, D // 2) and cos_t.shape == (S, D // 2)
+    y = np.empty_like(x)
+    _check(lib.oracle_rope_f64(_ptr(x), _ptr(sin_t), _ptr(cos_t), _ptr(y), B, S, H, D),
+           "rope_f64")
+    return y
+
+
+def rope(x: np.ndarray, sin_t: np.ndarray, cos_t: np.ndarray, dtype: str,
+         nthreads: int = 0, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Rotate-half RoPE of storage-typed ``x[B, S, H, D]`` with fp32 tables ``[S, D/2]``."""
+    lib = lib or load()
+    code, npt = _storage(dtype)
+    x = np.ascontiguousarray(x)
+    sin_t = np.ascontiguousarray(sin_t, dtype=np.float32)
+    cos_t = np.ascontiguousarray(cos_t, dtype=np.float32)
+    assert x.dtype == npt
+    B, S, H, D = x.shape
+    assert sin_t.shape == (S, D // 2) and cos_t.shape == (S, D // 2)
+    y = np.empty_like(x)
+    _check(lib.oracle_rope(_ptr(x), _ptr(sin_t), _ptr(cos_t), _ptr(y), B, S, H, D, code,
+                           int(nthreads)), "rope")
+    return y

@@ -1,0 +1,268 @@
+// CPU oracle for RMSNorm forward and rotate-half RoPE: plain, slow, fp64.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing on the product path may include, link, load or
+// call this file. Its callers are the tests, the smoke check of the package entry
+// point and the CPU-baseline leg of the benchmark. It shares no header, helper,
+// table or constant with the CUDA library: the only thing the two sides share is
+// the seeded input data.
+//
+// What it computes (the plain definitions, in fp64, rounded once at the end):
+//
+//   RMSNorm  (xserv "phase 4" design notes, RMSNorm section: rms = sqrt(sum(x^2)/hidden
+//            + eps), y = x / rms * gamma; gollamago README, "RMSNorm optimisation":
+//            accumulate and scale in fp32 or wider, round once on write-back)
+//       ss_r  = sum_j x[r,j]^2                  (Neumaier-compensated fp64 sum)
+//       rms_r = sqrt(ss_r / cols + eps)
+//       y[r,j] = x[r,j] / rms_r * w[j]          then one rounding to the storage type
+//
+//   RoPE, rotate-half  (gollamago README, "RoPE": rope(input, sin_table, cos_table),
+//            input [batch, sequence, heads, head_dim], tables [sequence, head_dim/2],
+//            each head split into two halves and rotated; tilelang tutorial ch. 02,
+//            exercise E13: y1 = x1 cos - x2 sin, y2 = x2 cos + x1 sin)
+//       for every (b, s, h) and i < D/2, with c = cos[s,i], sn = sin[s,i]:
+//       y[b,s,h,i]       = x[b,s,h,i] * c - x[b,s,h,i+D/2] * sn
+//       y[b,s,h,i+D/2]   = x[b,s,h,i+D/2] * c + x[b,s,h,i] * sn
+//       then one rounding to the storage type.
+//
+// Storage types: fp32 (IEEE binary32) and bf16 (the upper 16 bits of a binary32:
+// 1 sign, 8 exponent, 7 fraction bits). Decoding either to fp64 is exact. Encoding
+// rounds to nearest, ties to even (the pages are silent; this is the IEEE default).
+//
+// Build flags matter: no -ffast-math, and -ffp-contract=off so that no multiply-add
+// is fused (results must be identical on x86-64 and aarch64).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include <sched.h>
+
+namespace {
+
+constexpr int kOracleF32 = 1;
+constexpr int kOracleBF16 = 3;
+
+// ---------------------------------------------------------------- storage formats
+
+double bf16_to_double(uint16_t bits) {
+    uint32_t u = static_cast<uint32_t>(bits) << 16;
+    float f;
+    std::memcpy(&f, &u, sizeof f);
+    return static_cast<double>(f);
+}
+
+// Round an fp64 value to the nearest bf16, ties to even, directly (no detour through
+// fp32, which would round twice). Finite bf16 magnitudes are m * 2^(E-7) with integer
+// m in [128, 255] for E in [-126, 127], plus the subnormals m * 2^-133, m in [0, 127].
+uint16_t double_to_bf16(double v) {
+    const uint16_t sign = std::signbit(v) ? 0x8000u : 0x0000u;
+    if (std::isnan(v)) return static_cast<uint16_t>(sign | 0x7FC0u);
+    const double a = std::fabs(v);
+    if (std::isinf(a)) return static_cast<uint16_t>(sign | 0x7F80u);
+    if (a == 0.0) return sign;
+    int e2 = 0;
+    std::frexp(a, &e2);               // a = f * 2^e2, f in [0.5, 1)
+    int E = e2 - 1;                   // a in [2^E, 2^(E+1))
+    if (E < -126) E = -126;           // below the normal range the spacing stays 2^-133
+    const double q = std::ldexp(1.0, E - 7);   // spacing of bf16 values near a
+    const double n = a / q;                    // exact: division by a power of two
+    const double fl = std::floor(n);
+    const double frac = n - fl;                // exact
+    double m = fl;
+    if (frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0)) m = fl + 1.0;
+    const double r = m * q;                    // exact: m <= 256
+    if (r >= std::ldexp(1.0, 128)) return static_cast<uint16_t>(sign | 0x7F80u);
+    const float f = static_cast<float>(r);     // exact: every bf16 value is an fp32 value
+    uint32_t u;
+    std::memcpy(&u, &f, sizeof u);
+    return static_cast<uint16_t>(sign | (u >> 16));
+}
+
+double load_elem(const void* base, int64_t i, int dtype) {
+    if (dtype == kOracleBF16) return bf16_to_double(static_cast<const uint16_t*>(base)[i]);
+    return static_cast<double>(static_cast<const float*>(base)[i]);
+}
+
+// One rounding from fp64 to the storage type. The C++ conversion double -> float rounds
+// to nearest, ties to even, under the default floating-point environment.
+void store_elem(void* base, int64_t i, double v, int dtype) {
+    if (dtype == kOracleBF16) {
+        static_cast<uint16_t*>(base)[i] = double_to_bf16(v);
+    } else {
+        static_cast<float*>(base)[i] = static_cast<float>(v);
+    }
+}
+
+// ---------------------------------------------------------------- RMSNorm, fp64
+
+// Sum of squares with Neumaier's compensation (improved Kahan summation). Each square of
+// a bf16 or fp32 value is exact in fp64, so the only error is in the additions.
+double sum_of_squares(const double* x, int64_t n) {
+    double sum = 0.0;
+    double comp = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const double t = x[j] * x[j];
+        const double s = sum + t;
+        if (std::fabs(sum) >= std::fabs(t)) {
+            comp += (sum - s) + t;
+        } else {
+            comp += (t - s) + sum;
+        }
+        sum = s;
+    }
+    return sum + comp;
+}
+
+void rmsnorm_row(const double* x, const double* w, double* y, int64_t cols, double eps) {
+    const double ss = sum_of_squares(x, cols);
+    const double mean_sq = ss / static_cast<double>(cols);
+    const double rms = std::sqrt(mean_sq + eps);
+    for (int64_t j = 0; j < cols; ++j) {
+        y[j] = x[j] / rms * w[j];
+    }
+}
+
+// ---------------------------------------------------------------- RoPE, fp64
+
+// Rotate one head row of D = 2*half values by the table row (c[i], sn[i]).
+void rope_head(const double* x, const double* sn, const double* c, double* y, int64_t half) {
+    for (int64_t i = 0; i < half; ++i) {
+        const double x1 = x[i];
+        const double x2 = x[i + half];
+        y[i] = x1 * c[i] - x2 * sn[i];
+        y[i + half] = x2 * c[i] + x1 * sn[i];
+    }
+}
+
+// ---------------------------------------------------------------- threading
+
+int affinity_threads() {
+    cpu_set_t set;
+    CPU_ZERO(&set);
+    if (sched_getaffinity(0, sizeof set, &set) == 0) {
+        const int n = CPU_COUNT(&set);
+        if (n > 0) return n;
+    }
+    const unsigned hc = std::thread::hardware_concurrency();
+    return hc > 0 ? static_cast<int>(hc) : 1;
+}
+
+// Run body(begin, end) over [0, n) split into contiguous blocks, one per thread. The split
+// only decides which thread computes which rows; every row is computed the same way.
+template <typename Body>
+void parallel_blocks(int64_t n, int nthreads, Body body) {
+    if (nthreads <= 0) nthreads = affinity_threads();
+    if (n <= 0) return;
+    if (nthreads > n) nthreads = static_cast<int>(n);
+    if (nthreads <= 1) {
+        body(int64_t{0}, n);
+        return;
+    }
+    std::vector<std::thread> pool;
+    pool.reserve(static_cast<size_t>(nthreads));
+    for (int t = 0; t < nthreads; ++t) {
+        const int64_t b = n * t / nthreads;
+        const int64_t e = n * (t + 1) / nthreads;
+        pool.emplace_back([=] { body(b, e); });
+    }
+    for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Status: 0 on success, 1 on an invalid argument, 2 on an unknown storage type.
+
+uint16_t oracle_bf16_round(double v) { return double_to_bf16(v); }
+
+double oracle_bf16_value(uint16_t bits) { return bf16_to_double(bits); }
+
+int oracle_threads_available(void) { return affinity_threads(); }
+
+// RMSNorm over fp64 inputs, fp64 output, no rounding: x[rows, cols], w[cols], y[rows, cols].
+int oracle_rmsnorm_f64(const double* x, const double* w, double* y, int64_t rows, int64_t cols,
+                       double eps) {
+    if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
+    if (rows == 0) return 0;
+    if (!x || !w || !y) return 1;
+    for (int64_t r = 0; r < rows; ++r) {
+        rmsnorm_row(x + r * cols, w, y + r * cols, cols, eps);
+    }
+    return 0;
+}
+
+// RMSNorm over storage-typed inputs: decode exactly, compute in fp64, round once.
+// x, y: [rows, cols]; w: [cols]; all of storage type `dtype` (1 = fp32, 3 = bf16).
+// nthreads <= 0 uses every core this process may run on.
+int oracle_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int64_t cols, double eps,
+                   int dtype, int nthreads) {
+    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
+    if (rows == 0) return 0;
+    if (!x || !w || !y) return 1;
+    std::vector<double> wd(static_cast<size_t>(cols));
+    for (int64_t j = 0; j < cols; ++j) wd[j] = load_elem(w, j, dtype);
+    parallel_blocks(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        std::vector<double> xr(static_cast<size_t>(cols)), yr(static_cast<size_t>(cols));
+        for (int64_t r = r0; r < r1; ++r) {
+            for (int64_t j = 0; j < cols; ++j) xr[j] = load_elem(x, r * cols + j, dtype);
+            rmsnorm_row(xr.data(), wd.data(), yr.data(), cols, eps);
+            for (int64_t j = 0; j < cols; ++j) store_elem(y, r * cols + j, yr[j], dtype);
+        }
+    });
+    return 0;
+}
+
+// Rotate-half RoPE over fp64 inputs, fp64 output, no rounding.
+// x, y: [B, S, H, D]; sin_t, cos_t: [S, D/2].
+int oracle_rope_f64(const double* x, const double* sin_t, const double* cos_t, double* y,
+                    int64_t B, int64_t S, int64_t H, int64_t D) {
+    if (B < 0 || S < 0 || H < 0 || D <= 0 || D % 2 != 0) return 1;
+    if (B * S * H == 0) return 0;
+    if (!x || !sin_t || !cos_t || !y) return 1;
+    const int64_t half = D / 2;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t s = 0; s < S; ++s) {
+            for (int64_t h = 0; h < H; ++h) {
+                const int64_t off = ((b * S + s) * H + h) * D;
+                rope_head(x + off, sin_t + s * half, cos_t + s * half, y + off, half);
+            }
+        }
+    }
+    return 0;
+}
+
+// Rotate-half RoPE over storage-typed x/y (1 = fp32, 3 = bf16) and fp32 tables:
+// decode exactly, rotate in fp64, round once. Threads split the (b, s) positions.
+int oracle_rope(const void* x, const float* sin_t, const float* cos_t, void* y, int64_t B,
+                int64_t S, int64_t H, int64_t D, int dtype, int nthreads) {
+    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (B < 0 || S < 0 || H < 0 || D <= 0 || D % 2 != 0) return 1;
+    if (B * S * H == 0) return 0;
+    if (!x || !sin_t || !cos_t || !y) return 1;
+    const int64_t half = D / 2;
+    parallel_blocks(B * S, nthreads, [&](int64_t t0, int64_t t1) {
+        std::vector<double> xr(static_cast<size_t>(D)), yr(static_cast<size_t>(D));
+        std::vector<double> sn(static_cast<size_t>(half)), c(static_cast<size_t>(half));
+        for (int64_t t = t0; t < t1; ++t) {
+            const int64_t b = t / S;
+            const int64_t s = t - b * S;
+            for (int64_t i = 0; i < half; ++i) {
+                sn[i] = static_cast<double>(sin_t[s * half + i]);
+                c[i] = static_cast<double>(cos_t[s * half + i]);
+            }
+            for (int64_t h = 0; h < H; ++h) {
+                const int64_t off = ((b * S + s) * H + h) * D;
+                for (int64_t k = 0; k < D; ++k) xr[k] = load_elem(x, off + k, dtype);
+                rope_head(xr.data(), sn.data(), c.data(), yr.data(), half);
+                for (int64_t k = 0; k < D; ++k) store_elem(y, off + k, yr[k], dtype);
+            }
+        }
+    });
+    return 0;
+}
+
+}  // extern "C"
