@@ -1,0 +1,245 @@
+"""Python binding of libcamp's C ABI (``include/camp.h``): argument marshalling only.
+
+The functions named like the C entry points (``camp_rmsnorm``, ``camp_rope``, ...) take
+raw device pointers (ints) or torch tensors (their ``data_ptr()`` is passed), a dtype as
+``camp.BF16``/``camp.F32`` or ``"bf16"``/``"f32"``, and a stream as an int handle, a
+``torch.cuda.Stream`` or ``None`` (torch's current stream on the current device). They
+raise :class:`CampError` on any non-success status. Every step of the computation runs
+in libcamp's kernels; there is no other code path. The library is opened on first use
+and a missing library is an error, not a fallback.
+
+:func:`rmsnorm` and :func:`rope` are tensor-level conveniences on top: they check
+shapes, allocate the output with torch when none is given, and call the entry points.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(PKG, "libcamp.so")
+
+SUCCESS = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED_DTYPE = 2
+ERR_RUNTIME = 3
+ERR_NOT_SUPPORTED = 5
+
+F32 = 1
+BF16 = 3
+
+KERNEL_RMSNORM_ROWS = 1
+KERNEL_RMSNORM_WIDE = 2
+KERNEL_ROPE = 3
+
+# Every symbol include/camp.h declares.
+EXPORTS = (
+    "camp_rmsnorm", "camp_rope", "camp_status_string", "camp_last_cuda_error",
+    "camp_rmsnorm_plan", "camp_rope_plan", "camp_rmsnorm_with_plan", "camp_rope_with_plan",
+)
+
+
+class CampError(RuntimeError):
+    """A non-success status from libcamp."""
+
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        msg = f"{fn}: {status_string(status)} (status {status})"
+        if detail:
+            msg += f": {detail}"
+        super().__init__(msg)
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``camp_plan_t``."""
+    _fields_ = [
+        ("kernel", ctypes.c_int32),
+        ("vec_bytes", ctypes.c_int32),
+        ("group", ctypes.c_int32),
+        ("per_thread", ctypes.c_int32),
+        ("block", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("grid", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+    def __repr__(self) -> str:
+        return f"Plan({self.as_dict()})"
+
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+def load(path: str = LIBRARY) -> ctypes.CDLL:
+    """Open libcamp.so (once) and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libcamp.so is not built ({path}); run "
+                "`python -m block_memory_bound_gb300.build` or __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        vp, i64, f32, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+        pplan = ctypes.POINTER(Plan)
+        lib.camp_rmsnorm.argtypes = [vp, vp, vp, i64, i64, f32, c_int, vp]
+        lib.camp_rmsnorm.restype = c_int
+        lib.camp_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, vp]
+        lib.camp_rope.restype = c_int
+        lib.camp_status_string.argtypes = [c_int]
+        lib.camp_status_string.restype = ctypes.c_char_p
+        lib.camp_last_cuda_error.argtypes = []
+        lib.camp_last_cuda_error.restype = c_int
+        lib.camp_rmsnorm_plan.argtypes = [vp, vp, vp, i64, i64, c_int, pplan]
+        lib.camp_rmsnorm_plan.restype = c_int
+        lib.camp_rope_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, pplan]
+        lib.camp_rope_plan.restype = c_int
+        lib.camp_rmsnorm_with_plan.argtypes = [vp, vp, vp, i64, i64, f32, c_int, pplan, vp]
+        lib.camp_rmsnorm_with_plan.restype = c_int
+        lib.camp_rope_with_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, pplan, vp]
+        lib.camp_rope_with_plan.restype = c_int
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _ptr(a) -> int | None:
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()   # torch.Tensor
+
+
+def _dtype(d) -> int:
+    if d in (F32, BF16):
+        return d
+    if d in ("bf16", "bfloat16"):
+        return BF16
+    if d in ("f32", "fp32", "float32"):
+        return F32
+    name = str(d)
+    if name == "torch.bfloat16":
+        return BF16
+    if name == "torch.float32":
+        return F32
+    if isinstance(d, int):
+        return d   # passed through; the library rejects unknown codes
+    raise ValueError(f"unknown dtype {d!r}")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream   # torch.cuda.Stream
+
+
+def _check(fn: str, status: int) -> None:
+    if status != SUCCESS:
+        detail = ""
+        if status == ERR_RUNTIME:
+            detail = f"cudaError {load().camp_last_cuda_error()}"
+        raise CampError(fn, status, detail)
+
+
+# ------------------------------------------------------------------ C entry points
+
+def status_string(status: int) -> str:
+    return load().camp_status_string(int(status)).decode()
+
+
+camp_status_string = status_string
+
+
+def camp_last_cuda_error() -> int:
+    return load().camp_last_cuda_error()
+
+
+def camp_rmsnorm(x, w, y, rows: int, cols: int, eps: float, dtype, stream=None) -> None:
+    _check("camp_rmsnorm", load().camp_rmsnorm(
+        _ptr(x), _ptr(w), _ptr(y), int(rows), int(cols), float(eps), _dtype(dtype),
+        _stream(stream)))
+
+
+def camp_rope(x, sin, cos, y, B: int, S: int, H: int, D: int, dtype, stream=None) -> None:
+    _check("camp_rope", load().camp_rope(
+        _ptr(x), _ptr(sin), _ptr(cos), _ptr(y), int(B), int(S), int(H), int(D),
+        _dtype(dtype), _stream(stream)))
+
+
+def camp_rmsnorm_plan(x, w, y, rows: int, cols: int, dtype) -> Plan:
+    p = Plan()
+    _check("camp_rmsnorm_plan", load().camp_rmsnorm_plan(
+        _ptr(x), _ptr(w), _ptr(y), int(rows), int(cols), _dtype(dtype), ctypes.byref(p)))
+    return p
+
+
+def camp_rope_plan(x, sin, cos, y, B: int, S: int, H: int, D: int, dtype) -> Plan:
+    p = Plan()
+    _check("camp_rope_plan", load().camp_rope_plan(
+        _ptr(x), _ptr(sin), _ptr(cos), _ptr(y), int(B), int(S), int(H), int(D),
+        _dtype(dtype), ctypes.byref(p)))
+    return p
+
+
+def camp_rmsnorm_with_plan(x, w, y, rows: int, cols: int, eps: float, dtype, plan: Plan,
+                           stream=None) -> None:
+    _check("camp_rmsnorm_with_plan", load().camp_rmsnorm_with_plan(
+        _ptr(x), _ptr(w), _ptr(y), int(rows), int(cols), float(eps), _dtype(dtype),
+        ctypes.byref(plan), _stream(stream)))
+
+
+def camp_rope_with_plan(x, sin, cos, y, B: int, S: int, H: int, D: int, dtype, plan: Plan,
+                        stream=None) -> None:
+    _check("camp_rope_with_plan", load().camp_rope_with_plan(
+        _ptr(x), _ptr(sin), _ptr(cos), _ptr(y), int(B), int(S), int(H), int(D),
+        _dtype(dtype), ctypes.byref(plan), _stream(stream)))
+
+
+# ------------------------------------------------------------------ tensor conveniences
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def rmsnorm(x, w, eps: float = 1e-5, out=None, stream=None):
+    """RMSNorm over the last dimension of a contiguous CUDA tensor (bf16 or fp32)."""
+    import torch
+    _require(x.is_cuda and x.is_contiguous(), "x must be a contiguous CUDA tensor")
+    _require(w.dtype == x.dtype and w.is_contiguous() and w.numel() == x.shape[-1],
+             "w must be a contiguous [cols] tensor of x's dtype")
+    if out is None:
+        out = torch.empty_like(x)
+    _require(out.shape == x.shape and out.dtype == x.dtype and out.is_contiguous(),
+             "out must match x")
+    cols = x.shape[-1] if x.dim() > 0 else 1
+    rows = x.numel() // cols if cols else 0
+    camp_rmsnorm(x, w, out, rows, cols, eps, x.dtype, stream)
+    return out
+
+
+def rope(x, sin, cos, out=None, stream=None):
+    """Rotate-half RoPE of a contiguous CUDA tensor x[B, S, H, D] with fp32 tables [S, D/2]."""
+    import torch
+    _require(x.is_cuda and x.is_contiguous() and x.dim() == 4, "x must be contiguous [B,S,H,D]")
+    B, S, H, D = x.shape
+    for t, name in ((sin, "sin"), (cos, "cos")):
+        _require(t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == (S, D // 2),
+                 f"{name} must be a contiguous fp32 [S, D/2] tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    _require(out.shape == x.shape and out.dtype == x.dtype and out.is_contiguous(),
+             "out must match x")
+    camp_rope(x, sin, cos, out, B, S, H, D, x.dtype, stream)
+    return out

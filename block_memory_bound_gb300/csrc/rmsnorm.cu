@@ -1,0 +1,251 @@
+// RMSNorm forward kernels for sm_103a.
+//
+// Definition (xserv "phase 4" design notes, RMSNorm section): per row,
+// rms = sqrt(sum(x^2) / hidden + eps) and y = x / rms * gamma. Design constraints from
+// the gollamago README ("RMSNorm optimisation (TileLang)"): a bandwidth-bound operator
+// must read each row from global memory once (a second read "doubles the read
+// traffic") and write it once; the sum of squares and the scaling stay in fp32 and
+// the result is rounded once on write-back.
+//
+// rmsnorm_rows_kernel: a group of G threads owns one row. Each thread issues all of its
+// NV vector loads up front (16-byte accesses on the fast path), keeps the raw vectors in
+// registers, reduces its share of sum(x^2) in fp32, combines the group with a butterfly
+// warp shuffle (and, for G > 32, a small shared-memory exchange between the group's
+// warps), and then writes y from the registers. x is read from HBM exactly once; w is
+// read through the L1-cached read-only path and is shared by every row on the SM.
+//
+// rmsnorm_wide_kernel: rows wider than one CTA's registers (more than 1024 threads x 8
+// vectors) take two sweeps over x in one CTA per row; the second sweep mostly hits L2.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace camp {
+namespace {
+
+template <int G>
+struct RowsShape {
+    static constexpr int kBlock = G < 256 ? 256 : G;   // threads per CTA
+    static constexpr int kRowsPerCta = kBlock / G;
+    static constexpr int kWarpsPerRow = G / 32;
+};
+
+template <typename S, int VB, int G, int NV>
+__global__ void __launch_bounds__(RowsShape<G>::kBlock)
+rmsnorm_rows_kernel(const void* x, const void* __restrict__ w, void* y,
+                    int64_t rows, int64_t cols, float eps) {
+    static_assert(G % 32 == 0 && G <= 1024, "a row group is whole warps");
+    using Sh = RowsShape<G>;
+    using C = Codec<S, VB>;
+    constexpr int E = C::kElems;
+    constexpr int ES = Storage<S>::kBytes;
+
+    __shared__ float partial[Sh::kRowsPerCta][Sh::kWarpsPerRow];
+
+    const int g = threadIdx.x / G;       // row slot inside the CTA
+    const int t = threadIdx.x % G;       // thread inside the row group
+    const int64_t nvec = cols / E;       // vector accesses per row (cols is a multiple of E)
+    const int64_t pitch = cols * ES;     // bytes per row
+    const char* xb = static_cast<const char*>(x);
+    const char* wb = static_cast<const char*>(w);
+    char* yb = static_cast<char*>(y);
+    const float fcols = static_cast<float>(cols);
+
+    for (int64_t rb = blockIdx.x; rb * Sh::kRowsPerCta < rows; rb += gridDim.x) {
+        const int64_t row = rb * Sh::kRowsPerCta + g;
+        const bool active = row < rows;
+        const char* xr = xb + row * pitch;
+
+        // One sweep of loads: everything this thread needs is in flight at once.
+        Raw<VB> v[NV];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int64_t idx = static_cast<int64_t>(k) * G + t;
+            v[k] = (active && idx < nvec) ? ld_stream<VB>(xr + idx * VB) : raw_zero<VB>();
+        }
+
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            float f[E];
+            C::unpack(v[k], f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+        ss = warp_sum(ss);
+        if constexpr (Sh::kWarpsPerRow > 1) {
+            if ((threadIdx.x & 31) == 0) partial[g][t / 32] = ss;
+            __syncthreads();
+            ss = 0.0f;
+#pragma unroll
+            for (int i = 0; i < Sh::kWarpsPerRow; ++i) ss += partial[g][i];
+        }
+        const float rinv = rsqrtf(ss / fcols + eps);
+
+        if (active) {
+            char* yr = yb + row * pitch;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int64_t idx = static_cast<int64_t>(k) * G + t;
+                if (idx < nvec) {
+                    float xf[E], wf[E];
+                    C::unpack(v[k], xf);
+                    C::unpack(ld_shared_ro<VB>(wb + idx * VB), wf);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) xf[e] = (xf[e] * rinv) * wf[e];
+                    st_out<VB>(yr + idx * VB, C::pack(xf));
+                }
+            }
+        }
+        if constexpr (Sh::kWarpsPerRow > 1) __syncthreads();   // partial[] is reused
+    }
+}
+
+template <typename S, int VB>
+__global__ void __launch_bounds__(kWideBlock)
+rmsnorm_wide_kernel(const void* x, const void* __restrict__ w, void* y,
+                    int64_t rows, int64_t cols, float eps) {
+    using C = Codec<S, VB>;
+    constexpr int E = C::kElems;
+    constexpr int ES = Storage<S>::kBytes;
+    constexpr int kUnroll = 4;
+    __shared__ float partial[kWideBlock / 32];
+
+    const int64_t nvec = cols / E;
+    const int64_t pitch = cols * ES;
+    const char* xb = static_cast<const char*>(x);
+    const char* wb = static_cast<const char*>(w);
+    char* yb = static_cast<char*>(y);
+    const float fcols = static_cast<float>(cols);
+
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const char* xr = xb + row * pitch;
+        float ss = 0.0f;
+        for (int64_t base = threadIdx.x; base < nvec; base += kUnroll * kWideBlock) {
+            Raw<VB> v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t idx = base + static_cast<int64_t>(u) * kWideBlock;
+                v[u] = idx < nvec ? ld_stream<VB>(xr + idx * VB) : raw_zero<VB>();
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                float f[E];
+                C::unpack(v[u], f);
+#pragma unroll
+                for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+            }
+        }
+        ss = warp_sum(ss);
+        if ((threadIdx.x & 31) == 0) partial[threadIdx.x / 32] = ss;
+        __syncthreads();
+        ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kWideBlock / 32; ++i) ss += partial[i];
+        const float rinv = rsqrtf(ss / fcols + eps);
+
+        char* yr = yb + row * pitch;
+        for (int64_t idx = threadIdx.x; idx < nvec; idx += kWideBlock) {
+            float xf[E], wf[E];
+            C::unpack(ld_stream<VB>(xr + idx * VB), xf);
+            C::unpack(ld_shared_ro<VB>(wb + idx * VB), wf);
+#pragma unroll
+            for (int e = 0; e < E; ++e) xf[e] = (xf[e] * rinv) * wf[e];
+            st_out<VB>(yr + idx * VB, C::pack(xf));
+        }
+        __syncthreads();   // partial[] is reused by the next row
+    }
+}
+
+template <typename S, int VB, int G, int NV>
+void launch_rows(const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
+    rmsnorm_rows_kernel<S, VB, G, NV><<<static_cast<unsigned>(grid), RowsShape<G>::kBlock, 0, s>>>(
+        a.x, a.w, a.y, a.rows, a.cols, a.eps);
+}
+
+template <typename S, int VB>
+void launch_wide(const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
+    rmsnorm_wide_kernel<S, VB><<<static_cast<unsigned>(grid), kWideBlock, 0, s>>>(
+        a.x, a.w, a.y, a.rows, a.cols, a.eps);
+}
+
+using RowsFn = void (*)(const RmsnormArgs&, int64_t, cudaStream_t);
+
+struct RowsEntry {
+    DType t;
+    int vec_bytes, group, per_thread;
+    RowsFn fn;
+};
+
+#define CAMP_ROWS(S, DT, VB, G, NV) {DType::DT, VB, G, NV, &launch_rows<S, VB, G, NV>}
+
+#define CAMP_ROWS_NV16(S, DT, G)                                                              \
+    CAMP_ROWS(S, DT, 16, G, 1), CAMP_ROWS(S, DT, 16, G, 2), CAMP_ROWS(S, DT, 16, G, 3),       \
+    CAMP_ROWS(S, DT, 16, G, 4), CAMP_ROWS(S, DT, 16, G, 6), CAMP_ROWS(S, DT, 16, G, 8)
+
+#define CAMP_ROWS_FAST(S, DT)                                                                 \
+    CAMP_ROWS_NV16(S, DT, 32), CAMP_ROWS_NV16(S, DT, 64), CAMP_ROWS_NV16(S, DT, 128),         \
+    CAMP_ROWS_NV16(S, DT, 256), CAMP_ROWS_NV16(S, DT, 512), CAMP_ROWS_NV16(S, DT, 1024)
+
+#define CAMP_ROWS_ELEM_G(S, DT, VB, G)                                                        \
+    CAMP_ROWS(S, DT, VB, G, 1), CAMP_ROWS(S, DT, VB, G, 2), CAMP_ROWS(S, DT, VB, G, 4),       \
+    CAMP_ROWS(S, DT, VB, G, 8), CAMP_ROWS(S, DT, VB, G, 16)
+
+#define CAMP_ROWS_ELEM(S, DT, VB)                                                             \
+    CAMP_ROWS_ELEM_G(S, DT, VB, 32), CAMP_ROWS_ELEM_G(S, DT, VB, 256),                        \
+    CAMP_ROWS_ELEM_G(S, DT, VB, 1024)
+
+const RowsEntry kRows[] = {
+    CAMP_ROWS_FAST(bf16_t, BF16),
+    CAMP_ROWS_FAST(f32_t, F32),
+    CAMP_ROWS_ELEM(bf16_t, BF16, 2),
+    CAMP_ROWS_ELEM(f32_t, F32, 4),
+};
+
+#undef CAMP_ROWS_ELEM
+#undef CAMP_ROWS_ELEM_G
+#undef CAMP_ROWS_FAST
+#undef CAMP_ROWS_NV16
+#undef CAMP_ROWS
+
+const RowsEntry* find_rows(DType t, int vec_bytes, int group, int per_thread) {
+    for (const RowsEntry& e : kRows) {
+        if (e.t == t && e.vec_bytes == vec_bytes && e.group == group && e.per_thread == per_thread)
+            return &e;
+    }
+    return nullptr;
+}
+
+}  // namespace
+
+int rmsnorm_rows_block(int group) { return group < 256 ? 256 : group; }
+
+bool rmsnorm_rows_compiled(DType t, int vec_bytes, int group, int per_thread) {
+    return find_rows(t, vec_bytes, group, per_thread) != nullptr;
+}
+
+bool rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
+                         const RmsnormArgs& a, int64_t grid, int block, cudaStream_t s) {
+    const RowsEntry* e = find_rows(t, vec_bytes, group, per_thread);
+    if (e == nullptr || block != rmsnorm_rows_block(group)) return false;
+    e->fn(a, grid, s);
+    return true;
+}
+
+bool rmsnorm_wide_compiled(DType t, int vec_bytes) {
+    const int es = elem_bytes(t);
+    return vec_bytes == 16 || vec_bytes == es;
+}
+
+bool rmsnorm_wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t grid,
+                         cudaStream_t s) {
+    if (t == DType::BF16) {
+        if (vec_bytes == 16) { launch_wide<bf16_t, 16>(a, grid, s); return true; }
+        if (vec_bytes == 2) { launch_wide<bf16_t, 2>(a, grid, s); return true; }
+    } else {
+        if (vec_bytes == 16) { launch_wide<f32_t, 16>(a, grid, s); return true; }
+        if (vec_bytes == 4) { launch_wide<f32_t, 4>(a, grid, s); return true; }
+    }
+    return false;
+}
+
+}  // namespace camp

@@ -1,0 +1,41 @@
+"""Algorithmic bytes and FLOPs per launch (the roofline numerators).
+
+Accounting rules (tilelang tutorial ch. 02, section 2.1): every input is read once and
+every output written once; intermediates are not counted; an elementary operation or a
+transcendental counts 1 FLOP, a multiply-add 2. The roofline time bound is
+max(bytes / bandwidth, flops / peak).
+
+The pages' own RoPE ledger (ch. 02, exercise E13) leaves the precomputed sin/cos
+tables out; the gollamago effective-bandwidth figures count only the x read and the y
+write of RMSNorm. The numbers reported here include the weight and the tables
+(``weight=True``, ``tables=True``): each is read once per launch as well.
+"""
+
+from __future__ import annotations
+
+ELEM_BYTES = {"bf16": 2, "fp16": 2, "f32": 4, "fp32": 4}
+
+
+def rmsnorm_bytes(rows: int, cols: int, dtype: str = "bf16", weight: bool = True) -> int:
+    es = ELEM_BYTES[dtype]
+    return 2 * rows * cols * es + (cols * es if weight else 0)
+
+
+def rmsnorm_flops(rows: int, cols: int) -> int:
+    # per element: square-accumulate (2) + two multiplies (2); per row: divide, add, rsqrt
+    return 4 * rows * cols + 3 * rows
+
+
+def rope_bytes(B: int, S: int, H: int, D: int, dtype: str = "bf16", tables: bool = True) -> int:
+    es = ELEM_BYTES[dtype]
+    return 2 * B * S * H * D * es + (2 * S * (D // 2) * 4 if tables else 0)
+
+
+def rope_flops(B: int, S: int, H: int, D: int) -> int:
+    # per pair: 4 multiplies + 2 add/sub = 6 FLOP, i.e. 3 FLOP per element
+    return 3 * B * S * H * D
+
+
+def time_lower_bound_s(nbytes: float, flops: float, bw_bytes_per_s: float,
+                       peak_flops: float) -> float:
+    return max(nbytes / bw_bytes_per_s, flops / peak_flops)

@@ -1,0 +1,180 @@
+/*
+ * camp.h: C ABI of libcamp, GB300 (sm_103a) kernels for two bandwidth-bound per-row
+ * operators of a Llama-style transformer block.
+ *
+ *   camp_rmsnorm  RMSNorm forward, y = x / sqrt(mean(x^2) + eps) * w.
+ *                 Definition: xserv "phase 4" design notes, RMSNorm section
+ *                 (rms = sqrt(sum(x^2)/hidden + eps); y = x / rms * gamma). Precision:
+ *                 gollamago README, "RMSNorm optimisation (TileLang)": each row is read
+ *                 from global memory once and written once, the sum of squares and the
+ *                 scaling stay in fp32, and the result is rounded once on write-back.
+ *
+ *   camp_rope     Rotate-half rotary position embedding with the signature
+ *                 rope(input, sin_table, cos_table) -> output of the gollamago README,
+ *                 section "RoPE": input [batch, sequence, heads, head_dim], tables
+ *                 [sequence, head_dim/2]; each head is split into two halves that are
+ *                 rotated in fp32 registers and written once. Pair formula: tilelang
+ *                 tutorial ch. 02, exercise E13 (y1 = x1 cos - x2 sin, y2 = x2 cos + x1 sin).
+ *
+ * Conventions shared by every entry point
+ *   - The caller owns every buffer. The library allocates no memory, keeps no per-call
+ *     state and has no workspace.
+ *   - Tensor pointers are DEVICE pointers (or managed memory) to contiguous row-major
+ *     data. A pointer need only be aligned to its element size; better-aligned pointers
+ *     (16 bytes) and row pitches that are multiples of 16 bytes take the vector path.
+ *   - `stream` is a cudaStream_t passed as void*. NULL is the legacy default stream.
+ *   - Calls are asynchronous: nothing synchronizes the device. The return value reports
+ *     argument errors and launch errors. A fault during execution surfaces later on the
+ *     stream, as with any CUDA kernel.
+ *   - Status codes follow the Intro-ops operator runtime (include/operator_runtime/api.h:
+ *     success 0, invalid argument 1, unsupported dtype 2, runtime 3, not supported 5).
+ *   - Argument errors are detected on the host before any CUDA call, so they are
+ *     reported even on a machine without a GPU.
+ */
+#ifndef CAMP_H_
+#define CAMP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define CAMP_API __declspec(dllexport)
+#else
+#define CAMP_API __attribute__((visibility("default")))
+#endif
+
+typedef enum {
+    CAMP_SUCCESS = 0,
+    CAMP_ERR_INVALID_ARG = 1,      /* a null pointer, a bad size, eps, alignment or overlap */
+    CAMP_ERR_UNSUPPORTED_DTYPE = 2,
+    CAMP_ERR_RUNTIME = 3,          /* a CUDA call failed; see camp_last_cuda_error() */
+    CAMP_ERR_NOT_SUPPORTED = 5     /* a valid request that this build cannot run */
+} camp_status_t;
+
+/* Storage types. Arithmetic is fp32 for both; bf16 is the upper half of an fp32. */
+typedef enum {
+    CAMP_DTYPE_F32 = 1,
+    CAMP_DTYPE_BF16 = 3
+} camp_dtype_t;
+
+/*
+ * RMSNorm forward over `rows` independent rows of `cols` elements.
+ *
+ *   x     [rows, cols]  input, storage type `dtype`.
+ *   w     [cols]        per-column weight (gamma), storage type `dtype`.
+ *   y     [rows, cols]  output, storage type `dtype`. y == x (in place) is allowed;
+ *                       any other overlap of y with x, and any overlap of y with w, is
+ *                       rejected.
+ *   rows  >= 0. rows == 0 is a no-op that returns CAMP_SUCCESS without touching memory.
+ *   cols  >= 1.
+ *   eps   finite and >= 0; added to mean(x^2) inside the square root.
+ *
+ * For each row r: ss = sum_j x[r,j]^2 accumulated in fp32; rinv = rsqrt(ss / cols + eps);
+ * y[r,j] = round(x[r,j] * rinv * w[j]), where the products are fp32 and round() is the
+ * single conversion to the storage type (round to nearest even).
+ *
+ * Errors: CAMP_ERR_UNSUPPORTED_DTYPE for an unknown dtype; CAMP_ERR_INVALID_ARG for a
+ * null pointer (when rows > 0), rows < 0, cols < 1, a negative or non-finite eps, a
+ * pointer not aligned to the element size, a size whose byte count overflows int64,
+ * or a forbidden overlap; CAMP_ERR_RUNTIME if the launch fails.
+ */
+CAMP_API camp_status_t camp_rmsnorm(const void* x, const void* w, void* y, int64_t rows,
+                                    int64_t cols, float eps, camp_dtype_t dtype,
+                                    void* stream);
+
+/*
+ * Rotate-half RoPE of x[B, S, H, D] with fp32 tables sin[S, D/2] and cos[S, D/2].
+ *
+ *   x     [B, S, H, D]  input, storage type `dtype`.
+ *   sin   [S, D/2]      fp32 sine table, row s used by every (b, s, h).
+ *   cos   [S, D/2]      fp32 cosine table, same layout (note the order: sin before cos).
+ *   y     [B, S, H, D]  output, storage type `dtype`. y == x (in place) is allowed; any
+ *                       other overlap of y with x, or any overlap of y with a table, is
+ *                       rejected.
+ *   B, S, H >= 0; B*S*H == 0 is a no-op returning CAMP_SUCCESS.
+ *   D     even, >= 2.
+ *
+ * For every (b, s, h) and i < D/2, with c = cos[s, i] and sn = sin[s, i]:
+ *   y[.., i]       = round(x[.., i] * c - x[.., i + D/2] * sn)
+ *   y[.., i + D/2] = round(x[.., i + D/2] * c + x[.., i] * sn)
+ * evaluated in fp32 with a compensated product (the error stays relative to the
+ * result even under cancellation) and rounded once to the storage type. The table row
+ * s is derived on the device from the row index.
+ *
+ * Errors: CAMP_ERR_UNSUPPORTED_DTYPE for an unknown dtype; CAMP_ERR_INVALID_ARG for a
+ * null pointer (when B*S*H > 0), a negative size, D odd or < 2, a misaligned pointer,
+ * a byte count that overflows int64, or a forbidden overlap; CAMP_ERR_RUNTIME if the
+ * launch fails.
+ */
+CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* cos, void* y,
+                                 int64_t B, int64_t S, int64_t H, int64_t D,
+                                 camp_dtype_t dtype, void* stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+CAMP_API const char* camp_status_string(camp_status_t status);
+
+/*
+ * The cudaError_t value behind the most recent CAMP_ERR_RUNTIME returned on the calling
+ * thread (0 if none). Reading it does not clear it.
+ */
+CAMP_API int camp_last_cuda_error(void);
+
+/* ------------------------------------------------------------------ kernel plans
+ * A plan names the kernel variant that a call with the given shapes and pointers runs.
+ * Planning is host-only arithmetic (no CUDA call), so it works without a GPU; the
+ * benchmark and the tests use it to label and to enumerate kernel variants.
+ */
+typedef enum {
+    CAMP_KERNEL_RMSNORM_ROWS = 1,   /* a group of threads per row, row held in registers */
+    CAMP_KERNEL_RMSNORM_WIDE = 2,   /* one CTA per row, two sweeps over x (very wide rows) */
+    CAMP_KERNEL_ROPE = 3            /* heads of one position share the table vectors */
+} camp_kernel_t;
+
+typedef struct {
+    int32_t kernel;        /* camp_kernel_t */
+    int32_t vec_bytes;     /* bytes per vector access of x and y: 16, 8, 4 or 2 */
+    int32_t group;         /* RMSNorm: threads per row. RoPE: heads per thread */
+    int32_t per_thread;    /* RMSNorm: vector accesses per thread per row. RoPE: unused (0) */
+    int32_t block;         /* threads per CTA */
+    int32_t reserved;
+    int64_t grid;          /* CTAs launched */
+} camp_plan_t;
+
+/*
+ * Fill *plan with the variant camp_rmsnorm would launch for these arguments. Validation
+ * is the same as camp_rmsnorm's (pointers are only inspected, never dereferenced).
+ */
+CAMP_API camp_status_t camp_rmsnorm_plan(const void* x, const void* w, const void* y,
+                                         int64_t rows, int64_t cols, camp_dtype_t dtype,
+                                         camp_plan_t* plan);
+
+/* Like camp_rmsnorm_plan, for camp_rope. */
+CAMP_API camp_status_t camp_rope_plan(const void* x, const float* sin, const float* cos,
+                                      const void* y, int64_t B, int64_t S, int64_t H,
+                                      int64_t D, camp_dtype_t dtype, camp_plan_t* plan);
+
+/*
+ * camp_rmsnorm with an explicit plan (kernel, vec_bytes, group, per_thread; block and
+ * grid are derived), for tuning sweeps and for tests that cover every compiled variant.
+ * Returns CAMP_ERR_NOT_SUPPORTED if no compiled variant matches or if the plan cannot
+ * hold the row (vec_bytes must divide the row pitch and every pointer's alignment).
+ */
+CAMP_API camp_status_t camp_rmsnorm_with_plan(const void* x, const void* w, void* y,
+                                              int64_t rows, int64_t cols, float eps,
+                                              camp_dtype_t dtype, const camp_plan_t* plan,
+                                              void* stream);
+
+/* camp_rope with an explicit plan (vec_bytes and group = heads per thread). */
+CAMP_API camp_status_t camp_rope_with_plan(const void* x, const float* sin, const float* cos,
+                                           void* y, int64_t B, int64_t S, int64_t H, int64_t D,
+                                           camp_dtype_t dtype, const camp_plan_t* plan,
+                                           void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAMP_H_ */

@@ -1,0 +1,195 @@
+"""Host-side checks of libcamp that need no GPU.
+
+The library must load on a machine without a GPU and export every symbol that
+include/camp.h declares. Argument validation and kernel planning run on the host before
+any CUDA call, so their results can be checked here with fake (never dereferenced)
+pointer values.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from block_memory_bound_gb300 import build, camp
+
+HEADER = os.path.join(build.INCLUDE, "camp.h")
+
+# Fake device addresses: 256-byte aligned and far apart, never dereferenced.
+X = 0x7F0000000000
+W = 0x7F1000000000
+Y = 0x7F2000000000
+SIN = 0x7F3000000000
+COS = 0x7F4000000000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return camp.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    text = open(HEADER).read()
+    declared = set(re.findall(r"CAMP_API\s+[^;(]*?\b(camp_\w+)\s*\(", text))
+    assert declared == set(camp.EXPORTS), declared ^ set(camp.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert camp.status_string(camp.SUCCESS) == "success"
+    assert camp.status_string(camp.ERR_INVALID_ARG) == "invalid argument"
+    assert camp.status_string(camp.ERR_UNSUPPORTED_DTYPE) == "unsupported dtype"
+    assert camp.status_string(camp.ERR_RUNTIME) == "CUDA runtime error"
+    assert camp.status_string(camp.ERR_NOT_SUPPORTED) == "not supported"
+    assert camp.status_string(42) == "unknown status"
+    assert camp.camp_last_cuda_error() == 0
+
+
+def _rms(lib, x=X, w=W, y=Y, rows=4, cols=8, eps=1e-5, dtype=camp.BF16):
+    return lib.camp_rmsnorm(x, w, y, rows, cols, ctypes.c_float(eps), dtype, None)
+
+
+def _rope(lib, x=X, s=SIN, c=COS, y=Y, B=1, S=4, H=2, D=8, dtype=camp.BF16):
+    return lib.camp_rope(x, s, c, y, B, S, H, D, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"dtype": 0}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({"dtype": 2}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({"rows": -1}, camp.ERR_INVALID_ARG),
+    ({"cols": 0}, camp.ERR_INVALID_ARG),
+    ({"cols": -5}, camp.ERR_INVALID_ARG),
+    ({"eps": -1e-5}, camp.ERR_INVALID_ARG),
+    ({"eps": math.nan}, camp.ERR_INVALID_ARG),
+    ({"eps": math.inf}, camp.ERR_INVALID_ARG),
+    ({"x": None}, camp.ERR_INVALID_ARG),
+    ({"w": None}, camp.ERR_INVALID_ARG),
+    ({"y": None}, camp.ERR_INVALID_ARG),
+    ({"x": X + 1}, camp.ERR_INVALID_ARG),                       # not element aligned
+    ({"y": Y + 2, "dtype": camp.F32}, camp.ERR_INVALID_ARG),
+    ({"y": X + 2}, camp.ERR_INVALID_ARG),                       # partial overlap with x
+    ({"y": X - 2}, camp.ERR_INVALID_ARG),
+    ({"y": W}, camp.ERR_INVALID_ARG),                           # output over the weight
+    ({"y": W - 16}, camp.ERR_INVALID_ARG),
+    ({"rows": 2**62, "cols": 2**10}, camp.ERR_INVALID_ARG),     # byte count overflows
+])
+def test_rmsnorm_argument_errors(lib, kw, status):
+    assert _rms(lib, **kw) == status
+
+
+def test_rmsnorm_empty_is_success_without_cuda(lib):
+    assert _rms(lib, rows=0) == camp.SUCCESS
+    assert _rms(lib, x=None, w=None, y=None, rows=0) == camp.SUCCESS
+    # an invalid eps is still reported for an empty call
+    assert _rms(lib, rows=0, eps=-1.0) == camp.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"dtype": 7}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({"D": 7}, camp.ERR_INVALID_ARG),
+    ({"D": 0}, camp.ERR_INVALID_ARG),
+    ({"D": -2}, camp.ERR_INVALID_ARG),
+    ({"B": -1}, camp.ERR_INVALID_ARG),
+    ({"S": -1}, camp.ERR_INVALID_ARG),
+    ({"H": -3}, camp.ERR_INVALID_ARG),
+    ({"x": None}, camp.ERR_INVALID_ARG),
+    ({"s": None}, camp.ERR_INVALID_ARG),
+    ({"c": None}, camp.ERR_INVALID_ARG),
+    ({"y": None}, camp.ERR_INVALID_ARG),
+    ({"x": X + 1}, camp.ERR_INVALID_ARG),
+    ({"s": SIN + 2}, camp.ERR_INVALID_ARG),                     # tables are fp32
+    ({"y": X + 2}, camp.ERR_INVALID_ARG),                       # partial overlap with x
+    ({"y": SIN}, camp.ERR_INVALID_ARG),                         # output over a table
+    ({"y": COS - 8}, camp.ERR_INVALID_ARG),
+    ({"B": 2**40, "S": 2**20, "H": 2**10}, camp.ERR_INVALID_ARG),
+])
+def test_rope_argument_errors(lib, kw, status):
+    assert _rope(lib, **kw) == status
+
+
+def test_rope_empty_is_success_without_cuda(lib):
+    for kw in ({"B": 0}, {"S": 0}, {"H": 0}):
+        assert _rope(lib, x=None, s=None, c=None, y=None, **kw) == camp.SUCCESS
+    assert _rope(lib, B=0, D=3) == camp.ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ planning
+
+@pytest.mark.parametrize("rows,cols,dtype,expect", [
+    # (kernel, vec_bytes, group, per_thread, block, grid)
+    (4096, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 64, 4, 256, 1024)),
+    (16384, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 16384)),
+    (4096, 3000, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 3, 256, 2048)),
+    (64, 2048, "f32", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 4, 256, 32)),
+    (1, 8, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 32, 1, 256, 1)),
+    (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 256, 16, 256, 64)),
+    (5, 65536, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 8, 1024, 5)),
+    (5, 65544, "bf16", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 5)),
+    (5, 16385, "f32", (camp.KERNEL_RMSNORM_WIDE, 4, 1024, 0, 1024, 5)),
+])
+def test_rmsnorm_plans(lib, rows, cols, dtype, expect):
+    p = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype)
+    assert (p.kernel, p.vec_bytes, p.group, p.per_thread, p.block, p.grid) == expect
+
+
+def test_rmsnorm_plan_misaligned_pointer_uses_element_accesses(lib):
+    p = camp.camp_rmsnorm_plan(X + 2, W, Y + 2, 4, 2048, "bf16")
+    assert p.vec_bytes == 2
+    p = camp.camp_rmsnorm_plan(X, W + 4, Y, 4, 2048, "f32")
+    assert p.vec_bytes == 4
+
+
+@pytest.mark.parametrize("B,S,H,D,dtype,expect", [
+    # (vec_bytes, heads per thread, grid)
+    (1, 4096, 32, 64, "bf16", (16, 4, 512)),
+    (1, 4096, 8, 64, "bf16", (16, 4, 128)),
+    (1, 65536, 32, 128, "bf16", (16, 4, 16384)),
+    (2, 3, 5, 6, "bf16", (2, 1, 1)),
+    (1, 4, 6, 12, "bf16", (4, 2, 1)),
+    (1, 4, 6, 24, "f32", (16, 2, 1)),
+])
+def test_rope_plans(lib, B, S, H, D, dtype, expect):
+    p = camp.camp_rope_plan(X, SIN, COS, Y, B, S, H, D, dtype)
+    assert p.kernel == camp.KERNEL_ROPE and p.block == 256
+    assert (p.vec_bytes, p.group, p.grid) == expect
+
+
+def test_with_plan_rejects_plans_that_do_not_fit(lib):
+    bad = [
+        camp.Plan(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=16, group=32, per_thread=1),  # too small
+        camp.Plan(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=16, group=48, per_thread=8),  # not compiled
+        camp.Plan(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=8, group=32, per_thread=8),   # not compiled
+        camp.Plan(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=3, group=32, per_thread=8),
+        camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, group=4, per_thread=0),
+        camp.Plan(kernel=99, vec_bytes=16, group=32, per_thread=8),
+    ]
+    for p in bad:
+        st = lib.camp_rmsnorm_with_plan(X, W, Y, 4, 2048, ctypes.c_float(1e-5), camp.BF16,
+                                        ctypes.byref(p), None)
+        assert st == camp.ERR_NOT_SUPPORTED, p
+    # 16-byte accesses are refused when a pointer is only element aligned
+    p = camp.Plan(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=16, group=64, per_thread=4)
+    st = lib.camp_rmsnorm_with_plan(X + 2, W, Y, 4, 2048, ctypes.c_float(1e-5), camp.BF16,
+                                    ctypes.byref(p), None)
+    assert st == camp.ERR_NOT_SUPPORTED
+    rp = camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, group=3)
+    st = lib.camp_rope_with_plan(X, SIN, COS, Y, 1, 4, 6, 64, camp.BF16, ctypes.byref(rp), None)
+    assert st == camp.ERR_NOT_SUPPORTED
+    rp = camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, group=2)
+    st = lib.camp_rope_with_plan(X, SIN, COS, Y, 1, 4, 6, 6, camp.BF16, ctypes.byref(rp), None)
+    assert st == camp.ERR_NOT_SUPPORTED        # a 3-element half is not 16-byte vectors
+
+
+def test_binding_raises_on_errors(lib):
+    with pytest.raises(camp.CampError) as e:
+        camp.camp_rmsnorm(X, W, Y, 4, 0, 1e-5, "bf16", 0)
+    assert e.value.status == camp.ERR_INVALID_ARG
+    with pytest.raises(camp.CampError) as e:
+        camp.camp_rope(X, SIN, COS, Y, 1, 4, 2, 7, "bf16", 0)
+    assert e.value.status == camp.ERR_INVALID_ARG
