@@ -33,11 +33,14 @@ BF16 = 3
 KERNEL_RMSNORM_ROWS = 1
 KERNEL_RMSNORM_WIDE = 2
 KERNEL_ROPE = 3
+KERNEL_ROPE_FLAT = 4
+KERNEL_ROPE_SPLIT = 5
 
 # Every symbol include/camp.h declares.
 EXPORTS = (
     "camp_rmsnorm", "camp_rope", "camp_status_string", "camp_last_cuda_error",
     "camp_rmsnorm_plan", "camp_rope_plan", "camp_rmsnorm_with_plan", "camp_rope_with_plan",
+    "camp_rope_qk", "camp_rope_qk_plan", "camp_rope_qk_with_plan",
 )
 
 
@@ -104,6 +107,13 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_rmsnorm_with_plan.restype = c_int
         lib.camp_rope_with_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, pplan, vp]
         lib.camp_rope_with_plan.restype = c_int
+        qk = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int]
+        lib.camp_rope_qk.argtypes = qk + [vp]
+        lib.camp_rope_qk.restype = c_int
+        lib.camp_rope_qk_plan.argtypes = qk + [pplan]
+        lib.camp_rope_qk_plan.restype = c_int
+        lib.camp_rope_qk_with_plan.argtypes = qk + [pplan, vp]
+        lib.camp_rope_qk_with_plan.restype = c_int
         _lib = lib
         return lib
 
@@ -206,6 +216,29 @@ def camp_rope_with_plan(x, sin, cos, y, B: int, S: int, H: int, D: int, dtype, p
         _dtype(dtype), ctypes.byref(plan), _stream(stream)))
 
 
+def camp_rope_qk(q, k, sin, cos, yq, yk, B: int, S: int, Hq: int, Hk: int, D: int, dtype,
+                 stream=None) -> None:
+    _check("camp_rope_qk", load().camp_rope_qk(
+        _ptr(q), _ptr(k), _ptr(sin), _ptr(cos), _ptr(yq), _ptr(yk), int(B), int(S), int(Hq),
+        int(Hk), int(D), _dtype(dtype), _stream(stream)))
+
+
+def camp_rope_qk_plan(q, k, sin, cos, yq, yk, B: int, S: int, Hq: int, Hk: int, D: int,
+                      dtype) -> Plan:
+    p = Plan()
+    _check("camp_rope_qk_plan", load().camp_rope_qk_plan(
+        _ptr(q), _ptr(k), _ptr(sin), _ptr(cos), _ptr(yq), _ptr(yk), int(B), int(S), int(Hq),
+        int(Hk), int(D), _dtype(dtype), ctypes.byref(p)))
+    return p
+
+
+def camp_rope_qk_with_plan(q, k, sin, cos, yq, yk, B: int, S: int, Hq: int, Hk: int, D: int,
+                           dtype, plan: Plan, stream=None) -> None:
+    _check("camp_rope_qk_with_plan", load().camp_rope_qk_with_plan(
+        _ptr(q), _ptr(k), _ptr(sin), _ptr(cos), _ptr(yq), _ptr(yk), int(B), int(S), int(Hq),
+        int(Hk), int(D), _dtype(dtype), ctypes.byref(plan), _stream(stream)))
+
+
 # ------------------------------------------------------------------ tensor conveniences
 
 def _require(cond: bool, msg: str) -> None:
@@ -243,3 +276,21 @@ def rope(x, sin, cos, out=None, stream=None):
              "out must match x")
     camp_rope(x, sin, cos, out, B, S, H, D, x.dtype, stream)
     return out
+
+
+def rope_qk(q, k, sin, cos, out_q=None, out_k=None, stream=None):
+    """Rotate-half RoPE of Q[B, S, Hq, D] and K[B, S, Hk, D] with shared fp32 tables, one launch."""
+    import torch
+    _require(q.is_cuda and k.is_cuda and q.is_contiguous() and k.is_contiguous()
+             and q.dim() == 4 and k.dim() == 4, "q and k must be contiguous [B,S,H,D]")
+    B, S, Hq, D = q.shape
+    _require(k.shape[0] == B and k.shape[1] == S and k.shape[3] == D and k.dtype == q.dtype,
+             "k must match q in B, S, D and dtype")
+    Hk = k.shape[2]
+    for t, name in ((sin, "sin"), (cos, "cos")):
+        _require(t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == (S, D // 2),
+                 f"{name} must be a contiguous fp32 [S, D/2] tensor")
+    out_q = torch.empty_like(q) if out_q is None else out_q
+    out_k = torch.empty_like(k) if out_k is None else out_k
+    camp_rope_qk(q, k, sin, cos, out_q, out_k, B, S, Hq, Hk, D, q.dtype, stream)
+    return out_q, out_k

@@ -18,7 +18,7 @@ using camp::DType;
 
 thread_local int g_last_cuda_error = 0;
 
-constexpr int64_t kMaxGrid = 2147483647;   // gridDim.x limit; kernels loop past it
+constexpr int64_t kMaxGrid = 2147483647;   // gridDim.x limit for the looping kernels
 
 bool dtype_ok(camp_dtype_t d) { return d == CAMP_DTYPE_F32 || d == CAMP_DTYPE_BF16; }
 
@@ -44,8 +44,10 @@ bool mul_ok(int64_t a, int64_t b, int64_t c, int64_t* n) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-camp_status_t runtime_status() {
-    const cudaError_t e = cudaGetLastError();
+// Map a launch result (and any error the runtime recorded with it) to a status.
+camp_status_t runtime_status(cudaError_t launched) {
+    const cudaError_t recorded = cudaGetLastError();   // also clears the recorded error
+    const cudaError_t e = launched != cudaSuccess ? launched : recorded;
     if (e == cudaSuccess) return CAMP_SUCCESS;
     g_last_cuda_error = static_cast<int>(e);
     return CAMP_ERR_RUNTIME;
@@ -101,47 +103,77 @@ int round_up_in(int v, const int* set, int n) {
     return -1;
 }
 
-// Fill the kernel choice for the rows kernel; falls back to the two-sweep kernel when no
-// register-resident variant can hold the row.
-void rms_plan(const RmsCall& c, camp_plan_t* p) {
-    const int vb = rms_vec_bytes(c);
+struct RowsCandidate {
+    int group, per_thread;
+    int64_t ctas, idle;
+};
+
+// Is candidate a preferred over b? Measured on GB300 (L2-cold, back-to-back launches):
+//  1. cover as many SMs as there are (min(CTAs, SM count)); this only decides tiny row
+//     counts (decode), where one row per CTA spreads the rows over the most SMs;
+//  2. 2 to 4 accesses per thread with at most 256 threads per row: below that there is
+//     too little in flight per thread, above it the row group's barrier and the
+//     1024-thread CTAs cost more than they save;
+//  3. fewest idle vector slots (a ragged last access per thread wastes issue slots);
+//  4. fewer accesses per thread (more threads, shorter serial work per thread).
+// At 4096 x 2048 this picks 128 x 2, at 4096 x 3000 128 x 3 and at 16384 x 8192 256 x 4,
+// the fastest of the compiled variants at each.
+bool rows_better(const RowsCandidate& a, const RowsCandidate& b) {
+    const int64_t sa = a.ctas < camp::kSmCount ? a.ctas : camp::kSmCount;
+    const int64_t sb = b.ctas < camp::kSmCount ? b.ctas : camp::kSmCount;
+    if (sa != sb) return sa > sb;
+    const bool ma = a.per_thread >= 2 && a.per_thread <= 4 && a.group <= 256;
+    const bool mb = b.per_thread >= 2 && b.per_thread <= 4 && b.group <= 256;
+    if (ma != mb) return ma;
+    if (a.idle != b.idle) return a.idle < b.idle;
+    return a.per_thread < b.per_thread;
+}
+
+// Choose the register-resident variant; false if no compiled variant holds the row.
+bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread) {
     const int es = camp::elem_bytes(c.t);
     const int64_t nvec = c.a.cols * es / vb;
-    *p = camp_plan_t{};
-    p->vec_bytes = vb;
-    if (vb == 16) {
-        // Smallest group that needs at most 4 accesses per thread: short rows stay on one
-        // warp (no CTA barrier), long rows spread over more warps to keep the register
-        // footprint, and hence occupancy and bytes in flight, high.
-        static const int kGroups[] = {32, 64, 128, 256, 512, 1024};
-        static const int kPer[] = {1, 2, 3, 4, 6, 8};
-        for (int g : kGroups) {
-            const int64_t nv = ceil_div(nvec, g);
-            if (nv <= 4 || (g == 1024 && nv <= 8)) {
-                p->kernel = CAMP_KERNEL_RMSNORM_ROWS;
-                p->group = g;
-                p->per_thread = round_up_in(static_cast<int>(nv), kPer, 6);
-                break;
-            }
-        }
-    } else {
-        static const int kGroups[] = {32, 256, 1024};
-        static const int kPer[] = {1, 2, 4, 8, 16};
-        for (int g : kGroups) {
-            const int64_t nv = ceil_div(nvec, g);
-            if (nv <= 16) {
-                p->kernel = CAMP_KERNEL_RMSNORM_ROWS;
-                p->group = g;
-                p->per_thread = round_up_in(static_cast<int>(nv), kPer, 5);
-                break;
-            }
-        }
+    static const int kGroupsVec[] = {32, 64, 128, 256, 512, 1024};
+    static const int kPerVec[] = {1, 2, 3, 4, 6, 8};
+    static const int kGroupsElem[] = {32, 256, 1024};
+    static const int kPerElem[] = {1, 2, 4, 8, 16};
+    const bool vec = vb == 16;
+    const int* groups = vec ? kGroupsVec : kGroupsElem;
+    const int ngroups = vec ? 6 : 3;
+    const int* pers = vec ? kPerVec : kPerElem;
+    const int npers = vec ? 6 : 5;
+    const int max_per = pers[npers - 1];
+
+    bool found = false;
+    RowsCandidate best{};
+    for (int i = 0; i < ngroups; ++i) {
+        const int g = groups[i];
+        const int64_t need = ceil_div(nvec, g);
+        if (need > max_per) continue;
+        RowsCandidate k;
+        k.group = g;
+        k.per_thread = round_up_in(static_cast<int>(need), pers, npers);
+        k.ctas = ceil_div(c.a.rows, camp::rows_block(g) / g);
+        k.idle = static_cast<int64_t>(g) * k.per_thread - nvec;
+        if (!found || rows_better(k, best)) best = k;
+        found = true;
     }
-    if (p->kernel == CAMP_KERNEL_RMSNORM_ROWS) {
-        p->block = camp::rmsnorm_rows_block(p->group);
-        const int64_t rows_per_cta = p->block / p->group;
-        const int64_t blocks = ceil_div(c.a.rows, rows_per_cta);
-        p->grid = blocks < kMaxGrid ? blocks : kMaxGrid;
+    if (!found) return false;
+    *group = best.group;
+    *per_thread = best.per_thread;
+    return true;
+}
+
+void rms_plan(const RmsCall& c, camp_plan_t* p) {
+    *p = camp_plan_t{};
+    p->vec_bytes = rms_vec_bytes(c);
+    int g = 0, nv = 0;
+    if (rms_choose_rows(c, p->vec_bytes, &g, &nv)) {
+        p->kernel = CAMP_KERNEL_RMSNORM_ROWS;
+        p->group = g;
+        p->per_thread = nv;
+        p->block = camp::rows_block(g);
+        p->grid = ceil_div(c.a.rows, p->block / g);   // one row block per CTA
     } else {
         p->kernel = CAMP_KERNEL_RMSNORM_WIDE;
         p->group = camp::kWideBlock;
@@ -163,9 +195,8 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
             return CAMP_ERR_NOT_SUPPORTED;
         const int64_t nvec = c.a.cols * es / vb;
         if (static_cast<int64_t>(in.group) * in.per_thread < nvec) return CAMP_ERR_NOT_SUPPORTED;
-        p->block = camp::rmsnorm_rows_block(in.group);
-        const int64_t blocks = ceil_div(c.a.rows, p->block / in.group);
-        p->grid = blocks < kMaxGrid ? blocks : kMaxGrid;
+        p->block = camp::rows_block(in.group);
+        p->grid = ceil_div(c.a.rows, p->block / in.group);
         return CAMP_SUCCESS;
     }
     if (in.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
@@ -180,15 +211,13 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
 }
 
 camp_status_t rms_launch(const RmsCall& c, const camp_plan_t& p, cudaStream_t s) {
-    bool ok = false;
+    cudaError_t e = cudaErrorInvalidValue;
     if (p.kernel == CAMP_KERNEL_RMSNORM_ROWS) {
-        ok = camp::rmsnorm_rows_launch(c.t, p.vec_bytes, p.group, p.per_thread, c.a, p.grid,
-                                       p.block, s);
+        e = camp::rmsnorm_rows_launch(c.t, p.vec_bytes, p.group, p.per_thread, c.a, p.grid, s);
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
-        ok = camp::rmsnorm_wide_launch(c.t, p.vec_bytes, c.a, p.grid, s);
+        e = camp::rmsnorm_wide_launch(c.t, p.vec_bytes, c.a, p.grid, s);
     }
-    if (!ok) return CAMP_ERR_NOT_SUPPORTED;
-    return runtime_status();
+    return runtime_status(e);
 }
 
 bool eps_ok(float eps) { return std::isfinite(eps) && eps >= 0.0f; }
@@ -200,34 +229,66 @@ struct RopeCall {
     DType t;
 };
 
-camp_status_t rope_validate(const void* x, const float* sin_t, const float* cos_t,
-                            const void* y, int64_t B, int64_t S, int64_t H, int64_t D,
-                            camp_dtype_t dtype, RopeCall* c, bool* empty) {
+// Checks for one tensor (H2 == 0, x2/y2 ignored) or two tensors of the same [B, S, *, D]
+// layout sharing the tables. Every output must be disjoint from every input except its
+// own input (in place), from the other output and from the tables. A single remaining
+// tensor is always put in the first slot.
+camp_status_t rope_validate(const void* x, const void* x2, const float* sin_t,
+                            const float* cos_t, const void* y, const void* y2, int64_t B,
+                            int64_t S, int64_t H, int64_t H2, int64_t D, camp_dtype_t dtype,
+                            RopeCall* c, bool* empty) {
     *empty = false;
     if (!dtype_ok(dtype)) return CAMP_ERR_UNSUPPORTED_DTYPE;
-    if (B < 0 || S < 0 || H < 0 || D < 2 || D % 2 != 0) return CAMP_ERR_INVALID_ARG;
-    if (B == 0 || S == 0 || H == 0) { *empty = true; return CAMP_SUCCESS; }
-    if (x == nullptr || sin_t == nullptr || cos_t == nullptr || y == nullptr)
-        return CAMP_ERR_INVALID_ARG;
+    if (B < 0 || S < 0 || H < 0 || H2 < 0 || D < 2 || D % 2 != 0) return CAMP_ERR_INVALID_ARG;
+    if (B == 0 || S == 0 || (H == 0 && H2 == 0)) { *empty = true; return CAMP_SUCCESS; }
+    if (sin_t == nullptr || cos_t == nullptr) return CAMP_ERR_INVALID_ARG;
+    if (H > 0 && (x == nullptr || y == nullptr)) return CAMP_ERR_INVALID_ARG;
+    if (H2 > 0 && (x2 == nullptr || y2 == nullptr)) return CAMP_ERR_INVALID_ARG;
     const DType t = to_dtype(dtype);
     const int64_t es = camp::elem_bytes(t);
-    int64_t tokens = 0, rows = 0, bytes = 0, table_bytes = 0;
-    if (!mul_ok(B, S, 1, &tokens) || !mul_ok(tokens, H, 1, &rows) || !mul_ok(rows, D, es, &bytes))
+    int64_t tokens = 0, rows = 0, rows2 = 0, bytes = 0, bytes2 = 0, table_bytes = 0;
+    if (!mul_ok(B, S, 1, &tokens) || !mul_ok(tokens, H, 1, &rows) ||
+        !mul_ok(tokens, H2, 1, &rows2) || !mul_ok(rows, D, es, &bytes) ||
+        !mul_ok(rows2, D, es, &bytes2) || !mul_ok(S, D / 2, 4, &table_bytes))
         return CAMP_ERR_INVALID_ARG;
-    if (!mul_ok(S, D / 2, 4, &table_bytes)) return CAMP_ERR_INVALID_ARG;
-    if (!aligned(x, es) || !aligned(y, es) || !aligned(sin_t, 4) || !aligned(cos_t, 4))
-        return CAMP_ERR_INVALID_ARG;
-    if (y != x && overlaps(y, bytes, x, bytes)) return CAMP_ERR_INVALID_ARG;
-    if (overlaps(y, bytes, sin_t, table_bytes) || overlaps(y, bytes, cos_t, table_bytes))
-        return CAMP_ERR_INVALID_ARG;
-    c->a.x = x;
+    if (!aligned(sin_t, 4) || !aligned(cos_t, 4)) return CAMP_ERR_INVALID_ARG;
+    if (H > 0) {
+        if (!aligned(x, es) || !aligned(y, es)) return CAMP_ERR_INVALID_ARG;
+        if (y != x && overlaps(y, bytes, x, bytes)) return CAMP_ERR_INVALID_ARG;
+        if (overlaps(y, bytes, sin_t, table_bytes) || overlaps(y, bytes, cos_t, table_bytes))
+            return CAMP_ERR_INVALID_ARG;
+    }
+    if (H2 > 0) {
+        if (!aligned(x2, es) || !aligned(y2, es)) return CAMP_ERR_INVALID_ARG;
+        if (y2 != x2 && overlaps(y2, bytes2, x2, bytes2)) return CAMP_ERR_INVALID_ARG;
+        if (overlaps(y2, bytes2, sin_t, table_bytes) || overlaps(y2, bytes2, cos_t, table_bytes))
+            return CAMP_ERR_INVALID_ARG;
+    }
+    if (H > 0 && H2 > 0) {
+        if (overlaps(y, bytes, x2, bytes2) || overlaps(y2, bytes2, x, bytes) ||
+            overlaps(y, bytes, y2, bytes2))
+            return CAMP_ERR_INVALID_ARG;
+    }
+    c->a = camp::RopeArgs{};
     c->a.sin_t = sin_t;
     c->a.cos_t = cos_t;
-    c->a.y = const_cast<void*>(y);
     c->a.tokens = tokens;
     c->a.seq = S;
-    c->a.heads = H;
     c->a.half = D / 2;
+    if (H > 0) {
+        c->a.x = x;
+        c->a.y = const_cast<void*>(y);
+        c->a.heads = H;
+        if (H2 > 0) {
+            c->a.x2 = x2;
+            c->a.y2 = const_cast<void*>(y2);
+            c->a.heads2 = H2;
+        }
+    } else {
+        c->a.x = x2;
+        c->a.y = const_cast<void*>(y2);
+        c->a.heads = H2;
+    }
     c->t = t;
     return CAMP_SUCCESS;
 }
@@ -239,46 +300,118 @@ bool rope_vec_ok(const RopeCall& c, int vb) {
     if ((c.a.half * es) % vb != 0) return false;
     const int elems = vb / es;
     const int table_align = elems * 4 < 16 ? elems * 4 : 16;
+    if (c.a.heads2 > 0 && (!aligned(c.a.x2, vb) || !aligned(c.a.y2, vb))) return false;
     return aligned(c.a.x, vb) && aligned(c.a.y, vb) && aligned(c.a.sin_t, table_align) &&
            aligned(c.a.cos_t, table_align);
 }
 
-int64_t rope_grid(const RopeCall& c, int vb, int hpt) {
+int rope_widest_vec(const RopeCall& c) {
+    static const int kVec[] = {16, 8, 4, 2};
+    for (int vb : kVec)
+        if (rope_vec_ok(c, vb)) return vb;
+    return camp::elem_bytes(c.t);   // not reached: element accesses are always legal
+}
+
+// Positions one CTA of the tiled kernel covers, or 0 if the tiled kernel cannot run
+// this shape (a position needs more than one CTA, or the sizes exceed its 32-bit math).
+int64_t rope_positions_per_cta(const RopeCall& c, int vb, int hpt) {
     const int es = camp::elem_bytes(c.t);
-    const int64_t nvh = c.a.half * es / vb;
-    const int64_t work = c.a.tokens * ceil_div(c.a.heads, hpt) * nvh;
+    if (c.a.tokens > 0xFFFFFFFFll || c.a.heads > 0x7FFFFFFFll || c.a.heads2 > 0x7FFFFFFFll ||
+        c.a.half > 0x7FFFFFFFll)
+        return 0;
+    const int64_t per_pos =
+        (ceil_div(c.a.heads, hpt) + ceil_div(c.a.heads2, hpt)) * (c.a.half * es / vb);
+    return per_pos <= camp::kRopeBlock ? camp::kRopeBlock / per_pos : 0;
+}
+
+// CTAs launched: the tiled kernel runs one position block per CTA (any count; the launch
+// uses a second grid dimension past 2^31 - 1); the flat kernel loops, so its grid is capped.
+int64_t rope_grid(const RopeCall& c, int kernel, int vb, int hpt) {
+    if (kernel == CAMP_KERNEL_ROPE) return ceil_div(c.a.tokens, rope_positions_per_cta(c, vb, hpt));
+    const int es = camp::elem_bytes(c.t);
+    const int64_t work = c.a.tokens * ceil_div(c.a.heads, hpt) * (c.a.half * es / vb);
     const int64_t blocks = ceil_div(work, camp::kRopeBlock);
     return blocks < kMaxGrid ? blocks : kMaxGrid;
 }
 
+// The second tensor of a call as a single-tensor call of its own.
+RopeCall rope_second(const RopeCall& c) {
+    RopeCall d = c;
+    d.a.x = c.a.x2;
+    d.a.y = c.a.y2;
+    d.a.heads = c.a.heads2;
+    d.a.x2 = nullptr;
+    d.a.y2 = nullptr;
+    d.a.heads2 = 0;
+    return d;
+}
+
+RopeCall rope_first(const RopeCall& c) {
+    RopeCall d = c;
+    d.a.x2 = nullptr;
+    d.a.y2 = nullptr;
+    d.a.heads2 = 0;
+    return d;
+}
+
+// Choose the RoPE variant: the widest legal vector; 2 heads per thread when every head
+// count is even, else 1 (measured on GB300, L2-cold: 2 heads per thread is the fastest or
+// within 1% of it at 4096 and 65536 positions for H in {8, 32}, D in {64, 128}); the tiled
+// kernel when a position fits one CTA. Otherwise one tensor takes the flat kernel and two
+// tensors are split into two single-tensor launches.
 void rope_plan(const RopeCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
-    p->kernel = CAMP_KERNEL_ROPE;
-    static const int kVec[] = {16, 8, 4, 2};
-    for (int vb : kVec) {
-        if (rope_vec_ok(c, vb)) { p->vec_bytes = vb; break; }
-    }
-    // Heads per thread: the largest of 4, 2, 1 that divides H, so that no thread idles.
-    p->group = (c.a.heads % 4 == 0) ? 4 : (c.a.heads % 2 == 0) ? 2 : 1;
+    p->vec_bytes = rope_widest_vec(c);
+    const bool even = c.a.heads % 2 == 0 && c.a.heads2 % 2 == 0;
+    p->group = even ? 2 : 1;
     p->per_thread = 0;
     p->block = camp::kRopeBlock;
-    p->grid = rope_grid(c, p->vec_bytes, p->group);
+    if (rope_positions_per_cta(c, p->vec_bytes, p->group) > 0) {
+        p->kernel = CAMP_KERNEL_ROPE;
+        p->grid = rope_grid(c, CAMP_KERNEL_ROPE, p->vec_bytes, p->group);
+    } else if (c.a.heads2 == 0) {
+        p->kernel = CAMP_KERNEL_ROPE_FLAT;
+        p->grid = rope_grid(c, CAMP_KERNEL_ROPE_FLAT, p->vec_bytes, p->group);
+    } else {
+        camp_plan_t p1, p2;
+        rope_plan(rope_first(c), &p1);
+        rope_plan(rope_second(c), &p2);
+        p->kernel = CAMP_KERNEL_ROPE_SPLIT;
+        p->grid = p1.grid + p2.grid;
+    }
 }
 
 camp_status_t rope_accept_plan(const RopeCall& c, const camp_plan_t& in, camp_plan_t* p) {
-    if (in.kernel != CAMP_KERNEL_ROPE) return CAMP_ERR_NOT_SUPPORTED;
+    if (in.kernel != CAMP_KERNEL_ROPE && in.kernel != CAMP_KERNEL_ROPE_FLAT)
+        return CAMP_ERR_NOT_SUPPORTED;
+    if (in.kernel == CAMP_KERNEL_ROPE_FLAT && c.a.heads2 > 0) return CAMP_ERR_NOT_SUPPORTED;
     if (!rope_vec_ok(c, in.vec_bytes)) return CAMP_ERR_NOT_SUPPORTED;
     if (!camp::rope_compiled(c.t, in.vec_bytes, in.group)) return CAMP_ERR_NOT_SUPPORTED;
+    if (in.kernel == CAMP_KERNEL_ROPE && rope_positions_per_cta(c, in.vec_bytes, in.group) == 0)
+        return CAMP_ERR_NOT_SUPPORTED;
     *p = in;
     p->per_thread = 0;
     p->block = camp::kRopeBlock;
-    p->grid = rope_grid(c, in.vec_bytes, in.group);
+    p->grid = rope_grid(c, in.kernel, in.vec_bytes, in.group);
     return CAMP_SUCCESS;
 }
 
 camp_status_t rope_launch(const RopeCall& c, const camp_plan_t& p, cudaStream_t s) {
-    if (!camp::rope_launch(c.t, p.vec_bytes, p.group, c.a, p.grid, s)) return CAMP_ERR_NOT_SUPPORTED;
-    return runtime_status();
+    if (p.kernel == CAMP_KERNEL_ROPE_SPLIT) {
+        const RopeCall parts[2] = {rope_first(c), rope_second(c)};
+        for (const RopeCall& part : parts) {
+            camp_plan_t q;
+            rope_plan(part, &q);
+            const camp_status_t st = rope_launch(part, q, s);
+            if (st != CAMP_SUCCESS) return st;
+        }
+        return CAMP_SUCCESS;
+    }
+    const cudaError_t e =
+        p.kernel == CAMP_KERNEL_ROPE
+            ? camp::rope_tiled_launch(c.t, p.vec_bytes, p.group, c.a, p.grid, s)
+            : camp::rope_flat_launch(c.t, p.vec_bytes, p.group, c.a, p.grid, s);
+    return runtime_status(e);
 }
 
 }  // namespace
@@ -349,7 +482,8 @@ CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* c
                                  camp_dtype_t dtype, void* stream) {
     RopeCall c;
     bool empty = false;
-    camp_status_t st = rope_validate(x, sin, cos, y, B, S, H, D, dtype, &c, &empty);
+    camp_status_t st =
+        rope_validate(x, nullptr, sin, cos, y, nullptr, B, S, H, 0, D, dtype, &c, &empty);
     if (st != CAMP_SUCCESS || empty) return st;
     camp_plan_t p;
     rope_plan(c, &p);
@@ -362,7 +496,8 @@ CAMP_API camp_status_t camp_rope_plan(const void* x, const float* sin, const flo
     if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
     RopeCall c;
     bool empty = false;
-    camp_status_t st = rope_validate(x, sin, cos, y, B, S, H, D, dtype, &c, &empty);
+    camp_status_t st =
+        rope_validate(x, nullptr, sin, cos, y, nullptr, B, S, H, 0, D, dtype, &c, &empty);
     if (st != CAMP_SUCCESS) return st;
     if (empty) { *plan = camp_plan_t{}; return CAMP_SUCCESS; }
     rope_plan(c, plan);
@@ -376,7 +511,51 @@ CAMP_API camp_status_t camp_rope_with_plan(const void* x, const float* sin, cons
     if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
     RopeCall c;
     bool empty = false;
-    camp_status_t st = rope_validate(x, sin, cos, y, B, S, H, D, dtype, &c, &empty);
+    camp_status_t st =
+        rope_validate(x, nullptr, sin, cos, y, nullptr, B, S, H, 0, D, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS || empty) return st;
+    camp_plan_t p;
+    st = rope_accept_plan(c, *plan, &p);
+    if (st != CAMP_SUCCESS) return st;
+    return rope_launch(c, p, static_cast<cudaStream_t>(stream));
+}
+
+CAMP_API camp_status_t camp_rope_qk(const void* q, const void* k, const float* sin,
+                                    const float* cos, void* yq, void* yk, int64_t B, int64_t S,
+                                    int64_t Hq, int64_t Hk, int64_t D, camp_dtype_t dtype,
+                                    void* stream) {
+    RopeCall c;
+    bool empty = false;
+    camp_status_t st = rope_validate(q, k, sin, cos, yq, yk, B, S, Hq, Hk, D, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS || empty) return st;
+    camp_plan_t p;
+    rope_plan(c, &p);
+    return rope_launch(c, p, static_cast<cudaStream_t>(stream));
+}
+
+CAMP_API camp_status_t camp_rope_qk_plan(const void* q, const void* k, const float* sin,
+                                         const float* cos, const void* yq, const void* yk,
+                                         int64_t B, int64_t S, int64_t Hq, int64_t Hk,
+                                         int64_t D, camp_dtype_t dtype, camp_plan_t* plan) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    RopeCall c;
+    bool empty = false;
+    camp_status_t st = rope_validate(q, k, sin, cos, yq, yk, B, S, Hq, Hk, D, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (empty) { *plan = camp_plan_t{}; return CAMP_SUCCESS; }
+    rope_plan(c, plan);
+    return CAMP_SUCCESS;
+}
+
+CAMP_API camp_status_t camp_rope_qk_with_plan(const void* q, const void* k, const float* sin,
+                                              const float* cos, void* yq, void* yk, int64_t B,
+                                              int64_t S, int64_t Hq, int64_t Hk, int64_t D,
+                                              camp_dtype_t dtype, const camp_plan_t* plan,
+                                              void* stream) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    RopeCall c;
+    bool empty = false;
+    camp_status_t st = rope_validate(q, k, sin, cos, yq, yk, B, S, Hq, Hk, D, dtype, &c, &empty);
     if (st != CAMP_SUCCESS || empty) return st;
     camp_plan_t p;
     st = rope_accept_plan(c, *plan, &p);

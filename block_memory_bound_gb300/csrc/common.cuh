@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace camp {
 
 // ------------------------------------------------------------------ storage types
@@ -57,30 +59,32 @@ template <> __device__ __forceinline__ Raw<2> ld_stream<2>(const void* p) {
     return r;
 }
 
-// Read-only loads of data that many rows share (the RMSNorm weight, the RoPE tables):
-// through the non-coherent path, cached in L1. Never used on memory the launch writes.
+// Loads of data that many rows share (the RMSNorm weight, the RoPE tables): ordinary
+// coherent loads kept in L1 with the evict-last priority. (Read-only "nc" loads would let
+// the compiler hoist every one of them above the output stores, holding all of them in
+// registers at once.) Never used on memory the launch writes.
 template <int BYTES> __device__ __forceinline__ Raw<BYTES> ld_shared_ro(const void* p);
 
 template <> __device__ __forceinline__ Raw<16> ld_shared_ro<16>(const void* p) {
     Raw<16> r;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.L1::evict_last.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
                  : "l"(p));
     return r;
 }
 template <> __device__ __forceinline__ Raw<8> ld_shared_ro<8>(const void* p) {
     Raw<8> r;
-    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p));
+    asm volatile("ld.global.L1::evict_last.v2.u32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p));
     return r;
 }
 template <> __device__ __forceinline__ Raw<4> ld_shared_ro<4>(const void* p) {
     Raw<4> r;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
+    asm volatile("ld.global.L1::evict_last.u32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
     return r;
 }
 template <> __device__ __forceinline__ Raw<2> ld_shared_ro<2>(const void* p) {
     Raw<2> r;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r.h) : "l"(p));
+    asm volatile("ld.global.L1::evict_last.u16 %0, [%1];" : "=h"(r.h) : "l"(p));
     return r;
 }
 
@@ -104,53 +108,110 @@ template <> __device__ __forceinline__ void st_out<2>(void* p, const Raw<2>& r) 
     asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(r.h) : "memory");
 }
 
-// ------------------------------------------------------------------ unpack / pack
+// ------------------------------------------------------------------ element access
 // Elements in a vector access are in memory order; for bf16 the element at the lower
-// address is the low half of each 32-bit word (little endian).
+// address is the low half of each 32-bit word (little endian). The helpers below work one
+// 32-bit word at a time, so that only a couple of unpacked fp32 values are live at once:
+// every output word is packed as soon as its elements are computed.
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// The same two conversions through byte permutes. Kernels that read a vector twice (a
+// reduction pass, then an output pass) use one form per pass, so that the compiler
+// re-derives the values from the raw words instead of keeping every unpacked fp32 value
+// alive across the reduction (which would double the registers per vector).
+__device__ __forceinline__ float bf16_lo_p(uint32_t w) { return __uint_as_float(__byte_perm(w, 0u, 0x1044u)); }
+__device__ __forceinline__ float bf16_hi_p(uint32_t w) { return __uint_as_float(__byte_perm(w, 0u, 0x3244u)); }
+
+// Two fp32 values -> one word of two bf16, each rounded once to nearest even.
+__device__ __forceinline__ uint32_t bf16_pack2(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
 
 template <typename S, int BYTES> struct Codec;
 
 template <int BYTES> struct Codec<bf16_t, BYTES> {
     static constexpr int kElems = BYTES / 2;
-    __device__ __forceinline__ static void unpack(const Raw<BYTES>& r, float (&v)[kElems]) {
+
+    // f(e, v) for every element e in order.
+    template <typename F>
+    __device__ __forceinline__ static void each(const Raw<BYTES>& r, F f) {
         if constexpr (BYTES == 2) {
-            v[0] = __uint_as_float(static_cast<uint32_t>(r.h) << 16);
+            f(0, __uint_as_float(static_cast<uint32_t>(r.h) << 16));
         } else {
 #pragma unroll
             for (int k = 0; k < BYTES / 4; ++k) {
-                v[2 * k] = __uint_as_float(r.w[k] << 16);
-                v[2 * k + 1] = __uint_as_float(r.w[k] & 0xFFFF0000u);
+                f(2 * k, bf16_lo(r.w[k]));
+                f(2 * k + 1, bf16_hi(r.w[k]));
             }
         }
     }
-    // One rounding per element: fp32 -> bf16, round to nearest even.
-    __device__ __forceinline__ static Raw<BYTES> pack(const float (&v)[kElems]) {
-        Raw<BYTES> r;
+
+    // out_e = f(e, in_e); one rounding per element.
+    template <typename F>
+    __device__ __forceinline__ static Raw<BYTES> map(const Raw<BYTES>& r, F f) {
+        Raw<BYTES> o;
         if constexpr (BYTES == 2) {
-            r.h = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
+            o.h = __bfloat16_as_ushort(
+                __float2bfloat16_rn(f(0, __uint_as_float(static_cast<uint32_t>(r.h) << 16))));
+        } else {
+#pragma unroll
+            for (int k = 0; k < BYTES / 4; ++k)
+                o.w[k] = bf16_pack2(f(2 * k, bf16_lo_p(r.w[k])), f(2 * k + 1, bf16_hi_p(r.w[k])));
+        }
+        return o;
+    }
+
+    // (oa_e, ob_e) = f(e, a_e, b_e); f returns a float2 {oa, ob}.
+    template <typename F>
+    __device__ __forceinline__ static void map2(const Raw<BYTES>& a, const Raw<BYTES>& b,
+                                                Raw<BYTES>& oa, Raw<BYTES>& ob, F f) {
+        if constexpr (BYTES == 2) {
+            const float2 v = f(0, __uint_as_float(static_cast<uint32_t>(a.h) << 16),
+                               __uint_as_float(static_cast<uint32_t>(b.h) << 16));
+            oa.h = __bfloat16_as_ushort(__float2bfloat16_rn(v.x));
+            ob.h = __bfloat16_as_ushort(__float2bfloat16_rn(v.y));
         } else {
 #pragma unroll
             for (int k = 0; k < BYTES / 4; ++k) {
-                const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
-                r.w[k] = *reinterpret_cast<const uint32_t*>(&p);
+                const float2 v0 = f(2 * k, bf16_lo_p(a.w[k]), bf16_lo_p(b.w[k]));
+                const float2 v1 = f(2 * k + 1, bf16_hi_p(a.w[k]), bf16_hi_p(b.w[k]));
+                oa.w[k] = bf16_pack2(v0.x, v1.x);
+                ob.w[k] = bf16_pack2(v0.y, v1.y);
             }
         }
-        return r;
     }
 };
 
 template <int BYTES> struct Codec<f32_t, BYTES> {
     static_assert(BYTES % 4 == 0, "fp32 vector accesses are whole words");
     static constexpr int kElems = BYTES / 4;
-    __device__ __forceinline__ static void unpack(const Raw<BYTES>& r, float (&v)[kElems]) {
+
+    template <typename F>
+    __device__ __forceinline__ static void each(const Raw<BYTES>& r, F f) {
 #pragma unroll
-        for (int k = 0; k < kElems; ++k) v[k] = __uint_as_float(r.w[k]);
+        for (int k = 0; k < kElems; ++k) f(k, __uint_as_float(r.w[k]));
     }
-    __device__ __forceinline__ static Raw<BYTES> pack(const float (&v)[kElems]) {
-        Raw<BYTES> r;
+
+    template <typename F>
+    __device__ __forceinline__ static Raw<BYTES> map(const Raw<BYTES>& r, F f) {
+        Raw<BYTES> o;
 #pragma unroll
-        for (int k = 0; k < kElems; ++k) r.w[k] = __float_as_uint(v[k]);
-        return r;
+        for (int k = 0; k < kElems; ++k) o.w[k] = __float_as_uint(f(k, __uint_as_float(r.w[k])));
+        return o;
+    }
+
+    template <typename F>
+    __device__ __forceinline__ static void map2(const Raw<BYTES>& a, const Raw<BYTES>& b,
+                                                Raw<BYTES>& oa, Raw<BYTES>& ob, F f) {
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) {
+            const float2 v = f(k, __uint_as_float(a.w[k]), __uint_as_float(b.w[k]));
+            oa.w[k] = __float_as_uint(v.x);
+            ob.w[k] = __float_as_uint(v.y);
+        }
     }
 };
 
@@ -165,6 +226,21 @@ template <int BYTES> __device__ __forceinline__ Raw<BYTES> raw_zero() {
     return r;
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while the previous kernel in the stream is still running. griddep_wait()
+// blocks until that kernel has completed and its memory is visible, so every kernel here
+// calls it before its first global-memory access; without the launch attribute it returns
+// at once. griddep_launch_dependents() lets the next kernel be scheduled early.
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ reductions
 
 // Butterfly (xor) sum over a full warp: every lane receives the total.
@@ -172,6 +248,59 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
     return v;
+}
+
+// ------------------------------------------------------------------ integer division
+// Division of 32-bit unsigned integers by a divisor fixed for the whole launch, by
+// multiplication (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(m, n) + n) >> l for every 32-bit n. The sum is formed in 64 bits.
+
+struct FastDiv {
+    uint32_t d;      // divisor, >= 1
+    uint32_t m;      // magic multiplier
+    uint32_t l;      // shift
+};
+
+inline FastDiv make_fast_div(uint32_t d) {
+    uint32_t l = 0;
+    while (l < 32 && (uint64_t{1} << l) < d) ++l;
+    const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+    const uint64_t t = __umulhi(f.m, n);
+    return static_cast<uint32_t>((t + n) >> f.l);
+}
+
+// ------------------------------------------------------------------ host-side launch
+
+// Grid for `blocks` CTAs: 1-D up to 2^31 - 1 blocks, 2-D beyond (the kernels flatten
+// blockIdx and skip blocks past the end).
+inline dim3 grid_2d(int64_t blocks) {
+    const int64_t kMaxX = 2147483647;
+    if (blocks <= kMaxX) return dim3(static_cast<unsigned>(blocks));
+    return dim3(static_cast<unsigned>(kMaxX), static_cast<unsigned>((blocks + kMaxX - 1) / kMaxX));
+}
+
+// Launch with programmatic stream serialization, so that the kernel may be scheduled
+// while its predecessor in the stream drains (the kernel itself waits for the
+// predecessor's memory in griddep_wait()). Returns the launch status.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace camp

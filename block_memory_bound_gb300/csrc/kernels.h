@@ -1,5 +1,6 @@
-// Internal interface between the C ABI (camp_abi.cu) and the kernel translation units.
-// Host-only declarations; no CUDA types beyond cudaStream_t.
+// Internal interface between the C ABI (camp_abi.cu) and the kernel translation units,
+// and the compile-time occupancy rules that both the kernels' launch bounds and the
+// host-side planner use. Host-only declarations; no CUDA types beyond cudaStream_t.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,6 +12,10 @@ enum class DType : int { F32 = 1, BF16 = 3 };
 
 inline int elem_bytes(DType t) { return t == DType::BF16 ? 2 : 4; }
 
+// The planner sizes grids for GB300's 152 SMs; any other SM count only changes how well
+// the last wave is filled, never the result.
+constexpr int kSmCount = 152;
+
 struct RmsnormArgs {
     const void* x;
     const void* w;
@@ -20,6 +25,9 @@ struct RmsnormArgs {
     float eps;
 };
 
+// One or two tensors of the same [B, S, *, D] layout rotated by the same tables: the
+// first with `heads` heads, the second (Q and K of one layer, say) with `heads2` heads;
+// heads2 == 0 means a single tensor.
 struct RopeArgs {
     const void* x;
     const float* sin_t;
@@ -27,27 +35,60 @@ struct RopeArgs {
     void* y;
     int64_t tokens;   // B * S
     int64_t seq;      // S
-    int64_t heads;    // H
+    int64_t heads;    // H of the first tensor
     int64_t half;     // D / 2
+    const void* x2 = nullptr;
+    void* y2 = nullptr;
+    int64_t heads2 = 0;
 };
 
-// Register-resident RMSNorm: `group` threads per row, `per_thread` vector accesses of
-// `vec_bytes` each. Returns false (launching nothing) if that variant is not compiled.
+// ------------------------------------------------------------------ RMSNorm, registers
+// A group of `group` threads owns a row; each thread holds `per_thread` vector accesses
+// of `vec_bytes`. Each variant is compiled (via __launch_bounds__) to keep a fixed number
+// of threads resident per SM, chosen from its data registers: the planner relies on it.
+
+constexpr int rows_block(int group) { return group < 256 ? 256 : group; }
+
+constexpr int rows_threads_per_sm(int vec_bytes, int per_thread) {
+    // 32-bit registers of raw row data per thread
+    return (per_thread * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 8 ? 2048
+         : (per_thread * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 16 ? 1536
+         : 1024;
+}
+
+constexpr int rows_min_blocks(int vec_bytes, int group, int per_thread) {
+    return rows_threads_per_sm(vec_bytes, per_thread) / rows_block(group) < 1
+               ? 1
+               : rows_threads_per_sm(vec_bytes, per_thread) / rows_block(group);
+}
+
 bool rmsnorm_rows_compiled(DType t, int vec_bytes, int group, int per_thread);
-bool rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
-                         const RmsnormArgs& a, int64_t grid, int block, cudaStream_t s);
-int rmsnorm_rows_block(int group);   // threads per CTA of a group size
+cudaError_t rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
+                                const RmsnormArgs& a, int64_t grid, cudaStream_t s);
 
 // Two-sweep RMSNorm for rows too wide for registers: one CTA of kWideBlock threads per row.
 constexpr int kWideBlock = 1024;
 bool rmsnorm_wide_compiled(DType t, int vec_bytes);
-bool rmsnorm_wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t grid,
-                         cudaStream_t s);
+cudaError_t rmsnorm_wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t grid,
+                                cudaStream_t s);
 
-// Rotate-half RoPE: one thread per (position, head group, vector of the half-row).
+// ------------------------------------------------------------------ RoPE
+// Tiled: a CTA of kRopeBlock threads covers kRopeBlock / (threads per position)
+// positions; thread (position, head group, vector j) rotates vector j of both halves for
+// `heads_per_thread` heads, of the first or the second tensor. Needs
+// (ceil(H / hpt) + ceil(H2 / hpt)) * (half / elems) <= kRopeBlock, fewer than 2^32
+// positions, and H, H2, D/2 below 2^31.
+// Flat: one work item per (position, head group, vector), one tensor, any shape.
 constexpr int kRopeBlock = 256;
+
+constexpr int rope_min_blocks(int heads_per_thread) {
+    return heads_per_thread <= 1 ? 6 : heads_per_thread <= 2 ? 4 : heads_per_thread <= 4 ? 3 : 2;
+}
+
 bool rope_compiled(DType t, int vec_bytes, int heads_per_thread);
-bool rope_launch(DType t, int vec_bytes, int heads_per_thread, const RopeArgs& a,
-                 int64_t grid, cudaStream_t s);
+cudaError_t rope_tiled_launch(DType t, int vec_bytes, int heads_per_thread, const RopeArgs& a,
+                              int64_t grid, cudaStream_t s);
+cudaError_t rope_flat_launch(DType t, int vec_bytes, int heads_per_thread, const RopeArgs& a,
+                             int64_t grid, cudaStream_t s);
 
 }  // namespace camp

@@ -24,13 +24,13 @@ namespace {
 
 template <int G>
 struct RowsShape {
-    static constexpr int kBlock = G < 256 ? 256 : G;   // threads per CTA
+    static constexpr int kBlock = rows_block(G);        // threads per CTA
     static constexpr int kRowsPerCta = kBlock / G;
     static constexpr int kWarpsPerRow = G / 32;
 };
 
 template <typename S, int VB, int G, int NV>
-__global__ void __launch_bounds__(RowsShape<G>::kBlock)
+__global__ void __launch_bounds__(RowsShape<G>::kBlock, rows_min_blocks(VB, G, NV))
 rmsnorm_rows_kernel(const void* x, const void* __restrict__ w, void* y,
                     int64_t rows, int64_t cols, float eps) {
     static_assert(G % 32 == 0 && G <= 1024, "a row group is whole warps");
@@ -41,62 +41,53 @@ rmsnorm_rows_kernel(const void* x, const void* __restrict__ w, void* y,
 
     __shared__ float partial[Sh::kRowsPerCta][Sh::kWarpsPerRow];
 
+    griddep_wait();
+    griddep_launch_dependents();
+
+    // One row block per CTA (the host sizes the grid; a second grid dimension only
+    // appears for more than 2^31 - 1 blocks).
     const int g = threadIdx.x / G;       // row slot inside the CTA
     const int t = threadIdx.x % G;       // thread inside the row group
-    const int64_t nvec = cols / E;       // vector accesses per row (cols is a multiple of E)
-    const int64_t pitch = cols * ES;     // bytes per row
-    const char* xb = static_cast<const char*>(x);
-    const char* wb = static_cast<const char*>(w);
-    char* yb = static_cast<char*>(y);
-    const float fcols = static_cast<float>(cols);
+    const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+    const int64_t row = block * Sh::kRowsPerCta + g;
+    const bool active = row < rows;
+    // Access k of this thread is vector k*G + t of the row; it exists iff k*G < live.
+    // On this path a row has at most G*NV <= 16384 vectors, so 32 bits suffice.
+    const int live = static_cast<int>(cols / E) - t;
+    const int64_t off = row * cols * ES + static_cast<int64_t>(t) * VB;
 
-    for (int64_t rb = blockIdx.x; rb * Sh::kRowsPerCta < rows; rb += gridDim.x) {
-        const int64_t row = rb * Sh::kRowsPerCta + g;
-        const bool active = row < rows;
-        const char* xr = xb + row * pitch;
+    // One sweep of loads: everything this thread needs is in flight at once.
+    Raw<VB> v[NV];
+    const char* xr = static_cast<const char*>(x) + off;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        v[k] = (active && k * G < live) ? ld_stream<VB>(xr + k * G * VB) : raw_zero<VB>();
 
-        // One sweep of loads: everything this thread needs is in flight at once.
-        Raw<VB> v[NV];
+    float ss = 0.0f;
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int64_t idx = static_cast<int64_t>(k) * G + t;
-            v[k] = (active && idx < nvec) ? ld_stream<VB>(xr + idx * VB) : raw_zero<VB>();
-        }
+    for (int k = 0; k < NV; ++k) C::each(v[k], [&](int, float f) { ss = fmaf(f, f, ss); });
+    ss = warp_sum(ss);
+    if constexpr (Sh::kWarpsPerRow > 1) {
+        if ((threadIdx.x & 31) == 0) partial[g][t / 32] = ss;
+        __syncthreads();
+        ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < Sh::kWarpsPerRow; ++i) ss += partial[g][i];
+    }
+    const float rinv = rsqrtf(ss / static_cast<float>(cols) + eps);
 
-        float ss = 0.0f;
+    if (!active) return;
+    const char* wt = static_cast<const char*>(w) + static_cast<int64_t>(t) * VB;
+    char* yr = static_cast<char*>(y) + off;
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            float f[E];
-            C::unpack(v[k], f);
-#pragma unroll
-            for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+    for (int k = 0; k < NV; ++k) {
+        if (k * G < live) {
+            const Raw<VB> wv = ld_shared_ro<VB>(wt + k * G * VB);
+            float wf[E];
+            C::each(wv, [&](int e, float f) { wf[e] = f; });
+            st_out<VB>(yr + k * G * VB,
+                       C::map(v[k], [&](int e, float xf) { return (xf * rinv) * wf[e]; }));
         }
-        ss = warp_sum(ss);
-        if constexpr (Sh::kWarpsPerRow > 1) {
-            if ((threadIdx.x & 31) == 0) partial[g][t / 32] = ss;
-            __syncthreads();
-            ss = 0.0f;
-#pragma unroll
-            for (int i = 0; i < Sh::kWarpsPerRow; ++i) ss += partial[g][i];
-        }
-        const float rinv = rsqrtf(ss / fcols + eps);
-
-        if (active) {
-            char* yr = yb + row * pitch;
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int64_t idx = static_cast<int64_t>(k) * G + t;
-                if (idx < nvec) {
-                    float xf[E], wf[E];
-                    C::unpack(v[k], xf);
-                    C::unpack(ld_shared_ro<VB>(wb + idx * VB), wf);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) xf[e] = (xf[e] * rinv) * wf[e];
-                    st_out<VB>(yr + idx * VB, C::pack(xf));
-                }
-            }
-        }
-        if constexpr (Sh::kWarpsPerRow > 1) __syncthreads();   // partial[] is reused
     }
 }
 
@@ -109,6 +100,9 @@ rmsnorm_wide_kernel(const void* x, const void* __restrict__ w, void* y,
     constexpr int ES = Storage<S>::kBytes;
     constexpr int kUnroll = 4;
     __shared__ float partial[kWideBlock / 32];
+
+    griddep_wait();
+    griddep_launch_dependents();
 
     const int64_t nvec = cols / E;
     const int64_t pitch = cols * ES;
@@ -128,12 +122,7 @@ rmsnorm_wide_kernel(const void* x, const void* __restrict__ w, void* y,
                 v[u] = idx < nvec ? ld_stream<VB>(xr + idx * VB) : raw_zero<VB>();
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                float f[E];
-                C::unpack(v[u], f);
-#pragma unroll
-                for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
-            }
+            for (int u = 0; u < kUnroll; ++u) C::each(v[u], [&](int, float f) { ss = fmaf(f, f, ss); });
         }
         ss = warp_sum(ss);
         if ((threadIdx.x & 31) == 0) partial[threadIdx.x / 32] = ss;
@@ -145,30 +134,28 @@ rmsnorm_wide_kernel(const void* x, const void* __restrict__ w, void* y,
 
         char* yr = yb + row * pitch;
         for (int64_t idx = threadIdx.x; idx < nvec; idx += kWideBlock) {
-            float xf[E], wf[E];
-            C::unpack(ld_stream<VB>(xr + idx * VB), xf);
-            C::unpack(ld_shared_ro<VB>(wb + idx * VB), wf);
-#pragma unroll
-            for (int e = 0; e < E; ++e) xf[e] = (xf[e] * rinv) * wf[e];
-            st_out<VB>(yr + idx * VB, C::pack(xf));
+            const Raw<VB> xv = ld_stream<VB>(xr + idx * VB);
+            float wf[E];
+            C::each(ld_shared_ro<VB>(wb + idx * VB), [&](int e, float f) { wf[e] = f; });
+            st_out<VB>(yr + idx * VB, C::map(xv, [&](int e, float xf) { return (xf * rinv) * wf[e]; }));
         }
         __syncthreads();   // partial[] is reused by the next row
     }
 }
 
 template <typename S, int VB, int G, int NV>
-void launch_rows(const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
-    rmsnorm_rows_kernel<S, VB, G, NV><<<static_cast<unsigned>(grid), RowsShape<G>::kBlock, 0, s>>>(
-        a.x, a.w, a.y, a.rows, a.cols, a.eps);
+cudaError_t launch_rows(const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
+    return launch_pdl(rmsnorm_rows_kernel<S, VB, G, NV>, grid_2d(grid),
+                      dim3(RowsShape<G>::kBlock), s, a.x, a.w, a.y, a.rows, a.cols, a.eps);
 }
 
 template <typename S, int VB>
-void launch_wide(const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
-    rmsnorm_wide_kernel<S, VB><<<static_cast<unsigned>(grid), kWideBlock, 0, s>>>(
-        a.x, a.w, a.y, a.rows, a.cols, a.eps);
+cudaError_t launch_wide(const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
+    return launch_pdl(rmsnorm_wide_kernel<S, VB>, dim3(static_cast<unsigned>(grid)),
+                      dim3(kWideBlock), s, a.x, a.w, a.y, a.rows, a.cols, a.eps);
 }
 
-using RowsFn = void (*)(const RmsnormArgs&, int64_t, cudaStream_t);
+using RowsFn = cudaError_t (*)(const RmsnormArgs&, int64_t, cudaStream_t);
 
 struct RowsEntry {
     DType t;
@@ -217,18 +204,15 @@ const RowsEntry* find_rows(DType t, int vec_bytes, int group, int per_thread) {
 
 }  // namespace
 
-int rmsnorm_rows_block(int group) { return group < 256 ? 256 : group; }
-
 bool rmsnorm_rows_compiled(DType t, int vec_bytes, int group, int per_thread) {
     return find_rows(t, vec_bytes, group, per_thread) != nullptr;
 }
 
-bool rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
-                         const RmsnormArgs& a, int64_t grid, int block, cudaStream_t s) {
+cudaError_t rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
+                                const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
     const RowsEntry* e = find_rows(t, vec_bytes, group, per_thread);
-    if (e == nullptr || block != rmsnorm_rows_block(group)) return false;
-    e->fn(a, grid, s);
-    return true;
+    if (e == nullptr) return cudaErrorInvalidValue;
+    return e->fn(a, grid, s);
 }
 
 bool rmsnorm_wide_compiled(DType t, int vec_bytes) {
@@ -236,16 +220,16 @@ bool rmsnorm_wide_compiled(DType t, int vec_bytes) {
     return vec_bytes == 16 || vec_bytes == es;
 }
 
-bool rmsnorm_wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t grid,
-                         cudaStream_t s) {
+cudaError_t rmsnorm_wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t grid,
+                                cudaStream_t s) {
     if (t == DType::BF16) {
-        if (vec_bytes == 16) { launch_wide<bf16_t, 16>(a, grid, s); return true; }
-        if (vec_bytes == 2) { launch_wide<bf16_t, 2>(a, grid, s); return true; }
+        if (vec_bytes == 16) return launch_wide<bf16_t, 16>(a, grid, s);
+        if (vec_bytes == 2) return launch_wide<bf16_t, 2>(a, grid, s);
     } else {
-        if (vec_bytes == 16) { launch_wide<f32_t, 16>(a, grid, s); return true; }
-        if (vec_bytes == 4) { launch_wide<f32_t, 4>(a, grid, s); return true; }
+        if (vec_bytes == 16) return launch_wide<f32_t, 16>(a, grid, s);
+        if (vec_bytes == 4) return launch_wide<f32_t, 4>(a, grid, s);
     }
-    return false;
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace camp

@@ -31,6 +31,13 @@ def rope_bytes(B: int, S: int, H: int, D: int, dtype: str = "bf16", tables: bool
     return 2 * B * S * H * D * es + (2 * S * (D // 2) * 4 if tables else 0)
 
 
+def rope_qk_bytes(B: int, S: int, Hq: int, Hk: int, D: int, dtype: str = "bf16") -> int:
+    """Q and K rotated in one launch: both tensors read and written once, the shared
+    tables read once."""
+    es = ELEM_BYTES[dtype]
+    return 2 * B * S * (Hq + Hk) * D * es + 2 * S * (D // 2) * 4
+
+
 def rope_flops(B: int, S: int, H: int, D: int) -> int:
     # per pair: 4 multiplies + 2 add/sub = 6 FLOP, i.e. 3 FLOP per element
     return 3 * B * S * H * D

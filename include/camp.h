@@ -113,6 +113,32 @@ CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* c
                                  int64_t B, int64_t S, int64_t H, int64_t D,
                                  camp_dtype_t dtype, void* stream);
 
+/*
+ * Rotate-half RoPE of the query and key tensors of one attention layer in one launch:
+ * yq = rope(q), yk = rope(k), both with the same tables (the gollamago README's
+ * rope(input, sin_table, cos_table) applied to Q and to K; in Llama both are rotated
+ * right after the QKV projection). Sharing one launch saves a launch and lets every
+ * position's table vectors be read once, through L1, by the heads of both tensors.
+ *
+ *   q, yq  [B, S, Hq, D]  query input and output, storage type `dtype`.
+ *   k, yk  [B, S, Hk, D]  key input and output, storage type `dtype`.
+ *   sin, cos [S, D/2]     fp32 tables, as for camp_rope.
+ *   Hq, Hk >= 0. Hq == 0 (or Hk == 0) makes this camp_rope of the other tensor; pointers
+ *          of a tensor with no heads are not inspected.
+ *
+ * Each output may equal its own input (in place); otherwise every output must be
+ * disjoint from both inputs, from the other output and from both tables. The arithmetic
+ * of each element is exactly camp_rope's. One launch when a position's heads of both
+ * tensors fit one CTA (the plan reports CAMP_KERNEL_ROPE); otherwise Q and K are rotated
+ * by two camp_rope launches (CAMP_KERNEL_ROPE_SPLIT).
+ *
+ * Errors: as for camp_rope, for either tensor, plus the overlap rules above.
+ */
+CAMP_API camp_status_t camp_rope_qk(const void* q, const void* k, const float* sin,
+                                    const float* cos, void* yq, void* yk, int64_t B, int64_t S,
+                                    int64_t Hq, int64_t Hk, int64_t D, camp_dtype_t dtype,
+                                    void* stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 CAMP_API const char* camp_status_string(camp_status_t status);
 
@@ -130,7 +156,9 @@ CAMP_API int camp_last_cuda_error(void);
 typedef enum {
     CAMP_KERNEL_RMSNORM_ROWS = 1,   /* a group of threads per row, row held in registers */
     CAMP_KERNEL_RMSNORM_WIDE = 2,   /* one CTA per row, two sweeps over x (very wide rows) */
-    CAMP_KERNEL_ROPE = 3            /* heads of one position share the table vectors */
+    CAMP_KERNEL_ROPE = 3,           /* tiled: a CTA covers whole positions, all their heads */
+    CAMP_KERNEL_ROPE_FLAT = 4,      /* any shape: one work item per (position, heads, vector) */
+    CAMP_KERNEL_ROPE_SPLIT = 5      /* camp_rope_qk only: Q and K as two separate launches */
 } camp_kernel_t;
 
 typedef struct {
@@ -167,11 +195,24 @@ CAMP_API camp_status_t camp_rmsnorm_with_plan(const void* x, const void* w, void
                                               camp_dtype_t dtype, const camp_plan_t* plan,
                                               void* stream);
 
-/* camp_rope with an explicit plan (vec_bytes and group = heads per thread). */
+/* camp_rope with an explicit plan (kernel, vec_bytes and group = heads per thread). */
 CAMP_API camp_status_t camp_rope_with_plan(const void* x, const float* sin, const float* cos,
                                            void* y, int64_t B, int64_t S, int64_t H, int64_t D,
                                            camp_dtype_t dtype, const camp_plan_t* plan,
                                            void* stream);
+
+/* Like camp_rope_plan, for camp_rope_qk. */
+CAMP_API camp_status_t camp_rope_qk_plan(const void* q, const void* k, const float* sin,
+                                         const float* cos, const void* yq, const void* yk,
+                                         int64_t B, int64_t S, int64_t Hq, int64_t Hk,
+                                         int64_t D, camp_dtype_t dtype, camp_plan_t* plan);
+
+/* camp_rope_qk with an explicit plan: only the single fused launch (CAMP_KERNEL_ROPE). */
+CAMP_API camp_status_t camp_rope_qk_with_plan(const void* q, const void* k, const float* sin,
+                                              const float* cos, void* yq, void* yk, int64_t B,
+                                              int64_t S, int64_t Hq, int64_t Hk, int64_t D,
+                                              camp_dtype_t dtype, const camp_plan_t* plan,
+                                              void* stream);
 
 #ifdef __cplusplus
 }

@@ -123,12 +123,15 @@ def test_rope_empty_is_success_without_cuda(lib):
 
 @pytest.mark.parametrize("rows,cols,dtype,expect", [
     # (kernel, vec_bytes, group, per_thread, block, grid)
-    (4096, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 64, 4, 256, 1024)),
+    # 256 vectors a row: 128 x 2 and 64 x 4 both fit exactly; fewer accesses per thread wins
+    (4096, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 256, 2048)),
     (16384, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 16384)),
+    # 375 vectors a row: 128 x 3 leaves 9 slots idle, 256 x 2 leaves 137
     (4096, 3000, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 3, 256, 2048)),
-    (64, 2048, "f32", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 4, 256, 32)),
+    # 64 rows: one row per CTA reaches the most SMs
+    (64, 2048, "f32", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 2, 256, 64)),
     (1, 8, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 32, 1, 256, 1)),
-    (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 256, 16, 256, 64)),
+    (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 1024, 4, 1024, 64)),
     (5, 65536, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 8, 1024, 5)),
     (5, 65544, "bf16", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 5)),
     (5, 16385, "f32", (camp.KERNEL_RMSNORM_WIDE, 4, 1024, 0, 1024, 5)),
@@ -146,18 +149,22 @@ def test_rmsnorm_plan_misaligned_pointer_uses_element_accesses(lib):
 
 
 @pytest.mark.parametrize("B,S,H,D,dtype,expect", [
-    # (vec_bytes, heads per thread, grid)
-    (1, 4096, 32, 64, "bf16", (16, 4, 512)),
-    (1, 4096, 8, 64, "bf16", (16, 4, 128)),
-    (1, 65536, 32, 128, "bf16", (16, 4, 16384)),
-    (2, 3, 5, 6, "bf16", (2, 1, 1)),
-    (1, 4, 6, 12, "bf16", (4, 2, 1)),
-    (1, 4, 6, 24, "f32", (16, 2, 1)),
+    # (kernel, vec_bytes, heads per thread, grid)
+    # Q: 2 heads per thread, 16 x 4 threads per position, 4 positions per CTA
+    (1, 4096, 32, 64, "bf16", (camp.KERNEL_ROPE, 16, 2, 1024)),
+    (1, 4096, 8, 64, "bf16", (camp.KERNEL_ROPE, 16, 2, 256)),
+    (1, 65536, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 2, 32768)),
+    # odd head count: 1 head per thread
+    (2, 3, 5, 6, "bf16", (camp.KERNEL_ROPE, 2, 1, 1)),
+    (1, 4, 6, 12, "bf16", (camp.KERNEL_ROPE, 4, 2, 1)),
+    (1, 4, 6, 24, "f32", (camp.KERNEL_ROPE, 16, 2, 1)),
+    # a position needs more than one CTA: the flat kernel
+    (1, 4, 1024, 256, "bf16", (camp.KERNEL_ROPE_FLAT, 16, 2, 128)),
 ])
 def test_rope_plans(lib, B, S, H, D, dtype, expect):
     p = camp.camp_rope_plan(X, SIN, COS, Y, B, S, H, D, dtype)
-    assert p.kernel == camp.KERNEL_ROPE and p.block == 256
-    assert (p.vec_bytes, p.group, p.grid) == expect
+    assert p.block == 256
+    assert (p.kernel, p.vec_bytes, p.group, p.grid) == expect
 
 
 def test_with_plan_rejects_plans_that_do_not_fit(lib):
@@ -193,3 +200,91 @@ def test_binding_raises_on_errors(lib):
     with pytest.raises(camp.CampError) as e:
         camp.camp_rope(X, SIN, COS, Y, 1, 4, 2, 7, "bf16", 0)
     assert e.value.status == camp.ERR_INVALID_ARG
+
+
+def test_fast_division_algorithm():
+    # The RoPE kernel derives the table row with Granlund-Montgomery division by an
+    # invariant: l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+    # n / d = (umulhi(m, n) + n) >> l. Check the algorithm on edge and random cases.
+    import random
+    rng = random.Random(5)
+    divisors = [1, 2, 3, 5, 7, 31, 32, 33, 4095, 4096, 4097, 65536, 70001, 2**31 - 1, 2**31,
+                2**31 + 1, 2**32 - 1] + [rng.randrange(1, 2**32) for _ in range(200)]
+    for d in divisors:
+        l = 0
+        while (1 << l) < d:
+            l += 1
+        m = ((1 << 32) * ((1 << l) - d)) // d + 1
+        assert 0 < m < (1 << 32)
+        ns = [0, 1, d - 1, d, d + 1, 2**32 - 1, 2**32 - 2] + [rng.randrange(2**32) for _ in range(300)]
+        for n in ns:
+            if n >= 2**32:
+                continue
+            t = (m * n) >> 32
+            assert (t + n) >> l == n // d, (n, d)
+
+
+# ------------------------------------------------------------------ fused Q + K RoPE
+
+K_ = 0x7F5000000000
+YQ = 0x7F6000000000
+YK = 0x7F7000000000
+
+
+def _qk(lib, q=X, k=K_, s=SIN, c=COS, yq=YQ, yk=YK, B=1, S=4, Hq=4, Hk=2, D=8,
+        dtype=camp.BF16):
+    return lib.camp_rope_qk(q, k, s, c, yq, yk, B, S, Hq, Hk, D, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"dtype": 5}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({"D": 5}, camp.ERR_INVALID_ARG),
+    ({"Hq": -1}, camp.ERR_INVALID_ARG),
+    ({"Hk": -1}, camp.ERR_INVALID_ARG),
+    ({"q": None}, camp.ERR_INVALID_ARG),
+    ({"k": None}, camp.ERR_INVALID_ARG),
+    ({"yq": None}, camp.ERR_INVALID_ARG),
+    ({"yk": None}, camp.ERR_INVALID_ARG),
+    ({"s": None}, camp.ERR_INVALID_ARG),
+    ({"k": K_ + 1}, camp.ERR_INVALID_ARG),                 # misaligned
+    ({"yq": K_}, camp.ERR_INVALID_ARG),                    # Q's output over K's input
+    ({"yk": X + 16}, camp.ERR_INVALID_ARG),                # K's output inside Q's input
+    ({"yk": YQ + 32}, camp.ERR_INVALID_ARG),               # the two outputs overlap
+    ({"yk": COS}, camp.ERR_INVALID_ARG),                   # an output over a table
+    ({"yq": X + 2}, camp.ERR_INVALID_ARG),                 # partial in-place overlap
+])
+def test_rope_qk_argument_errors(lib, kw, status):
+    assert _qk(lib, **kw) == status
+
+
+def test_rope_qk_empty_and_single_tensor_calls_need_no_cuda(lib):
+    assert _qk(lib, q=None, k=None, s=None, c=None, yq=None, yk=None, B=0) == camp.SUCCESS
+    assert _qk(lib, q=None, k=None, s=None, c=None, yq=None, yk=None, Hq=0, Hk=0) == camp.SUCCESS
+    # with no heads, a tensor's pointers are not inspected (this one would overlap)
+    p = camp.camp_rope_qk_plan(X, X + 2, SIN, COS, YQ, X + 2, 1, 4096, 32, 0, 64, "bf16")
+    assert (p.kernel, p.group, p.grid) == (camp.KERNEL_ROPE, 2, 1024)
+    p = camp.camp_rope_qk_plan(X + 2, K_, SIN, COS, X + 2, YK, 1, 4096, 0, 8, 64, "bf16")
+    assert (p.kernel, p.vec_bytes, p.group, p.grid) == (camp.KERNEL_ROPE, 16, 2, 256)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hk,D,expect", [
+    # Q 32 + K 8 heads of 64, 2 heads per thread: (16 + 4) x 4 = 80 threads a position,
+    # 3 positions per CTA
+    (1, 4096, 32, 8, 64, (camp.KERNEL_ROPE, 16, 2, 1366)),
+    (2, 128, 14, 2, 128, (camp.KERNEL_ROPE, 16, 2, 64)),
+    (1, 16, 3, 1, 64, (camp.KERNEL_ROPE, 16, 1, 1)),
+    # the heads of a position do not fit one CTA: two launches
+    (1, 4, 1024, 8, 256, (camp.KERNEL_ROPE_SPLIT, 16, 2, 129)),
+])
+def test_rope_qk_plans(lib, B, S, Hq, Hk, D, expect):
+    p = camp.camp_rope_qk_plan(X, K_, SIN, COS, YQ, YK, B, S, Hq, Hk, D, "bf16")
+    assert (p.kernel, p.vec_bytes, p.group, p.grid) == expect
+
+
+def test_rope_qk_with_plan_accepts_only_the_fused_launch(lib):
+    for p in (camp.Plan(kernel=camp.KERNEL_ROPE_FLAT, vec_bytes=16, group=2),
+              camp.Plan(kernel=camp.KERNEL_ROPE_SPLIT, vec_bytes=16, group=2),
+              camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, group=3)):
+        st = lib.camp_rope_qk_with_plan(X, K_, SIN, COS, YQ, YK, 1, 4, 4, 2, 64, camp.BF16,
+                                        ctypes.byref(p), None)
+        assert st == camp.ERR_NOT_SUPPORTED

@@ -44,5 +44,7 @@ def test_benchmark_step_bytes():
     assert ledger.rmsnorm_bytes(4096, 2048) == 33_558_528
     assert ledger.rope_bytes(1, 4096, 32, 64) == 34_603_008
     assert ledger.rope_bytes(1, 4096, 8, 64) == 9_437_184
+    # fused Q + K: the shared tables counted once
+    assert ledger.rope_qk_bytes(1, 4096, 32, 8, 64) == 42_991_616
     assert ledger.rmsnorm_bytes(16384, 8192) == 536_887_296
     assert ledger.rmsnorm_bytes(64, 2048, "f32") == 1_056_768

@@ -91,17 +91,27 @@ def test_position_zero_is_identity(dtype):
     np.testing.assert_array_equal(got, inputs.to_numpy(x_cpu)[:, 0])
 
 
+@pytest.mark.parametrize("kernel", ["tiled", "flat"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_every_variant(dtype):
+def test_every_variant(dtype, kernel):
     es = 2 if dtype == "bf16" else 4
     vbs = (16, 8, 4, 2) if dtype == "bf16" else (16, 8, 4)
+    kid = camp.KERNEL_ROPE if kernel == "tiled" else camp.KERNEL_ROPE_FLAT
     for vb in vbs:
         for hpt in (1, 2, 4, 8):
             e = vb // es
             D = 2 * e * 3                       # three vectors per half
             H = 2 * hpt + 1                     # a ragged last head group
-            plan = camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=vb, group=hpt)
+            plan = camp.Plan(kernel=kid, vec_bytes=vb, group=hpt)
             run_case(2, 5, H, D, dtype, seed=vb + hpt, plan=plan)
+            run_case(3, 37, H, D, dtype, seed=vb + hpt + 1, plan=plan)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 33, 1000, 4097, 70001])
+def test_table_row_of_every_position(S):
+    # B > 1 makes the flattened position b*S + s wrap around S; the table row is derived
+    # on the device by a multiply-shift division.
+    run_case(3, S, 2, 16, "bf16", seed=S)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
