@@ -354,16 +354,21 @@ RopeCall rope_first(const RopeCall& c) {
     return d;
 }
 
-// Choose the RoPE variant: the widest legal vector; 2 heads per thread when every head
-// count is even, else 1 (measured on GB300, L2-cold: 2 heads per thread is the fastest or
-// within 1% of it at 4096 and 65536 positions for H in {8, 32}, D in {64, 128}); the tiled
-// kernel when a position fits one CTA. Otherwise one tensor takes the flat kernel and two
+// Choose the RoPE variant: the widest legal vector, then the heads per thread, then the
+// kernel. Measured on GB300 (L2-cold, back-to-back launches): with many positions (16384
+// and up, many waves) 4 heads per thread is fastest (Q+K of 32+8 heads of 128 at 65536
+// positions: 196 us against 208 us with 2); with fewer positions 2 heads per thread is
+// fastest or within 1% (4096 positions: Q+K 8.37 us, Q 6.87 us, K 3.16 us). A ragged head
+// count takes the largest of 4, 2, 1 that divides every head count. The tiled kernel runs
+// when a position fits one CTA; otherwise one tensor takes the flat kernel and two
 // tensors are split into two single-tensor launches.
 void rope_plan(const RopeCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
     p->vec_bytes = rope_widest_vec(c);
-    const bool even = c.a.heads % 2 == 0 && c.a.heads2 % 2 == 0;
-    p->group = even ? 2 : 1;
+    const bool by4 = c.a.heads % 4 == 0 && c.a.heads2 % 4 == 0;
+    const bool by2 = c.a.heads % 2 == 0 && c.a.heads2 % 2 == 0;
+    p->group = (by4 && c.a.tokens >= 16384 && rope_positions_per_cta(c, p->vec_bytes, 4) > 0)
+                   ? 4 : by2 ? 2 : 1;
     p->per_thread = 0;
     p->block = camp::kRopeBlock;
     if (rope_positions_per_cta(c, p->vec_bytes, p->group) > 0) {

@@ -153,7 +153,9 @@ def test_rmsnorm_plan_misaligned_pointer_uses_element_accesses(lib):
     # Q: 2 heads per thread, 16 x 4 threads per position, 4 positions per CTA
     (1, 4096, 32, 64, "bf16", (camp.KERNEL_ROPE, 16, 2, 1024)),
     (1, 4096, 8, 64, "bf16", (camp.KERNEL_ROPE, 16, 2, 256)),
-    (1, 65536, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 2, 32768)),
+    # many positions: 4 heads per thread
+    (1, 65536, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 4, 16384)),
+    (1, 65536, 6, 128, "bf16", (camp.KERNEL_ROPE, 16, 2, 6554)),
     # odd head count: 1 head per thread
     (2, 3, 5, 6, "bf16", (camp.KERNEL_ROPE, 2, 1, 1)),
     (1, 4, 6, 12, "bf16", (camp.KERNEL_ROPE, 4, 2, 1)),
@@ -272,6 +274,7 @@ def test_rope_qk_empty_and_single_tensor_calls_need_no_cuda(lib):
     # 3 positions per CTA
     (1, 4096, 32, 8, 64, (camp.KERNEL_ROPE, 16, 2, 1366)),
     (2, 128, 14, 2, 128, (camp.KERNEL_ROPE, 16, 2, 64)),
+    (1, 65536, 32, 8, 128, (camp.KERNEL_ROPE, 16, 4, 21846)),
     (1, 16, 3, 1, 64, (camp.KERNEL_ROPE, 16, 1, 1)),
     # the heads of a position do not fit one CTA: two launches
     (1, 4, 1024, 8, 256, (camp.KERNEL_ROPE_SPLIT, 16, 2, 129)),
