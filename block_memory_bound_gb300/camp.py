@@ -35,6 +35,7 @@ KERNEL_RMSNORM_WIDE = 2
 KERNEL_ROPE = 3
 KERNEL_ROPE_FLAT = 4
 KERNEL_ROPE_SPLIT = 5
+KERNEL_RMSNORM_CLUSTER = 6
 
 # Every symbol include/camp.h declares.
 EXPORTS = (
@@ -63,12 +64,12 @@ class Plan(ctypes.Structure):
         ("group", ctypes.c_int32),
         ("per_thread", ctypes.c_int32),
         ("block", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("cluster", ctypes.c_int32),
         ("grid", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
     def __repr__(self) -> str:
         return f"Plan({self.as_dict()})"

@@ -115,9 +115,11 @@ struct RowsCandidate {
 //     too little in flight per thread, above it the row group's barrier and the
 //     1024-thread CTAs cost more than they save;
 //  3. fewest idle vector slots (a ragged last access per thread wastes issue slots);
-//  4. fewer accesses per thread (more threads, shorter serial work per thread).
-// At 4096 x 2048 this picks 128 x 2, at 4096 x 3000 128 x 3 and at 16384 x 8192 256 x 4,
-// the fastest of the compiled variants at each.
+//  4. within 2., fewer accesses per thread (more threads, shorter serial work per thread);
+//     outside it, the smaller group (512-thread CTAs beat 1024-thread ones: 16384 bf16
+//     columns at 4096 rows run 42 us with 512 x 4 and 50 us with 1024 x 2).
+// At 4096 x 2048 this picks 128 x 2, at 4096 x 3000 128 x 3, at 16384 x 8192 256 x 4 and at
+// 4096 x 12288 / 16384 512 x 3 / 4, the fastest of the compiled variants at each.
 bool rows_better(const RowsCandidate& a, const RowsCandidate& b) {
     const int64_t sa = a.ctas < camp::kSmCount ? a.ctas : camp::kSmCount;
     const int64_t sb = b.ctas < camp::kSmCount ? b.ctas : camp::kSmCount;
@@ -126,7 +128,8 @@ bool rows_better(const RowsCandidate& a, const RowsCandidate& b) {
     const bool mb = b.per_thread >= 2 && b.per_thread <= 4 && b.group <= 256;
     if (ma != mb) return ma;
     if (a.idle != b.idle) return a.idle < b.idle;
-    return a.per_thread < b.per_thread;
+    if (ma) return a.per_thread < b.per_thread;
+    return a.group < b.group;
 }
 
 // Choose the register-resident variant; false if no compiled variant holds the row.
@@ -164,11 +167,43 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread) {
     return true;
 }
 
+// Cluster split of one row: the smallest power-of-two cluster (2..16 CTAs of 256 threads)
+// whose CTAs hold the row with at most 8 accesses per thread (measured: 256 rows of 131072
+// bf16 run 29.6 us as 8 x 8 and 31.3 us as 16 x 4). Used for rows of more than
+// kClusterFrom 16-byte vectors, which no single CTA holds in registers; up to that width
+// one CTA of 256..1024 threads measured as fast as or faster than a cluster, which is
+// gang-scheduled and pays a cluster barrier. False if even 16 x 256 x 8 vectors cannot
+// hold the row (the two-sweep kernel takes it).
+constexpr int64_t kClusterFrom = 8192;
+
+bool rms_choose_cluster(const RmsCall& c, int64_t nvec, int* cluster, int* per_thread) {
+    static const int kPer[] = {1, 2, 3, 4, 6, 8};
+    if (c.a.rows > kMaxGrid / 16) return false;   // the grid is rows * cluster CTAs
+    for (int cl : {2, 4, 8, 16}) {
+        const int64_t need = ceil_div(nvec, static_cast<int64_t>(cl) * camp::kClusterBlock);
+        if (need <= 8) {
+            *cluster = cl;
+            *per_thread = round_up_in(static_cast<int>(need), kPer, 6);
+            return true;
+        }
+    }
+    return false;
+}
+
 void rms_plan(const RmsCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
     p->vec_bytes = rms_vec_bytes(c);
-    int g = 0, nv = 0;
-    if (rms_choose_rows(c, p->vec_bytes, &g, &nv)) {
+    p->cluster = 1;
+    const int64_t nvec = c.a.cols * camp::elem_bytes(c.t) / p->vec_bytes;
+    int g = 0, nv = 0, cl = 0;
+    if (p->vec_bytes == 16 && nvec > kClusterFrom && rms_choose_cluster(c, nvec, &cl, &nv)) {
+        p->kernel = CAMP_KERNEL_RMSNORM_CLUSTER;
+        p->group = cl * camp::kClusterBlock;
+        p->per_thread = nv;
+        p->block = camp::kClusterBlock;
+        p->cluster = cl;
+        p->grid = c.a.rows * cl;
+    } else if (rms_choose_rows(c, p->vec_bytes, &g, &nv)) {
         p->kernel = CAMP_KERNEL_RMSNORM_ROWS;
         p->group = g;
         p->per_thread = nv;
@@ -189,14 +224,28 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
     const int vb = in.vec_bytes;
     if (vb != 16 && vb != 8 && vb != 4 && vb != 2) return CAMP_ERR_NOT_SUPPORTED;
     if (vb < es || vb > rms_vec_bytes(c) || (c.a.cols * es) % vb != 0) return CAMP_ERR_NOT_SUPPORTED;
+    const int64_t nvec = c.a.cols * es / vb;
     *p = in;
+    p->cluster = 1;
     if (in.kernel == CAMP_KERNEL_RMSNORM_ROWS) {
         if (!camp::rmsnorm_rows_compiled(c.t, vb, in.group, in.per_thread))
             return CAMP_ERR_NOT_SUPPORTED;
-        const int64_t nvec = c.a.cols * es / vb;
         if (static_cast<int64_t>(in.group) * in.per_thread < nvec) return CAMP_ERR_NOT_SUPPORTED;
         p->block = camp::rows_block(in.group);
         p->grid = ceil_div(c.a.rows, p->block / in.group);
+        return CAMP_SUCCESS;
+    }
+    if (in.kernel == CAMP_KERNEL_RMSNORM_CLUSTER) {
+        const int cl = in.cluster;
+        if (vb != 16 || (cl != 2 && cl != 4 && cl != 8 && cl != 16)) return CAMP_ERR_NOT_SUPPORTED;
+        if (!camp::rmsnorm_cluster_compiled(c.t, in.per_thread)) return CAMP_ERR_NOT_SUPPORTED;
+        if (static_cast<int64_t>(cl) * camp::kClusterBlock * in.per_thread < nvec)
+            return CAMP_ERR_NOT_SUPPORTED;
+        if (c.a.rows > kMaxGrid / cl) return CAMP_ERR_NOT_SUPPORTED;
+        p->group = cl * camp::kClusterBlock;
+        p->block = camp::kClusterBlock;
+        p->cluster = cl;
+        p->grid = c.a.rows * cl;
         return CAMP_SUCCESS;
     }
     if (in.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
@@ -214,6 +263,8 @@ camp_status_t rms_launch(const RmsCall& c, const camp_plan_t& p, cudaStream_t s)
     cudaError_t e = cudaErrorInvalidValue;
     if (p.kernel == CAMP_KERNEL_RMSNORM_ROWS) {
         e = camp::rmsnorm_rows_launch(c.t, p.vec_bytes, p.group, p.per_thread, c.a, p.grid, s);
+    } else if (p.kernel == CAMP_KERNEL_RMSNORM_CLUSTER) {
+        e = camp::rmsnorm_cluster_launch(c.t, p.per_thread, p.cluster, c.a, s);
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
         e = camp::rmsnorm_wide_launch(c.t, p.vec_bytes, c.a, p.grid, s);
     }
@@ -364,6 +415,7 @@ RopeCall rope_first(const RopeCall& c) {
 // tensors are split into two single-tensor launches.
 void rope_plan(const RopeCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
+    p->cluster = 1;
     p->vec_bytes = rope_widest_vec(c);
     const bool by4 = c.a.heads % 4 == 0 && c.a.heads2 % 4 == 0;
     const bool by2 = c.a.heads % 2 == 0 && c.a.heads2 % 2 == 0;
@@ -396,6 +448,7 @@ camp_status_t rope_accept_plan(const RopeCall& c, const camp_plan_t& in, camp_pl
         return CAMP_ERR_NOT_SUPPORTED;
     *p = in;
     p->per_thread = 0;
+    p->cluster = 1;
     p->block = camp::kRopeBlock;
     p->grid = rope_grid(c, in.kernel, in.vec_bytes, in.group);
     return CAMP_SUCCESS;

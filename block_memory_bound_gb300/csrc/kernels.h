@@ -66,6 +66,13 @@ bool rmsnorm_rows_compiled(DType t, int vec_bytes, int group, int per_thread);
 cudaError_t rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
                                 const RmsnormArgs& a, int64_t grid, cudaStream_t s);
 
+// Cluster-per-row RMSNorm: a cluster of `cluster` CTAs (2..16) of kClusterBlock threads owns
+// a row; each thread holds `per_thread` 16-byte accesses of the CTA's contiguous chunk.
+constexpr int kClusterBlock = 256;
+bool rmsnorm_cluster_compiled(DType t, int per_thread);
+cudaError_t rmsnorm_cluster_launch(DType t, int per_thread, int cluster, const RmsnormArgs& a,
+                                   cudaStream_t s);
+
 // Two-sweep RMSNorm for rows too wide for registers: one CTA of kWideBlock threads per row.
 constexpr int kWideBlock = 1024;
 bool rmsnorm_wide_compiled(DType t, int vec_bytes);

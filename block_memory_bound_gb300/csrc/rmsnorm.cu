@@ -14,8 +14,17 @@
 // warps), and then writes y from the registers. x is read from HBM exactly once; w is
 // read through the L1-cached read-only path and is shared by every row on the SM.
 //
+// rmsnorm_cluster_kernel: a cluster of C CTAs owns one row, each CTA a contiguous chunk
+// of 256 * NV vectors held in registers (rows too wide for one CTA's registers). Every
+// CTA reduces its chunk and stores the partial sum into a slot of every CTA of the
+// cluster (distributed shared memory); after one hardware cluster barrier each CTA sums
+// the C slots in rank order, so all get the same sum. x is read from HBM once; there is
+// no spinning.
+//
 // rmsnorm_wide_kernel: rows wider than one CTA's registers (more than 1024 threads x 8
 // vectors) take two sweeps over x in one CTA per row; the second sweep mostly hits L2.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -91,6 +100,76 @@ rmsnorm_rows_kernel(const void* x, const void* __restrict__ w, void* y,
     }
 }
 
+template <typename S, int NV>
+__global__ void __launch_bounds__(kClusterBlock, rows_min_blocks(16, kClusterBlock, NV))
+rmsnorm_cluster_kernel(const void* x, const void* __restrict__ w, void* y, int64_t rows,
+                       int64_t cols, float eps) {
+    namespace cg = cooperative_groups;
+    constexpr int VB = 16;
+    using C = Codec<S, VB>;
+    constexpr int E = C::kElems;
+    constexpr int ES = Storage<S>::kBytes;
+    constexpr int kWarps = kClusterBlock / 32;
+
+    __shared__ float partial[kWarps];
+    __shared__ float slot[16];   // slot[r]: the partial sum of cluster rank r
+
+    griddep_wait();
+    griddep_launch_dependents();
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const unsigned nct = cluster.num_blocks();
+    const unsigned rank = cluster.block_rank();
+    const int t = threadIdx.x;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) / nct;   // the host launches rows * C CTAs
+    // Access k of this thread is vector (rank*NV + k)*256 + t of the row; live iff < nvec.
+    const int live = static_cast<int>(cols / E) - static_cast<int>(rank) * NV * kClusterBlock - t;
+    const int64_t off = row * cols * ES +
+                        (static_cast<int64_t>(rank) * NV * kClusterBlock + t) * VB;
+
+    Raw<VB> v[NV];
+    const char* xr = static_cast<const char*>(x) + off;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        v[k] = (k * kClusterBlock < live) ? ld_stream<VB>(xr + k * kClusterBlock * VB)
+                                          : raw_zero<VB>();
+
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) C::each(v[k], [&](int, float f) { ss = fmaf(f, f, ss); });
+    ss = warp_sum(ss);
+    if ((t & 31) == 0) partial[t / 32] = ss;
+    __syncthreads();
+    // Thread r < C writes this CTA's partial into slot[rank] of cluster rank r: one round of
+    // remote stores, then a single cluster barrier (its release/acquire makes the stores
+    // visible, and no shared memory of another CTA is touched after it).
+    if (t < static_cast<int>(nct)) {
+        float c = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i) c += partial[i];
+        *cluster.map_shared_rank(&slot[rank], static_cast<unsigned>(t)) = c;
+    }
+    cluster.sync();
+    ss = 0.0f;
+    for (unsigned r = 0; r < nct; ++r) ss += slot[r];          // rank order in every CTA
+    const float rinv = rsqrtf(ss / static_cast<float>(cols) + eps);
+
+    (void)rows;
+    const char* wt = static_cast<const char*>(w) +
+                     (static_cast<int64_t>(rank) * NV * kClusterBlock + t) * VB;
+    char* yr = static_cast<char*>(y) + off;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        if (k * kClusterBlock < live) {
+            const Raw<VB> wv = ld_shared_ro<VB>(wt + k * kClusterBlock * VB);
+            float wf[E];
+            C::each(wv, [&](int e, float f) { wf[e] = f; });
+            st_out<VB>(yr + k * kClusterBlock * VB,
+                       C::map(v[k], [&](int e, float xf) { return (xf * rinv) * wf[e]; }));
+        }
+    }
+}
+
 template <typename S, int VB>
 __global__ void __launch_bounds__(kWideBlock)
 rmsnorm_wide_kernel(const void* x, const void* __restrict__ w, void* y,
@@ -155,6 +234,31 @@ cudaError_t launch_wide(const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
                       dim3(kWideBlock), s, a.x, a.w, a.y, a.rows, a.cols, a.eps);
 }
 
+template <typename S, int NV>
+cudaError_t launch_cluster(const RmsnormArgs& a, int cluster, cudaStream_t s) {
+    auto kernel = rmsnorm_cluster_kernel<S, NV>;
+    if (cluster > 8) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.rows * cluster));
+    cfg.blockDim = dim3(kClusterBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, a.x, a.w, a.y, a.rows, a.cols, a.eps);
+}
+
 using RowsFn = cudaError_t (*)(const RmsnormArgs&, int64_t, cudaStream_t);
 
 struct RowsEntry {
@@ -213,6 +317,26 @@ cudaError_t rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_threa
     const RowsEntry* e = find_rows(t, vec_bytes, group, per_thread);
     if (e == nullptr) return cudaErrorInvalidValue;
     return e->fn(a, grid, s);
+}
+
+bool rmsnorm_cluster_compiled(DType, int per_thread) {
+    return per_thread == 1 || per_thread == 2 || per_thread == 3 || per_thread == 4 ||
+           per_thread == 6 || per_thread == 8;
+}
+
+cudaError_t rmsnorm_cluster_launch(DType t, int per_thread, int cluster, const RmsnormArgs& a,
+                                   cudaStream_t s) {
+    if (cluster < 2 || cluster > 16 || (cluster & (cluster - 1)) != 0) return cudaErrorInvalidValue;
+    const bool bf = t == DType::BF16;
+    switch (per_thread) {
+        case 1: return bf ? launch_cluster<bf16_t, 1>(a, cluster, s) : launch_cluster<f32_t, 1>(a, cluster, s);
+        case 2: return bf ? launch_cluster<bf16_t, 2>(a, cluster, s) : launch_cluster<f32_t, 2>(a, cluster, s);
+        case 3: return bf ? launch_cluster<bf16_t, 3>(a, cluster, s) : launch_cluster<f32_t, 3>(a, cluster, s);
+        case 4: return bf ? launch_cluster<bf16_t, 4>(a, cluster, s) : launch_cluster<f32_t, 4>(a, cluster, s);
+        case 6: return bf ? launch_cluster<bf16_t, 6>(a, cluster, s) : launch_cluster<f32_t, 6>(a, cluster, s);
+        case 8: return bf ? launch_cluster<bf16_t, 8>(a, cluster, s) : launch_cluster<f32_t, 8>(a, cluster, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 bool rmsnorm_wide_compiled(DType t, int vec_bytes) {

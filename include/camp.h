@@ -158,7 +158,8 @@ typedef enum {
     CAMP_KERNEL_RMSNORM_WIDE = 2,   /* one CTA per row, two sweeps over x (very wide rows) */
     CAMP_KERNEL_ROPE = 3,           /* tiled: a CTA covers whole positions, all their heads */
     CAMP_KERNEL_ROPE_FLAT = 4,      /* any shape: one work item per (position, heads, vector) */
-    CAMP_KERNEL_ROPE_SPLIT = 5      /* camp_rope_qk only: Q and K as two separate launches */
+    CAMP_KERNEL_ROPE_SPLIT = 5,     /* camp_rope_qk only: Q and K as two separate launches */
+    CAMP_KERNEL_RMSNORM_CLUSTER = 6 /* a cluster of CTAs per row, sums combined over DSMEM */
 } camp_kernel_t;
 
 typedef struct {
@@ -167,7 +168,7 @@ typedef struct {
     int32_t group;         /* RMSNorm: threads per row. RoPE: heads per thread */
     int32_t per_thread;    /* RMSNorm: vector accesses per thread per row. RoPE: unused (0) */
     int32_t block;         /* threads per CTA */
-    int32_t reserved;
+    int32_t cluster;       /* CTAs per cluster (RMSNorm cluster kernel: 2..16), else 1 */
     int64_t grid;          /* CTAs launched */
 } camp_plan_t;
 
@@ -185,8 +186,9 @@ CAMP_API camp_status_t camp_rope_plan(const void* x, const float* sin, const flo
                                       int64_t D, camp_dtype_t dtype, camp_plan_t* plan);
 
 /*
- * camp_rmsnorm with an explicit plan (kernel, vec_bytes, group, per_thread; block and
- * grid are derived), for tuning sweeps and for tests that cover every compiled variant.
+ * camp_rmsnorm with an explicit plan (kernel, vec_bytes, group, per_thread, and cluster for
+ * the cluster kernel; block and grid are derived), for tuning sweeps and for tests that
+ * cover every compiled variant.
  * Returns CAMP_ERR_NOT_SUPPORTED if no compiled variant matches or if the plan cannot
  * hold the row (vec_bytes must divide the row pitch and every pointer's alignment).
  */

@@ -131,14 +131,24 @@ def test_rope_empty_is_success_without_cuda(lib):
     # 64 rows: one row per CTA reaches the most SMs
     (64, 2048, "f32", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 2, 256, 64)),
     (1, 8, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 32, 1, 256, 1)),
-    (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 1024, 4, 1024, 64)),
+    (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 256, 16, 256, 64)),
+    # wider rows: one CTA of up to 1024 threads while it holds the row (8192 vectors)...
+    (4096, 12288, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 6, 256, 4096)),
+    (4096, 16384, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 8, 256, 4096)),
+    (1024, 32768, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 8, 512, 1024)),
     (5, 65536, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 8, 1024, 5)),
-    (5, 65544, "bf16", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 5)),
-    (5, 16385, "f32", (camp.KERNEL_RMSNORM_WIDE, 4, 1024, 0, 1024, 5)),
+    # ...then a cluster of 256-thread CTAs per row, the smallest with <= 8 accesses a thread
+    (5, 65544, "bf16", (camp.KERNEL_RMSNORM_CLUSTER, 16, 2048, 6, 256, 40, 8)),
+    (256, 131072, "bf16", (camp.KERNEL_RMSNORM_CLUSTER, 16, 2048, 8, 256, 2048, 8)),
+    (2, 262144, "bf16", (camp.KERNEL_RMSNORM_CLUSTER, 16, 4096, 8, 256, 32, 16)),
+    (3, 131080, "f32", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 3, 1)),
+    (2, 262152, "bf16", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 2, 1)),
+    (5, 16385, "f32", (camp.KERNEL_RMSNORM_WIDE, 4, 1024, 0, 1024, 5, 1)),
 ])
 def test_rmsnorm_plans(lib, rows, cols, dtype, expect):
     p = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype)
-    assert (p.kernel, p.vec_bytes, p.group, p.per_thread, p.block, p.grid) == expect
+    got = (p.kernel, p.vec_bytes, p.group, p.per_thread, p.block, p.grid, p.cluster)
+    assert got == (expect if len(expect) == 7 else expect + (1,))
 
 
 def test_rmsnorm_plan_misaligned_pointer_uses_element_accesses(lib):
@@ -165,7 +175,7 @@ def test_rmsnorm_plan_misaligned_pointer_uses_element_accesses(lib):
 ])
 def test_rope_plans(lib, B, S, H, D, dtype, expect):
     p = camp.camp_rope_plan(X, SIN, COS, Y, B, S, H, D, dtype)
-    assert p.block == 256
+    assert p.block == 256 and p.cluster == 1
     assert (p.kernel, p.vec_bytes, p.group, p.grid) == expect
 
 
@@ -291,3 +301,16 @@ def test_rope_qk_with_plan_accepts_only_the_fused_launch(lib):
         st = lib.camp_rope_qk_with_plan(X, K_, SIN, COS, YQ, YK, 1, 4, 4, 2, 64, camp.BF16,
                                         ctypes.byref(p), None)
         assert st == camp.ERR_NOT_SUPPORTED
+
+
+def test_cluster_plans_that_do_not_fit_are_refused(lib):
+    for cl, nv, cols in ((3, 4, 8192), (2, 5, 8192), (2, 1, 8192), (32, 1, 8192)):
+        p = camp.Plan(kernel=camp.KERNEL_RMSNORM_CLUSTER, vec_bytes=16, per_thread=nv, cluster=cl)
+        st = lib.camp_rmsnorm_with_plan(X, W, Y, 4, cols, ctypes.c_float(1e-5), camp.BF16,
+                                        ctypes.byref(p), None)
+        assert st == camp.ERR_NOT_SUPPORTED, (cl, nv)
+    # the cluster kernel uses 16-byte accesses only
+    p = camp.Plan(kernel=camp.KERNEL_RMSNORM_CLUSTER, vec_bytes=2, per_thread=4, cluster=2)
+    st = lib.camp_rmsnorm_with_plan(X, W, Y, 4, 2048, ctypes.c_float(1e-5), camp.BF16,
+                                    ctypes.byref(p), None)
+    assert st == camp.ERR_NOT_SUPPORTED

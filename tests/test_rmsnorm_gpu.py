@@ -100,9 +100,14 @@ def test_shapes_and_tails(rows, cols, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("cols", [40000, 65536, 70000, 131072, 300001])
+@pytest.mark.parametrize("cols", [12288, 16384, 40000, 65536, 70000, 131072, 262144, 300001,
+                                  524296])
 def test_wide_rows(cols, dtype):
     run_case(3, cols, dtype, seed=cols)
+
+
+def test_cluster_rows_many():
+    run_case(777, 16384, "bf16", seed=9)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -158,6 +163,22 @@ def test_every_rows_variant(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("cluster", [2, 4, 8, 16])
+def test_every_cluster_variant(dtype, cluster):
+    e = 8 if dtype == "bf16" else 4
+    for nv in (1, 2, 3, 4, 6, 8):
+        # one vector short of the capacity: the last CTA's last access is masked
+        cols = (cluster * 256 * nv - 1) * e
+        plan = camp.Plan(kernel=camp.KERNEL_RMSNORM_CLUSTER, vec_bytes=16, per_thread=nv,
+                         cluster=cluster)
+        run_case(3, cols, dtype, seed=cluster * 10 + nv, plan=plan)
+    # rows far shorter than the cluster: most CTAs have nothing to load
+    plan = camp.Plan(kernel=camp.KERNEL_RMSNORM_CLUSTER, vec_bytes=16, per_thread=1,
+                     cluster=cluster)
+    run_case(4, 8 * e, dtype, seed=cluster, plan=plan)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("vb", ["vector", "element"])
 def test_wide_kernel_forced(dtype, vb):
     es = 2 if dtype == "bf16" else 4
@@ -169,7 +190,7 @@ def test_wide_kernel_forced(dtype, vb):
 # ------------------------------------------------------------------ aliasing, alignment, streams
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("cols", [2048, 3001, 70000])
+@pytest.mark.parametrize("cols", [2048, 3001, 40000, 70000, 524296])
 def test_in_place(cols, dtype):
     run_case(7, cols, dtype, seed=cols + 1, inplace=True)
 
