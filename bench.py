@@ -114,8 +114,10 @@ def recorded_traffic(kernel_name: str):
 
 def plan_name(kind: str, p: camp.Plan) -> str:
     if kind == "rmsnorm":
-        k = "rmsnorm_rows" if p.kernel == camp.KERNEL_RMSNORM_ROWS else "rmsnorm_wide"
-        return f"{k}<bf16,vec{p.vec_bytes},group{p.group},nv{p.per_thread}>"
+        k = {camp.KERNEL_RMSNORM_ROWS: "rmsnorm_rows", camp.KERNEL_RMSNORM_CLUSTER: "rmsnorm_cluster",
+             camp.KERNEL_RMSNORM_WIDE: "rmsnorm_wide"}.get(p.kernel, "rmsnorm")
+        extra = f",cluster{p.cluster}" if p.kernel == camp.KERNEL_RMSNORM_CLUSTER else ""
+        return f"{k}<bf16,vec{p.vec_bytes},group{p.group},nv{p.per_thread}{extra}>"
     k = {camp.KERNEL_ROPE: "rope_tiled", camp.KERNEL_ROPE_FLAT: "rope_flat",
          camp.KERNEL_ROPE_SPLIT: "rope_split"}.get(p.kernel, "rope")
     return f"{k}<bf16,vec{p.vec_bytes},hpt{p.group}>"
@@ -324,6 +326,9 @@ def large_configs(peak: float, reps: int) -> list[dict]:
         ("rmsnorm bf16 [65536,8192]", "rms", (65536, 8192, False, 1e-5)),
         ("rmsnorm bf16 [65536,3000]", "rms", (65536, 3000, False, 1e-5)),
         ("rmsnorm bf16 [65536,2048]", "rms", (65536, 2048, False, 1e-5)),
+        ("add_rmsnorm bf16 [16384,8192]", "add", (16384, 8192)),
+        ("add_rmsnorm bf16 [65536,2048]", "add", (65536, 2048)),
+        ("rmsnorm bf16 [256,131072] (cluster per row)", "rms", (256, 131072, False, 1e-5)),
         ("rope bf16 [1,65536,32,128]", "rope", (65536, 32, 128)),
         ("rope bf16 [1,65536,32,64]", "rope", (65536, 32, 64)),
         ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),
@@ -340,6 +345,17 @@ def large_configs(peak: float, reps: int) -> list[dict]:
             pname = plan_name("rmsnorm", plan)
             fn = lambda: camp.camp_rmsnorm(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, cols,
                                            eps, camp.BF16, stream)
+        elif kind == "add":
+            rows, cols = shp
+            x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
+            r, _ = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=1, device="cuda")
+            h, y = torch.empty_like(x), torch.empty_like(x)
+            nbytes = ledger.add_rmsnorm_bytes(rows, cols)
+            plan = camp.camp_add_rmsnorm_plan(x, r, w, h, y, rows, cols, "bf16")
+            pname = "add_" + plan_name("rmsnorm", plan)
+            fn = lambda: camp.camp_add_rmsnorm(x.data_ptr(), r.data_ptr(), w.data_ptr(),
+                                               h.data_ptr(), y.data_ptr(), rows, cols, 1e-5,
+                                               camp.BF16, stream)
         elif kind == "rope_qk":
             S, Hq, Hk, D = shp
             q, sn, cs = inputs.rope_inputs(1, S, Hq, D, "bf16", seed=0, device="cuda")

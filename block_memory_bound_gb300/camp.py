@@ -42,6 +42,7 @@ EXPORTS = (
     "camp_rmsnorm", "camp_rope", "camp_status_string", "camp_last_cuda_error",
     "camp_rmsnorm_plan", "camp_rope_plan", "camp_rmsnorm_with_plan", "camp_rope_with_plan",
     "camp_rope_qk", "camp_rope_qk_plan", "camp_rope_qk_with_plan",
+    "camp_add_rmsnorm", "camp_add_rmsnorm_plan", "camp_add_rmsnorm_with_plan",
 )
 
 
@@ -108,6 +109,13 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_rmsnorm_with_plan.restype = c_int
         lib.camp_rope_with_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, pplan, vp]
         lib.camp_rope_with_plan.restype = c_int
+        lib.camp_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, c_int, vp]
+        lib.camp_add_rmsnorm.restype = c_int
+        lib.camp_add_rmsnorm_plan.argtypes = [vp, vp, vp, vp, vp, i64, i64, c_int, pplan]
+        lib.camp_add_rmsnorm_plan.restype = c_int
+        lib.camp_add_rmsnorm_with_plan.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, c_int,
+                                                   pplan, vp]
+        lib.camp_add_rmsnorm_with_plan.restype = c_int
         qk = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int]
         lib.camp_rope_qk.argtypes = qk + [vp]
         lib.camp_rope_qk.restype = c_int
@@ -217,6 +225,27 @@ def camp_rope_with_plan(x, sin, cos, y, B: int, S: int, H: int, D: int, dtype, p
         _dtype(dtype), ctypes.byref(plan), _stream(stream)))
 
 
+def camp_add_rmsnorm(x, r, w, h, y, rows: int, cols: int, eps: float, dtype, stream=None) -> None:
+    _check("camp_add_rmsnorm", load().camp_add_rmsnorm(
+        _ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), int(rows), int(cols), float(eps),
+        _dtype(dtype), _stream(stream)))
+
+
+def camp_add_rmsnorm_plan(x, r, w, h, y, rows: int, cols: int, dtype) -> Plan:
+    p = Plan()
+    _check("camp_add_rmsnorm_plan", load().camp_add_rmsnorm_plan(
+        _ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), int(rows), int(cols), _dtype(dtype),
+        ctypes.byref(p)))
+    return p
+
+
+def camp_add_rmsnorm_with_plan(x, r, w, h, y, rows: int, cols: int, eps: float, dtype,
+                               plan: Plan, stream=None) -> None:
+    _check("camp_add_rmsnorm_with_plan", load().camp_add_rmsnorm_with_plan(
+        _ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), int(rows), int(cols), float(eps),
+        _dtype(dtype), ctypes.byref(plan), _stream(stream)))
+
+
 def camp_rope_qk(q, k, sin, cos, yq, yk, B: int, S: int, Hq: int, Hk: int, D: int, dtype,
                  stream=None) -> None:
     _check("camp_rope_qk", load().camp_rope_qk(
@@ -295,3 +324,18 @@ def rope_qk(q, k, sin, cos, out_q=None, out_k=None, stream=None):
     out_k = torch.empty_like(k) if out_k is None else out_k
     camp_rope_qk(q, k, sin, cos, out_q, out_k, B, S, Hq, Hk, D, q.dtype, stream)
     return out_q, out_k
+
+
+def add_rmsnorm(x, r, w, eps: float = 1e-5, out_h=None, out_y=None, stream=None):
+    """h = x + r and y = RMSNorm(h) * w over the last dimension, in one launch."""
+    import torch
+    _require(x.is_cuda and x.is_contiguous() and r.shape == x.shape and r.dtype == x.dtype
+             and r.is_contiguous(), "x and r must be contiguous CUDA tensors of one shape")
+    _require(w.dtype == x.dtype and w.is_contiguous() and w.numel() == x.shape[-1],
+             "w must be a contiguous [cols] tensor of x's dtype")
+    out_h = torch.empty_like(x) if out_h is None else out_h
+    out_y = torch.empty_like(x) if out_y is None else out_y
+    cols = x.shape[-1]
+    rows = x.numel() // cols
+    camp_add_rmsnorm(x, r, w, out_h, out_y, rows, cols, eps, x.dtype, stream)
+    return out_h, out_y

@@ -58,7 +58,8 @@ camp_status_t runtime_status(cudaError_t launched) {
 struct RmsCall {
     camp::RmsnormArgs a;
     DType t;
-    int64_t bytes;   // bytes of x (and of y)
+    int64_t bytes;     // bytes of x (and of y)
+    bool add = false;  // fused residual add: h = x + r is stored and normalized
 };
 
 // Checks shared by camp_rmsnorm, camp_rmsnorm_plan and camp_rmsnorm_with_plan.
@@ -77,6 +78,7 @@ camp_status_t rms_validate(const void* x, const void* w, const void* y, int64_t 
     if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es)) return CAMP_ERR_INVALID_ARG;
     if (y != x && overlaps(y, bytes, x, bytes)) return CAMP_ERR_INVALID_ARG;
     if (overlaps(y, bytes, w, cols * es)) return CAMP_ERR_INVALID_ARG;
+    c->a = camp::RmsnormArgs{};
     c->a.x = x;
     c->a.w = w;
     c->a.y = const_cast<void*>(y);
@@ -88,13 +90,52 @@ camp_status_t rms_validate(const void* x, const void* w, const void* y, int64_t 
     return CAMP_SUCCESS;
 }
 
+// Checks of camp_add_rmsnorm: as rms_validate, but every output (h and y) either equals
+// one input (x or r) exactly, in place, or is disjoint from both; h and y are disjoint from
+// each other and from w. Each element of x and r is read by the thread that writes h and y
+// at that index, before it writes them, so an exact alias is safe.
+camp_status_t rms_add_validate(const void* x, const void* r, const void* w, const void* h,
+                               const void* y, int64_t rows, int64_t cols, camp_dtype_t dtype,
+                               RmsCall* c, bool* empty) {
+    *empty = false;
+    if (!dtype_ok(dtype)) return CAMP_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || cols < 1) return CAMP_ERR_INVALID_ARG;
+    if (rows == 0) { *empty = true; return CAMP_SUCCESS; }
+    if (x == nullptr || r == nullptr || w == nullptr || h == nullptr || y == nullptr)
+        return CAMP_ERR_INVALID_ARG;
+    const DType t = to_dtype(dtype);
+    const int64_t es = camp::elem_bytes(t);
+    int64_t bytes = 0;
+    if (!mul_ok(rows, cols, es, &bytes)) return CAMP_ERR_INVALID_ARG;
+    for (const void* p : {x, r, w, h, y})
+        if (!aligned(p, es)) return CAMP_ERR_INVALID_ARG;
+    for (const void* out : {h, y})
+        for (const void* in : {x, r})
+            if (out != in && overlaps(out, bytes, in, bytes)) return CAMP_ERR_INVALID_ARG;
+    if (overlaps(h, bytes, y, bytes)) return CAMP_ERR_INVALID_ARG;
+    if (overlaps(h, bytes, w, cols * es) || overlaps(y, bytes, w, cols * es))
+        return CAMP_ERR_INVALID_ARG;
+    c->a = camp::RmsnormArgs{};
+    c->a.x = x;
+    c->a.w = w;
+    c->a.y = const_cast<void*>(y);
+    c->a.r = r;
+    c->a.h = const_cast<void*>(h);
+    c->a.rows = rows;
+    c->a.cols = cols;
+    c->t = t;
+    c->bytes = bytes;
+    c->add = true;
+    return CAMP_SUCCESS;
+}
+
 // The widest vector access that every row start and every pointer allows.
 int rms_vec_bytes(const RmsCall& c) {
     const int es = camp::elem_bytes(c.t);
     const int64_t pitch = c.a.cols * es;
-    if (pitch % 16 == 0 && aligned(c.a.x, 16) && aligned(c.a.w, 16) && aligned(c.a.y, 16))
-        return 16;
-    return es;
+    bool ok = pitch % 16 == 0 && aligned(c.a.x, 16) && aligned(c.a.w, 16) && aligned(c.a.y, 16);
+    if (c.add) ok = ok && aligned(c.a.r, 16) && aligned(c.a.h, 16);
+    return ok ? 16 : es;
 }
 
 int round_up_in(int v, const int* set, int n) {
@@ -156,6 +197,7 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread) {
         RowsCandidate k;
         k.group = g;
         k.per_thread = round_up_in(static_cast<int>(need), pers, npers);
+        if (!camp::rows_variant_compiled(c.add, vb, g, k.per_thread)) continue;
         k.ctas = ceil_div(c.a.rows, camp::rows_block(g) / g);
         k.idle = static_cast<int64_t>(g) * k.per_thread - nvec;
         if (!found || rows_better(k, best)) best = k;
@@ -196,7 +238,8 @@ void rms_plan(const RmsCall& c, camp_plan_t* p) {
     p->cluster = 1;
     const int64_t nvec = c.a.cols * camp::elem_bytes(c.t) / p->vec_bytes;
     int g = 0, nv = 0, cl = 0;
-    if (p->vec_bytes == 16 && nvec > kClusterFrom && rms_choose_cluster(c, nvec, &cl, &nv)) {
+    const int64_t cluster_from = c.add ? kClusterFrom / 2 : kClusterFrom;
+    if (p->vec_bytes == 16 && nvec > cluster_from && rms_choose_cluster(c, nvec, &cl, &nv)) {
         p->kernel = CAMP_KERNEL_RMSNORM_CLUSTER;
         p->group = cl * camp::kClusterBlock;
         p->per_thread = nv;
@@ -228,7 +271,7 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
     *p = in;
     p->cluster = 1;
     if (in.kernel == CAMP_KERNEL_RMSNORM_ROWS) {
-        if (!camp::rmsnorm_rows_compiled(c.t, vb, in.group, in.per_thread))
+        if (!camp::rmsnorm_rows_compiled(c.add, c.t, vb, in.group, in.per_thread))
             return CAMP_ERR_NOT_SUPPORTED;
         if (static_cast<int64_t>(in.group) * in.per_thread < nvec) return CAMP_ERR_NOT_SUPPORTED;
         p->block = camp::rows_block(in.group);
@@ -262,11 +305,12 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
 camp_status_t rms_launch(const RmsCall& c, const camp_plan_t& p, cudaStream_t s) {
     cudaError_t e = cudaErrorInvalidValue;
     if (p.kernel == CAMP_KERNEL_RMSNORM_ROWS) {
-        e = camp::rmsnorm_rows_launch(c.t, p.vec_bytes, p.group, p.per_thread, c.a, p.grid, s);
+        e = camp::rmsnorm_rows_launch(c.add, c.t, p.vec_bytes, p.group, p.per_thread, c.a,
+                                      p.grid, s);
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_CLUSTER) {
-        e = camp::rmsnorm_cluster_launch(c.t, p.per_thread, p.cluster, c.a, s);
+        e = camp::rmsnorm_cluster_launch(c.add, c.t, p.per_thread, p.cluster, c.a, s);
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
-        e = camp::rmsnorm_wide_launch(c.t, p.vec_bytes, c.a, p.grid, s);
+        e = camp::rmsnorm_wide_launch(c.add, c.t, p.vec_bytes, c.a, p.grid, s);
     }
     return runtime_status(e);
 }
@@ -525,6 +569,53 @@ CAMP_API camp_status_t camp_rmsnorm_with_plan(const void* x, const void* w, void
     RmsCall c;
     bool empty = false;
     camp_status_t st = rms_validate(x, w, y, rows, cols, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (!eps_ok(eps)) return CAMP_ERR_INVALID_ARG;
+    if (empty) return CAMP_SUCCESS;
+    c.a.eps = eps;
+    camp_plan_t p;
+    st = rms_accept_plan(c, *plan, &p);
+    if (st != CAMP_SUCCESS) return st;
+    return rms_launch(c, p, static_cast<cudaStream_t>(stream));
+}
+
+CAMP_API camp_status_t camp_add_rmsnorm(const void* x, const void* r, const void* w, void* h,
+                                        void* y, int64_t rows, int64_t cols, float eps,
+                                        camp_dtype_t dtype, void* stream) {
+    RmsCall c;
+    bool empty = false;
+    camp_status_t st = rms_add_validate(x, r, w, h, y, rows, cols, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (!eps_ok(eps)) return CAMP_ERR_INVALID_ARG;
+    if (empty) return CAMP_SUCCESS;
+    c.a.eps = eps;
+    camp_plan_t p;
+    rms_plan(c, &p);
+    return rms_launch(c, p, static_cast<cudaStream_t>(stream));
+}
+
+CAMP_API camp_status_t camp_add_rmsnorm_plan(const void* x, const void* r, const void* w,
+                                             const void* h, const void* y, int64_t rows,
+                                             int64_t cols, camp_dtype_t dtype,
+                                             camp_plan_t* plan) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    RmsCall c;
+    bool empty = false;
+    camp_status_t st = rms_add_validate(x, r, w, h, y, rows, cols, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (empty) { *plan = camp_plan_t{}; return CAMP_SUCCESS; }
+    rms_plan(c, plan);
+    return CAMP_SUCCESS;
+}
+
+CAMP_API camp_status_t camp_add_rmsnorm_with_plan(const void* x, const void* r, const void* w,
+                                                  void* h, void* y, int64_t rows, int64_t cols,
+                                                  float eps, camp_dtype_t dtype,
+                                                  const camp_plan_t* plan, void* stream) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    RmsCall c;
+    bool empty = false;
+    camp_status_t st = rms_add_validate(x, r, w, h, y, rows, cols, dtype, &c, &empty);
     if (st != CAMP_SUCCESS) return st;
     if (!eps_ok(eps)) return CAMP_ERR_INVALID_ARG;
     if (empty) return CAMP_SUCCESS;

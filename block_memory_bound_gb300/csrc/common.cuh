@@ -164,6 +164,22 @@ template <int BYTES> struct Codec<bf16_t, BYTES> {
         return o;
     }
 
+    // o_e = a_e + b_e, formed in fp32 and rounded once to bf16.
+    __device__ __forceinline__ static Raw<BYTES> add(const Raw<BYTES>& a, const Raw<BYTES>& b) {
+        Raw<BYTES> o;
+        if constexpr (BYTES == 2) {
+            o.h = __bfloat16_as_ushort(__float2bfloat16_rn(
+                __uint_as_float(static_cast<uint32_t>(a.h) << 16) +
+                __uint_as_float(static_cast<uint32_t>(b.h) << 16)));
+        } else {
+#pragma unroll
+            for (int k = 0; k < BYTES / 4; ++k)
+                o.w[k] = bf16_pack2(bf16_lo_p(a.w[k]) + bf16_lo_p(b.w[k]),
+                                    bf16_hi_p(a.w[k]) + bf16_hi_p(b.w[k]));
+        }
+        return o;
+    }
+
     // (oa_e, ob_e) = f(e, a_e, b_e); f returns a float2 {oa, ob}.
     template <typename F>
     __device__ __forceinline__ static void map2(const Raw<BYTES>& a, const Raw<BYTES>& b,
@@ -200,6 +216,14 @@ template <int BYTES> struct Codec<f32_t, BYTES> {
         Raw<BYTES> o;
 #pragma unroll
         for (int k = 0; k < kElems; ++k) o.w[k] = __float_as_uint(f(k, __uint_as_float(r.w[k])));
+        return o;
+    }
+
+    __device__ __forceinline__ static Raw<BYTES> add(const Raw<BYTES>& a, const Raw<BYTES>& b) {
+        Raw<BYTES> o;
+#pragma unroll
+        for (int k = 0; k < kElems; ++k)
+            o.w[k] = __float_as_uint(__uint_as_float(a.w[k]) + __uint_as_float(b.w[k]));
         return o;
     }
 

@@ -16,6 +16,7 @@ inline int elem_bytes(DType t) { return t == DType::BF16 ? 2 : 4; }
 // the last wave is filled, never the result.
 constexpr int kSmCount = 152;
 
+// RMSNorm of x, or (add path) of h = x + r, which is also stored.
 struct RmsnormArgs {
     const void* x;
     const void* w;
@@ -23,6 +24,8 @@ struct RmsnormArgs {
     int64_t rows;
     int64_t cols;
     float eps;
+    const void* r = nullptr;   // add path: the residual
+    void* h = nullptr;         // add path: h = x + r, rounded once to the storage type
 };
 
 // One or two tensors of the same [B, S, *, D] layout rotated by the same tables: the
@@ -49,35 +52,56 @@ struct RopeArgs {
 
 constexpr int rows_block(int group) { return group < 256 ? 256 : group; }
 
-constexpr int rows_threads_per_sm(int vec_bytes, int per_thread) {
+// `loads` raw accesses are live per thread at the peak: per_thread, or twice that on the
+// add path (x and r are both in flight before h is formed).
+constexpr int rows_threads_per_sm(int vec_bytes, int loads) {
     // 32-bit registers of raw row data per thread
-    return (per_thread * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 8 ? 2048
-         : (per_thread * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 16 ? 1536
-         : 1024;
+    return (loads * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 8 ? 2048
+         : (loads * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 16 ? 1536
+         : (loads * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 32 ? 1024
+         : 512;
 }
 
-constexpr int rows_min_blocks(int vec_bytes, int group, int per_thread) {
-    return rows_threads_per_sm(vec_bytes, per_thread) / rows_block(group) < 1
+constexpr int rows_min_blocks(int vec_bytes, int group, int loads) {
+    return rows_threads_per_sm(vec_bytes, loads) / rows_block(group) < 1
                ? 1
-               : rows_threads_per_sm(vec_bytes, per_thread) / rows_block(group);
+               : rows_threads_per_sm(vec_bytes, loads) / rows_block(group);
 }
 
-bool rmsnorm_rows_compiled(DType t, int vec_bytes, int group, int per_thread);
-cudaError_t rmsnorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
+// The add path keeps x and r in flight together; with 1024 threads (64 registers each) and
+// 8 16-byte accesses that is 64 raw registers, which would spill, so that one variant is not built
+// (the planner sends such rows to the cluster kernel).
+constexpr bool rows_variant_compiled(bool add, int vec_bytes, int group, int per_thread) {
+    return !(add && vec_bytes == 16 && group == 1024 && per_thread == 8);
+}
+
+// `add` selects the fused residual-add variants throughout.
+bool rmsnorm_rows_compiled(bool add, DType t, int vec_bytes, int group, int per_thread);
+cudaError_t rmsnorm_rows_launch(bool add, DType t, int vec_bytes, int group, int per_thread,
                                 const RmsnormArgs& a, int64_t grid, cudaStream_t s);
 
 // Cluster-per-row RMSNorm: a cluster of `cluster` CTAs (2..16) of kClusterBlock threads owns
 // a row; each thread holds `per_thread` 16-byte accesses of the CTA's contiguous chunk.
 constexpr int kClusterBlock = 256;
 bool rmsnorm_cluster_compiled(DType t, int per_thread);
-cudaError_t rmsnorm_cluster_launch(DType t, int per_thread, int cluster, const RmsnormArgs& a,
-                                   cudaStream_t s);
+cudaError_t rmsnorm_cluster_launch(bool add, DType t, int per_thread, int cluster,
+                                   const RmsnormArgs& a, cudaStream_t s);
 
 // Two-sweep RMSNorm for rows too wide for registers: one CTA of kWideBlock threads per row.
 constexpr int kWideBlock = 1024;
 bool rmsnorm_wide_compiled(DType t, int vec_bytes);
-cudaError_t rmsnorm_wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t grid,
-                                cudaStream_t s);
+cudaError_t rmsnorm_wide_launch(bool add, DType t, int vec_bytes, const RmsnormArgs& a,
+                                int64_t grid, cudaStream_t s);
+
+// The add-path tables live in their own translation unit (compiled in parallel).
+namespace add_path {
+cudaError_t rows_launch(DType t, int vec_bytes, int group, int per_thread, const RmsnormArgs& a,
+                        int64_t grid, cudaStream_t s);
+cudaError_t cluster_launch(DType t, int per_thread, int cluster, const RmsnormArgs& a,
+                           cudaStream_t s);
+cudaError_t wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t grid,
+                        cudaStream_t s);
+}  // namespace add_path
 
 // ------------------------------------------------------------------ RoPE
 // Tiled: a CTA of kRopeBlock threads covers kRopeBlock / (threads per position)

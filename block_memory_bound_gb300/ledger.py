@@ -21,6 +21,12 @@ def rmsnorm_bytes(rows: int, cols: int, dtype: str = "bf16", weight: bool = True
     return 2 * rows * cols * es + (cols * es if weight else 0)
 
 
+def add_rmsnorm_bytes(rows: int, cols: int, dtype: str = "bf16") -> int:
+    """Fused residual add + RMSNorm: x and r read once, h and y written once, w read once."""
+    es = ELEM_BYTES[dtype]
+    return 4 * rows * cols * es + cols * es
+
+
 def rmsnorm_flops(rows: int, cols: int) -> int:
     # per element: square-accumulate (2) + two multiplies (2); per row: divide, add, rsqrt
     return 4 * rows * cols + 3 * rows

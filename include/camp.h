@@ -86,6 +86,28 @@ CAMP_API camp_status_t camp_rmsnorm(const void* x, const void* w, void* y, int64
                                     void* stream);
 
 /*
+ * Fused residual add + RMSNorm: h = x + r, y = RMSNorm(h) * w, in one pass over the rows.
+ * The TileLang tutorial (ch. 02, section 4.2) cites the fusion of "the Add before RmsNorm"
+ * with the RMSNorm (Ascend's AddRmsNorm operators) as a way to save moving data in and
+ * out; the pages define no more than that. Here h is formed in fp32, rounded once to the
+ * storage type and stored (the residual stream of the next block), and the row that is
+ * normalized is h as stored, exactly as camp_rmsnorm does it; so the result is bit for bit
+ * that of an add followed by camp_rmsnorm, while x and r are read once and h is never
+ * re-read from memory.
+ *
+ *   x, r  [rows, cols]  the two addends (block output and residual), storage type `dtype`.
+ *   w     [cols]        weight.
+ *   h     [rows, cols]  output: x + r, rounded once.
+ *   y     [rows, cols]  output: RMSNorm(h) * w.
+ *   Each output may equal x or r exactly (in place; for example h == r updates the
+ *   residual where it is); otherwise it must be disjoint from both. h and y must be
+ *   disjoint from each other and from w. Sizes, eps and errors as for camp_rmsnorm.
+ */
+CAMP_API camp_status_t camp_add_rmsnorm(const void* x, const void* r, const void* w, void* h,
+                                        void* y, int64_t rows, int64_t cols, float eps,
+                                        camp_dtype_t dtype, void* stream);
+
+/*
  * Rotate-half RoPE of x[B, S, H, D] with fp32 tables sin[S, D/2] and cos[S, D/2].
  *
  *   x     [B, S, H, D]  input, storage type `dtype`.
@@ -215,6 +237,18 @@ CAMP_API camp_status_t camp_rope_qk_with_plan(const void* q, const void* k, cons
                                               int64_t S, int64_t Hq, int64_t Hk, int64_t D,
                                               camp_dtype_t dtype, const camp_plan_t* plan,
                                               void* stream);
+
+/* Like camp_rmsnorm_plan, for camp_add_rmsnorm (same kernels, add variants). */
+CAMP_API camp_status_t camp_add_rmsnorm_plan(const void* x, const void* r, const void* w,
+                                             const void* h, const void* y, int64_t rows,
+                                             int64_t cols, camp_dtype_t dtype,
+                                             camp_plan_t* plan);
+
+/* camp_add_rmsnorm with an explicit plan, as camp_rmsnorm_with_plan. */
+CAMP_API camp_status_t camp_add_rmsnorm_with_plan(const void* x, const void* r, const void* w,
+                                                  void* h, void* y, int64_t rows, int64_t cols,
+                                                  float eps, camp_dtype_t dtype,
+                                                  const camp_plan_t* plan, void* stream);
 
 #ifdef __cplusplus
 }

@@ -60,6 +60,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_rmsnorm_f64.restype = c_int
     lib.oracle_rmsnorm.argtypes = [vp, vp, vp, i64, i64, dbl, c_int, c_int]
     lib.oracle_rmsnorm.restype = c_int
+    lib.oracle_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i64, dbl, c_int, c_int]
+    lib.oracle_add_rmsnorm.restype = c_int
     lib.oracle_rope_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64]
     lib.oracle_rope_f64.restype = c_int
     lib.oracle_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, c_int]
@@ -144,6 +146,26 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float, dtype: str, nthreads: int 
     _check(lib.oracle_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, cols, float(eps), code,
                               int(nthreads)), "rmsnorm")
     return y
+
+
+def add_rmsnorm(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: float, dtype: str,
+                nthreads: int = 0, lib: ctypes.CDLL | None = None
+                ) -> tuple[np.ndarray, np.ndarray]:
+    """(h, y): h = x + r rounded once, y = RMSNorm(h as stored) * w rounded once."""
+    lib = lib or load()
+    code, npt = _storage(dtype)
+    x = np.ascontiguousarray(x)
+    r = np.ascontiguousarray(r)
+    w = np.ascontiguousarray(w)
+    assert x.dtype == npt and r.dtype == npt and w.dtype == npt
+    assert r.shape == x.shape
+    rows, cols = x.shape
+    assert w.shape == (cols,)
+    h = np.empty_like(x)
+    y = np.empty_like(x)
+    _check(lib.oracle_add_rmsnorm(_ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), rows, cols,
+                                  float(eps), code, int(nthreads)), "add_rmsnorm")
+    return h, y
 
 
 def rope_f64(x, sin_t, cos_t, lib: ctypes.CDLL | None = None) -> np.ndarray:

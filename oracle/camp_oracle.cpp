@@ -15,6 +15,11 @@
 //       rms_r = sqrt(ss_r / cols + eps)
 //       y[r,j] = x[r,j] / rms_r * w[j]          then one rounding to the storage type
 //
+//   Residual add + RMSNorm  (TileLang tutorial ch. 02, section 4.2: the "Add before
+//            RmsNorm" fused into it; the pages give no formula beyond the two operations)
+//       h[r,j] = round(x[r,j] + r[r,j])         (the exact sum, one rounding)
+//       y      = RMSNorm(h as stored) * w       (as above)
+//
 //   RoPE, rotate-half  (gollamago README, "RoPE": rope(input, sin_table, cos_table),
 //            input [batch, sequence, heads, head_dim], tables [sequence, head_dim/2],
 //            each head split into two halves and rotated; tilelang tutorial ch. 02,
@@ -211,6 +216,32 @@ int oracle_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int64_t 
             for (int64_t j = 0; j < cols; ++j) xr[j] = load_elem(x, r * cols + j, dtype);
             rmsnorm_row(xr.data(), wd.data(), yr.data(), cols, eps);
             for (int64_t j = 0; j < cols; ++j) store_elem(y, r * cols + j, yr[j], dtype);
+        }
+    });
+    return 0;
+}
+
+// Residual add then RMSNorm over storage-typed x, r (summands), w; outputs h = x + r rounded
+// once (the sum of two bf16 or two fp32 values is exact in fp64) and y = RMSNorm(h) * w
+// computed from h as stored, rounded once. nthreads as for oracle_rmsnorm.
+int oracle_add_rmsnorm(const void* x, const void* r, const void* w, void* h, void* y,
+                       int64_t rows, int64_t cols, double eps, int dtype, int nthreads) {
+    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
+    if (rows == 0) return 0;
+    if (!x || !r || !w || !h || !y) return 1;
+    std::vector<double> wd(static_cast<size_t>(cols));
+    for (int64_t j = 0; j < cols; ++j) wd[j] = load_elem(w, j, dtype);
+    parallel_blocks(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        std::vector<double> hr(static_cast<size_t>(cols)), yr(static_cast<size_t>(cols));
+        for (int64_t row = r0; row < r1; ++row) {
+            for (int64_t j = 0; j < cols; ++j) {
+                const int64_t i = row * cols + j;
+                store_elem(h, i, load_elem(x, i, dtype) + load_elem(r, i, dtype), dtype);
+                hr[j] = load_elem(h, i, dtype);
+            }
+            rmsnorm_row(hr.data(), wd.data(), yr.data(), cols, eps);
+            for (int64_t j = 0; j < cols; ++j) store_elem(y, row * cols + j, yr[j], dtype);
         }
     });
     return 0;

@@ -314,3 +314,56 @@ def test_cluster_plans_that_do_not_fit_are_refused(lib):
     st = lib.camp_rmsnorm_with_plan(X, W, Y, 4, 2048, ctypes.c_float(1e-5), camp.BF16,
                                     ctypes.byref(p), None)
     assert st == camp.ERR_NOT_SUPPORTED
+
+
+# ------------------------------------------------------------------ fused residual add + RMSNorm
+
+R_ = 0x7F8000000000
+H_ = 0x7F9000000000
+
+
+def _addrms(lib, x=X, r=R_, w=W, h=H_, y=Y, rows=4, cols=8, eps=1e-5, dtype=camp.BF16):
+    return lib.camp_add_rmsnorm(x, r, w, h, y, rows, cols, ctypes.c_float(eps), dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"dtype": 9}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({"cols": 0}, camp.ERR_INVALID_ARG),
+    ({"eps": -1.0}, camp.ERR_INVALID_ARG),
+    ({"r": None}, camp.ERR_INVALID_ARG),
+    ({"h": None}, camp.ERR_INVALID_ARG),
+    ({"r": R_ + 1}, camp.ERR_INVALID_ARG),              # misaligned
+    ({"h": Y}, camp.ERR_INVALID_ARG),                   # the two outputs coincide
+    ({"h": Y + 8}, camp.ERR_INVALID_ARG),               # ...or overlap
+    ({"h": X + 2}, camp.ERR_INVALID_ARG),               # partial overlap with an input
+    ({"y": R_ - 4}, camp.ERR_INVALID_ARG),
+    ({"h": W}, camp.ERR_INVALID_ARG),                   # output over the weight
+])
+def test_add_rmsnorm_argument_errors(lib, kw, status):
+    assert _addrms(lib, **kw) == status
+
+
+def test_add_rmsnorm_exact_aliases_are_accepted(lib):
+    # h == r (residual updated in place) with y == x, and the other way round; planning
+    # needs no CUDA, so a plan proves the arguments were accepted.
+    for h, y in ((R_, X), (X, R_), (R_, Y), (H_, X)):
+        p = camp.camp_add_rmsnorm_plan(X, R_, W, h, y, 4096, 2048, "bf16")
+        assert p.kernel == camp.KERNEL_RMSNORM_ROWS
+
+
+@pytest.mark.parametrize("rows,cols,expect", [
+    (4096, 2048, (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 1)),
+    (16384, 8192, (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 1)),
+    # the add path holds x and r at once: past 4096 vectors a row it takes a cluster
+    (64, 40000, (camp.KERNEL_RMSNORM_CLUSTER, 16, 1024, 5 + 1, 4)),
+])
+def test_add_rmsnorm_plans(lib, rows, cols, expect):
+    p = camp.camp_add_rmsnorm_plan(X, R_, W, H_, Y, rows, cols, "bf16")
+    assert (p.kernel, p.vec_bytes, p.group, p.per_thread, p.cluster) == expect
+
+
+def test_add_rmsnorm_unbuilt_variant_is_refused(lib):
+    p = camp.Plan(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=16, group=1024, per_thread=8)
+    st = lib.camp_add_rmsnorm_with_plan(X, R_, W, H_, Y, 4, 65536, ctypes.c_float(1e-5),
+                                        camp.BF16, ctypes.byref(p), None)
+    assert st == camp.ERR_NOT_SUPPORTED

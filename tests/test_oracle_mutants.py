@@ -42,6 +42,11 @@ MUTANTS = {
          "static_cast<uint16_t*>(base)[i] = double_to_bf16(static_cast<float>(v));"),
     "subnormal spacing wrong":
         ("if (E < -126) E = -126;", "if (E < -127) E = -127;"),
+    "add path normalizes x instead of h":
+        ("hr[j] = load_elem(h, i, dtype);", "hr[j] = load_elem(x, i, dtype);"),
+    "add path normalizes the unrounded sum":
+        ("hr[j] = load_elem(h, i, dtype);",
+         "hr[j] = load_elem(x, i, dtype) + load_elem(r, i, dtype);"),
 }
 
 
@@ -64,6 +69,8 @@ def _battery(lib):
         ("rope interleaved", lambda: pins.test_rope_rotate_half_equals_interleaved_on_deinterleaved_input(lib)),
         ("rope storage", lambda: pins.test_rope_storage_path_rounds_the_fp64_result_once(lib, "f32")),
         ("rope single rounding", lambda: pins.test_rope_single_rounding_crafted_case(lib)),
+        ("add rmsnorm", lambda: [pins.test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, d)
+                                 for d in ("bf16", "f32")]),
     ]
     failed = []
     for name, fn in checks:

@@ -235,6 +235,46 @@ def test_rmsnorm_argument_checks(lib):
     assert oracle.rmsnorm_f64(np.zeros((0, 3)), np.zeros(3), 1e-5, lib=lib).shape == (0, 3)
 
 
+# ------------------------------------------------------------------------ residual add
+
+def _storage_pair(rng, shape, dtype, scale=1.0):
+    f = (rng.standard_normal(shape) * scale).astype(np.float32)
+    t = torch.from_numpy(f)
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+        return t, t.view(torch.int16).numpy().view(np.uint16)
+    return t, f
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, dtype):
+    # h must equal torch's storage-type addition (round to nearest even of the exact sum),
+    # and y the (separately pinned) RMSNorm of h as stored.
+    rng = np.random.default_rng(31)
+    for scale_r in (1.0, 1e-3, 300.0):
+        xt, xs = _storage_pair(rng, (7, 301), dtype)
+        rt, rs = _storage_pair(rng, (7, 301), dtype, scale_r)
+        wt, ws = _storage_pair(rng, (301,), dtype, 0.1)
+        ws = (torch.from_numpy(np.ones(301, np.float32)).to(wt.dtype) + wt)
+        ws = ws.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else ws.numpy()
+        h, y = oracle.add_rmsnorm(xs, rs, ws, 1e-5, dtype, lib=lib)
+        want_h = xt + rt
+        want_h = (want_h.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16"
+                  else want_h.numpy())
+        np.testing.assert_array_equal(h, want_h)
+        np.testing.assert_array_equal(y, oracle.rmsnorm(h, ws, 1e-5, dtype, lib=lib))
+
+
+def test_add_rmsnorm_zero_residual_is_rmsnorm(lib):
+    rng = np.random.default_rng(32)
+    _, xs = _storage_pair(rng, (5, 64), "bf16")
+    _, ws = _storage_pair(rng, (64,), "bf16")
+    zero = np.zeros_like(xs)
+    h, y = oracle.add_rmsnorm(xs, zero, ws, 1e-5, "bf16", lib=lib)
+    np.testing.assert_array_equal(h, xs)
+    np.testing.assert_array_equal(y, oracle.rmsnorm(xs, ws, 1e-5, "bf16", lib=lib))
+
+
 # ------------------------------------------------------------------------ RoPE
 
 def _tables(S, half, angle_fn, dtype=np.float64):
