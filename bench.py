@@ -333,6 +333,7 @@ def large_configs(peak: float, reps: int) -> list[dict]:
         ("rope bf16 [1,65536,32,64]", "rope", (65536, 32, 64)),
         ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),
         ("rope_qk bf16 Q[1,65536,32,128] + K[1,65536,8,128]", "rope_qk", (65536, 32, 8, 128)),
+        ("kv rmsnorm+rope+cache bf16 kv[1,65536,512+64] -> 131072 slots", "kv", (65536, 512, 64)),
     ]
     stream = torch.cuda.current_stream().cuda_stream
     for name, kind, shp in cases:
@@ -356,6 +357,22 @@ def large_configs(peak: float, reps: int) -> list[dict]:
             fn = lambda: camp.camp_add_rmsnorm(x.data_ptr(), r.data_ptr(), w.data_ptr(),
                                                h.data_ptr(), y.data_ptr(), rows, cols, 1e-5,
                                                camp.BF16, stream)
+        elif kind == "kv":
+            S, Dn, Dr = shp
+            ns = 2 * S
+            x = torch.randn(1, S, Dn + Dr, device="cuda").to(torch.bfloat16)
+            gam = torch.ones(Dn, device="cuda", dtype=torch.bfloat16)
+            _, sn, cs = inputs.rope_inputs(1, S, 1, Dr, "bf16", seed=0, device="cuda")
+            slots = torch.randperm(ns, device="cuda")[:S].to(torch.int64)
+            y = torch.empty(ns, Dn, device="cuda", dtype=torch.bfloat16)
+            yr = torch.empty(ns, Dr, device="cuda", dtype=torch.bfloat16)
+            nbytes = ledger.kv_cache_bytes(1, S, Dn, Dr)
+            plan = camp.camp_kv_rmsnorm_rope_cache_plan(x, gam, sn, cs, slots, y, yr, 1, S, Dn,
+                                                        Dr, ns, "bf16")
+            pname = f"kv_cache<bf16,vec{plan.vec_bytes},nv{plan.per_thread}>"
+            fn = lambda: camp.camp_kv_rmsnorm_rope_cache(
+                x.data_ptr(), gam.data_ptr(), sn.data_ptr(), cs.data_ptr(), slots.data_ptr(),
+                y.data_ptr(), yr.data_ptr(), 1, S, Dn, Dr, ns, 1e-5, camp.BF16, stream)
         elif kind == "rope_qk":
             S, Hq, Hk, D = shp
             q, sn, cs = inputs.rope_inputs(1, S, Hq, D, "bf16", seed=0, device="cuda")

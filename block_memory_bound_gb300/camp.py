@@ -36,6 +36,7 @@ KERNEL_ROPE = 3
 KERNEL_ROPE_FLAT = 4
 KERNEL_ROPE_SPLIT = 5
 KERNEL_RMSNORM_CLUSTER = 6
+KERNEL_KV_CACHE = 7
 
 # Every symbol include/camp.h declares.
 EXPORTS = (
@@ -43,6 +44,8 @@ EXPORTS = (
     "camp_rmsnorm_plan", "camp_rope_plan", "camp_rmsnorm_with_plan", "camp_rope_with_plan",
     "camp_rope_qk", "camp_rope_qk_plan", "camp_rope_qk_with_plan",
     "camp_add_rmsnorm", "camp_add_rmsnorm_plan", "camp_add_rmsnorm_with_plan",
+    "camp_kv_rmsnorm_rope_cache", "camp_kv_rmsnorm_rope_cache_plan",
+    "camp_kv_rmsnorm_rope_cache_with_plan",
 )
 
 
@@ -116,6 +119,13 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_add_rmsnorm_with_plan.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, c_int,
                                                    pplan, vp]
         lib.camp_add_rmsnorm_with_plan.restype = c_int
+        kvsig = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64]
+        lib.camp_kv_rmsnorm_rope_cache.argtypes = kvsig + [f32, c_int, vp]
+        lib.camp_kv_rmsnorm_rope_cache.restype = c_int
+        lib.camp_kv_rmsnorm_rope_cache_plan.argtypes = kvsig + [c_int, pplan]
+        lib.camp_kv_rmsnorm_rope_cache_plan.restype = c_int
+        lib.camp_kv_rmsnorm_rope_cache_with_plan.argtypes = kvsig + [f32, c_int, pplan, vp]
+        lib.camp_kv_rmsnorm_rope_cache_with_plan.restype = c_int
         qk = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int]
         lib.camp_rope_qk.argtypes = qk + [vp]
         lib.camp_rope_qk.restype = c_int
@@ -244,6 +254,33 @@ def camp_add_rmsnorm_with_plan(x, r, w, h, y, rows: int, cols: int, eps: float, 
     _check("camp_add_rmsnorm_with_plan", load().camp_add_rmsnorm_with_plan(
         _ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), int(rows), int(cols), float(eps),
         _dtype(dtype), ctypes.byref(plan), _stream(stream)))
+
+
+def camp_kv_rmsnorm_rope_cache(kv, gamma, sin, cos, slots, cache_n, cache_r, B: int, S: int,
+                               Dn: int, Dr: int, num_slots: int, eps: float, dtype,
+                               stream=None) -> None:
+    _check("camp_kv_rmsnorm_rope_cache", load().camp_kv_rmsnorm_rope_cache(
+        _ptr(kv), _ptr(gamma), _ptr(sin), _ptr(cos), _ptr(slots), _ptr(cache_n), _ptr(cache_r),
+        int(B), int(S), int(Dn), int(Dr), int(num_slots), float(eps), _dtype(dtype),
+        _stream(stream)))
+
+
+def camp_kv_rmsnorm_rope_cache_plan(kv, gamma, sin, cos, slots, cache_n, cache_r, B: int,
+                                    S: int, Dn: int, Dr: int, num_slots: int, dtype) -> Plan:
+    p = Plan()
+    _check("camp_kv_rmsnorm_rope_cache_plan", load().camp_kv_rmsnorm_rope_cache_plan(
+        _ptr(kv), _ptr(gamma), _ptr(sin), _ptr(cos), _ptr(slots), _ptr(cache_n), _ptr(cache_r),
+        int(B), int(S), int(Dn), int(Dr), int(num_slots), _dtype(dtype), ctypes.byref(p)))
+    return p
+
+
+def camp_kv_rmsnorm_rope_cache_with_plan(kv, gamma, sin, cos, slots, cache_n, cache_r, B: int,
+                                         S: int, Dn: int, Dr: int, num_slots: int, eps: float,
+                                         dtype, plan: Plan, stream=None) -> None:
+    _check("camp_kv_rmsnorm_rope_cache_with_plan", load().camp_kv_rmsnorm_rope_cache_with_plan(
+        _ptr(kv), _ptr(gamma), _ptr(sin), _ptr(cos), _ptr(slots), _ptr(cache_n), _ptr(cache_r),
+        int(B), int(S), int(Dn), int(Dr), int(num_slots), float(eps), _dtype(dtype),
+        ctypes.byref(plan), _stream(stream)))
 
 
 def camp_rope_qk(q, k, sin, cos, yq, yk, B: int, S: int, Hq: int, Hk: int, D: int, dtype,

@@ -516,6 +516,93 @@ camp_status_t rope_launch(const RopeCall& c, const camp_plan_t& p, cudaStream_t 
     return runtime_status(e);
 }
 
+// ------------------------------------------------------------------ KV RMSNorm + RoPE + cache
+
+struct KvCall {
+    camp::KvCacheArgs a;
+    DType t;
+};
+
+camp_status_t kv_validate(const void* kv, const void* gamma, const float* sin_t,
+                          const float* cos_t, const int64_t* slots, const void* cache_n,
+                          const void* cache_r, int64_t B, int64_t S, int64_t dn, int64_t dr,
+                          int64_t num_slots, camp_dtype_t dtype, KvCall* c, bool* empty) {
+    *empty = false;
+    if (!dtype_ok(dtype)) return CAMP_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || S < 0 || dn < 1 || dr < 2 || dr % 2 != 0 || num_slots < 0)
+        return CAMP_ERR_INVALID_ARG;
+    if (dn > 0x7FFFFFFF || dr > 0x7FFFFFFF) return CAMP_ERR_INVALID_ARG;
+    if (B == 0 || S == 0) { *empty = true; return CAMP_SUCCESS; }
+    if (!kv || !gamma || !sin_t || !cos_t || !slots || !cache_n || !cache_r)
+        return CAMP_ERR_INVALID_ARG;
+    const DType t = to_dtype(dtype);
+    const int64_t es = camp::elem_bytes(t);
+    int64_t tokens = 0, kv_bytes = 0, cn_bytes = 0, cr_bytes = 0, table_bytes = 0, slot_bytes = 0;
+    if (!mul_ok(B, S, 1, &tokens) || !mul_ok(tokens, dn + dr, es, &kv_bytes) ||
+        !mul_ok(num_slots, dn, es, &cn_bytes) || !mul_ok(num_slots, dr, es, &cr_bytes) ||
+        !mul_ok(S, dr / 2, 4, &table_bytes) || !mul_ok(tokens, 8, 1, &slot_bytes))
+        return CAMP_ERR_INVALID_ARG;
+    for (const void* p : {kv, gamma, cache_n, cache_r})
+        if (!aligned(p, es)) return CAMP_ERR_INVALID_ARG;
+    if (!aligned(sin_t, 4) || !aligned(cos_t, 4) || !aligned(slots, 8)) return CAMP_ERR_INVALID_ARG;
+    // The caches are outputs: disjoint from every input and from each other.
+    const void* ins[] = {kv, gamma, sin_t, cos_t, slots};
+    const int64_t in_bytes[] = {kv_bytes, dn * es, table_bytes, table_bytes, slot_bytes};
+    for (int i = 0; i < 5; ++i) {
+        if (overlaps(cache_n, cn_bytes, ins[i], in_bytes[i]) ||
+            overlaps(cache_r, cr_bytes, ins[i], in_bytes[i]))
+            return CAMP_ERR_INVALID_ARG;
+    }
+    if (overlaps(cache_n, cn_bytes, cache_r, cr_bytes)) return CAMP_ERR_INVALID_ARG;
+    c->a = camp::KvCacheArgs{kv, gamma, sin_t, cos_t, slots, const_cast<void*>(cache_n),
+                             const_cast<void*>(cache_r), tokens, S, dn, dr, num_slots, 0.0f};
+    c->t = t;
+    return CAMP_SUCCESS;
+}
+
+// 16-byte accesses when every row start and pointer allows them, else element accesses.
+int kv_vec_bytes(const KvCall& c) {
+    const int es = camp::elem_bytes(c.t);
+    const bool ok = (c.a.dn * es) % 16 == 0 && ((c.a.dr / 2) * es) % 16 == 0 &&
+                    aligned(c.a.kv, 16) && aligned(c.a.gamma, 16) && aligned(c.a.cache_n, 16) &&
+                    aligned(c.a.cache_r, 16) && aligned(c.a.sin_t, 16) && aligned(c.a.cos_t, 16);
+    return ok ? 16 : es;
+}
+
+// Norm accesses per lane for a vector width, or 0 if the row does not fit one warp
+// (at most 8 16-byte or 16 element accesses per lane for the norm part, one vector per
+// lane for each rope half).
+int kv_nvn(const KvCall& c, int vb) {
+    const int es = camp::elem_bytes(c.t);
+    const int64_t nvec = c.a.dn * es / vb;
+    const int64_t need = ceil_div(nvec, 32);
+    const int max_nvn = vb == 16 ? 8 : 16;
+    if (need > max_nvn || (c.a.dr / 2) * es / vb > 32) return 0;
+    static const int kNvn[] = {1, 2, 4, 8, 16};
+    return round_up_in(static_cast<int>(need), kNvn, 5);
+}
+
+camp_status_t kv_plan(const KvCall& c, const camp_plan_t* forced, camp_plan_t* p) {
+    *p = camp_plan_t{};
+    p->kernel = CAMP_KERNEL_KV_CACHE;
+    p->vec_bytes = forced ? forced->vec_bytes : kv_vec_bytes(c);
+    const int es = camp::elem_bytes(c.t);
+    if (p->vec_bytes != 16 && p->vec_bytes != es) return CAMP_ERR_NOT_SUPPORTED;
+    if (p->vec_bytes > kv_vec_bytes(c)) return CAMP_ERR_NOT_SUPPORTED;
+    const int need = kv_nvn(c, p->vec_bytes);
+    if (need == 0) return CAMP_ERR_NOT_SUPPORTED;
+    p->per_thread = forced ? forced->per_thread : need;
+    if (p->per_thread < need) return CAMP_ERR_NOT_SUPPORTED;
+    const int pt = p->per_thread;
+    if (!(pt == 1 || pt == 2 || pt == 4 || pt == 8 || (pt == 16 && p->vec_bytes != 16)))
+        return CAMP_ERR_NOT_SUPPORTED;
+    p->group = 32;
+    p->block = camp::kKvBlock;
+    p->cluster = 1;
+    p->grid = ceil_div(c.a.tokens, camp::kKvTokensPerCta);
+    return CAMP_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -624,6 +711,48 @@ CAMP_API camp_status_t camp_add_rmsnorm_with_plan(const void* x, const void* r, 
     st = rms_accept_plan(c, *plan, &p);
     if (st != CAMP_SUCCESS) return st;
     return rms_launch(c, p, static_cast<cudaStream_t>(stream));
+}
+
+CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_plan(
+    const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
+    const void* cache_n, const void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
+    int64_t num_slots, camp_dtype_t dtype, camp_plan_t* plan) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    KvCall c;
+    bool empty = false;
+    camp_status_t st = kv_validate(kv, gamma, sin, cos, slots, cache_n, cache_r, B, S, Dn, Dr,
+                                   num_slots, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (empty) { *plan = camp_plan_t{}; return CAMP_SUCCESS; }
+    return kv_plan(c, nullptr, plan);
+}
+
+CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_with_plan(
+    const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
+    void* cache_n, void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
+    int64_t num_slots, float eps, camp_dtype_t dtype, const camp_plan_t* plan, void* stream) {
+    KvCall c;
+    bool empty = false;
+    camp_status_t st = kv_validate(kv, gamma, sin, cos, slots, cache_n, cache_r, B, S, Dn, Dr,
+                                   num_slots, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (!eps_ok(eps)) return CAMP_ERR_INVALID_ARG;
+    if (empty) return CAMP_SUCCESS;
+    c.a.eps = eps;
+    camp_plan_t p;
+    st = kv_plan(c, plan, &p);
+    if (st != CAMP_SUCCESS) return st;
+    return runtime_status(camp::kv_cache_launch(c.t, p.vec_bytes, p.per_thread, c.a,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache(
+    const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
+    void* cache_n, void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
+    int64_t num_slots, float eps, camp_dtype_t dtype, void* stream) {
+    return camp_kv_rmsnorm_rope_cache_with_plan(kv, gamma, sin, cos, slots, cache_n, cache_r,
+                                                B, S, Dn, Dr, num_slots, eps, dtype, nullptr,
+                                                stream);
 }
 
 CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* cos, void* y,

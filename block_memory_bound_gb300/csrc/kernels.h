@@ -122,4 +122,30 @@ cudaError_t rope_tiled_launch(DType t, int vec_bytes, int heads_per_thread, cons
 cudaError_t rope_flat_launch(DType t, int vec_bytes, int heads_per_thread, const RopeArgs& a,
                              int64_t grid, cudaStream_t s);
 
+// ------------------------------------------------------------------ KV RMSNorm + RoPE + cache
+// One warp per token of kv[tokens, dn + dr]: RMSNorm of the first dn elements into row
+// slots[t] of cache_n[num_slots, dn], rotate-half RoPE of the last dr into cache_r.
+struct KvCacheArgs {
+    const void* kv;
+    const void* gamma;
+    const float* sin_t;
+    const float* cos_t;
+    const int64_t* slots;
+    void* cache_n;
+    void* cache_r;
+    int64_t tokens;     // B * S
+    int64_t seq;        // S
+    int64_t dn;         // norm width
+    int64_t dr;         // rope width (even)
+    int64_t num_slots;
+    float eps;
+};
+
+constexpr int kKvBlock = 256;
+constexpr int kKvTokensPerCta = kKvBlock / 32;   // one warp per token
+
+// `nvn`: norm accesses per lane (1, 2, 4, 8; 16 on the element path only).
+cudaError_t kv_cache_launch(DType t, int vec_bytes, int nvn, const KvCacheArgs& a,
+                            cudaStream_t s);
+
 }  // namespace camp

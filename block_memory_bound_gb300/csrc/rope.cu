@@ -26,43 +26,6 @@
 namespace camp {
 namespace {
 
-// a*b - c*d
-__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
-    const float p = __fmul_rn(c, d);
-    const float e = fmaf(c, d, -p);
-    const float f = fmaf(a, b, -p);
-    return __fsub_rn(f, e);
-}
-
-// a*b + c*d
-__device__ __forceinline__ float sum_of_products(float a, float b, float c, float d) {
-    const float p = __fmul_rn(c, d);
-    const float e = fmaf(c, d, -p);
-    const float f = fmaf(a, b, p);
-    return __fadd_rn(f, e);
-}
-
-// N consecutive fp32 table values through the read-only path, in the widest aligned
-// accesses (the host guarantees alignment to min(16, 4N) bytes).
-template <int N>
-__device__ __forceinline__ void load_table(const float* p, float (&out)[N]) {
-    if constexpr (N % 4 == 0) {
-#pragma unroll
-        for (int k = 0; k < N / 4; ++k) {
-            const Raw<16> r = ld_shared_ro<16>(p + 4 * k);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) out[4 * k + i] = __uint_as_float(r.w[i]);
-        }
-    } else if constexpr (N == 2) {
-        const Raw<8> r = ld_shared_ro<8>(p);
-        out[0] = __uint_as_float(r.w[0]);
-        out[1] = __uint_as_float(r.w[1]);
-    } else {
-        static_assert(N == 1, "table accesses are 1, 2 or a multiple of 4 floats");
-        out[0] = __uint_as_float(ld_shared_ro<4>(p).w[0]);
-    }
-}
-
 // Rotate one head's vector pair (j of each half) and store it.
 template <typename S, int VB>
 __device__ __forceinline__ void rotate_store(const Raw<VB>& lo, const Raw<VB>& hi,

@@ -44,6 +44,13 @@ def rope_qk_bytes(B: int, S: int, Hq: int, Hk: int, D: int, dtype: str = "bf16")
     return 2 * B * S * (Hq + Hk) * D * es + 2 * S * (D // 2) * 4
 
 
+def kv_cache_bytes(B: int, S: int, Dn: int, Dr: int, dtype: str = "bf16") -> int:
+    """KV RMSNorm + RoPE + cache scatter with every token written: kv read once, both cache
+    rows written once, gamma, the tables and the int64 slot array read once."""
+    es = ELEM_BYTES[dtype]
+    return 2 * B * S * (Dn + Dr) * es + Dn * es + 2 * S * (Dr // 2) * 4 + 8 * B * S
+
+
 def rope_flops(B: int, S: int, H: int, D: int) -> int:
     # per pair: 4 multiplies + 2 add/sub = 6 FLOP, i.e. 3 FLOP per element
     return 3 * B * S * H * D

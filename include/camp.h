@@ -161,6 +161,38 @@ CAMP_API camp_status_t camp_rope_qk(const void* q, const void* k, const float* s
                                     int64_t Hq, int64_t Hk, int64_t D, camp_dtype_t dtype,
                                     void* stream);
 
+/*
+ * Fused KV RMSNorm + RoPE + cache scatter. The TileLang tutorial (ch. 02, section 1.2)
+ * describes Ascend's KvRmsNormRopeCache operator: the last axis of the kv tensor is split,
+ * the left part goes through RMSNorm, the right part through RoPE, and the two results are
+ * scattered into two caches (paged caches are addressed by block tables). Here:
+ *
+ *   kv       [B, S, Dn + Dr]  one KV head per token (as in multi-head latent attention),
+ *                             storage type `dtype`.
+ *   gamma    [Dn]             RMSNorm weight, storage type `dtype`.
+ *   sin, cos [S, Dr/2]        fp32 RoPE tables; token (b, s) uses row s.
+ *   slots    [B*S] int64      destination row of token t = b*S + s in both caches (a paged
+ *                             cache is addressed as block * block_size + offset). A slot
+ *                             outside [0, num_slots) means "do not write" (padding); two
+ *                             tokens with the same slot race, so slots must be distinct.
+ *   cache_n  [num_slots, Dn]  receives RMSNorm(kv[t, :Dn]) * gamma (camp_rmsnorm's
+ *                             arithmetic, one rounding).
+ *   cache_r  [num_slots, Dr]  receives rotate-half RoPE of kv[t, Dn:] (camp_rope's
+ *                             arithmetic, one rounding).
+ *   Dn >= 1; Dr even, >= 2; eps as for camp_rmsnorm. B*S == 0 is a no-op.
+ *
+ * One read of kv, one write of each cache row. Supported widths: up to 256 x 16-byte
+ * vectors for the norm part and 32 per rope half (bf16: Dn <= 2048, Dr <= 512; element
+ * accesses: Dn <= 512, Dr <= 64); otherwise CAMP_ERR_NOT_SUPPORTED. The caches must be
+ * disjoint from every input and from each other. Errors as for camp_rmsnorm.
+ */
+CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache(const void* kv, const void* gamma,
+                                                  const float* sin, const float* cos,
+                                                  const int64_t* slots, void* cache_n,
+                                                  void* cache_r, int64_t B, int64_t S,
+                                                  int64_t Dn, int64_t Dr, int64_t num_slots,
+                                                  float eps, camp_dtype_t dtype, void* stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 CAMP_API const char* camp_status_string(camp_status_t status);
 
@@ -181,7 +213,8 @@ typedef enum {
     CAMP_KERNEL_ROPE = 3,           /* tiled: a CTA covers whole positions, all their heads */
     CAMP_KERNEL_ROPE_FLAT = 4,      /* any shape: one work item per (position, heads, vector) */
     CAMP_KERNEL_ROPE_SPLIT = 5,     /* camp_rope_qk only: Q and K as two separate launches */
-    CAMP_KERNEL_RMSNORM_CLUSTER = 6 /* a cluster of CTAs per row, sums combined over DSMEM */
+    CAMP_KERNEL_RMSNORM_CLUSTER = 6, /* a cluster of CTAs per row, sums combined over DSMEM */
+    CAMP_KERNEL_KV_CACHE = 7        /* camp_kv_rmsnorm_rope_cache: one warp per token */
 } camp_kernel_t;
 
 typedef struct {
@@ -249,6 +282,20 @@ CAMP_API camp_status_t camp_add_rmsnorm_with_plan(const void* x, const void* r, 
                                                   void* h, void* y, int64_t rows, int64_t cols,
                                                   float eps, camp_dtype_t dtype,
                                                   const camp_plan_t* plan, void* stream);
+
+/* Like camp_rmsnorm_plan, for camp_kv_rmsnorm_rope_cache (vec_bytes, per_thread = norm
+ * accesses per lane; group = 32 threads, one warp per token). */
+CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_plan(
+    const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
+    const void* cache_n, const void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
+    int64_t num_slots, camp_dtype_t dtype, camp_plan_t* plan);
+
+/* camp_kv_rmsnorm_rope_cache with an explicit plan (vec_bytes, per_thread); NULL plan = the
+ * default one. */
+CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_with_plan(
+    const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
+    void* cache_n, void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
+    int64_t num_slots, float eps, camp_dtype_t dtype, const camp_plan_t* plan, void* stream);
 
 #ifdef __cplusplus
 }

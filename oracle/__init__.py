@@ -62,6 +62,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_rmsnorm.restype = c_int
     lib.oracle_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i64, dbl, c_int, c_int]
     lib.oracle_add_rmsnorm.restype = c_int
+    lib.oracle_kv_rmsnorm_rope_cache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                                 i64, i64, dbl, c_int]
+    lib.oracle_kv_rmsnorm_rope_cache.restype = c_int
     lib.oracle_rope_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64]
     lib.oracle_rope_f64.restype = c_int
     lib.oracle_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, c_int]
@@ -166,6 +169,33 @@ def add_rmsnorm(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: float, dtype: 
     _check(lib.oracle_add_rmsnorm(_ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), rows, cols,
                                   float(eps), code, int(nthreads)), "add_rmsnorm")
     return h, y
+
+
+def kv_rmsnorm_rope_cache(kv: np.ndarray, gamma: np.ndarray, sin_t: np.ndarray,
+                          cos_t: np.ndarray, slots: np.ndarray, cache_n: np.ndarray,
+                          cache_r: np.ndarray, Dn: int, eps: float, dtype: str,
+                          lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """Copies of (cache_n, cache_r) after scattering RMSNorm(kv[..., :Dn]) * gamma and the
+    rotate-half RoPE of kv[..., Dn:] of every token to the row its slot names."""
+    lib = lib or load()
+    code, npt = _storage(dtype)
+    kv = np.ascontiguousarray(kv)
+    B, S, W = kv.shape
+    Dr = W - Dn
+    gamma = np.ascontiguousarray(gamma)
+    sin_t = np.ascontiguousarray(sin_t, dtype=np.float32)
+    cos_t = np.ascontiguousarray(cos_t, dtype=np.float32)
+    slots = np.ascontiguousarray(slots, dtype=np.int64)
+    cn = np.array(cache_n, copy=True, order="C")
+    cr = np.array(cache_r, copy=True, order="C")
+    assert kv.dtype == npt and gamma.dtype == npt and cn.dtype == npt and cr.dtype == npt
+    assert gamma.shape == (Dn,) and slots.shape == (B * S,)
+    assert sin_t.shape == (S, Dr // 2) and cos_t.shape == (S, Dr // 2)
+    assert cn.shape[1] == Dn and cr.shape[1] == Dr and cn.shape[0] == cr.shape[0]
+    _check(lib.oracle_kv_rmsnorm_rope_cache(
+        _ptr(kv), _ptr(gamma), _ptr(sin_t), _ptr(cos_t), _ptr(slots), _ptr(cn), _ptr(cr),
+        B, S, Dn, Dr, cn.shape[0], float(eps), code), "kv_rmsnorm_rope_cache")
+    return cn, cr
 
 
 def rope_f64(x, sin_t, cos_t, lib: ctypes.CDLL | None = None) -> np.ndarray:

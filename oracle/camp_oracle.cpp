@@ -20,6 +20,14 @@
 //       h[r,j] = round(x[r,j] + r[r,j])         (the exact sum, one rounding)
 //       y      = RMSNorm(h as stored) * w       (as above)
 //
+//   KV RMSNorm + RoPE + cache scatter  (TileLang tutorial ch. 02, section 1.2, describing
+//            Ascend's KvRmsNormRopeCache: split the kv tail axis, RMSNorm the left part,
+//            RoPE the right part, scatter both into two caches)
+//       for token t = b*S + s with 0 <= slots[t] < num_slots:
+//       cache_n[slots[t], :] = RMSNorm(kv[t, :Dn]) * gamma      (as above)
+//       cache_r[slots[t], :] = rotate-half RoPE of kv[t, Dn:] with table row s (below)
+//       other cache rows are left as they are.
+//
 //   RoPE, rotate-half  (gollamago README, "RoPE": rope(input, sin_table, cos_table),
 //            input [batch, sequence, heads, head_dim], tables [sequence, head_dim/2],
 //            each head split into two halves and rotated; tilelang tutorial ch. 02,
@@ -244,6 +252,44 @@ int oracle_add_rmsnorm(const void* x, const void* r, const void* w, void* h, voi
             for (int64_t j = 0; j < cols; ++j) store_elem(y, row * cols + j, yr[j], dtype);
         }
     });
+    return 0;
+}
+
+// KV RMSNorm + RoPE + cache scatter over storage-typed kv [B, S, Dn + Dr], gamma [Dn] and
+// caches [num_slots, Dn] / [num_slots, Dr] (updated in place), fp32 tables [S, Dr/2] and
+// int64 slots [B*S]. Tokens whose slot is outside [0, num_slots) are skipped.
+int oracle_kv_rmsnorm_rope_cache(const void* kv, const void* gamma, const float* sin_t,
+                                 const float* cos_t, const int64_t* slots, void* cache_n,
+                                 void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
+                                 int64_t num_slots, double eps, int dtype) {
+    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (B < 0 || S < 0 || Dn < 1 || Dr < 2 || Dr % 2 != 0 || num_slots < 0 || !(eps >= 0.0))
+        return 1;
+    if (B * S == 0) return 0;
+    if (!kv || !gamma || !sin_t || !cos_t || !slots || !cache_n || !cache_r) return 1;
+    const int64_t half = Dr / 2;
+    std::vector<double> g(static_cast<size_t>(Dn)), xn(static_cast<size_t>(Dn)),
+        yn(static_cast<size_t>(Dn)), xr(static_cast<size_t>(Dr)), yr(static_cast<size_t>(Dr)),
+        sn(static_cast<size_t>(half)), c(static_cast<size_t>(half));
+    for (int64_t j = 0; j < Dn; ++j) g[j] = load_elem(gamma, j, dtype);
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t s = 0; s < S; ++s) {
+            const int64_t t = b * S + s;
+            const int64_t slot = slots[t];
+            if (slot < 0 || slot >= num_slots) continue;
+            const int64_t base = t * (Dn + Dr);
+            for (int64_t j = 0; j < Dn; ++j) xn[j] = load_elem(kv, base + j, dtype);
+            for (int64_t j = 0; j < Dr; ++j) xr[j] = load_elem(kv, base + Dn + j, dtype);
+            for (int64_t i = 0; i < half; ++i) {
+                sn[i] = static_cast<double>(sin_t[s * half + i]);
+                c[i] = static_cast<double>(cos_t[s * half + i]);
+            }
+            rmsnorm_row(xn.data(), g.data(), yn.data(), Dn, eps);
+            rope_head(xr.data(), sn.data(), c.data(), yr.data(), half);
+            for (int64_t j = 0; j < Dn; ++j) store_elem(cache_n, slot * Dn + j, yn[j], dtype);
+            for (int64_t j = 0; j < Dr; ++j) store_elem(cache_r, slot * Dr + j, yr[j], dtype);
+        }
+    }
     return 0;
 }
 

@@ -367,3 +367,42 @@ def test_add_rmsnorm_unbuilt_variant_is_refused(lib):
     st = lib.camp_add_rmsnorm_with_plan(X, R_, W, H_, Y, 4, 65536, ctypes.c_float(1e-5),
                                         camp.BF16, ctypes.byref(p), None)
     assert st == camp.ERR_NOT_SUPPORTED
+
+
+# ------------------------------------------------------------------ KV RMSNorm + RoPE + cache
+
+KVP = [0x7E0000000000 + i * 0x1000000000 for i in range(7)]   # kv, gamma, sin, cos, slots, cn, cr
+
+
+def _kv(lib, ptrs=None, B=1, S=16, Dn=512, Dr=64, ns=64, eps=1e-5, dtype=camp.BF16):
+    p = list(KVP if ptrs is None else ptrs)
+    return lib.camp_kv_rmsnorm_rope_cache(*p, B, S, Dn, Dr, ns, ctypes.c_float(eps), dtype, None)
+
+
+@pytest.mark.parametrize("change,kw,status", [
+    ({}, {"dtype": 4}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({}, {"Dr": 63}, camp.ERR_INVALID_ARG),
+    ({}, {"Dr": 0}, camp.ERR_INVALID_ARG),
+    ({}, {"Dn": 0}, camp.ERR_INVALID_ARG),
+    ({}, {"ns": -1}, camp.ERR_INVALID_ARG),
+    ({}, {"eps": math.nan}, camp.ERR_INVALID_ARG),
+    ({4: None}, {}, camp.ERR_INVALID_ARG),                      # no slots
+    ({4: KVP[4] + 4}, {}, camp.ERR_INVALID_ARG),                # slots not 8-byte aligned
+    ({5: KVP[0]}, {}, camp.ERR_INVALID_ARG),                    # cache over kv
+    ({6: KVP[5] + 64}, {}, camp.ERR_INVALID_ARG),               # the caches overlap
+    ({6: KVP[2]}, {}, camp.ERR_INVALID_ARG),                    # cache over a table
+    ({}, {"Dn": 4096}, camp.ERR_NOT_SUPPORTED),                 # norm part wider than a warp holds
+])
+def test_kv_cache_argument_errors(lib, change, kw, status):
+    ptrs = list(KVP)
+    for i, v in change.items():
+        ptrs[i] = v
+    assert _kv(lib, ptrs, **kw) == status
+
+
+def test_kv_cache_plans(lib):
+    p = camp.camp_kv_rmsnorm_rope_cache_plan(*KVP, 1, 65536, 512, 64, 131072, "bf16")
+    assert (p.kernel, p.vec_bytes, p.group, p.per_thread, p.grid) == (camp.KERNEL_KV_CACHE, 16, 32, 2, 8192)
+    p = camp.camp_kv_rmsnorm_rope_cache_plan(*KVP, 2, 3, 33, 6, 8, "bf16")   # odd widths
+    assert (p.vec_bytes, p.per_thread) == (2, 2)
+    assert _kv(lib, B=0) == camp.SUCCESS

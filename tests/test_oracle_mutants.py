@@ -44,6 +44,12 @@ MUTANTS = {
         ("if (E < -126) E = -126;", "if (E < -127) E = -127;"),
     "add path normalizes x instead of h":
         ("hr[j] = load_elem(h, i, dtype);", "hr[j] = load_elem(x, i, dtype);"),
+    "cache scatter uses the token index instead of its slot":
+        ("store_elem(cache_n, slot * Dn + j, yn[j], dtype);",
+         "store_elem(cache_n, (t % num_slots) * Dn + j, yn[j], dtype);"),
+    "cache rope part uses the batch's first table row":
+        ("sn[i] = static_cast<double>(sin_t[s * half + i]);\n                c[i] = static_cast<double>(cos_t[s * half + i]);\n            }\n            rmsnorm_row",
+         "sn[i] = static_cast<double>(sin_t[0 * s * half + i]);\n                c[i] = static_cast<double>(cos_t[0 * s * half + i]);\n            }\n            rmsnorm_row"),
     "add path normalizes the unrounded sum":
         ("hr[j] = load_elem(h, i, dtype);",
          "hr[j] = load_elem(x, i, dtype) + load_elem(r, i, dtype);"),
@@ -69,6 +75,8 @@ def _battery(lib):
         ("rope interleaved", lambda: pins.test_rope_rotate_half_equals_interleaved_on_deinterleaved_input(lib)),
         ("rope storage", lambda: pins.test_rope_storage_path_rounds_the_fp64_result_once(lib, "f32")),
         ("rope single rounding", lambda: pins.test_rope_single_rounding_crafted_case(lib)),
+        ("kv cache", lambda: [pins.test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, d)
+                              for d in ("bf16", "f32")]),
         ("add rmsnorm", lambda: [pins.test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, d)
                                  for d in ("bf16", "f32")]),
     ]

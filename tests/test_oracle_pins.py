@@ -275,6 +275,44 @@ def test_add_rmsnorm_zero_residual_is_rmsnorm(lib):
     np.testing.assert_array_equal(y, oracle.rmsnorm(xs, ws, 1e-5, "bf16", lib=lib))
 
 
+# ------------------------------------------------------------------------ KV norm + rope + cache
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, dtype):
+    # Every written cache row must equal the (separately pinned) RMSNorm of the token's left
+    # part and rotate-half RoPE of its right part with table row s; padding slots (negative
+    # or past the end) and rows no token names stay as they were.
+    rng = np.random.default_rng(41)
+    B, S, Dn, Dr, nslots = 2, 5, 24, 8, 16
+    kvt, kvs = _storage_pair(rng, (B, S, Dn + Dr), dtype)
+    _, gs = _storage_pair(rng, (Dn,), dtype)
+    sin_t = rng.uniform(-1, 1, (S, Dr // 2)).astype(np.float32)
+    cos_t = rng.uniform(-1, 1, (S, Dr // 2)).astype(np.float32)
+    slots = rng.permutation(nslots)[:B * S].astype(np.int64)
+    slots[3] = -1
+    slots[7] = nslots + 2
+    _, cn0 = _storage_pair(rng, (nslots, Dn), dtype)
+    _, cr0 = _storage_pair(rng, (nslots, Dr), dtype)
+    cn, cr = oracle.kv_rmsnorm_rope_cache(kvs, gs, sin_t, cos_t, slots, cn0, cr0, Dn, 1e-5,
+                                          dtype, lib=lib)
+    written = set()
+    for t in range(B * S):
+        b, s_ = divmod(t, S)
+        slot = int(slots[t])
+        if not 0 <= slot < nslots:
+            continue
+        written.add(slot)
+        tok = kvs[b, s_]
+        want_n = oracle.rmsnorm(tok[None, :Dn], gs, 1e-5, dtype, lib=lib)[0]
+        want_r = oracle.rope(tok[None, None, None, Dn:], sin_t[s_:s_ + 1], cos_t[s_:s_ + 1],
+                             dtype, lib=lib)[0, 0, 0]
+        np.testing.assert_array_equal(cn[slot], want_n)
+        np.testing.assert_array_equal(cr[slot], want_r)
+    for slot in set(range(nslots)) - written:
+        np.testing.assert_array_equal(cn[slot], cn0[slot])
+        np.testing.assert_array_equal(cr[slot], cr0[slot])
+
+
 # ------------------------------------------------------------------------ RoPE
 
 def _tables(S, half, angle_fn, dtype=np.float64):
