@@ -334,6 +334,7 @@ def large_configs(peak: float, reps: int) -> list[dict]:
         ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),
         ("rope_qk bf16 Q[1,65536,32,128] + K[1,65536,8,128]", "rope_qk", (65536, 32, 8, 128)),
         ("kv rmsnorm+rope+cache bf16 kv[1,65536,512+64] -> 131072 slots", "kv", (65536, 512, 64)),
+        ("rope interleaved bf16 x[65536,32,128], random positions < 131072", "ril", (65536, 32, 128)),
     ]
     stream = torch.cuda.current_stream().cuda_stream
     for name, kind, shp in cases:
@@ -357,6 +358,21 @@ def large_configs(peak: float, reps: int) -> list[dict]:
             fn = lambda: camp.camp_add_rmsnorm(x.data_ptr(), r.data_ptr(), w.data_ptr(),
                                                h.data_ptr(), y.data_ptr(), rows, cols, 1e-5,
                                                camp.BF16, stream)
+        elif kind == "ril":
+            T, H, D = shp
+            mp = 2 * T
+            x = torch.randn(T, H, D, device="cuda").to(torch.bfloat16)
+            y = torch.empty_like(x)
+            sn = torch.empty(mp, D // 2, device="cuda")
+            cs = torch.empty(mp, D // 2, device="cuda")
+            camp.camp_rope_tables(sn, cs, mp, D, THETA, stream)
+            pos = torch.randint(0, mp, (T,), device="cuda", dtype=torch.int32)
+            nbytes = 2 * T * H * D * 2 + 2 * T * (D // 2) * 4 + 4 * T
+            plan = camp.camp_rope_interleaved_plan(x, sn, cs, pos, y, T, H, D, mp, "bf16")
+            pname = f"rope_interleaved<bf16,vec{plan.vec_bytes},hpt{plan.group}>"
+            fn = lambda: camp.camp_rope_interleaved(x.data_ptr(), sn.data_ptr(), cs.data_ptr(),
+                                                    pos.data_ptr(), y.data_ptr(), T, H, D, mp,
+                                                    camp.BF16, stream)
         elif kind == "kv":
             S, Dn, Dr = shp
             ns = 2 * S

@@ -37,6 +37,7 @@ KERNEL_ROPE_FLAT = 4
 KERNEL_ROPE_SPLIT = 5
 KERNEL_RMSNORM_CLUSTER = 6
 KERNEL_KV_CACHE = 7
+KERNEL_ROPE_INTERLEAVED = 8
 
 # Every symbol include/camp.h declares.
 EXPORTS = (
@@ -46,6 +47,8 @@ EXPORTS = (
     "camp_add_rmsnorm", "camp_add_rmsnorm_plan", "camp_add_rmsnorm_with_plan",
     "camp_kv_rmsnorm_rope_cache", "camp_kv_rmsnorm_rope_cache_plan",
     "camp_kv_rmsnorm_rope_cache_with_plan",
+    "camp_rope_interleaved", "camp_rope_interleaved_plan", "camp_rope_interleaved_with_plan",
+    "camp_rope_tables",
 )
 
 
@@ -119,6 +122,15 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_add_rmsnorm_with_plan.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, c_int,
                                                    pplan, vp]
         lib.camp_add_rmsnorm_with_plan.restype = c_int
+        ilsig = [vp, vp, vp, vp, vp, i64, i64, i64, i64, c_int]
+        lib.camp_rope_interleaved.argtypes = ilsig + [vp]
+        lib.camp_rope_interleaved.restype = c_int
+        lib.camp_rope_interleaved_plan.argtypes = ilsig + [pplan]
+        lib.camp_rope_interleaved_plan.restype = c_int
+        lib.camp_rope_interleaved_with_plan.argtypes = ilsig + [pplan, vp]
+        lib.camp_rope_interleaved_with_plan.restype = c_int
+        lib.camp_rope_tables.argtypes = [vp, vp, i64, i64, ctypes.c_double, vp]
+        lib.camp_rope_tables.restype = c_int
         kvsig = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64]
         lib.camp_kv_rmsnorm_rope_cache.argtypes = kvsig + [f32, c_int, vp]
         lib.camp_kv_rmsnorm_rope_cache.restype = c_int
@@ -281,6 +293,34 @@ def camp_kv_rmsnorm_rope_cache_with_plan(kv, gamma, sin, cos, slots, cache_n, ca
         _ptr(kv), _ptr(gamma), _ptr(sin), _ptr(cos), _ptr(slots), _ptr(cache_n), _ptr(cache_r),
         int(B), int(S), int(Dn), int(Dr), int(num_slots), float(eps), _dtype(dtype),
         ctypes.byref(plan), _stream(stream)))
+
+
+def camp_rope_interleaved(x, sin, cos, positions, y, tokens: int, H: int, D: int, max_pos: int,
+                          dtype, stream=None) -> None:
+    _check("camp_rope_interleaved", load().camp_rope_interleaved(
+        _ptr(x), _ptr(sin), _ptr(cos), _ptr(positions), _ptr(y), int(tokens), int(H), int(D),
+        int(max_pos), _dtype(dtype), _stream(stream)))
+
+
+def camp_rope_interleaved_plan(x, sin, cos, positions, y, tokens: int, H: int, D: int,
+                               max_pos: int, dtype) -> Plan:
+    p = Plan()
+    _check("camp_rope_interleaved_plan", load().camp_rope_interleaved_plan(
+        _ptr(x), _ptr(sin), _ptr(cos), _ptr(positions), _ptr(y), int(tokens), int(H), int(D),
+        int(max_pos), _dtype(dtype), ctypes.byref(p)))
+    return p
+
+
+def camp_rope_interleaved_with_plan(x, sin, cos, positions, y, tokens: int, H: int, D: int,
+                                    max_pos: int, dtype, plan: Plan, stream=None) -> None:
+    _check("camp_rope_interleaved_with_plan", load().camp_rope_interleaved_with_plan(
+        _ptr(x), _ptr(sin), _ptr(cos), _ptr(positions), _ptr(y), int(tokens), int(H), int(D),
+        int(max_pos), _dtype(dtype), ctypes.byref(plan), _stream(stream)))
+
+
+def camp_rope_tables(sin, cos, max_pos: int, D: int, theta: float, stream=None) -> None:
+    _check("camp_rope_tables", load().camp_rope_tables(
+        _ptr(sin), _ptr(cos), int(max_pos), int(D), float(theta), _stream(stream)))
 
 
 def camp_rope_qk(q, k, sin, cos, yq, yk, B: int, S: int, Hq: int, Hk: int, D: int, dtype,

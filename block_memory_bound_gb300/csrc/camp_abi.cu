@@ -603,6 +603,84 @@ camp_status_t kv_plan(const KvCall& c, const camp_plan_t* forced, camp_plan_t* p
     return CAMP_SUCCESS;
 }
 
+// ------------------------------------------------------------------ interleaved RoPE
+
+struct RopeIlCall {
+    camp::RopeInterleavedArgs a;
+    DType t;
+};
+
+camp_status_t rope_il_validate(const void* x, const float* sin_t, const float* cos_t,
+                               const int32_t* positions, const void* y, int64_t tokens,
+                               int64_t H, int64_t D, int64_t max_pos, camp_dtype_t dtype,
+                               RopeIlCall* c, bool* empty) {
+    *empty = false;
+    if (!dtype_ok(dtype)) return CAMP_ERR_UNSUPPORTED_DTYPE;
+    if (tokens < 0 || H < 0 || D < 2 || D % 2 != 0 || max_pos < 0) return CAMP_ERR_INVALID_ARG;
+    if (H > 0x7FFFFFFF || D > 0x7FFFFFFF) return CAMP_ERR_INVALID_ARG;
+    if (tokens == 0 || H == 0) { *empty = true; return CAMP_SUCCESS; }
+    if (!x || !sin_t || !cos_t || !positions || !y) return CAMP_ERR_INVALID_ARG;
+    const DType t = to_dtype(dtype);
+    const int64_t es = camp::elem_bytes(t);
+    int64_t rows = 0, bytes = 0, table_bytes = 0, pos_bytes = 0;
+    if (!mul_ok(tokens, H, 1, &rows) || !mul_ok(rows, D, es, &bytes) ||
+        !mul_ok(max_pos, D / 2, 4, &table_bytes) || !mul_ok(tokens, 4, 1, &pos_bytes))
+        return CAMP_ERR_INVALID_ARG;
+    if (!aligned(x, es) || !aligned(y, es) || !aligned(sin_t, 4) || !aligned(cos_t, 4) ||
+        !aligned(positions, 4))
+        return CAMP_ERR_INVALID_ARG;
+    if (y != x && overlaps(y, bytes, x, bytes)) return CAMP_ERR_INVALID_ARG;
+    if (overlaps(y, bytes, sin_t, table_bytes) || overlaps(y, bytes, cos_t, table_bytes) ||
+        overlaps(y, bytes, positions, pos_bytes))
+        return CAMP_ERR_INVALID_ARG;
+    c->a = camp::RopeInterleavedArgs{x, sin_t, cos_t, positions, const_cast<void*>(y), tokens,
+                                     H, D, max_pos};
+    c->t = t;
+    return CAMP_SUCCESS;
+}
+
+bool rope_il_vec_ok(const RopeIlCall& c, int vb) {
+    const int es = camp::elem_bytes(c.t);
+    if (vb < 2 * es) return false;                           // a vector holds whole pairs
+    if ((c.a.dim * es) % vb != 0) return false;
+    const int pairs = vb / es / 2;
+    const int table_align = pairs * 4 < 16 ? pairs * 4 : 16;
+    return aligned(c.a.x, vb) && aligned(c.a.y, vb) && aligned(c.a.sin_t, table_align) &&
+           aligned(c.a.cos_t, table_align);
+}
+
+int64_t rope_il_tpc(const RopeIlCall& c, int vb, int hpt) {
+    const int es = camp::elem_bytes(c.t);
+    const int64_t per_pos = ceil_div(c.a.heads, hpt) * (c.a.dim * es / vb);
+    return per_pos <= camp::kRopeBlock ? camp::kRopeBlock / per_pos : 0;
+}
+
+// Widest legal vector; 2 heads per thread (1 for odd head counts), more when a token's
+// heads would not fit one CTA; CAMP_ERR_NOT_SUPPORTED when even 8 do not.
+camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_plan_t* p) {
+    *p = camp_plan_t{};
+    p->kernel = CAMP_KERNEL_ROPE_INTERLEAVED;
+    p->cluster = 1;
+    p->block = camp::kRopeBlock;
+    if (forced) {
+        p->vec_bytes = forced->vec_bytes;
+        p->group = forced->group;
+        if (!rope_il_vec_ok(c, p->vec_bytes)) return CAMP_ERR_NOT_SUPPORTED;
+    } else {
+        for (int vb : {16, 8, 4}) {
+            if (rope_il_vec_ok(c, vb)) { p->vec_bytes = vb; break; }
+        }
+        if (p->vec_bytes == 0) return CAMP_ERR_NOT_SUPPORTED;   // pointers not pair-aligned
+        p->group = c.a.heads % 2 == 0 ? 2 : 1;
+        while (p->group < 8 && rope_il_tpc(c, p->vec_bytes, p->group) == 0) p->group *= 2;
+    }
+    if (!camp::rope_interleaved_compiled(c.t, p->vec_bytes, p->group)) return CAMP_ERR_NOT_SUPPORTED;
+    const int64_t tpc = rope_il_tpc(c, p->vec_bytes, p->group);
+    if (tpc == 0 || c.a.tokens > 0xFFFFFFFFll) return CAMP_ERR_NOT_SUPPORTED;
+    p->grid = ceil_div(c.a.tokens, tpc);
+    return CAMP_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -753,6 +831,61 @@ CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache(
     return camp_kv_rmsnorm_rope_cache_with_plan(kv, gamma, sin, cos, slots, cache_n, cache_r,
                                                 B, S, Dn, Dr, num_slots, eps, dtype, nullptr,
                                                 stream);
+}
+
+CAMP_API camp_status_t camp_rope_interleaved_plan(const void* x, const float* sin,
+                                                  const float* cos, const int32_t* positions,
+                                                  const void* y, int64_t tokens, int64_t H,
+                                                  int64_t D, int64_t max_pos, camp_dtype_t dtype,
+                                                  camp_plan_t* plan) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    RopeIlCall c;
+    bool empty = false;
+    camp_status_t st = rope_il_validate(x, sin, cos, positions, y, tokens, H, D, max_pos, dtype,
+                                        &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (empty) { *plan = camp_plan_t{}; return CAMP_SUCCESS; }
+    return rope_il_plan(c, nullptr, plan);
+}
+
+CAMP_API camp_status_t camp_rope_interleaved_with_plan(const void* x, const float* sin,
+                                                       const float* cos,
+                                                       const int32_t* positions, void* y,
+                                                       int64_t tokens, int64_t H, int64_t D,
+                                                       int64_t max_pos, camp_dtype_t dtype,
+                                                       const camp_plan_t* plan, void* stream) {
+    RopeIlCall c;
+    bool empty = false;
+    camp_status_t st = rope_il_validate(x, sin, cos, positions, y, tokens, H, D, max_pos, dtype,
+                                        &c, &empty);
+    if (st != CAMP_SUCCESS || empty) return st;
+    camp_plan_t p;
+    st = rope_il_plan(c, plan, &p);
+    if (st != CAMP_SUCCESS) return st;
+    return runtime_status(camp::rope_interleaved_launch(c.t, p.vec_bytes, p.group, c.a, p.grid,
+                                                        static_cast<cudaStream_t>(stream)));
+}
+
+CAMP_API camp_status_t camp_rope_interleaved(const void* x, const float* sin, const float* cos,
+                                             const int32_t* positions, void* y, int64_t tokens,
+                                             int64_t H, int64_t D, int64_t max_pos,
+                                             camp_dtype_t dtype, void* stream) {
+    return camp_rope_interleaved_with_plan(x, sin, cos, positions, y, tokens, H, D, max_pos,
+                                           dtype, nullptr, stream);
+}
+
+CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos, int64_t D,
+                                        double theta, void* stream) {
+    if (max_pos < 0 || D < 2 || D % 2 != 0 || !std::isfinite(theta) || !(theta > 0.0))
+        return CAMP_ERR_INVALID_ARG;
+    if (max_pos == 0) return CAMP_SUCCESS;
+    if (sin == nullptr || cos == nullptr || !aligned(sin, 4) || !aligned(cos, 4))
+        return CAMP_ERR_INVALID_ARG;
+    int64_t table_bytes = 0;
+    if (!mul_ok(max_pos, D / 2, 4, &table_bytes)) return CAMP_ERR_INVALID_ARG;
+    if (overlaps(sin, table_bytes, cos, table_bytes)) return CAMP_ERR_INVALID_ARG;
+    return runtime_status(camp::rope_tables_launch(sin, cos, max_pos, D, theta,
+                                                   static_cast<cudaStream_t>(stream)));
 }
 
 CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* cos, void* y,

@@ -122,6 +122,29 @@ cudaError_t rope_tiled_launch(DType t, int vec_bytes, int heads_per_thread, cons
 cudaError_t rope_flat_launch(DType t, int vec_bytes, int heads_per_thread, const RopeArgs& a,
                              int64_t grid, cudaStream_t s);
 
+// ------------------------------------------------------------------ interleaved RoPE
+// x [tokens, heads, dim], pairs (2i, 2i+1); table row positions[token] of [max_pos, dim/2].
+struct RopeInterleavedArgs {
+    const void* x;
+    const float* sin_t;
+    const float* cos_t;
+    const int32_t* positions;
+    void* y;
+    int64_t tokens;
+    int64_t heads;
+    int64_t dim;
+    int64_t max_pos;
+};
+
+// Tiled like rope_tiled: kRopeBlock threads, positions per CTA = 256 / (ceil(H/hpt) *
+// dim/elems); vec_bytes 16, 8 or 4 (bf16) / 16 or 8 (fp32): a vector holds whole pairs.
+bool rope_interleaved_compiled(DType t, int vec_bytes, int heads_per_thread);
+cudaError_t rope_interleaved_launch(DType t, int vec_bytes, int heads_per_thread,
+                                    const RopeInterleavedArgs& a, int64_t grid, cudaStream_t s);
+// sin/cos [max_pos, dim/2] with angle = p * theta^(-2i/dim), fp64, rounded once to fp32.
+cudaError_t rope_tables_launch(float* sin_t, float* cos_t, int64_t max_pos, int64_t dim,
+                               double theta, cudaStream_t s);
+
 // ------------------------------------------------------------------ KV RMSNorm + RoPE + cache
 // One warp per token of kv[tokens, dn + dr]: RMSNorm of the first dn elements into row
 // slots[t] of cache_n[num_slots, dn], rotate-half RoPE of the last dr into cache_r.

@@ -193,6 +193,42 @@ CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache(const void* kv, const void* ga
                                                   int64_t Dn, int64_t Dr, int64_t num_slots,
                                                   float eps, camp_dtype_t dtype, void* stream);
 
+/*
+ * Interleaved RoPE with per-token position ids, as in the xserv "phase 4" kernel
+ * (csrc/embedding/rope.cu): for each pair (x[2i], x[2i+1]) of every head of token t,
+ * at position p = positions[t], with c = cos[p, i] and sn = sin[p, i]:
+ *   y[2i]   = round(x[2i] * c - x[2i+1] * sn)
+ *   y[2i+1] = round(x[2i] * sn + x[2i+1] * c)
+ * (the same compensated fp32 products as camp_rope, one rounding).
+ *
+ *   x, y       [tokens, H, D]  storage type `dtype`; y == x (in place) is allowed.
+ *   sin, cos   [max_pos, D/2]  fp32 tables (camp_rope_tables makes them).
+ *   positions  [tokens] int32  device array; a position outside [0, max_pos) leaves the
+ *                              token's rows of y unwritten (nothing is read out of bounds).
+ *   D even, >= 2; tokens, H >= 0 (0 is a no-op).
+ *
+ * Pointers must be aligned to one pair (2 elements); CAMP_ERR_NOT_SUPPORTED if a token's
+ * heads need more than one CTA even at 8 heads per thread (H * D too large).
+ */
+CAMP_API camp_status_t camp_rope_interleaved(const void* x, const float* sin, const float* cos,
+                                             const int32_t* positions, void* y, int64_t tokens,
+                                             int64_t H, int64_t D, int64_t max_pos,
+                                             camp_dtype_t dtype, void* stream);
+
+/*
+ * RoPE tables on the device: sin[p, i] and cos[p, i] for p < max_pos, i < D/2, with
+ * angle = p * theta^(-2i/D) (the table of the xserv compute_rope_cache kernel; theta is
+ * 10000 in the original Llama and 500000 in Llama 3). Computed in fp64 with CUDA's
+ * double-precision pow and sincos, each value rounded once to fp32 (an fp32 angle is off
+ * by about 4e-3 rad at position 65536). The tables serve camp_rope, camp_rope_qk,
+ * camp_rope_interleaved and camp_kv_rmsnorm_rope_cache alike.
+ *
+ *   sin, cos  [max_pos, D/2] fp32 outputs (disjoint). max_pos >= 0 (0 is a no-op);
+ *   D even, >= 2; theta finite and > 0. Errors: CAMP_ERR_INVALID_ARG, CAMP_ERR_RUNTIME.
+ */
+CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos, int64_t D,
+                                        double theta, void* stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 CAMP_API const char* camp_status_string(camp_status_t status);
 
@@ -214,7 +250,8 @@ typedef enum {
     CAMP_KERNEL_ROPE_FLAT = 4,      /* any shape: one work item per (position, heads, vector) */
     CAMP_KERNEL_ROPE_SPLIT = 5,     /* camp_rope_qk only: Q and K as two separate launches */
     CAMP_KERNEL_RMSNORM_CLUSTER = 6, /* a cluster of CTAs per row, sums combined over DSMEM */
-    CAMP_KERNEL_KV_CACHE = 7        /* camp_kv_rmsnorm_rope_cache: one warp per token */
+    CAMP_KERNEL_KV_CACHE = 7,       /* camp_kv_rmsnorm_rope_cache: one warp per token */
+    CAMP_KERNEL_ROPE_INTERLEAVED = 8 /* camp_rope_interleaved: tiled like CAMP_KERNEL_ROPE */
 } camp_kernel_t;
 
 typedef struct {
@@ -296,6 +333,21 @@ CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_with_plan(
     const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
     void* cache_n, void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
     int64_t num_slots, float eps, camp_dtype_t dtype, const camp_plan_t* plan, void* stream);
+
+/* Like camp_rope_plan, for camp_rope_interleaved (vec_bytes; group = heads per thread). */
+CAMP_API camp_status_t camp_rope_interleaved_plan(const void* x, const float* sin,
+                                                  const float* cos, const int32_t* positions,
+                                                  const void* y, int64_t tokens, int64_t H,
+                                                  int64_t D, int64_t max_pos, camp_dtype_t dtype,
+                                                  camp_plan_t* plan);
+
+/* camp_rope_interleaved with an explicit plan (vec_bytes, group); NULL plan = the default. */
+CAMP_API camp_status_t camp_rope_interleaved_with_plan(const void* x, const float* sin,
+                                                       const float* cos,
+                                                       const int32_t* positions, void* y,
+                                                       int64_t tokens, int64_t H, int64_t D,
+                                                       int64_t max_pos, camp_dtype_t dtype,
+                                                       const camp_plan_t* plan, void* stream);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_kv_rmsnorm_rope_cache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                                  i64, i64, dbl, c_int]
     lib.oracle_kv_rmsnorm_rope_cache.restype = c_int
+    lib.oracle_rope_interleaved.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, c_int]
+    lib.oracle_rope_interleaved.restype = c_int
+    lib.oracle_rope_tables.argtypes = [vp, vp, i64, i64, dbl]
+    lib.oracle_rope_tables.restype = c_int
     lib.oracle_rope_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64]
     lib.oracle_rope_f64.restype = c_int
     lib.oracle_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, c_int]
@@ -196,6 +200,39 @@ def kv_rmsnorm_rope_cache(kv: np.ndarray, gamma: np.ndarray, sin_t: np.ndarray,
         _ptr(kv), _ptr(gamma), _ptr(sin_t), _ptr(cos_t), _ptr(slots), _ptr(cn), _ptr(cr),
         B, S, Dn, Dr, cn.shape[0], float(eps), code), "kv_rmsnorm_rope_cache")
     return cn, cr
+
+
+def rope_interleaved(x: np.ndarray, sin_t: np.ndarray, cos_t: np.ndarray,
+                     positions: np.ndarray, y0: np.ndarray, dtype: str,
+                     lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Interleaved RoPE of x [tokens, H, D] at table rows positions[t]; a copy of y0 with the
+    rows of every token that has a valid position overwritten."""
+    lib = lib or load()
+    code, npt = _storage(dtype)
+    x = np.ascontiguousarray(x)
+    tokens, H, D = x.shape
+    sin_t = np.ascontiguousarray(sin_t, dtype=np.float32)
+    cos_t = np.ascontiguousarray(cos_t, dtype=np.float32)
+    positions = np.ascontiguousarray(positions, dtype=np.int32)
+    y = np.array(y0, copy=True, order="C")
+    assert x.dtype == npt and y.dtype == npt and y.shape == x.shape
+    assert sin_t.shape == cos_t.shape and sin_t.shape[1] == D // 2
+    assert positions.shape == (tokens,)
+    _check(lib.oracle_rope_interleaved(_ptr(x), _ptr(sin_t), _ptr(cos_t), _ptr(positions),
+                                       _ptr(y), tokens, H, D, sin_t.shape[0], code),
+           "rope_interleaved")
+    return y
+
+
+def rope_tables(max_pos: int, D: int, theta: float, lib: ctypes.CDLL | None = None
+                ) -> tuple[np.ndarray, np.ndarray]:
+    """(sin, cos) fp32 [max_pos, D/2]: angle = p * theta^(-2i/D) in fp64, rounded once."""
+    lib = lib or load()
+    sin_t = np.empty((max_pos, D // 2), np.float32)
+    cos_t = np.empty((max_pos, D // 2), np.float32)
+    _check(lib.oracle_rope_tables(_ptr(sin_t), _ptr(cos_t), max_pos, D, float(theta)),
+           "rope_tables")
+    return sin_t, cos_t
 
 
 def rope_f64(x, sin_t, cos_t, lib: ctypes.CDLL | None = None) -> np.ndarray:

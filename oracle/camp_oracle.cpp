@@ -41,6 +41,13 @@
 // 1 sign, 8 exponent, 7 fraction bits). Decoding either to fp64 is exact. Encoding
 // rounds to nearest, ties to even (the pages are silent; this is the IEEE default).
 //
+//   Interleaved RoPE with position ids  (xserv "phase 4" rope kernel: pairs (x[2i], x[2i+1]),
+//            y0 = x0 cos - x1 sin, y1 = x0 sin + x1 cos, table row positions[token])
+//       tokens whose position is outside [0, max_pos) are left unwritten.
+//
+//   RoPE tables  (xserv compute_rope_cache: freq_i = theta^(-2i/D), angle = p * freq_i)
+//       sin[p, i] = round_fp32(sin(p * theta^(-2i/D))), cos likewise, all in fp64.
+//
 // Build flags matter: no -ffast-math, and -ffp-contract=off so that no multiply-add
 // is fused (results must be identical on x86-64 and aarch64).
 
@@ -288,6 +295,52 @@ int oracle_kv_rmsnorm_rope_cache(const void* kv, const void* gamma, const float*
             rope_head(xr.data(), sn.data(), c.data(), yr.data(), half);
             for (int64_t j = 0; j < Dn; ++j) store_elem(cache_n, slot * Dn + j, yn[j], dtype);
             for (int64_t j = 0; j < Dr; ++j) store_elem(cache_r, slot * Dr + j, yr[j], dtype);
+        }
+    }
+    return 0;
+}
+
+// Interleaved RoPE over storage-typed x [tokens, H, D], fp32 tables [max_pos, D/2] and int32
+// positions [tokens]; y (same layout) is updated only for tokens with a valid position.
+int oracle_rope_interleaved(const void* x, const float* sin_t, const float* cos_t,
+                            const int32_t* positions, void* y, int64_t tokens, int64_t H,
+                            int64_t D, int64_t max_pos, int dtype) {
+    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (tokens < 0 || H < 0 || D < 2 || D % 2 != 0 || max_pos < 0) return 1;
+    if (tokens * H == 0) return 0;
+    if (!x || !sin_t || !cos_t || !positions || !y) return 1;
+    const int64_t half = D / 2;
+    for (int64_t t = 0; t < tokens; ++t) {
+        const int64_t p = positions[t];
+        if (p < 0 || p >= max_pos) continue;
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t base = (t * H + h) * D;
+            for (int64_t i = 0; i < half; ++i) {
+                const double x0 = load_elem(x, base + 2 * i, dtype);
+                const double x1 = load_elem(x, base + 2 * i + 1, dtype);
+                const double c = static_cast<double>(cos_t[p * half + i]);
+                const double sn = static_cast<double>(sin_t[p * half + i]);
+                store_elem(y, base + 2 * i, x0 * c - x1 * sn, dtype);
+                store_elem(y, base + 2 * i + 1, x0 * sn + x1 * c, dtype);
+            }
+        }
+    }
+    return 0;
+}
+
+// RoPE tables [max_pos, D/2]: angle = p * theta^(-2i/D) in fp64, sin and cos rounded once.
+int oracle_rope_tables(float* sin_t, float* cos_t, int64_t max_pos, int64_t D, double theta) {
+    if (max_pos < 0 || D < 2 || D % 2 != 0 || !(theta > 0.0)) return 1;
+    if (max_pos == 0) return 0;
+    if (!sin_t || !cos_t) return 1;
+    const int64_t half = D / 2;
+    for (int64_t p = 0; p < max_pos; ++p) {
+        for (int64_t i = 0; i < half; ++i) {
+            const double freq = std::pow(theta, (-2.0 * static_cast<double>(i)) /
+                                                    static_cast<double>(D));
+            const double angle = static_cast<double>(p) * freq;
+            sin_t[p * half + i] = static_cast<float>(std::sin(angle));
+            cos_t[p * half + i] = static_cast<float>(std::cos(angle));
         }
     }
     return 0;

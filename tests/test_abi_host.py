@@ -406,3 +406,45 @@ def test_kv_cache_plans(lib):
     p = camp.camp_kv_rmsnorm_rope_cache_plan(*KVP, 2, 3, 33, 6, 8, "bf16")   # odd widths
     assert (p.vec_bytes, p.per_thread) == (2, 2)
     assert _kv(lib, B=0) == camp.SUCCESS
+
+
+# ------------------------------------------------------------------ interleaved RoPE, tables
+
+ILP = [0x7D0000000000 + i * 0x1000000000 for i in range(5)]   # x, sin, cos, positions, y
+
+
+@pytest.mark.parametrize("change,kw,status", [
+    ({}, {"dtype": 0}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({}, {"D": 7}, camp.ERR_INVALID_ARG),
+    ({}, {"mp": -1}, camp.ERR_INVALID_ARG),
+    ({3: None}, {}, camp.ERR_INVALID_ARG),
+    ({3: ILP[3] + 2}, {}, camp.ERR_INVALID_ARG),             # positions are int32
+    ({4: ILP[3]}, {}, camp.ERR_INVALID_ARG),                 # output over the positions
+    ({4: ILP[0] + 4}, {}, camp.ERR_INVALID_ARG),             # partial in-place overlap
+    ({0: ILP[0] + 2, 4: ILP[4] + 2}, {}, camp.ERR_NOT_SUPPORTED),   # not pair-aligned (bf16)
+    ({}, {"H": 128, "D": 256}, camp.ERR_NOT_SUPPORTED),      # a token needs more than one CTA
+])
+def test_rope_interleaved_argument_errors(lib, change, kw, status):
+    p = list(ILP)
+    for i, v in change.items():
+        p[i] = v
+    a = {"T": 16, "H": 4, "D": 64, "mp": 32, "dtype": camp.BF16}
+    a.update(kw)
+    assert lib.camp_rope_interleaved(*p, a["T"], a["H"], a["D"], a["mp"], a["dtype"], None) == status
+
+
+def test_rope_interleaved_plans(lib):
+    p = camp.camp_rope_interleaved_plan(*ILP, 65536, 32, 128, 131072, "bf16")
+    assert (p.kernel, p.vec_bytes, p.group, p.grid) == (camp.KERNEL_ROPE_INTERLEAVED, 16, 2, 65536)
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 5, 6, 16, "bf16")
+    assert (p.vec_bytes, p.group, p.grid) == (4, 1, 1)
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 64, 128, 16, "bf16")     # 2 heads: 512 threads
+    assert p.group == 4
+
+
+def test_rope_tables_argument_errors(lib):
+    S_, C_ = ILP[1], ILP[2]
+    for args in ((S_, C_, 16, 7, 1e4), (S_, C_, -1, 8, 1e4), (S_, C_, 16, 8, 0.0),
+                 (S_, C_, 16, 8, math.inf), (None, C_, 16, 8, 1e4), (S_, S_ + 8, 16, 8, 1e4)):
+        assert lib.camp_rope_tables(*args, None) == camp.ERR_INVALID_ARG
+    assert lib.camp_rope_tables(None, None, 0, 8, 1e4, None) == camp.SUCCESS

@@ -50,6 +50,15 @@ MUTANTS = {
     "cache rope part uses the batch's first table row":
         ("sn[i] = static_cast<double>(sin_t[s * half + i]);\n                c[i] = static_cast<double>(cos_t[s * half + i]);\n            }\n            rmsnorm_row",
          "sn[i] = static_cast<double>(sin_t[0 * s * half + i]);\n                c[i] = static_cast<double>(cos_t[0 * s * half + i]);\n            }\n            rmsnorm_row"),
+    "interleaved pair order swapped":
+        ("store_elem(y, base + 2 * i, x0 * c - x1 * sn, dtype);",
+         "store_elem(y, base + 2 * i, x1 * c - x0 * sn, dtype);"),
+    "interleaved table row from the token, not its position":
+        ("const double c = static_cast<double>(cos_t[p * half + i]);",
+         "const double c = static_cast<double>(cos_t[(t % max_pos) * half + i]);"),
+    "tables use theta^(-i/D)":
+        ("const double freq = std::pow(theta, (-2.0 * static_cast<double>(i)) /",
+         "const double freq = std::pow(theta, (-1.0 * static_cast<double>(i)) /"),
     "add path normalizes the unrounded sum":
         ("hr[j] = load_elem(h, i, dtype);",
          "hr[j] = load_elem(x, i, dtype) + load_elem(r, i, dtype);"),
@@ -77,6 +86,9 @@ def _battery(lib):
         ("rope single rounding", lambda: pins.test_rope_single_rounding_crafted_case(lib)),
         ("kv cache", lambda: [pins.test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, d)
                               for d in ("bf16", "f32")]),
+        ("rope interleaved", lambda: [pins.test_rope_interleaved_is_rotate_half_on_deinterleaved_input(lib, d)
+                                      for d in ("bf16", "f32")]),
+        ("rope tables", lambda: pins.test_rope_tables_match_numpy_and_closed_forms(lib)),
         ("add rmsnorm", lambda: [pins.test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, d)
                                  for d in ("bf16", "f32")]),
     ]

@@ -313,6 +313,58 @@ def test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, dtype):
         np.testing.assert_array_equal(cr[slot], cr0[slot])
 
 
+# ------------------------------------------------------------------------ interleaved RoPE, tables
+
+def _f32_ulps(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    ia = np.asarray(a, np.float32).view(np.int32).astype(np.int64)
+    ib = np.asarray(b, np.float32).view(np.int32).astype(np.int64)
+    ia = np.where(ia < 0, -(ia & 0x7FFFFFFF), ia)
+    ib = np.where(ib < 0, -(ib & 0x7FFFFFFF), ib)
+    return np.abs(ia - ib)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_rope_interleaved_is_rotate_half_on_deinterleaved_input(lib, dtype):
+    # Interleaved RoPE at positions p_t equals the (separately pinned) rotate-half RoPE of the
+    # de-interleaved heads with the table rows p_t, re-interleaved; tokens with a position
+    # outside the table are left as they were.
+    rng = np.random.default_rng(51)
+    T, H, D, P = 9, 3, 12, 20
+    xt, xs = _storage_pair(rng, (T, H, D), dtype)
+    _, y0 = _storage_pair(rng, (T, H, D), dtype)
+    sin_t = rng.uniform(-1, 1, (P, D // 2)).astype(np.float32)
+    cos_t = rng.uniform(-1, 1, (P, D // 2)).astype(np.float32)
+    pos = rng.integers(0, P, T).astype(np.int32)
+    pos[2] = -3
+    pos[5] = P
+    y = oracle.rope_interleaved(xs, sin_t, cos_t, pos, y0, dtype, lib=lib)
+    for t in range(T):
+        if not 0 <= pos[t] < P:
+            np.testing.assert_array_equal(y[t], y0[t])
+            continue
+        half = np.concatenate([xs[t][:, 0::2], xs[t][:, 1::2]], axis=-1)     # [H, D]
+        r = oracle.rope(half[None, None], sin_t[pos[t]:pos[t] + 1], cos_t[pos[t]:pos[t] + 1],
+                        dtype, lib=lib)[0, 0]
+        np.testing.assert_array_equal(y[t][:, 0::2], r[:, :D // 2])
+        np.testing.assert_array_equal(y[t][:, 1::2], r[:, D // 2:])
+
+
+def test_rope_tables_match_numpy_and_closed_forms(lib):
+    P, D, theta = 4097, 128, 500000.0
+    s, c = oracle.rope_tables(P, D, theta, lib=lib)
+    np.testing.assert_array_equal(s[0], 0.0)                 # position 0: angle 0
+    np.testing.assert_array_equal(c[0], 1.0)
+    # column 0: theta^0 = 1, angle = p exactly
+    p = np.arange(P, dtype=np.float64)
+    assert _f32_ulps(s[:, 0], np.sin(p).astype(np.float32)).max() <= 1
+    # everything: numpy's own fp64 pow / sin / cos (the benchmark's host recipe)
+    from block_memory_bound_gb300 import inputs
+    ns, nc = inputs.rope_tables(P, D, theta)
+    assert _f32_ulps(s, ns).max() <= 1 and _f32_ulps(c, nc).max() <= 1
+    # the two columns are a rotation: sin^2 + cos^2 = 1 up to fp32 rounding
+    assert np.abs(s.astype(np.float64) ** 2 + c.astype(np.float64) ** 2 - 1).max() < 2e-7
+
+
 # ------------------------------------------------------------------------ RoPE
 
 def _tables(S, half, angle_fn, dtype=np.float64):
