@@ -113,6 +113,8 @@ def recorded_traffic(kernel_name: str):
 
 
 def plan_name(kind: str, p: camp.Plan) -> str:
+    if kind == "layernorm":
+        return f"layernorm_rows<bf16,vec{p.vec_bytes},group{p.group},nv{p.per_thread}>"
     if kind == "rmsnorm":
         k = {camp.KERNEL_RMSNORM_ROWS: "rmsnorm_rows", camp.KERNEL_RMSNORM_CLUSTER: "rmsnorm_cluster",
              camp.KERNEL_RMSNORM_WIDE: "rmsnorm_wide"}.get(p.kernel, "rmsnorm")
@@ -329,6 +331,9 @@ def large_configs(peak: float, reps: int) -> list[dict]:
         ("add_rmsnorm bf16 [16384,8192]", "add", (16384, 8192)),
         ("add_rmsnorm bf16 [65536,2048]", "add", (65536, 2048)),
         ("rmsnorm bf16 [256,131072] (cluster per row)", "rms", (256, 131072, False, 1e-5)),
+        ("layernorm bf16 [8192,4096]", "ln", (8192, 4096)),
+        ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),
+        ("layernorm bf16 [16384,8192]", "ln", (16384, 8192)),
         ("rope bf16 [1,65536,32,128]", "rope", (65536, 32, 128)),
         ("rope bf16 [1,65536,32,64]", "rope", (65536, 32, 64)),
         ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),
@@ -358,6 +363,15 @@ def large_configs(peak: float, reps: int) -> list[dict]:
             fn = lambda: camp.camp_add_rmsnorm(x.data_ptr(), r.data_ptr(), w.data_ptr(),
                                                h.data_ptr(), y.data_ptr(), rows, cols, 1e-5,
                                                camp.BF16, stream)
+        elif kind == "ln":
+            rows, cols = shp
+            x, w, bt = inputs.layernorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
+            y = torch.empty_like(x)
+            nbytes = ledger.layernorm_bytes(rows, cols)
+            plan = camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16")
+            pname = plan_name("layernorm", plan)
+            fn = lambda: camp.camp_layernorm(x.data_ptr(), w.data_ptr(), bt.data_ptr(),
+                                             y.data_ptr(), rows, cols, 1e-5, camp.BF16, stream)
         elif kind == "ril":
             T, H, D = shp
             mp = 2 * T
@@ -447,6 +461,13 @@ def run_case(case: str, launches: int) -> None:
         plan = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, "bf16"))
         for _ in range(launches):
             camp.camp_rmsnorm(x, w, y, rows, cols, EPS, camp.BF16, stream)
+    elif kind == "layernorm":
+        rows, cols = dims
+        x, w, bt = inputs.layernorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
+        y = torch.empty_like(x)
+        plan = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16"))
+        for _ in range(launches):
+            camp.camp_layernorm(x, w, bt, y, rows, cols, EPS, camp.BF16, stream)
     elif kind == "rope_qk":
         B, S, Hq, Hk, D = dims
         q, sn, cs = inputs.rope_inputs(B, S, Hq, D, "bf16", seed=0, device="cuda")

@@ -38,6 +38,7 @@ KERNEL_ROPE_SPLIT = 5
 KERNEL_RMSNORM_CLUSTER = 6
 KERNEL_KV_CACHE = 7
 KERNEL_ROPE_INTERLEAVED = 8
+KERNEL_LAYERNORM_ROWS = 9
 
 # Every symbol include/camp.h declares.
 EXPORTS = (
@@ -49,6 +50,7 @@ EXPORTS = (
     "camp_kv_rmsnorm_rope_cache_with_plan",
     "camp_rope_interleaved", "camp_rope_interleaved_plan", "camp_rope_interleaved_with_plan",
     "camp_rope_tables",
+    "camp_layernorm", "camp_layernorm_plan", "camp_layernorm_with_plan",
 )
 
 
@@ -122,6 +124,12 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_add_rmsnorm_with_plan.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, c_int,
                                                    pplan, vp]
         lib.camp_add_rmsnorm_with_plan.restype = c_int
+        lib.camp_layernorm.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int, vp]
+        lib.camp_layernorm.restype = c_int
+        lib.camp_layernorm_plan.argtypes = [vp, vp, vp, vp, i64, i64, c_int, pplan]
+        lib.camp_layernorm_plan.restype = c_int
+        lib.camp_layernorm_with_plan.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int, pplan, vp]
+        lib.camp_layernorm_with_plan.restype = c_int
         ilsig = [vp, vp, vp, vp, vp, i64, i64, i64, i64, c_int]
         lib.camp_rope_interleaved.argtypes = ilsig + [vp]
         lib.camp_rope_interleaved.restype = c_int
@@ -295,6 +303,27 @@ def camp_kv_rmsnorm_rope_cache_with_plan(kv, gamma, sin, cos, slots, cache_n, ca
         ctypes.byref(plan), _stream(stream)))
 
 
+def camp_layernorm(x, gamma, beta, y, rows: int, cols: int, eps: float, dtype, stream=None) -> None:
+    _check("camp_layernorm", load().camp_layernorm(
+        _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), int(rows), int(cols), float(eps),
+        _dtype(dtype), _stream(stream)))
+
+
+def camp_layernorm_plan(x, gamma, beta, y, rows: int, cols: int, dtype) -> Plan:
+    p = Plan()
+    _check("camp_layernorm_plan", load().camp_layernorm_plan(
+        _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), int(rows), int(cols), _dtype(dtype),
+        ctypes.byref(p)))
+    return p
+
+
+def camp_layernorm_with_plan(x, gamma, beta, y, rows: int, cols: int, eps: float, dtype,
+                             plan: Plan, stream=None) -> None:
+    _check("camp_layernorm_with_plan", load().camp_layernorm_with_plan(
+        _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), int(rows), int(cols), float(eps),
+        _dtype(dtype), ctypes.byref(plan), _stream(stream)))
+
+
 def camp_rope_interleaved(x, sin, cos, positions, y, tokens: int, H: int, D: int, max_pos: int,
                           dtype, stream=None) -> None:
     _check("camp_rope_interleaved", load().camp_rope_interleaved(
@@ -416,3 +445,20 @@ def add_rmsnorm(x, r, w, eps: float = 1e-5, out_h=None, out_y=None, stream=None)
     rows = x.numel() // cols
     camp_add_rmsnorm(x, r, w, out_h, out_y, rows, cols, eps, x.dtype, stream)
     return out_h, out_y
+
+
+def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
+    """LayerNorm over the last dimension of a contiguous CUDA tensor (bf16 or fp32)."""
+    import torch
+    _require(x.is_cuda and x.is_contiguous(), "x must be a contiguous CUDA tensor")
+    for t, name in ((gamma, "gamma"), (beta, "beta")):
+        _require(t.dtype == x.dtype and t.is_contiguous() and t.numel() == x.shape[-1],
+                 f"{name} must be a contiguous [cols] tensor of x's dtype")
+    if out is None:
+        out = torch.empty_like(x)
+    _require(out.shape == x.shape and out.dtype == x.dtype and out.is_contiguous(),
+             "out must match x")
+    cols = x.shape[-1] if x.dim() > 0 else 1
+    rows = x.numel() // cols if cols else 0
+    camp_layernorm(x, gamma, beta, out, rows, cols, eps, x.dtype, stream)
+    return out

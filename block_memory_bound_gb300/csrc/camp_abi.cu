@@ -583,6 +583,7 @@ int kv_nvn(const KvCall& c, int vb) {
 }
 
 camp_status_t kv_plan(const KvCall& c, const camp_plan_t* forced, camp_plan_t* p) {
+    if (forced && forced->kernel != CAMP_KERNEL_KV_CACHE) return CAMP_ERR_NOT_SUPPORTED;
     *p = camp_plan_t{};
     p->kernel = CAMP_KERNEL_KV_CACHE;
     p->vec_bytes = forced ? forced->vec_bytes : kv_vec_bytes(c);
@@ -658,6 +659,7 @@ int64_t rope_il_tpc(const RopeIlCall& c, int vb, int hpt) {
 // Widest legal vector; 2 heads per thread (1 for odd head counts), more when a token's
 // heads would not fit one CTA; CAMP_ERR_NOT_SUPPORTED when even 8 do not.
 camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_plan_t* p) {
+    if (forced && forced->kernel != CAMP_KERNEL_ROPE_INTERLEAVED) return CAMP_ERR_NOT_SUPPORTED;
     *p = camp_plan_t{};
     p->kernel = CAMP_KERNEL_ROPE_INTERLEAVED;
     p->cluster = 1;
@@ -678,6 +680,56 @@ camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_
     const int64_t tpc = rope_il_tpc(c, p->vec_bytes, p->group);
     if (tpc == 0 || c.a.tokens > 0xFFFFFFFFll) return CAMP_ERR_NOT_SUPPORTED;
     p->grid = ceil_div(c.a.tokens, tpc);
+    return CAMP_SUCCESS;
+}
+
+// ------------------------------------------------------------------ LayerNorm
+
+struct LnCall {
+    RmsCall rc;          // x, w = gamma, y, sizes: planned like the RMSNorm rows kernel
+    const void* beta;
+};
+
+camp_status_t ln_validate(const void* x, const void* gamma, const void* beta, const void* y,
+                          int64_t rows, int64_t cols, camp_dtype_t dtype, LnCall* c,
+                          bool* empty) {
+    camp_status_t st = rms_validate(x, gamma, y, rows, cols, dtype, &c->rc, empty);
+    if (st != CAMP_SUCCESS || *empty) return st;
+    if (beta == nullptr) return CAMP_ERR_INVALID_ARG;
+    const int64_t es = camp::elem_bytes(c->rc.t);
+    if (!aligned(beta, es)) return CAMP_ERR_INVALID_ARG;
+    if (overlaps(y, c->rc.bytes, beta, cols * es)) return CAMP_ERR_INVALID_ARG;
+    c->beta = beta;
+    return CAMP_SUCCESS;
+}
+
+camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p) {
+    if (forced && forced->kernel != CAMP_KERNEL_LAYERNORM_ROWS) return CAMP_ERR_NOT_SUPPORTED;
+    const RmsCall& rc = c.rc;
+    const int es = camp::elem_bytes(rc.t);
+    const int widest = (rms_vec_bytes(rc) == 16 && aligned(c.beta, 16)) ? 16 : es;
+    *p = camp_plan_t{};
+    p->kernel = CAMP_KERNEL_LAYERNORM_ROWS;
+    p->cluster = 1;
+    if (forced) {
+        p->vec_bytes = forced->vec_bytes;
+        p->group = forced->group;
+        p->per_thread = forced->per_thread;
+        if (p->vec_bytes != 16 && p->vec_bytes != es) return CAMP_ERR_NOT_SUPPORTED;
+        if (p->vec_bytes > widest) return CAMP_ERR_NOT_SUPPORTED;
+        if (!camp::rmsnorm_rows_compiled(false, rc.t, p->vec_bytes, p->group, p->per_thread))
+            return CAMP_ERR_NOT_SUPPORTED;   // the same variant set
+        const int64_t nvec = rc.a.cols * es / p->vec_bytes;
+        if (static_cast<int64_t>(p->group) * p->per_thread < nvec) return CAMP_ERR_NOT_SUPPORTED;
+    } else {
+        p->vec_bytes = widest;
+        int g = 0, nv = 0;
+        if (!rms_choose_rows(rc, widest, &g, &nv)) return CAMP_ERR_NOT_SUPPORTED;
+        p->group = g;
+        p->per_thread = nv;
+    }
+    p->block = camp::rows_block(p->group);
+    p->grid = ceil_div(rc.a.rows, p->block / p->group);
     return CAMP_SUCCESS;
 }
 
@@ -886,6 +938,43 @@ CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos,
     if (overlaps(sin, table_bytes, cos, table_bytes)) return CAMP_ERR_INVALID_ARG;
     return runtime_status(camp::rope_tables_launch(sin, cos, max_pos, D, theta,
                                                    static_cast<cudaStream_t>(stream)));
+}
+
+CAMP_API camp_status_t camp_layernorm_plan(const void* x, const void* gamma, const void* beta,
+                                           const void* y, int64_t rows, int64_t cols,
+                                           camp_dtype_t dtype, camp_plan_t* plan) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    LnCall c;
+    bool empty = false;
+    camp_status_t st = ln_validate(x, gamma, beta, y, rows, cols, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (empty) { *plan = camp_plan_t{}; return CAMP_SUCCESS; }
+    return ln_plan(c, nullptr, plan);
+}
+
+CAMP_API camp_status_t camp_layernorm_with_plan(const void* x, const void* gamma,
+                                                const void* beta, void* y, int64_t rows,
+                                                int64_t cols, float eps, camp_dtype_t dtype,
+                                                const camp_plan_t* plan, void* stream) {
+    LnCall c;
+    bool empty = false;
+    camp_status_t st = ln_validate(x, gamma, beta, y, rows, cols, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (!eps_ok(eps)) return CAMP_ERR_INVALID_ARG;
+    if (empty) return CAMP_SUCCESS;
+    camp_plan_t p;
+    st = ln_plan(c, plan, &p);
+    if (st != CAMP_SUCCESS) return st;
+    const camp::LayernormArgs a{x, gamma, c.beta, y, rows, cols, eps};
+    return runtime_status(camp::layernorm_rows_launch(c.rc.t, p.vec_bytes, p.group,
+                                                      p.per_thread, a, p.grid,
+                                                      static_cast<cudaStream_t>(stream)));
+}
+
+CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const void* beta,
+                                      void* y, int64_t rows, int64_t cols, float eps,
+                                      camp_dtype_t dtype, void* stream) {
+    return camp_layernorm_with_plan(x, gamma, beta, y, rows, cols, eps, dtype, nullptr, stream);
 }
 
 CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* cos, void* y,

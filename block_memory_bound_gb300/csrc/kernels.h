@@ -122,6 +122,22 @@ cudaError_t rope_tiled_launch(DType t, int vec_bytes, int heads_per_thread, cons
 cudaError_t rope_flat_launch(DType t, int vec_bytes, int heads_per_thread, const RopeArgs& a,
                              int64_t grid, cudaStream_t s);
 
+// ------------------------------------------------------------------ LayerNorm
+// Register-resident rows kernel, the same (vec_bytes, group, per_thread) variants as the
+// RMSNorm rows kernel; no cluster or two-sweep path.
+struct LayernormArgs {
+    const void* x;
+    const void* gamma;
+    const void* beta;
+    void* y;
+    int64_t rows;
+    int64_t cols;
+    float eps;
+};
+
+cudaError_t layernorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
+                                  const LayernormArgs& a, int64_t grid, cudaStream_t s);
+
 // ------------------------------------------------------------------ interleaved RoPE
 // x [tokens, heads, dim], pairs (2i, 2i+1); table row positions[token] of [max_pos, dim/2].
 struct RopeInterleavedArgs {

@@ -1,0 +1,181 @@
+// LayerNorm forward for sm_103a.
+//
+// Definition (xserv "phase 4", csrc/normalization/layernorm.cu and the design notes'
+// LayerNorm section): y = gamma * (x - mean) / sqrt(var + eps) + beta per row, with the
+// population variance (divisor: the row length). The TileLang tutorial (ch. 02, example 2)
+// counts it as one read of x and one write of y when fused.
+//
+// The row is held in registers, as in the RMSNorm rows kernel (one sweep of 16-byte
+// loads, a group of G threads per row), so the statistics cost no extra memory traffic
+// and are taken in two passes over the registers instead of xserv's single pass
+// var = E[x^2] - mean^2, which cancels catastrophically when |mean| >> sigma:
+//   1. shift K = x[row, 0] and mu = sum(x - K) / n, so mean = K + mu is kept as the pair
+//      (K, mu) and never rounded to one fp32 number: every deviation is formed as
+//      d = (x - K) - mu, whose rounding errors are relative to the spread of the row, not
+//      to |mean| (an fp32 mean alone is off by up to ulp(mean) / 2);
+//   2. var = sum(d^2) / n from the registers;
+//   3. y = fma(d * rsqrt(var + eps), gamma, beta), rounded once.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace camp {
+namespace {
+
+template <int G>
+struct LnShape {
+    static constexpr int kBlock = rows_block(G);
+    static constexpr int kRowsPerCta = kBlock / G;
+    static constexpr int kWarpsPerRow = G / 32;
+};
+
+// Sum over the row group; for G > 32 through `scratch` (one slot per warp of the group).
+// The caller separates two uses of one scratch array with a barrier or uses two arrays.
+template <int G>
+__device__ __forceinline__ float group_sum(float v, float (&scratch)[LnShape<G>::kRowsPerCta]
+                                                             [LnShape<G>::kWarpsPerRow],
+                                           int g, int t) {
+    v = warp_sum(v);
+    if constexpr (LnShape<G>::kWarpsPerRow > 1) {
+        if ((threadIdx.x & 31) == 0) scratch[g][t / 32] = v;
+        __syncthreads();
+        v = 0.0f;
+#pragma unroll
+        for (int i = 0; i < LnShape<G>::kWarpsPerRow; ++i) v += scratch[g][i];
+    }
+    return v;
+}
+
+// Occupancy budget: for fp32 the deviations x - mean of the variance pass stay live into
+// the output pass (the raw words are the values themselves), so budget twice the data.
+template <typename S, int NV>
+constexpr int ln_live_loads() { return Storage<S>::kBytes == 4 ? 2 * NV : NV; }
+
+template <typename S, int VB, int G, int NV>
+__global__ void __launch_bounds__(LnShape<G>::kBlock, rows_min_blocks(VB, G, ln_live_loads<S, NV>()))
+layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
+                      const void* __restrict__ beta, void* y, int64_t rows, int64_t cols,
+                      float eps) {
+    using Sh = LnShape<G>;
+    using C = Codec<S, VB>;
+    constexpr int E = C::kElems;
+    constexpr int ES = Storage<S>::kBytes;
+
+    __shared__ float part_mean[Sh::kRowsPerCta][Sh::kWarpsPerRow];
+    __shared__ float part_var[Sh::kRowsPerCta][Sh::kWarpsPerRow];
+
+    griddep_wait();
+    griddep_launch_dependents();
+
+    const int g = threadIdx.x / G;
+    const int t = threadIdx.x % G;
+    const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+    const int64_t row = block * Sh::kRowsPerCta + g;
+    const bool active = row < rows;
+    const int live = static_cast<int>(cols / E) - t;
+    const int64_t row_off = row * cols * ES;
+    const int64_t off = row_off + static_cast<int64_t>(t) * VB;
+
+    Raw<VB> v[NV];
+    const char* xr = static_cast<const char*>(x) + off;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        v[k] = (active && k * G < live) ? ld_stream<VB>(xr + k * G * VB) : raw_zero<VB>();
+    // The shift: the row's first element (read before any of this row's outputs is written:
+    // every store below follows a group reduction that every thread of the group reaches).
+    float shift = 0.0f;
+    if (active) {
+        const Raw<ES> k0 = ld_stream<ES>(static_cast<const char*>(x) + row_off);
+        Codec<S, ES>::each(k0, [&](int, float f) { shift = f; });
+    }
+
+    const float n = static_cast<float>(cols);
+    float s1 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        C::each(v[k], [&](int, float f) {
+            if (k * G < live) s1 += f - shift;
+        });
+    }
+    const float mu = group_sum<G>(s1, part_mean, g, t) / n;   // mean - shift
+
+    float s2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        C::each(v[k], [&](int, float f) {
+            const float d = (f - shift) - mu;
+            if (k * G < live) s2 = fmaf(d, d, s2);
+        });
+    }
+    const float var = group_sum<G>(s2, part_var, g, t) / n;
+    const float rstd = rsqrtf(var + eps);
+
+    if (!active) return;
+    const char* gt = static_cast<const char*>(gamma) + static_cast<int64_t>(t) * VB;
+    const char* bt = static_cast<const char*>(beta) + static_cast<int64_t>(t) * VB;
+    char* yr = static_cast<char*>(y) + off;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        if (k * G < live) {
+            float gf[E], bf[E];
+            C::each(ld_shared_ro<VB>(gt + k * G * VB), [&](int e, float f) { gf[e] = f; });
+            C::each(ld_shared_ro<VB>(bt + k * G * VB), [&](int e, float f) { bf[e] = f; });
+            st_out<VB>(yr + k * G * VB, C::map(v[k], [&](int e, float xf) {
+                return fmaf(((xf - shift) - mu) * rstd, gf[e], bf[e]);
+            }));
+        }
+    }
+}
+
+template <typename S, int VB, int G, int NV>
+cudaError_t launch_ln(const LayernormArgs& a, int64_t grid, cudaStream_t s) {
+    return launch_pdl(layernorm_rows_kernel<S, VB, G, NV>, grid_2d(grid), dim3(LnShape<G>::kBlock),
+                      s, a.x, a.gamma, a.beta, a.y, a.rows, a.cols, a.eps);
+}
+
+using LnFn = cudaError_t (*)(const LayernormArgs&, int64_t, cudaStream_t);
+
+struct LnEntry {
+    DType t;
+    int vec_bytes, group, per_thread;
+    LnFn fn;
+};
+
+#define CAMP_LN(S, DT, VB, G, NV) {DType::DT, VB, G, NV, &launch_ln<S, VB, G, NV>}
+#define CAMP_LN_NV16(S, DT, G)                                                              \
+    CAMP_LN(S, DT, 16, G, 1), CAMP_LN(S, DT, 16, G, 2), CAMP_LN(S, DT, 16, G, 3),           \
+    CAMP_LN(S, DT, 16, G, 4), CAMP_LN(S, DT, 16, G, 6), CAMP_LN(S, DT, 16, G, 8)
+#define CAMP_LN_FAST(S, DT)                                                                 \
+    CAMP_LN_NV16(S, DT, 32), CAMP_LN_NV16(S, DT, 64), CAMP_LN_NV16(S, DT, 128),             \
+    CAMP_LN_NV16(S, DT, 256), CAMP_LN_NV16(S, DT, 512), CAMP_LN_NV16(S, DT, 1024)
+#define CAMP_LN_ELEM_G(S, DT, VB, G)                                                        \
+    CAMP_LN(S, DT, VB, G, 1), CAMP_LN(S, DT, VB, G, 2), CAMP_LN(S, DT, VB, G, 4),           \
+    CAMP_LN(S, DT, VB, G, 8), CAMP_LN(S, DT, VB, G, 16)
+#define CAMP_LN_ELEM(S, DT, VB)                                                             \
+    CAMP_LN_ELEM_G(S, DT, VB, 32), CAMP_LN_ELEM_G(S, DT, VB, 256), CAMP_LN_ELEM_G(S, DT, VB, 1024)
+
+const LnEntry kLn[] = {
+    CAMP_LN_FAST(bf16_t, BF16),
+    CAMP_LN_FAST(f32_t, F32),
+    CAMP_LN_ELEM(bf16_t, BF16, 2),
+    CAMP_LN_ELEM(f32_t, F32, 4),
+};
+
+#undef CAMP_LN_ELEM
+#undef CAMP_LN_ELEM_G
+#undef CAMP_LN_FAST
+#undef CAMP_LN_NV16
+#undef CAMP_LN
+
+}  // namespace
+
+cudaError_t layernorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
+                                  const LayernormArgs& a, int64_t grid, cudaStream_t s) {
+    for (const LnEntry& e : kLn) {
+        if (e.t == t && e.vec_bytes == vec_bytes && e.group == group &&
+            e.per_thread == per_thread)
+            return e.fn(a, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace camp

@@ -11,8 +11,14 @@ path and the CPU oracle both consume, so that the two are compared on identical 
   ``sin, cos [S, D/2]`` at ``angle = s * theta^(-2i/D)``, ``i = 0 .. D/2-1``, computed in
   fp64 and rounded once to fp32 (Llama-3.2-1B uses theta = 500000).
 
+* LayerNorm: ``x[r, :] = o_r + s_r * N(0, 1)`` with a per-row scale ``s_r`` drawn from
+  {1e-2, 1, 10} and an offset ratio ``o_r / s_r`` from {0, +-3, +-100} (bf16) or
+  {0, +-3, +-1e3} (fp32), so some rows have |mean| >> spread; ``gamma ~ N(1, 0.1)``,
+  ``beta ~ N(0, 1)`` (beta and gamma * xhat then cancel somewhere in every long row).
+
 Sub-seeds: x uses ``seed*16 + 0``, w ``seed*16 + 1``, the stress-row permutation
-``seed*16 + 2`` and the RoPE input ``seed*16 + 3``. ``device`` selects where the numbers
+``seed*16 + 2``, the RoPE input ``seed*16 + 3``, and the LayerNorm beta ``seed*16 + 4``
+and row scales and offsets ``seed*16 + 5``. ``device`` selects where the numbers
 are drawn (torch's CPU and CUDA generators give different streams for one seed; the
 recipe is the distribution, and every comparison uses one draw for both sides).
 """
@@ -47,6 +53,25 @@ def rmsnorm_inputs(rows: int, cols: int, dtype: str = "bf16", seed: int = 0,
             x[perm[:n1]] *= 1e3
             x[perm[n1:2 * n1]] *= 1e-4
     return x.to(st), w.to(st)
+
+
+def layernorm_inputs(rows: int, cols: int, dtype: str = "bf16", seed: int = 0,
+                     device="cpu") -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Return ``(x[rows, cols], gamma[cols], beta[cols])`` of storage type ``dtype``."""
+    st = STORAGE[dtype]
+    x = torch.randn(rows, cols, generator=_gen(seed, 0, device), dtype=torch.float32,
+                    device=device)
+    g = torch.randn(cols, generator=_gen(seed, 1, device), dtype=torch.float32, device=device)
+    g = g.mul_(0.1).add_(1.0)
+    b = torch.randn(cols, generator=_gen(seed, 4, device), dtype=torch.float32, device=device)
+    pick = torch.randint(0, 1 << 30, (rows, 2), generator=_gen(seed, 5, "cpu"))
+    scales = torch.tensor([1e-2, 1.0, 10.0])
+    ratios = torch.tensor([0.0, 3.0, -3.0, 100.0, -100.0] if dtype == "bf16"
+                          else [0.0, 3.0, -3.0, 1e3, -1e3])
+    s_r = scales[pick[:, 0] % len(scales)]
+    o_r = ratios[pick[:, 1] % len(ratios)] * s_r
+    x = x * s_r.to(device)[:, None] + o_r.to(device)[:, None]
+    return x.to(st), g.to(st), b.to(st)
 
 
 def rope_tables(S: int, D: int, theta: float = 500000.0) -> tuple[np.ndarray, np.ndarray]:

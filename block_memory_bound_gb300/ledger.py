@@ -27,6 +27,20 @@ def add_rmsnorm_bytes(rows: int, cols: int, dtype: str = "bf16") -> int:
     return 4 * rows * cols * es + cols * es
 
 
+def layernorm_bytes(rows: int, cols: int, dtype: str = "bf16", affine: bool = True,
+                    passes: int = 1) -> int:
+    """LayerNorm: x read ``passes`` times (1 when fused; the three-pass split of mean,
+    variance and normalize + affine reads it 3 times), y written once, gamma and beta read
+    once (``affine=True``; the tutorial's example 2 leaves them out)."""
+    es = ELEM_BYTES[dtype]
+    return (passes + 1) * rows * cols * es + (2 * cols * es if affine else 0)
+
+
+def layernorm_flops(rows: int, cols: int) -> int:
+    # the tutorial's convention for example 2: about 8 FLOP per element
+    return 8 * rows * cols
+
+
 def rmsnorm_flops(rows: int, cols: int) -> int:
     # per element: square-accumulate (2) + two multiplies (2); per row: divide, add, rsqrt
     return 4 * rows * cols + 3 * rows

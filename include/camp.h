@@ -229,6 +229,24 @@ CAMP_API camp_status_t camp_rope_interleaved(const void* x, const float* sin, co
 CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos, int64_t D,
                                         double theta, void* stream);
 
+/*
+ * LayerNorm forward: y = gamma * (x - mean) / sqrt(var + eps) + beta per row, with the
+ * population variance (xserv "phase 4", csrc/normalization/layernorm.cu).
+ *
+ *   x, y   [rows, cols]  storage type `dtype`; y == x (in place) is allowed.
+ *   gamma, beta [cols]   storage type `dtype`; y must not overlap them.
+ *
+ * The row is held in registers (camp_rmsnorm's rows kernel layout: x read once, y written
+ * once) and the statistics are taken in two passes over the registers, in fp32: with
+ * K = x[row, 0], mu = sum(x - K) / n and d = (x - K) - mu, var = sum(d^2) / n and
+ * y = fma(d * rsqrt(var + eps), gamma, beta), rounded once to the storage type. Rows up to 1024 threads x 8 16-byte accesses (65536
+ * bf16 / 32768 fp32 columns; 16384 columns on the element path); wider rows return
+ * CAMP_ERR_NOT_SUPPORTED. Errors otherwise as for camp_rmsnorm.
+ */
+CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const void* beta,
+                                      void* y, int64_t rows, int64_t cols, float eps,
+                                      camp_dtype_t dtype, void* stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 CAMP_API const char* camp_status_string(camp_status_t status);
 
@@ -241,7 +259,9 @@ CAMP_API int camp_last_cuda_error(void);
 /* ------------------------------------------------------------------ kernel plans
  * A plan names the kernel variant that a call with the given shapes and pointers runs.
  * Planning is host-only arithmetic (no CUDA call), so it works without a GPU; the
- * benchmark and the tests use it to label and to enumerate kernel variants.
+ * benchmark and the tests use it to label and to enumerate kernel variants. A *_with_plan
+ * call given a plan whose kernel the operation does not have, or a variant that is not
+ * built or does not cover the row, returns CAMP_ERR_NOT_SUPPORTED without launching.
  */
 typedef enum {
     CAMP_KERNEL_RMSNORM_ROWS = 1,   /* a group of threads per row, row held in registers */
@@ -251,7 +271,8 @@ typedef enum {
     CAMP_KERNEL_ROPE_SPLIT = 5,     /* camp_rope_qk only: Q and K as two separate launches */
     CAMP_KERNEL_RMSNORM_CLUSTER = 6, /* a cluster of CTAs per row, sums combined over DSMEM */
     CAMP_KERNEL_KV_CACHE = 7,       /* camp_kv_rmsnorm_rope_cache: one warp per token */
-    CAMP_KERNEL_ROPE_INTERLEAVED = 8 /* camp_rope_interleaved: tiled like CAMP_KERNEL_ROPE */
+    CAMP_KERNEL_ROPE_INTERLEAVED = 8, /* camp_rope_interleaved: tiled like CAMP_KERNEL_ROPE */
+    CAMP_KERNEL_LAYERNORM_ROWS = 9  /* camp_layernorm: a group of threads per row, registers */
 } camp_kernel_t;
 
 typedef struct {
@@ -348,6 +369,17 @@ CAMP_API camp_status_t camp_rope_interleaved_with_plan(const void* x, const floa
                                                        int64_t tokens, int64_t H, int64_t D,
                                                        int64_t max_pos, camp_dtype_t dtype,
                                                        const camp_plan_t* plan, void* stream);
+
+/* Like camp_rmsnorm_plan, for camp_layernorm (kernel CAMP_KERNEL_LAYERNORM_ROWS). */
+CAMP_API camp_status_t camp_layernorm_plan(const void* x, const void* gamma, const void* beta,
+                                           const void* y, int64_t rows, int64_t cols,
+                                           camp_dtype_t dtype, camp_plan_t* plan);
+
+/* camp_layernorm with an explicit plan (vec_bytes, group, per_thread); NULL = default. */
+CAMP_API camp_status_t camp_layernorm_with_plan(const void* x, const void* gamma,
+                                                const void* beta, void* y, int64_t rows,
+                                                int64_t cols, float eps, camp_dtype_t dtype,
+                                                const camp_plan_t* plan, void* stream);
 
 #ifdef __cplusplus
 }

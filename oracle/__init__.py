@@ -65,6 +65,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_kv_rmsnorm_rope_cache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                                  i64, i64, dbl, c_int]
     lib.oracle_kv_rmsnorm_rope_cache.restype = c_int
+    lib.oracle_layernorm_f64.argtypes = [vp, vp, vp, vp, vp, i64, i64, dbl]
+    lib.oracle_layernorm_f64.restype = c_int
+    lib.oracle_layernorm.argtypes = [vp, vp, vp, vp, i64, i64, dbl, c_int, c_int]
+    lib.oracle_layernorm.restype = c_int
     lib.oracle_rope_interleaved.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, c_int]
     lib.oracle_rope_interleaved.restype = c_int
     lib.oracle_rope_tables.argtypes = [vp, vp, i64, i64, dbl]
@@ -200,6 +204,38 @@ def kv_rmsnorm_rope_cache(kv: np.ndarray, gamma: np.ndarray, sin_t: np.ndarray,
         _ptr(kv), _ptr(gamma), _ptr(sin_t), _ptr(cos_t), _ptr(slots), _ptr(cn), _ptr(cr),
         B, S, Dn, Dr, cn.shape[0], float(eps), code), "kv_rmsnorm_rope_cache")
     return cn, cr
+
+
+def layernorm_f64(x, gamma, beta, eps: float, lib: ctypes.CDLL | None = None
+                  ) -> tuple[np.ndarray, np.ndarray]:
+    """(y, scale): unrounded fp64 LayerNorm of fp64 x [rows, cols] and, per element,
+    |xhat * gamma| + |beta| (the magnitude fp32 arithmetic errors are relative to)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    g = np.ascontiguousarray(gamma, dtype=np.float64)
+    b = np.ascontiguousarray(beta, dtype=np.float64)
+    rows, cols = x.shape
+    y = np.empty_like(x)
+    scale = np.empty_like(x)
+    _check(lib.oracle_layernorm_f64(_ptr(x), _ptr(g), _ptr(b), _ptr(y), _ptr(scale), rows, cols,
+                                    float(eps)), "layernorm_f64")
+    return y, scale
+
+
+def layernorm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float, dtype: str,
+              nthreads: int = 0, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """LayerNorm of storage-typed x [rows, cols]: fp64 inside, one rounding."""
+    lib = lib or load()
+    code, npt = _storage(dtype)
+    x = np.ascontiguousarray(x)
+    gamma = np.ascontiguousarray(gamma)
+    beta = np.ascontiguousarray(beta)
+    assert x.dtype == npt and gamma.dtype == npt and beta.dtype == npt
+    rows, cols = x.shape
+    y = np.empty_like(x)
+    _check(lib.oracle_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, cols,
+                                float(eps), code, int(nthreads)), "layernorm")
+    return y
 
 
 def rope_interleaved(x: np.ndarray, sin_t: np.ndarray, cos_t: np.ndarray,

@@ -41,6 +41,11 @@
 // 1 sign, 8 exponent, 7 fraction bits). Decoding either to fp64 is exact. Encoding
 // rounds to nearest, ties to even (the pages are silent; this is the IEEE default).
 //
+//   LayerNorm  (xserv "phase 4", csrc/normalization/layernorm.cu: y = gamma * (x - mean) /
+//            sqrt(var + eps) + beta, population variance)
+//       mean = sum_j x_j / n,  var = sum_j (x_j - mean)^2 / n   (Neumaier sums, fp64)
+//       y_j  = (x_j - mean) / sqrt(var + eps) * gamma_j + beta_j, one rounding.
+//
 //   Interleaved RoPE with position ids  (xserv "phase 4" rope kernel: pairs (x[2i], x[2i+1]),
 //            y0 = x0 cos - x1 sin, y1 = x0 sin + x1 cos, table row positions[token])
 //       tokens whose position is outside [0, max_pos) are left unwritten.
@@ -141,6 +146,40 @@ void rmsnorm_row(const double* x, const double* w, double* y, int64_t cols, doub
     const double rms = std::sqrt(mean_sq + eps);
     for (int64_t j = 0; j < cols; ++j) {
         y[j] = x[j] / rms * w[j];
+    }
+}
+
+// ---------------------------------------------------------------- LayerNorm, fp64
+
+double neumaier_sum(const double* v, int64_t n) {
+    double sum = 0.0;
+    double comp = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const double t = v[j];
+        const double s = sum + t;
+        if (std::fabs(sum) >= std::fabs(t)) {
+            comp += (sum - s) + t;
+        } else {
+            comp += (t - s) + sum;
+        }
+        sum = s;
+    }
+    return sum + comp;
+}
+
+// y = normalized row * gamma + beta; `scale` (may be null) receives |xhat * gamma| + |beta|,
+// the magnitude the fp32 arithmetic of a kernel is relative to.
+void layernorm_row(const double* x, const double* g, const double* b, double* y, double* scale,
+                   int64_t n, double eps) {
+    const double mean = neumaier_sum(x, n) / static_cast<double>(n);
+    std::vector<double> d2(static_cast<size_t>(n));
+    for (int64_t j = 0; j < n; ++j) d2[j] = (x[j] - mean) * (x[j] - mean);
+    const double var = neumaier_sum(d2.data(), n) / static_cast<double>(n);
+    const double den = std::sqrt(var + eps);
+    for (int64_t j = 0; j < n; ++j) {
+        const double xhat = (x[j] - mean) / den;
+        y[j] = xhat * g[j] + b[j];
+        if (scale) scale[j] = std::fabs(xhat * g[j]) + std::fabs(b[j]);
     }
 }
 
@@ -297,6 +336,40 @@ int oracle_kv_rmsnorm_rope_cache(const void* kv, const void* gamma, const float*
             for (int64_t j = 0; j < Dr; ++j) store_elem(cache_r, slot * Dr + j, yr[j], dtype);
         }
     }
+    return 0;
+}
+
+// LayerNorm over fp64 x [rows, cols], gamma, beta [cols]: unrounded y and the error scale.
+int oracle_layernorm_f64(const double* x, const double* g, const double* b, double* y,
+                         double* scale, int64_t rows, int64_t cols, double eps) {
+    if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
+    if (rows == 0) return 0;
+    if (!x || !g || !b || !y || !scale) return 1;
+    for (int64_t r = 0; r < rows; ++r)
+        layernorm_row(x + r * cols, g, b, y + r * cols, scale + r * cols, cols, eps);
+    return 0;
+}
+
+// LayerNorm over storage-typed x, gamma, beta: decode, fp64, one rounding of y.
+int oracle_layernorm(const void* x, const void* gamma, const void* beta, void* y, int64_t rows,
+                     int64_t cols, double eps, int dtype, int nthreads) {
+    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
+    if (rows == 0) return 0;
+    if (!x || !gamma || !beta || !y) return 1;
+    std::vector<double> g(static_cast<size_t>(cols)), b(static_cast<size_t>(cols));
+    for (int64_t j = 0; j < cols; ++j) {
+        g[j] = load_elem(gamma, j, dtype);
+        b[j] = load_elem(beta, j, dtype);
+    }
+    parallel_blocks(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        std::vector<double> xr(static_cast<size_t>(cols)), yr(static_cast<size_t>(cols));
+        for (int64_t r = r0; r < r1; ++r) {
+            for (int64_t j = 0; j < cols; ++j) xr[j] = load_elem(x, r * cols + j, dtype);
+            layernorm_row(xr.data(), g.data(), b.data(), yr.data(), nullptr, cols, eps);
+            for (int64_t j = 0; j < cols; ++j) store_elem(y, r * cols + j, yr[j], dtype);
+        }
+    });
     return 0;
 }
 

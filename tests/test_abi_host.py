@@ -448,3 +448,91 @@ def test_rope_tables_argument_errors(lib):
                  (S_, C_, 16, 8, math.inf), (None, C_, 16, 8, 1e4), (S_, S_ + 8, 16, 8, 1e4)):
         assert lib.camp_rope_tables(*args, None) == camp.ERR_INVALID_ARG
     assert lib.camp_rope_tables(None, None, 0, 8, 1e4, None) == camp.SUCCESS
+
+
+# ------------------------------------------------------------------ LayerNorm
+
+BETA = 0x7FA000000000
+
+
+def _ln(lib, x=X, g=W, b=BETA, y=Y, rows=4, cols=8, eps=1e-5, dtype=camp.BF16):
+    return lib.camp_layernorm(x, g, b, y, rows, cols, ctypes.c_float(eps), dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"dtype": 4}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({"cols": 0}, camp.ERR_INVALID_ARG),
+    ({"rows": -2}, camp.ERR_INVALID_ARG),
+    ({"eps": -1.0}, camp.ERR_INVALID_ARG),
+    ({"eps": math.nan}, camp.ERR_INVALID_ARG),
+    ({"g": None}, camp.ERR_INVALID_ARG),
+    ({"b": None}, camp.ERR_INVALID_ARG),
+    ({"b": BETA + 1}, camp.ERR_INVALID_ARG),            # not element aligned
+    ({"y": BETA}, camp.ERR_INVALID_ARG),                # output over beta
+    ({"y": BETA - 8}, camp.ERR_INVALID_ARG),
+    ({"y": W}, camp.ERR_INVALID_ARG),                   # output over gamma
+    ({"y": X + 2}, camp.ERR_INVALID_ARG),               # partial overlap with x
+])
+def test_layernorm_argument_errors(lib, kw, status):
+    assert _ln(lib, **kw) == status
+
+
+def test_layernorm_empty_and_in_place(lib):
+    assert _ln(lib, x=None, g=None, b=None, y=None, rows=0) == camp.SUCCESS
+    assert _ln(lib, rows=0, eps=-1.0) == camp.ERR_INVALID_ARG
+    p = camp.camp_layernorm_plan(X, W, BETA, X, 4096, 2048, "bf16")   # y == x is accepted
+    assert p.kernel == camp.KERNEL_LAYERNORM_ROWS
+
+
+@pytest.mark.parametrize("rows,cols,dtype", [
+    (4096, 2048, "bf16"), (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"),
+    (1, 8, "bf16"), (64, 3001, "bf16"), (4096, 12288, "bf16"), (1024, 32768, "bf16"),
+    (5, 65536, "bf16"), (7, 32768, "f32"), (3, 16384, "f32"),
+])
+def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype):
+    # the same register-resident row mapping as RMSNorm: the same group and accesses a thread
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
+    q = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype)
+    assert q.kernel == camp.KERNEL_RMSNORM_ROWS
+    assert p.kernel == camp.KERNEL_LAYERNORM_ROWS
+    assert (p.vec_bytes, p.group, p.per_thread, p.block, p.grid, p.cluster) == \
+        (q.vec_bytes, q.group, q.per_thread, q.block, q.grid, 1)
+
+
+def test_layernorm_rows_that_do_not_fit_one_group_are_refused(lib):
+    # 1024 threads x 8 sixteen-byte accesses hold 65536 bf16 / 32768 fp32 elements; the
+    # element path holds 1024 x 16
+    for cols, dtype, b in ((65544, "bf16", BETA), (32772, "f32", BETA), (16385, "bf16", BETA + 2)):
+        with pytest.raises(camp.CampError):
+            camp.camp_layernorm_plan(X, W, b, Y, 4, cols, dtype)
+
+
+def test_layernorm_misaligned_beta_uses_element_accesses(lib):
+    p = camp.camp_layernorm_plan(X, W, BETA + 2, Y, 4, 2048, "bf16")
+    assert p.vec_bytes == 2
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 2048, "bf16")
+    assert p.vec_bytes == 16
+
+
+def test_layernorm_with_plan_checks_the_forced_plan(lib):
+    bad = [
+        camp.Plan(kernel=camp.KERNEL_LAYERNORM_ROWS, vec_bytes=8, group=128, per_thread=2),
+        camp.Plan(kernel=camp.KERNEL_LAYERNORM_ROWS, vec_bytes=16, group=128, per_thread=1),
+        camp.Plan(kernel=camp.KERNEL_LAYERNORM_ROWS, vec_bytes=16, group=100, per_thread=4),
+        camp.Plan(kernel=camp.KERNEL_LAYERNORM_ROWS, vec_bytes=16, group=128, per_thread=5),
+        camp.Plan(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=16, group=128, per_thread=2),
+    ]
+    for p in bad:
+        st = lib.camp_layernorm_with_plan(X, W, BETA, Y, 4, 2048, ctypes.c_float(1e-5),
+                                          camp.BF16, ctypes.byref(p), None)
+        assert st == camp.ERR_NOT_SUPPORTED, (p.vec_bytes, p.group, p.per_thread)
+
+
+def test_single_kernel_ops_refuse_a_plan_for_another_kernel(lib):
+    p = camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, per_thread=1)
+    assert lib.camp_kv_rmsnorm_rope_cache_with_plan(
+        X, W, SIN, COS, R_, Y, H_, 1, 4, 512, 64, 16, ctypes.c_float(1e-6), camp.BF16,
+        ctypes.byref(p), None) == camp.ERR_NOT_SUPPORTED
+    p = camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, group=1)
+    assert lib.camp_rope_interleaved_with_plan(X, SIN, COS, R_, Y, 4, 8, 64, 16, camp.BF16,
+                                               ctypes.byref(p), None) == camp.ERR_NOT_SUPPORTED

@@ -38,6 +38,17 @@ def test_rmsnorm_effective_bandwidth_matches_gollamago_table(key):
     assert round(nbytes / (ms * 1e-3) / 1e9) == pytest.approx(gbs, abs=1)
 
 
+def test_layernorm_ledger_matches_tutorial_example_2():
+    g = _golden()
+    fused = ledger.layernorm_bytes(8192, 4096, "fp16", affine=False)
+    split = ledger.layernorm_bytes(8192, 4096, "fp16", affine=False, passes=3)
+    assert round(fused / 1e6, 1) == float(g["ln_ex2_fused_bytes"])
+    assert round(split / 1e6, 1) == float(g["ln_ex2_unfused_bytes"])
+    assert round(ledger.layernorm_flops(8192, 4096) / 1e9, 3) == float(g["ln_ex2_flops"])
+    # with gamma and beta read once each, as reported by the benchmark
+    assert ledger.layernorm_bytes(8192, 4096, "fp16") == fused + 2 * 4096 * 2
+
+
 def test_benchmark_step_bytes():
     # RMSNorm bf16 [4096, 2048] + RoPE Q [1,4096,32,64] + RoPE K [1,4096,8,64], with the
     # weight and the fp32 tables counted once per launch.

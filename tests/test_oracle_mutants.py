@@ -59,6 +59,11 @@ MUTANTS = {
     "tables use theta^(-i/D)":
         ("const double freq = std::pow(theta, (-2.0 * static_cast<double>(i)) /",
          "const double freq = std::pow(theta, (-1.0 * static_cast<double>(i)) /"),
+    "layernorm variance divides by n - 1":
+        ("const double var = neumaier_sum(d2.data(), n) / static_cast<double>(n);",
+         "const double var = neumaier_sum(d2.data(), n) / static_cast<double>(n - 1);"),
+    "layernorm beta added before the weight":
+        ("y[j] = xhat * g[j] + b[j];", "y[j] = (xhat + b[j]) * g[j];"),
     "add path normalizes the unrounded sum":
         ("hr[j] = load_elem(h, i, dtype);",
          "hr[j] = load_elem(x, i, dtype) + load_elem(r, i, dtype);"),
@@ -89,6 +94,8 @@ def _battery(lib):
         ("rope interleaved", lambda: [pins.test_rope_interleaved_is_rotate_half_on_deinterleaved_input(lib, d)
                                       for d in ("bf16", "f32")]),
         ("rope tables", lambda: pins.test_rope_tables_match_numpy_and_closed_forms(lib)),
+        ("layernorm worked", lambda: pins.test_layernorm_worked_case(lib)),
+        ("layernorm numpy", lambda: pins.test_layernorm_matches_numpy_mean_and_std(lib)),
         ("add rmsnorm", lambda: [pins.test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, d)
                                  for d in ("bf16", "f32")]),
     ]

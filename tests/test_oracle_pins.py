@@ -313,6 +313,80 @@ def test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, dtype):
         np.testing.assert_array_equal(cr[slot], cr0[slot])
 
 
+# ------------------------------------------------------------------------ LayerNorm
+
+def test_layernorm_worked_case(lib):
+    # [1, 2, 3, 4]: mean 2.5, var 1.25 -> (x - 2.5) / sqrt(1.25); then gamma 2, beta -1.
+    y, _ = oracle.layernorm_f64(np.array([[1.0, 2.0, 3.0, 4.0]]), np.full(4, 2.0),
+                                np.full(4, -1.0), 0.0, lib=lib)
+    want = [2 * (k - 2.5) / math.sqrt(1.25) - 1 for k in (1, 2, 3, 4)]
+    np.testing.assert_allclose(y[0], want, rtol=1e-15)
+
+
+def test_layernorm_constant_row_gives_beta(lib):
+    # x_j = c: every deviation is 0, so y = beta exactly (eps > 0).
+    b = np.linspace(-1, 1, 33)
+    y, _ = oracle.layernorm_f64(np.full((2, 33), 7.25), np.linspace(0.5, 2, 33), b, 1e-5, lib=lib)
+    np.testing.assert_array_equal(y, np.stack([b, b]))
+
+
+@pytest.mark.parametrize("a,shift", [(2.0, 0.0), (0.01, 100.0), (1e3, -3.0)])
+def test_layernorm_affine_invariance(lib, a, shift):
+    # eps = 0: LayerNorm(a x + b) = LayerNorm(x) for a > 0.
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((3, 257))
+    g, b = rng.standard_normal(257), rng.standard_normal(257)
+    y1, _ = oracle.layernorm_f64(x, g, b, 0.0, lib=lib)
+    y2, _ = oracle.layernorm_f64(a * x + shift, g, b, 0.0, lib=lib)
+    np.testing.assert_allclose(y2, y1, rtol=1e-9, atol=1e-10)
+
+
+def test_layernorm_matches_numpy_mean_and_std(lib):
+    # numpy's mean and population std (ddof = 0) as the library routines.
+    rng = np.random.default_rng(62)
+    for n in (1, 2, 7, 768, 4099):
+        x = rng.standard_normal((2, n)) * 3 + 50
+        g, b = rng.standard_normal(n), rng.standard_normal(n)
+        y, _ = oracle.layernorm_f64(x, g, b, 1e-5, lib=lib)
+        for r in range(2):
+            want = (x[r] - x[r].mean()) / np.sqrt(x[r].var() + 1e-5) * g + b
+            np.testing.assert_allclose(y[r], want, rtol=1e-9, atol=1e-12)
+
+
+def test_layernorm_brute_force_exact_rationals(lib):
+    rng = np.random.default_rng(63)
+    for cols in range(1, 20):
+        x = rng.standard_normal(cols) * rng.choice([1e-3, 1.0, 1e3]) + rng.choice([0.0, 100.0])
+        g, b = rng.standard_normal(cols), rng.standard_normal(cols)
+        eps = float(rng.choice([1e-6, 1e-5, 0.5]))
+        y, _ = oracle.layernorm_f64(x[None], g, b, eps, lib=lib)
+        xs = [Fraction(float(v)) for v in x]
+        mean = sum(xs) / cols
+        var = sum((v - mean) ** 2 for v in xs) / cols + Fraction(eps)
+        den = _dsqrt(var)
+        # fp64 rounds the mean by ~u|mean|; relative to a deviation that is |mean| / sigma.
+        cond = 1 + abs(float(mean)) / float(den)
+        for j in range(cols):
+            d = xs[j] - mean
+            want = Decimal(d.numerator) / Decimal(d.denominator) / den * Decimal(float(g[j])) \
+                + Decimal(float(b[j]))
+            bound = 1e-14 * cond * (1 + abs(float(d / 1) / float(den) * float(g[j])) + abs(b[j]))
+            assert abs(y[0, j] - float(want)) <= bound
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_layernorm_storage_path_rounds_the_fp64_result_once(lib, dtype):
+    rng = np.random.default_rng(64)
+    xt, xs = _storage_pair(rng, (5, 300), dtype)
+    _, gs = _storage_pair(rng, (300,), dtype)
+    _, bs = _storage_pair(rng, (300,), dtype, 0.1)
+    dec = (lambda a: oracle.bf16_value(a, lib=lib)) if dtype == "bf16" else (lambda a: a.astype(np.float64))
+    y64, _ = oracle.layernorm_f64(dec(xs), dec(gs), dec(bs), 1e-5, lib=lib)
+    y = oracle.layernorm(xs, gs, bs, 1e-5, dtype, lib=lib)
+    want = oracle.bf16_round(y64, lib=lib) if dtype == "bf16" else y64.astype(np.float32)
+    np.testing.assert_array_equal(y, want)
+
+
 # ------------------------------------------------------------------------ interleaved RoPE, tables
 
 def _f32_ulps(a: np.ndarray, b: np.ndarray) -> np.ndarray:
