@@ -236,6 +236,46 @@ def capture_kernel(sets, kind: str, first: int, count: int):
     return g
 
 
+def copy_calibration(sets, M: int, blocks: int, peak: float) -> dict:
+    """The floor of this harness: per operator, a plain device-to-device copy of the bytes
+    the operator reads (its x, or Q and K as one flat buffer) into a buffer of the same
+    size, on the same rotating input sets, as CUDA graphs of M back-to-back copies timed
+    with events exactly like the kernels. A copy moves its bytes twice (read + write), as
+    the operators do; the weight and the tables are left out (under 3% of either)."""
+    out = {}
+    R = len(sets)
+    for kind in KERNELS:
+        if kind == "rmsnorm":
+            pairs = [(s.x, torch.empty_like(s.x)) for s in sets]
+        else:
+            n = (sets[0].q.numel() + sets[0].k.numel()) * sets[0].q.element_size()
+            pairs = [(torch.empty(n, dtype=torch.uint8, device="cuda"),
+                      torch.empty(n, dtype=torch.uint8, device="cuda")) for _ in sets]
+            for src, _ in pairs:
+                src.random_(0, 256)
+        moved = 2 * pairs[0][0].numel() * pairs[0][0].element_size()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(M):
+                src, dst = pairs[i % R]
+                dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(blocks):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / (blocks * M)
+        out[kind] = {"bytes_moved": moved, "us": t * 1e6, "GB/s": moved / t / 1e9,
+                     "frac": moved / t / 1e9 / peak}
+        del g, pairs
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ CPU legs (oracle)
 
 def _host_step_inputs(s: InputSet) -> dict:
@@ -468,6 +508,21 @@ def run_case(case: str, launches: int) -> None:
         plan = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16"))
         for _ in range(launches):
             camp.camp_layernorm(x, w, bt, y, rows, cols, EPS, camp.BF16, stream)
+    elif kind == "kv":
+        S, Dn, Dr = dims
+        ns = 2 * S
+        x = torch.randn(1, S, Dn + Dr, device="cuda").to(torch.bfloat16)
+        gam = torch.ones(Dn, device="cuda", dtype=torch.bfloat16)
+        _, sn, cs = inputs.rope_inputs(1, S, 1, Dr, "bf16", seed=0, device="cuda")
+        slots = torch.randperm(ns, device="cuda")[:S].to(torch.int64)
+        y = torch.empty(ns, Dn, device="cuda", dtype=torch.bfloat16)
+        yr = torch.empty(ns, Dr, device="cuda", dtype=torch.bfloat16)
+        p = camp.camp_kv_rmsnorm_rope_cache_plan(x, gam, sn, cs, slots, y, yr, 1, S, Dn, Dr, ns,
+                                                 "bf16")
+        plan = f"kv_cache<bf16,vec{p.vec_bytes},nv{p.per_thread}>"
+        for _ in range(launches):
+            camp.camp_kv_rmsnorm_rope_cache(x, gam, sn, cs, slots, y, yr, 1, S, Dn, Dr, ns, EPS,
+                                            camp.BF16, stream)
     elif kind == "rope_qk":
         B, S, Hq, Hk, D = dims
         q, sn, cs = inputs.rope_inputs(B, S, Hq, D, "bf16", seed=0, device="cuda")
@@ -508,8 +563,9 @@ def main() -> None:
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", default=None,
                     help="profiling mode: launch one operator at one shape --launches times "
-                         "and exit, e.g. rmsnorm:16384x8192, rope:1x16384x32x128 or "
-                         "rope_qk:1x16384x32x8x128 (B x S x Hq x Hk x D)")
+                         "and exit, e.g. rmsnorm:16384x8192, layernorm:16384x2048, "
+                         "rope:1x16384x32x128, rope_qk:1x16384x32x8x128 (B x S x Hq x Hk x D) "
+                         "or kv:65536x512x64 (S x Dn x Dr)")
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.case:
@@ -660,6 +716,8 @@ def main() -> None:
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
            "ms_per_step": e2e_t / args.e2e_steps * 1e3}
 
+    calibration = copy_calibration(sets, M, 50, peak)
+
     large = None
     if rank == 0 and not args.no_large:
         large = large_configs(peak, args.large_reps)
@@ -691,6 +749,10 @@ def main() -> None:
         "e2e": e2e,
         "gpu_launches": len(KERNELS) * args.steps,
         "clocks": clocks,
+        "calibration": {"plain_copy_same_bytes": calibration,
+                        "note": "device-to-device copies of each operator's bytes in the same "
+                                "graph and rotation harness (outside the timed region): the "
+                                "launch, ramp and drain cost any kernel of this size pays"},
     }
     if large is not None:
         line["large_configs"] = large

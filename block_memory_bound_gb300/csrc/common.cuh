@@ -130,6 +130,56 @@ __device__ __forceinline__ uint32_t bf16_pack2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&p);
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+// sm_100-class SMs execute add, sub, mul and fma on two fp32 values held in a 64-bit
+// register pair as one instruction (PTX .f32x2). Each lane is rounded to nearest even,
+// exactly as the scalar instruction rounds it, so pairing elements changes the
+// instruction count, not the arithmetic.
+
+struct f32x2 { unsigned long long v; };
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ f32x2 f2_words(uint32_t lo, uint32_t hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2_lo(f32x2 a) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    return lo;
+}
+__device__ __forceinline__ float f2_hi(f32x2 a) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    return hi;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+// a * b + c, each lane fused (one rounding).
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+
 template <typename S, int BYTES> struct Codec;
 
 template <int BYTES> struct Codec<bf16_t, BYTES> {
@@ -199,11 +249,51 @@ template <int BYTES> struct Codec<bf16_t, BYTES> {
             }
         }
     }
+
+    // Element pairs (2p, 2p + 1) as packed operands: p = 0 .. kPairs - 1 (BYTES >= 4).
+    static constexpr int kPairs = BYTES / 4;
+
+    template <typename F>
+    __device__ __forceinline__ static void each_pair(const Raw<BYTES>& r, F f) {
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) f(k, f2_make(bf16_lo(r.w[k]), bf16_hi(r.w[k])));
+    }
+
+    // out pair p = f(p, in pair p), each element rounded once to bf16.
+    template <typename F>
+    __device__ __forceinline__ static Raw<BYTES> map_pair(const Raw<BYTES>& r, F f) {
+        Raw<BYTES> o;
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+            const f32x2 q = f(k, f2_make(bf16_lo_p(r.w[k]), bf16_hi_p(r.w[k])));
+            o.w[k] = bf16_pack2(f2_lo(q), f2_hi(q));
+        }
+        return o;
+    }
 };
 
 template <int BYTES> struct Codec<f32_t, BYTES> {
     static_assert(BYTES % 4 == 0, "fp32 vector accesses are whole words");
     static constexpr int kElems = BYTES / 4;
+    static constexpr int kPairs = BYTES / 8;
+
+    template <typename F>
+    __device__ __forceinline__ static void each_pair(const Raw<BYTES>& r, F f) {
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) f(k, f2_words(r.w[2 * k], r.w[2 * k + 1]));
+    }
+
+    template <typename F>
+    __device__ __forceinline__ static Raw<BYTES> map_pair(const Raw<BYTES>& r, F f) {
+        Raw<BYTES> o;
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+            const f32x2 q = f(k, f2_words(r.w[2 * k], r.w[2 * k + 1]));
+            o.w[2 * k] = __float_as_uint(f2_lo(q));
+            o.w[2 * k + 1] = __float_as_uint(f2_hi(q));
+        }
+        return o;
+    }
 
     template <typename F>
     __device__ __forceinline__ static void each(const Raw<BYTES>& r, F f) {
@@ -311,11 +401,34 @@ __device__ __forceinline__ void load_table(const float* p, float (&out)[N]) {
 
 // ------------------------------------------------------------------ reductions
 
-// Butterfly (xor) sum over a full warp: every lane receives the total.
+// Butterfly (xor) sum over a full warp: every lane receives the total, with the same bits
+// in every lane (each step adds the same two values in either order).
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
     return v;
+}
+
+// Sum of the W partials p[0 .. W-1] (W a power of two, at most 32; shared memory), taken by
+// the whole warp; every lane gets the same bits. Up to 8 partials: W independent loads
+// and a sequential sum (the shortest dependency chain: measured faster than a butterfly
+// at W = 4). Beyond: lane l loads p[l mod W] and a butterfly over aligned groups of W
+// lanes adds them (one load per lane instead of W, which at W = 32 also keeps 32 values
+// out of the registers).
+template <int W>
+__device__ __forceinline__ float sum_partials(const float* p) {
+    static_assert(W >= 1 && W <= 32 && (W & (W - 1)) == 0, "W is a power of two <= 32");
+    if constexpr (W <= 8) {
+        float v = 0.0f;
+#pragma unroll
+        for (int i = 0; i < W; ++i) v += p[i];
+        return v;
+    } else {
+        float v = p[threadIdx.x & (W - 1)];
+#pragma unroll
+        for (int off = W / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        return v;
+    }
 }
 
 // ------------------------------------------------------------------ integer division

@@ -38,20 +38,93 @@ __device__ __forceinline__ float group_sum(float v, float (&scratch)[LnShape<G>:
     if constexpr (LnShape<G>::kWarpsPerRow > 1) {
         if ((threadIdx.x & 31) == 0) scratch[g][t / 32] = v;
         __syncthreads();
-        v = 0.0f;
-#pragma unroll
-        for (int i = 0; i < LnShape<G>::kWarpsPerRow; ++i) v += scratch[g][i];
+        v = sum_partials<LnShape<G>::kWarpsPerRow>(scratch[g]);
     }
     return v;
 }
 
+// Pass 1: this thread's sum of (x - K) over its live accesses.
+template <typename C, int G, int NV, int VB>
+__device__ __forceinline__ float shifted_sum(const Raw<VB> (&v)[NV], float shift, int live) {
+    if constexpr (C::kElems >= 2) {
+        const f32x2 k2 = f2_make(shift, shift);
+        f32x2 acc = f2_make(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (k * G < live) C::each_pair(v[k], [&](int, f32x2 p) { acc = f2_add(acc, f2_sub(p, k2)); });
+        return f2_lo(acc) + f2_hi(acc);
+    } else {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (k * G < live) C::each(v[k], [&](int, float f) { s += f - shift; });
+        return s;
+    }
+}
+
+// Pass 2: this thread's sum of d^2, d = (x - K) - mu, over its live accesses.
+template <typename C, int G, int NV, int VB>
+__device__ __forceinline__ float squared_deviations(const Raw<VB> (&v)[NV], float shift,
+                                                    float mu, int live) {
+    if constexpr (C::kElems >= 2) {
+        const f32x2 k2 = f2_make(shift, shift), m2 = f2_make(mu, mu);
+        f32x2 acc = f2_make(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (k * G < live)
+                C::each_pair(v[k], [&](int, f32x2 p) {
+                    const f32x2 d = f2_sub(f2_sub(p, k2), m2);
+                    acc = f2_fma(d, d, acc);
+                });
+        return f2_lo(acc) + f2_hi(acc);
+    } else {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (k * G < live)
+                C::each(v[k], [&](int, float f) {
+                    const float d = (f - shift) - mu;
+                    s = fmaf(d, d, s);
+                });
+        return s;
+    }
+}
+
+// One output access: fma(((x - K) - mu) * rstd, gamma, beta), rounded once.
+template <typename C, int VB>
+__device__ __forceinline__ Raw<VB> normalize(const Raw<VB>& xv, const Raw<VB>& gv,
+                                             const Raw<VB>& bv, float shift, float mu,
+                                             float rstd) {
+    if constexpr (C::kElems >= 2) {
+        f32x2 gp[C::kPairs], bp[C::kPairs];
+        C::each_pair(gv, [&](int p, f32x2 q) { gp[p] = q; });
+        C::each_pair(bv, [&](int p, f32x2 q) { bp[p] = q; });
+        const f32x2 k2 = f2_make(shift, shift), m2 = f2_make(mu, mu), r2 = f2_make(rstd, rstd);
+        return C::map_pair(xv, [&](int p, f32x2 xp) {
+            return f2_fma(f2_mul(f2_sub(f2_sub(xp, k2), m2), r2), gp[p], bp[p]);
+        });
+    } else {
+        float gf[C::kElems], bf[C::kElems];
+        C::each(gv, [&](int e, float f) { gf[e] = f; });
+        C::each(bv, [&](int e, float f) { bf[e] = f; });
+        return C::map(xv, [&](int e, float xf) {
+            return fmaf(((xf - shift) - mu) * rstd, gf[e], bf[e]);
+        });
+    }
+}
+
 // Occupancy budget: for fp32 the deviations x - mean of the variance pass stay live into
 // the output pass (the raw words are the values themselves), so budget twice the data.
-template <typename S, int NV>
-constexpr int ln_live_loads() { return Storage<S>::kBytes == 4 ? 2 * NV : NV; }
+// The one bf16 variant that does not fit 32 registers at two 1024-thread CTAs per SM
+// (1024 threads x 2 accesses; the planner prefers 256 x 8 for the same rows) runs one CTA
+// per SM instead of spilling.
+template <typename S, int G, int NV>
+constexpr int ln_live_loads() {
+    return Storage<S>::kBytes == 4 ? 2 * NV : (G == 1024 && NV == 2 ? NV + 1 : NV);
+}
 
 template <typename S, int VB, int G, int NV>
-__global__ void __launch_bounds__(LnShape<G>::kBlock, rows_min_blocks(VB, G, ln_live_loads<S, NV>()))
+__global__ void __launch_bounds__(LnShape<G>::kBlock, rows_min_blocks(VB, G, ln_live_loads<S, G, NV>()))
 layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
                       const void* __restrict__ beta, void* y, int64_t rows, int64_t cols,
                       float eps) {
@@ -89,24 +162,8 @@ layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
     }
 
     const float n = static_cast<float>(cols);
-    float s1 = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        C::each(v[k], [&](int, float f) {
-            if (k * G < live) s1 += f - shift;
-        });
-    }
-    const float mu = group_sum<G>(s1, part_mean, g, t) / n;   // mean - shift
-
-    float s2 = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        C::each(v[k], [&](int, float f) {
-            const float d = (f - shift) - mu;
-            if (k * G < live) s2 = fmaf(d, d, s2);
-        });
-    }
-    const float var = group_sum<G>(s2, part_var, g, t) / n;
+    const float mu = group_sum<G>(shifted_sum<C, G>(v, shift, live), part_mean, g, t) / n;
+    const float var = group_sum<G>(squared_deviations<C, G>(v, shift, mu, live), part_var, g, t) / n;
     const float rstd = rsqrtf(var + eps);
 
     if (!active) return;
@@ -115,14 +172,10 @@ layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
     char* yr = static_cast<char*>(y) + off;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        if (k * G < live) {
-            float gf[E], bf[E];
-            C::each(ld_shared_ro<VB>(gt + k * G * VB), [&](int e, float f) { gf[e] = f; });
-            C::each(ld_shared_ro<VB>(bt + k * G * VB), [&](int e, float f) { bf[e] = f; });
-            st_out<VB>(yr + k * G * VB, C::map(v[k], [&](int e, float xf) {
-                return fmaf(((xf - shift) - mu) * rstd, gf[e], bf[e]);
-            }));
-        }
+        if (k * G < live)
+            st_out<VB>(yr + k * G * VB,
+                       normalize<C>(v[k], ld_shared_ro<VB>(gt + k * G * VB),
+                                    ld_shared_ro<VB>(bt + k * G * VB), shift, mu, rstd));
     }
 }
 

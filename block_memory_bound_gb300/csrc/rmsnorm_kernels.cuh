@@ -47,6 +47,38 @@ struct RowsShape {
     static constexpr int kWarpsPerRow = G / 32;
 };
 
+// This thread's share of sum(x^2) over its NV raw vectors (zeros where it has none), in
+// fp32: two packed accumulators (even and odd elements) where an access holds pairs.
+template <typename C, int NV, int VB>
+__device__ __forceinline__ float sum_squares(const Raw<VB> (&v)[NV]) {
+    if constexpr (C::kElems >= 2) {
+        f32x2 acc = f2_make(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) C::each_pair(v[k], [&](int, f32x2 p) { acc = f2_fma(p, p, acc); });
+        return f2_lo(acc) + f2_hi(acc);
+    } else {
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) C::each(v[k], [&](int, float f) { ss = fmaf(f, f, ss); });
+        return ss;
+    }
+}
+
+// One output access: (x * rinv) * w per element, in fp32, rounded once.
+template <typename C, int VB>
+__device__ __forceinline__ Raw<VB> scale_row(const Raw<VB>& xv, const Raw<VB>& wv, float rinv) {
+    if constexpr (C::kElems >= 2) {
+        f32x2 wp[C::kPairs];
+        C::each_pair(wv, [&](int p, f32x2 q) { wp[p] = q; });
+        const f32x2 r2 = f2_make(rinv, rinv);
+        return C::map_pair(xv, [&](int p, f32x2 xp) { return f2_mul(f2_mul(xp, r2), wp[p]); });
+    } else {
+        float wf[C::kElems];
+        C::each(wv, [&](int e, float f) { wf[e] = f; });
+        return C::map(xv, [&](int e, float xf) { return (xf * rinv) * wf[e]; });
+    }
+}
+
 // Load access k of this thread (x, or h = x + r stored on the way on the add path).
 template <typename S, int VB, bool ADD, int NV>
 __device__ __forceinline__ void load_row(const char* xr, const char* rr, char* hr, int live,
@@ -108,16 +140,12 @@ rmsnorm_rows_kernel(const void* x, const void* r, void* h, const void* __restric
                              ADD ? static_cast<char*>(h) + off : nullptr, live, G * VB, G, v,
                              active);
 
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) C::each(v[k], [&](int, float f) { ss = fmaf(f, f, ss); });
+    float ss = sum_squares<C>(v);
     ss = warp_sum(ss);
     if constexpr (Sh::kWarpsPerRow > 1) {
         if ((threadIdx.x & 31) == 0) partial[g][t / 32] = ss;
         __syncthreads();
-        ss = 0.0f;
-#pragma unroll
-        for (int i = 0; i < Sh::kWarpsPerRow; ++i) ss += partial[g][i];
+        ss = sum_partials<Sh::kWarpsPerRow>(partial[g]);
     }
     const float rinv = rsqrtf(ss / static_cast<float>(cols) + eps);
 
@@ -126,13 +154,8 @@ rmsnorm_rows_kernel(const void* x, const void* r, void* h, const void* __restric
     char* yr = static_cast<char*>(y) + off;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        if (k * G < live) {
-            const Raw<VB> wv = ld_shared_ro<VB>(wt + k * G * VB);
-            float wf[E];
-            C::each(wv, [&](int e, float f) { wf[e] = f; });
-            st_out<VB>(yr + k * G * VB,
-                       C::map(v[k], [&](int e, float xf) { return (xf * rinv) * wf[e]; }));
-        }
+        if (k * G < live)
+            st_out<VB>(yr + k * G * VB, scale_row<C>(v[k], ld_shared_ro<VB>(wt + k * G * VB), rinv));
     }
 }
 
@@ -169,10 +192,7 @@ rmsnorm_cluster_kernel(const void* x, const void* r, void* h, const void* __rest
                              ADD ? static_cast<char*>(h) + off : nullptr, live,
                              kClusterBlock * VB, kClusterBlock, v, true);
 
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) C::each(v[k], [&](int, float f) { ss = fmaf(f, f, ss); });
-    ss = warp_sum(ss);
+    float ss = warp_sum(sum_squares<C>(v));
     if ((t & 31) == 0) partial[t / 32] = ss;
     __syncthreads();
     // Thread r < C writes this CTA's partial into slot[rank] of cluster rank r: one round of
@@ -195,13 +215,9 @@ rmsnorm_cluster_kernel(const void* x, const void* r, void* h, const void* __rest
     char* yr = static_cast<char*>(y) + off;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        if (k * kClusterBlock < live) {
-            const Raw<VB> wv = ld_shared_ro<VB>(wt + k * kClusterBlock * VB);
-            float wf[E];
-            C::each(wv, [&](int e, float f) { wf[e] = f; });
+        if (k * kClusterBlock < live)
             st_out<VB>(yr + k * kClusterBlock * VB,
-                       C::map(v[k], [&](int e, float xf) { return (xf * rinv) * wf[e]; }));
-        }
+                       scale_row<C>(v[k], ld_shared_ro<VB>(wt + k * kClusterBlock * VB), rinv));
     }
 }
 
@@ -243,19 +259,15 @@ rmsnorm_wide_kernel(const void* x, const void* r, void* h, const void* __restric
         ss = warp_sum(ss);
         if ((threadIdx.x & 31) == 0) partial[threadIdx.x / 32] = ss;
         __syncthreads();
-        ss = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kWideBlock / 32; ++i) ss += partial[i];
+        ss = sum_partials<kWideBlock / 32>(partial);
         const float rinv = rsqrtf(ss / fcols + eps);
 
         // Sweep 2: normalize the row as stored (x, or h on the add path).
         const char* src = ADD ? static_cast<const char*>(hr) : xr;
         char* yr = static_cast<char*>(y) + row * pitch;
         for (int64_t idx = threadIdx.x; idx < nvec; idx += kWideBlock) {
-            const Raw<VB> xv = ld_stream<VB>(src + idx * VB);
-            float wf[E];
-            C::each(ld_shared_ro<VB>(wb + idx * VB), [&](int e, float f) { wf[e] = f; });
-            st_out<VB>(yr + idx * VB, C::map(xv, [&](int e, float xf) { return (xf * rinv) * wf[e]; }));
+            st_out<VB>(yr + idx * VB,
+                       scale_row<C>(ld_stream<VB>(src + idx * VB), ld_shared_ro<VB>(wb + idx * VB), rinv));
         }
         __syncthreads();   // partial[] is reused by the next row
     }

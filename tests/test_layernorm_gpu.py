@@ -1,9 +1,10 @@
 """LayerNorm parity: camp_layernorm (through the C ABI) against the fp64 oracle.
 
-Tolerance, derived from the kernel's fp32 arithmetic (u = 2^-24). A row is summed as L
-terms per thread (accesses x elements per access), then a 5-level warp tree and a
-sequential sum of G/32 warp partials: k = L + 5 + G/32 roundings at most, and Higham's
-bound |fl(sum a) - sum a| <= k u sum |a| applies to both sums. With K = x[row, 0],
+Tolerance, derived from the kernel's fp32 arithmetic (u = 2^-24). A thread sums its L
+terms (accesses x elements per access) in two interleaved accumulators joined by one add
+(L/2 + 1 roundings; L for one-element accesses), then a 5-level warp tree and a
+log2(G/32)-level tree of the warp partials; k = L + 5 + G/32 bounds that count, and
+Higham's bound |fl(sum a) - sum a| <= k u sum |a| applies to both sums. With K = x[row, 0],
 c = mean|x - K| / sqrt(var + eps) (a property of the input row) and xhat the exact
 normalized value, the fp32 kernel satisfies, per element,
 
