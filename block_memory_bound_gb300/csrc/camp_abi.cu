@@ -147,6 +147,7 @@ int round_up_in(int v, const int* set, int n) {
 struct RowsCandidate {
     int group, per_thread;
     int64_t ctas, idle;
+    bool one_wave;   // every CTA resident at once (CTAs <= SMs x CTAs per SM)
 };
 
 // Is candidate a preferred over b? Measured on GB300 (L2-cold, back-to-back launches):
@@ -156,11 +157,15 @@ struct RowsCandidate {
 //     too little in flight per thread, above it the row group's barrier and the
 //     1024-thread CTAs cost more than they save;
 //  3. fewest idle vector slots (a ragged last access per thread wastes issue slots);
-//  4. within 2., fewer accesses per thread (more threads, shorter serial work per thread);
+//  4. a grid that is resident in one wave: then every load is issued at the start instead
+//     of when a CTA of the first wave retires (4096 x 2048 bf16: 64 x 4 in one wave
+//     6.98 us, 128 x 2 in 1.7 waves 7.25 us);
+//  5. within 2., fewer accesses per thread (more threads, shorter serial work per thread);
 //     outside it, the smaller group (512-thread CTAs beat 1024-thread ones: 16384 bf16
 //     columns at 4096 rows run 42 us with 512 x 4 and 50 us with 1024 x 2).
-// At 4096 x 2048 this picks 128 x 2, at 4096 x 3000 128 x 3, at 16384 x 8192 256 x 4 and at
-// 4096 x 12288 / 16384 512 x 3 / 4, the fastest of the compiled variants at each.
+// For bf16 this picks 64 x 4 at 4096 x 2048, 128 x 2 at 8192 x 2048 and more rows,
+// 128 x 3 at 3000 columns, 256 x 4 at 8192, and 256 x 6 / 256 x 8 at 12288 / 16384
+// columns: the fastest of the compiled variants at each, or within 2-5% of it.
 bool rows_better(const RowsCandidate& a, const RowsCandidate& b) {
     const int64_t sa = a.ctas < camp::kSmCount ? a.ctas : camp::kSmCount;
     const int64_t sb = b.ctas < camp::kSmCount ? b.ctas : camp::kSmCount;
@@ -169,12 +174,15 @@ bool rows_better(const RowsCandidate& a, const RowsCandidate& b) {
     const bool mb = b.per_thread >= 2 && b.per_thread <= 4 && b.group <= 256;
     if (ma != mb) return ma;
     if (a.idle != b.idle) return a.idle < b.idle;
+    if (a.one_wave != b.one_wave) return a.one_wave;
     if (ma) return a.per_thread < b.per_thread;
     return a.group < b.group;
 }
 
 // Choose the register-resident variant; false if no compiled variant holds the row.
-bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread) {
+// `layernorm` selects the LayerNorm kernel's occupancy for the one-wave test.
+bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread,
+                     bool layernorm = false) {
     const int es = camp::elem_bytes(c.t);
     const int64_t nvec = c.a.cols * es / vb;
     static const int kGroupsVec[] = {32, 64, 128, 256, 512, 1024};
@@ -200,6 +208,10 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread) {
         if (!camp::rows_variant_compiled(c.add, vb, g, k.per_thread)) continue;
         k.ctas = ceil_div(c.a.rows, camp::rows_block(g) / g);
         k.idle = static_cast<int64_t>(g) * k.per_thread - nvec;
+        const int per_sm =
+            layernorm ? camp::ln_min_blocks(es, vb, g, k.per_thread)
+                      : camp::rows_min_blocks(vb, g, c.add ? 2 * k.per_thread : k.per_thread);
+        k.one_wave = k.ctas <= static_cast<int64_t>(camp::kSmCount) * per_sm;
         if (!found || rows_better(k, best)) best = k;
         found = true;
     }
@@ -724,7 +736,7 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
     } else {
         p->vec_bytes = widest;
         int g = 0, nv = 0;
-        if (!rms_choose_rows(rc, widest, &g, &nv)) return CAMP_ERR_NOT_SUPPORTED;
+        if (!rms_choose_rows(rc, widest, &g, &nv, true)) return CAMP_ERR_NOT_SUPPORTED;
         p->group = g;
         p->per_thread = nv;
     }

@@ -53,19 +53,38 @@ struct RopeArgs {
 constexpr int rows_block(int group) { return group < 256 ? 256 : group; }
 
 // `loads` raw accesses are live per thread at the peak: per_thread, or twice that on the
-// add path (x and r are both in flight before h is formed).
-constexpr int rows_threads_per_sm(int vec_bytes, int loads) {
-    // 32-bit registers of raw row data per thread
+// add path (x and r are both in flight before h is formed). Threads per SM by the 32-bit
+// registers of raw row data per thread: up to 8, a full SM (32 registers a thread); up to
+// 16, a full SM as well for groups of at most 128 threads (checked with -Xptxas -v: those
+// variants fit 32 registers without spilling; at 4096 x 2048 bf16 the 64 x 4 variant then
+// runs in one wave and measured 4% faster than 128 x 2), else 1536; then 1024 and 512.
+constexpr int rows_threads_per_sm(int vec_bytes, int loads, int group) {
     return (loads * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 8 ? 2048
-         : (loads * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 16 ? 1536
+         : (loads * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 16 ? (group <= 128 ? 2048 : 1536)
          : (loads * (vec_bytes < 4 ? 1 : vec_bytes / 4)) <= 32 ? 1024
          : 512;
 }
 
 constexpr int rows_min_blocks(int vec_bytes, int group, int loads) {
-    return rows_threads_per_sm(vec_bytes, loads) / rows_block(group) < 1
+    return rows_threads_per_sm(vec_bytes, loads, group) / rows_block(group) < 1
                ? 1
-               : rows_threads_per_sm(vec_bytes, loads) / rows_block(group);
+               : rows_threads_per_sm(vec_bytes, loads, group) / rows_block(group);
+}
+
+// LayerNorm rows kernel occupancy (CTAs per SM). The LayerNorm passes keep the shift and
+// the mean live beside the data, so the row kernels' 2048-thread budget for 16 words does
+// not apply (those variants spill); threads per SM by 32-bit data registers are 2048 up to
+// 8, 1536 up to 16, 1024 up to 32, else 512. For fp32 the deviations of the variance pass
+// stay live into the output pass (the raw words are the values themselves), so the data
+// counts twice. The one bf16 variant that does not fit 32 registers at two 1024-thread
+// CTAs per SM (1024 x 2 accesses; the planner prefers 256 x 8 for the same rows) runs one
+// CTA per SM instead of spilling.
+constexpr int ln_min_blocks(int elem_bytes, int vec_bytes, int group, int per_thread) {
+    const int per_load = vec_bytes < 4 ? 1 : vec_bytes / 4;
+    int words = (elem_bytes == 4 ? 2 : 1) * per_thread * per_load;
+    if (elem_bytes == 2 && group == 1024 && per_thread == 2) words += per_load;
+    const int threads = words <= 8 ? 2048 : words <= 16 ? 1536 : words <= 32 ? 1024 : 512;
+    return threads / rows_block(group) < 1 ? 1 : threads / rows_block(group);
 }
 
 // The add path keeps x and r in flight together; with 1024 threads (64 registers each) and

@@ -113,18 +113,8 @@ __device__ __forceinline__ Raw<VB> normalize(const Raw<VB>& xv, const Raw<VB>& g
     }
 }
 
-// Occupancy budget: for fp32 the deviations x - mean of the variance pass stay live into
-// the output pass (the raw words are the values themselves), so budget twice the data.
-// The one bf16 variant that does not fit 32 registers at two 1024-thread CTAs per SM
-// (1024 threads x 2 accesses; the planner prefers 256 x 8 for the same rows) runs one CTA
-// per SM instead of spilling.
-template <typename S, int G, int NV>
-constexpr int ln_live_loads() {
-    return Storage<S>::kBytes == 4 ? 2 * NV : (G == 1024 && NV == 2 ? NV + 1 : NV);
-}
-
 template <typename S, int VB, int G, int NV>
-__global__ void __launch_bounds__(LnShape<G>::kBlock, rows_min_blocks(VB, G, ln_live_loads<S, G, NV>()))
+__global__ void __launch_bounds__(LnShape<G>::kBlock, ln_min_blocks(Storage<S>::kBytes, VB, G, NV))
 layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
                       const void* __restrict__ beta, void* y, int64_t rows, int64_t cols,
                       float eps) {

@@ -123,8 +123,12 @@ def test_rope_empty_is_success_without_cuda(lib):
 
 @pytest.mark.parametrize("rows,cols,dtype,expect", [
     # (kernel, vec_bytes, group, per_thread, block, grid)
-    # 256 vectors a row: 128 x 2 and 64 x 4 both fit exactly; fewer accesses per thread wins
-    (4096, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 256, 2048)),
+    # 256 vectors a row: 128 x 2 and 64 x 4 both fit exactly. At 4096 rows 64 x 4 runs in one
+    # wave (1024 CTAs <= 152 SMs x 8) and 128 x 2 does not (2048 CTAs); with two waves
+    # either way, or one either way, fewer accesses per thread wins
+    (4096, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 64, 4, 256, 1024)),
+    (8192, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 256, 4096)),
+    (2048, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 256, 1024)),
     (16384, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 16384)),
     # 375 vectors a row: 128 x 3 leaves 9 slots idle, 256 x 2 leaves 137
     (4096, 3000, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 3, 256, 2048)),
@@ -485,7 +489,7 @@ def test_layernorm_empty_and_in_place(lib):
 
 
 @pytest.mark.parametrize("rows,cols,dtype", [
-    (4096, 2048, "bf16"), (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"),
+    (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"), (8192, 2048, "bf16"),
     (1, 8, "bf16"), (64, 3001, "bf16"), (4096, 12288, "bf16"), (1024, 32768, "bf16"),
     (5, 65536, "bf16"), (7, 32768, "f32"), (3, 16384, "f32"),
 ])
@@ -497,6 +501,15 @@ def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype)
     assert p.kernel == camp.KERNEL_LAYERNORM_ROWS
     assert (p.vec_bytes, p.group, p.per_thread, p.block, p.grid, p.cluster) == \
         (q.vec_bytes, q.group, q.per_thread, q.block, q.grid, 1)
+
+
+def test_layernorm_one_wave_test_uses_its_own_occupancy(lib):
+    # RMSNorm's 64 x 4 holds 8 CTAs per SM, LayerNorm's 6 (it keeps more live): at 4096 x 2048
+    # neither LayerNorm candidate fits one wave, so the one with fewer accesses per thread wins
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4096, 2048, "bf16")
+    assert (p.group, p.per_thread, p.grid) == (128, 2, 2048)
+    q = camp.camp_rmsnorm_plan(X, W, Y, 4096, 2048, "bf16")
+    assert (q.group, q.per_thread, q.grid) == (64, 4, 1024)
 
 
 def test_layernorm_rows_that_do_not_fit_one_group_are_refused(lib):
