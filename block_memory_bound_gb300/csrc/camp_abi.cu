@@ -572,44 +572,73 @@ camp_status_t kv_validate(const void* kv, const void* gamma, const float* sin_t,
     return CAMP_SUCCESS;
 }
 
-// 16-byte accesses when every row start and pointer allows them, else element accesses.
+bool kv_rope_ok(const KvCall& c, int rb);
+
+// 16-byte norm accesses when the norm part of every row starts on a 16-byte boundary, the
+// pointers allow them and the rope part can take 4-, 8- or 16-byte accesses; else element
+// accesses for both parts.
 int kv_vec_bytes(const KvCall& c) {
     const int es = camp::elem_bytes(c.t);
-    const bool ok = (c.a.dn * es) % 16 == 0 && ((c.a.dr / 2) * es) % 16 == 0 &&
+    const bool ok = (c.a.dn * es) % 16 == 0 && ((c.a.dn + c.a.dr) * es) % 16 == 0 &&
                     aligned(c.a.kv, 16) && aligned(c.a.gamma, 16) && aligned(c.a.cache_n, 16) &&
-                    aligned(c.a.cache_r, 16) && aligned(c.a.sin_t, 16) && aligned(c.a.cos_t, 16);
+                    ((es == 2 && kv_rope_ok(c, 4)) || kv_rope_ok(c, 8) || kv_rope_ok(c, 16));
     return ok ? 16 : es;
 }
 
-// Norm accesses per lane for a vector width, or 0 if the row does not fit one warp
-// (at most 8 16-byte or 16 element accesses per lane for the norm part, one vector per
-// lane for each rope half).
+// Can the rope part use rb-byte accesses per half and lane (rb/es elements of each half
+// and as many sine and cosine values) within one warp?
+bool kv_rope_ok(const KvCall& c, int rb) {
+    const int es = camp::elem_bytes(c.t);
+    const int64_t half_bytes = (c.a.dr / 2) * es;
+    const int re = rb / es;
+    const int table_align = 4 * re < 16 ? 4 * re : 16;
+    return half_bytes % rb == 0 && half_bytes / rb <= 32 && (c.a.dn * es) % rb == 0 &&
+           aligned(c.a.kv, rb) && aligned(c.a.cache_r, rb) && aligned(c.a.sin_t, table_align) &&
+           aligned(c.a.cos_t, table_align);
+}
+
+// The rope access width for a norm access width: the element size on the element path;
+// with 16-byte norm accesses the narrowest of 4, 8 and 16 bytes that holds a pair and
+// fits (the rope part spread over the most lanes); 0 if none does.
+int kv_rope_bytes(const KvCall& c, int vb) {
+    const int es = camp::elem_bytes(c.t);
+    if (vb != 16) return kv_rope_ok(c, es) ? es : 0;
+    for (int rb : {4, 8, 16})
+        if (rb >= 2 * es && kv_rope_ok(c, rb)) return rb;
+    return 0;
+}
+
+// Norm accesses per lane for a vector width, or 0 if the norm part does not fit one warp
+// (at most 8 16-byte or 16 element accesses per lane).
 int kv_nvn(const KvCall& c, int vb) {
     const int es = camp::elem_bytes(c.t);
     const int64_t nvec = c.a.dn * es / vb;
     const int64_t need = ceil_div(nvec, 32);
     const int max_nvn = vb == 16 ? 8 : 16;
-    if (need > max_nvn || (c.a.dr / 2) * es / vb > 32) return 0;
+    if (need > max_nvn) return 0;
     static const int kNvn[] = {1, 2, 4, 8, 16};
     return round_up_in(static_cast<int>(need), kNvn, 5);
 }
 
+// Plan fields: vec_bytes = norm access width, per_thread = norm accesses per lane,
+// group = rope access width per half and lane (0 in a forced plan: the default for its
+// vec_bytes).
 camp_status_t kv_plan(const KvCall& c, const camp_plan_t* forced, camp_plan_t* p) {
     if (forced && forced->kernel != CAMP_KERNEL_KV_CACHE) return CAMP_ERR_NOT_SUPPORTED;
     *p = camp_plan_t{};
     p->kernel = CAMP_KERNEL_KV_CACHE;
-    p->vec_bytes = forced ? forced->vec_bytes : kv_vec_bytes(c);
     const int es = camp::elem_bytes(c.t);
+    p->vec_bytes = forced ? forced->vec_bytes : kv_vec_bytes(c);
     if (p->vec_bytes != 16 && p->vec_bytes != es) return CAMP_ERR_NOT_SUPPORTED;
     if (p->vec_bytes > kv_vec_bytes(c)) return CAMP_ERR_NOT_SUPPORTED;
     const int need = kv_nvn(c, p->vec_bytes);
     if (need == 0) return CAMP_ERR_NOT_SUPPORTED;
     p->per_thread = forced ? forced->per_thread : need;
     if (p->per_thread < need) return CAMP_ERR_NOT_SUPPORTED;
-    const int pt = p->per_thread;
-    if (!(pt == 1 || pt == 2 || pt == 4 || pt == 8 || (pt == 16 && p->vec_bytes != 16)))
+    p->group = forced && forced->group != 0 ? forced->group : kv_rope_bytes(c, p->vec_bytes);
+    if (p->group == 0 || !kv_rope_ok(c, p->group)) return CAMP_ERR_NOT_SUPPORTED;
+    if (!camp::kv_cache_compiled(c.t, p->vec_bytes, p->per_thread, p->group))
         return CAMP_ERR_NOT_SUPPORTED;
-    p->group = 32;
     p->block = camp::kKvBlock;
     p->cluster = 1;
     p->grid = ceil_div(c.a.tokens, camp::kKvTokensPerCta);
@@ -884,7 +913,7 @@ CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_with_plan(
     camp_plan_t p;
     st = kv_plan(c, plan, &p);
     if (st != CAMP_SUCCESS) return st;
-    return runtime_status(camp::kv_cache_launch(c.t, p.vec_bytes, p.per_thread, c.a,
+    return runtime_status(camp::kv_cache_launch(c.t, p.vec_bytes, p.per_thread, p.group, c.a,
                                                 static_cast<cudaStream_t>(stream)));
 }
 

@@ -202,8 +202,24 @@ struct KvCacheArgs {
 constexpr int kKvBlock = 256;
 constexpr int kKvTokensPerCta = kKvBlock / 32;   // one warp per token
 
-// `nvn`: norm accesses per lane (1, 2, 4, 8; 16 on the element path only).
-cudaError_t kv_cache_launch(DType t, int vec_bytes, int nvn, const KvCacheArgs& a,
-                            cudaStream_t s);
+// CTAs per SM of the KV kernel by the 32-bit registers of data a lane holds: its norm
+// accesses, both rope halves and as many sine and cosine values as rope elements (element
+// accesses counted twice: each takes a whole register and its own address). Up to 16
+// words: 8 CTAs (2048 threads, 32 registers); 22: 6; 40: 4; beyond: 2 (checked with
+// -Xptxas -v: no variant spills).
+constexpr int kv_min_blocks(int elem_bytes, int vec_bytes, int nvn, int rope_bytes) {
+    const int norm = vec_bytes == 16 ? 4 * nvn : 2 * nvn;
+    const int rope_words = rope_bytes < 4 ? 1 : rope_bytes / 4;
+    const int words = norm + 2 * rope_words + 2 * (rope_bytes / elem_bytes);
+    return words <= 16 ? 8 : words <= 22 ? 6 : words <= 40 ? 4 : 2;
+}
+
+// `vec_bytes`: norm access width (16, or the element size); `nvn`: norm accesses per lane
+// (1, 2, 4, 8; 16 on the element path only); `rope_bytes`: rope access width per half and
+// lane (with 16-byte norm accesses, 4, 8 or 16 bytes holding at least one pair; the
+// element size on the element path).
+bool kv_cache_compiled(DType t, int vec_bytes, int nvn, int rope_bytes);
+cudaError_t kv_cache_launch(DType t, int vec_bytes, int nvn, int rope_bytes,
+                            const KvCacheArgs& a, cudaStream_t s);
 
 }  // namespace camp

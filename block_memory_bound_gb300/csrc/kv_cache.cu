@@ -10,24 +10,31 @@
 // cache_r[num_slots, Dr]; a slot outside [0, num_slots) is not written (padding).
 //
 // Mapping: one warp per token, 8 tokens per CTA. Lane l loads norm accesses l, l+32, ...
-// (NVN of them) and, for l < (Dr/2)/E, vector l of both rope halves; all loads are issued
-// before any arithmetic. The sum of squares is a butterfly warp shuffle (no barrier), the
-// table row is s = t mod S, and both outputs are written once to the cache rows.
+// (NVN accesses of VB bytes) and, for l < (Dr/2) / RE, elements l*RE .. l*RE + RE - 1 of
+// both rope halves (RB bytes each, RE = RB / element size) with their RE sine and cosine
+// values; all loads are issued before any arithmetic. The rope width is spread over as
+// many lanes as it fills (RB is the narrowest access that holds a pair and keeps it within
+// one warp), so that no lane holds much more than another: at the common widths the
+// kernel fits 32 registers and a full SM of warps keeps enough bytes in flight. The sum of squares is a butterfly warp shuffle
+// (no barrier); the table row s = t mod S is a multiply-shift division when there are
+// fewer than 2^32 tokens, else a 64-bit remainder; both outputs are written once.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace camp {
 namespace {
 
-template <typename S, int VB, int NVN>
-__global__ void __launch_bounds__(kKvBlock, 4)
+template <typename S, int VB, int NVN, int RB>
+__global__ void __launch_bounds__(kKvBlock, kv_min_blocks(Storage<S>::kBytes, VB, NVN, RB))
 kv_rmsnorm_rope_cache_kernel(const void* kv, const void* __restrict__ gamma,
                              const float* __restrict__ sin_t, const float* __restrict__ cos_t,
                              const int64_t* __restrict__ slots, void* cache_n, void* cache_r,
-                             int64_t tokens, int64_t seq, int dn, int dr, int64_t num_slots,
-                             float eps) {
+                             int64_t tokens, int64_t seq, FastDiv seq_div, bool fast_seq,
+                             int dn, int dr, int64_t num_slots, float eps) {
     using C = Codec<S, VB>;
+    using CR = Codec<S, RB>;
     constexpr int E = C::kElems;
+    constexpr int RE = CR::kElems;
     constexpr int ES = Storage<S>::kBytes;
 
     griddep_wait();
@@ -37,31 +44,39 @@ kv_rmsnorm_rope_cache_kernel(const void* kv, const void* __restrict__ gamma,
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
     const int64_t token = block * kKvTokensPerCta + threadIdx.x / 32;
     if (token >= tokens) return;                       // whole warps only; no barrier below
-    const int64_t slot = slots[token];
-    if (slot < 0 || slot >= num_slots) return;         // padding: nothing is written
 
     const int half = dr / 2;
-    const int nvh = half / E;                          // rope vectors per half
     const int live = dn / E - lane;                    // norm access k exists iff k*32 < live
     const char* row = static_cast<const char*>(kv) + token * static_cast<int64_t>(dn + dr) * ES;
     const char* xn = row + static_cast<int64_t>(lane) * VB;
-    const char* xr = row + static_cast<int64_t>(dn) * ES + static_cast<int64_t>(lane) * VB;
+    const char* xr = row + static_cast<int64_t>(dn) * ES + static_cast<int64_t>(lane) * RB;
 
     Raw<VB> v[NVN];
 #pragma unroll
     for (int k = 0; k < NVN; ++k)
         v[k] = (k * 32 < live) ? ld_stream<VB>(xn + k * 32 * VB) : raw_zero<VB>();
-    const bool roper = lane < nvh;
-    Raw<VB> lo = raw_zero<VB>(), hi = raw_zero<VB>();
+    const bool roper = lane < half / RE;
+    Raw<RB> lo = raw_zero<RB>(), hi = raw_zero<RB>();
+    float sn[RE], cs[RE];
     if (roper) {
-        lo = ld_stream<VB>(xr);
-        hi = ld_stream<VB>(xr + static_cast<int64_t>(half) * ES);
+        lo = ld_stream<RB>(xr);
+        hi = ld_stream<RB>(xr + static_cast<int64_t>(half) * ES);
+        const int64_t s = fast_seq ? static_cast<int64_t>(
+                                         static_cast<uint32_t>(token) -
+                                         fast_div(static_cast<uint32_t>(token), seq_div) *
+                                             static_cast<uint32_t>(seq))
+                                   : token % seq;
+        const int64_t toff = s * half + static_cast<int64_t>(lane) * RE;
+        load_table<RE>(sin_t + toff, sn);
+        load_table<RE>(cos_t + toff, cs);
     }
+    const int64_t slot = slots[token];
 
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < NVN; ++k) C::each(v[k], [&](int, float f) { ss = fmaf(f, f, ss); });
     ss = warp_sum(ss);
+    if (slot < 0 || slot >= num_slots) return;         // padding: nothing is written
     const float rinv = rsqrtf(ss / static_cast<float>(dn) + eps);
 
     char* yn = static_cast<char*>(cache_n) + slot * static_cast<int64_t>(dn) * ES +
@@ -78,58 +93,87 @@ kv_rmsnorm_rope_cache_kernel(const void* kv, const void* __restrict__ gamma,
     }
 
     if (roper) {
-        const int64_t s = token % seq;
-        float sn[E], cs[E];
-        const int64_t toff = s * half + static_cast<int64_t>(lane) * E;
-        load_table<E>(sin_t + toff, sn);
-        load_table<E>(cos_t + toff, cs);
-        Raw<VB> o1, o2;
-        C::map2(lo, hi, o1, o2, [&](int e, float x1, float x2) {
+        Raw<RB> o1, o2;
+        CR::map2(lo, hi, o1, o2, [&](int e, float x1, float x2) {
             return make_float2(diff_of_products(x1, cs[e], x2, sn[e]),
                                sum_of_products(x2, cs[e], x1, sn[e]));
         });
         char* yr = static_cast<char*>(cache_r) + slot * static_cast<int64_t>(dr) * ES +
-                   static_cast<int64_t>(lane) * VB;
-        st_out<VB>(yr, o1);
-        st_out<VB>(yr + static_cast<int64_t>(half) * ES, o2);
+                   static_cast<int64_t>(lane) * RB;
+        st_out<RB>(yr, o1);
+        st_out<RB>(yr + static_cast<int64_t>(half) * ES, o2);
     }
 }
 
-template <typename S, int VB, int NVN>
+template <typename S, int VB, int NVN, int RB>
 cudaError_t launch_kv(const KvCacheArgs& a, cudaStream_t s) {
     const int64_t blocks = (a.tokens + kKvTokensPerCta - 1) / kKvTokensPerCta;
-    return launch_pdl(kv_rmsnorm_rope_cache_kernel<S, VB, NVN>, grid_2d(blocks), dim3(kKvBlock),
-                      s, a.kv, a.gamma, a.sin_t, a.cos_t, a.slots, a.cache_n, a.cache_r,
-                      a.tokens, a.seq, static_cast<int>(a.dn), static_cast<int>(a.dr),
-                      a.num_slots, a.eps);
+    const bool fast = a.tokens <= 0xFFFFFFFFll;
+    const FastDiv d = make_fast_div(static_cast<uint32_t>(fast ? a.seq : 1));
+    return launch_pdl(kv_rmsnorm_rope_cache_kernel<S, VB, NVN, RB>, grid_2d(blocks),
+                      dim3(kKvBlock), s, a.kv, a.gamma, a.sin_t, a.cos_t, a.slots, a.cache_n,
+                      a.cache_r, a.tokens, a.seq, d, fast, static_cast<int>(a.dn),
+                      static_cast<int>(a.dr), a.num_slots, a.eps);
 }
 
-template <typename S, int VB>
-cudaError_t launch_kv_nvn(int nvn, const KvCacheArgs& a, cudaStream_t s) {
+// 16-byte norm accesses: the rope part takes 4- (bf16 only), 8- or 16-byte accesses.
+template <typename S, int NVN>
+cudaError_t launch_kv_rb(int rb, const KvCacheArgs& a, cudaStream_t s) {
+    switch (rb) {
+        case 4:
+            if constexpr (Storage<S>::kBytes == 2) return launch_kv<S, 16, NVN, 4>(a, s);
+            else return cudaErrorInvalidValue;
+        case 8: return launch_kv<S, 16, NVN, 8>(a, s);
+        case 16: return launch_kv<S, 16, NVN, 16>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename S>
+cudaError_t launch_kv_vec(int nvn, int rb, const KvCacheArgs& a, cudaStream_t s) {
     switch (nvn) {
-        case 1: return launch_kv<S, VB, 1>(a, s);
-        case 2: return launch_kv<S, VB, 2>(a, s);
-        case 4: return launch_kv<S, VB, 4>(a, s);
-        case 8: return launch_kv<S, VB, 8>(a, s);
-        case 16:
-            if constexpr (VB == 16) return cudaErrorInvalidValue;   // not built: would spill
-            else return launch_kv<S, VB, 16>(a, s);
+        case 1: return launch_kv_rb<S, 1>(rb, a, s);
+        case 2: return launch_kv_rb<S, 2>(rb, a, s);
+        case 4: return launch_kv_rb<S, 4>(rb, a, s);
+        case 8: return launch_kv_rb<S, 8>(rb, a, s);
+        default: return cudaErrorInvalidValue;   // 16 is not built here: it would spill
+    }
+}
+
+// Element accesses for both parts.
+template <typename S>
+cudaError_t launch_kv_elem(int nvn, const KvCacheArgs& a, cudaStream_t s) {
+    constexpr int ES = Storage<S>::kBytes;
+    switch (nvn) {
+        case 1: return launch_kv<S, ES, 1, ES>(a, s);
+        case 2: return launch_kv<S, ES, 2, ES>(a, s);
+        case 4: return launch_kv<S, ES, 4, ES>(a, s);
+        case 8: return launch_kv<S, ES, 8, ES>(a, s);
+        case 16: return launch_kv<S, ES, 16, ES>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t kv_cache_launch(DType t, int vec_bytes, int nvn, const KvCacheArgs& a,
-                            cudaStream_t s) {
-    if (t == DType::BF16) {
-        if (vec_bytes == 16) return launch_kv_nvn<bf16_t, 16>(nvn, a, s);
-        if (vec_bytes == 2) return launch_kv_nvn<bf16_t, 2>(nvn, a, s);
-    } else {
-        if (vec_bytes == 16) return launch_kv_nvn<f32_t, 16>(nvn, a, s);
-        if (vec_bytes == 4) return launch_kv_nvn<f32_t, 4>(nvn, a, s);
-    }
-    return cudaErrorInvalidValue;
+bool kv_cache_compiled(DType t, int vec_bytes, int nvn, int rope_bytes) {
+    const int es = elem_bytes(t);
+    if (vec_bytes == 16)
+        return (nvn == 1 || nvn == 2 || nvn == 4 || nvn == 8) &&
+               ((rope_bytes == 4 && es == 2) || rope_bytes == 8 || rope_bytes == 16);
+    if (vec_bytes == es)
+        return (nvn == 1 || nvn == 2 || nvn == 4 || nvn == 8 || nvn == 16) && rope_bytes == es;
+    return false;
+}
+
+cudaError_t kv_cache_launch(DType t, int vec_bytes, int nvn, int rope_bytes,
+                            const KvCacheArgs& a, cudaStream_t s) {
+    if (!kv_cache_compiled(t, vec_bytes, nvn, rope_bytes)) return cudaErrorInvalidValue;
+    if (t == DType::BF16)
+        return vec_bytes == 16 ? launch_kv_vec<bf16_t>(nvn, rope_bytes, a, s)
+                               : launch_kv_elem<bf16_t>(nvn, a, s);
+    return vec_bytes == 16 ? launch_kv_vec<f32_t>(nvn, rope_bytes, a, s)
+                           : launch_kv_elem<f32_t>(nvn, a, s);
 }
 
 }  // namespace camp

@@ -181,10 +181,13 @@ CAMP_API camp_status_t camp_rope_qk(const void* q, const void* k, const float* s
  *                             arithmetic, one rounding).
  *   Dn >= 1; Dr even, >= 2; eps as for camp_rmsnorm. B*S == 0 is a no-op.
  *
- * One read of kv, one write of each cache row. Supported widths: up to 256 x 16-byte
- * vectors for the norm part and 32 per rope half (bf16: Dn <= 2048, Dr <= 512; element
- * accesses: Dn <= 512, Dr <= 64); otherwise CAMP_ERR_NOT_SUPPORTED. The caches must be
- * disjoint from every input and from each other. Errors as for camp_rmsnorm.
+ * One read of kv, one write of each cache row; a padding token's kv row is read (with the
+ * rest of the warp's loads, before its slot is known) but nothing is written for it.
+ * Supported widths: up to 256 16-byte vectors for the norm part and 32 lanes of at most
+ * 16 bytes per rope half (bf16: Dn <= 2048, Dr <= 512; fp32: Dn <= 1024, Dr <= 256); when
+ * the norm rows or the pointers are not 16-byte aligned, element accesses (Dn <= 512,
+ * Dr <= 64); otherwise CAMP_ERR_NOT_SUPPORTED. The caches must be disjoint from every
+ * input and from each other. Errors as for camp_rmsnorm.
  */
 CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache(const void* kv, const void* gamma,
                                                   const float* sin, const float* cos,
@@ -278,7 +281,8 @@ typedef enum {
 typedef struct {
     int32_t kernel;        /* camp_kernel_t */
     int32_t vec_bytes;     /* bytes per vector access of x and y: 16, 8, 4 or 2 */
-    int32_t group;         /* RMSNorm: threads per row. RoPE: heads per thread */
+    int32_t group;         /* RMSNorm: threads per row. RoPE: heads per thread. KV cache:
+                              rope access bytes per half and lane */
     int32_t per_thread;    /* RMSNorm: vector accesses per thread per row. RoPE: unused (0) */
     int32_t block;         /* threads per CTA */
     int32_t cluster;       /* CTAs per cluster (RMSNorm cluster kernel: 2..16), else 1 */
@@ -341,15 +345,17 @@ CAMP_API camp_status_t camp_add_rmsnorm_with_plan(const void* x, const void* r, 
                                                   float eps, camp_dtype_t dtype,
                                                   const camp_plan_t* plan, void* stream);
 
-/* Like camp_rmsnorm_plan, for camp_kv_rmsnorm_rope_cache (vec_bytes, per_thread = norm
- * accesses per lane; group = 32 threads, one warp per token). */
+/* Like camp_rmsnorm_plan, for camp_kv_rmsnorm_rope_cache: one warp per token; vec_bytes =
+ * norm access width (16 or the element size), per_thread = norm accesses per lane, group =
+ * rope access width per half and lane (4, 8 or 16 bytes with 16-byte norm accesses, the
+ * element size otherwise). */
 CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_plan(
     const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
     const void* cache_n, const void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
     int64_t num_slots, camp_dtype_t dtype, camp_plan_t* plan);
 
-/* camp_kv_rmsnorm_rope_cache with an explicit plan (vec_bytes, per_thread); NULL plan = the
- * default one. */
+/* camp_kv_rmsnorm_rope_cache with an explicit plan (vec_bytes, per_thread, group; group 0
+ * takes the default rope width for vec_bytes); NULL plan = the default one. */
 CAMP_API camp_status_t camp_kv_rmsnorm_rope_cache_with_plan(
     const void* kv, const void* gamma, const float* sin, const float* cos, const int64_t* slots,
     void* cache_n, void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,

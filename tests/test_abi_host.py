@@ -404,12 +404,40 @@ def test_kv_cache_argument_errors(lib, change, kw, status):
     assert _kv(lib, ptrs, **kw) == status
 
 
-def test_kv_cache_plans(lib):
-    p = camp.camp_kv_rmsnorm_rope_cache_plan(*KVP, 1, 65536, 512, 64, 131072, "bf16")
-    assert (p.kernel, p.vec_bytes, p.group, p.per_thread, p.grid) == (camp.KERNEL_KV_CACHE, 16, 32, 2, 8192)
-    p = camp.camp_kv_rmsnorm_rope_cache_plan(*KVP, 2, 3, 33, 6, 8, "bf16")   # odd widths
-    assert (p.vec_bytes, p.per_thread) == (2, 2)
+@pytest.mark.parametrize("dtype,Dn,Dr,expect", [
+    # (vec_bytes, per_thread, group = rope bytes per half and lane)
+    # bf16 Dr 64: 64 bytes a half -> 4-byte accesses (one pair) over 16 lanes
+    ("bf16", 512, 64, (16, 2, 4)),
+    ("bf16", 512, 128, (16, 2, 4)),      # 32 lanes
+    ("bf16", 512, 256, (16, 2, 8)),      # 4 bytes would need 64 lanes
+    ("bf16", 2048, 512, (16, 8, 16)),
+    ("f32", 512, 64, (16, 4, 8)),        # fp32 pairs: 8 bytes
+    ("f32", 1024, 256, (16, 8, 16)),
+    ("bf16", 33, 6, (2, 2, 2)),          # odd widths: element accesses for both parts
+])
+def test_kv_cache_plans(lib, dtype, Dn, Dr, expect):
+    p = camp.camp_kv_rmsnorm_rope_cache_plan(*KVP, 1, 65536, Dn, Dr, 131072, dtype)
+    assert p.kernel == camp.KERNEL_KV_CACHE
+    assert (p.vec_bytes, p.per_thread, p.group) == expect
+    assert p.grid == 8192
+
+
+def test_kv_cache_plan_edges(lib):
     assert _kv(lib, B=0) == camp.SUCCESS
+    assert _kv(lib, Dr=1024) == camp.ERR_NOT_SUPPORTED              # 16 bytes x 32 lanes < a half
+    # a rope cache that is not 4-byte aligned sends both parts to element accesses
+    ptrs = list(KVP)
+    ptrs[6] += 2
+    p = camp.camp_kv_rmsnorm_rope_cache_plan(*ptrs, 1, 16, 512, 64, 64, "bf16")
+    assert (p.vec_bytes, p.per_thread, p.group) == (2, 16, 2)
+    # forced plans: a rope width that does not cover a half, or that is not built
+    for vb, nvn, rb, dtype in ((16, 2, 4, "bf16"), (16, 4, 4, "f32"), (16, 2, 2, "bf16")):
+        plan = camp.Plan(kernel=camp.KERNEL_KV_CACHE, vec_bytes=vb, per_thread=nvn, group=rb)
+        Dr = 512 if rb == 4 and dtype == "bf16" else 64
+        st = lib.camp_kv_rmsnorm_rope_cache_with_plan(
+            *KVP, 1, 16, 512, Dr, 64, ctypes.c_float(1e-5), camp.BF16 if dtype == "bf16" else camp.F32,
+            ctypes.byref(plan), None)
+        assert st == camp.ERR_NOT_SUPPORTED, (vb, nvn, rb, dtype)
 
 
 # ------------------------------------------------------------------ interleaved RoPE, tables

@@ -87,13 +87,22 @@ def test_shapes(shape, dtype):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_every_variant(dtype):
     es = 2 if dtype == "bf16" else 4
-    for vb, nvns in ((16, (1, 2, 4, 8)), (es, (1, 2, 4, 8, 16))):
-        e = vb // es
-        for nvn in nvns:
-            Dn = max(e, (32 * nvn - 1) * e)          # one access short: a ragged last lane
-            Dr = 2 * e * 3
-            plan = camp.Plan(kernel=camp.KERNEL_KV_CACHE, vec_bytes=vb, per_thread=nvn)
-            run_case(2, 6, Dn, Dr, dtype, seed=vb * nvn, plan=plan)
+    # (norm access bytes, norm accesses per lane, rope access bytes per half and lane)
+    variants = [(16, nvn, rb) for nvn in (1, 2, 4, 8) for rb in (4, 8, 16) if rb >= 2 * es]
+    variants += [(es, nvn, es) for nvn in (1, 2, 4, 8, 16)]
+    for vb, nvn, rb in variants:
+        e, re = vb // es, rb // es
+        Dn = max(e, (32 * nvn - 1) * e)              # one access short: a ragged last lane
+        for lanes in (6, 32):                        # a few rope lanes, and a full warp
+            Dr = 2 * re * lanes
+            plan = camp.Plan(kernel=camp.KERNEL_KV_CACHE, vec_bytes=vb, per_thread=nvn,
+                             group=rb)
+            run_case(2, 6, Dn, Dr, dtype, seed=vb * nvn + rb + lanes, plan=plan)
+
+
+def test_many_tokens_uses_the_table_row_of_each_position():
+    # 3 x 1500 tokens: the table row is t mod S for every token (multiply-shift division)
+    run_case(3, 1500, 64, 64, "bf16", seed=11, pad=True)
 
 
 def test_no_padding_full_cache():
