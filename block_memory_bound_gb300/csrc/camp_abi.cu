@@ -147,7 +147,8 @@ int round_up_in(int v, const int* set, int n) {
 struct RowsCandidate {
     int group, per_thread;
     int64_t ctas, idle;
-    bool one_wave;   // every CTA resident at once (CTAs <= SMs x CTAs per SM)
+    bool one_wave;     // every CTA resident at once (CTAs <= SMs x CTAs per SM)
+    bool many_waves;   // at least 2 waves of CTAs
 };
 
 // Is candidate a preferred over b? Measured on GB300 (L2-cold, back-to-back launches):
@@ -166,7 +167,12 @@ struct RowsCandidate {
 // For bf16 this picks 64 x 4 at 4096 x 2048, 128 x 2 at 8192 x 2048 and more rows,
 // 128 x 3 at 3000 columns, 256 x 4 at 8192, and 256 x 6 / 256 x 8 at 12288 / 16384
 // columns: the fastest of the compiled variants at each, or within 2-5% of it.
-bool rows_better(const RowsCandidate& a, const RowsCandidate& b) {
+// LayerNorm (`layernorm`) differs in 5.: its per-thread cost (two reductions) is higher,
+// so when both candidates run at least 2 waves the one with more accesses per thread
+// wins (bf16, 64 x 4 against 128 x 2: 65536 x 2048 80.5 / 90.9 us, 8192 x 2048 14.3 /
+// 14.5 us; 8192 x 4096: 128 x 4 24.2 us, 256 x 2 24.6 us); closer to one wave the RMSNorm
+// order holds (4096 x 2048: 128 x 2 9.0 us, 64 x 4 in 1.1 waves 10.2 us).
+bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm) {
     const int64_t sa = a.ctas < camp::kSmCount ? a.ctas : camp::kSmCount;
     const int64_t sb = b.ctas < camp::kSmCount ? b.ctas : camp::kSmCount;
     if (sa != sb) return sa > sb;
@@ -175,6 +181,7 @@ bool rows_better(const RowsCandidate& a, const RowsCandidate& b) {
     if (ma != mb) return ma;
     if (a.idle != b.idle) return a.idle < b.idle;
     if (a.one_wave != b.one_wave) return a.one_wave;
+    if (ma && layernorm && a.many_waves && b.many_waves) return a.per_thread > b.per_thread;
     if (ma) return a.per_thread < b.per_thread;
     return a.group < b.group;
 }
@@ -212,7 +219,8 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread,
             layernorm ? camp::ln_min_blocks(es, vb, g, k.per_thread)
                       : camp::rows_min_blocks(vb, g, c.add ? 2 * k.per_thread : k.per_thread);
         k.one_wave = k.ctas <= static_cast<int64_t>(camp::kSmCount) * per_sm;
-        if (!found || rows_better(k, best)) best = k;
+        k.many_waves = k.ctas >= 2 * static_cast<int64_t>(camp::kSmCount) * per_sm;
+        if (!found || rows_better(k, best, layernorm)) best = k;
         found = true;
     }
     if (!found) return false;
@@ -697,8 +705,12 @@ int64_t rope_il_tpc(const RopeIlCall& c, int vb, int hpt) {
     return per_pos <= camp::kRopeBlock ? camp::kRopeBlock / per_pos : 0;
 }
 
-// Widest legal vector; 2 heads per thread (1 for odd head counts), more when a token's
-// heads would not fit one CTA; CAMP_ERR_NOT_SUPPORTED when even 8 do not.
+// Widest legal vector; 4 heads per thread when the head count is a multiple of 4, else 2
+// (1 for odd head counts), more when a token's heads would not fit one CTA;
+// CAMP_ERR_NOT_SUPPORTED when even 8 do not. Measured on GB300 (bf16, random positions,
+// L2-cold): 4 heads per thread against 2 run 65536 x 32 x 128 in 160.9 / 185.0 us,
+// 4096 x 32 x 128 in 12.3 / 13.6 us, 65536 x 8 x 64 in 23.7 / 26.7 us (each token's
+// table row is loaded once per head group, so more heads per thread load it fewer times).
 camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_plan_t* p) {
     if (forced && forced->kernel != CAMP_KERNEL_ROPE_INTERLEAVED) return CAMP_ERR_NOT_SUPPORTED;
     *p = camp_plan_t{};
@@ -714,7 +726,7 @@ camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_
             if (rope_il_vec_ok(c, vb)) { p->vec_bytes = vb; break; }
         }
         if (p->vec_bytes == 0) return CAMP_ERR_NOT_SUPPORTED;   // pointers not pair-aligned
-        p->group = c.a.heads % 2 == 0 ? 2 : 1;
+        p->group = c.a.heads % 4 == 0 ? 4 : c.a.heads % 2 == 0 ? 2 : 1;
         while (p->group < 8 && rope_il_tpc(c, p->vec_bytes, p->group) == 0) p->group *= 2;
     }
     if (!camp::rope_interleaved_compiled(c.t, p->vec_bytes, p->group)) return CAMP_ERR_NOT_SUPPORTED;

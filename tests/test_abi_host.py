@@ -466,12 +466,17 @@ def test_rope_interleaved_argument_errors(lib, change, kw, status):
 
 
 def test_rope_interleaved_plans(lib):
+    # 32 heads of 128: 4 heads a thread, 8 x 16 = 128 threads a token, 2 tokens a CTA
     p = camp.camp_rope_interleaved_plan(*ILP, 65536, 32, 128, 131072, "bf16")
-    assert (p.kernel, p.vec_bytes, p.group, p.grid) == (camp.KERNEL_ROPE_INTERLEAVED, 16, 2, 65536)
-    p = camp.camp_rope_interleaved_plan(*ILP, 16, 5, 6, 16, "bf16")
+    assert (p.kernel, p.vec_bytes, p.group, p.grid) == (camp.KERNEL_ROPE_INTERLEAVED, 16, 4, 32768)
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 5, 6, 16, "bf16")       # odd head count
     assert (p.vec_bytes, p.group, p.grid) == (4, 1, 1)
-    p = camp.camp_rope_interleaved_plan(*ILP, 16, 64, 128, 16, "bf16")     # 2 heads: 512 threads
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 6, 64, 16, "bf16")      # even, not 4k
+    assert p.group == 2
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 64, 128, 16, "bf16")    # 4 heads: 256 threads
     assert p.group == 4
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 128, 128, 16, "bf16")   # 4 heads: 512 threads
+    assert p.group == 8
 
 
 def test_rope_tables_argument_errors(lib):
@@ -517,18 +522,33 @@ def test_layernorm_empty_and_in_place(lib):
 
 
 @pytest.mark.parametrize("rows,cols,dtype", [
-    (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"), (8192, 2048, "bf16"),
+    (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"),
     (1, 8, "bf16"), (64, 3001, "bf16"), (4096, 12288, "bf16"), (1024, 32768, "bf16"),
-    (5, 65536, "bf16"), (7, 32768, "f32"), (3, 16384, "f32"),
+    (5, 65536, "bf16"), (7, 32768, "f32"), (3, 16384, "f32"), (4096, 1024, "bf16"),
 ])
 def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype):
-    # the same register-resident row mapping as RMSNorm: the same group and accesses a thread
+    # the same register-resident row mapping as RMSNorm: where neither the one-wave test
+    # nor the many-wave rule separates them, the same group and accesses a thread
     p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
     q = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype)
     assert q.kernel == camp.KERNEL_RMSNORM_ROWS
     assert p.kernel == camp.KERNEL_LAYERNORM_ROWS
     assert (p.vec_bytes, p.group, p.per_thread, p.block, p.grid, p.cluster) == \
         (q.vec_bytes, q.group, q.per_thread, q.block, q.grid, 1)
+
+
+@pytest.mark.parametrize("rows,cols,expect", [
+    # at least 2 waves either way: more accesses per thread
+    (65536, 2048, (64, 4, 16384)),
+    (8192, 4096, (128, 4, 4096)),
+    (8192, 2048, (64, 4, 2048)),
+    (32768, 1024, (32, 4, 4096)),
+])
+def test_layernorm_many_waves_prefer_more_work_per_thread(lib, rows, cols, expect):
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, "bf16")
+    assert (p.group, p.per_thread, p.grid) == expect
+    q = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, "bf16")
+    assert q.per_thread <= p.per_thread
 
 
 def test_layernorm_one_wave_test_uses_its_own_occupancy(lib):
