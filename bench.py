@@ -312,7 +312,25 @@ def cpu_baseline(h: dict, seconds: float) -> dict:
     dt = time.perf_counter() - t0
     return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} whole steps of the workload (fp64 oracle, {cores} threads, "
-                      f"{dt:.1f} s)"}
+                      f"{dt:.1f} s)",
+            "rmsnorm_f32_64x2048_1_thread": _oracle_small_case(lib)}
+
+
+def _oracle_small_case(lib) -> dict:
+    """The oracle on RMSNorm fp32 x[64, 2048] (the small configuration) on one thread: the
+    median of 50 calls."""
+    import oracle
+    x, w = inputs.rmsnorm_inputs(64, 2048, "f32", seed=0)
+    xs, ws = inputs.to_numpy(x), inputs.to_numpy(w)
+    eps32 = float(__import__("numpy").float32(EPS))
+    ts = []
+    for _ in range(51):
+        t0 = time.perf_counter()
+        oracle.rmsnorm(xs, ws, eps32, "f32", nthreads=1, lib=lib)
+        ts.append(time.perf_counter() - t0)
+    t = statistics.median(ts[1:])
+    nbytes = ledger.rmsnorm_bytes(64, 2048, "f32")
+    return {"us": t * 1e6, "GB/s": nbytes / t / 1e9, "threads": 1}
 
 
 # ------------------------------------------------------------------ reference arm
@@ -508,6 +526,19 @@ def run_case(case: str, launches: int) -> None:
         plan = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16"))
         for _ in range(launches):
             camp.camp_layernorm(x, w, bt, y, rows, cols, EPS, camp.BF16, stream)
+    elif kind == "rope_il":
+        T, H, D = dims
+        mp = 2 * T
+        x = torch.randn(T, H, D, device="cuda").to(torch.bfloat16)
+        y = torch.empty_like(x)
+        sn = torch.empty(mp, D // 2, device="cuda")
+        cs = torch.empty(mp, D // 2, device="cuda")
+        camp.camp_rope_tables(sn, cs, mp, D, THETA, stream)
+        pos = torch.randint(0, mp, (T,), device="cuda", dtype=torch.int32)
+        p = camp.camp_rope_interleaved_plan(x, sn, cs, pos, y, T, H, D, mp, "bf16")
+        plan = f"rope_interleaved<bf16,vec{p.vec_bytes},hpt{p.group}>"
+        for _ in range(launches):
+            camp.camp_rope_interleaved(x, sn, cs, pos, y, T, H, D, mp, camp.BF16, stream)
     elif kind == "kv":
         S, Dn, Dr = dims
         ns = 2 * S
@@ -564,8 +595,9 @@ def main() -> None:
     ap.add_argument("--case", default=None,
                     help="profiling mode: launch one operator at one shape --launches times "
                          "and exit, e.g. rmsnorm:16384x8192, layernorm:16384x2048, "
-                         "rope:1x16384x32x128, rope_qk:1x16384x32x8x128 (B x S x Hq x Hk x D) "
-                         "or kv:65536x512x64 (S x Dn x Dr)")
+                         "rope:1x16384x32x128, rope_qk:1x16384x32x8x128 (B x S x Hq x Hk x D), "
+                         "kv:65536x512x64 (S x Dn x Dr) or rope_il:16384x32x128 (T x H x D, "
+                         "random positions)")
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.case:

@@ -131,8 +131,12 @@ cudaError_t wide_launch(DType t, int vec_bytes, const RmsnormArgs& a, int64_t gr
 // Flat: one work item per (position, head group, vector), one tensor, any shape.
 constexpr int kRopeBlock = 256;
 
+// CTAs per SM of the tiled RoPE kernel by heads per thread (each head holds two vectors
+// and the thread the E sine and cosine values of its position). Two heads per thread fit
+// 48 registers at 5 CTAs per SM without spilling (6 would spill); at 4096 positions of
+// Q[32 heads] + K[8 heads] x 64 that measured 8.19 us against 8.34 us at 4 CTAs per SM.
 constexpr int rope_min_blocks(int heads_per_thread) {
-    return heads_per_thread <= 1 ? 6 : heads_per_thread <= 2 ? 4 : heads_per_thread <= 4 ? 3 : 2;
+    return heads_per_thread <= 1 ? 6 : heads_per_thread <= 2 ? 5 : heads_per_thread <= 4 ? 3 : 2;
 }
 
 bool rope_compiled(DType t, int vec_bytes, int heads_per_thread);

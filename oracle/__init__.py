@@ -69,6 +69,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_layernorm_f64.restype = c_int
     lib.oracle_layernorm.argtypes = [vp, vp, vp, vp, i64, i64, dbl, c_int, c_int]
     lib.oracle_layernorm.restype = c_int
+    lib.oracle_kv_cat_repeat.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int]
+    lib.oracle_kv_cat_repeat.restype = c_int
     lib.oracle_rope_interleaved.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, c_int]
     lib.oracle_rope_interleaved.restype = c_int
     lib.oracle_rope_tables.argtypes = [vp, vp, i64, i64, dbl]
@@ -236,6 +238,36 @@ def layernorm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float, dt
     _check(lib.oracle_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, cols,
                                 float(eps), code, int(nthreads)), "layernorm")
     return y
+
+
+def kv_cat_repeat(past, new, sin, cos, n_rep: int, dtype: str,
+                  lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Storage-typed past [B, P, Hk, D] (or None when P = 0) and new [B, S, Hk, D] ->
+    out [B, P+S, Hk*n_rep, D]: concatenated along the sequence, each head repeated n_rep
+    times in place, new rows rotated at positions P + s with fp32 tables [P+S, D/2]
+    (sin = cos = None: copied)."""
+    lib = lib or load()
+    code, npt = _storage(dtype)
+    new = np.ascontiguousarray(new)
+    assert new.dtype == npt and new.ndim == 4
+    B, S, Hk, D = new.shape
+    if past is None:
+        past = np.zeros((B, 0, Hk, D), dtype=npt)
+    past = np.ascontiguousarray(past)
+    assert past.dtype == npt and past.shape[0] == B and past.shape[2:] == (Hk, D)
+    P = past.shape[1]
+    out = np.empty((B, P + S, Hk * max(int(n_rep), 0), D), dtype=npt)
+    if sin is not None:
+        sin = np.ascontiguousarray(sin, dtype=np.float32)
+        assert sin.shape == (P + S, D // 2)
+    if cos is not None:
+        cos = np.ascontiguousarray(cos, dtype=np.float32)
+        assert cos.shape == (P + S, D // 2)
+    _check(lib.oracle_kv_cat_repeat(_ptr(past) if P else None, _ptr(new) if S else None,
+                                    None if sin is None else _ptr(sin),
+                                    None if cos is None else _ptr(cos), _ptr(out), B, P, S,
+                                    Hk, D, int(n_rep), code), "kv_cat_repeat")
+    return out
 
 
 def rope_interleaved(x: np.ndarray, sin_t: np.ndarray, cos_t: np.ndarray,

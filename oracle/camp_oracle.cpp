@@ -46,6 +46,13 @@
 //       mean = sum_j x_j / n,  var = sum_j (x_j - mean)^2 / n   (Neumaier sums, fp64)
 //       y_j  = (x_j - mean) / sqrt(var + eps) * gamma_j + beta_j, one rounding.
 //
+//   KV concatenation + GQA head repeat (gollamago README, "not handled" list: attention's
+//   repeat_interleave is left on the PyTorch path; the torch.cat of cached and new keys
+//   along the sequence): out [B, P+S, Hk*n_rep, D] with
+//       out[b, t, h*n_rep + r, :] = past[b, t, h, :]                      t < P
+//       out[b, P+s, h*n_rep + r, :] = rope(new[b, s, h, :], table row P+s)  s < S
+//   (rotate-half, as above; without tables the new rows are copied unrotated).
+//
 //   Interleaved RoPE with position ids  (xserv "phase 4" rope kernel: pairs (x[2i], x[2i+1]),
 //            y0 = x0 cos - x1 sin, y1 = x0 sin + x1 cos, table row positions[token])
 //       tokens whose position is outside [0, max_pos) are left unwritten.
@@ -370,6 +377,53 @@ int oracle_layernorm(const void* x, const void* gamma, const void* beta, void* y
             for (int64_t j = 0; j < cols; ++j) store_elem(y, r * cols + j, yr[j], dtype);
         }
     });
+    return 0;
+}
+
+// Concatenation of past [B, P, Hk, D] and new [B, S, Hk, D] along the sequence, with each
+// head repeated n_rep times in place (head h -> heads h*n_rep .. h*n_rep + n_rep - 1) and
+// the new rows rotated at their absolute positions P + s (tables [P + S, D/2]; sin_t and
+// cos_t both null: no rotation). Storage-typed; a copied value is exact, a rotated one is
+// the fp64 pair formula rounded once.
+int oracle_kv_cat_repeat(const void* past, const void* fresh, const float* sin_t,
+                         const float* cos_t, void* out, int64_t B, int64_t P, int64_t S,
+                         int64_t Hk, int64_t D, int64_t n_rep, int dtype) {
+    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (B < 0 || P < 0 || S < 0 || Hk < 0 || D <= 0 || D % 2 != 0 || n_rep < 1) return 1;
+    if ((sin_t == nullptr) != (cos_t == nullptr)) return 1;
+    const int64_t T = P + S;
+    if (B * T * Hk == 0) return 0;
+    if (!out || (P > 0 && !past) || (S > 0 && !fresh)) return 1;
+    const int64_t half = D / 2;
+    const int64_t Hout = Hk * n_rep;
+    std::vector<double> xr(static_cast<size_t>(D)), yr(static_cast<size_t>(D));
+    std::vector<double> sn(static_cast<size_t>(half)), c(static_cast<size_t>(half));
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t t = 0; t < T; ++t) {
+            const bool old_row = t < P;
+            const bool rotate = !old_row && sin_t != nullptr;
+            if (rotate) {
+                for (int64_t i = 0; i < half; ++i) {
+                    sn[i] = static_cast<double>(sin_t[t * half + i]);
+                    c[i] = static_cast<double>(cos_t[t * half + i]);
+                }
+            }
+            for (int64_t h = 0; h < Hk; ++h) {
+                const void* src = old_row ? past : fresh;
+                const int64_t src_row = old_row ? (b * P + t) * Hk + h : (b * S + (t - P)) * Hk + h;
+                for (int64_t j = 0; j < D; ++j) xr[j] = load_elem(src, src_row * D + j, dtype);
+                if (rotate) {
+                    rope_head(xr.data(), sn.data(), c.data(), yr.data(), half);
+                } else {
+                    yr = xr;
+                }
+                for (int64_t r = 0; r < n_rep; ++r) {
+                    const int64_t dst_row = (b * T + t) * Hout + h * n_rep + r;
+                    for (int64_t j = 0; j < D; ++j) store_elem(out, dst_row * D + j, yr[j], dtype);
+                }
+            }
+        }
+    }
     return 0;
 }
 

@@ -64,6 +64,14 @@ MUTANTS = {
          "const double var = neumaier_sum(d2.data(), n) / static_cast<double>(n - 1);"),
     "layernorm beta added before the weight":
         ("y[j] = xhat * g[j] + b[j];", "y[j] = (xhat + b[j]) * g[j];"),
+    "kv repeat tiles the heads instead of interleaving them":
+        ("const int64_t dst_row = (b * T + t) * Hout + h * n_rep + r;",
+         "const int64_t dst_row = (b * T + t) * Hout + r * Hk + h;"),
+    "kv new rows use the table row of their index among the new rows":
+        ("sn[i] = static_cast<double>(sin_t[t * half + i]);\n                    c[i] = static_cast<double>(cos_t[t * half + i]);",
+         "sn[i] = static_cast<double>(sin_t[(t - P) * half + i]);\n                    c[i] = static_cast<double>(cos_t[(t - P) * half + i]);"),
+    "kv past rows rotated too":
+        ("const bool rotate = !old_row && sin_t != nullptr;", "const bool rotate = sin_t != nullptr;"),
     "add path normalizes the unrounded sum":
         ("hr[j] = load_elem(h, i, dtype);",
          "hr[j] = load_elem(x, i, dtype) + load_elem(r, i, dtype);"),
@@ -96,6 +104,9 @@ def _battery(lib):
         ("rope tables", lambda: pins.test_rope_tables_match_numpy_and_closed_forms(lib)),
         ("layernorm worked", lambda: pins.test_layernorm_worked_case(lib)),
         ("layernorm numpy", lambda: pins.test_layernorm_matches_numpy_mean_and_std(lib)),
+        ("kv cat repeat", lambda: [pins.test_kv_cat_repeat_without_tables_is_numpy_concatenate_and_repeat(
+            lib, "bf16", 2, 5, 3, 3, 8, 4)]),
+        ("kv cat repeat rope", lambda: pins.test_kv_cat_repeat_rotates_new_rows_at_their_absolute_positions(lib)),
         ("add rmsnorm", lambda: [pins.test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, d)
                                  for d in ("bf16", "f32")]),
     ]

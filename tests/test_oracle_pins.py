@@ -313,6 +313,52 @@ def test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, dtype):
         np.testing.assert_array_equal(cr[slot], cr0[slot])
 
 
+# ------------------------------------------------------------------------ KV cat + head repeat
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,P,S,Hk,D,n_rep", [(2, 5, 3, 3, 8, 4), (1, 0, 4, 2, 6, 1),
+                                               (1, 7, 0, 1, 4, 3), (3, 1, 1, 4, 2, 2)])
+def test_kv_cat_repeat_without_tables_is_numpy_concatenate_and_repeat(lib, dtype, B, P, S, Hk,
+                                                                      D, n_rep):
+    rng = np.random.default_rng(71 + P)
+    _, past = _storage_pair(rng, (B, P, Hk, D), dtype)
+    _, new = _storage_pair(rng, (B, S, Hk, D), dtype)
+    out = oracle.kv_cat_repeat(past if P else None, new, None, None, n_rep, dtype, lib=lib)
+    want = np.repeat(np.concatenate([past, new], axis=1), n_rep, axis=2)
+    np.testing.assert_array_equal(out, want)
+
+
+def test_kv_cat_repeat_rotates_new_rows_at_their_absolute_positions(lib):
+    # fp32 storage: the rotated rows are numpy's complex product (x1 + i x2)(c + i s) with the
+    # table row P + s, rounded to fp32; past rows pass through untouched; every repeated
+    # copy of a head is the same
+    rng = np.random.default_rng(72)
+    B, P, S, Hk, D, n_rep = 2, 6, 3, 3, 8, 4
+    past = rng.standard_normal((B, P, Hk, D)).astype(np.float32)
+    new = rng.standard_normal((B, S, Hk, D)).astype(np.float32)
+    ang = rng.uniform(-4, 4, (P + S, D // 2))
+    sin, cos = np.sin(ang).astype(np.float32), np.cos(ang).astype(np.float32)
+    out = oracle.kv_cat_repeat(past, new, sin, cos, n_rep, "f32", lib=lib)
+    o = out.reshape(B, P + S, Hk, n_rep, D)
+    for r in range(1, n_rep):
+        np.testing.assert_array_equal(o[:, :, :, r], o[:, :, :, 0])
+    np.testing.assert_array_equal(o[:, :P, :, 0], past)
+    half = D // 2
+    z = (new[..., :half].astype(np.float64) + 1j * new[..., half:].astype(np.float64)) * \
+        (cos[P:].astype(np.float64) + 1j * sin[P:].astype(np.float64))[None, :, None, :]
+    want = np.concatenate([z.real, z.imag], axis=-1).astype(np.float32)
+    np.testing.assert_allclose(o[:, P:, :, 0], want, rtol=2e-7, atol=1e-30)
+
+
+def test_kv_cat_repeat_argument_errors(lib):
+    new = np.zeros((1, 2, 1, 4), np.float32)
+    t = np.zeros((2, 2), np.float32)
+    with pytest.raises(ValueError):
+        oracle.kv_cat_repeat(None, new, t, None, 2, "f32", lib=lib)     # one table only
+    with pytest.raises(ValueError):
+        oracle.kv_cat_repeat(None, new, None, None, 0, "f32", lib=lib)  # n_rep < 1
+
+
 # ------------------------------------------------------------------------ LayerNorm
 
 def test_layernorm_worked_case(lib):
