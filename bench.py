@@ -378,6 +378,15 @@ def run_reference(args) -> None:
 
 # ------------------------------------------------------------------ large configurations
 
+def _kv_cat_tensors(B, P, S, Hk, D, n_rep):
+    """Device inputs of one KV concat + repeat call: past, new, tables [P+S, D/2], output."""
+    past = torch.randn(B, P, Hk, D, device="cuda").to(torch.bfloat16)
+    new = torch.randn(B, S, Hk, D, device="cuda").to(torch.bfloat16)
+    _, sn, cs = inputs.rope_inputs(1, P + S, 1, D, "bf16", seed=0, device="cuda")
+    out = torch.empty(B, P + S, Hk * n_rep, D, device="cuda", dtype=torch.bfloat16)
+    return past, new, sn, cs, out
+
+
 def large_configs(peak: float, reps: int) -> list[dict]:
     """Single-kernel timings at the large sweep shapes (inputs far larger than L2)."""
     out = []
@@ -398,6 +407,10 @@ def large_configs(peak: float, reps: int) -> list[dict]:
         ("rope_qk bf16 Q[1,65536,32,128] + K[1,65536,8,128]", "rope_qk", (65536, 32, 8, 128)),
         ("kv rmsnorm+rope+cache bf16 kv[1,65536,512+64] -> 131072 slots", "kv", (65536, 512, 64)),
         ("rope interleaved bf16 x[65536,32,128], random positions < 131072", "ril", (65536, 32, 128)),
+        ("kv cat + repeat bf16 K[8,8192,8,128] -> [8,8192,32,128], last 1024 rotated", "cat",
+         (8, 7168, 1024, 8, 128, 4)),
+        ("kv cat + repeat bf16 K[1,65536,8,64] -> [1,65536,32,64], last 4096 rotated", "cat",
+         (1, 61440, 4096, 8, 64, 4)),
     ]
     stream = torch.cuda.current_stream().cuda_stream
     for name, kind, shp in cases:
@@ -461,6 +474,15 @@ def large_configs(peak: float, reps: int) -> list[dict]:
             fn = lambda: camp.camp_kv_rmsnorm_rope_cache(
                 x.data_ptr(), gam.data_ptr(), sn.data_ptr(), cs.data_ptr(), slots.data_ptr(),
                 y.data_ptr(), yr.data_ptr(), 1, S, Dn, Dr, ns, 1e-5, camp.BF16, stream)
+        elif kind == "cat":
+            B, P, S, Hk, D, nr = shp
+            x, nw, sn, cs, y = _kv_cat_tensors(B, P, S, Hk, D, nr)
+            nbytes = ledger.kv_cat_repeat_bytes(B, P, S, Hk, D, nr)
+            plan = camp.camp_kv_cat_repeat_plan(x, nw, sn, cs, y, B, P, S, Hk, D, nr, "bf16")
+            pname = f"kv_cat_repeat<bf16,vec{plan.vec_bytes},hpt{plan.group}>"
+            fn = lambda: camp.camp_kv_cat_repeat(x.data_ptr(), nw.data_ptr(), sn.data_ptr(),
+                                                 cs.data_ptr(), y.data_ptr(), B, P, S, Hk, D, nr,
+                                                 camp.BF16, stream)
         elif kind == "rope_qk":
             S, Hq, Hk, D = shp
             q, sn, cs = inputs.rope_inputs(1, S, Hq, D, "bf16", seed=0, device="cuda")
@@ -554,6 +576,13 @@ def run_case(case: str, launches: int) -> None:
         for _ in range(launches):
             camp.camp_kv_rmsnorm_rope_cache(x, gam, sn, cs, slots, y, yr, 1, S, Dn, Dr, ns, EPS,
                                             camp.BF16, stream)
+    elif kind == "kvcat":
+        B, P, S, Hk, D, nr = dims
+        x, nw, sn, cs, y = _kv_cat_tensors(B, P, S, Hk, D, nr)
+        p = camp.camp_kv_cat_repeat_plan(x, nw, sn, cs, y, B, P, S, Hk, D, nr, "bf16")
+        plan = f"kv_cat_repeat<bf16,vec{p.vec_bytes},hpt{p.group}>"
+        for _ in range(launches):
+            camp.camp_kv_cat_repeat(x, nw, sn, cs, y, B, P, S, Hk, D, nr, camp.BF16, stream)
     elif kind == "rope_qk":
         B, S, Hq, Hk, D = dims
         q, sn, cs = inputs.rope_inputs(B, S, Hq, D, "bf16", seed=0, device="cuda")
@@ -596,8 +625,9 @@ def main() -> None:
                     help="profiling mode: launch one operator at one shape --launches times "
                          "and exit, e.g. rmsnorm:16384x8192, layernorm:16384x2048, "
                          "rope:1x16384x32x128, rope_qk:1x16384x32x8x128 (B x S x Hq x Hk x D), "
-                         "kv:65536x512x64 (S x Dn x Dr) or rope_il:16384x32x128 (T x H x D, "
-                         "random positions)")
+                         "kv:65536x512x64 (S x Dn x Dr), rope_il:16384x32x128 (T x H x D, "
+                         "random positions) or kvcat:1x3584x512x8x64x4 "
+                         "(B x P x S x Hk x D x n_rep)")
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.case:

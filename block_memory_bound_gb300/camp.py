@@ -39,6 +39,7 @@ KERNEL_RMSNORM_CLUSTER = 6
 KERNEL_KV_CACHE = 7
 KERNEL_ROPE_INTERLEAVED = 8
 KERNEL_LAYERNORM_ROWS = 9
+KERNEL_KV_CAT = 10
 
 # Every symbol include/camp.h declares.
 EXPORTS = (
@@ -51,6 +52,7 @@ EXPORTS = (
     "camp_rope_interleaved", "camp_rope_interleaved_plan", "camp_rope_interleaved_with_plan",
     "camp_rope_tables",
     "camp_layernorm", "camp_layernorm_plan", "camp_layernorm_with_plan",
+    "camp_kv_cat_repeat", "camp_kv_cat_repeat_plan", "camp_kv_cat_repeat_with_plan",
 )
 
 
@@ -146,6 +148,13 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_kv_rmsnorm_rope_cache_plan.restype = c_int
         lib.camp_kv_rmsnorm_rope_cache_with_plan.argtypes = kvsig + [f32, c_int, pplan, vp]
         lib.camp_kv_rmsnorm_rope_cache_with_plan.restype = c_int
+        catsig = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int]
+        lib.camp_kv_cat_repeat.argtypes = catsig + [vp]
+        lib.camp_kv_cat_repeat.restype = c_int
+        lib.camp_kv_cat_repeat_plan.argtypes = catsig + [pplan]
+        lib.camp_kv_cat_repeat_plan.restype = c_int
+        lib.camp_kv_cat_repeat_with_plan.argtypes = catsig + [pplan, vp]
+        lib.camp_kv_cat_repeat_with_plan.restype = c_int
         qk = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int]
         lib.camp_rope_qk.argtypes = qk + [vp]
         lib.camp_rope_qk.restype = c_int
@@ -347,6 +356,29 @@ def camp_rope_interleaved_with_plan(x, sin, cos, positions, y, tokens: int, H: i
         int(max_pos), _dtype(dtype), ctypes.byref(plan), _stream(stream)))
 
 
+def camp_kv_cat_repeat(past, fresh, sin, cos, out, B: int, P: int, S: int, Hk: int, D: int,
+                       n_rep: int, dtype, stream=None) -> None:
+    _check("camp_kv_cat_repeat", load().camp_kv_cat_repeat(
+        _ptr(past), _ptr(fresh), _ptr(sin), _ptr(cos), _ptr(out), int(B), int(P), int(S),
+        int(Hk), int(D), int(n_rep), _dtype(dtype), _stream(stream)))
+
+
+def camp_kv_cat_repeat_plan(past, fresh, sin, cos, out, B: int, P: int, S: int, Hk: int, D: int,
+                            n_rep: int, dtype) -> Plan:
+    p = Plan()
+    _check("camp_kv_cat_repeat_plan", load().camp_kv_cat_repeat_plan(
+        _ptr(past), _ptr(fresh), _ptr(sin), _ptr(cos), _ptr(out), int(B), int(P), int(S),
+        int(Hk), int(D), int(n_rep), _dtype(dtype), ctypes.byref(p)))
+    return p
+
+
+def camp_kv_cat_repeat_with_plan(past, fresh, sin, cos, out, B: int, P: int, S: int, Hk: int,
+                                 D: int, n_rep: int, dtype, plan: Plan, stream=None) -> None:
+    _check("camp_kv_cat_repeat_with_plan", load().camp_kv_cat_repeat_with_plan(
+        _ptr(past), _ptr(fresh), _ptr(sin), _ptr(cos), _ptr(out), int(B), int(P), int(S),
+        int(Hk), int(D), int(n_rep), _dtype(dtype), ctypes.byref(plan), _stream(stream)))
+
+
 def camp_rope_tables(sin, cos, max_pos: int, D: int, theta: float, stream=None) -> None:
     _check("camp_rope_tables", load().camp_rope_tables(
         _ptr(sin), _ptr(cos), int(max_pos), int(D), float(theta), _stream(stream)))
@@ -461,4 +493,32 @@ def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
     cols = x.shape[-1] if x.dim() > 0 else 1
     rows = x.numel() // cols if cols else 0
     camp_layernorm(x, gamma, beta, out, rows, cols, eps, x.dtype, stream)
+    return out
+
+
+def kv_cat_repeat(past, fresh, n_rep: int, sin=None, cos=None, out=None, stream=None):
+    """out[B, P+S, Hk*n_rep, D] from past[B, P, Hk, D] (or None) and fresh[B, S, Hk, D]:
+    concatenated along the sequence, each head repeated n_rep times, the new rows rotated at
+    positions P + s when fp32 tables [>= P+S, D/2] are given."""
+    import torch
+    _require(fresh.is_cuda and fresh.is_contiguous() and fresh.dim() == 4,
+             "fresh must be a contiguous CUDA [B, S, Hk, D] tensor")
+    B, S, Hk, D = fresh.shape
+    P = 0
+    if past is not None:
+        _require(past.is_contiguous() and past.dim() == 4 and past.dtype == fresh.dtype
+                 and past.shape[0] == B and tuple(past.shape[2:]) == (Hk, D),
+                 "past must be a contiguous [B, P, Hk, D] tensor of fresh's dtype")
+        P = past.shape[1]
+    _require((sin is None) == (cos is None), "give both tables or neither")
+    for t, name in ((sin, "sin"), (cos, "cos")):
+        if t is not None:
+            _require(t.dtype == torch.float32 and t.is_contiguous() and t.dim() == 2
+                     and t.shape[0] >= P + S and t.shape[1] == D // 2,
+                     f"{name} must be a contiguous fp32 [>= P+S, D/2] tensor")
+    if out is None:
+        out = torch.empty(B, P + S, Hk * n_rep, D, dtype=fresh.dtype, device=fresh.device)
+    _require(tuple(out.shape) == (B, P + S, Hk * n_rep, D) and out.dtype == fresh.dtype
+             and out.is_contiguous(), "out must be a contiguous [B, P+S, Hk*n_rep, D] tensor")
+    camp_kv_cat_repeat(past, fresh, sin, cos, out, B, P, S, Hk, D, n_rep, fresh.dtype, stream)
     return out

@@ -736,6 +736,107 @@ camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_
     return CAMP_SUCCESS;
 }
 
+// ------------------------------------------------------------------ KV concat + head repeat
+
+struct KvCatCall {
+    camp::KvCatArgs a;
+    DType t;
+    int64_t rows;      // B * (P + S)
+};
+
+camp_status_t kv_cat_validate(const void* past, const void* fresh, const float* sin_t,
+                              const float* cos_t, const void* out, int64_t B, int64_t P,
+                              int64_t S, int64_t Hk, int64_t D, int64_t n_rep,
+                              camp_dtype_t dtype, KvCatCall* c, bool* empty) {
+    *empty = false;
+    if (!dtype_ok(dtype)) return CAMP_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || P < 0 || S < 0 || Hk < 0 || D < 2 || D % 2 != 0 || n_rep < 1)
+        return CAMP_ERR_INVALID_ARG;
+    if ((sin_t == nullptr) != (cos_t == nullptr)) return CAMP_ERR_INVALID_ARG;
+    if (Hk > 0x7FFFFFFF || D > 0x7FFFFFFF || n_rep > 0x7FFFFFFF) return CAMP_ERR_INVALID_ARG;
+    const int64_t kMax = std::numeric_limits<int64_t>::max();
+    if (P > kMax - S) return CAMP_ERR_INVALID_ARG;
+    const int64_t T = P + S;
+    if (B == 0 || T == 0 || Hk == 0) { *empty = true; return CAMP_SUCCESS; }
+    if (out == nullptr || (P > 0 && past == nullptr) || (S > 0 && fresh == nullptr))
+        return CAMP_ERR_INVALID_ARG;
+    const DType t = to_dtype(dtype);
+    const int64_t es = camp::elem_bytes(t);
+    int64_t rows = 0, hout = 0, out_bytes = 0, past_bytes = 0, new_bytes = 0, table_bytes = 0;
+    int64_t past_rows = 0, new_rows = 0;
+    if (!mul_ok(B, T, 1, &rows) || !mul_ok(Hk, n_rep, 1, &hout) ||
+        !mul_ok(rows, hout, 1, &out_bytes) || !mul_ok(out_bytes, D, es, &out_bytes) ||
+        !mul_ok(B, P, Hk, &past_rows) || !mul_ok(past_rows, D, es, &past_bytes) ||
+        !mul_ok(B, S, Hk, &new_rows) || !mul_ok(new_rows, D, es, &new_bytes) ||
+        !mul_ok(T, D / 2, 4, &table_bytes))
+        return CAMP_ERR_INVALID_ARG;
+    if (!aligned(out, es) || (P > 0 && !aligned(past, es)) || (S > 0 && !aligned(fresh, es)))
+        return CAMP_ERR_INVALID_ARG;
+    // The output is disjoint from every input (its shape differs, so in place is impossible).
+    if (P > 0 && overlaps(out, out_bytes, past, past_bytes)) return CAMP_ERR_INVALID_ARG;
+    if (S > 0 && overlaps(out, out_bytes, fresh, new_bytes)) return CAMP_ERR_INVALID_ARG;
+    if (sin_t != nullptr) {
+        if (!aligned(sin_t, 4) || !aligned(cos_t, 4)) return CAMP_ERR_INVALID_ARG;
+        if (overlaps(out, out_bytes, sin_t, table_bytes) ||
+            overlaps(out, out_bytes, cos_t, table_bytes))
+            return CAMP_ERR_INVALID_ARG;
+    }
+    c->a = camp::KvCatArgs{P > 0 ? past : nullptr, S > 0 ? fresh : nullptr,
+                           S > 0 ? sin_t : nullptr, S > 0 ? cos_t : nullptr,
+                           const_cast<void*>(out), B, P, S, Hk, D / 2, n_rep};
+    c->t = t;
+    c->rows = rows;
+    return CAMP_SUCCESS;
+}
+
+// Is an access of vb bytes per half legal for every pointer and every half-row start?
+bool kv_cat_vec_ok(const KvCatCall& c, int vb) {
+    const int es = camp::elem_bytes(c.t);
+    if (vb < es || (c.a.half * es) % vb != 0) return false;
+    const int table_align = (vb / es) * 4 < 16 ? (vb / es) * 4 : 16;
+    if (c.a.past != nullptr && !aligned(c.a.past, vb)) return false;
+    if (c.a.fresh != nullptr && !aligned(c.a.fresh, vb)) return false;
+    if (c.a.sin_t != nullptr && (!aligned(c.a.sin_t, table_align) || !aligned(c.a.cos_t, table_align)))
+        return false;
+    return aligned(c.a.out, vb);
+}
+
+// Rows per CTA, or 0 if a row's heads need more than one CTA or the row count exceeds the
+// kernel's 32-bit row arithmetic.
+int64_t kv_cat_tpc(const KvCatCall& c, int vb, int hpt) {
+    if (c.rows > 0xFFFFFFFFll) return 0;
+    const int es = camp::elem_bytes(c.t);
+    const int64_t per_row = ceil_div(c.a.heads, hpt) * (c.a.half * es / vb);
+    return per_row <= camp::kRopeBlock ? camp::kRopeBlock / per_row : 0;
+}
+
+// Widest legal access; 2 heads per thread when the head count is even (each thread then
+// issues 4 loads and 4 * n_rep stores), 1 for odd counts, more when a row's heads would not
+// fit one CTA; CAMP_ERR_NOT_SUPPORTED when even 8 do not.
+camp_status_t kv_cat_plan(const KvCatCall& c, const camp_plan_t* forced, camp_plan_t* p) {
+    if (forced && forced->kernel != CAMP_KERNEL_KV_CAT) return CAMP_ERR_NOT_SUPPORTED;
+    *p = camp_plan_t{};
+    p->kernel = CAMP_KERNEL_KV_CAT;
+    p->cluster = 1;
+    p->block = camp::kRopeBlock;
+    if (forced) {
+        p->vec_bytes = forced->vec_bytes;
+        p->group = forced->group;
+        if (!kv_cat_vec_ok(c, p->vec_bytes)) return CAMP_ERR_NOT_SUPPORTED;
+    } else {
+        for (int vb : {16, 8, 4, 2}) {
+            if (kv_cat_vec_ok(c, vb)) { p->vec_bytes = vb; break; }
+        }
+        p->group = c.a.heads % 2 == 0 ? 2 : 1;
+        while (p->group < 8 && kv_cat_tpc(c, p->vec_bytes, p->group) == 0) p->group *= 2;
+    }
+    if (!camp::kv_cat_compiled(c.t, p->vec_bytes, p->group)) return CAMP_ERR_NOT_SUPPORTED;
+    const int64_t tpc = kv_cat_tpc(c, p->vec_bytes, p->group);
+    if (tpc == 0) return CAMP_ERR_NOT_SUPPORTED;
+    p->grid = ceil_div(c.rows, tpc);
+    return CAMP_SUCCESS;
+}
+
 // ------------------------------------------------------------------ LayerNorm
 
 struct LnCall {
@@ -977,6 +1078,47 @@ CAMP_API camp_status_t camp_rope_interleaved(const void* x, const float* sin, co
                                              camp_dtype_t dtype, void* stream) {
     return camp_rope_interleaved_with_plan(x, sin, cos, positions, y, tokens, H, D, max_pos,
                                            dtype, nullptr, stream);
+}
+
+CAMP_API camp_status_t camp_kv_cat_repeat_plan(const void* past, const void* fresh,
+                                               const float* sin, const float* cos,
+                                               const void* out, int64_t B, int64_t P, int64_t S,
+                                               int64_t Hk, int64_t D, int64_t n_rep,
+                                               camp_dtype_t dtype, camp_plan_t* plan) {
+    if (plan == nullptr) return CAMP_ERR_INVALID_ARG;
+    KvCatCall c;
+    bool empty = false;
+    camp_status_t st = kv_cat_validate(past, fresh, sin, cos, out, B, P, S, Hk, D, n_rep, dtype,
+                                       &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (empty) { *plan = camp_plan_t{}; return CAMP_SUCCESS; }
+    return kv_cat_plan(c, nullptr, plan);
+}
+
+CAMP_API camp_status_t camp_kv_cat_repeat_with_plan(const void* past, const void* fresh,
+                                                    const float* sin, const float* cos,
+                                                    void* out, int64_t B, int64_t P, int64_t S,
+                                                    int64_t Hk, int64_t D, int64_t n_rep,
+                                                    camp_dtype_t dtype, const camp_plan_t* plan,
+                                                    void* stream) {
+    KvCatCall c;
+    bool empty = false;
+    camp_status_t st = kv_cat_validate(past, fresh, sin, cos, out, B, P, S, Hk, D, n_rep, dtype,
+                                       &c, &empty);
+    if (st != CAMP_SUCCESS || empty) return st;
+    camp_plan_t p;
+    st = kv_cat_plan(c, plan, &p);
+    if (st != CAMP_SUCCESS) return st;
+    return runtime_status(camp::kv_cat_launch(c.t, p.vec_bytes, p.group, c.a, p.grid,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+CAMP_API camp_status_t camp_kv_cat_repeat(const void* past, const void* fresh, const float* sin,
+                                          const float* cos, void* out, int64_t B, int64_t P,
+                                          int64_t S, int64_t Hk, int64_t D, int64_t n_rep,
+                                          camp_dtype_t dtype, void* stream) {
+    return camp_kv_cat_repeat_with_plan(past, fresh, sin, cos, out, B, P, S, Hk, D, n_rep, dtype,
+                                        nullptr, stream);
 }
 
 CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos, int64_t D,

@@ -226,4 +226,35 @@ bool kv_cache_compiled(DType t, int vec_bytes, int nvn, int rope_bytes);
 cudaError_t kv_cache_launch(DType t, int vec_bytes, int nvn, int rope_bytes,
                             const KvCacheArgs& a, cudaStream_t s);
 
+// ------------------------------------------------------------------ KV concat + head repeat
+// out[b, t, h*n_rep + r, :] from past[b, t, h, :] (t < P) or from fresh[b, t - P, h, :],
+// rotated at table row t when sin_t is not null. Tiled like rope_tiled over the B*(P+S)
+// rows: kRopeBlock threads, rows per CTA = 256 / (ceil(heads / hpt) * (half / elems)).
+// Needs B*(P+S) < 2^32.
+struct KvCatArgs {
+    const void* past;      // [batch, past_len, heads, 2*half]; null when past_len == 0
+    const void* fresh;     // [batch, new_len, heads, 2*half]; null when new_len == 0
+    const float* sin_t;    // [past_len + new_len, half] or null (copy the new rows)
+    const float* cos_t;
+    void* out;             // [batch, past_len + new_len, heads * n_rep, 2*half]
+    int64_t batch;
+    int64_t past_len;
+    int64_t new_len;
+    int64_t heads;
+    int64_t half;
+    int64_t n_rep;
+};
+
+// CTAs per SM by heads per thread: camp_rope's budget, except that one head per thread also
+// runs 5 CTAs (48 registers): at 6 the 16-byte bf16 variant (8 sine and 8 cosine values
+// beside its data) spilled (checked with -Xptxas -v).
+constexpr int kv_cat_min_blocks(int heads_per_thread) {
+    return heads_per_thread <= 2 ? 5 : heads_per_thread <= 4 ? 3 : 2;
+}
+
+// vec_bytes 16, 8, 4, 2 (bf16) / 16, 8, 4 (fp32): bytes per access of each half.
+bool kv_cat_compiled(DType t, int vec_bytes, int heads_per_thread);
+cudaError_t kv_cat_launch(DType t, int vec_bytes, int heads_per_thread, const KvCatArgs& a,
+                          int64_t grid, cudaStream_t s);
+
 }  // namespace camp

@@ -65,6 +65,15 @@ def kv_cache_bytes(B: int, S: int, Dn: int, Dr: int, dtype: str = "bf16") -> int
     return 2 * B * S * (Dn + Dr) * es + Dn * es + 2 * S * (Dr // 2) * 4 + 8 * B * S
 
 
+def kv_cat_repeat_bytes(B: int, P: int, S: int, Hk: int, D: int, n_rep: int,
+                        dtype: str = "bf16", tables: bool = True) -> int:
+    """KV concatenation + head repeat: past and new rows read once, every one of the n_rep
+    copies of each row written once, the table rows of the new positions read once."""
+    es = ELEM_BYTES[dtype]
+    return (B * (P + S) * Hk * D * es * (1 + n_rep)
+            + (2 * S * (D // 2) * 4 if tables and S > 0 else 0))
+
+
 def rope_flops(B: int, S: int, H: int, D: int) -> int:
     # per pair: 4 multiplies + 2 add/sub = 6 FLOP, i.e. 3 FLOP per element
     return 3 * B * S * H * D

@@ -219,6 +219,38 @@ CAMP_API camp_status_t camp_rope_interleaved(const void* x, const float* sin, co
                                              camp_dtype_t dtype, void* stream);
 
 /*
+ * Concatenation of cached and new keys (or values) along the sequence, with the head repeat
+ * of grouped-query attention, in one pass. The gollamago README (RoPE and RMSNorm notes, the
+ * list of what is not handled) leaves attention's repeat_interleave on the PyTorch path:
+ * there the cached keys and the new ones are joined with torch.cat and each of the Hk key
+ * heads is then repeated n_rep = Hq / Hk times for the Hq query heads, two passes that read
+ * and write the whole cache. Here each source element is read once and its n_rep copies are
+ * written once, and the new rows can be rotated (rotate-half RoPE) on the way:
+ *
+ *   out[b, t,     h*n_rep + r, :] = past[b, t, h, :]                           t < P
+ *   out[b, P + s, h*n_rep + r, :] = rope(fresh[b, s, h, :], table row P + s)     s < S
+ *
+ * for every r < n_rep (torch.repeat_interleave order: copies of one head are adjacent).
+ *
+ *   past     [B, P, Hk, D]   cached rows, storage type `dtype`; may be NULL when P == 0.
+ *   fresh    [B, S, Hk, D]   new rows, storage type `dtype`; may be NULL when S == 0.
+ *   sin, cos [P + S, D/2]    fp32 tables indexed by absolute position (only rows P .. P+S-1
+ *                            are read), or both NULL: the new rows are copied unrotated.
+ *                            A longer table (say [max_pos, D/2]) may be passed.
+ *   out      [B, P + S, Hk * n_rep, D]  output, disjoint from every input.
+ *   B, P, S, Hk >= 0 (B*(P+S)*Hk == 0 is a no-op); D even, >= 2; n_rep >= 1.
+ *
+ * Copied values are bit-exact; rotated values are camp_rope's arithmetic (compensated fp32
+ * products, one rounding). CAMP_ERR_NOT_SUPPORTED when B*(P+S) >= 2^32 or a row's heads need
+ * more than one CTA even at 8 heads per thread (Hk * D too large). Errors otherwise as for
+ * camp_rope, plus CAMP_ERR_INVALID_ARG when only one of sin and cos is NULL.
+ */
+CAMP_API camp_status_t camp_kv_cat_repeat(const void* past, const void* fresh, const float* sin,
+                                          const float* cos, void* out, int64_t B, int64_t P,
+                                          int64_t S, int64_t Hk, int64_t D, int64_t n_rep,
+                                          camp_dtype_t dtype, void* stream);
+
+/*
  * RoPE tables on the device: sin[p, i] and cos[p, i] for p < max_pos, i < D/2, with
  * angle = p * theta^(-2i/D) (the table of the xserv compute_rope_cache kernel; theta is
  * 10000 in the original Llama and 500000 in Llama 3). Computed in fp64 with CUDA's
@@ -275,14 +307,15 @@ typedef enum {
     CAMP_KERNEL_RMSNORM_CLUSTER = 6, /* a cluster of CTAs per row, sums combined over DSMEM */
     CAMP_KERNEL_KV_CACHE = 7,       /* camp_kv_rmsnorm_rope_cache: one warp per token */
     CAMP_KERNEL_ROPE_INTERLEAVED = 8, /* camp_rope_interleaved: tiled like CAMP_KERNEL_ROPE */
-    CAMP_KERNEL_LAYERNORM_ROWS = 9  /* camp_layernorm: a group of threads per row, registers */
+    CAMP_KERNEL_LAYERNORM_ROWS = 9, /* camp_layernorm: a group of threads per row, registers */
+    CAMP_KERNEL_KV_CAT = 10         /* camp_kv_cat_repeat: tiled like CAMP_KERNEL_ROPE */
 } camp_kernel_t;
 
 typedef struct {
     int32_t kernel;        /* camp_kernel_t */
     int32_t vec_bytes;     /* bytes per vector access of x and y: 16, 8, 4 or 2 */
-    int32_t group;         /* RMSNorm: threads per row. RoPE: heads per thread. KV cache:
-                              rope access bytes per half and lane */
+    int32_t group;         /* RMSNorm: threads per row. RoPE, KV concat: heads per thread.
+                              KV cache: rope access bytes per half and lane */
     int32_t per_thread;    /* RMSNorm: vector accesses per thread per row. RoPE: unused (0) */
     int32_t block;         /* threads per CTA */
     int32_t cluster;       /* CTAs per cluster (RMSNorm cluster kernel: 2..16), else 1 */
@@ -375,6 +408,22 @@ CAMP_API camp_status_t camp_rope_interleaved_with_plan(const void* x, const floa
                                                        int64_t tokens, int64_t H, int64_t D,
                                                        int64_t max_pos, camp_dtype_t dtype,
                                                        const camp_plan_t* plan, void* stream);
+
+/* Like camp_rope_plan, for camp_kv_cat_repeat (vec_bytes = access bytes per half;
+ * group = heads per thread). */
+CAMP_API camp_status_t camp_kv_cat_repeat_plan(const void* past, const void* fresh,
+                                               const float* sin, const float* cos,
+                                               const void* out, int64_t B, int64_t P, int64_t S,
+                                               int64_t Hk, int64_t D, int64_t n_rep,
+                                               camp_dtype_t dtype, camp_plan_t* plan);
+
+/* camp_kv_cat_repeat with an explicit plan (vec_bytes, group); NULL plan = the default. */
+CAMP_API camp_status_t camp_kv_cat_repeat_with_plan(const void* past, const void* fresh,
+                                                    const float* sin, const float* cos,
+                                                    void* out, int64_t B, int64_t P, int64_t S,
+                                                    int64_t Hk, int64_t D, int64_t n_rep,
+                                                    camp_dtype_t dtype, const camp_plan_t* plan,
+                                                    void* stream);
 
 /* Like camp_rmsnorm_plan, for camp_layernorm (kernel CAMP_KERNEL_LAYERNORM_ROWS). */
 CAMP_API camp_status_t camp_layernorm_plan(const void* x, const void* gamma, const void* beta,

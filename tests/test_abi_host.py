@@ -597,3 +597,85 @@ def test_single_kernel_ops_refuse_a_plan_for_another_kernel(lib):
     p = camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, group=1)
     assert lib.camp_rope_interleaved_with_plan(X, SIN, COS, R_, Y, 4, 8, 64, 16, camp.BF16,
                                                ctypes.byref(p), None) == camp.ERR_NOT_SUPPORTED
+
+
+# ------------------------------------------------------------------ KV concat + head repeat
+
+CAT = [0x7C0000000000 + i * 0x1000000000 for i in range(5)]   # past, fresh, sin, cos, out
+
+
+def _cat(lib, p, B=2, P=5, S=3, Hk=8, D=64, n_rep=4, dtype=camp.BF16):
+    return lib.camp_kv_cat_repeat(*p, B, P, S, Hk, D, n_rep, dtype, None)
+
+
+@pytest.mark.parametrize("change,kw,status", [
+    ({}, {"dtype": 0}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({}, {"D": 7}, camp.ERR_INVALID_ARG),
+    ({}, {"D": 0}, camp.ERR_INVALID_ARG),
+    ({}, {"n_rep": 0}, camp.ERR_INVALID_ARG),
+    ({}, {"P": -1}, camp.ERR_INVALID_ARG),
+    ({}, {"Hk": -1}, camp.ERR_INVALID_ARG),
+    ({0: None}, {}, camp.ERR_INVALID_ARG),                   # past needed when P > 0
+    ({1: None}, {}, camp.ERR_INVALID_ARG),                   # fresh needed when S > 0
+    ({4: None}, {}, camp.ERR_INVALID_ARG),
+    ({2: None}, {}, camp.ERR_INVALID_ARG),                   # one table without the other
+    ({3: None}, {}, camp.ERR_INVALID_ARG),
+    ({2: CAT[2] + 2}, {}, camp.ERR_INVALID_ARG),             # table not fp32-aligned
+    ({4: CAT[4] + 1}, {}, camp.ERR_INVALID_ARG),             # out not element-aligned
+    ({4: CAT[0] + 64}, {}, camp.ERR_INVALID_ARG),            # out over past
+    ({4: CAT[1]}, {}, camp.ERR_INVALID_ARG),                 # out over fresh (no in place)
+    ({2: CAT[4] + 128}, {}, camp.ERR_INVALID_ARG),           # a table inside out
+    ({}, {"Hk": 256, "D": 1024}, camp.ERR_NOT_SUPPORTED),    # a row needs more than one CTA
+    ({}, {"B": 1 << 20, "P": 1 << 12, "Hk": 1, "D": 2}, camp.ERR_NOT_SUPPORTED),  # B*(P+S) >= 2^32
+])
+def test_kv_cat_argument_errors(lib, change, kw, status):
+    p = list(CAT)
+    for i, v in change.items():
+        p[i] = v
+    assert _cat(lib, p, **kw) == status
+
+
+def test_kv_cat_empty_and_optional_pointers(lib):
+    nil = [None] * 5
+    for kw in ({"B": 0}, {"P": 0, "S": 0}, {"Hk": 0}):
+        assert _cat(lib, nil, **kw) == camp.SUCCESS
+    # P == 0: past may be NULL; S == 0: fresh and the tables may be NULL (planned only).
+    p = camp.camp_kv_cat_repeat_plan(None, CAT[1], CAT[2], CAT[3], CAT[4], 1, 0, 16, 8, 64, 4,
+                                     "bf16")
+    assert p.kernel == camp.KERNEL_KV_CAT
+    p = camp.camp_kv_cat_repeat_plan(CAT[0], None, None, None, CAT[4], 1, 16, 0, 8, 64, 4, "bf16")
+    assert p.kernel == camp.KERNEL_KV_CAT
+    # both tables NULL: copy the new rows
+    p = camp.camp_kv_cat_repeat_plan(CAT[0], CAT[1], None, None, CAT[4], 1, 16, 4, 8, 64, 4, "f32")
+    assert p.kernel == camp.KERNEL_KV_CAT
+
+
+def test_kv_cat_plans(lib):
+    # Llama-3.2-1B keys: 8 heads of 64, 4 query heads a key head. bf16: 4 vectors a half,
+    # 2 heads a thread: 16 threads a row, 16 rows a CTA.
+    p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 4095, 1, 8, 64, 4, "bf16")
+    assert (p.kernel, p.vec_bytes, p.group, p.block, p.grid) == (camp.KERNEL_KV_CAT, 16, 2, 256, 256)
+    p = camp.camp_kv_cat_repeat_plan(*CAT, 2, 0, 4096, 8, 128, 4, "f32")
+    assert (p.vec_bytes, p.group, p.grid) == (16, 2, 2 * 4096 // 4)   # 64 threads a row
+    p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 3, 4, 5, 6, 2, "bf16")     # odd heads, D/2 = 3
+    assert (p.vec_bytes, p.group, p.grid) == (2, 1, 1)
+    p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 3, 4, 64, 256, 2, "bf16")  # 64 heads of 256
+    assert (p.vec_bytes, p.group) == (16, 4)                             # 16 x 16 threads
+    p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 3, 4, 128, 256, 2, "bf16")
+    assert (p.vec_bytes, p.group) == (16, 8)
+    # a misaligned input narrows the accesses of every tensor
+    q = list(CAT)
+    q[1] += 4
+    p = camp.camp_kv_cat_repeat_plan(*q, 1, 3, 4, 8, 64, 4, "bf16")
+    assert p.vec_bytes == 4
+
+
+def test_kv_cat_with_plan_checks_the_forced_plan(lib):
+    bad = [camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=16, group=2),
+           camp.Plan(kernel=camp.KERNEL_KV_CAT, vec_bytes=16, group=3),
+           camp.Plan(kernel=camp.KERNEL_KV_CAT, vec_bytes=2, group=1),    # fp32 has no 2-byte
+           camp.Plan(kernel=camp.KERNEL_KV_CAT, vec_bytes=16, group=1)]   # 3 floats a half
+    for plan in bad:
+        st = lib.camp_kv_cat_repeat_with_plan(*CAT, 1, 4, 4, 3, 6, 2, camp.F32,
+                                              ctypes.byref(plan), None)
+        assert st == camp.ERR_NOT_SUPPORTED, plan

@@ -59,3 +59,12 @@ def test_benchmark_step_bytes():
     assert ledger.rope_qk_bytes(1, 4096, 32, 8, 64) == 42_991_616
     assert ledger.rmsnorm_bytes(16384, 8192) == 536_887_296
     assert ledger.rmsnorm_bytes(64, 2048, "f32") == 1_056_768
+
+
+def test_kv_cat_repeat_bytes():
+    # Llama-3.2-1B keys, 4096 positions (3584 cached + 512 new), 8 heads of 64 repeated 4
+    # times: 4096*8*64*2 bytes read, four times that written, 512 table rows of 32 sin + cos.
+    rows = 4096 * 8 * 64 * 2
+    assert ledger.kv_cat_repeat_bytes(1, 3584, 512, 8, 64, 4) == 5 * rows + 2 * 512 * 32 * 4
+    assert ledger.kv_cat_repeat_bytes(1, 3584, 512, 8, 64, 4, tables=False) == 5 * rows
+    assert ledger.kv_cat_repeat_bytes(2, 5, 0, 2, 8, 3, "f32") == 2 * 5 * 2 * 8 * 4 * 4
