@@ -376,6 +376,97 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ end to end
+
+def _e2e_serial(sets, host_in, host_out, steps: int, stream) -> float:
+    """Every step on one stream: copy in, the two kernels, copy out. Returns seconds."""
+    R = len(sets)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for i in range(steps):
+            s = sets[i % R]
+            for d, h in zip(s.inputs_(), host_in):
+                d.copy_(h, non_blocking=True)
+            launch_step(s, stream.cuda_stream)
+            for h, d in zip(host_out[i % 2], s.outputs_()):
+                h.copy_(d, non_blocking=True)
+        e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3
+
+
+def _e2e_pipelined(sets, host_in, host_out, steps: int) -> float:
+    """Double-buffered over two device input sets and three streams: the host-to-device
+    copy of step i + 1, the kernels of step i and the device-to-host copy of step i - 1 run
+    at the same time. Events keep each set's inputs from being overwritten before the
+    kernels of its previous step have read them, and its outputs before they have been
+    copied out. Returns seconds from the first copy in to the last copy out."""
+    h2d, comp, d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev(), ev()]
+    comp_done = [ev(), ev()]
+    out_done = [ev(), ev()]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(h2d)
+    comp.wait_event(e0)
+    d2h.wait_event(e0)
+    for i in range(steps):
+        k = i % 2
+        s = sets[k]
+        if i >= 2:
+            h2d.wait_event(comp_done[k])     # step i - 2 has read this set's inputs
+        with torch.cuda.stream(h2d):
+            for d, h in zip(s.inputs_(), host_in):
+                d.copy_(h, non_blocking=True)
+        in_ready[k].record(h2d)
+        comp.wait_event(in_ready[k])
+        if i >= 2:
+            comp.wait_event(out_done[k])     # step i - 2's outputs have been copied out
+        launch_step(s, comp.cuda_stream)
+        comp_done[k].record(comp)
+        d2h.wait_event(comp_done[k])
+        with torch.cuda.stream(d2h):
+            for h, d in zip(host_out[k], s.outputs_()):
+                h.copy_(d, non_blocking=True)
+        out_done[k].record(d2h)
+    e1.record(d2h)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3
+
+
+def end_to_end(sets, steps: int, world: int, dist) -> dict:
+    """The step metric through the C ABI with host buffers: each step copies its inputs
+    from pinned host memory, runs both kernels and copies its outputs back to pinned host
+    memory, all inside the timed region. Reported pipelined (the value) and serial."""
+    host_in = [t.cpu().pin_memory() for t in sets[0].inputs_()]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in sets[0].outputs_()]
+                for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    stream = torch.cuda.Stream()
+    _e2e_serial(sets, host_in, host_out, 3, stream)          # warm-up
+    _e2e_pipelined(sets, host_in, host_out, 3)
+    if dist is not None:
+        dist.barrier()
+    t_pipe = _e2e_pipelined(sets, host_in, host_out, steps)
+    t_serial = _e2e_serial(sets, host_in, host_out, steps, stream)
+    if dist is not None:
+        t = torch.tensor([t_pipe, t_serial], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_pipe, t_serial = (float(v) for v in t.tolist())
+    return {"value": STEP_BYTES * steps * world / t_pipe / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": t_pipe / steps * 1e3,
+            "schedule": "double-buffered: copy in of step i+1, kernels of step i and copy out "
+                        "of step i-1 on three streams, ordered by events",
+            "serial": {"value": STEP_BYTES * steps * world / t_serial / 1e9,
+                       "ms_per_step": t_serial / steps * 1e3,
+                       "schedule": "one stream: copy in, kernels, copy out"},
+            "copy_GB/s": (h2d + d2h) * steps / t_pipe / 1e9}
+
+
 # ------------------------------------------------------------------ large configurations
 
 def _kv_cat_tensors(B, P, S, Hk, D, n_rep):
@@ -744,39 +835,7 @@ def main() -> None:
                 if peak_kind == "measured" else "fallback 6800 GB/s"}
 
     # End to end through the C ABI with host buffers (pinned), copies inside the timing.
-    host_in = [t.cpu().pin_memory() for t in sets[0].inputs_()]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in sets[0].outputs_()]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
-    for i in range(3):
-        s = sets[i % R]
-        for d, hsrc in zip(s.inputs_(), host_in):
-            d.copy_(hsrc, non_blocking=True)
-        launch_step(s, stream)
-        for hdst, d in zip(host_out, s.outputs_()):
-            hdst.copy_(d, non_blocking=True)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.e2e_steps):
-        s = sets[i % R]
-        for d, hsrc in zip(s.inputs_(), host_in):
-            d.copy_(hsrc, non_blocking=True)
-        launch_step(s, stream)
-        for hdst, d in zip(host_out, s.outputs_()):
-            hdst.copy_(d, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_t = e0.elapsed_time(e1) * 1e-3
-    if dist is not None:
-        t = torch.tensor([e2e_t], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_t = float(t.item())
-    e2e = {"value": STEP_BYTES * args.e2e_steps * world / e2e_t / 1e9, "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-           "ms_per_step": e2e_t / args.e2e_steps * 1e3}
+    e2e = end_to_end(sets, args.e2e_steps, world, dist)
 
     calibration = copy_calibration(sets, M, 50, peak)
 
