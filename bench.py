@@ -478,139 +478,164 @@ def _kv_cat_tensors(B, P, S, Hk, D, n_rep):
     return past, new, sn, cs, out
 
 
+LARGE_CASES = [
+    ("rmsnorm bf16 [16384,8192] stress, eps 1e-6", "rms", (16384, 8192, True, 1e-6)),
+    ("rmsnorm bf16 [65536,8192]", "rms", (65536, 8192, False, 1e-5)),
+    ("rmsnorm bf16 [65536,3000]", "rms", (65536, 3000, False, 1e-5)),
+    ("rmsnorm bf16 [65536,2048]", "rms", (65536, 2048, False, 1e-5)),
+    ("add_rmsnorm bf16 [16384,8192]", "add", (16384, 8192)),
+    ("add_rmsnorm bf16 [65536,2048]", "add", (65536, 2048)),
+    ("rmsnorm bf16 [256,131072] (cluster per row)", "rms", (256, 131072, False, 1e-5)),
+    ("layernorm bf16 [8192,4096]", "ln", (8192, 4096)),
+    ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),
+    ("layernorm bf16 [16384,8192]", "ln", (16384, 8192)),
+    ("rope bf16 [1,65536,32,128]", "rope", (65536, 32, 128)),
+    ("rope bf16 [1,65536,32,64]", "rope", (65536, 32, 64)),
+    ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),
+    ("rope_qk bf16 Q[1,65536,32,128] + K[1,65536,8,128]", "rope_qk", (65536, 32, 8, 128)),
+    ("kv rmsnorm+rope+cache bf16 kv[1,65536,512+64] -> 131072 slots", "kv", (65536, 512, 64)),
+    ("rope interleaved bf16 x[65536,32,128], random positions < 131072", "ril", (65536, 32, 128)),
+    ("kv cat + repeat bf16 K[8,8192,8,128] -> [8,8192,32,128], last 1024 rotated", "cat",
+     (8, 7168, 1024, 8, 128, 4)),
+    ("kv cat + repeat bf16 K[1,65536,8,64] -> [1,65536,32,64], last 4096 rotated", "cat",
+     (1, 61440, 4096, 8, 64, 4)),
+]
+
+
+def _large_case(kind: str, shp: tuple, seed: int):
+    """One input set of a large configuration: (launch(stream), bytes, kernel name, tensors).
+    The launch closure keeps its own tensors alive; `tensors` is returned so that the
+    caller can hold them across graph capture and replay as well."""
+    if kind == "rms":
+        rows, cols, stress, eps = shp
+        x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=seed, stress=stress, device="cuda")
+        y = torch.empty_like(x)
+        pname = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, "bf16"))
+        fn = lambda st: camp.camp_rmsnorm(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, cols,
+                                          eps, camp.BF16, st)
+        return fn, ledger.rmsnorm_bytes(rows, cols), pname, (x, w, y)
+    if kind == "add":
+        rows, cols = shp
+        x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=seed, device="cuda")
+        r, _ = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=seed + 100, device="cuda")
+        h, y = torch.empty_like(x), torch.empty_like(x)
+        pname = "add_" + plan_name("rmsnorm", camp.camp_add_rmsnorm_plan(x, r, w, h, y, rows,
+                                                                         cols, "bf16"))
+        fn = lambda st: camp.camp_add_rmsnorm(x.data_ptr(), r.data_ptr(), w.data_ptr(),
+                                              h.data_ptr(), y.data_ptr(), rows, cols, 1e-5,
+                                              camp.BF16, st)
+        return fn, ledger.add_rmsnorm_bytes(rows, cols), pname, (x, w, r, h, y)
+    if kind == "ln":
+        rows, cols = shp
+        x, w, bt = inputs.layernorm_inputs(rows, cols, "bf16", seed=seed, device="cuda")
+        y = torch.empty_like(x)
+        pname = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16"))
+        fn = lambda st: camp.camp_layernorm(x.data_ptr(), w.data_ptr(), bt.data_ptr(),
+                                            y.data_ptr(), rows, cols, 1e-5, camp.BF16, st)
+        return fn, ledger.layernorm_bytes(rows, cols), pname, (x, w, bt, y)
+    if kind == "ril":
+        T, H, D = shp
+        mp = 2 * T
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed)
+        x = torch.randn(T, H, D, device="cuda", generator=g).to(torch.bfloat16)
+        y = torch.empty_like(x)
+        sn = torch.empty(mp, D // 2, device="cuda")
+        cs = torch.empty(mp, D // 2, device="cuda")
+        camp.camp_rope_tables(sn, cs, mp, D, THETA)
+        pos = torch.randint(0, mp, (T,), device="cuda", dtype=torch.int32, generator=g)
+        plan = camp.camp_rope_interleaved_plan(x, sn, cs, pos, y, T, H, D, mp, "bf16")
+        pname = f"rope_interleaved<bf16,vec{plan.vec_bytes},hpt{plan.group}>"
+        fn = lambda st: camp.camp_rope_interleaved(x.data_ptr(), sn.data_ptr(), cs.data_ptr(),
+                                                   pos.data_ptr(), y.data_ptr(), T, H, D, mp,
+                                                   camp.BF16, st)
+        nbytes = 2 * T * H * D * 2 + 2 * T * (D // 2) * 4 + 4 * T
+        return fn, nbytes, pname, (x, y, sn, cs, pos)
+    if kind == "kv":
+        S, Dn, Dr = shp
+        ns = 2 * S
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed)
+        x = torch.randn(1, S, Dn + Dr, device="cuda", generator=g).to(torch.bfloat16)
+        gam = torch.ones(Dn, device="cuda", dtype=torch.bfloat16)
+        _, sn, cs = inputs.rope_inputs(1, S, 1, Dr, "bf16", seed=seed, device="cuda")
+        slots = torch.randperm(ns, device="cuda", generator=g)[:S].to(torch.int64)
+        y = torch.empty(ns, Dn, device="cuda", dtype=torch.bfloat16)
+        yr = torch.empty(ns, Dr, device="cuda", dtype=torch.bfloat16)
+        plan = camp.camp_kv_rmsnorm_rope_cache_plan(x, gam, sn, cs, slots, y, yr, 1, S, Dn, Dr,
+                                                    ns, "bf16")
+        pname = f"kv_cache<bf16,vec{plan.vec_bytes},nv{plan.per_thread}>"
+        fn = lambda st: camp.camp_kv_rmsnorm_rope_cache(
+            x.data_ptr(), gam.data_ptr(), sn.data_ptr(), cs.data_ptr(), slots.data_ptr(),
+            y.data_ptr(), yr.data_ptr(), 1, S, Dn, Dr, ns, 1e-5, camp.BF16, st)
+        return fn, ledger.kv_cache_bytes(1, S, Dn, Dr), pname, (x, gam, sn, cs, slots, y, yr)
+    if kind == "cat":
+        B, P, S, Hk, D, nr = shp
+        x, nw, sn, cs, y = _kv_cat_tensors(B, P, S, Hk, D, nr)
+        plan = camp.camp_kv_cat_repeat_plan(x, nw, sn, cs, y, B, P, S, Hk, D, nr, "bf16")
+        pname = f"kv_cat_repeat<bf16,vec{plan.vec_bytes},hpt{plan.group}>"
+        fn = lambda st: camp.camp_kv_cat_repeat(x.data_ptr(), nw.data_ptr(), sn.data_ptr(),
+                                                cs.data_ptr(), y.data_ptr(), B, P, S, Hk, D, nr,
+                                                camp.BF16, st)
+        return fn, ledger.kv_cat_repeat_bytes(B, P, S, Hk, D, nr), pname, (x, nw, sn, cs, y)
+    if kind == "rope_qk":
+        S, Hq, Hk, D = shp
+        q, sn, cs = inputs.rope_inputs(1, S, Hq, D, "bf16", seed=seed, device="cuda")
+        k, _, _ = inputs.rope_inputs(1, S, Hk, D, "bf16", seed=seed + 100, device="cuda")
+        yq, yk = torch.empty_like(q), torch.empty_like(k)
+        pname = plan_name("rope", camp.camp_rope_qk_plan(q, k, sn, cs, yq, yk, 1, S, Hq, Hk, D,
+                                                         "bf16"))
+        fn = lambda st: camp.camp_rope_qk(q.data_ptr(), k.data_ptr(), sn.data_ptr(),
+                                          cs.data_ptr(), yq.data_ptr(), yk.data_ptr(), 1, S, Hq,
+                                          Hk, D, camp.BF16, st)
+        return fn, ledger.rope_qk_bytes(1, S, Hq, Hk, D), pname, (q, k, sn, cs, yq, yk)
+    S, H, D = shp
+    x, sn, cs = inputs.rope_inputs(1, S, H, D, "bf16", seed=seed, device="cuda")
+    y = torch.empty_like(x)
+    pname = plan_name("rope", camp.camp_rope_plan(x, sn, cs, y, 1, S, H, D, "bf16"))
+    fn = lambda st: camp.camp_rope(x.data_ptr(), sn.data_ptr(), cs.data_ptr(), y.data_ptr(), 1,
+                                   S, H, D, camp.BF16, st)
+    return fn, ledger.rope_bytes(1, S, H, D), pname, (x, sn, cs, y)
+
+
 def large_configs(peak: float, reps: int) -> list[dict]:
-    """Single-kernel timings at the large sweep shapes (inputs far larger than L2)."""
+    """Single-operator timings at the large sweep shapes, timed like the step: a CUDA graph
+    of N back-to-back launches rotating over R input sets (R x bytes > 4 x L2, so every
+    launch reads from HBM), one event pair per graph replay; the median over `reps`
+    replays of the replay time / N."""
     out = []
-    cases = [
-        ("rmsnorm bf16 [16384,8192] stress, eps 1e-6", "rms", (16384, 8192, True, 1e-6)),
-        ("rmsnorm bf16 [65536,8192]", "rms", (65536, 8192, False, 1e-5)),
-        ("rmsnorm bf16 [65536,3000]", "rms", (65536, 3000, False, 1e-5)),
-        ("rmsnorm bf16 [65536,2048]", "rms", (65536, 2048, False, 1e-5)),
-        ("add_rmsnorm bf16 [16384,8192]", "add", (16384, 8192)),
-        ("add_rmsnorm bf16 [65536,2048]", "add", (65536, 2048)),
-        ("rmsnorm bf16 [256,131072] (cluster per row)", "rms", (256, 131072, False, 1e-5)),
-        ("layernorm bf16 [8192,4096]", "ln", (8192, 4096)),
-        ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),
-        ("layernorm bf16 [16384,8192]", "ln", (16384, 8192)),
-        ("rope bf16 [1,65536,32,128]", "rope", (65536, 32, 128)),
-        ("rope bf16 [1,65536,32,64]", "rope", (65536, 32, 64)),
-        ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),
-        ("rope_qk bf16 Q[1,65536,32,128] + K[1,65536,8,128]", "rope_qk", (65536, 32, 8, 128)),
-        ("kv rmsnorm+rope+cache bf16 kv[1,65536,512+64] -> 131072 slots", "kv", (65536, 512, 64)),
-        ("rope interleaved bf16 x[65536,32,128], random positions < 131072", "ril", (65536, 32, 128)),
-        ("kv cat + repeat bf16 K[8,8192,8,128] -> [8,8192,32,128], last 1024 rotated", "cat",
-         (8, 7168, 1024, 8, 128, 4)),
-        ("kv cat + repeat bf16 K[1,65536,8,64] -> [1,65536,32,64], last 4096 rotated", "cat",
-         (1, 61440, 4096, 8, 64, 4)),
-    ]
-    stream = torch.cuda.current_stream().cuda_stream
-    for name, kind, shp in cases:
-        if kind == "rms":
-            rows, cols, stress, eps = shp
-            x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=0, stress=stress, device="cuda")
-            y = torch.empty_like(x)
-            nbytes = ledger.rmsnorm_bytes(rows, cols)
-            plan = camp.camp_rmsnorm_plan(x, w, y, rows, cols, "bf16")
-            pname = plan_name("rmsnorm", plan)
-            fn = lambda: camp.camp_rmsnorm(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, cols,
-                                           eps, camp.BF16, stream)
-        elif kind == "add":
-            rows, cols = shp
-            x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
-            r, _ = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=1, device="cuda")
-            h, y = torch.empty_like(x), torch.empty_like(x)
-            nbytes = ledger.add_rmsnorm_bytes(rows, cols)
-            plan = camp.camp_add_rmsnorm_plan(x, r, w, h, y, rows, cols, "bf16")
-            pname = "add_" + plan_name("rmsnorm", plan)
-            fn = lambda: camp.camp_add_rmsnorm(x.data_ptr(), r.data_ptr(), w.data_ptr(),
-                                               h.data_ptr(), y.data_ptr(), rows, cols, 1e-5,
-                                               camp.BF16, stream)
-        elif kind == "ln":
-            rows, cols = shp
-            x, w, bt = inputs.layernorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
-            y = torch.empty_like(x)
-            nbytes = ledger.layernorm_bytes(rows, cols)
-            plan = camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16")
-            pname = plan_name("layernorm", plan)
-            fn = lambda: camp.camp_layernorm(x.data_ptr(), w.data_ptr(), bt.data_ptr(),
-                                             y.data_ptr(), rows, cols, 1e-5, camp.BF16, stream)
-        elif kind == "ril":
-            T, H, D = shp
-            mp = 2 * T
-            x = torch.randn(T, H, D, device="cuda").to(torch.bfloat16)
-            y = torch.empty_like(x)
-            sn = torch.empty(mp, D // 2, device="cuda")
-            cs = torch.empty(mp, D // 2, device="cuda")
-            camp.camp_rope_tables(sn, cs, mp, D, THETA, stream)
-            pos = torch.randint(0, mp, (T,), device="cuda", dtype=torch.int32)
-            nbytes = 2 * T * H * D * 2 + 2 * T * (D // 2) * 4 + 4 * T
-            plan = camp.camp_rope_interleaved_plan(x, sn, cs, pos, y, T, H, D, mp, "bf16")
-            pname = f"rope_interleaved<bf16,vec{plan.vec_bytes},hpt{plan.group}>"
-            fn = lambda: camp.camp_rope_interleaved(x.data_ptr(), sn.data_ptr(), cs.data_ptr(),
-                                                    pos.data_ptr(), y.data_ptr(), T, H, D, mp,
-                                                    camp.BF16, stream)
-        elif kind == "kv":
-            S, Dn, Dr = shp
-            ns = 2 * S
-            x = torch.randn(1, S, Dn + Dr, device="cuda").to(torch.bfloat16)
-            gam = torch.ones(Dn, device="cuda", dtype=torch.bfloat16)
-            _, sn, cs = inputs.rope_inputs(1, S, 1, Dr, "bf16", seed=0, device="cuda")
-            slots = torch.randperm(ns, device="cuda")[:S].to(torch.int64)
-            y = torch.empty(ns, Dn, device="cuda", dtype=torch.bfloat16)
-            yr = torch.empty(ns, Dr, device="cuda", dtype=torch.bfloat16)
-            nbytes = ledger.kv_cache_bytes(1, S, Dn, Dr)
-            plan = camp.camp_kv_rmsnorm_rope_cache_plan(x, gam, sn, cs, slots, y, yr, 1, S, Dn,
-                                                        Dr, ns, "bf16")
-            pname = f"kv_cache<bf16,vec{plan.vec_bytes},nv{plan.per_thread}>"
-            fn = lambda: camp.camp_kv_rmsnorm_rope_cache(
-                x.data_ptr(), gam.data_ptr(), sn.data_ptr(), cs.data_ptr(), slots.data_ptr(),
-                y.data_ptr(), yr.data_ptr(), 1, S, Dn, Dr, ns, 1e-5, camp.BF16, stream)
-        elif kind == "cat":
-            B, P, S, Hk, D, nr = shp
-            x, nw, sn, cs, y = _kv_cat_tensors(B, P, S, Hk, D, nr)
-            nbytes = ledger.kv_cat_repeat_bytes(B, P, S, Hk, D, nr)
-            plan = camp.camp_kv_cat_repeat_plan(x, nw, sn, cs, y, B, P, S, Hk, D, nr, "bf16")
-            pname = f"kv_cat_repeat<bf16,vec{plan.vec_bytes},hpt{plan.group}>"
-            fn = lambda: camp.camp_kv_cat_repeat(x.data_ptr(), nw.data_ptr(), sn.data_ptr(),
-                                                 cs.data_ptr(), y.data_ptr(), B, P, S, Hk, D, nr,
-                                                 camp.BF16, stream)
-        elif kind == "rope_qk":
-            S, Hq, Hk, D = shp
-            q, sn, cs = inputs.rope_inputs(1, S, Hq, D, "bf16", seed=0, device="cuda")
-            k, _, _ = inputs.rope_inputs(1, S, Hk, D, "bf16", seed=1, device="cuda")
-            x, y = q, torch.empty_like(q)
-            yk = torch.empty_like(k)
-            nbytes = ledger.rope_qk_bytes(1, S, Hq, Hk, D)
-            plan = camp.camp_rope_qk_plan(q, k, sn, cs, y, yk, 1, S, Hq, Hk, D, "bf16")
-            pname = plan_name("rope", plan)
-            fn = lambda: camp.camp_rope_qk(q.data_ptr(), k.data_ptr(), sn.data_ptr(), cs.data_ptr(),
-                                           y.data_ptr(), yk.data_ptr(), 1, S, Hq, Hk, D,
-                                           camp.BF16, stream)
-        else:
-            S, H, D = shp
-            x, sn, cs = inputs.rope_inputs(1, S, H, D, "bf16", seed=0, device="cuda")
-            y = torch.empty_like(x)
-            nbytes = ledger.rope_bytes(1, S, H, D)
-            plan = camp.camp_rope_plan(x, sn, cs, y, 1, S, H, D, "bf16")
-            pname = plan_name("rope", plan)
-            fn = lambda: camp.camp_rope(x.data_ptr(), sn.data_ptr(), cs.data_ptr(), y.data_ptr(),
-                                        1, S, H, D, camp.BF16, stream)
-        for _ in range(3):
-            fn()
+    l2 = getattr(torch.cuda.get_device_properties(torch.cuda.current_device()),
+                 "L2_cache_size", 0) or 129 * 2**20
+    for name, kind, shp in LARGE_CASES:
+        first = _large_case(kind, shp, 0)
+        nbytes = first[1]
+        R = max(1, min(8, math.ceil(4 * l2 / nbytes)))
+        sets = [first] + [_large_case(kind, shp, i) for i in range(1, R)]
+        N = R * max(1, round(16 / R))
+        stream = torch.cuda.current_stream().cuda_stream
+        for f in sets:
+            f[0](stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        with torch.cuda.graph(g, stream=cap):
+            h = torch.cuda.current_stream().cuda_stream
+            for j in range(N):
+                sets[j % R][0](h)
+        g.replay()
+        torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(reps)]
-        torch.cuda.synchronize()
         for a, b in evs:
             a.record()
-            fn()
+            g.replay()
             b.record()
         torch.cuda.synchronize()
-        ts = sorted(a.elapsed_time(b) * 1e-3 for a, b in evs)
-        t = statistics.median(ts)
+        t = statistics.median(a.elapsed_time(b) * 1e-3 for a, b in evs) / N
         gbs = nbytes / t / 1e9
-        out.append({"config": name, "kernel": pname, "bytes": nbytes, "us_median": t * 1e6,
-                    "GB/s": gbs, "frac": gbs / peak})
-        del x, y
+        out.append({"config": name, "kernel": first[2], "bytes": nbytes, "us": t * 1e6,
+                    "GB/s": gbs, "frac": gbs / peak, "input_sets": R, "launches_per_graph": N})
+        del g, sets, first
         torch.cuda.empty_cache()
     return out
 
@@ -632,6 +657,15 @@ def run_case(case: str, launches: int) -> None:
         plan = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, "bf16"))
         for _ in range(launches):
             camp.camp_rmsnorm(x, w, y, rows, cols, EPS, camp.BF16, stream)
+    elif kind == "add":
+        rows, cols = dims
+        x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
+        r, _ = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=1, device="cuda")
+        h, y = torch.empty_like(x), torch.empty_like(x)
+        plan = "add_" + plan_name("rmsnorm", camp.camp_add_rmsnorm_plan(x, r, w, h, y, rows, cols,
+                                                                        "bf16"))
+        for _ in range(launches):
+            camp.camp_add_rmsnorm(x, r, w, h, y, rows, cols, EPS, camp.BF16, stream)
     elif kind == "layernorm":
         rows, cols = dims
         x, w, bt = inputs.layernorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
@@ -714,7 +748,8 @@ def main() -> None:
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", default=None,
                     help="profiling mode: launch one operator at one shape --launches times "
-                         "and exit, e.g. rmsnorm:16384x8192, layernorm:16384x2048, "
+                         "and exit, e.g. rmsnorm:16384x8192, add:16384x8192, "
+                         "layernorm:16384x2048, "
                          "rope:1x16384x32x128, rope_qk:1x16384x32x8x128 (B x S x Hq x Hk x D), "
                          "kv:65536x512x64 (S x Dn x Dr), rope_il:16384x32x128 (T x H x D, "
                          "random positions) or kvcat:1x3584x512x8x64x4 "
