@@ -116,6 +116,9 @@ def plan_name(kind: str, p: camp.Plan) -> str:
     if kind == "layernorm":
         return f"layernorm_rows<bf16,vec{p.vec_bytes},group{p.group},nv{p.per_thread}>"
     if kind == "rmsnorm":
+        if p.kernel == camp.KERNEL_RMSNORM_STAGED:
+            return (f"rmsnorm_staged<bf16,cluster{p.cluster},chunk{p.group}vec,"
+                    f"stages{p.per_thread}>")
         k = {camp.KERNEL_RMSNORM_ROWS: "rmsnorm_rows", camp.KERNEL_RMSNORM_CLUSTER: "rmsnorm_cluster",
              camp.KERNEL_RMSNORM_WIDE: "rmsnorm_wide"}.get(p.kernel, "rmsnorm")
         extra = f",cluster{p.cluster}" if p.kernel == camp.KERNEL_RMSNORM_CLUSTER else ""
@@ -378,30 +381,57 @@ def run_reference(args) -> None:
 
 # ------------------------------------------------------------------ end to end
 
+class SlabSet:
+    """One step's tensors for the end-to-end leg, packed so that each direction is a single
+    copy: the inputs (x, w, Q, K, sin, cos) are views of one device slab, the outputs (y,
+    yQ, yK) of another; each view starts on a 256-byte boundary."""
+
+    def __init__(self, src: InputSet):
+        self.ins = self._pack(src.inputs_(), fill=True)
+        self.outs = self._pack(src.outputs_(), fill=False)
+        self.x, self.w, self.q, self.k, self.sq, self.cq = self.ins[1]
+        self.y, self.yq, self.yk = self.outs[1]
+        self.p = {n: getattr(self, n).data_ptr()
+                  for n in ("x", "w", "q", "k", "sq", "cq", "y", "yq", "yk")}
+
+    @staticmethod
+    def _pack(tensors, fill: bool):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        slab = torch.empty(n, dtype=torch.uint8, device="cuda")
+        views = []
+        for t, o in zip(tensors, offs):
+            nb = t.numel() * t.element_size()
+            v = slab[o:o + nb].view(t.dtype).view(t.shape)
+            if fill:
+                v.copy_(t)
+            views.append(v)
+        return slab, views
+
+
 def _e2e_serial(sets, host_in, host_out, steps: int, stream) -> float:
     """Every step on one stream: copy in, the two kernels, copy out. Returns seconds."""
-    R = len(sets)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record()
         for i in range(steps):
-            s = sets[i % R]
-            for d, h in zip(s.inputs_(), host_in):
-                d.copy_(h, non_blocking=True)
+            s = sets[i % 2]
+            s.ins[0].copy_(host_in, non_blocking=True)
             launch_step(s, stream.cuda_stream)
-            for h, d in zip(host_out[i % 2], s.outputs_()):
-                h.copy_(d, non_blocking=True)
+            host_out[i % 2].copy_(s.outs[0], non_blocking=True)
         e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e-3
 
 
 def _e2e_pipelined(sets, host_in, host_out, steps: int) -> float:
-    """Double-buffered over two device input sets and three streams: the host-to-device
-    copy of step i + 1, the kernels of step i and the device-to-host copy of step i - 1 run
-    at the same time. Events keep each set's inputs from being overwritten before the
-    kernels of its previous step have read them, and its outputs before they have been
-    copied out. Returns seconds from the first copy in to the last copy out."""
+    """Double-buffered over two device slab sets and three streams: the host-to-device copy
+    of step i + 1, the kernels of step i and the device-to-host copy of step i - 1 run at
+    the same time. Events keep each set's inputs from being overwritten before the kernels
+    of its previous step have read them, and its outputs before they have been copied out.
+    Returns seconds from the first copy in to the last copy out."""
     h2d, comp, d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     in_ready = [ev(), ev()]
@@ -418,8 +448,7 @@ def _e2e_pipelined(sets, host_in, host_out, steps: int) -> float:
         if i >= 2:
             h2d.wait_event(comp_done[k])     # step i - 2 has read this set's inputs
         with torch.cuda.stream(h2d):
-            for d, h in zip(s.inputs_(), host_in):
-                d.copy_(h, non_blocking=True)
+            s.ins[0].copy_(host_in, non_blocking=True)
         in_ready[k].record(h2d)
         comp.wait_event(in_ready[k])
         if i >= 2:
@@ -428,8 +457,7 @@ def _e2e_pipelined(sets, host_in, host_out, steps: int) -> float:
         comp_done[k].record(comp)
         d2h.wait_event(comp_done[k])
         with torch.cuda.stream(d2h):
-            for h, d in zip(host_out[k], s.outputs_()):
-                h.copy_(d, non_blocking=True)
+            host_out[k].copy_(s.outs[0], non_blocking=True)
         out_done[k].record(d2h)
     e1.record(d2h)
     torch.cuda.synchronize()
@@ -440,18 +468,19 @@ def end_to_end(sets, steps: int, world: int, dist) -> dict:
     """The step metric through the C ABI with host buffers: each step copies its inputs
     from pinned host memory, runs both kernels and copies its outputs back to pinned host
     memory, all inside the timed region. Reported pipelined (the value) and serial."""
-    host_in = [t.cpu().pin_memory() for t in sets[0].inputs_()]
-    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in sets[0].outputs_()]
+    slabs = [SlabSet(sets[0]), SlabSet(sets[1 % len(sets)])]
+    host_in = slabs[0].ins[0].cpu().pin_memory()
+    host_out = [torch.empty(slabs[0].outs[0].numel(), dtype=torch.uint8, pin_memory=True)
                 for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    h2d = host_in.numel()
+    d2h = host_out[0].numel()
     stream = torch.cuda.Stream()
-    _e2e_serial(sets, host_in, host_out, 3, stream)          # warm-up
-    _e2e_pipelined(sets, host_in, host_out, 3)
+    _e2e_serial(slabs, host_in, host_out, 3, stream)          # warm-up
+    _e2e_pipelined(slabs, host_in, host_out, 3)
     if dist is not None:
         dist.barrier()
-    t_pipe = _e2e_pipelined(sets, host_in, host_out, steps)
-    t_serial = _e2e_serial(sets, host_in, host_out, steps, stream)
+    t_pipe = _e2e_pipelined(slabs, host_in, host_out, steps)
+    t_serial = _e2e_serial(slabs, host_in, host_out, steps, stream)
     if dist is not None:
         t = torch.tensor([t_pipe, t_serial], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -460,7 +489,8 @@ def end_to_end(sets, steps: int, world: int, dist) -> dict:
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": t_pipe / steps * 1e3,
             "schedule": "double-buffered: copy in of step i+1, kernels of step i and copy out "
-                        "of step i-1 on three streams, ordered by events",
+                        "of step i-1 on three streams, ordered by events; each direction one "
+                        "copy of a packed slab (inputs, outputs 256-byte aligned in it)",
             "serial": {"value": STEP_BYTES * steps * world / t_serial / 1e9,
                        "ms_per_step": t_serial / steps * 1e3,
                        "schedule": "one stream: copy in, kernels, copy out"},
@@ -485,7 +515,9 @@ LARGE_CASES = [
     ("rmsnorm bf16 [65536,2048]", "rms", (65536, 2048, False, 1e-5)),
     ("add_rmsnorm bf16 [16384,8192]", "add", (16384, 8192)),
     ("add_rmsnorm bf16 [65536,2048]", "add", (65536, 2048)),
-    ("rmsnorm bf16 [256,131072] (cluster per row)", "rms", (256, 131072, False, 1e-5)),
+    ("rmsnorm bf16 [1024,65536] (staged in shared memory)", "rms", (1024, 65536, False, 1e-5)),
+    ("rmsnorm bf16 [256,131072] (staged in shared memory)", "rms", (256, 131072, False, 1e-5)),
+    ("add_rmsnorm bf16 [512,131072] (staged in shared memory)", "add", (512, 131072)),
     ("layernorm bf16 [8192,4096]", "ln", (8192, 4096)),
     ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),
     ("layernorm bf16 [16384,8192]", "ln", (16384, 8192)),
@@ -598,15 +630,31 @@ def _large_case(kind: str, shp: tuple, seed: int):
     return fn, ledger.rope_bytes(1, S, H, D), pname, (x, sn, cs, y)
 
 
-def large_configs(peak: float, reps: int) -> list[dict]:
-    """Single-operator timings at the large sweep shapes, timed like the step: a CUDA graph
-    of N back-to-back launches rotating over R input sets (R x bytes > 4 x L2, so every
-    launch reads from HBM), one event pair per graph replay; the median over `reps`
-    replays of the replay time / N."""
+SWEEP_TOKENS = (1, 8, 64, 512, 4096, 65536)
+
+
+def sweep_cases() -> list:
+    """The shape sweep: RMSNorm bf16 over tokens x hidden {2048, 3000, 8192} and RoPE bf16
+    over tokens x heads {32, 8} x head_dim {64, 128} (B = 1, S = tokens, theta 500000)."""
+    cases = []
+    for t in SWEEP_TOKENS:
+        for hidden in (2048, 3000, 8192):
+            cases.append((f"rmsnorm bf16 [{t},{hidden}]", "rms", (t, hidden, False, 1e-5)))
+        for heads in (32, 8):
+            for d in (64, 128):
+                cases.append((f"rope bf16 [1,{t},{heads},{d}]", "rope", (t, heads, d)))
+    return cases
+
+
+def large_configs(peak: float, reps: int, cases=None) -> list[dict]:
+    """Single-operator timings, timed like the step: a CUDA graph of N back-to-back launches
+    rotating over R input sets (R x bytes > 4 x L2 where R <= 8 allows it, so every launch
+    reads from HBM), one event pair per graph replay; the median over `reps` replays of
+    the replay time / N."""
     out = []
     l2 = getattr(torch.cuda.get_device_properties(torch.cuda.current_device()),
                  "L2_cache_size", 0) or 129 * 2**20
-    for name, kind, shp in LARGE_CASES:
+    for name, kind, shp in (LARGE_CASES if cases is None else cases):
         first = _large_case(kind, shp, 0)
         nbytes = first[1]
         R = max(1, min(8, math.ceil(4 * l2 / nbytes)))
@@ -634,7 +682,8 @@ def large_configs(peak: float, reps: int) -> list[dict]:
         t = statistics.median(a.elapsed_time(b) * 1e-3 for a, b in evs) / N
         gbs = nbytes / t / 1e9
         out.append({"config": name, "kernel": first[2], "bytes": nbytes, "us": t * 1e6,
-                    "GB/s": gbs, "frac": gbs / peak, "input_sets": R, "launches_per_graph": N})
+                    "GB/s": gbs, "frac": gbs / peak, "input_sets": R, "launches_per_graph": N,
+                    "l2_cold": R * nbytes > 4 * l2})
         del g, sets, first
         torch.cuda.empty_cache()
     return out
@@ -874,9 +923,10 @@ def main() -> None:
 
     calibration = copy_calibration(sets, M, 50, peak)
 
-    large = None
+    large = sweep = None
     if rank == 0 and not args.no_large:
         large = large_configs(peak, args.large_reps)
+        sweep = large_configs(peak, args.large_reps, sweep_cases())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -912,6 +962,8 @@ def main() -> None:
     }
     if large is not None:
         line["large_configs"] = large
+    if sweep is not None:
+        line["sweep"] = sweep
     print(json.dumps(line), flush=True)
 
 

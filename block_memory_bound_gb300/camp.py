@@ -40,6 +40,9 @@ KERNEL_KV_CACHE = 7
 KERNEL_ROPE_INTERLEAVED = 8
 KERNEL_LAYERNORM_ROWS = 9
 KERNEL_KV_CAT = 10
+KERNEL_RMSNORM_STAGED = 11
+
+DEVICE_ERROR_WAIT_TIMEOUT = 1
 
 # Every symbol include/camp.h declares.
 EXPORTS = (
@@ -53,6 +56,7 @@ EXPORTS = (
     "camp_rope_tables",
     "camp_layernorm", "camp_layernorm_plan", "camp_layernorm_with_plan",
     "camp_kv_cat_repeat", "camp_kv_cat_repeat_plan", "camp_kv_cat_repeat_with_plan",
+    "camp_device_errors",
 )
 
 
@@ -111,6 +115,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_status_string.restype = ctypes.c_char_p
         lib.camp_last_cuda_error.argtypes = []
         lib.camp_last_cuda_error.restype = c_int
+        lib.camp_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), c_int]
+        lib.camp_device_errors.restype = c_int
         lib.camp_rmsnorm_plan.argtypes = [vp, vp, vp, i64, i64, c_int, pplan]
         lib.camp_rmsnorm_plan.restype = c_int
         lib.camp_rope_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, pplan]
@@ -221,6 +227,13 @@ camp_status_string = status_string
 
 def camp_last_cuda_error() -> int:
     return load().camp_last_cuda_error()
+
+
+def camp_device_errors(clear: bool = False) -> int:
+    """The library's device error word (0: no kernel's bounded wait ran out); synchronizes."""
+    v = ctypes.c_uint32(0)
+    _check("camp_device_errors", load().camp_device_errors(ctypes.byref(v), int(bool(clear))))
+    return v.value
 
 
 def camp_rmsnorm(x, w, y, rows: int, cols: int, eps: float, dtype, stream=None) -> None:

@@ -252,14 +252,67 @@ bool rms_choose_cluster(const RmsCall& c, int64_t nvec, int* cluster, int* per_t
     return false;
 }
 
+// Staged (shared-memory) split of a row: chunk vectors per CTA for `cluster` CTAs, and
+// the resulting dynamic shared memory; false if the variant cannot hold the row.
+bool rms_staged_fits(const RmsCall& c, int64_t nvec, int cluster, int stages,
+                     int64_t* chunk) {
+    if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1)) != 0) return false;
+    if (stages < 2 || stages > camp::kStagedMaxStages) return false;
+    *chunk = ceil_div(nvec, cluster);
+    return *chunk <= static_cast<int64_t>(camp::kStagedMaxVecsPerThread) * camp::kStagedBlock &&
+           camp::staged_smem_bytes(c.add, *chunk, stages) <= camp::kStagedSmemMax;
+}
+
+// Fill the plan fields of a staged launch: group = vectors per CTA chunk, per_thread =
+// stages, grid = an estimate of the CTAs launched (the launch sizes the grid to the
+// clusters the device holds at once, at most one per row).
+void rms_staged_plan_fields(const RmsCall& c, int cluster, int stages, int64_t chunk,
+                            camp_plan_t* p) {
+    p->kernel = CAMP_KERNEL_RMSNORM_STAGED;
+    p->vec_bytes = 16;
+    p->group = static_cast<int32_t>(chunk);
+    p->per_thread = stages;
+    p->block = camp::kStagedBlock;
+    p->cluster = cluster;
+    const int64_t per_sm = camp::kSmSmemBytes / (camp::staged_smem_bytes(c.add, chunk, stages) + 1024);
+    int64_t clusters = (camp::kSmCount * (per_sm < 1 ? 1 : per_sm)) / cluster;
+    if (clusters < 1) clusters = 1;
+    if (clusters > c.a.rows) clusters = c.a.rows;
+    p->grid = clusters * cluster;
+}
+
+// Rows of more than kStagedFrom 16-byte vectors go to the shared-memory-staged kernel:
+// C = the power of two (at most 16) that makes a CTA's chunk about 1024 vectors (16 KB),
+// 3 buffers deep, 2 at C = 16. Measured on GB300 (bf16, L2-cold, graphs of back-to-back
+// launches), against the register kernels' default plans: 1024 x 65536 0.90 / 0.80 of the
+// measured HBM peak, 512 x 131072 0.84 / 0.75, 256 x 131072 0.76 / 0.67, 64 x 262144
+// 0.63 / 0.50; with the residual add 1024 x 65536 0.92 / 0.80, 512 x 131072 0.98 / 0.77;
+// fp32 256 x 65536 0.83 / 0.68. At 4096 vectors and below the register kernels are as
+// fast (2048 x 32768: 0.87 / 0.88) and keep those rows.
+constexpr int64_t kStagedFrom = 4096;
+
+bool rms_choose_staged(const RmsCall& c, int64_t nvec, int* cluster, int* stages,
+                       int64_t* chunk) {
+    int cl = 1;
+    while (cl < 16 && ceil_div(nvec, cl) > 1024) cl *= 2;
+    const int st = cl == 16 ? 2 : 3;
+    if (!rms_staged_fits(c, nvec, cl, st, chunk)) return false;
+    *cluster = cl;
+    *stages = st;
+    return true;
+}
+
 void rms_plan(const RmsCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
     p->vec_bytes = rms_vec_bytes(c);
     p->cluster = 1;
     const int64_t nvec = c.a.cols * camp::elem_bytes(c.t) / p->vec_bytes;
-    int g = 0, nv = 0, cl = 0;
+    int g = 0, nv = 0, cl = 0, st = 0;
+    int64_t chunk = 0;
     const int64_t cluster_from = c.add ? kClusterFrom / 2 : kClusterFrom;
-    if (p->vec_bytes == 16 && nvec > cluster_from && rms_choose_cluster(c, nvec, &cl, &nv)) {
+    if (p->vec_bytes == 16 && nvec > kStagedFrom && rms_choose_staged(c, nvec, &cl, &st, &chunk)) {
+        rms_staged_plan_fields(c, cl, st, chunk, p);
+    } else if (p->vec_bytes == 16 && nvec > cluster_from && rms_choose_cluster(c, nvec, &cl, &nv)) {
         p->kernel = CAMP_KERNEL_RMSNORM_CLUSTER;
         p->group = cl * camp::kClusterBlock;
         p->per_thread = nv;
@@ -311,6 +364,13 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
         p->grid = c.a.rows * cl;
         return CAMP_SUCCESS;
     }
+    if (in.kernel == CAMP_KERNEL_RMSNORM_STAGED) {
+        int64_t chunk = 0;
+        if (vb != 16 || !rms_staged_fits(c, nvec, in.cluster, in.per_thread, &chunk))
+            return CAMP_ERR_NOT_SUPPORTED;
+        rms_staged_plan_fields(c, in.cluster, in.per_thread, chunk, p);
+        return CAMP_SUCCESS;
+    }
     if (in.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
         if (!camp::rmsnorm_wide_compiled(c.t, vb)) return CAMP_ERR_NOT_SUPPORTED;
         p->group = camp::kWideBlock;
@@ -331,6 +391,8 @@ camp_status_t rms_launch(const RmsCall& c, const camp_plan_t& p, cudaStream_t s)
         e = camp::rmsnorm_cluster_launch(c.add, c.t, p.per_thread, p.cluster, c.a, s);
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
         e = camp::rmsnorm_wide_launch(c.add, c.t, p.vec_bytes, c.a, p.grid, s);
+    } else if (p.kernel == CAMP_KERNEL_RMSNORM_STAGED) {
+        e = camp::rmsnorm_staged_launch(c.add, c.t, p.cluster, p.per_thread, c.a, s);
     }
     return runtime_status(e);
 }
@@ -903,6 +965,14 @@ CAMP_API const char* camp_status_string(camp_status_t status) {
 }
 
 CAMP_API int camp_last_cuda_error(void) { return g_last_cuda_error; }
+
+CAMP_API camp_status_t camp_device_errors(uint32_t* flags, int clear) {
+    if (flags == nullptr) return CAMP_ERR_INVALID_ARG;
+    unsigned int v = 0;
+    const camp_status_t st = runtime_status(camp::read_device_errors(&v, clear != 0));
+    *flags = st == CAMP_SUCCESS ? v : 0u;
+    return st;
+}
 
 CAMP_API camp_status_t camp_rmsnorm(const void* x, const void* w, void* y, int64_t rows,
                                     int64_t cols, float eps, camp_dtype_t dtype,

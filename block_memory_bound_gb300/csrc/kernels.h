@@ -112,6 +112,27 @@ bool rmsnorm_wide_compiled(DType t, int vec_bytes);
 cudaError_t rmsnorm_wide_launch(bool add, DType t, int vec_bytes, const RmsnormArgs& a,
                                 int64_t grid, cudaStream_t s);
 
+// TMA-staged RMSNorm (rows staged in shared memory by bulk asynchronous copies): persistent
+// clusters of `cluster` (1..16) CTAs of kStagedBlock threads; each CTA owns a contiguous
+// chunk of ceil(nvec / cluster) <= 8 * 256 16-byte vectors of every row of its cluster,
+// holds its chunk of w, and keeps `stages` (2..kStagedMaxStages) row chunks in flight (x,
+// and r on the add path). Needs 16-byte accesses (row pitch and pointers) and
+// staged_smem_bytes(add, chunk, stages) <= kStagedSmemMax.
+constexpr int kStagedBlock = 256;
+constexpr int kStagedMaxStages = 4;
+constexpr int kStagedMaxVecsPerThread = 8;   // a CTA chunk holds at most 8 * 256 vectors
+constexpr int64_t kStagedSmemMax = 224 * 1024;   // dynamic shared memory per CTA
+constexpr int64_t kSmSmemBytes = 228 * 1024;     // shared memory per SM
+inline int64_t staged_smem_bytes(bool add, int64_t chunk_vecs, int stages) {
+    return chunk_vecs * 16 * (1 + (add ? 2 : 1) * stages);   // w, then the row buffers
+}
+cudaError_t rmsnorm_staged_launch(bool add, DType t, int cluster, int stages,
+                                  const RmsnormArgs& a, cudaStream_t s);
+
+// The library's device error word: kernels whose bounded waits ran out set bits in it.
+constexpr unsigned int kDeviceErrorWaitTimeout = 1u;
+cudaError_t read_device_errors(unsigned int* flags, bool clear);
+
 // The add-path tables live in their own translation unit (compiled in parallel).
 namespace add_path {
 cudaError_t rows_launch(DType t, int vec_bytes, int group, int per_thread, const RmsnormArgs& a,

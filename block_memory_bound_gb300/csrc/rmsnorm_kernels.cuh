@@ -26,7 +26,7 @@
 // CTA reduces its chunk and stores the partial sum into a slot of every CTA of the
 // cluster (distributed shared memory); after one hardware cluster barrier each CTA sums
 // the C slots in rank order, so all get the same sum. x is read from HBM once; there is
-// no spinning.
+// no spinning. (rmsnorm_staged.cu holds the shared-memory-staged alternative.)
 //
 // rmsnorm_wide_kernel: rows wider than a cluster's registers take two sweeps in one CTA per
 // row (the second sweep re-reads x, or h on the add path, mostly from L2).
@@ -173,6 +173,11 @@ rmsnorm_cluster_kernel(const void* x, const void* r, void* h, const void* __rest
     __shared__ float partial[kWarps];
     __shared__ float slot[16];   // slot[r]: the partial sum of cluster rank r
 
+    // First phase of the cluster barrier, split: arrive now, wait just before the remote
+    // stores below, so every CTA of the cluster has started (and owns its shared memory)
+    // before any CTA writes into it; the wait costs nothing by then.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
     griddep_wait();
     griddep_launch_dependents();
 
@@ -195,6 +200,7 @@ rmsnorm_cluster_kernel(const void* x, const void* r, void* h, const void* __rest
     float ss = warp_sum(sum_squares<C>(v));
     if ((t & 31) == 0) partial[t / 32] = ss;
     __syncthreads();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     // Thread r < C writes this CTA's partial into slot[rank] of cluster rank r: one round of
     // remote stores, then a single cluster barrier (its release/acquire makes the stores
     // visible, and no shared memory of another CTA is touched after it).

@@ -282,6 +282,16 @@ CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const vo
                                       void* y, int64_t rows, int64_t cols, float eps,
                                       camp_dtype_t dtype, void* stream);
 
+/*
+ * The library's device error word: bit CAMP_DEVICE_ERROR_WAIT_TIMEOUT is set by a kernel
+ * whose bounded wait (on an asynchronous copy; one second at most) ran out, in which case
+ * that kernel's output is incomplete. Correct operation never sets it. *flags receives the
+ * word; clear != 0 resets it to 0. Synchronizes the device (it reads device memory).
+ * Errors: CAMP_ERR_INVALID_ARG for a NULL flags; CAMP_ERR_RUNTIME if the read fails.
+ */
+#define CAMP_DEVICE_ERROR_WAIT_TIMEOUT 1u
+CAMP_API camp_status_t camp_device_errors(uint32_t* flags, int clear);
+
 /* A static, human-readable name for a status code (never NULL). */
 CAMP_API const char* camp_status_string(camp_status_t status);
 
@@ -308,15 +318,19 @@ typedef enum {
     CAMP_KERNEL_KV_CACHE = 7,       /* camp_kv_rmsnorm_rope_cache: one warp per token */
     CAMP_KERNEL_ROPE_INTERLEAVED = 8, /* camp_rope_interleaved: tiled like CAMP_KERNEL_ROPE */
     CAMP_KERNEL_LAYERNORM_ROWS = 9, /* camp_layernorm: a group of threads per row, registers */
-    CAMP_KERNEL_KV_CAT = 10         /* camp_kv_cat_repeat: tiled like CAMP_KERNEL_ROPE */
+    CAMP_KERNEL_KV_CAT = 10,        /* camp_kv_cat_repeat: tiled like CAMP_KERNEL_ROPE */
+    CAMP_KERNEL_RMSNORM_STAGED = 11 /* persistent clusters, rows staged in shared memory by
+                                       bulk asynchronous copies, `per_thread` buffers deep */
 } camp_kernel_t;
 
 typedef struct {
     int32_t kernel;        /* camp_kernel_t */
     int32_t vec_bytes;     /* bytes per vector access of x and y: 16, 8, 4 or 2 */
-    int32_t group;         /* RMSNorm: threads per row. RoPE, KV concat: heads per thread.
+    int32_t group;         /* RMSNorm: threads per row (staged kernel: 16-byte vectors of a
+                              row per CTA). RoPE, KV concat: heads per thread.
                               KV cache: rope access bytes per half and lane */
-    int32_t per_thread;    /* RMSNorm: vector accesses per thread per row. RoPE: unused (0) */
+    int32_t per_thread;    /* RMSNorm: vector accesses per thread per row (staged kernel:
+                              shared-memory buffers per CTA). RoPE: unused (0) */
     int32_t block;         /* threads per CTA */
     int32_t cluster;       /* CTAs per cluster (RMSNorm cluster kernel: 2..16), else 1 */
     int64_t grid;          /* CTAs launched */

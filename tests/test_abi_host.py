@@ -140,11 +140,15 @@ def test_rope_empty_is_success_without_cuda(lib):
     (4096, 12288, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 6, 256, 4096)),
     (4096, 16384, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 8, 256, 4096)),
     (1024, 32768, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 8, 512, 1024)),
-    (5, 65536, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 8, 1024, 5)),
-    # ...then a cluster of 256-thread CTAs per row, the smallest with <= 8 accesses a thread
-    (5, 65544, "bf16", (camp.KERNEL_RMSNORM_CLUSTER, 16, 2048, 6, 256, 40, 8)),
-    (256, 131072, "bf16", (camp.KERNEL_RMSNORM_CLUSTER, 16, 2048, 8, 256, 2048, 8)),
-    (2, 262144, "bf16", (camp.KERNEL_RMSNORM_CLUSTER, 16, 4096, 8, 256, 32, 16)),
+    # ...then (past 4096 vectors) rows staged in shared memory by persistent clusters:
+    # group = vectors a CTA (about 1024), per_thread = buffers (3; 2 with 16 CTAs),
+    # grid = the clusters that fit (estimated), at most one per row, x the cluster size
+    (5, 65536, "bf16", (camp.KERNEL_RMSNORM_STAGED, 16, 1024, 3, 256, 40, 8)),
+    (5, 65544, "bf16", (camp.KERNEL_RMSNORM_STAGED, 16, 513, 2, 256, 80, 16)),
+    (256, 131072, "bf16", (camp.KERNEL_RMSNORM_STAGED, 16, 1024, 2, 256, 608, 16)),
+    (2, 262144, "bf16", (camp.KERNEL_RMSNORM_STAGED, 16, 2048, 2, 256, 32, 16)),
+    (7, 32768, "f32", (camp.KERNEL_RMSNORM_STAGED, 16, 1024, 3, 256, 56, 8)),
+    # past 16 x 2048 vectors: two sweeps over the row in one CTA
     (3, 131080, "f32", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 3, 1)),
     (2, 262152, "bf16", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 2, 1)),
     (5, 16385, "f32", (camp.KERNEL_RMSNORM_WIDE, 4, 1024, 0, 1024, 5, 1)),
@@ -358,8 +362,8 @@ def test_add_rmsnorm_exact_aliases_are_accepted(lib):
 @pytest.mark.parametrize("rows,cols,expect", [
     (4096, 2048, (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 1)),
     (16384, 8192, (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 1)),
-    # the add path holds x and r at once: past 4096 vectors a row it takes a cluster
-    (64, 40000, (camp.KERNEL_RMSNORM_CLUSTER, 16, 1024, 5 + 1, 4)),
+    # past 4096 vectors a row the add path stages x and r in shared memory
+    (64, 40000, (camp.KERNEL_RMSNORM_STAGED, 16, 625, 3, 8)),
 ])
 def test_add_rmsnorm_plans(lib, rows, cols, expect):
     p = camp.camp_add_rmsnorm_plan(X, R_, W, H_, Y, rows, cols, "bf16")
@@ -524,7 +528,7 @@ def test_layernorm_empty_and_in_place(lib):
 @pytest.mark.parametrize("rows,cols,dtype", [
     (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"),
     (1, 8, "bf16"), (64, 3001, "bf16"), (4096, 12288, "bf16"), (1024, 32768, "bf16"),
-    (5, 65536, "bf16"), (7, 32768, "f32"), (3, 16384, "f32"), (4096, 1024, "bf16"),
+    (3, 16384, "f32"), (4096, 1024, "bf16"),
 ])
 def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype):
     # the same register-resident row mapping as RMSNorm: where neither the one-wave test
@@ -535,6 +539,16 @@ def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype)
     assert p.kernel == camp.KERNEL_LAYERNORM_ROWS
     assert (p.vec_bytes, p.group, p.per_thread, p.block, p.grid, p.cluster) == \
         (q.vec_bytes, q.group, q.per_thread, q.block, q.grid, 1)
+
+
+def test_layernorm_keeps_its_rows_kernel_where_rmsnorm_stages_the_row(lib):
+    # RMSNorm stages rows past 4096 vectors; LayerNorm has no staged kernel and keeps one
+    # CTA of up to 1024 threads per row (up to 8192 vectors)
+    for rows, cols, dtype, g in ((5, 65536, "bf16", 1024), (7, 32768, "f32", 1024)):
+        assert camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype).kernel == \
+            camp.KERNEL_RMSNORM_STAGED
+        p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
+        assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, g, 8)
 
 
 @pytest.mark.parametrize("rows,cols,expect", [
@@ -679,3 +693,52 @@ def test_kv_cat_with_plan_checks_the_forced_plan(lib):
         st = lib.camp_kv_cat_repeat_with_plan(*CAT, 1, 4, 4, 3, 6, 2, camp.F32,
                                               ctypes.byref(plan), None)
         assert st == camp.ERR_NOT_SUPPORTED, plan
+
+
+# ------------------------------------------------------------------ staged RMSNorm plans
+
+def _staged(cluster, stages):
+    return camp.Plan(kernel=camp.KERNEL_RMSNORM_STAGED, vec_bytes=16, cluster=cluster,
+                     per_thread=stages)
+
+
+def test_staged_plans_that_do_not_fit_are_refused(lib):
+    # Only refusals are checked here: an accepted plan would launch (the GPU tests run every
+    # accepted variant on real memory). rows == 0 is a no-op whatever the plan.
+    st = lib.camp_rmsnorm_with_plan(X, W, Y, 0, 131072, ctypes.c_float(1e-5), camp.BF16,
+                                    ctypes.byref(_staged(8, 3)), None)
+    assert st == camp.SUCCESS
+    for (cols, dt, cl, stg) in [
+        (131072, camp.BF16, 1, 2),      # a CTA chunk above 8 x 256 vectors
+        (131072, camp.F32, 4, 3),       # 8192 vectors a CTA
+        (65536, camp.F32, 8, 5),        # 5 buffers are not built
+        (16384, camp.BF16, 3, 2),       # cluster not a power of two
+        (16384, camp.BF16, 32, 2),      # cluster above 16
+        (16384, camp.BF16, 2, 1),       # one buffer: no ring
+        (16384, camp.BF16, 2, 5),       # more buffers than built
+        (3001, camp.BF16, 1, 2),        # row pitch not a multiple of 16 bytes
+    ]:
+        st = lib.camp_rmsnorm_with_plan(X, W, Y, 2, cols, ctypes.c_float(1e-5), dt,
+                                        ctypes.byref(_staged(cl, stg)), None)
+        assert st == camp.ERR_NOT_SUPPORTED, (cols, cl, stg)
+
+
+def test_staged_add_path_counts_both_staged_tensors(lib):
+    R_ = 0x7F5000000000
+    H_ = 0x7F6000000000
+    # 32768 bf16 = 4096 vectors; x and r are both staged: 1 CTA would hold 4096 vectors
+    # (above 8 x 256); 2 CTAs x 4 buffers need w + 8 x 32 KB, above the 224 KB budget
+    for cl, stg in [(1, 2), (2, 4)]:
+        st = lib.camp_add_rmsnorm_with_plan(X, R_, W, H_, Y, 2, 32768, ctypes.c_float(1e-5),
+                                            camp.BF16, ctypes.byref(_staged(cl, stg)), None)
+        assert st == camp.ERR_NOT_SUPPORTED, (cl, stg)
+
+
+def test_staged_plan_needs_16_byte_accesses(lib):
+    st = lib.camp_rmsnorm_with_plan(X + 2, W, Y, 2, 16384, ctypes.c_float(1e-5), camp.BF16,
+                                    ctypes.byref(_staged(2, 2)), None)
+    assert st == camp.ERR_NOT_SUPPORTED
+
+
+def test_device_errors_argument_check(lib):
+    assert lib.camp_device_errors(None, 0) == camp.ERR_INVALID_ARG
