@@ -190,6 +190,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+# ------------------------------------------------------------------ ranks
+
+def ranks_max(values: list[float], dist, device: str = "cuda") -> list[float]:
+    """Element-wise maximum of `values` over all ranks (the slowest rank's times); the
+    values themselves when there is no process group."""
+    if dist is None:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_value(step_bytes: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job GB/s: every rank runs its own replica of `steps` steps of `step_bytes`
+    (weak scaling), and the job takes the slowest rank's `seconds`."""
+    return step_bytes * steps * world / seconds / 1e9
+
+
 # ------------------------------------------------------------------ the workload
 
 class InputSet:
@@ -481,17 +499,14 @@ def end_to_end(sets, steps: int, world: int, dist) -> dict:
         dist.barrier()
     t_pipe = _e2e_pipelined(slabs, host_in, host_out, steps)
     t_serial = _e2e_serial(slabs, host_in, host_out, steps, stream)
-    if dist is not None:
-        t = torch.tensor([t_pipe, t_serial], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_pipe, t_serial = (float(v) for v in t.tolist())
-    return {"value": STEP_BYTES * steps * world / t_pipe / 1e9, "unit": UNIT,
+    t_pipe, t_serial = ranks_max([t_pipe, t_serial], dist)
+    return {"value": job_value(STEP_BYTES, steps, world, t_pipe), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": t_pipe / steps * 1e3,
             "schedule": "double-buffered: copy in of step i+1, kernels of step i and copy out "
                         "of step i-1 on three streams, ordered by events; each direction one "
                         "copy of a packed slab (inputs, outputs 256-byte aligned in it)",
-            "serial": {"value": STEP_BYTES * steps * world / t_serial / 1e9,
+            "serial": {"value": job_value(STEP_BYTES, steps, world, t_serial),
                        "ms_per_step": t_serial / steps * 1e3,
                        "schedule": "one stream: copy in, kernels, copy out"},
             "copy_GB/s": (h2d + d2h) * steps / t_pipe / 1e9}
@@ -889,10 +904,7 @@ def main() -> None:
     elapsed = start.elapsed_time(end) * 1e-3
     clocks = sampler.summary(t_host0, t_host1)
 
-    if dist is not None:
-        t = torch.tensor([elapsed], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = ranks_max([elapsed], dist)[0]
 
     # Per-kernel time: the intervals between consecutive marks, summed over the region.
     per_kernel = {kind: 0.0 for kind in KERNELS}
@@ -905,7 +917,7 @@ def main() -> None:
     kernel_timing = (f"per kernel: summed time of its {M}-launch graphs over the timed "
                      f"region / K")
 
-    value = STEP_BYTES * args.steps * world / elapsed / 1e9
+    value = job_value(STEP_BYTES, args.steps, world, elapsed)
     kernels = []
     for kind in KERNELS:
         t = per_kernel[kind]
