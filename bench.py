@@ -661,7 +661,61 @@ def sweep_cases() -> list:
     return cases
 
 
-def large_configs(peak: float, reps: int, cases=None) -> list[dict]:
+def case_rows(kind: str, shp: tuple) -> tuple[int, str]:
+    """Rows a launch of this case processes, and what a row is: an RMSNorm / LayerNorm row,
+    a (token, head) row of RoPE, a token of the KV kernels."""
+    if kind in ("rms", "add", "ln"):
+        return shp[0], "row"
+    if kind in ("rope", "ril"):
+        return shp[0] * shp[1], "head row"
+    if kind == "rope_qk":
+        return shp[0] * (shp[1] + shp[2]), "head row"
+    if kind == "kv":
+        return shp[0], "token"
+    B, P, S = shp[:3]
+    return B * (P + S), "token"
+
+
+def oracle_case(kind: str, tensors: tuple, shp: tuple, budget_bytes: int = 64 << 20,
+                runs: int = 5) -> dict | None:
+    """CPU leg (the fp64 oracle, as it stands, on all host cores) of an RMSNorm or RoPE
+    configuration: the median of `runs` calls on the first rows of its inputs (at most
+    `budget_bytes` of input), as GB/s over the same algorithmic bytes and rows/s."""
+    import numpy as np
+    import oracle
+    lib = oracle.load()
+    cores = oracle.threads_available(lib)
+    if kind == "rms":
+        x, w = tensors[0], tensors[1]
+        rows, cols, _, eps = shp
+        n = max(1, min(rows, budget_bytes // (cols * x.element_size())))
+        xs, ws = inputs.to_numpy(x[:n]), inputs.to_numpy(w)
+        fn = lambda: oracle.rmsnorm(xs, ws, float(np.float32(eps)), "bf16", lib=lib)
+        nbytes, what = ledger.rmsnorm_bytes(n, cols), f"{n} of {rows} rows"
+        nrows = n
+    elif kind == "rope":
+        x, sn, cs = tensors[0], tensors[1], tensors[2]
+        S, H, D = shp
+        n = max(1, min(S, budget_bytes // (H * D * x.element_size())))
+        xs = inputs.to_numpy(x[:, :n])
+        ss, cc = sn[:n].cpu().numpy(), cs[:n].cpu().numpy()
+        fn = lambda: oracle.rope(xs, ss, cc, "bf16", lib=lib)
+        nbytes, what = ledger.rope_bytes(1, n, H, D), f"{n} of {S} positions"
+        nrows = n * H
+    else:
+        return None
+    fn()
+    ts = []
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+    t = statistics.median(ts)
+    return {"GB/s": nbytes / t / 1e9, "rows_per_s": nrows / t, "cores": cores,
+            "kind": "oracle", "sample": f"{what}, median of {runs}"}
+
+
+def large_configs(peak: float, reps: int, cases=None, cpu: bool = False) -> list[dict]:
     """Single-operator timings, timed like the step: a CUDA graph of N back-to-back launches
     rotating over R input sets (R x bytes > 4 x L2 where R <= 8 allows it, so every launch
     reads from HBM), one event pair per graph replay; the median over `reps` replays of
@@ -696,9 +750,13 @@ def large_configs(peak: float, reps: int, cases=None) -> list[dict]:
         torch.cuda.synchronize()
         t = statistics.median(a.elapsed_time(b) * 1e-3 for a, b in evs) / N
         gbs = nbytes / t / 1e9
-        out.append({"config": name, "kernel": first[2], "bytes": nbytes, "us": t * 1e6,
-                    "GB/s": gbs, "frac": gbs / peak, "input_sets": R, "launches_per_graph": N,
-                    "l2_cold": R * nbytes > 4 * l2})
+        nrows, row_kind = case_rows(kind, shp)
+        entry = {"config": name, "kernel": first[2], "bytes": nbytes, "us": t * 1e6,
+                 "GB/s": gbs, "frac": gbs / peak, "rows_per_s": nrows / t, "row": row_kind,
+                 "input_sets": R, "launches_per_graph": N, "l2_cold": R * nbytes > 4 * l2}
+        if cpu and kind in ("rms", "rope"):
+            entry["cpu_baseline"] = oracle_case(kind, first[3], shp)
+        out.append(entry)
         del g, sets, first
         torch.cuda.empty_cache()
     return out
@@ -922,8 +980,10 @@ def main() -> None:
     for kind in KERNELS:
         t = per_kernel[kind]
         gbs = KERNEL_BYTES[kind] / t / 1e9
+        rows = TOKENS if kind == "rmsnorm" else TOKENS * (HQ + HK)
         kernels.append({"name": kind, "kernel": plans[kind], "bytes": KERNEL_BYTES[kind],
-                        "us": t * 1e6, "GB/s": gbs, "frac": gbs / peak})
+                        "us": t * 1e6, "GB/s": gbs, "frac": gbs / peak, "rows_per_s": rows / t,
+                        "row": "row" if kind == "rmsnorm" else "head row"})
     dom = max(kernels, key=lambda k: k["us"])
     roofline = {"bound": "hbm", "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
                 "frac": dom["GB/s"] / peak, "traffic": recorded_traffic(dom["kernel"]),
@@ -937,8 +997,9 @@ def main() -> None:
 
     large = sweep = None
     if rank == 0 and not args.no_large:
-        large = large_configs(peak, args.large_reps)
-        sweep = large_configs(peak, args.large_reps, sweep_cases())
+        cpu_cases = rank == 0 and world == 1 and not args.no_cpu
+        large = large_configs(peak, args.large_reps, cpu=cpu_cases)
+        sweep = large_configs(peak, args.large_reps, sweep_cases(), cpu=cpu_cases)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
