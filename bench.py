@@ -524,6 +524,8 @@ def _kv_cat_tensors(B, P, S, Hk, D, n_rep):
 
 
 LARGE_CASES = [
+    ("rmsnorm fp32 [64,2048] (the small configuration; launch-bound)", "rms",
+     (64, 2048, False, 1e-5, "f32")),
     ("rmsnorm bf16 [16384,8192] stress, eps 1e-6", "rms", (16384, 8192, True, 1e-6)),
     ("rmsnorm bf16 [65536,8192]", "rms", (65536, 8192, False, 1e-5)),
     ("rmsnorm bf16 [65536,3000]", "rms", (65536, 3000, False, 1e-5)),
@@ -554,13 +556,17 @@ def _large_case(kind: str, shp: tuple, seed: int):
     The launch closure keeps its own tensors alive; `tensors` is returned so that the
     caller can hold them across graph capture and replay as well."""
     if kind == "rms":
-        rows, cols, stress, eps = shp
-        x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=seed, stress=stress, device="cuda")
+        rows, cols, stress, eps = shp[:4]
+        dt = shp[4] if len(shp) > 4 else "bf16"
+        x, w = inputs.rmsnorm_inputs(rows, cols, dt, seed=seed, stress=stress, device="cuda")
         y = torch.empty_like(x)
-        pname = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, "bf16"))
+        pname = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, dt))
+        if dt != "bf16":
+            pname = pname.replace("<bf16,", f"<{dt},")
+        code = camp.BF16 if dt == "bf16" else camp.F32
         fn = lambda st: camp.camp_rmsnorm(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, cols,
-                                          eps, camp.BF16, st)
-        return fn, ledger.rmsnorm_bytes(rows, cols), pname, (x, w, y)
+                                          eps, code, st)
+        return fn, ledger.rmsnorm_bytes(rows, cols, dt), pname, (x, w, y)
     if kind == "add":
         rows, cols = shp
         x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=seed, device="cuda")
@@ -687,11 +693,12 @@ def oracle_case(kind: str, tensors: tuple, shp: tuple, budget_bytes: int = 64 <<
     cores = oracle.threads_available(lib)
     if kind == "rms":
         x, w = tensors[0], tensors[1]
-        rows, cols, _, eps = shp
+        rows, cols, _, eps = shp[:4]
+        dt = shp[4] if len(shp) > 4 else "bf16"
         n = max(1, min(rows, budget_bytes // (cols * x.element_size())))
         xs, ws = inputs.to_numpy(x[:n]), inputs.to_numpy(w)
-        fn = lambda: oracle.rmsnorm(xs, ws, float(np.float32(eps)), "bf16", lib=lib)
-        nbytes, what = ledger.rmsnorm_bytes(n, cols), f"{n} of {rows} rows"
+        fn = lambda: oracle.rmsnorm(xs, ws, float(np.float32(eps)), dt, lib=lib)
+        nbytes, what = ledger.rmsnorm_bytes(n, cols, dt), f"{n} of {rows} rows"
         nrows = n
     elif kind == "rope":
         x, sn, cs = tensors[0], tensors[1], tensors[2]
