@@ -18,7 +18,8 @@
  *
  * Conventions shared by every entry point
  *   - The caller owns every buffer. The library allocates no memory, keeps no per-call
- *     state and has no workspace.
+ *     state and has no workspace; its only device state is one static status word that a
+ *     kernel sets if a bounded wait ever runs out (camp_device_errors).
  *   - Tensor pointers are DEVICE pointers (or managed memory) to contiguous row-major
  *     data. A pointer need only be aligned to its element size; better-aligned pointers
  *     (16 bytes) and row pitches that are multiples of 16 bytes take the vector path.
