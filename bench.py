@@ -114,6 +114,9 @@ def recorded_traffic(kernel_name: str):
 
 def plan_name(kind: str, p: camp.Plan) -> str:
     if kind == "layernorm":
+        if p.kernel == camp.KERNEL_LAYERNORM_STAGED:
+            return (f"layernorm_staged<bf16,cluster{p.cluster},chunk{p.group}vec,"
+                    f"stages{p.per_thread}>")
         return f"layernorm_rows<bf16,vec{p.vec_bytes},group{p.group},nv{p.per_thread}>"
     if kind == "rmsnorm":
         if p.kernel == camp.KERNEL_RMSNORM_STAGED:
@@ -538,6 +541,8 @@ LARGE_CASES = [
     ("layernorm bf16 [8192,4096]", "ln", (8192, 4096)),
     ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),
     ("layernorm bf16 [16384,8192]", "ln", (16384, 8192)),
+    ("layernorm bf16 [1024,65536] (staged in shared memory)", "ln", (1024, 65536)),
+    ("layernorm bf16 [256,131072] (staged in shared memory)", "ln", (256, 131072)),
     ("rope bf16 [1,65536,32,128]", "rope", (65536, 32, 128)),
     ("rope bf16 [1,65536,32,64]", "rope", (65536, 32, 64)),
     ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),

@@ -41,6 +41,7 @@ KERNEL_ROPE_INTERLEAVED = 8
 KERNEL_LAYERNORM_ROWS = 9
 KERNEL_KV_CAT = 10
 KERNEL_RMSNORM_STAGED = 11
+KERNEL_LAYERNORM_STAGED = 12
 
 DEVICE_ERROR_WAIT_TIMEOUT = 1
 

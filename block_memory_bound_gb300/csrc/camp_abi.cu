@@ -919,14 +919,58 @@ camp_status_t ln_validate(const void* x, const void* gamma, const void* beta, co
     return CAMP_SUCCESS;
 }
 
+// Staged LayerNorm: chunk vectors per CTA and whether the ring fits shared memory.
+bool ln_staged_fits(int64_t nvec, int cluster, int stages, int64_t* chunk) {
+    if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1)) != 0) return false;
+    if (stages < 2 || stages > camp::kStagedMaxStages) return false;
+    *chunk = ceil_div(nvec, cluster);
+    return *chunk <= static_cast<int64_t>(camp::kStagedMaxVecsPerThread) * camp::kStagedBlock &&
+           camp::ln_staged_smem_bytes(*chunk, stages) <= camp::kStagedSmemMax;
+}
+
+void ln_staged_plan_fields(const LnCall& c, int cluster, int stages, int64_t chunk,
+                           camp_plan_t* p) {
+    p->kernel = CAMP_KERNEL_LAYERNORM_STAGED;
+    p->vec_bytes = 16;
+    p->group = static_cast<int32_t>(chunk);
+    p->per_thread = stages;
+    p->block = camp::kStagedBlock;
+    p->cluster = cluster;
+    const int64_t per_sm = camp::kSmSmemBytes / (camp::ln_staged_smem_bytes(chunk, stages) + 1024);
+    int64_t clusters = (camp::kSmCount * (per_sm < 1 ? 1 : per_sm)) / cluster;
+    if (clusters < 1) clusters = 1;
+    if (clusters > c.rc.a.rows) clusters = c.rc.a.rows;
+    p->grid = clusters * cluster;
+}
+
+// Rows of more than kLnStagedFrom 16-byte vectors take the staged kernel, with the
+// RMSNorm staged kernel's cluster size (CTA chunks of about 1024 vectors) and 2 buffers:
+// LayerNorm also holds gamma and beta, and a third buffer costs more occupancy than it
+// hides. Measured on GB300 (L2-cold, graphs of back-to-back launches), staged against the
+// best register variant: bf16 2048 x 32768 0.69 / 0.67 of the measured HBM peak, 1024 x
+// 65536 0.62 / 0.55 (3 buffers: 0.50), fp32 2048 x 16384 0.84 / 0.79; at 2048 vectors
+// (bf16 4096 x 16384) the register kernel stays ahead, 0.86 / 0.72. Past 8192 vectors only
+// the staged kernel holds the row (512 x 131072: 0.54, 64 x 262144: 0.35).
+constexpr int64_t kLnStagedFrom = 2048;
+
 camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p) {
-    if (forced && forced->kernel != CAMP_KERNEL_LAYERNORM_ROWS) return CAMP_ERR_NOT_SUPPORTED;
+    if (forced && forced->kernel != CAMP_KERNEL_LAYERNORM_ROWS &&
+        forced->kernel != CAMP_KERNEL_LAYERNORM_STAGED)
+        return CAMP_ERR_NOT_SUPPORTED;
     const RmsCall& rc = c.rc;
     const int es = camp::elem_bytes(rc.t);
     const int widest = (rms_vec_bytes(rc) == 16 && aligned(c.beta, 16)) ? 16 : es;
     *p = camp_plan_t{};
     p->kernel = CAMP_KERNEL_LAYERNORM_ROWS;
     p->cluster = 1;
+    const int64_t nvec16 = rc.a.cols * es / 16;
+    if (forced && forced->kernel == CAMP_KERNEL_LAYERNORM_STAGED) {
+        int64_t chunk = 0;
+        if (widest != 16 || !ln_staged_fits(nvec16, forced->cluster, forced->per_thread, &chunk))
+            return CAMP_ERR_NOT_SUPPORTED;
+        ln_staged_plan_fields(c, forced->cluster, forced->per_thread, chunk, p);
+        return CAMP_SUCCESS;
+    }
     if (forced) {
         p->vec_bytes = forced->vec_bytes;
         p->group = forced->group;
@@ -938,6 +982,15 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
         const int64_t nvec = rc.a.cols * es / p->vec_bytes;
         if (static_cast<int64_t>(p->group) * p->per_thread < nvec) return CAMP_ERR_NOT_SUPPORTED;
     } else {
+        if (widest == 16 && nvec16 > kLnStagedFrom) {
+            int cl = 0, st = 0;
+            int64_t chunk = 0;
+            if (rms_choose_staged(rc, nvec16, &cl, &st, &chunk) &&
+                ln_staged_fits(nvec16, cl, (st = 2), &chunk)) {
+                ln_staged_plan_fields(c, cl, st, chunk, p);
+                return CAMP_SUCCESS;
+            }
+        }
         p->vec_bytes = widest;
         int g = 0, nv = 0;
         if (!rms_choose_rows(rc, widest, &g, &nv, true)) return CAMP_ERR_NOT_SUPPORTED;
@@ -968,9 +1021,10 @@ CAMP_API int camp_last_cuda_error(void) { return g_last_cuda_error; }
 
 CAMP_API camp_status_t camp_device_errors(uint32_t* flags, int clear) {
     if (flags == nullptr) return CAMP_ERR_INVALID_ARG;
-    unsigned int v = 0;
-    const camp_status_t st = runtime_status(camp::read_device_errors(&v, clear != 0));
-    *flags = st == CAMP_SUCCESS ? v : 0u;
+    unsigned int a = 0, b = 0;
+    camp_status_t st = runtime_status(camp::read_device_errors(&a, clear != 0));
+    if (st == CAMP_SUCCESS) st = runtime_status(camp::read_layernorm_device_errors(&b, clear != 0));
+    *flags = st == CAMP_SUCCESS ? (a | b) : 0u;
     return st;
 }
 
@@ -1231,6 +1285,9 @@ CAMP_API camp_status_t camp_layernorm_with_plan(const void* x, const void* gamma
     st = ln_plan(c, plan, &p);
     if (st != CAMP_SUCCESS) return st;
     const camp::LayernormArgs a{x, gamma, c.beta, y, rows, cols, eps};
+    if (p.kernel == CAMP_KERNEL_LAYERNORM_STAGED)
+        return runtime_status(camp::layernorm_staged_launch(c.rc.t, p.cluster, p.per_thread, a,
+                                                            static_cast<cudaStream_t>(stream)));
     return runtime_status(camp::layernorm_rows_launch(c.rc.t, p.vec_bytes, p.group,
                                                       p.per_thread, a, p.grid,
                                                       static_cast<cudaStream_t>(stream)));

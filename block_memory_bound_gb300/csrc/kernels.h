@@ -129,9 +129,11 @@ inline int64_t staged_smem_bytes(bool add, int64_t chunk_vecs, int stages) {
 cudaError_t rmsnorm_staged_launch(bool add, DType t, int cluster, int stages,
                                   const RmsnormArgs& a, cudaStream_t s);
 
-// The library's device error word: kernels whose bounded waits ran out set bits in it.
+// The library's device error words (one per translation unit with bounded waits): kernels
+// whose bounded waits ran out set bits in them; camp_device_errors reports their union.
 constexpr unsigned int kDeviceErrorWaitTimeout = 1u;
-cudaError_t read_device_errors(unsigned int* flags, bool clear);
+cudaError_t read_device_errors(unsigned int* flags, bool clear);            // staged RMSNorm
+cudaError_t read_layernorm_device_errors(unsigned int* flags, bool clear);  // staged LayerNorm
 
 // The add-path tables live in their own translation unit (compiled in parallel).
 namespace add_path {
@@ -181,6 +183,15 @@ struct LayernormArgs {
 
 cudaError_t layernorm_rows_launch(DType t, int vec_bytes, int group, int per_thread,
                                   const LayernormArgs& a, int64_t grid, cudaStream_t s);
+
+// Staged LayerNorm (layernorm_staged.cu): the staged RMSNorm kernel's persistent clusters,
+// with gamma and beta chunks held in shared memory and each row buffer carrying the row's
+// first 16 bytes (the shift) ahead of the CTA's chunk.
+inline int64_t ln_staged_smem_bytes(int64_t chunk_vecs, int stages) {
+    return 2 * chunk_vecs * 16 + stages * (16 + chunk_vecs * 16);
+}
+cudaError_t layernorm_staged_launch(DType t, int cluster, int stages, const LayernormArgs& a,
+                                    cudaStream_t s);
 
 // ------------------------------------------------------------------ interleaved RoPE
 // x [tokens, heads, dim], pairs (2i, 2i+1); table row positions[token] of [max_pos, dim/2].

@@ -1,0 +1,100 @@
+// Device building blocks of the shared-memory-staged kernels (rmsnorm_staged.cu,
+// layernorm_staged.cu): mbarriers with bounded waits, bulk asynchronous copies from global
+// into shared memory, st.async stores into a cluster peer's shared memory, 16-byte shared
+// memory accesses.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+// Each translation unit that uses these keeps its own device error word (device variables
+// do not link across translation units in this build) and reports it through a host function
+// that camp_device_errors combines.
+
+namespace camp {
+namespace staged {
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase of `bar` with this parity to complete; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_test(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// Bulk asynchronous copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// The shared::cluster address of this CTA's shared variable at `addr` in cluster rank `rank`.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Store v into a (possibly remote) CTA's shared memory; the write is counted, in bytes, on
+// that CTA's mbarrier `bar` (both shared::cluster addresses).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 ::"r"(addr), "r"(__float_as_uint(v)), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ Raw<16> ld_smem16(const unsigned char* p) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    Raw<16> r;
+    r.w[0] = q.x;
+    r.w[1] = q.y;
+    r.w[2] = q.z;
+    r.w[3] = q.w;
+    return r;
+}
+
+__device__ __forceinline__ void st_smem16(unsigned char* p, const Raw<16>& r) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]);
+}
+
+}  // namespace staged
+}  // namespace camp

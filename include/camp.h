@@ -275,9 +275,12 @@ CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos,
  * The row is held in registers (camp_rmsnorm's rows kernel layout: x read once, y written
  * once) and the statistics are taken in two passes over the registers, in fp32: with
  * K = x[row, 0], mu = sum(x - K) / n and d = (x - K) - mu, var = sum(d^2) / n and
- * y = fma(d * rsqrt(var + eps), gamma, beta), rounded once to the storage type. Rows up to 1024 threads x 8 16-byte accesses (65536
- * bf16 / 32768 fp32 columns; 16384 columns on the element path); wider rows return
- * CAMP_ERR_NOT_SUPPORTED. Errors otherwise as for camp_rmsnorm.
+ * y = fma(d * rsqrt(var + eps), gamma, beta), rounded once to the storage type. Rows of
+ * more than 4096 16-byte vectors (32768 bf16 / 16384 fp32 columns; all pointers and the row
+ * pitch 16-byte aligned) are staged in shared memory by persistent clusters of CTAs instead
+ * (up to 16 x 2048 vectors: 262144 bf16 / 131072 fp32 columns). Wider rows, and rows past
+ * 16384 columns on the element path, return CAMP_ERR_NOT_SUPPORTED. Errors otherwise as for
+ * camp_rmsnorm.
  */
 CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const void* beta,
                                       void* y, int64_t rows, int64_t cols, float eps,
@@ -320,8 +323,9 @@ typedef enum {
     CAMP_KERNEL_ROPE_INTERLEAVED = 8, /* camp_rope_interleaved: tiled like CAMP_KERNEL_ROPE */
     CAMP_KERNEL_LAYERNORM_ROWS = 9, /* camp_layernorm: a group of threads per row, registers */
     CAMP_KERNEL_KV_CAT = 10,        /* camp_kv_cat_repeat: tiled like CAMP_KERNEL_ROPE */
-    CAMP_KERNEL_RMSNORM_STAGED = 11 /* persistent clusters, rows staged in shared memory by
-                                       bulk asynchronous copies, `per_thread` buffers deep */
+    CAMP_KERNEL_RMSNORM_STAGED = 11, /* persistent clusters, rows staged in shared memory by
+                                        bulk asynchronous copies, `per_thread` buffers deep */
+    CAMP_KERNEL_LAYERNORM_STAGED = 12 /* camp_layernorm: the same, for rows past 4096 vectors */
 } camp_kernel_t;
 
 typedef struct {

@@ -527,8 +527,8 @@ def test_layernorm_empty_and_in_place(lib):
 
 @pytest.mark.parametrize("rows,cols,dtype", [
     (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"),
-    (1, 8, "bf16"), (64, 3001, "bf16"), (4096, 12288, "bf16"), (1024, 32768, "bf16"),
-    (3, 16384, "f32"), (4096, 1024, "bf16"),
+    (1, 8, "bf16"), (64, 3001, "bf16"), (4096, 12288, "bf16"), (4096, 16384, "bf16"),
+    (3, 8192, "f32"), (4096, 1024, "bf16"),
 ])
 def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype):
     # the same register-resident row mapping as RMSNorm: where neither the one-wave test
@@ -541,14 +541,38 @@ def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype)
         (q.vec_bytes, q.group, q.per_thread, q.block, q.grid, 1)
 
 
-def test_layernorm_keeps_its_rows_kernel_where_rmsnorm_stages_the_row(lib):
-    # RMSNorm stages rows past 4096 vectors; LayerNorm has no staged kernel and keeps one
-    # CTA of up to 1024 threads per row (up to 8192 vectors)
-    for rows, cols, dtype, g in ((5, 65536, "bf16", 1024), (7, 32768, "f32", 1024)):
-        assert camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype).kernel == \
-            camp.KERNEL_RMSNORM_STAGED
+def test_layernorm_stages_rows_past_2048_vectors(lib):
+    # past 4096 vectors both operators stage the row in shared memory with the same cluster
+    # size; LayerNorm keeps 2 buffers (it also holds gamma and beta, and each buffer carries
+    # the row's first 16 bytes) and starts staging at 2048 vectors
+    for rows, cols, dtype in ((5, 65536, "bf16"), (7, 32768, "f32"), (64, 262144, "bf16"),
+                              (3, 40000, "bf16")):
+        q = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype)
         p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
-        assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, g, 8)
+        assert q.kernel == camp.KERNEL_RMSNORM_STAGED
+        assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
+        assert (p.vec_bytes, p.group, p.cluster, p.block, p.per_thread) == \
+            (q.vec_bytes, q.group, q.cluster, q.block, 2)
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 32768, "bf16")   # 4096 vectors
+    assert (p.kernel, p.cluster, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_STAGED, 4, 1024, 2)
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 16384, "bf16")   # 2048 vectors: rows
+    assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, 256, 8)
+
+
+def test_layernorm_staged_plans_that_do_not_fit_are_refused(lib):
+    # only refusals (an accepted plan would launch)
+    for cols, dt, cl, stg in ((262144, camp.BF16, 8, 2),    # 4096 vectors a CTA
+                              (131072, camp.BF16, 16, 5),   # 5 buffers are not built
+                              (65536, camp.BF16, 3, 2)):    # cluster not a power of two
+        plan = camp.Plan(kernel=camp.KERNEL_LAYERNORM_STAGED, vec_bytes=16, cluster=cl,
+                         per_thread=stg)
+        st = lib.camp_layernorm_with_plan(X, W, BETA, Y, 2, cols, ctypes.c_float(1e-5), dt,
+                                          ctypes.byref(plan), None)
+        assert st == camp.ERR_NOT_SUPPORTED, (cols, cl, stg)
+    plan = camp.Plan(kernel=camp.KERNEL_LAYERNORM_STAGED, vec_bytes=16, cluster=4, per_thread=2)
+    st = lib.camp_layernorm_with_plan(X, W, BETA + 2, Y, 2, 65536, ctypes.c_float(1e-5),
+                                      camp.BF16, ctypes.byref(plan), None)
+    assert st == camp.ERR_NOT_SUPPORTED   # beta not 16-byte aligned
 
 
 @pytest.mark.parametrize("rows,cols,expect", [
@@ -574,12 +598,14 @@ def test_layernorm_one_wave_test_uses_its_own_occupancy(lib):
     assert (q.group, q.per_thread, q.grid) == (64, 4, 1024)
 
 
-def test_layernorm_rows_that_do_not_fit_one_group_are_refused(lib):
-    # 1024 threads x 8 sixteen-byte accesses hold 65536 bf16 / 32768 fp32 elements; the
-    # element path holds 1024 x 16
-    for cols, dtype, b in ((65544, "bf16", BETA), (32772, "f32", BETA), (16385, "bf16", BETA + 2)):
+def test_layernorm_rows_that_do_not_fit_are_refused(lib):
+    # the staged kernel holds up to 16 x 2048 sixteen-byte vectors (262144 bf16 / 131072
+    # fp32 elements); the element path holds 1024 x 16 elements
+    for cols, dtype, b in ((262152, "bf16", BETA), (131076, "f32", BETA), (16385, "bf16", BETA + 2)):
         with pytest.raises(camp.CampError):
             camp.camp_layernorm_plan(X, W, b, Y, 4, cols, dtype)
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 65544, "bf16")   # staged now
+    assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
 
 
 def test_layernorm_misaligned_beta_uses_element_accesses(lib):

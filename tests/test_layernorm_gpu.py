@@ -65,7 +65,13 @@ def _canaries_ok(buf, n):
 def check(got: torch.Tensor, x_cpu, g_cpu, b_cpu, eps32: float, plan: camp.Plan, what: str):
     rows, cols = x_cpu.shape
     es = 2 if x_cpu.dtype == torch.bfloat16 else 4
-    k = plan.per_thread * (plan.vec_bytes // es) + 5 + plan.group // 32
+    if plan.kernel == camp.KERNEL_LAYERNORM_STAGED:
+        # a thread's vectors (its share of the CTA chunk), the warp butterfly, the CTA's 8
+        # warp partials, the cluster's partials
+        per_thread = -(-plan.group // 256)
+        k = per_thread * (16 // es) + 5 + 8 + plan.cluster
+    else:
+        k = plan.per_thread * (plan.vec_bytes // es) + 5 + plan.group // 32
     g, b = _decode(g_cpu), _decode(b_cpu)
     step = max(1, (1 << 22) // cols)
     for r0 in range(0, rows, step):
