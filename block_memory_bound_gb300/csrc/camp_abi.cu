@@ -172,10 +172,24 @@ struct RowsCandidate {
 // wins (bf16, 64 x 4 against 128 x 2: 65536 x 2048 80.5 / 90.9 us, 8192 x 2048 14.3 /
 // 14.5 us; 8192 x 4096: 128 x 4 24.2 us, 256 x 2 24.6 us); closer to one wave the RMSNorm
 // order holds (4096 x 2048: 128 x 2 9.0 us, 64 x 4 in 1.1 waves 10.2 us).
-bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm) {
+// At decode sizes (no more rows than SMs) a launch is latency-bound, not bandwidth-bound,
+// and after 1. the rule is: groups of at most 512 threads, the fewest accesses per thread
+// (the shortest serial chain of loads and arithmetic), the fewest idle slots, the smaller
+// group. Measured on GB300 (bf16, graphs of back-to-back launches): 1 x 8192 512 x 2
+// 1.97 us against 256 x 4 2.22 us, 1 x 3000 512 x 1 1.70 against 128 x 3 1.94, 8 x 8192
+// 512 x 2 2.05 against 2.21, 64 x 8192 2.07 against 2.32; 1 x 2048 256 x 1 1.52.
+bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm,
+                 bool latency) {
     const int64_t sa = a.ctas < camp::kSmCount ? a.ctas : camp::kSmCount;
     const int64_t sb = b.ctas < camp::kSmCount ? b.ctas : camp::kSmCount;
     if (sa != sb) return sa > sb;
+    if (latency) {
+        const bool la = a.group <= 512, lb = b.group <= 512;
+        if (la != lb) return la;
+        if (a.per_thread != b.per_thread) return a.per_thread < b.per_thread;
+        if (a.idle != b.idle) return a.idle < b.idle;
+        return a.group < b.group;
+    }
     const bool ma = a.per_thread >= 2 && a.per_thread <= 4 && a.group <= 256;
     const bool mb = b.per_thread >= 2 && b.per_thread <= 4 && b.group <= 256;
     if (ma != mb) return ma;
@@ -220,7 +234,7 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread,
                       : camp::rows_min_blocks(vb, g, c.add ? 2 * k.per_thread : k.per_thread);
         k.one_wave = k.ctas <= static_cast<int64_t>(camp::kSmCount) * per_sm;
         k.many_waves = k.ctas >= 2 * static_cast<int64_t>(camp::kSmCount) * per_sm;
-        if (!found || rows_better(k, best, layernorm)) best = k;
+        if (!found || rows_better(k, best, layernorm, c.a.rows <= camp::kSmCount)) best = k;
         found = true;
     }
     if (!found) return false;

@@ -132,8 +132,13 @@ def test_rope_empty_is_success_without_cuda(lib):
     (16384, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 16384)),
     # 375 vectors a row: 128 x 3 leaves 9 slots idle, 256 x 2 leaves 137
     (4096, 3000, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 128, 3, 256, 2048)),
-    # 64 rows: one row per CTA reaches the most SMs
-    (64, 2048, "f32", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 2, 256, 64)),
+    # 64 rows: one row per CTA reaches the most SMs; with no more rows than SMs the launch
+    # is latency-bound: the fewest accesses per thread in a group of at most 512 threads
+    (64, 2048, "f32", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 1, 512, 64)),
+    (1, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 2, 512, 1)),
+    (8, 3000, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 1, 512, 8)),
+    (152, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 1, 256, 152)),
+    (153, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 153)),   # past the SMs
     (1, 8, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 32, 1, 256, 1)),
     (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 256, 16, 256, 64)),
     # wider rows: one CTA of up to 1024 threads while it holds the row (8192 vectors)...
@@ -556,7 +561,7 @@ def test_layernorm_stages_rows_past_2048_vectors(lib):
     p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 32768, "bf16")   # 4096 vectors
     assert (p.kernel, p.cluster, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_STAGED, 4, 1024, 2)
     p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 16384, "bf16")   # 2048 vectors: rows
-    assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, 256, 8)
+    assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, 512, 4)
 
 
 def test_layernorm_staged_plans_that_do_not_fit_are_refused(lib):
