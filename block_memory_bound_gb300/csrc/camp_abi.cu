@@ -553,9 +553,42 @@ RopeCall rope_first(const RopeCall& c) {
 // count takes the largest of 4, 2, 1 that divides every head count. The tiled kernel runs
 // when a position fits one CTA; otherwise one tensor takes the flat kernel and two
 // tensors are split into two single-tensor launches.
+// Decode sizes (no more positions than SMs) are latency-bound: the tiled variant with the
+// most threads per position (up to one CTA), then the widest access, then the fewest heads
+// per thread. Measured on GB300 (bf16, graphs of back-to-back launches), against the
+// bandwidth choice (16-byte accesses, 2 heads per thread): 8 positions x 32 heads x 64
+// 1.41 / 1.81 us, 64 x 8 x 64 1.39 / 1.81, 8 x 8 x 128 1.29 / 1.79, Q+K 8 x (32 + 8) x 64
+// 1.53 / 1.80; from 512 positions on the bandwidth choice is as fast or faster.
+bool rope_plan_latency(const RopeCall& c, camp_plan_t* p) {
+    const int es = camp::elem_bytes(c.t);
+    int64_t best = 0;
+    for (int vb : {16, 8, 4}) {
+        if (vb < 2 * es || !rope_vec_ok(c, vb)) continue;
+        for (int hpt : {1, 2, 4, 8}) {
+            if (!camp::rope_compiled(c.t, vb, hpt) || rope_positions_per_cta(c, vb, hpt) == 0)
+                continue;
+            const int64_t per_pos =
+                (ceil_div(c.a.heads, hpt) + ceil_div(c.a.heads2, hpt)) * (c.a.half * es / vb);
+            if (per_pos > best) {   // ties keep the wider access / fewer heads seen first
+                best = per_pos;
+                p->vec_bytes = vb;
+                p->group = hpt;
+            }
+        }
+    }
+    return best > 0;
+}
+
 void rope_plan(const RopeCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
     p->cluster = 1;
+    if (c.a.tokens <= camp::kSmCount && rope_plan_latency(c, p)) {
+        p->kernel = CAMP_KERNEL_ROPE;
+        p->per_thread = 0;
+        p->block = camp::kRopeBlock;
+        p->grid = rope_grid(c, CAMP_KERNEL_ROPE, p->vec_bytes, p->group);
+        return;
+    }
     p->vec_bytes = rope_widest_vec(c);
     const bool by4 = c.a.heads % 4 == 0 && c.a.heads2 % 4 == 0;
     const bool by2 = c.a.heads % 2 == 0 && c.a.heads2 % 2 == 0;

@@ -181,8 +181,14 @@ def test_rmsnorm_plan_misaligned_pointer_uses_element_accesses(lib):
     (1, 65536, 6, 128, "bf16", (camp.KERNEL_ROPE, 16, 2, 6554)),
     # odd head count: 1 head per thread
     (2, 3, 5, 6, "bf16", (camp.KERNEL_ROPE, 2, 1, 1)),
-    (1, 4, 6, 12, "bf16", (camp.KERNEL_ROPE, 4, 2, 1)),
-    (1, 4, 6, 24, "f32", (camp.KERNEL_ROPE, 16, 2, 1)),
+    # no more positions than SMs: the most threads per position (narrow accesses, 1 head
+    # per thread), accesses of at least one pair
+    (1, 4, 6, 12, "bf16", (camp.KERNEL_ROPE, 4, 1, 1)),
+    (1, 4, 6, 24, "f32", (camp.KERNEL_ROPE, 8, 1, 1)),
+    (1, 8, 32, 64, "bf16", (camp.KERNEL_ROPE, 8, 1, 8)),        # 256 threads a position
+    (1, 64, 8, 128, "bf16", (camp.KERNEL_ROPE, 4, 1, 64)),
+    (1, 152, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 1, 152)),
+    (1, 153, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 2, 77)),   # past the SMs
     # a position needs more than one CTA: the flat kernel
     (1, 4, 1024, 256, "bf16", (camp.KERNEL_ROPE_FLAT, 16, 2, 128)),
 ])
@@ -298,9 +304,10 @@ def test_rope_qk_empty_and_single_tensor_calls_need_no_cuda(lib):
     (1, 4096, 32, 8, 64, (camp.KERNEL_ROPE, 16, 2, 1366)),
     (2, 128, 14, 2, 128, (camp.KERNEL_ROPE, 16, 2, 64)),
     (1, 65536, 32, 8, 128, (camp.KERNEL_ROPE, 16, 4, 21846)),
-    (1, 16, 3, 1, 64, (camp.KERNEL_ROPE, 16, 1, 1)),
-    # the heads of a position do not fit one CTA: two launches
-    (1, 4, 1024, 8, 256, (camp.KERNEL_ROPE_SPLIT, 16, 2, 129)),
+    (1, 16, 3, 1, 64, (camp.KERNEL_ROPE, 4, 1, 4)),         # decode size: 64 threads a position
+    (1, 8, 32, 8, 64, (camp.KERNEL_ROPE, 16, 1, 8)),         # 160 threads: the widest of 3 ties
+    # the heads of a position do not fit one CTA: two launches (K alone takes the decode rule)
+    (1, 4, 1024, 8, 256, (camp.KERNEL_ROPE_SPLIT, 16, 2, 132)),
 ])
 def test_rope_qk_plans(lib, B, S, Hq, Hk, D, expect):
     p = camp.camp_rope_qk_plan(X, K_, SIN, COS, YQ, YK, B, S, Hq, Hk, D, "bf16")
