@@ -830,6 +830,25 @@ camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_
         p->vec_bytes = forced->vec_bytes;
         p->group = forced->group;
         if (!rope_il_vec_ok(c, p->vec_bytes)) return CAMP_ERR_NOT_SUPPORTED;
+    } else if (c.a.tokens <= camp::kSmCount) {
+        // Decode sizes: the most threads per token within one CTA, then the widest access,
+        // then the fewest heads per thread (the rotate-half planner's latency rule).
+        int64_t best = 0;
+        const int es = camp::elem_bytes(c.t);
+        for (int vb : {16, 8, 4}) {
+            if (!rope_il_vec_ok(c, vb)) continue;
+            for (int hpt : {1, 2, 4, 8}) {
+                if (!camp::rope_interleaved_compiled(c.t, vb, hpt) || rope_il_tpc(c, vb, hpt) == 0)
+                    continue;
+                const int64_t per_tok = ceil_div(c.a.heads, hpt) * (c.a.dim * es / vb);
+                if (per_tok > best) {
+                    best = per_tok;
+                    p->vec_bytes = vb;
+                    p->group = hpt;
+                }
+            }
+        }
+        if (best == 0) return CAMP_ERR_NOT_SUPPORTED;
     } else {
         for (int vb : {16, 8, 4}) {
             if (rope_il_vec_ok(c, vb)) { p->vec_bytes = vb; break; }

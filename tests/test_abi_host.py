@@ -485,14 +485,21 @@ def test_rope_interleaved_plans(lib):
     # 32 heads of 128: 4 heads a thread, 8 x 16 = 128 threads a token, 2 tokens a CTA
     p = camp.camp_rope_interleaved_plan(*ILP, 65536, 32, 128, 131072, "bf16")
     assert (p.kernel, p.vec_bytes, p.group, p.grid) == (camp.KERNEL_ROPE_INTERLEAVED, 16, 4, 32768)
-    p = camp.camp_rope_interleaved_plan(*ILP, 16, 5, 6, 16, "bf16")       # odd head count
-    assert (p.vec_bytes, p.group, p.grid) == (4, 1, 1)
-    p = camp.camp_rope_interleaved_plan(*ILP, 16, 6, 64, 16, "bf16")      # even, not 4k
+    p = camp.camp_rope_interleaved_plan(*ILP, 1000, 5, 6, 16, "bf16")     # odd head count
+    assert (p.vec_bytes, p.group, p.grid) == (4, 1, 59)
+    p = camp.camp_rope_interleaved_plan(*ILP, 1000, 6, 64, 16, "bf16")    # even, not 4k
     assert p.group == 2
-    p = camp.camp_rope_interleaved_plan(*ILP, 16, 64, 128, 16, "bf16")    # 4 heads: 256 threads
+    p = camp.camp_rope_interleaved_plan(*ILP, 1000, 64, 128, 16, "bf16")  # 4 heads: 256 threads
     assert p.group == 4
-    p = camp.camp_rope_interleaved_plan(*ILP, 16, 128, 128, 16, "bf16")   # 4 heads: 512 threads
+    p = camp.camp_rope_interleaved_plan(*ILP, 1000, 128, 128, 16, "bf16")  # 4 heads: 512 threads
     assert p.group == 8
+    # decode sizes (no more tokens than SMs): the most threads a token within one CTA
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 6, 64, 16, "bf16")      # 6 x 32 = 192
+    assert (p.vec_bytes, p.group, p.grid) == (4, 1, 16)
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 32, 128, 16, "bf16")    # 16 x 16 = 256
+    assert (p.vec_bytes, p.group, p.grid) == (16, 2, 16)
+    p = camp.camp_rope_interleaved_plan(*ILP, 16, 128, 128, 16, "bf16")   # 16 x 16 = 256
+    assert (p.vec_bytes, p.group, p.grid) == (16, 8, 16)
 
 
 def test_rope_tables_argument_errors(lib):
