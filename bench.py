@@ -22,11 +22,18 @@ launch duration is its summed graph time / K. nvidia-smi samples the SM clock an
 throttle reasons during the timed region.
 
 ``e2e`` is the same metric through the C ABI with host buffers: every step copies its
-inputs from pinned host memory, runs the two kernels and copies the outputs back.
+inputs (one packed slab) from pinned host memory, runs the two kernels and copies the
+outputs (one packed slab) back, double-buffered on three streams (``e2e.serial``: the same
+on one stream).
+
+``large_configs`` and ``sweep`` time each operator alone at the large shapes and at every
+shape of the token x hidden / heads x head_dim sweep, as graphs of back-to-back launches
+over rotating input sets (GB/s, fraction of the peak, rows/s).
 
 ``cpu_baseline`` times the fp64 oracle (test infrastructure, as it stands) on the host
-cores on whole steps of the same workload. ``--impl reference`` prints the reference arm's
-line instead: that oracle, timed on a bounded sample of the workload per step.
+cores on whole steps of the same workload, and on a bounded sample of each RMSNorm and
+RoPE configuration. ``--impl reference`` prints the reference arm's line instead: that
+oracle, timed on a bounded sample of the workload per step.
 
 Multi-GPU (under torchrun): every rank runs an independent replica of the workload (the
 rows are independent; there is no exchange step), so scaling is weak and ``value`` sums

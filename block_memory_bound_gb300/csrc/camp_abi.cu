@@ -243,13 +243,13 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread,
     return true;
 }
 
-// Cluster split of one row: the smallest power-of-two cluster (2..16 CTAs of 256 threads)
-// whose CTAs hold the row with at most 8 accesses per thread (measured: 256 rows of 131072
-// bf16 run 29.6 us as 8 x 8 and 31.3 us as 16 x 4). Used for rows of more than
-// kClusterFrom 16-byte vectors, which no single CTA holds in registers; up to that width
-// one CTA of 256..1024 threads measured as fast as or faster than a cluster, which is
-// gang-scheduled and pays a cluster barrier. False if even 16 x 256 x 8 vectors cannot
-// hold the row (the two-sweep kernel takes it).
+// Cluster split of one row (register cluster kernel): the smallest power-of-two cluster
+// (2..16 CTAs of 256 threads) whose CTAs hold the row with at most 8 accesses per thread
+// (measured: 256 rows of 131072 bf16 run 29.6 us as 8 x 8 and 31.3 us as 16 x 4). The
+// planner reaches it only for rows past kClusterFrom vectors that the staged kernel cannot
+// hold; with today's limits (both 16 x 2048 vectors) that never happens, so it runs through
+// explicit plans (the staged kernel replaced it: 0.67 -> 0.76 at 256 x 131072). False if
+// even 16 x 256 x 8 vectors cannot hold the row (the two-sweep kernel takes it).
 constexpr int64_t kClusterFrom = 8192;
 
 bool rms_choose_cluster(const RmsCall& c, int64_t nvec, int* cluster, int* per_thread) {

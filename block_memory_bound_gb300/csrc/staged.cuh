@@ -1,7 +1,7 @@
 // Device building blocks of the shared-memory-staged kernels (rmsnorm_staged.cu,
 // layernorm_staged.cu): mbarriers with bounded waits, bulk asynchronous copies from global
 // into shared memory, st.async stores into a cluster peer's shared memory, 16-byte shared
-// memory accesses.
+// memory loads.
 #pragma once
 
 #include "common.cuh"
@@ -90,10 +90,6 @@ __device__ __forceinline__ Raw<16> ld_smem16(const unsigned char* p) {
     r.w[2] = q.z;
     r.w[3] = q.w;
     return r;
-}
-
-__device__ __forceinline__ void st_smem16(unsigned char* p, const Raw<16>& r) {
-    *reinterpret_cast<uint4*>(p) = make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]);
 }
 
 }  // namespace staged
