@@ -8,7 +8,7 @@ product package.
 The arithmetic lives in ``camp_oracle.cpp`` (see its header for the definitions and the
 passages they follow). This file only compiles that source with the host C++ compiler
 and marshals numpy arrays through ctypes. bf16 arrays are passed as ``numpy.uint16`` bit
-patterns, fp32 arrays as ``numpy.float32``.
+patterns, fp16 arrays as ``numpy.float16``, fp32 arrays as ``numpy.float32``.
 """
 
 from __future__ import annotations
@@ -25,6 +25,7 @@ SOURCE = os.path.join(_HERE, "camp_oracle.cpp")
 LIBRARY = os.path.join(_HERE, "libcamp_oracle.so")
 
 # Storage-type codes understood by the oracle's C entry points.
+F16 = 0
 F32 = 1
 BF16 = 3
 
@@ -54,6 +55,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_bf16_round.restype = ctypes.c_uint16
     lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_value.restype = dbl
+    lib.oracle_f16_round.argtypes = [dbl]
+    lib.oracle_f16_round.restype = ctypes.c_uint16
+    lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_value.restype = dbl
     lib.oracle_threads_available.argtypes = []
     lib.oracle_threads_available.restype = c_int
     lib.oracle_rmsnorm_f64.argtypes = [vp, vp, vp, i64, i64, dbl]
@@ -102,6 +107,8 @@ def _storage(dtype: str) -> tuple[int, type]:
         return BF16, np.uint16
     if dtype == "f32":
         return F32, np.float32
+    if dtype == "f16":
+        return F16, np.float16
     raise ValueError(f"unknown storage type {dtype!r}")
 
 
@@ -128,6 +135,24 @@ def bf16_value(bits, lib: ctypes.CDLL | None = None) -> np.ndarray:
     lib = lib or load()
     b = np.asarray(bits, dtype=np.uint16).ravel()
     out = np.fromiter((lib.oracle_bf16_value(int(t)) for t in b), dtype=np.float64,
+                      count=b.size)
+    return out.reshape(np.shape(bits))
+
+
+def f16_round(values, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """fp64 values -> IEEE binary16 bit patterns, rounded once to nearest, ties to even."""
+    lib = lib or load()
+    v = np.asarray(values, dtype=np.float64).ravel()
+    out = np.fromiter((lib.oracle_f16_round(float(t)) for t in v), dtype=np.uint16,
+                      count=v.size)
+    return out.reshape(np.shape(values))
+
+
+def f16_value(bits, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """binary16 bit patterns -> their exact values as fp64."""
+    lib = lib or load()
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    out = np.fromiter((lib.oracle_f16_value(int(t)) for t in b), dtype=np.float64,
                       count=b.size)
     return out.reshape(np.shape(bits))
 

@@ -37,9 +37,11 @@
 //       y[b,s,h,i+D/2]   = x[b,s,h,i+D/2] * c + x[b,s,h,i] * sn
 //       then one rounding to the storage type.
 //
-// Storage types: fp32 (IEEE binary32) and bf16 (the upper 16 bits of a binary32:
-// 1 sign, 8 exponent, 7 fraction bits). Decoding either to fp64 is exact. Encoding
-// rounds to nearest, ties to even (the pages are silent; this is the IEEE default).
+// Storage types: fp32 (IEEE binary32), bf16 (the upper 16 bits of a binary32: 1 sign,
+// 8 exponent, 7 fraction bits) and fp16 (IEEE binary16: 1 sign, 5 exponent, 10 fraction
+// bits; the Intro-ops runtime's F16, code 0). Decoding any of them to fp64 is exact.
+// Encoding rounds to nearest, ties to even (the pages are silent; this is the IEEE
+// default).
 //
 //   LayerNorm  (xserv "phase 4", csrc/normalization/layernorm.cu: y = gamma * (x - mean) /
 //            sqrt(var + eps) + beta, population variance)
@@ -73,8 +75,13 @@
 
 namespace {
 
+constexpr int kOracleF16 = 0;
 constexpr int kOracleF32 = 1;
 constexpr int kOracleBF16 = 3;
+
+bool storage_ok(int dtype) {
+    return dtype == kOracleF16 || dtype == kOracleF32 || dtype == kOracleBF16;
+}
 
 // ---------------------------------------------------------------- storage formats
 
@@ -112,8 +119,49 @@ uint16_t double_to_bf16(double v) {
     return static_cast<uint16_t>(sign | (u >> 16));
 }
 
+// IEEE binary16: sign, 5 exponent bits (bias 15), 10 fraction bits. Normal values are
+// (1024 + f) * 2^(e - 25) for exponent field e in [1, 30]; subnormals f * 2^-24.
+double f16_to_double(uint16_t bits) {
+    const double sign = (bits & 0x8000u) ? -1.0 : 1.0;
+    const int e = (bits >> 10) & 0x1F;
+    const int f = bits & 0x3FF;
+    if (e == 31) return f ? std::nan("") : sign * INFINITY;
+    if (e == 0) return sign * std::ldexp(static_cast<double>(f), -24);
+    return sign * std::ldexp(static_cast<double>(1024 + f), e - 25);
+}
+
+// Round an fp64 value to the nearest binary16, ties to even, in one rounding. Finite
+// magnitudes are m * 2^(E-10) with integer m in [1024, 2047] for E in [-14, 15], plus the
+// subnormals m * 2^-24, m in [0, 1023]; from 65520 (the tie above 65504) on: infinity.
+uint16_t double_to_f16(double v) {
+    const uint16_t sign = std::signbit(v) ? 0x8000u : 0x0000u;
+    if (std::isnan(v)) return static_cast<uint16_t>(sign | 0x7E00u);
+    const double a = std::fabs(v);
+    if (std::isinf(a)) return static_cast<uint16_t>(sign | 0x7C00u);
+    if (a == 0.0) return sign;
+    int e2 = 0;
+    std::frexp(a, &e2);               // a = f * 2^e2, f in [0.5, 1)
+    int E = e2 - 1;                   // a in [2^E, 2^(E+1))
+    if (E < -14) E = -14;             // below the normal range the spacing stays 2^-24
+    const double q = std::ldexp(1.0, E - 10);   // spacing of binary16 values near a
+    const double n = a / q;                     // exact: division by a power of two
+    const double fl = std::floor(n);
+    const double frac = n - fl;                 // exact
+    double m = fl;
+    if (frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0)) m = fl + 1.0;
+    const double r = m * q;                     // exact: m <= 2048
+    if (r >= 65536.0) return static_cast<uint16_t>(sign | 0x7C00u);
+    if (r < std::ldexp(1.0, -14))               // subnormal (m <= 1024; 1024 encodes 2^-14)
+        return static_cast<uint16_t>(sign | static_cast<uint16_t>(std::ldexp(r, 24)));
+    std::frexp(r, &e2);
+    const int Er = e2 - 1;
+    const int mant = static_cast<int>(std::ldexp(r, 10 - Er)) - 1024;
+    return static_cast<uint16_t>(sign | ((Er + 15) << 10) | mant);
+}
+
 double load_elem(const void* base, int64_t i, int dtype) {
     if (dtype == kOracleBF16) return bf16_to_double(static_cast<const uint16_t*>(base)[i]);
+    if (dtype == kOracleF16) return f16_to_double(static_cast<const uint16_t*>(base)[i]);
     return static_cast<double>(static_cast<const float*>(base)[i]);
 }
 
@@ -122,6 +170,8 @@ double load_elem(const void* base, int64_t i, int dtype) {
 void store_elem(void* base, int64_t i, double v, int dtype) {
     if (dtype == kOracleBF16) {
         static_cast<uint16_t*>(base)[i] = double_to_bf16(v);
+    } else if (dtype == kOracleF16) {
+        static_cast<uint16_t*>(base)[i] = double_to_f16(v);
     } else {
         static_cast<float*>(base)[i] = static_cast<float>(v);
     }
@@ -246,6 +296,10 @@ uint16_t oracle_bf16_round(double v) { return double_to_bf16(v); }
 
 double oracle_bf16_value(uint16_t bits) { return bf16_to_double(bits); }
 
+uint16_t oracle_f16_round(double v) { return double_to_f16(v); }
+
+double oracle_f16_value(uint16_t bits) { return f16_to_double(bits); }
+
 int oracle_threads_available(void) { return affinity_threads(); }
 
 // RMSNorm over fp64 inputs, fp64 output, no rounding: x[rows, cols], w[cols], y[rows, cols].
@@ -265,7 +319,7 @@ int oracle_rmsnorm_f64(const double* x, const double* w, double* y, int64_t rows
 // nthreads <= 0 uses every core this process may run on.
 int oracle_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int64_t cols, double eps,
                    int dtype, int nthreads) {
-    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (!storage_ok(dtype)) return 2;
     if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
     if (rows == 0) return 0;
     if (!x || !w || !y) return 1;
@@ -287,7 +341,7 @@ int oracle_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int64_t 
 // computed from h as stored, rounded once. nthreads as for oracle_rmsnorm.
 int oracle_add_rmsnorm(const void* x, const void* r, const void* w, void* h, void* y,
                        int64_t rows, int64_t cols, double eps, int dtype, int nthreads) {
-    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (!storage_ok(dtype)) return 2;
     if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
     if (rows == 0) return 0;
     if (!x || !r || !w || !h || !y) return 1;
@@ -315,7 +369,7 @@ int oracle_kv_rmsnorm_rope_cache(const void* kv, const void* gamma, const float*
                                  const float* cos_t, const int64_t* slots, void* cache_n,
                                  void* cache_r, int64_t B, int64_t S, int64_t Dn, int64_t Dr,
                                  int64_t num_slots, double eps, int dtype) {
-    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (!storage_ok(dtype)) return 2;
     if (B < 0 || S < 0 || Dn < 1 || Dr < 2 || Dr % 2 != 0 || num_slots < 0 || !(eps >= 0.0))
         return 1;
     if (B * S == 0) return 0;
@@ -360,7 +414,7 @@ int oracle_layernorm_f64(const double* x, const double* g, const double* b, doub
 // LayerNorm over storage-typed x, gamma, beta: decode, fp64, one rounding of y.
 int oracle_layernorm(const void* x, const void* gamma, const void* beta, void* y, int64_t rows,
                      int64_t cols, double eps, int dtype, int nthreads) {
-    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (!storage_ok(dtype)) return 2;
     if (rows < 0 || cols <= 0 || !(eps >= 0.0)) return 1;
     if (rows == 0) return 0;
     if (!x || !gamma || !beta || !y) return 1;
@@ -388,7 +442,7 @@ int oracle_layernorm(const void* x, const void* gamma, const void* beta, void* y
 int oracle_kv_cat_repeat(const void* past, const void* fresh, const float* sin_t,
                          const float* cos_t, void* out, int64_t B, int64_t P, int64_t S,
                          int64_t Hk, int64_t D, int64_t n_rep, int dtype) {
-    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (!storage_ok(dtype)) return 2;
     if (B < 0 || P < 0 || S < 0 || Hk < 0 || D <= 0 || D % 2 != 0 || n_rep < 1) return 1;
     if ((sin_t == nullptr) != (cos_t == nullptr)) return 1;
     const int64_t T = P + S;
@@ -432,7 +486,7 @@ int oracle_kv_cat_repeat(const void* past, const void* fresh, const float* sin_t
 int oracle_rope_interleaved(const void* x, const float* sin_t, const float* cos_t,
                             const int32_t* positions, void* y, int64_t tokens, int64_t H,
                             int64_t D, int64_t max_pos, int dtype) {
-    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (!storage_ok(dtype)) return 2;
     if (tokens < 0 || H < 0 || D < 2 || D % 2 != 0 || max_pos < 0) return 1;
     if (tokens * H == 0) return 0;
     if (!x || !sin_t || !cos_t || !positions || !y) return 1;
@@ -496,7 +550,7 @@ int oracle_rope_f64(const double* x, const double* sin_t, const double* cos_t, d
 // decode exactly, rotate in fp64, round once. Threads split the (b, s) positions.
 int oracle_rope(const void* x, const float* sin_t, const float* cos_t, void* y, int64_t B,
                 int64_t S, int64_t H, int64_t D, int dtype, int nthreads) {
-    if (dtype != kOracleF32 && dtype != kOracleBF16) return 2;
+    if (!storage_ok(dtype)) return 2;
     if (B < 0 || S < 0 || H < 0 || D <= 0 || D % 2 != 0) return 1;
     if (B * S * H == 0) return 0;
     if (!x || !sin_t || !cos_t || !y) return 1;

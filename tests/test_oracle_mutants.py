@@ -2,7 +2,8 @@
 
 Each case below plants one plausible mistake in a copy of the oracle's source (a wrong
 divisor, eps outside the square root, a dropped index, a flipped sign, swapped operands,
-a wrong table row, ties rounded away from even, a second rounding), compiles the copy
+a wrong table row, ties rounded away from even, a second rounding, a wrong binary16
+exponent bias, overflow or subnormal range), compiles the copy
 with the host compiler into a temporary directory and runs the pin battery against it.
 Every mutant must fail at least one pin. The real oracle is never modified.
 """
@@ -35,13 +36,29 @@ MUTANTS = {
     "table row fixed at 0 in the storage path":
         ("const int64_t s = t - b * S;", "const int64_t s = 0 * (t - b * S);"),
     "ties rounded away from zero":
-        ("if (frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0)) m = fl + 1.0;",
-         "if (frac >= 0.5) m = fl + 1.0;"),
+        ("if (frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0)) m = fl + 1.0;\n"
+         "    const double r = m * q;                    // exact: m <= 256",
+         "if (frac >= 0.5) m = fl + 1.0;\n"
+         "    const double r = m * q;                    // exact: m <= 256"),
+    "binary16 ties rounded away from zero":
+        ("if (frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0)) m = fl + 1.0;\n"
+         "    const double r = m * q;                     // exact: m <= 2048",
+         "if (frac >= 0.5) m = fl + 1.0;\n"
+         "    const double r = m * q;                     // exact: m <= 2048"),
     "rounded twice through fp32":
         ("static_cast<uint16_t*>(base)[i] = double_to_bf16(v);",
          "static_cast<uint16_t*>(base)[i] = double_to_bf16(static_cast<float>(v));"),
     "subnormal spacing wrong":
         ("if (E < -126) E = -126;", "if (E < -127) E = -127;"),
+    "binary16 exponent bias 14":
+        ("return static_cast<uint16_t>(sign | ((Er + 15) << 10) | mant);",
+         "return static_cast<uint16_t>(sign | ((Er + 14) << 10) | mant);"),
+    "binary16 overflow one binade late":
+        ("if (r >= 65536.0) return static_cast<uint16_t>(sign | 0x7C00u);",
+         "if (r >= 131072.0) return static_cast<uint16_t>(sign | 0x7C00u);"),
+    "binary16 subnormals flushed to zero":
+        ("        return static_cast<uint16_t>(sign | static_cast<uint16_t>(std::ldexp(r, 24)));",
+         "        return sign;"),
     "add path normalizes x instead of h":
         ("hr[j] = load_elem(h, i, dtype);", "hr[j] = load_elem(x, i, dtype);"),
     "cache scatter uses the token index instead of its slot":
@@ -83,6 +100,10 @@ def _battery(lib):
     checks = [
         ("bf16 hand", lambda: [pins.test_bf16_round_hand(lib, v, b) for v, b in pins.BF16_HAND]),
         ("bf16 vs torch", lambda: pins.test_bf16_round_matches_torch_on_fp32_inputs(lib)),
+        ("f16 hand", lambda: [pins.test_f16_round_hand(lib, v, b) for v, b in pins.F16_HAND]),
+        ("f16 vs numpy", lambda: pins.test_f16_round_matches_numpy_on_fp64_inputs(lib)),
+        ("f16 decode", lambda: pins.test_f16_value_matches_numpy_on_every_pattern(lib)),
+        ("rms storage f16", lambda: pins.test_rmsnorm_storage_path_rounds_the_fp64_result_once(lib, "f16")),
         ("rms worked", lambda: [pins.test_rmsnorm_worked_cases(lib, [3.0, 4.0], [1.0, 1.0],
                                                                 [3 / 12.5**0.5, 4 / 12.5**0.5]),
                                 pins.test_rmsnorm_worked_cases(lib, [1.0, -1.0, 1.0, -1.0],

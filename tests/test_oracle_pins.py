@@ -5,6 +5,8 @@ something fixed independently of it:
 
 * bf16 rounding: hand-derived bit patterns at ties, overflow and subnormal boundaries,
   and torch's fp32 -> bf16 conversion (a library routine) on exactly representable input;
+* fp16 (IEEE binary16) rounding: hand-derived bit patterns, numpy's float64 -> float16
+  conversion (one rounding) and its float16 decoding of every pattern;
 * RMSNorm (xserv "phase 4" design notes, RMSNorm section: y = x / sqrt(sum(x^2)/hidden
   + eps) * gamma): worked cases in exact closed form, the constant-row closed form,
   the zero row, positive-scale invariance and odd symmetry at eps = 0, numpy's vector
@@ -94,6 +96,64 @@ def test_bf16_value_matches_torch_on_every_pattern(lib):
     pats = np.arange(65536, dtype=np.uint16)
     want = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).double().numpy()
     got = oracle.bf16_value(pats, lib=lib)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], want[~nan])
+
+
+# IEEE binary16: hand-derived patterns around ties, overflow and the subnormal range.
+F16_HAND = [
+    (1.0, 0x3C00),
+    (-2.0, 0xC000),
+    (0.0, 0x0000),
+    (-0.0, 0x8000),
+    (1.0 + TWO**-10, 0x3C01),
+    (1.0 + TWO**-11, 0x3C00),                 # tie between 1 and 1 + 2^-10: even is 1
+    (1.0 + 3 * TWO**-11, 0x3C02),             # tie between mantissas 1 and 2: even is 2
+    (1.0 + TWO**-11 + TWO**-30, 0x3C01),      # just above the tie
+    (65504.0, 0x7BFF),                        # largest finite
+    (65519.99, 0x7BFF),
+    (65520.0, 0x7C00),                        # tie above it: odd mantissa, rounds to inf
+    (-1e6, 0xFC00),
+    (TWO**-14, 0x0400),                       # smallest normal
+    (TWO**-24, 0x0001),                       # smallest subnormal
+    (TWO**-25, 0x0000),                       # tie between 0 and it: even is 0
+    (3 * TWO**-25, 0x0002),                   # tie between 1 and 2 ulps: even is 2
+    (1023.5 * TWO**-24, 0x0400),              # tie between the largest subnormal and 2^-14
+    (0.1, 0x2E66),
+    (-3.14159265358979, 0xC248),
+]
+
+
+@pytest.mark.parametrize("value,bits", F16_HAND)
+def test_f16_round_hand(lib, value, bits):
+    assert lib.oracle_f16_round(value) == bits
+
+
+def test_f16_round_nan(lib):
+    b = lib.oracle_f16_round(math.nan)
+    assert (b & 0x7C00) == 0x7C00 and (b & 0x03FF) != 0
+
+
+def test_f16_round_matches_numpy_on_fp64_inputs(lib):
+    # numpy converts float64 to float16 in one rounding to nearest, ties to even.
+    rng = np.random.default_rng(99)
+    mags = np.exp(rng.uniform(np.log(2.0**-27), np.log(7e4), 30000))
+    vals = mags * rng.choice([-1.0, 1.0], mags.size)
+    grid = np.arange(-2048, 2048, dtype=np.float64)
+    ties = np.concatenate([(grid + 0.5) * 2.0**-24, (1024 + grid[2048:] + 0.5) * 2.0**-10,
+                           (1024 + grid[2048:] + 0.5) * 2.0**5])
+    vals = np.concatenate([vals, ties, [65504.0, 65519.0, 65520.0, 65535.0]])
+    with np.errstate(over="ignore"):
+        want = vals.astype(np.float16).view(np.uint16)
+    got = oracle.f16_round(vals, lib=lib)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_f16_value_matches_numpy_on_every_pattern(lib):
+    pats = np.arange(65536, dtype=np.uint16)
+    want = pats.view(np.float16).astype(np.float64)
+    got = oracle.f16_value(pats, lib=lib)
     nan = np.isnan(want)
     assert np.array_equal(np.isnan(got), nan)
     np.testing.assert_array_equal(got[~nan], want[~nan])
@@ -192,7 +252,7 @@ def test_rmsnorm_brute_force_exact_rationals(lib):
                 np.testing.assert_allclose(y[r], want, rtol=1e-14, atol=0)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 def test_rmsnorm_storage_path_rounds_the_fp64_result_once(lib, dtype):
     rng = np.random.default_rng(5)
     xf = rng.standard_normal((7, 300)).astype(np.float32)
@@ -202,6 +262,9 @@ def test_rmsnorm_storage_path_rounds_the_fp64_result_once(lib, dtype):
         ws = torch.from_numpy(wf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         xd = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).double().numpy()
         wd = torch.from_numpy(ws.view(np.int16)).view(torch.bfloat16).double().numpy()
+    elif dtype == "f16":
+        xs, ws = xf.astype(np.float16), wf.astype(np.float16)
+        xd, wd = xs.astype(np.float64), ws.astype(np.float64)
     else:
         xs, ws, xd, wd = xf, wf, xf.astype(np.float64), wf.astype(np.float64)
     y = oracle.rmsnorm(xs, ws, 1e-5, dtype, lib=lib)
@@ -210,6 +273,8 @@ def test_rmsnorm_storage_path_rounds_the_fp64_result_once(lib, dtype):
         # The exact values (to ~1e-16) rounded once by the hand-pinned bf16 rounding.
         want = oracle.bf16_round(exact, lib=lib)
         np.testing.assert_array_equal(y, want)
+    elif dtype == "f16":
+        np.testing.assert_array_equal(y, exact.astype(np.float16))   # numpy: one rounding
     else:
         np.testing.assert_array_equal(y, exact.astype(np.float32))
 
@@ -243,10 +308,13 @@ def _storage_pair(rng, shape, dtype, scale=1.0):
     if dtype == "bf16":
         t = t.to(torch.bfloat16)
         return t, t.view(torch.int16).numpy().view(np.uint16)
+    if dtype == "f16":
+        t = t.to(torch.float16)
+        return t, t.numpy()
     return t, f
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 def test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, dtype):
     # h must equal torch's storage-type addition (round to nearest even of the exact sum),
     # and y the (separately pinned) RMSNorm of h as stored.
@@ -261,6 +329,8 @@ def test_add_rmsnorm_h_is_the_library_sum_and_y_the_rmsnorm_of_h(lib, dtype):
         want_h = xt + rt
         want_h = (want_h.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16"
                   else want_h.numpy())
+        if dtype == "f16":   # the library sum of two binary16 values, rounded once
+            assert want_h.dtype == np.float16
         np.testing.assert_array_equal(h, want_h)
         np.testing.assert_array_equal(y, oracle.rmsnorm(h, ws, 1e-5, dtype, lib=lib))
 
@@ -277,7 +347,7 @@ def test_add_rmsnorm_zero_residual_is_rmsnorm(lib):
 
 # ------------------------------------------------------------------------ KV norm + rope + cache
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 def test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, dtype):
     # Every written cache row must equal the (separately pinned) RMSNorm of the token's left
     # part and rotate-half RoPE of its right part with table row s; padding slots (negative
@@ -315,7 +385,7 @@ def test_kv_cache_scatter_is_rmsnorm_and_rope_of_each_token(lib, dtype):
 
 # ------------------------------------------------------------------------ KV cat + head repeat
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("B,P,S,Hk,D,n_rep", [(2, 5, 3, 3, 8, 4), (1, 0, 4, 2, 6, 1),
                                                (1, 7, 0, 1, 4, 3), (3, 1, 1, 4, 2, 2)])
 def test_kv_cat_repeat_without_tables_is_numpy_concatenate_and_repeat(lib, dtype, B, P, S, Hk,
@@ -420,7 +490,7 @@ def test_layernorm_brute_force_exact_rationals(lib):
             assert abs(y[0, j] - float(want)) <= bound
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 def test_layernorm_storage_path_rounds_the_fp64_result_once(lib, dtype):
     rng = np.random.default_rng(64)
     xt, xs = _storage_pair(rng, (5, 300), dtype)
@@ -429,7 +499,12 @@ def test_layernorm_storage_path_rounds_the_fp64_result_once(lib, dtype):
     dec = (lambda a: oracle.bf16_value(a, lib=lib)) if dtype == "bf16" else (lambda a: a.astype(np.float64))
     y64, _ = oracle.layernorm_f64(dec(xs), dec(gs), dec(bs), 1e-5, lib=lib)
     y = oracle.layernorm(xs, gs, bs, 1e-5, dtype, lib=lib)
-    want = oracle.bf16_round(y64, lib=lib) if dtype == "bf16" else y64.astype(np.float32)
+    if dtype == "bf16":
+        want = oracle.bf16_round(y64, lib=lib)
+    elif dtype == "f16":
+        want = y64.astype(np.float16)          # numpy: one rounding from fp64
+    else:
+        want = y64.astype(np.float32)
     np.testing.assert_array_equal(y, want)
 
 
@@ -443,7 +518,7 @@ def _f32_ulps(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(ia - ib)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 def test_rope_interleaved_is_rotate_half_on_deinterleaved_input(lib, dtype):
     # Interleaved RoPE at positions p_t equals the (separately pinned) rotate-half RoPE of the
     # de-interleaved heads with the table rows p_t, re-interleaved; tokens with a position
@@ -587,7 +662,7 @@ def test_rope_rotate_half_equals_interleaved_on_deinterleaved_input(lib):
     np.testing.assert_allclose(y[..., h:], out[..., 1::2], rtol=1e-15, atol=1e-15)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 def test_rope_storage_path_rounds_the_fp64_result_once(lib, dtype):
     rng = np.random.default_rng(17)
     B, S, H, D = 2, 6, 3, 32
@@ -597,6 +672,9 @@ def test_rope_storage_path_rounds_the_fp64_result_once(lib, dtype):
     if dtype == "bf16":
         xs = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         xd = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).double().numpy()
+    elif dtype == "f16":
+        xs = xf.astype(np.float16)
+        xd = xs.astype(np.float64)
     else:
         xs, xd = xf, xf.astype(np.float64)
     y = oracle.rope(xs, sin_t, cos_t, dtype, lib=lib)
@@ -606,6 +684,8 @@ def test_rope_storage_path_rounds_the_fp64_result_once(lib, dtype):
     exact = np.concatenate([z.real, z.imag], axis=-1)
     if dtype == "bf16":
         np.testing.assert_array_equal(y, oracle.bf16_round(exact, lib=lib))
+    elif dtype == "f16":
+        np.testing.assert_array_equal(y, exact.astype(np.float16))
     else:
         np.testing.assert_array_equal(y, exact.astype(np.float32))
 
