@@ -122,23 +122,23 @@ def recorded_traffic(kernel_name: str):
     return None if entry is None else entry.get("dram_bytes_per_launch")
 
 
-def plan_name(kind: str, p: camp.Plan) -> str:
+def plan_name(kind: str, p: camp.Plan, dt: str = "bf16") -> str:
     if kind == "layernorm":
         if p.kernel == camp.KERNEL_LAYERNORM_STAGED:
-            return (f"layernorm_staged<bf16,cluster{p.cluster},chunk{p.group}vec,"
+            return (f"layernorm_staged<{dt},cluster{p.cluster},chunk{p.group}vec,"
                     f"stages{p.per_thread}>")
-        return f"layernorm_rows<bf16,vec{p.vec_bytes},group{p.group},nv{p.per_thread}>"
+        return f"layernorm_rows<{dt},vec{p.vec_bytes},group{p.group},nv{p.per_thread}>"
     if kind == "rmsnorm":
         if p.kernel == camp.KERNEL_RMSNORM_STAGED:
-            return (f"rmsnorm_staged<bf16,cluster{p.cluster},chunk{p.group}vec,"
+            return (f"rmsnorm_staged<{dt},cluster{p.cluster},chunk{p.group}vec,"
                     f"stages{p.per_thread}>")
         k = {camp.KERNEL_RMSNORM_ROWS: "rmsnorm_rows", camp.KERNEL_RMSNORM_CLUSTER: "rmsnorm_cluster",
              camp.KERNEL_RMSNORM_WIDE: "rmsnorm_wide"}.get(p.kernel, "rmsnorm")
         extra = f",cluster{p.cluster}" if p.kernel == camp.KERNEL_RMSNORM_CLUSTER else ""
-        return f"{k}<bf16,vec{p.vec_bytes},group{p.group},nv{p.per_thread}{extra}>"
+        return f"{k}<{dt},vec{p.vec_bytes},group{p.group},nv{p.per_thread}{extra}>"
     k = {camp.KERNEL_ROPE: "rope_tiled", camp.KERNEL_ROPE_FLAT: "rope_flat",
          camp.KERNEL_ROPE_SPLIT: "rope_split"}.get(p.kernel, "rope")
-    return f"{k}<bf16,vec{p.vec_bytes},hpt{p.group}>"
+    return f"{k}<{dt},vec{p.vec_bytes},hpt{p.group}>"
 
 
 class ClockSampler:
@@ -549,11 +549,14 @@ LARGE_CASES = [
     ("rmsnorm bf16 [256,131072] (staged in shared memory)", "rms", (256, 131072, False, 1e-5)),
     ("add_rmsnorm bf16 [512,131072] (staged in shared memory)", "add", (512, 131072)),
     ("layernorm bf16 [8192,4096]", "ln", (8192, 4096)),
+    ("layernorm fp16 [8192,4096] (the TileLang tutorial's example 2)", "ln", (8192, 4096, "f16")),
     ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),
     ("layernorm bf16 [16384,8192]", "ln", (16384, 8192)),
     ("layernorm bf16 [1024,65536] (staged in shared memory)", "ln", (1024, 65536)),
     ("layernorm bf16 [256,131072] (staged in shared memory)", "ln", (256, 131072)),
     ("rope bf16 [1,65536,32,128]", "rope", (65536, 32, 128)),
+    ("rope fp16 [1,4096,32,128] (the TileLang tutorial's exercise E13)", "rope",
+     (4096, 32, 128, "f16")),
     ("rope bf16 [1,65536,32,64]", "rope", (65536, 32, 64)),
     ("rope bf16 [1,65536,8,128]", "rope", (65536, 8, 128)),
     ("rope_qk bf16 Q[1,65536,32,128] + K[1,65536,8,128]", "rope_qk", (65536, 32, 8, 128)),
@@ -575,10 +578,8 @@ def _large_case(kind: str, shp: tuple, seed: int):
         dt = shp[4] if len(shp) > 4 else "bf16"
         x, w = inputs.rmsnorm_inputs(rows, cols, dt, seed=seed, stress=stress, device="cuda")
         y = torch.empty_like(x)
-        pname = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, dt))
-        if dt != "bf16":
-            pname = pname.replace("<bf16,", f"<{dt},")
-        code = camp.BF16 if dt == "bf16" else camp.F32
+        pname = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, dt), dt)
+        code = camp._dtype(dt)
         fn = lambda st: camp.camp_rmsnorm(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, cols,
                                           eps, code, st)
         return fn, ledger.rmsnorm_bytes(rows, cols, dt), pname, (x, w, y)
@@ -594,13 +595,15 @@ def _large_case(kind: str, shp: tuple, seed: int):
                                               camp.BF16, st)
         return fn, ledger.add_rmsnorm_bytes(rows, cols), pname, (x, w, r, h, y)
     if kind == "ln":
-        rows, cols = shp
-        x, w, bt = inputs.layernorm_inputs(rows, cols, "bf16", seed=seed, device="cuda")
+        rows, cols = shp[:2]
+        dt = shp[2] if len(shp) > 2 else "bf16"
+        x, w, bt = inputs.layernorm_inputs(rows, cols, dt, seed=seed, device="cuda")
         y = torch.empty_like(x)
-        pname = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16"))
+        pname = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, dt), dt)
+        code = camp._dtype(dt)
         fn = lambda st: camp.camp_layernorm(x.data_ptr(), w.data_ptr(), bt.data_ptr(),
-                                            y.data_ptr(), rows, cols, 1e-5, camp.BF16, st)
-        return fn, ledger.layernorm_bytes(rows, cols), pname, (x, w, bt, y)
+                                            y.data_ptr(), rows, cols, 1e-5, code, st)
+        return fn, ledger.layernorm_bytes(rows, cols, dt), pname, (x, w, bt, y)
     if kind == "ril":
         T, H, D = shp
         mp = 2 * T
@@ -657,13 +660,15 @@ def _large_case(kind: str, shp: tuple, seed: int):
                                           cs.data_ptr(), yq.data_ptr(), yk.data_ptr(), 1, S, Hq,
                                           Hk, D, camp.BF16, st)
         return fn, ledger.rope_qk_bytes(1, S, Hq, Hk, D), pname, (q, k, sn, cs, yq, yk)
-    S, H, D = shp
-    x, sn, cs = inputs.rope_inputs(1, S, H, D, "bf16", seed=seed, device="cuda")
+    S, H, D = shp[:3]
+    dt = shp[3] if len(shp) > 3 else "bf16"
+    x, sn, cs = inputs.rope_inputs(1, S, H, D, dt, seed=seed, device="cuda")
     y = torch.empty_like(x)
-    pname = plan_name("rope", camp.camp_rope_plan(x, sn, cs, y, 1, S, H, D, "bf16"))
+    pname = plan_name("rope", camp.camp_rope_plan(x, sn, cs, y, 1, S, H, D, dt), dt)
+    code = camp._dtype(dt)
     fn = lambda st: camp.camp_rope(x.data_ptr(), sn.data_ptr(), cs.data_ptr(), y.data_ptr(), 1,
-                                   S, H, D, camp.BF16, st)
-    return fn, ledger.rope_bytes(1, S, H, D), pname, (x, sn, cs, y)
+                                   S, H, D, code, st)
+    return fn, ledger.rope_bytes(1, S, H, D, dt), pname, (x, sn, cs, y)
 
 
 SWEEP_TOKENS = (1, 8, 64, 512, 4096, 65536)
@@ -717,12 +722,13 @@ def oracle_case(kind: str, tensors: tuple, shp: tuple, budget_bytes: int = 64 <<
         nrows = n
     elif kind == "rope":
         x, sn, cs = tensors[0], tensors[1], tensors[2]
-        S, H, D = shp
+        S, H, D = shp[:3]
+        dt = shp[3] if len(shp) > 3 else "bf16"
         n = max(1, min(S, budget_bytes // (H * D * x.element_size())))
         xs = inputs.to_numpy(x[:, :n])
         ss, cc = sn[:n].cpu().numpy(), cs[:n].cpu().numpy()
-        fn = lambda: oracle.rope(xs, ss, cc, "bf16", lib=lib)
-        nbytes, what = ledger.rope_bytes(1, n, H, D), f"{n} of {S} positions"
+        fn = lambda: oracle.rope(xs, ss, cc, dt, lib=lib)
+        nbytes, what = ledger.rope_bytes(1, n, H, D, dt), f"{n} of {S} positions"
         nrows = n * H
     else:
         return None

@@ -2,7 +2,7 @@
 
 The functions named like the C entry points (``camp_rmsnorm``, ``camp_rope``, ...) take
 raw device pointers (ints) or torch tensors (their ``data_ptr()`` is passed), a dtype as
-``camp.BF16``/``camp.F32`` or ``"bf16"``/``"f32"``, and a stream as an int handle, a
+``camp.BF16``/``camp.F16``/``camp.F32`` or ``"bf16"``/``"f16"``/``"f32"``, and a stream as an int handle, a
 ``torch.cuda.Stream`` or ``None`` (torch's current stream on the current device). They
 raise :class:`CampError` on any non-success status. Every step of the computation runs
 in libcamp's kernels; there is no other code path. The library is opened on first use
@@ -27,6 +27,7 @@ ERR_UNSUPPORTED_DTYPE = 2
 ERR_RUNTIME = 3
 ERR_NOT_SUPPORTED = 5
 
+F16 = 0
 F32 = 1
 BF16 = 3
 
@@ -184,15 +185,19 @@ def _ptr(a) -> int | None:
 
 
 def _dtype(d) -> int:
-    if d in (F32, BF16):
+    if isinstance(d, int) and d in (F16, F32, BF16):
         return d
     if d in ("bf16", "bfloat16"):
         return BF16
+    if d in ("f16", "fp16", "float16"):
+        return F16
     if d in ("f32", "fp32", "float32"):
         return F32
     name = str(d)
     if name == "torch.bfloat16":
         return BF16
+    if name == "torch.float16":
+        return F16
     if name == "torch.float32":
         return F32
     if isinstance(d, int):
@@ -429,7 +434,7 @@ def _require(cond: bool, msg: str) -> None:
 
 
 def rmsnorm(x, w, eps: float = 1e-5, out=None, stream=None):
-    """RMSNorm over the last dimension of a contiguous CUDA tensor (bf16 or fp32)."""
+    """RMSNorm over the last dimension of a contiguous CUDA tensor (bf16, fp16 or fp32)."""
     import torch
     _require(x.is_cuda and x.is_contiguous(), "x must be a contiguous CUDA tensor")
     _require(w.dtype == x.dtype and w.is_contiguous() and w.numel() == x.shape[-1],
@@ -494,7 +499,7 @@ def add_rmsnorm(x, r, w, eps: float = 1e-5, out_h=None, out_y=None, stream=None)
 
 
 def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
-    """LayerNorm over the last dimension of a contiguous CUDA tensor (bf16 or fp32)."""
+    """LayerNorm over the last dimension of a contiguous CUDA tensor (bf16, fp16 or fp32)."""
     import torch
     _require(x.is_cuda and x.is_contiguous(), "x must be a contiguous CUDA tensor")
     for t, name in ((gamma, "gamma"), (beta, "beta")):

@@ -20,9 +20,13 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int64_t kMaxGrid = 2147483647;   // gridDim.x limit for the looping kernels
 
-bool dtype_ok(camp_dtype_t d) { return d == CAMP_DTYPE_F32 || d == CAMP_DTYPE_BF16; }
+bool dtype_ok(camp_dtype_t d) {
+    return d == CAMP_DTYPE_F16 || d == CAMP_DTYPE_F32 || d == CAMP_DTYPE_BF16;
+}
 
-DType to_dtype(camp_dtype_t d) { return d == CAMP_DTYPE_BF16 ? DType::BF16 : DType::F32; }
+DType to_dtype(camp_dtype_t d) {
+    return d == CAMP_DTYPE_BF16 ? DType::BF16 : d == CAMP_DTYPE_F16 ? DType::F16 : DType::F32;
+}
 
 bool aligned(const void* p, int64_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 

@@ -1,12 +1,14 @@
 // Device-side building blocks shared by the RMSNorm and RoPE kernels: raw vector
-// accesses with explicit cache policy, bf16/fp32 unpacking and packing, and warp
+// accesses with explicit cache policy, bf16/f16/fp32 unpacking and packing, and warp
 // reductions.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
 #include <utility>
 
 namespace camp {
@@ -14,10 +16,12 @@ namespace camp {
 // ------------------------------------------------------------------ storage types
 
 struct bf16_t {};   // tag: 16-bit brain float, stored as the upper half of an fp32
+struct f16_t {};    // tag: IEEE binary16
 struct f32_t {};    // tag: IEEE binary32
 
 template <typename S> struct Storage;
 template <> struct Storage<bf16_t> { static constexpr int kBytes = 2; };
+template <> struct Storage<f16_t> { static constexpr int kBytes = 2; };
 template <> struct Storage<f32_t> { static constexpr int kBytes = 4; };
 
 // A vector access of BYTES bytes, kept as raw 32-bit words (16-bit for BYTES == 2).
@@ -267,6 +271,105 @@ template <int BYTES> struct Codec<bf16_t, BYTES> {
         for (int k = 0; k < kPairs; ++k) {
             const f32x2 q = f(k, f2_make(bf16_lo_p(r.w[k]), bf16_hi_p(r.w[k])));
             o.w[k] = bf16_pack2(f2_lo(q), f2_hi(q));
+        }
+        return o;
+    }
+};
+
+// binary16 <-> fp32. Every binary16 value is exactly an fp32 value; fp32 -> binary16
+// rounds to nearest, ties to even (cvt.rn). The "_p" forms issue the same conversion from
+// inline assembly, which the compiler does not merge with the intrinsic's: as with the
+// byte-permute forms of bf16, a value unpacked for a reduction pass is unpacked again in
+// the output pass rather than kept alive across the reduction.
+__device__ __forceinline__ float f16_val(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+__device__ __forceinline__ float f16_lo(uint32_t w) { return f16_val(static_cast<uint16_t>(w & 0xFFFFu)); }
+__device__ __forceinline__ float f16_hi(uint32_t w) { return f16_val(static_cast<uint16_t>(w >> 16)); }
+__device__ __forceinline__ float f16_val_p(uint16_t h) {
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+    return f;
+}
+__device__ __forceinline__ float f16_lo_p(uint32_t w) { return f16_val_p(static_cast<uint16_t>(w & 0xFFFFu)); }
+__device__ __forceinline__ float f16_hi_p(uint32_t w) { return f16_val_p(static_cast<uint16_t>(w >> 16)); }
+__device__ __forceinline__ uint32_t f16_pack2(float lo, float hi) {
+    const __half2 p = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+template <int BYTES> struct Codec<f16_t, BYTES> {
+    static constexpr int kElems = BYTES / 2;
+    static constexpr int kPairs = BYTES / 4;
+
+    template <typename F>
+    __device__ __forceinline__ static void each(const Raw<BYTES>& r, F f) {
+        if constexpr (BYTES == 2) {
+            f(0, f16_val(r.h));
+        } else {
+#pragma unroll
+            for (int k = 0; k < BYTES / 4; ++k) {
+                f(2 * k, f16_lo(r.w[k]));
+                f(2 * k + 1, f16_hi(r.w[k]));
+            }
+        }
+    }
+
+    template <typename F>
+    __device__ __forceinline__ static Raw<BYTES> map(const Raw<BYTES>& r, F f) {
+        Raw<BYTES> o;
+        if constexpr (BYTES == 2) {
+            o.h = __half_as_ushort(__float2half_rn(f(0, f16_val_p(r.h))));
+        } else {
+#pragma unroll
+            for (int k = 0; k < BYTES / 4; ++k)
+                o.w[k] = f16_pack2(f(2 * k, f16_lo_p(r.w[k])), f(2 * k + 1, f16_hi_p(r.w[k])));
+        }
+        return o;
+    }
+
+    __device__ __forceinline__ static Raw<BYTES> add(const Raw<BYTES>& a, const Raw<BYTES>& b) {
+        Raw<BYTES> o;
+        if constexpr (BYTES == 2) {
+            o.h = __half_as_ushort(__float2half_rn(f16_val(a.h) + f16_val(b.h)));
+        } else {
+#pragma unroll
+            for (int k = 0; k < BYTES / 4; ++k)
+                o.w[k] = f16_pack2(f16_lo_p(a.w[k]) + f16_lo_p(b.w[k]),
+                                   f16_hi_p(a.w[k]) + f16_hi_p(b.w[k]));
+        }
+        return o;
+    }
+
+    template <typename F>
+    __device__ __forceinline__ static void map2(const Raw<BYTES>& a, const Raw<BYTES>& b,
+                                                Raw<BYTES>& oa, Raw<BYTES>& ob, F f) {
+        if constexpr (BYTES == 2) {
+            const float2 v = f(0, f16_val_p(a.h), f16_val_p(b.h));
+            oa.h = __half_as_ushort(__float2half_rn(v.x));
+            ob.h = __half_as_ushort(__float2half_rn(v.y));
+        } else {
+#pragma unroll
+            for (int k = 0; k < BYTES / 4; ++k) {
+                const float2 v0 = f(2 * k, f16_lo_p(a.w[k]), f16_lo_p(b.w[k]));
+                const float2 v1 = f(2 * k + 1, f16_hi_p(a.w[k]), f16_hi_p(b.w[k]));
+                oa.w[k] = f16_pack2(v0.x, v1.x);
+                ob.w[k] = f16_pack2(v0.y, v1.y);
+            }
+        }
+    }
+
+    template <typename F>
+    __device__ __forceinline__ static void each_pair(const Raw<BYTES>& r, F f) {
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) f(k, f2_make(f16_lo(r.w[k]), f16_hi(r.w[k])));
+    }
+
+    template <typename F>
+    __device__ __forceinline__ static Raw<BYTES> map_pair(const Raw<BYTES>& r, F f) {
+        Raw<BYTES> o;
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+            const f32x2 q = f(k, f2_make(f16_lo_p(r.w[k]), f16_hi_p(r.w[k])));
+            o.w[k] = f16_pack2(f2_lo(q), f2_hi(q));
         }
         return o;
     }

@@ -8,9 +8,9 @@
 
 namespace camp {
 
-enum class DType : int { F32 = 1, BF16 = 3 };
+enum class DType : int { F16 = 0, F32 = 1, BF16 = 3 };
 
-inline int elem_bytes(DType t) { return t == DType::BF16 ? 2 : 4; }
+inline int elem_bytes(DType t) { return t == DType::F32 ? 4 : 2; }
 
 // The planner sizes grids for GB300's 152 SMs; any other SM count only changes how well
 // the last wave is filled, never the result.
@@ -208,7 +208,7 @@ struct RopeInterleavedArgs {
 };
 
 // Tiled like rope_tiled: kRopeBlock threads, positions per CTA = 256 / (ceil(H/hpt) *
-// dim/elems); vec_bytes 16, 8 or 4 (bf16) / 16 or 8 (fp32): a vector holds whole pairs.
+// dim/elems); vec_bytes 16, 8 or 4 (bf16, fp16) / 16 or 8 (fp32): a vector holds whole pairs.
 bool rope_interleaved_compiled(DType t, int vec_bytes, int heads_per_thread);
 cudaError_t rope_interleaved_launch(DType t, int vec_bytes, int heads_per_thread,
                                     const RopeInterleavedArgs& a, int64_t grid, cudaStream_t s);
@@ -279,12 +279,14 @@ struct KvCatArgs {
 
 // CTAs per SM by heads per thread: camp_rope's budget, except that one head per thread also
 // runs 5 CTAs (48 registers): at 6 the 16-byte bf16 variant (8 sine and 8 cosine values
-// beside its data) spilled (checked with -Xptxas -v).
-constexpr int kv_cat_min_blocks(int heads_per_thread) {
-    return heads_per_thread <= 2 ? 5 : heads_per_thread <= 4 ? 3 : 2;
+// beside its data) spilled. The fp16 unpack is a conversion, not a shift, and the 16-byte
+// fp16 variant with two heads per thread spilled at 5: it runs 4 (checked with -Xptxas -v).
+constexpr int kv_cat_min_blocks(int heads_per_thread, bool f16) {
+    return heads_per_thread == 1 ? 5 : heads_per_thread == 2 ? (f16 ? 4 : 5)
+                                     : heads_per_thread <= 4 ? 3 : 2;
 }
 
-// vec_bytes 16, 8, 4, 2 (bf16) / 16, 8, 4 (fp32): bytes per access of each half.
+// vec_bytes 16, 8, 4, 2 (bf16, fp16) / 16, 8, 4 (fp32): bytes per access of each half.
 bool kv_cat_compiled(DType t, int vec_bytes, int heads_per_thread);
 cudaError_t kv_cat_launch(DType t, int vec_bytes, int heads_per_thread, const KvCatArgs& a,
                           int64_t grid, cudaStream_t s);

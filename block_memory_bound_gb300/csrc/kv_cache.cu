@@ -116,7 +116,7 @@ cudaError_t launch_kv(const KvCacheArgs& a, cudaStream_t s) {
                       static_cast<int>(a.dr), a.num_slots, a.eps);
 }
 
-// 16-byte norm accesses: the rope part takes 4- (bf16 only), 8- or 16-byte accesses.
+// 16-byte norm accesses: the rope part takes 4- (16-bit types only), 8- or 16-byte accesses.
 template <typename S, int NVN>
 cudaError_t launch_kv_rb(int rb, const KvCacheArgs& a, cudaStream_t s) {
     switch (rb) {
@@ -172,6 +172,9 @@ cudaError_t kv_cache_launch(DType t, int vec_bytes, int nvn, int rope_bytes,
     if (t == DType::BF16)
         return vec_bytes == 16 ? launch_kv_vec<bf16_t>(nvn, rope_bytes, a, s)
                                : launch_kv_elem<bf16_t>(nvn, a, s);
+    if (t == DType::F16)
+        return vec_bytes == 16 ? launch_kv_vec<f16_t>(nvn, rope_bytes, a, s)
+                               : launch_kv_elem<f16_t>(nvn, a, s);
     return vec_bytes == 16 ? launch_kv_vec<f32_t>(nvn, rope_bytes, a, s)
                            : launch_kv_elem<f32_t>(nvn, a, s);
 }

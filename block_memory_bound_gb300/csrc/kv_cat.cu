@@ -23,7 +23,7 @@ namespace camp {
 namespace {
 
 template <typename S, int VB, int HPT>
-__global__ void __launch_bounds__(kRopeBlock, kv_cat_min_blocks(HPT))
+__global__ void __launch_bounds__(kRopeBlock, kv_cat_min_blocks(HPT, std::is_same_v<S, f16_t>))
 kv_cat_repeat_kernel(const void* past, const void* fresh, const float* __restrict__ sin_t,
                      const float* __restrict__ cos_t, void* out, int64_t rows, FastDiv seq,
                      uint32_t past_len, int heads, int n_rep, int half) {
@@ -126,7 +126,7 @@ cudaError_t launch_kv_cat_hpt(int hpt, const KvCatArgs& a, int64_t grid, cudaStr
 bool kv_cat_compiled(DType t, int vec_bytes, int heads_per_thread) {
     const bool hpt = heads_per_thread == 1 || heads_per_thread == 2 || heads_per_thread == 4 ||
                      heads_per_thread == 8;
-    if (t == DType::BF16)
+    if (t != DType::F32)
         return hpt && (vec_bytes == 16 || vec_bytes == 8 || vec_bytes == 4 || vec_bytes == 2);
     return hpt && (vec_bytes == 16 || vec_bytes == 8 || vec_bytes == 4);
 }
@@ -139,6 +139,14 @@ cudaError_t kv_cat_launch(DType t, int vec_bytes, int heads_per_thread, const Kv
             case 8: return launch_kv_cat_hpt<bf16_t, 8>(heads_per_thread, a, grid, s);
             case 4: return launch_kv_cat_hpt<bf16_t, 4>(heads_per_thread, a, grid, s);
             case 2: return launch_kv_cat_hpt<bf16_t, 2>(heads_per_thread, a, grid, s);
+            default: break;
+        }
+    } else if (t == DType::F16) {
+        switch (vec_bytes) {
+            case 16: return launch_kv_cat_hpt<f16_t, 16>(heads_per_thread, a, grid, s);
+            case 8: return launch_kv_cat_hpt<f16_t, 8>(heads_per_thread, a, grid, s);
+            case 4: return launch_kv_cat_hpt<f16_t, 4>(heads_per_thread, a, grid, s);
+            case 2: return launch_kv_cat_hpt<f16_t, 2>(heads_per_thread, a, grid, s);
             default: break;
         }
     } else {

@@ -198,8 +198,10 @@ struct LnEntry {
 
 const LnEntry kLn[] = {
     CAMP_LN_FAST(bf16_t, BF16),
+    CAMP_LN_FAST(f16_t, F16),
     CAMP_LN_FAST(f32_t, F32),
     CAMP_LN_ELEM(bf16_t, BF16, 2),
+    CAMP_LN_ELEM(f16_t, F16, 2),
     CAMP_LN_ELEM(f32_t, F32, 4),
 };
 

@@ -318,8 +318,11 @@ cudaError_t layernorm_staged_launch(DType t, int cluster, int stages, const Laye
                                     cudaStream_t s) {
     if (cluster < 1 || cluster > 16 || stages < 2 || stages > kStagedMaxStages)
         return cudaErrorInvalidValue;
-    return t == DType::BF16 ? launch_ln_staged_nvt<bf16_t>(a, cluster, stages, s)
-                            : launch_ln_staged_nvt<f32_t>(a, cluster, stages, s);
+    switch (t) {
+        case DType::BF16: return launch_ln_staged_nvt<bf16_t>(a, cluster, stages, s);
+        case DType::F16: return launch_ln_staged_nvt<f16_t>(a, cluster, stages, s);
+        default: return launch_ln_staged_nvt<f32_t>(a, cluster, stages, s);
+    }
 }
 
 cudaError_t read_layernorm_device_errors(unsigned int* flags, bool clear) {

@@ -358,8 +358,10 @@ struct Tables {
                             const RmsnormArgs& a, int64_t grid, cudaStream_t s) {
         static const RowsEntry kRows[] = {
             CAMP_ROWS_FAST(bf16_t, BF16, ADD),
+            CAMP_ROWS_FAST(f16_t, F16, ADD),
             CAMP_ROWS_FAST(f32_t, F32, ADD),
             CAMP_ROWS_ELEM(bf16_t, BF16, 2, ADD),
+            CAMP_ROWS_ELEM(f16_t, F16, 2, ADD),
             CAMP_ROWS_ELEM(f32_t, F32, 4, ADD),
         };
         for (const RowsEntry& e : kRows) {
@@ -373,14 +375,22 @@ struct Tables {
     static cudaError_t cluster(DType t, int per_thread, int cl, const RmsnormArgs& a,
                                cudaStream_t s) {
         if (cl < 2 || cl > 16 || (cl & (cl - 1)) != 0) return cudaErrorInvalidValue;
-        const bool bf = t == DType::BF16;
+        switch (t) {
+            case DType::BF16: return cluster_nv<bf16_t>(per_thread, cl, a, s);
+            case DType::F16: return cluster_nv<f16_t>(per_thread, cl, a, s);
+            default: return cluster_nv<f32_t>(per_thread, cl, a, s);
+        }
+    }
+
+    template <typename S>
+    static cudaError_t cluster_nv(int per_thread, int cl, const RmsnormArgs& a, cudaStream_t s) {
         switch (per_thread) {
-            case 1: return bf ? launch_cluster<bf16_t, 1, ADD>(a, cl, s) : launch_cluster<f32_t, 1, ADD>(a, cl, s);
-            case 2: return bf ? launch_cluster<bf16_t, 2, ADD>(a, cl, s) : launch_cluster<f32_t, 2, ADD>(a, cl, s);
-            case 3: return bf ? launch_cluster<bf16_t, 3, ADD>(a, cl, s) : launch_cluster<f32_t, 3, ADD>(a, cl, s);
-            case 4: return bf ? launch_cluster<bf16_t, 4, ADD>(a, cl, s) : launch_cluster<f32_t, 4, ADD>(a, cl, s);
-            case 6: return bf ? launch_cluster<bf16_t, 6, ADD>(a, cl, s) : launch_cluster<f32_t, 6, ADD>(a, cl, s);
-            case 8: return bf ? launch_cluster<bf16_t, 8, ADD>(a, cl, s) : launch_cluster<f32_t, 8, ADD>(a, cl, s);
+            case 1: return launch_cluster<S, 1, ADD>(a, cl, s);
+            case 2: return launch_cluster<S, 2, ADD>(a, cl, s);
+            case 3: return launch_cluster<S, 3, ADD>(a, cl, s);
+            case 4: return launch_cluster<S, 4, ADD>(a, cl, s);
+            case 6: return launch_cluster<S, 6, ADD>(a, cl, s);
+            case 8: return launch_cluster<S, 8, ADD>(a, cl, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -390,6 +400,9 @@ struct Tables {
         if (t == DType::BF16) {
             if (vec_bytes == 16) return launch_wide<bf16_t, 16, ADD>(a, grid, s);
             if (vec_bytes == 2) return launch_wide<bf16_t, 2, ADD>(a, grid, s);
+        } else if (t == DType::F16) {
+            if (vec_bytes == 16) return launch_wide<f16_t, 16, ADD>(a, grid, s);
+            if (vec_bytes == 2) return launch_wide<f16_t, 2, ADD>(a, grid, s);
         } else {
             if (vec_bytes == 16) return launch_wide<f32_t, 16, ADD>(a, grid, s);
             if (vec_bytes == 4) return launch_wide<f32_t, 4, ADD>(a, grid, s);

@@ -297,6 +297,9 @@ cudaError_t rmsnorm_staged_launch(bool add, DType t, int cluster, int stages,
     if (t == DType::BF16)
         return add ? launch_staged_nvt<bf16_t, true>(a, cluster, stages, s)
                    : launch_staged_nvt<bf16_t, false>(a, cluster, stages, s);
+    if (t == DType::F16)
+        return add ? launch_staged_nvt<f16_t, true>(a, cluster, stages, s)
+                   : launch_staged_nvt<f16_t, false>(a, cluster, stages, s);
     return add ? launch_staged_nvt<f32_t, true>(a, cluster, stages, s)
                : launch_staged_nvt<f32_t, false>(a, cluster, stages, s);
 }

@@ -190,6 +190,8 @@ struct RopeEntry {
 const RopeEntry kRope[] = {
     CAMP_ROPE_H(bf16_t, BF16, 16), CAMP_ROPE_H(bf16_t, BF16, 8), CAMP_ROPE_H(bf16_t, BF16, 4),
     CAMP_ROPE_H(bf16_t, BF16, 2),
+    CAMP_ROPE_H(f16_t, F16, 16), CAMP_ROPE_H(f16_t, F16, 8), CAMP_ROPE_H(f16_t, F16, 4),
+    CAMP_ROPE_H(f16_t, F16, 2),
     CAMP_ROPE_H(f32_t, F32, 16), CAMP_ROPE_H(f32_t, F32, 8), CAMP_ROPE_H(f32_t, F32, 4),
 };
 

@@ -125,7 +125,7 @@ rope_tables_kernel(float* sin_t, float* cos_t, int64_t max_pos, int half, double
 bool rope_interleaved_compiled(DType t, int vec_bytes, int heads_per_thread) {
     const bool hpt = heads_per_thread == 1 || heads_per_thread == 2 || heads_per_thread == 4 ||
                      heads_per_thread == 8;
-    if (t == DType::BF16) return hpt && (vec_bytes == 16 || vec_bytes == 8 || vec_bytes == 4);
+    if (t != DType::F32) return hpt && (vec_bytes == 16 || vec_bytes == 8 || vec_bytes == 4);
     return hpt && (vec_bytes == 16 || vec_bytes == 8);
 }
 
@@ -136,6 +136,10 @@ cudaError_t rope_interleaved_launch(DType t, int vec_bytes, int heads_per_thread
         if (vec_bytes == 16) return launch_interleaved_hpt<bf16_t, 16>(heads_per_thread, a, grid, s);
         if (vec_bytes == 8) return launch_interleaved_hpt<bf16_t, 8>(heads_per_thread, a, grid, s);
         if (vec_bytes == 4) return launch_interleaved_hpt<bf16_t, 4>(heads_per_thread, a, grid, s);
+    } else if (t == DType::F16) {
+        if (vec_bytes == 16) return launch_interleaved_hpt<f16_t, 16>(heads_per_thread, a, grid, s);
+        if (vec_bytes == 8) return launch_interleaved_hpt<f16_t, 8>(heads_per_thread, a, grid, s);
+        if (vec_bytes == 4) return launch_interleaved_hpt<f16_t, 4>(heads_per_thread, a, grid, s);
     } else {
         if (vec_bytes == 16) return launch_interleaved_hpt<f32_t, 16>(heads_per_thread, a, grid, s);
         if (vec_bytes == 8) return launch_interleaved_hpt<f32_t, 8>(heads_per_thread, a, grid, s);

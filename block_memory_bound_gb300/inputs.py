@@ -6,13 +6,14 @@ path and the CPU oracle both consume, so that the two are compared on identical 
 * RMSNorm: ``x[rows, cols] ~ N(0, 1)``, ``w[cols] ~ N(1, 0.1)``; in the stress recipe
   1% of the rows (chosen by a seeded permutation) are scaled by 1e3 and another,
   disjoint 1% by 1e-4. Values are drawn in fp32 and rounded once to the storage type
-  (bf16 rounding is torch's, round to nearest even).
+  (bf16 and fp16 rounding is torch's, round to nearest even; in fp16 the 1e-4 rows are
+  partly subnormal).
 * RoPE: ``x[B, S, H, D] ~ N(0, 1)`` rounded to the storage type, and fp32 tables
   ``sin, cos [S, D/2]`` at ``angle = s * theta^(-2i/D)``, ``i = 0 .. D/2-1``, computed in
   fp64 and rounded once to fp32 (Llama-3.2-1B uses theta = 500000).
 
 * LayerNorm: ``x[r, :] = o_r + s_r * N(0, 1)`` with a per-row scale ``s_r`` drawn from
-  {1e-2, 1, 10} and an offset ratio ``o_r / s_r`` from {0, +-3, +-100} (bf16) or
+  {1e-2, 1, 10} and an offset ratio ``o_r / s_r`` from {0, +-3, +-100} (bf16, fp16) or
   {0, +-3, +-1e3} (fp32), so some rows have |mean| >> spread; ``gamma ~ N(1, 0.1)``,
   ``beta ~ N(0, 1)`` (beta and gamma * xhat then cancel somewhere in every long row).
 
@@ -28,7 +29,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-STORAGE = {"bf16": torch.bfloat16, "f32": torch.float32}
+STORAGE = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 
 
 def _gen(seed: int, k: int, device) -> torch.Generator:
@@ -66,8 +67,8 @@ def layernorm_inputs(rows: int, cols: int, dtype: str = "bf16", seed: int = 0,
     b = torch.randn(cols, generator=_gen(seed, 4, device), dtype=torch.float32, device=device)
     pick = torch.randint(0, 1 << 30, (rows, 2), generator=_gen(seed, 5, "cpu"))
     scales = torch.tensor([1e-2, 1.0, 10.0])
-    ratios = torch.tensor([0.0, 3.0, -3.0, 100.0, -100.0] if dtype == "bf16"
-                          else [0.0, 3.0, -3.0, 1e3, -1e3])
+    ratios = torch.tensor([0.0, 3.0, -3.0, 1e3, -1e3] if dtype == "f32"
+                          else [0.0, 3.0, -3.0, 100.0, -100.0])
     s_r = scales[pick[:, 0] % len(scales)]
     o_r = ratios[pick[:, 1] % len(ratios)] * s_r
     x = x * s_r.to(device)[:, None] + o_r.to(device)[:, None]
@@ -104,7 +105,8 @@ def p3_style_rmsnorm_inputs(rows: int, cols: int, dtype: str = "bf16"
 
 
 def to_numpy(t: torch.Tensor) -> np.ndarray:
-    """CPU copy as numpy: bf16 as ``uint16`` bit patterns, fp32 as ``float32``."""
+    """CPU copy as numpy: bf16 as ``uint16`` bit patterns, fp16 as ``float16``, fp32 as
+    ``float32``."""
     t = t.detach().contiguous().cpu()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
@@ -112,7 +114,8 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
 
 
 def from_numpy(a: np.ndarray) -> torch.Tensor:
-    """Inverse of :func:`to_numpy` (``uint16`` is read as bf16 bit patterns)."""
+    """Inverse of :func:`to_numpy` (``uint16`` is read as bf16 bit patterns, ``float16`` as
+    fp16)."""
     if a.dtype == np.uint16:
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
     return torch.from_numpy(np.ascontiguousarray(a))

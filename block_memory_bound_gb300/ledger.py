@@ -13,7 +13,7 @@ write of RMSNorm. The numbers reported here include the weight and the tables
 
 from __future__ import annotations
 
-ELEM_BYTES = {"bf16": 2, "fp16": 2, "f32": 4, "fp32": 4}
+ELEM_BYTES = {"bf16": 2, "f16": 2, "fp16": 2, "f32": 4, "fp32": 4}
 
 
 def rmsnorm_bytes(rows: int, cols: int, dtype: str = "bf16", weight: bool = True) -> int:

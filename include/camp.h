@@ -55,8 +55,11 @@ typedef enum {
     CAMP_ERR_NOT_SUPPORTED = 5     /* a valid request that this build cannot run */
 } camp_status_t;
 
-/* Storage types. Arithmetic is fp32 for both; bf16 is the upper half of an fp32. */
+/* Storage types. Arithmetic is fp32 for all three: bf16 is the upper half of an fp32,
+ * f16 is IEEE binary16 (every value exact in fp32); results are rounded once to the
+ * storage type, to nearest, ties to even. */
 typedef enum {
+    CAMP_DTYPE_F16 = 0,
     CAMP_DTYPE_F32 = 1,
     CAMP_DTYPE_BF16 = 3
 } camp_dtype_t;
@@ -185,7 +188,7 @@ CAMP_API camp_status_t camp_rope_qk(const void* q, const void* k, const float* s
  * One read of kv, one write of each cache row; a padding token's kv row is read (with the
  * rest of the warp's loads, before its slot is known) but nothing is written for it.
  * Supported widths: up to 256 16-byte vectors for the norm part and 32 lanes of at most
- * 16 bytes per rope half (bf16: Dn <= 2048, Dr <= 512; fp32: Dn <= 1024, Dr <= 256); when
+ * 16 bytes per rope half (bf16/f16: Dn <= 2048, Dr <= 512; fp32: Dn <= 1024, Dr <= 256); when
  * the norm rows or the pointers are not 16-byte aligned, element accesses (Dn <= 512,
  * Dr <= 64); otherwise CAMP_ERR_NOT_SUPPORTED. The caches must be disjoint from every
  * input and from each other. Errors as for camp_rmsnorm.
@@ -276,9 +279,9 @@ CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos,
  * once) and the statistics are taken in two passes over the registers, in fp32: with
  * K = x[row, 0], mu = sum(x - K) / n and d = (x - K) - mu, var = sum(d^2) / n and
  * y = fma(d * rsqrt(var + eps), gamma, beta), rounded once to the storage type. Rows of
- * more than 4096 16-byte vectors (32768 bf16 / 16384 fp32 columns; all pointers and the row
- * pitch 16-byte aligned) are staged in shared memory by persistent clusters of CTAs instead
- * (up to 16 x 2048 vectors: 262144 bf16 / 131072 fp32 columns). Wider rows, and rows past
+ * more than 2048 16-byte vectors (16384 bf16/f16 / 8192 fp32 columns; all pointers and the
+ * row pitch 16-byte aligned) are staged in shared memory by persistent clusters of CTAs
+ * instead (up to 16 x 2048 vectors: 262144 bf16/f16 / 131072 fp32 columns). Wider rows, and rows past
  * 16384 columns on the element path, return CAMP_ERR_NOT_SUPPORTED. Errors otherwise as for
  * camp_rmsnorm.
  */

@@ -60,7 +60,7 @@ def _rope(lib, x=X, s=SIN, c=COS, y=Y, B=1, S=4, H=2, D=8, dtype=camp.BF16):
 
 
 @pytest.mark.parametrize("kw,status", [
-    ({"dtype": 0}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({"dtype": -1}, camp.ERR_UNSUPPORTED_DTYPE),
     ({"dtype": 2}, camp.ERR_UNSUPPORTED_DTYPE),
     ({"rows": -1}, camp.ERR_INVALID_ARG),
     ({"cols": 0}, camp.ERR_INVALID_ARG),
@@ -462,7 +462,7 @@ ILP = [0x7D0000000000 + i * 0x1000000000 for i in range(5)]   # x, sin, cos, pos
 
 
 @pytest.mark.parametrize("change,kw,status", [
-    ({}, {"dtype": 0}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({}, {"dtype": 6}, camp.ERR_UNSUPPORTED_DTYPE),
     ({}, {"D": 7}, camp.ERR_INVALID_ARG),
     ({}, {"mp": -1}, camp.ERR_INVALID_ARG),
     ({3: None}, {}, camp.ERR_INVALID_ARG),
@@ -668,7 +668,7 @@ def _cat(lib, p, B=2, P=5, S=3, Hk=8, D=64, n_rep=4, dtype=camp.BF16):
 
 
 @pytest.mark.parametrize("change,kw,status", [
-    ({}, {"dtype": 0}, camp.ERR_UNSUPPORTED_DTYPE),
+    ({}, {"dtype": 8}, camp.ERR_UNSUPPORTED_DTYPE),
     ({}, {"D": 7}, camp.ERR_INVALID_ARG),
     ({}, {"D": 0}, camp.ERR_INVALID_ARG),
     ({}, {"n_rep": 0}, camp.ERR_INVALID_ARG),
@@ -787,3 +787,48 @@ def test_staged_plan_needs_16_byte_accesses(lib):
 
 def test_device_errors_argument_check(lib):
     assert lib.camp_device_errors(None, 0) == camp.ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ fp16 storage
+
+def _fields(plan, dtype):
+    """The plan's fields, or the status of a refused request."""
+    try:
+        p = plan(dtype)
+    except camp.CampError as e:
+        return e.status
+    return (p.kernel, p.vec_bytes, p.group, p.per_thread, p.block, p.grid, p.cluster)
+
+
+def _same(plan):
+    assert _fields(plan, "f16") == _fields(plan, "bf16")
+
+
+@pytest.mark.parametrize("shape", [(4096, 2048), (1, 8192), (64, 3001), (4096, 16384),
+                                   (5, 65536), (256, 131072), (2, 262152), (3, 3000)])
+def test_f16_plans_are_the_bf16_plans(lib, shape):
+    """The planners look at the element size only: binary16 gets bf16's plans everywhere."""
+    rows, cols = shape
+    _same(lambda d: camp.camp_rmsnorm_plan(X, W, Y, rows, cols, d))
+    _same(lambda d: camp.camp_add_rmsnorm_plan(X, R_, W, H_, Y, rows, cols, d))
+    _same(lambda d: camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, d))
+
+
+@pytest.mark.parametrize("B,S,H,D", [(1, 4096, 32, 64), (1, 8, 32, 64), (2, 3, 5, 6),
+                                     (1, 65536, 32, 128), (1, 4, 1024, 256)])
+def test_f16_rope_plans_are_the_bf16_plans(lib, B, S, H, D):
+    _same(lambda d: camp.camp_rope_plan(X, SIN, COS, Y, B, S, H, D, d))
+    _same(lambda d: camp.camp_rope_qk_plan(X, K_, SIN, COS, YQ, YK, B, S, H, 8, D, d))
+    _same(lambda d: camp.camp_rope_interleaved_plan(*ILP, B * S, H, D, 16, d))
+    _same(lambda d: camp.camp_kv_cat_repeat_plan(*CAT, B, S, S, 8, D, 4, d))
+
+
+@pytest.mark.parametrize("Dn,Dr", [(512, 64), (128, 64), (100, 6)])
+def test_f16_kv_cache_plans_are_the_bf16_plans(lib, Dn, Dr):
+    _same(lambda d: camp.camp_kv_rmsnorm_rope_cache_plan(*KVP, 1, 4096, Dn, Dr, 8192, d))
+
+
+def test_f16_dtype_names(lib):
+    import torch
+    for name in ("f16", "fp16", "float16", torch.float16, camp.F16):
+        assert camp._dtype(name) == camp.F16 == 0

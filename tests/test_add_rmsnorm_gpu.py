@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
-from parity import assert_bf16_close, assert_f32_close
+from parity import DTYPES, ES, assert_f32_close, assert_rounded_close
 
 pytestmark = pytest.mark.gpu
 
@@ -27,14 +27,14 @@ def _device():
 
 def _guarded(n, st):
     buf = torch.empty(n + 2 * PAD, dtype=st, device="cuda")
-    buf.view(torch.int16 if st == torch.bfloat16 else torch.int32).fill_(
-        0x7FA5 if st == torch.bfloat16 else 0x7FA5A5A5)
+    buf.view(torch.int16 if st.itemsize == 2 else torch.int32).fill_(
+        0x7FA5 if st.itemsize == 2 else 0x7FA5A5A5)
     return buf[PAD:PAD + n], buf
 
 
 def _canaries_ok(buf, n):
-    raw = buf.view(torch.int16 if buf.dtype == torch.bfloat16 else torch.int32).cpu()
-    sentinel = 0x7FA5 if buf.dtype == torch.bfloat16 else 0x7FA5A5A5
+    raw = buf.view(torch.int16 if buf.element_size() == 2 else torch.int32).cpu()
+    sentinel = 0x7FA5 if buf.element_size() == 2 else 0x7FA5A5A5
     return bool((raw[:PAD] == sentinel).all()) and bool((raw[PAD + n:] == sentinel).all())
 
 
@@ -66,9 +66,9 @@ def run_case(rows, cols, dtype, eps=1e-5, seed=0, plan=None, alias=None):
     got_h = inputs.to_numpy(h).reshape(rows, cols)
     got_y = inputs.to_numpy(y).reshape(rows, cols)
     what = f"add_rmsnorm {dtype} {rows}x{cols}"
-    if dtype == "bf16":
+    if dtype != "f32":
         np.testing.assert_array_equal(got_h, want_h, err_msg=what + " h")
-        assert_bf16_close(got_y, want_y, what + " y")
+        assert_rounded_close(got_y, want_y, dtype, what + " y")
     else:
         np.testing.assert_array_equal(got_h, want_h, err_msg=what + " h")
         ref = oracle.rmsnorm_f64(want_h.astype(np.float64), ws.astype(np.float64), eps32)
@@ -77,23 +77,23 @@ def run_case(rows, cols, dtype, eps=1e-5, seed=0, plan=None, alias=None):
         assert _canaries_ok(b, n), "write outside an output"
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cols", [1, 7, 8, 64, 1000, 2048, 3000, 3001, 8192, 20000, 40000,
                                   70000, 300001])
 def test_shapes(cols, dtype):
     run_case(3, cols, dtype, seed=cols)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("alias", ["h=r,y=x", "h=x,y=r"])
 @pytest.mark.parametrize("cols", [2048, 3001, 40000, 300001])
 def test_in_place(cols, dtype, alias):
     run_case(5, cols, dtype, seed=cols + 3, alias=alias)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_variant(dtype):
-    es = 2 if dtype == "bf16" else 4
+    es = ES[dtype]
     e = 16 // es
     for g in (32, 64, 128, 256, 512, 1024):
         for nv in (1, 2, 3, 4, 6, 8):

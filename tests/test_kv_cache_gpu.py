@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
-from parity import assert_bf16_close, assert_f32_close
+from parity import DTYPES, ES, assert_f32_close, assert_rounded_close
 
 pytestmark = pytest.mark.gpu
 
@@ -57,9 +57,9 @@ def run_case(B, S, Dn, Dr, dtype, seed=0, plan=None, num_slots=None, pad=True):
     # untouched rows: bit for bit
     np.testing.assert_array_equal(got_n[~written], inputs.to_numpy(cn_cpu)[~written], what)
     np.testing.assert_array_equal(got_r[~written], inputs.to_numpy(cr_cpu)[~written], what)
-    if dtype == "bf16":
-        assert_bf16_close(got_n[written], want_n[written], what + " norm")
-        assert_bf16_close(got_r[written], want_r[written], what + " rope")
+    if dtype != "f32":
+        assert_rounded_close(got_n[written], want_n[written], dtype, what + " norm")
+        assert_rounded_close(got_r[written], want_r[written], dtype, what + " rope")
     else:
         # fp32: compare with the unrounded fp64 results of the two pinned operators
         kvs = inputs.to_numpy(kv_cpu).astype(np.float64)
@@ -77,16 +77,16 @@ def run_case(B, S, Dn, Dr, dtype, seed=0, plan=None, num_slots=None, pad=True):
             assert_f32_close(got_r[slot], ref_r, what + " rope")
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", [(2, 300, 512, 64), (1, 7, 512, 64), (3, 17, 128, 32),
                                    (2, 9, 33, 6), (1, 5, 1000, 128), (2, 4, 8, 2)])
 def test_shapes(shape, dtype):
     run_case(*shape, dtype, seed=sum(shape))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_variant(dtype):
-    es = 2 if dtype == "bf16" else 4
+    es = ES[dtype]
     # (norm access bytes, norm accesses per lane, rope access bytes per half and lane)
     variants = [(16, nvn, rb) for nvn in (1, 2, 4, 8) for rb in (4, 8, 16) if rb >= 2 * es]
     variants += [(es, nvn, es) for nvn in (1, 2, 4, 8, 16)]

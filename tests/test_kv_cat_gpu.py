@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
-from parity import assert_bf16_close, assert_f32_close
+from parity import DTYPES, ES, assert_f32_close, assert_rounded_close
 
 pytestmark = pytest.mark.gpu
 
@@ -78,8 +78,8 @@ def run_case(B, P, S, Hk, D, n_rep, dtype, seed=0, plan=None, tables=True, shift
     np.testing.assert_array_equal(got[:, :copied], want[:, :copied], what + " (copied rows)")
     if not tables or S == 0:
         return
-    if dtype == "bf16":
-        assert_bf16_close(got[:, P:], want[:, P:], what)
+    if dtype != "f32":
+        assert_rounded_close(got[:, P:], want[:, P:], dtype, what)
     else:
         # fp32: against the unrounded fp64 rotation at table rows P .. P+S-1, repeated
         ref = oracle.rope_f64(inputs.to_numpy(new_cpu), sin_np[P:T], cos_np[P:T])
@@ -96,27 +96,27 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", SHAPES)
 def test_shapes(shape, dtype):
     run_case(*shape, dtype, seed=sum(shape))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_without_tables_is_a_copy(dtype):
     run_case(2, 40, 24, 8, 64, 4, dtype, seed=3, tables=False)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_element_aligned_pointers(dtype):
     # inputs one element past a 16-byte boundary: element accesses
     run_case(2, 33, 9, 8, 64, 4, dtype, seed=5, shift=1)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_variant(dtype):
-    es = 2 if dtype == "bf16" else 4
-    for vb in ((16, 8, 4, 2) if dtype == "bf16" else (16, 8, 4)):
+    es = ES[dtype]
+    for vb in ((16, 8, 4, 2) if ES[dtype] == 2 else (16, 8, 4)):
         for hpt in (1, 2, 4, 8):
             D = 2 * 3 * vb // es                      # three vectors a half
             plan = camp.Plan(kernel=camp.KERNEL_KV_CAT, vec_bytes=vb, group=hpt)

@@ -13,7 +13,7 @@ normalized value, the fp32 kernel satisfies, per element,
 (the deviation d = (x - K) - mu is off by <= (k + 3) u mean|x - K|; var by a relative
 (k + 2) u + 2 (k + 3) u c; rsqrtf adds 2 ulp, var + eps and the product one rounding each,
 and the final fma one rounding of |y|). A bf16 result adds the half ulp of its last
-rounding. LayerNorm has no 1-ulp rule like RMSNorm's: beta and gamma * xhat can cancel, and
+rounding, and an fp16 result the half ulp of binary16. LayerNorm has no 1-ulp rule like RMSNorm's: beta and gamma * xhat can cancel, and
 then the fp32 error, relative to the operands, is many ulps of the tiny result.
 """
 
@@ -25,6 +25,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
+from parity import DTYPES, ES, half_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -44,27 +45,23 @@ def _decode(t: torch.Tensor) -> np.ndarray:
     return inputs.to_numpy(t.float()).astype(np.float64)
 
 
-def _bf16_half_ulp(a: np.ndarray) -> np.ndarray:
-    e = np.floor(np.log2(np.maximum(np.abs(a), 2.0 ** -126)))
-    return np.ldexp(1.0, (e - 8).astype(np.int64))
-
-
 def _guarded(n, st):
     buf = torch.empty(n + 2 * PAD, dtype=st, device="cuda")
-    buf.view(torch.int16 if st == torch.bfloat16 else torch.int32).fill_(
-        0x7FA5 if st == torch.bfloat16 else 0x7FA5A5A5)
+    buf.view(torch.int16 if st.itemsize == 2 else torch.int32).fill_(
+        0x7FA5 if st.itemsize == 2 else 0x7FA5A5A5)
     return buf[PAD:PAD + n], buf
 
 
 def _canaries_ok(buf, n):
-    raw = buf.view(torch.int16 if buf.dtype == torch.bfloat16 else torch.int32).cpu()
-    sentinel = 0x7FA5 if buf.dtype == torch.bfloat16 else 0x7FA5A5A5
+    raw = buf.view(torch.int16 if buf.element_size() == 2 else torch.int32).cpu()
+    sentinel = 0x7FA5 if buf.element_size() == 2 else 0x7FA5A5A5
     return bool((raw[:PAD] == sentinel).all()) and bool((raw[PAD + n:] == sentinel).all())
 
 
 def check(got: torch.Tensor, x_cpu, g_cpu, b_cpu, eps32: float, plan: camp.Plan, what: str):
     rows, cols = x_cpu.shape
-    es = 2 if x_cpu.dtype == torch.bfloat16 else 4
+    dtype = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[x_cpu.dtype]
+    es = ES[dtype]
     if plan.kernel == camp.KERNEL_LAYERNORM_STAGED:
         # a thread's vectors (its share of the CTA chunk), the warp butterfly, the CTA's 8
         # warp partials, the cluster's partials
@@ -77,10 +74,10 @@ def check(got: torch.Tensor, x_cpu, g_cpu, b_cpu, eps32: float, plan: camp.Plan,
     for r0 in range(0, rows, step):
         r1 = min(rows, r0 + step)
         _check_rows(_decode(got[r0:r1]), _decode(x_cpu[r0:r1]), g, b, eps32, k, r0,
-                    x_cpu.dtype == torch.bfloat16, what)
+                    dtype, what)
 
 
-def _check_rows(y, x, g, b, eps32, k, r0, bf16, what):
+def _check_rows(y, x, g, b, eps32, k, r0, dtype, what):
     ref, _ = oracle.layernorm_f64(x, g, b, eps32)
     dev = x - x[:, :1]
     var = ((x - x.mean(axis=1, keepdims=True)) ** 2).mean(axis=1, keepdims=True)
@@ -88,8 +85,8 @@ def _check_rows(y, x, g, b, eps32, k, r0, bf16, what):
     c = np.abs(dev).mean(axis=1, keepdims=True) / sig
     xhat = (x - x.mean(axis=1, keepdims=True)) / sig
     bound = U32 * ((k + 4) * np.abs(g) * (c + np.abs(xhat) * (1 + c)) + np.abs(ref))
-    if bf16:
-        bound = bound + _bf16_half_ulp(np.maximum(np.abs(ref), np.abs(y)))
+    if dtype != "f32":
+        bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(y)), dtype)
     err = np.abs(y - ref)
     bad = ~(err <= bound)
     if bad.any():
@@ -125,7 +122,7 @@ def run_case(rows, cols, dtype, eps=1e-5, seed=0, plan=None, in_place=False):
         assert _canaries_ok(buf, n), "write outside the output"
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cols", [1, 2, 7, 8, 64, 768, 1000, 2048, 3000, 3001, 4096, 8192,
                                   12288, 16384, 20000, 32768])
 def test_shapes(cols, dtype):
@@ -136,15 +133,15 @@ def test_widest_bf16_row():
     run_case(5, 65536, "bf16", seed=4)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cols", [8, 2048, 3001, 20000])
 def test_in_place(cols, dtype):
     run_case(7, cols, dtype, seed=cols + 1, in_place=True)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_variant(dtype):
-    es = 2 if dtype == "bf16" else 4
+    es = ES[dtype]
     e = 16 // es
     for g in (32, 64, 128, 256, 512, 1024):
         for nv in (1, 2, 3, 4, 6, 8):
@@ -158,7 +155,7 @@ def test_every_variant(dtype):
             run_case(3, max(1, g * nv - 1), dtype, seed=g * nv, plan=plan)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_constant_rows_give_beta_exactly(dtype):
     # every deviation is exactly 0 in both the kernel and the definition: y = beta
     rows, cols = 6, 3001
@@ -207,3 +204,8 @@ def test_config_bf16_4096x2048():
 
 def test_config_bf16_16384x8192():
     run_case(16384, 8192, "bf16", eps=1e-6, seed=0)
+
+
+def test_config_f16_8192x4096():
+    # the TileLang tutorial's example 2 (chapter 02): M = 8192 rows, H = 4096 columns, fp16
+    run_case(8192, 4096, "f16", seed=0)

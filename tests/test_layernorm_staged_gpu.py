@@ -9,6 +9,7 @@ import pytest
 import torch
 
 from block_memory_bound_gb300 import camp
+from parity import DTYPES, ES
 
 import test_layernorm_gpu as ln_tests
 
@@ -31,7 +32,7 @@ def plan(cluster: int, stages: int) -> camp.Plan:
                      per_thread=stages)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cols", [40000, 65536, 65544, 131072, 262144])
 def test_wide_rows_default_plan(cols, dtype):
     if dtype == "f32" and cols > 131072:
@@ -39,24 +40,24 @@ def test_wide_rows_default_plan(cols, dtype):
     ln_tests.run_case(6, cols, dtype, seed=cols % 97)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("stages", [2, 3, 4])
 def test_every_variant(dtype, cluster, stages):
-    e = 8 if dtype == "bf16" else 4
+    e = 16 // ES[dtype]
     ln_tests.run_case(23, (cluster * 500 - 3) * e, dtype, seed=cluster * 10 + stages,
                       plan=plan(cluster, stages))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_ctas_with_only_the_head_to_load(dtype):
-    e = 8 if dtype == "bf16" else 4
+    e = 16 // ES[dtype]
     ln_tests.run_case(5, 3 * e, dtype, seed=1, plan=plan(16, 2))   # ranks 3..15 own nothing
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_many_rows_per_cluster(dtype):
-    cols = 65536 if dtype == "bf16" else 32768
+    cols = 65536 if ES[dtype] == 2 else 32768
     ln_tests.run_case(700, cols, dtype, seed=2)
     ln_tests.run_case(2000, 16384, dtype, seed=3, plan=plan(2, 3))
 

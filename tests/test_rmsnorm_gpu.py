@@ -2,7 +2,7 @@
 
 Element-by-element at sizes the oracle finishes in seconds (several tiles and ragged
 tails), at the full benchmark configurations, and on sampled rows at the largest sweep
-sizes. bf16 outputs must be within 1 ulp of the oracle rounded once; fp32 outputs within
+sizes. bf16 and fp16 outputs must be within 1 ulp of the oracle rounded once; fp32 outputs within
 1e-6 + 2e-6 |ref| of the oracle's fp64 result.
 """
 
@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
-from parity import assert_bf16_close, assert_f32_close
+from parity import DTYPES, ES, assert_bf16_close, assert_f32_close, assert_rounded_close
 
 pytestmark = pytest.mark.gpu
 
@@ -32,16 +32,16 @@ def _device():
 def _guarded_empty(n: int, dtype: torch.dtype, offset: int = 0):
     """An output of n elements inside a canary-filled buffer; returns (view, buffer)."""
     buf = torch.empty(n + 2 * PAD + offset, dtype=dtype, device="cuda")
-    if dtype == torch.bfloat16:
-        buf.view(torch.int16).fill_(0x7FA5)      # a NaN pattern no kernel produces
+    if dtype.itemsize == 2:
+        buf.view(torch.int16).fill_(0x7FA5)      # a NaN pattern (bf16 and fp16) no kernel produces
     else:
         buf.view(torch.int32).fill_(0x7FA5A5A5)
     return buf[PAD + offset:PAD + offset + n], buf
 
 
 def _check_canaries(buf: torch.Tensor, n: int, offset: int = 0) -> None:
-    raw = buf.view(torch.int16 if buf.dtype == torch.bfloat16 else torch.int32).cpu()
-    sentinel = 0x7FA5 if buf.dtype == torch.bfloat16 else 0x7FA5A5A5
+    raw = buf.view(torch.int16 if buf.element_size() == 2 else torch.int32).cpu()
+    sentinel = 0x7FA5 if buf.element_size() == 2 else 0x7FA5A5A5
     head = raw[:PAD + offset]
     tail = raw[PAD + offset + n:]
     assert bool((head == sentinel).all()), "write before the output"
@@ -53,9 +53,9 @@ def _oracle_check(x_cpu, w_cpu, y_dev, eps: float, dtype: str, what: str) -> Non
     xs = inputs.to_numpy(x_cpu).reshape(-1, x_cpu.shape[-1])
     ws = inputs.to_numpy(w_cpu)
     got = inputs.to_numpy(y_dev).reshape(xs.shape)
-    if dtype == "bf16":
-        want = oracle.rmsnorm(xs, ws, eps32, "bf16")
-        assert_bf16_close(got, want, what)
+    if dtype != "f32":
+        want = oracle.rmsnorm(xs, ws, eps32, dtype)
+        assert_rounded_close(got, want, dtype, what)
     else:
         ref = oracle.rmsnorm_f64(xs.astype(np.float64), ws.astype(np.float64), eps32)
         assert_f32_close(got, ref, what)
@@ -92,14 +92,14 @@ def run_case(rows, cols, dtype, eps=1e-5, seed=0, stress=False, plan=None, inpla
 COLS = [1, 2, 7, 8, 33, 64, 256, 1000, 2048, 2056, 3000, 3001, 4096, 8192, 8200, 20000]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cols", COLS)
 @pytest.mark.parametrize("rows", [1, 3, 37])
 def test_shapes_and_tails(rows, cols, dtype):
     run_case(rows, cols, dtype, seed=rows * 7 + cols)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cols", [12288, 16384, 40000, 65536, 70000, 131072, 262144, 300001,
                                   524296])
 def test_wide_rows(cols, dtype):
@@ -110,14 +110,14 @@ def test_cluster_rows_many():
     run_case(777, 16384, "bf16", seed=9)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_many_rows_ragged(dtype):
     run_case(1001, 3000, dtype, seed=5)
 
 
 def test_p3_style_deterministic_case():
     # xserv unit-test style data: 4 rows of 768, x = ((i mod 17) - 8) / 10, gamma 0.5/0.7/0.9.
-    for dtype in ("bf16", "f32"):
+    for dtype in DTYPES:
         x_cpu, w_cpu = inputs.p3_style_rmsnorm_inputs(4, 768, dtype)
         run_case(4, 768, dtype, x_cpu=x_cpu, w_cpu=w_cpu)
 
@@ -125,6 +125,7 @@ def test_p3_style_deterministic_case():
 @pytest.mark.parametrize("eps", [0.0, 1e-6, 1e-5, 1e-2])
 def test_eps_values(eps):
     run_case(17, 2048, "bf16", eps=eps, seed=11)
+    run_case(17, 2048, "f16", eps=eps, seed=13)
     run_case(17, 2048, "f32", eps=eps, seed=12)
 
 
@@ -140,7 +141,7 @@ def test_constant_rows_match_closed_form_within_tolerance():
 # ------------------------------------------------------------------ every compiled variant
 
 def _variants(dtype: str):
-    es = 2 if dtype == "bf16" else 4
+    es = ES[dtype]
     out = []
     for g in (32, 64, 128, 256, 512, 1024):
         for nv in (1, 2, 3, 4, 6, 8):
@@ -151,9 +152,9 @@ def _variants(dtype: str):
     return out
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_rows_variant(dtype):
-    es = 2 if dtype == "bf16" else 4
+    es = ES[dtype]
     for vb, g, nv in _variants(dtype):
         e = vb // es
         # Widest row the variant holds, minus one vector: the last accesses are masked.
@@ -162,10 +163,10 @@ def test_every_rows_variant(dtype):
         run_case(5, cols, dtype, seed=g + nv, plan=plan)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cluster", [2, 4, 8, 16])
 def test_every_cluster_variant(dtype, cluster):
-    e = 8 if dtype == "bf16" else 4
+    e = 16 // ES[dtype]
     for nv in (1, 2, 3, 4, 6, 8):
         # one vector short of the capacity: the last CTA's last access is masked
         cols = (cluster * 256 * nv - 1) * e
@@ -178,10 +179,10 @@ def test_every_cluster_variant(dtype, cluster):
     run_case(4, 8 * e, dtype, seed=cluster, plan=plan)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("vb", ["vector", "element"])
 def test_wide_kernel_forced(dtype, vb):
-    es = 2 if dtype == "bf16" else 4
+    es = ES[dtype]
     plan = camp.Plan(kernel=camp.KERNEL_RMSNORM_WIDE, vec_bytes=16 if vb == "vector" else es)
     run_case(9, 8192, dtype, seed=2, plan=plan)
     run_case(4, 24, dtype, seed=3, plan=plan)
@@ -189,19 +190,19 @@ def test_wide_kernel_forced(dtype, vb):
 
 # ------------------------------------------------------------------ aliasing, alignment, streams
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("cols", [2048, 3001, 40000, 70000, 524296])
 def test_in_place(cols, dtype):
     run_case(7, cols, dtype, seed=cols + 1, inplace=True)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_misaligned_pointers_take_the_element_path(dtype):
     x_cpu, w_cpu = inputs.rmsnorm_inputs(9, 2048, dtype, seed=4)
     x = torch.empty(9 * 2048 + 1, dtype=inputs.STORAGE[dtype], device="cuda")[1:].view(9, 2048)
     w = w_cpu.cuda()
     plan = camp.camp_rmsnorm_plan(x, w, torch.empty_like(x), 9, 2048, dtype)
-    assert plan.vec_bytes == (2 if dtype == "bf16" else 4)
+    assert plan.vec_bytes == (2 if ES[dtype] == 2 else 4)
     run_case(9, 2048, dtype, x_offset=1, y_offset=1, x_cpu=x_cpu, w_cpu=w_cpu)
 
 
@@ -232,6 +233,24 @@ def test_config_bf16_4096x2048():
 
 def test_config_bf16_16384x8192_stress():
     run_case(16384, 8192, "bf16", eps=1e-6, seed=0, stress=True)
+
+
+def test_f16_stress_rows_partly_subnormal():
+    # binary16: the stress recipe's 1e-4 rows hold subnormal inputs, its 1e3 rows reach ~4e3
+    run_case(1000, 4096, "f16", eps=1e-6, seed=21, stress=True)
+
+
+def test_f16_overflow_rounds_to_infinity():
+    # One nonzero element a row: y = x / sqrt(x^2 / 64 + eps) * w, about 8 * 10000 in
+    # magnitude, past binary16's largest finite value (65504): +inf and -inf, as in the oracle.
+    cols = 64
+    x = torch.zeros(2, cols)
+    x[0, 0] = 1.0
+    x[1, 5] = -3.0
+    w = torch.full((cols,), 10000.0)
+    y = run_case(2, cols, "f16", x_cpu=x.to(torch.float16), w_cpu=w.to(torch.float16)).cpu()
+    assert y[0, 0].item() == float("inf") and y[1, 5].item() == float("-inf")
+    assert int(torch.isinf(y).sum()) == 2
 
 
 def _sampled_rows(rows: int, k: int, seed: int) -> torch.Tensor:

@@ -1,6 +1,6 @@
 """Rotate-half RoPE parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
-bf16 outputs must be within 1 ulp of the oracle rounded once; fp32 outputs within
+bf16 and fp16 outputs must be within 1 ulp of the oracle rounded once; fp32 outputs within
 1e-6 + 2e-6 |ref| of the oracle's fp64 result. Position 0 (cos = 1, sin = 0) must
 reproduce the input bit for bit.
 """
@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
-from parity import assert_bf16_close, assert_f32_close
+from parity import DTYPES, ES, assert_bf16_close, assert_f32_close, assert_rounded_close
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +33,8 @@ def _oracle_check(x_cpu, sin_cpu, cos_cpu, y_dev, dtype, what):
     got = inputs.to_numpy(y_dev).reshape(xs.shape)
     s = sin_cpu.numpy()
     c = cos_cpu.numpy()
-    if dtype == "bf16":
-        assert_bf16_close(got, oracle.rope(xs, s, c, "bf16"), what)
+    if dtype != "f32":
+        assert_rounded_close(got, oracle.rope(xs, s, c, dtype), dtype, what)
     else:
         assert_f32_close(got, oracle.rope_f64(xs.astype(np.float64), s, c), what)
 
@@ -57,8 +57,8 @@ def run_case(B, S, H, D, dtype, seed=0, plan=None, inplace=False, x_offset=0, y_
         y, ybuf = x, None
     else:
         ybuf = torch.empty(n + 2 * PAD + y_offset, dtype=st, device="cuda")
-        ybuf.view(torch.int16 if st == torch.bfloat16 else torch.int32).fill_(
-            0x7FA5 if st == torch.bfloat16 else 0x7FA5A5A5)
+        ybuf.view(torch.int16 if st.itemsize == 2 else torch.int32).fill_(
+            0x7FA5 if st.itemsize == 2 else 0x7FA5A5A5)
         y = ybuf[PAD + y_offset:PAD + y_offset + n].view(B, S, H, D)
     if plan is None:
         camp.camp_rope(x, sin_d, cos_d, y, B, S, H, D, dtype)
@@ -67,8 +67,8 @@ def run_case(B, S, H, D, dtype, seed=0, plan=None, inplace=False, x_offset=0, y_
     torch.cuda.synchronize()
     _oracle_check(x_cpu, sin_cpu, cos_cpu, y, dtype, f"rope {dtype} {(B, S, H, D)}")
     if ybuf is not None:
-        raw = ybuf.view(torch.int16 if st == torch.bfloat16 else torch.int32).cpu()
-        sentinel = 0x7FA5 if st == torch.bfloat16 else 0x7FA5A5A5
+        raw = ybuf.view(torch.int16 if st.itemsize == 2 else torch.int32).cpu()
+        sentinel = 0x7FA5 if st.itemsize == 2 else 0x7FA5A5A5
         assert bool((raw[:PAD + y_offset] == sentinel).all()), "write before the output"
         assert bool((raw[PAD + y_offset + n:] == sentinel).all()), "write past the output"
     return x_cpu, y
@@ -78,13 +78,13 @@ SHAPES = [(1, 1, 1, 2), (2, 3, 5, 6), (1, 7, 32, 64), (1, 16, 8, 128), (2, 33, 3
           (3, 5, 7, 136), (1, 9, 4, 16), (2, 4, 6, 32), (1, 300, 32, 64), (4, 64, 8, 128)]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", SHAPES)
 def test_shapes(shape, dtype):
     run_case(*shape, dtype, seed=sum(shape))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_position_zero_is_identity(dtype):
     x_cpu, y = run_case(2, 5, 8, 64, dtype, seed=1)
     got = inputs.to_numpy(y)[:, 0]
@@ -92,10 +92,10 @@ def test_position_zero_is_identity(dtype):
 
 
 @pytest.mark.parametrize("kernel", ["tiled", "flat"])
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_variant(dtype, kernel):
-    es = 2 if dtype == "bf16" else 4
-    vbs = (16, 8, 4, 2) if dtype == "bf16" else (16, 8, 4)
+    es = ES[dtype]
+    vbs = (16, 8, 4, 2) if ES[dtype] == 2 else (16, 8, 4)
     kid = camp.KERNEL_ROPE if kernel == "tiled" else camp.KERNEL_ROPE_FLAT
     for vb in vbs:
         for hpt in (1, 2, 4, 8):
@@ -114,13 +114,13 @@ def test_table_row_of_every_position(S):
     run_case(3, S, 2, 16, "bf16", seed=S)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", [(1, 8, 32, 64), (2, 3, 5, 6)])
 def test_in_place(shape, dtype):
     run_case(*shape, dtype, seed=3, inplace=True)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_misaligned_pointers(dtype):
     run_case(1, 6, 4, 64, dtype, seed=5, x_offset=1, y_offset=1, table_offset=1)
 
@@ -138,6 +138,11 @@ def test_config_q_1x4096x32x64():
 
 def test_config_k_1x4096x8x64():
     run_case(1, 4096, 8, 64, "bf16", seed=0)
+
+
+def test_config_f16_1x4096x32x128():
+    # the TileLang tutorial's exercise E13 (chapter 02): B = 1, 32 heads, S = 4096, d = 128, fp16
+    run_case(1, 4096, 32, 128, "f16", seed=0)
 
 
 @pytest.mark.parametrize("tokens", [1, 8, 64, 512, 4096, 65536])

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
-from parity import assert_bf16_close, assert_f32_close
+from parity import DTYPES, ES, assert_f32_close, assert_rounded_close
 
 pytestmark = pytest.mark.gpu
 
@@ -54,8 +54,8 @@ def run_case(T, H, D, dtype, max_pos=None, seed=0, plan=None, inplace=False):
                                    inputs.to_numpy(base), dtype)
     got = inputs.to_numpy(y)
     what = f"rope interleaved {dtype} {(T, H, D)}"
-    if dtype == "bf16":
-        assert_bf16_close(got, want, what)
+    if dtype != "f32":
+        assert_rounded_close(got, want, dtype, what)
     else:
         # fp32: against the unrounded fp64 pair formula (written out here for the check)
         xs = inputs.to_numpy(x_cpu).astype(np.float64)
@@ -72,24 +72,24 @@ def run_case(T, H, D, dtype, max_pos=None, seed=0, plan=None, inplace=False):
         assert_f32_close(got, ref, what)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", [(1, 1, 2), (7, 3, 6), (33, 32, 64), (64, 8, 128), (300, 5, 20),
                                    (16, 64, 128), (2048, 32, 128)])
 def test_shapes(shape, dtype):
     run_case(*shape, dtype, seed=sum(shape))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_variant(dtype):
-    es = 2 if dtype == "bf16" else 4
-    for vb in ((16, 8, 4) if dtype == "bf16" else (16, 8)):
+    es = ES[dtype]
+    for vb in ((16, 8, 4) if ES[dtype] == 2 else (16, 8)):
         for hpt in (1, 2, 4, 8):
             D = 3 * vb // es                      # three vectors per head row
             plan = camp.Plan(kernel=camp.KERNEL_ROPE_INTERLEAVED, vec_bytes=vb, group=hpt)
             run_case(11, 2 * hpt + 1, D, dtype, seed=vb * hpt, plan=plan)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_in_place(dtype):
     run_case(40, 8, 64, dtype, seed=9, inplace=True)
 

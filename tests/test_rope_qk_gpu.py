@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from block_memory_bound_gb300 import camp, inputs
-from parity import assert_bf16_close, assert_f32_close
+from parity import DTYPES, ES, assert_f32_close, assert_rounded_close
 
 pytestmark = pytest.mark.gpu
 
@@ -25,8 +25,9 @@ def _device():
 def _check(x_cpu, sin_cpu, cos_cpu, y_dev, dtype, what):
     xs = inputs.to_numpy(x_cpu)
     got = inputs.to_numpy(y_dev).reshape(xs.shape)
-    if dtype == "bf16":
-        assert_bf16_close(got, oracle.rope(xs, sin_cpu.numpy(), cos_cpu.numpy(), "bf16"), what)
+    if dtype != "f32":
+        assert_rounded_close(got, oracle.rope(xs, sin_cpu.numpy(), cos_cpu.numpy(), dtype),
+                             dtype, what)
     else:
         assert_f32_close(got, oracle.rope_f64(xs.astype(np.float64), sin_cpu.numpy(),
                                               cos_cpu.numpy()), what)
@@ -53,23 +54,23 @@ SHAPES = [(1, 4096, 32, 8, 64), (2, 33, 6, 2, 16), (1, 7, 3, 1, 64), (3, 17, 4, 
           (2, 9, 5, 3, 6), (1, 5, 1024, 8, 256)]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", SHAPES)
 def test_shapes(shape, dtype):
     run_qk(*shape, dtype, seed=sum(shape))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_fused_variant(dtype):
-    es = 2 if dtype == "bf16" else 4
-    for vb in ((16, 8, 4, 2) if dtype == "bf16" else (16, 8, 4)):
+    es = ES[dtype]
+    for vb in ((16, 8, 4, 2) if ES[dtype] == 2 else (16, 8, 4)):
         for hpt in (1, 2, 4, 8):
             D = 2 * (vb // es) * 3
             plan = camp.Plan(kernel=camp.KERNEL_ROPE, vec_bytes=vb, group=hpt)
             run_qk(2, 11, 2 * hpt + 1, hpt + 1, D, dtype, seed=vb * hpt, plan=plan)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_in_place(dtype):
     run_qk(2, 19, 8, 2, 64, dtype, seed=4, inplace=True)
 
