@@ -527,12 +527,13 @@ def end_to_end(sets, steps: int, world: int, dist) -> dict:
 
 # ------------------------------------------------------------------ large configurations
 
-def _kv_cat_tensors(B, P, S, Hk, D, n_rep):
+def _kv_cat_tensors(B, P, S, Hk, D, n_rep, dt="bf16"):
     """Device inputs of one KV concat + repeat call: past, new, tables [P+S, D/2], output."""
-    past = torch.randn(B, P, Hk, D, device="cuda").to(torch.bfloat16)
-    new = torch.randn(B, S, Hk, D, device="cuda").to(torch.bfloat16)
-    _, sn, cs = inputs.rope_inputs(1, P + S, 1, D, "bf16", seed=0, device="cuda")
-    out = torch.empty(B, P + S, Hk * n_rep, D, device="cuda", dtype=torch.bfloat16)
+    st = inputs.STORAGE[dt]
+    past = torch.randn(B, P, Hk, D, device="cuda").to(st)
+    new = torch.randn(B, S, Hk, D, device="cuda").to(st)
+    _, sn, cs = inputs.rope_inputs(1, P + S, 1, D, dt, seed=0, device="cuda")
+    out = torch.empty(B, P + S, Hk * n_rep, D, device="cuda", dtype=st)
     return past, new, sn, cs, out
 
 
@@ -794,86 +795,91 @@ def large_configs(peak: float, reps: int, cases=None, cpu: bool = False) -> list
 
 def run_case(case: str, launches: int) -> None:
     """Launch one operator `launches` times at one shape (inputs drawn on the device),
-    for profilers; prints the plan and the launch count."""
-    kind, _, shape = case.partition(":")
+    for profilers; prints the plan and the launch count. `case` is kind:AxBx..[:dtype]
+    (dtype bf16 when left out)."""
+    kind, _, rest = case.partition(":")
+    shape, _, dt = rest.partition(":")
+    dt = dt or "bf16"
+    code = camp._dtype(dt)
+    st = inputs.STORAGE[dt]
     dims = [int(v) for v in shape.split("x")]
     torch.cuda.set_device(0)
     camp.load()
     stream = torch.cuda.current_stream().cuda_stream
     if kind == "rmsnorm":
         rows, cols = dims
-        x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
+        x, w = inputs.rmsnorm_inputs(rows, cols, dt, seed=0, device="cuda")
         y = torch.empty_like(x)
-        plan = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, "bf16"))
+        plan = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, dt), dt)
         for _ in range(launches):
-            camp.camp_rmsnorm(x, w, y, rows, cols, EPS, camp.BF16, stream)
+            camp.camp_rmsnorm(x, w, y, rows, cols, EPS, code, stream)
     elif kind == "add":
         rows, cols = dims
-        x, w = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
-        r, _ = inputs.rmsnorm_inputs(rows, cols, "bf16", seed=1, device="cuda")
+        x, w = inputs.rmsnorm_inputs(rows, cols, dt, seed=0, device="cuda")
+        r, _ = inputs.rmsnorm_inputs(rows, cols, dt, seed=1, device="cuda")
         h, y = torch.empty_like(x), torch.empty_like(x)
         plan = "add_" + plan_name("rmsnorm", camp.camp_add_rmsnorm_plan(x, r, w, h, y, rows, cols,
-                                                                        "bf16"))
+                                                                        dt), dt)
         for _ in range(launches):
-            camp.camp_add_rmsnorm(x, r, w, h, y, rows, cols, EPS, camp.BF16, stream)
+            camp.camp_add_rmsnorm(x, r, w, h, y, rows, cols, EPS, code, stream)
     elif kind == "layernorm":
         rows, cols = dims
-        x, w, bt = inputs.layernorm_inputs(rows, cols, "bf16", seed=0, device="cuda")
+        x, w, bt = inputs.layernorm_inputs(rows, cols, dt, seed=0, device="cuda")
         y = torch.empty_like(x)
-        plan = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, "bf16"))
+        plan = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, dt), dt)
         for _ in range(launches):
-            camp.camp_layernorm(x, w, bt, y, rows, cols, EPS, camp.BF16, stream)
+            camp.camp_layernorm(x, w, bt, y, rows, cols, EPS, code, stream)
     elif kind == "rope_il":
         T, H, D = dims
         mp = 2 * T
-        x = torch.randn(T, H, D, device="cuda").to(torch.bfloat16)
+        x = torch.randn(T, H, D, device="cuda").to(st)
         y = torch.empty_like(x)
         sn = torch.empty(mp, D // 2, device="cuda")
         cs = torch.empty(mp, D // 2, device="cuda")
         camp.camp_rope_tables(sn, cs, mp, D, THETA, stream)
         pos = torch.randint(0, mp, (T,), device="cuda", dtype=torch.int32)
-        p = camp.camp_rope_interleaved_plan(x, sn, cs, pos, y, T, H, D, mp, "bf16")
-        plan = f"rope_interleaved<bf16,vec{p.vec_bytes},hpt{p.group}>"
+        p = camp.camp_rope_interleaved_plan(x, sn, cs, pos, y, T, H, D, mp, dt)
+        plan = f"rope_interleaved<{dt},vec{p.vec_bytes},hpt{p.group}>"
         for _ in range(launches):
-            camp.camp_rope_interleaved(x, sn, cs, pos, y, T, H, D, mp, camp.BF16, stream)
+            camp.camp_rope_interleaved(x, sn, cs, pos, y, T, H, D, mp, code, stream)
     elif kind == "kv":
         S, Dn, Dr = dims
         ns = 2 * S
-        x = torch.randn(1, S, Dn + Dr, device="cuda").to(torch.bfloat16)
-        gam = torch.ones(Dn, device="cuda", dtype=torch.bfloat16)
-        _, sn, cs = inputs.rope_inputs(1, S, 1, Dr, "bf16", seed=0, device="cuda")
+        x = torch.randn(1, S, Dn + Dr, device="cuda").to(st)
+        gam = torch.ones(Dn, device="cuda", dtype=st)
+        _, sn, cs = inputs.rope_inputs(1, S, 1, Dr, dt, seed=0, device="cuda")
         slots = torch.randperm(ns, device="cuda")[:S].to(torch.int64)
-        y = torch.empty(ns, Dn, device="cuda", dtype=torch.bfloat16)
-        yr = torch.empty(ns, Dr, device="cuda", dtype=torch.bfloat16)
+        y = torch.empty(ns, Dn, device="cuda", dtype=st)
+        yr = torch.empty(ns, Dr, device="cuda", dtype=st)
         p = camp.camp_kv_rmsnorm_rope_cache_plan(x, gam, sn, cs, slots, y, yr, 1, S, Dn, Dr, ns,
-                                                 "bf16")
-        plan = f"kv_cache<bf16,vec{p.vec_bytes},nv{p.per_thread}>"
+                                                 dt)
+        plan = f"kv_cache<{dt},vec{p.vec_bytes},nv{p.per_thread}>"
         for _ in range(launches):
             camp.camp_kv_rmsnorm_rope_cache(x, gam, sn, cs, slots, y, yr, 1, S, Dn, Dr, ns, EPS,
-                                            camp.BF16, stream)
+                                            code, stream)
     elif kind == "kvcat":
         B, P, S, Hk, D, nr = dims
-        x, nw, sn, cs, y = _kv_cat_tensors(B, P, S, Hk, D, nr)
-        p = camp.camp_kv_cat_repeat_plan(x, nw, sn, cs, y, B, P, S, Hk, D, nr, "bf16")
-        plan = f"kv_cat_repeat<bf16,vec{p.vec_bytes},hpt{p.group}>"
+        x, nw, sn, cs, y = _kv_cat_tensors(B, P, S, Hk, D, nr, dt)
+        p = camp.camp_kv_cat_repeat_plan(x, nw, sn, cs, y, B, P, S, Hk, D, nr, dt)
+        plan = f"kv_cat_repeat<{dt},vec{p.vec_bytes},hpt{p.group}>"
         for _ in range(launches):
-            camp.camp_kv_cat_repeat(x, nw, sn, cs, y, B, P, S, Hk, D, nr, camp.BF16, stream)
+            camp.camp_kv_cat_repeat(x, nw, sn, cs, y, B, P, S, Hk, D, nr, code, stream)
     elif kind == "rope_qk":
         B, S, Hq, Hk, D = dims
-        q, sn, cs = inputs.rope_inputs(B, S, Hq, D, "bf16", seed=0, device="cuda")
-        k, _, _ = inputs.rope_inputs(B, S, Hk, D, "bf16", seed=1, device="cuda")
+        q, sn, cs = inputs.rope_inputs(B, S, Hq, D, dt, seed=0, device="cuda")
+        k, _, _ = inputs.rope_inputs(B, S, Hk, D, dt, seed=1, device="cuda")
         yq, yk = torch.empty_like(q), torch.empty_like(k)
         plan = plan_name("rope", camp.camp_rope_qk_plan(q, k, sn, cs, yq, yk, B, S, Hq, Hk, D,
-                                                        "bf16"))
+                                                        dt), dt)
         for _ in range(launches):
-            camp.camp_rope_qk(q, k, sn, cs, yq, yk, B, S, Hq, Hk, D, camp.BF16, stream)
+            camp.camp_rope_qk(q, k, sn, cs, yq, yk, B, S, Hq, Hk, D, code, stream)
     elif kind == "rope":
         B, S, H, D = dims
-        x, sn, cs = inputs.rope_inputs(B, S, H, D, "bf16", seed=0, device="cuda")
+        x, sn, cs = inputs.rope_inputs(B, S, H, D, dt, seed=0, device="cuda")
         y = torch.empty_like(x)
-        plan = plan_name("rope", camp.camp_rope_plan(x, sn, cs, y, B, S, H, D, "bf16"))
+        plan = plan_name("rope", camp.camp_rope_plan(x, sn, cs, y, B, S, H, D, dt), dt)
         for _ in range(launches):
-            camp.camp_rope(x, sn, cs, y, B, S, H, D, camp.BF16, stream)
+            camp.camp_rope(x, sn, cs, y, B, S, H, D, code, stream)
     else:
         raise SystemExit(f"unknown case {case!r}")
     torch.cuda.synchronize()
@@ -903,7 +909,8 @@ def main() -> None:
                          "rope:1x16384x32x128, rope_qk:1x16384x32x8x128 (B x S x Hq x Hk x D), "
                          "kv:65536x512x64 (S x Dn x Dr), rope_il:16384x32x128 (T x H x D, "
                          "random positions) or kvcat:1x3584x512x8x64x4 "
-                         "(B x P x S x Hk x D x n_rep)")
+                         "(B x P x S x Hk x D x n_rep); a third field picks the storage "
+                         "type, e.g. layernorm:8192x4096:f16 (bf16 when left out)")
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.case:

@@ -447,8 +447,9 @@ template <int BYTES> __device__ __forceinline__ Raw<BYTES> raw_zero() {
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization
 // may start while the previous kernel in the stream is still running. griddep_wait()
 // blocks until that kernel has completed and its memory is visible, so every kernel here
-// calls it before its first global-memory access; without the launch attribute it returns
-// at once. griddep_launch_dependents() lets the next kernel be scheduled early.
+// calls it before its first global-memory load or store (an L2 prefetch, below, may come
+// first); without the launch attribute it returns at once. griddep_launch_dependents()
+// lets the next kernel be scheduled early.
 
 __device__ __forceinline__ void griddep_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -456,6 +457,28 @@ __device__ __forceinline__ void griddep_wait() {
 
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// L2 prefetch of a CTA's first inputs, issued by one thread BEFORE griddep_wait(), so that
+// their HBM reads overlap the tail of the previous kernel in the stream instead of
+// following it. cp.async.bulk.prefetch.L2 only fills L2 lines: it returns no data,
+// completes on its own and needs no barrier. L2 is where the SMs' global accesses meet
+// (every store of the previous kernel lands there, in the line a prefetch may already
+// have filled), and this kernel's loads of the same bytes are issued after
+// griddep_wait(), so they return what the previous kernel wrote whether a prefetch ran
+// before, after or during those writes; at worst a prefetch reads a line that is about
+// to be overwritten. Only the 16-byte-aligned interior of [p, p + bytes) is fetched, in
+// pieces of at most 32 KB, so nothing outside the buffer is touched; bytes <= 0 is a no-op.
+__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
+    if (bytes <= 0) return;
+    const uint64_t a = reinterpret_cast<uint64_t>(p);
+    uint64_t lo = (a + 15) & ~uint64_t{15};
+    const uint64_t hi = (a + static_cast<uint64_t>(bytes)) & ~uint64_t{15};
+    while (lo < hi) {
+        const uint32_t n = hi - lo < 32768 ? static_cast<uint32_t>(hi - lo) : 32768u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"(n) : "memory");
+        lo += n;
+    }
 }
 
 // ------------------------------------------------------------------ rotation helpers

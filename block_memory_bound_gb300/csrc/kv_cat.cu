@@ -30,14 +30,37 @@ kv_cat_repeat_kernel(const void* past, const void* fresh, const float* __restric
     constexpr int E = Codec<S, VB>::kElems;
     constexpr int ES = Storage<S>::kBytes;
 
-    griddep_wait();
-    griddep_launch_dependents();
-
     const int nvh = half / E;                                  // vectors per half
     const int per_row = ((heads + HPT - 1) / HPT) * nvh;       // threads per (b, t) row
     const int tpc = kRopeBlock / per_row;
     const int tk = static_cast<int>(threadIdx.x) / per_row;
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+    if (threadIdx.x == 0) {
+        // The source rows of this CTA's output rows, as runs that are contiguous in past or
+        // in fresh (at most a few per batch entry the CTA spans), and the table rows of
+        // the rotated ones.
+        const int64_t T = seq.d, P = past_len, S = T - P;
+        const int64_t hb = static_cast<int64_t>(heads) * 2 * ES * half;   // one (b, t) row
+        int64_t g = block * tpc;
+        const int64_t g1 = rows - g < tpc ? rows : g + tpc;
+        while (g < g1) {
+            const int64_t b = g / T, t = g - b * T;
+            const bool old = t < P;
+            const int64_t end = old ? (b * T + P < g1 ? b * T + P : g1) : (b * T + T < g1 ? b * T + T : g1);
+            if (old) {
+                prefetch_l2(static_cast<const char*>(past) + (b * P + t) * hb, (end - g) * hb);
+            } else {
+                prefetch_l2(static_cast<const char*>(fresh) + (b * S + t - P) * hb, (end - g) * hb);
+                if (sin_t != nullptr) {
+                    prefetch_l2(sin_t + t * half, (end - g) * half * 4);
+                    prefetch_l2(cos_t + t * half, (end - g) * half * 4);
+                }
+            }
+            g = end;
+        }
+    }
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t g = block * tpc + tk;                        // b * (P + S) + t
     if (tk >= tpc || g >= rows) return;                        // no barrier in this kernel
     const int r = static_cast<int>(threadIdx.x) - tk * per_row;

@@ -118,6 +118,15 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
         mbar_init(smem_u32(&bar_x[1]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         timed_out = 0;
+        // The chunks that the first bulk loads below will read (after griddep_wait).
+        prefetch_l2(static_cast<const char*>(gamma) + v0 * 16, my_bytes);
+        prefetch_l2(static_cast<const char*>(beta) + v0 * 16, my_bytes);
+        for (int s = 0; s < stages; ++s) {
+            const int64_t row = cid + s * ncl;
+            if (row >= rows) break;
+            prefetch_l2(static_cast<const char*>(x) + row * pitch, 16);
+            prefetch_l2(static_cast<const char*>(x) + row * pitch + v0 * 16, my_bytes);
+        }
     }
     // Every CTA of the cluster has started and initialized its barriers before any CTA
     // stores into a peer's shared memory (split cluster barrier).

@@ -118,14 +118,20 @@ rmsnorm_rows_kernel(const void* x, const void* r, void* h, const void* __restric
 
     __shared__ float partial[Sh::kRowsPerCta][Sh::kWarpsPerRow];
 
+    // One row block per CTA (the host sizes the grid; a second grid dimension only
+    // appears for more than 2^31 - 1 blocks).
+    const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+    if (threadIdx.x == 0) {   // this CTA's rows of x (and r), contiguous
+        const int64_t row0 = block * Sh::kRowsPerCta;
+        const int64_t n = (rows - row0 < Sh::kRowsPerCta ? rows - row0 : Sh::kRowsPerCta) * cols * ES;
+        prefetch_l2(static_cast<const char*>(x) + row0 * cols * ES, n);
+        if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + row0 * cols * ES, n);
+    }
     griddep_wait();
     griddep_launch_dependents();
 
-    // One row block per CTA (the host sizes the grid; a second grid dimension only
-    // appears for more than 2^31 - 1 blocks).
     const int g = threadIdx.x / G;       // row slot inside the CTA
     const int t = threadIdx.x % G;       // thread inside the row group
-    const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
     const int64_t row = block * Sh::kRowsPerCta + g;
     const bool active = row < rows;
     // Access k of this thread is vector k*G + t of the row; it exists iff k*G < live.
@@ -178,14 +184,21 @@ rmsnorm_cluster_kernel(const void* x, const void* r, void* h, const void* __rest
     // before any CTA writes into it; the wait costs nothing by then.
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-    griddep_wait();
-    griddep_launch_dependents();
-
     cg::cluster_group cluster = cg::this_cluster();
     const unsigned nct = cluster.num_blocks();
     const unsigned rank = cluster.block_rank();
     const int t = threadIdx.x;
     const int64_t row = static_cast<int64_t>(blockIdx.x) / nct;   // the host launches rows * C CTAs
+    if (t == 0) {   // this CTA's chunk of the row (and of r)
+        const int64_t v0 = static_cast<int64_t>(rank) * NV * kClusterBlock;
+        const int64_t left = cols / E - v0;
+        const int64_t n = (left < NV * kClusterBlock ? left : NV * kClusterBlock) * VB;
+        prefetch_l2(static_cast<const char*>(x) + row * cols * ES + v0 * VB, n);
+        if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + row * cols * ES + v0 * VB, n);
+    }
+
+    griddep_wait();
+    griddep_launch_dependents();
     // Access k of this thread is vector (rank*NV + k)*256 + t of the row; live iff < nvec.
     const int live = static_cast<int>(cols / E) - static_cast<int>(rank) * NV * kClusterBlock - t;
     const int64_t off = row * cols * ES +
@@ -237,11 +250,17 @@ rmsnorm_wide_kernel(const void* x, const void* r, void* h, const void* __restric
     constexpr int kUnroll = 4;
     __shared__ float partial[kWideBlock / 32];
 
+    const int64_t nvec = cols / E;
+    const int64_t pitch = cols * ES;
+    if (threadIdx.x == 0 && blockIdx.x < rows) {   // the start of this CTA's first row
+        const int64_t n = pitch < 65536 ? pitch : 65536;
+        prefetch_l2(static_cast<const char*>(x) + blockIdx.x * pitch, n);
+        if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + blockIdx.x * pitch, n);
+    }
+
     griddep_wait();
     griddep_launch_dependents();
 
-    const int64_t nvec = cols / E;
-    const int64_t pitch = cols * ES;
     const char* wb = static_cast<const char*>(w);
     const float fcols = static_cast<float>(cols);
 

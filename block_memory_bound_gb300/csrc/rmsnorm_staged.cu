@@ -109,6 +109,14 @@ rmsnorm_staged_kernel(const void* x, const void* r, void* h, const void* __restr
         mbar_init(smem_u32(&sum_bar[1]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         timed_out = 0;
+        // The chunks that the first bulk loads below will read (after griddep_wait).
+        prefetch_l2(static_cast<const char*>(w) + v0 * 16, my_bytes);
+        for (int s = 0; s < stages; ++s) {
+            const int64_t row = cid + s * ncl;
+            if (row >= rows) break;
+            prefetch_l2(static_cast<const char*>(x) + row * pitch + v0 * 16, my_bytes);
+            if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + row * pitch + v0 * 16, my_bytes);
+        }
     }
     // Every CTA of the cluster has started, and its barriers are initialized, before any
     // CTA stores into a peer's shared memory (split cluster barrier: arrive now, wait

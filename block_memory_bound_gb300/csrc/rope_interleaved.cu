@@ -34,14 +34,19 @@ rope_interleaved_kernel(const void* x, const float* __restrict__ sin_t,
     constexpr int ES = Storage<S>::kBytes;
     static_assert(E % 2 == 0, "a vector holds whole pairs");
 
-    griddep_wait();
-    griddep_launch_dependents();
-
     const int nv = dim / E;                                    // vectors per head row
     const int per_pos = ((heads + HPT - 1) / HPT) * nv;        // threads per token
     const int tpc = kRopeBlock / per_pos;
     const int tk = static_cast<int>(threadIdx.x) / per_pos;
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+    if (threadIdx.x == 0) {   // this CTA's tokens of x (the table rows depend on positions)
+        const int64_t t0 = block * tpc;
+        const int64_t nt = tokens - t0 < tpc ? tokens - t0 : tpc;
+        const int64_t rb = static_cast<int64_t>(dim) * ES * heads;
+        prefetch_l2(static_cast<const char*>(x) + t0 * rb, nt * rb);
+    }
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t tok = block * tpc + tk;
     if (tk >= tpc || tok >= tokens) return;                    // no barrier in this kernel
     const int64_t p = positions[tok];
