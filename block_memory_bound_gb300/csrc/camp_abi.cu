@@ -166,14 +166,20 @@ struct RowsCandidate {
 //     of when a CTA of the first wave retires (4096 x 2048 bf16: 64 x 4 in one wave
 //     6.98 us, 128 x 2 in 1.7 waves 7.25 us);
 //  5. within 2., fewer accesses per thread (more threads, shorter serial work per thread);
-//     outside it, the smaller group (512-thread CTAs beat 1024-thread ones: 16384 bf16
-//     columns at 4096 rows run 42 us with 512 x 4 and 50 us with 1024 x 2).
+//     outside it (rows of more than 1024 vectors), at most 4 accesses in groups of at
+//     most 512 threads, then the smaller group. With each CTA's rows prefetched into L2
+//     before it waits on the previous kernel, 512 x 3 / 512 x 4 beat 256 x 6 / 256 x 8
+//     (bf16, 4096 rows of 12288 / 16384 columns: RMSNorm 0.97 / 0.98 of the measured peak
+//     against 0.94 / 0.94, with the residual add 1.00 / 1.00 against 0.97 / 0.97), and
+//     1024-thread CTAs lose where the rule would otherwise reach them (1024 x 4 at 32768
+//     columns: 0.75 against 512 x 8's 0.92).
 // For bf16 this picks 64 x 4 at 4096 x 2048, 128 x 2 at 8192 x 2048 and more rows,
-// 128 x 3 at 3000 columns, 256 x 4 at 8192, and 256 x 6 / 256 x 8 at 12288 / 16384
+// 128 x 3 at 3000 columns, 256 x 4 at 8192, and 512 x 3 / 512 x 4 at 12288 / 16384
 // columns: the fastest of the compiled variants at each, or within 2-5% of it.
 // LayerNorm (`layernorm`) differs in 5.: its per-thread cost (two reductions) is higher,
-// so when both candidates run at least 2 waves the one with more accesses per thread
-// wins (bf16, 64 x 4 against 128 x 2: 65536 x 2048 80.5 / 90.9 us, 8192 x 2048 14.3 /
+// so outside the band it keeps the smaller group (4096 x 12288: 256 x 6 0.86, 512 x 3
+// 0.82), and when both candidates run at least 2 waves the one with more accesses per
+// thread wins (bf16, 64 x 4 against 128 x 2: 65536 x 2048 80.5 / 90.9 us, 8192 x 2048 14.3 /
 // 14.5 us; 8192 x 4096: 128 x 4 24.2 us, 256 x 2 24.6 us); closer to one wave the RMSNorm
 // order holds (4096 x 2048: 128 x 2 9.0 us, 64 x 4 in 1.1 waves 10.2 us).
 // At decode sizes (no more rows than SMs) a launch is latency-bound, not bandwidth-bound,
@@ -201,6 +207,11 @@ bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm,
     if (a.one_wave != b.one_wave) return a.one_wave;
     if (ma && layernorm && a.many_waves && b.many_waves) return a.per_thread > b.per_thread;
     if (ma) return a.per_thread < b.per_thread;
+    if (!layernorm) {
+        const bool na = a.per_thread <= 4 && a.group <= 512;
+        const bool nb = b.per_thread <= 4 && b.group <= 512;
+        if (na != nb) return na;
+    }
     return a.group < b.group;
 }
 
@@ -1013,15 +1024,19 @@ void ln_staged_plan_fields(const LnCall& c, int cluster, int stages, int64_t chu
     p->grid = clusters * cluster;
 }
 
-// Rows of more than kLnStagedFrom 16-byte vectors take the staged kernel, with the
+// Rows of more than kLnStagedFrom 16-byte vectors, and rows of more than kLnStagedFewFrom
+// vectors when there are at most kLnFewRows of them, take the staged kernel, with the
 // RMSNorm staged kernel's cluster size (CTA chunks of about 1024 vectors) and 2 buffers:
 // LayerNorm also holds gamma and beta, and a third buffer costs more occupancy than it
-// hides. Measured on GB300 (L2-cold, graphs of back-to-back launches), staged against the
-// best register variant: bf16 2048 x 32768 0.69 / 0.67 of the measured HBM peak, 1024 x
-// 65536 0.62 / 0.55 (3 buffers: 0.50), fp32 2048 x 16384 0.84 / 0.79; at 2048 vectors
-// (bf16 4096 x 16384) the register kernel stays ahead, 0.86 / 0.72. Past 8192 vectors only
-// the staged kernel holds the row (512 x 131072: 0.54, 64 x 262144: 0.35).
-constexpr int64_t kLnStagedFrom = 2048;
+// hides. Measured on GB300 (bf16, L2-cold, graphs of back-to-back launches, each CTA's
+// first inputs prefetched into L2 before the dependent-launch wait), fraction of the
+// measured HBM peak, register kernel against staged: 4096 x 16384 0.89 / 0.75, 2048 x
+// 24576 0.77 / 0.65, 2048 x 32768 0.78 / 0.72, but 1024 x 32768 0.63 / 0.68 (a few waves
+// of 512-thread CTAs); 1024 x 65536 (8192 vectors) 0.57 / 0.64. Past 8192 vectors only the
+// staged kernel holds the row (256 x 131072: 0.54).
+constexpr int64_t kLnStagedFrom = 4096;
+constexpr int64_t kLnStagedFewFrom = 2048;
+constexpr int64_t kLnFewRows = 1024;
 
 camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p) {
     if (forced && forced->kernel != CAMP_KERNEL_LAYERNORM_ROWS &&
@@ -1052,7 +1067,8 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
         const int64_t nvec = rc.a.cols * es / p->vec_bytes;
         if (static_cast<int64_t>(p->group) * p->per_thread < nvec) return CAMP_ERR_NOT_SUPPORTED;
     } else {
-        if (widest == 16 && nvec16 > kLnStagedFrom) {
+        if (widest == 16 && (nvec16 > kLnStagedFrom ||
+                             (nvec16 > kLnStagedFewFrom && rc.a.rows <= kLnFewRows))) {
             int cl = 0, st = 0;
             int64_t chunk = 0;
             if (rms_choose_staged(rc, nvec16, &cl, &st, &chunk) &&

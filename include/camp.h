@@ -279,10 +279,11 @@ CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos,
  * once) and the statistics are taken in two passes over the registers, in fp32: with
  * K = x[row, 0], mu = sum(x - K) / n and d = (x - K) - mu, var = sum(d^2) / n and
  * y = fma(d * rsqrt(var + eps), gamma, beta), rounded once to the storage type. Rows of
- * more than 2048 16-byte vectors (16384 bf16/f16 / 8192 fp32 columns; all pointers and the
- * row pitch 16-byte aligned) are staged in shared memory by persistent clusters of CTAs
- * instead (up to 16 x 2048 vectors: 262144 bf16/f16 / 131072 fp32 columns). Wider rows, and rows past
- * 16384 columns on the element path, return CAMP_ERR_NOT_SUPPORTED. Errors otherwise as for
+ * more than 4096 16-byte vectors (32768 bf16/f16 / 16384 fp32 columns), or of more than
+ * 2048 when there are at most 1024 rows (all pointers and the row pitch 16-byte aligned),
+ * are staged in shared memory by persistent clusters of CTAs instead (up to 16 x 2048
+ * vectors: 262144 bf16/f16 / 131072 fp32 columns). Wider rows, and rows past 16384 columns
+ * on the element path, return CAMP_ERR_NOT_SUPPORTED. Errors otherwise as for
  * camp_rmsnorm.
  */
 CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const void* beta,
@@ -328,7 +329,7 @@ typedef enum {
     CAMP_KERNEL_KV_CAT = 10,        /* camp_kv_cat_repeat: tiled like CAMP_KERNEL_ROPE */
     CAMP_KERNEL_RMSNORM_STAGED = 11, /* persistent clusters, rows staged in shared memory by
                                         bulk asynchronous copies, `per_thread` buffers deep */
-    CAMP_KERNEL_LAYERNORM_STAGED = 12 /* camp_layernorm: the same, for rows past 4096 vectors */
+    CAMP_KERNEL_LAYERNORM_STAGED = 12 /* camp_layernorm: the same, for the widest rows */
 } camp_kernel_t;
 
 typedef struct {

@@ -141,9 +141,11 @@ def test_rope_empty_is_success_without_cuda(lib):
     (153, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 153)),   # past the SMs
     (1, 8, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 32, 1, 256, 1)),
     (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 256, 16, 256, 64)),
-    # wider rows: one CTA of up to 1024 threads while it holds the row (8192 vectors)...
-    (4096, 12288, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 6, 256, 4096)),
-    (4096, 16384, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 8, 256, 4096)),
+    # wider rows: one CTA of up to 1024 threads while it holds the row (8192 vectors);
+    # past 1024 vectors at most 4 accesses in groups of at most 512 threads...
+    (4096, 12288, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 3, 512, 4096)),
+    (4096, 16384, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 4, 512, 4096)),
+    (2048, 24576, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 6, 512, 2048)),
     (1024, 32768, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 8, 512, 1024)),
     # ...then (past 4096 vectors) rows staged in shared memory by persistent clusters:
     # group = vectors a CTA (about 1024), per_thread = buffers (3; 2 with 16 CTAs),
@@ -546,8 +548,7 @@ def test_layernorm_empty_and_in_place(lib):
 
 @pytest.mark.parametrize("rows,cols,dtype", [
     (16384, 8192, "bf16"), (4096, 3000, "bf16"), (64, 2048, "f32"),
-    (1, 8, "bf16"), (64, 3001, "bf16"), (4096, 12288, "bf16"), (4096, 16384, "bf16"),
-    (3, 8192, "f32"), (4096, 1024, "bf16"),
+    (1, 8, "bf16"), (64, 3001, "bf16"), (3, 8192, "f32"), (4096, 1024, "bf16"),
 ])
 def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype):
     # the same register-resident row mapping as RMSNorm: where neither the one-wave test
@@ -560,10 +561,20 @@ def test_layernorm_plans_follow_the_rmsnorm_rows_chooser(lib, rows, cols, dtype)
         (q.vec_bytes, q.group, q.per_thread, q.block, q.grid, 1)
 
 
-def test_layernorm_stages_rows_past_2048_vectors(lib):
+def test_layernorm_keeps_the_smaller_group_past_1024_vectors(lib):
+    # outside the 2-4 accesses band RMSNorm takes at most 4 accesses in groups of at most
+    # 512 threads; LayerNorm (two reductions a row) keeps the smaller group
+    for cols, ln, rms in ((12288, (256, 6), (512, 3)), (16384, (256, 8), (512, 4))):
+        p = camp.camp_layernorm_plan(X, W, BETA, Y, 4096, cols, "bf16")
+        q = camp.camp_rmsnorm_plan(X, W, Y, 4096, cols, "bf16")
+        assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS,) + ln
+        assert (q.kernel, q.group, q.per_thread) == (camp.KERNEL_RMSNORM_ROWS,) + rms
+
+
+def test_layernorm_stages_rows_past_4096_vectors(lib):
     # past 4096 vectors both operators stage the row in shared memory with the same cluster
     # size; LayerNorm keeps 2 buffers (it also holds gamma and beta, and each buffer carries
-    # the row's first 16 bytes) and starts staging at 2048 vectors
+    # the row's first 16 bytes), and with at most 1024 rows it stages from 2048 vectors
     for rows, cols, dtype in ((5, 65536, "bf16"), (7, 32768, "f32"), (64, 262144, "bf16"),
                               (3, 40000, "bf16")):
         q = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype)
@@ -572,10 +583,15 @@ def test_layernorm_stages_rows_past_2048_vectors(lib):
         assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
         assert (p.vec_bytes, p.group, p.cluster, p.block, p.per_thread) == \
             (q.vec_bytes, q.group, q.cluster, q.block, 2)
-    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 32768, "bf16")   # 4096 vectors
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 32768, "bf16")   # 4096 vectors, few rows
     assert (p.kernel, p.cluster, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_STAGED, 4, 1024, 2)
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 1024, 24576, "bf16")   # 3072 vectors, few rows
+    assert (p.kernel, p.cluster, p.per_thread) == (camp.KERNEL_LAYERNORM_STAGED, 4, 2)
     p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 16384, "bf16")   # 2048 vectors: rows
     assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, 512, 4)
+    for rows, cols, nv in ((1025, 24576, 6), (2048, 24576, 6), (2048, 32768, 8)):   # rows
+        p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, "bf16")
+        assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, 512, nv)
 
 
 def test_layernorm_staged_plans_that_do_not_fit_are_refused(lib):
