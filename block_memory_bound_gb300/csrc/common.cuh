@@ -469,6 +469,13 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // before, after or during those writes; at worst a prefetch reads a line that is about
 // to be overwritten. Only the 16-byte-aligned interior of [p, p + bytes) is fetched, in
 // pieces of at most 32 KB, so nothing outside the buffer is touched; bytes <= 0 is a no-op.
+// Number of SM identifiers on this device (at least the SM count).
+__device__ __forceinline__ uint32_t sm_id_count() {
+    uint32_t n;
+    asm("mov.u32 %0, %%nsmid;" : "=r"(n));
+    return n;
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
     if (bytes <= 0) return;
     const uint64_t a = reinterpret_cast<uint64_t>(p);

@@ -39,18 +39,16 @@ kv_rmsnorm_rope_cache_kernel(const void* kv, const void* __restrict__ gamma,
 
     const int lane = threadIdx.x & 31;
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-    if (threadIdx.x == 0) {   // this CTA's kv rows, their slots and their table rows
-        const int64_t t0 = block * kKvTokensPerCta;
+    if (threadIdx.x == 0 && block * kKvTokensPerCta < tokens) {   // this CTA's kv rows, their
+        const int64_t t0 = block * kKvTokensPerCta;               // slots and table rows
         const int64_t nt = tokens - t0 < kKvTokensPerCta ? tokens - t0 : kKvTokensPerCta;
         const int64_t rb = static_cast<int64_t>(dn + dr) * ES;
         prefetch_l2(static_cast<const char*>(kv) + t0 * rb, nt * rb);
         prefetch_l2(slots + t0, nt * 8);
-        if (nt > 0) {
-            const int64_t s0 = t0 % seq;
-            const int64_t ns = nt < seq - s0 ? nt : seq - s0;
-            prefetch_l2(sin_t + s0 * (dr / 2), ns * (dr / 2) * 4);
-            prefetch_l2(cos_t + s0 * (dr / 2), ns * (dr / 2) * 4);
-        }
+        const int64_t s0 = t0 % seq;
+        const int64_t ns = nt < seq - s0 ? nt : seq - s0;
+        prefetch_l2(sin_t + s0 * (dr / 2), ns * (dr / 2) * 4);
+        prefetch_l2(cos_t + s0 * (dr / 2), ns * (dr / 2) * 4);
     }
     griddep_wait();
     griddep_launch_dependents();

@@ -127,7 +127,7 @@ layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
     __shared__ float part_var[Sh::kRowsPerCta][Sh::kWarpsPerRow];
 
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-    if (threadIdx.x == 0) {   // this CTA's rows of x, contiguous
+    if (threadIdx.x == 0 && block * Sh::kRowsPerCta < rows) {   // this CTA's rows of x
         const int64_t row0 = block * Sh::kRowsPerCta;
         const int64_t n = (rows - row0 < Sh::kRowsPerCta ? rows - row0 : Sh::kRowsPerCta) * cols * ES;
         prefetch_l2(static_cast<const char*>(x) + row0 * cols * ES, n);

@@ -121,11 +121,24 @@ rmsnorm_rows_kernel(const void* x, const void* r, void* h, const void* __restric
     // One row block per CTA (the host sizes the grid; a second grid dimension only
     // appears for more than 2^31 - 1 blocks).
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-    if (threadIdx.x == 0) {   // this CTA's rows of x (and r), contiguous
+    if (threadIdx.x == 0 && block * Sh::kRowsPerCta < rows) {   // this CTA's rows of x (and r)
         const int64_t row0 = block * Sh::kRowsPerCta;
         const int64_t n = (rows - row0 < Sh::kRowsPerCta ? rows - row0 : Sh::kRowsPerCta) * cols * ES;
         prefetch_l2(static_cast<const char*>(x) + row0 * cols * ES, n);
         if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + row0 * cols * ES, n);
+        // When the whole input is small next to L2 (at most 32 MB), also the rows of the
+        // CTA one resident wave later, so that a second wave finds its rows in L2 (4096 x
+        // 3000 bf16: 9.47 -> 8.97 us; with the residual add, 4096 x 2048: 12.0 -> 11.4 us).
+        if (rows * cols * ES * (ADD ? 2 : 1) <= (int64_t{32} << 20)) {
+            const int64_t wave =
+                static_cast<int64_t>(rows_min_blocks(VB, G, ADD ? 2 * NV : NV)) * sm_id_count();
+            const int64_t r1 = (block + wave) * Sh::kRowsPerCta;
+            if (r1 < rows) {
+                const int64_t n1 = (rows - r1 < Sh::kRowsPerCta ? rows - r1 : Sh::kRowsPerCta) * cols * ES;
+                prefetch_l2(static_cast<const char*>(x) + r1 * cols * ES, n1);
+                if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + r1 * cols * ES, n1);
+            }
+        }
     }
     griddep_wait();
     griddep_launch_dependents();
@@ -189,7 +202,7 @@ rmsnorm_cluster_kernel(const void* x, const void* r, void* h, const void* __rest
     const unsigned rank = cluster.block_rank();
     const int t = threadIdx.x;
     const int64_t row = static_cast<int64_t>(blockIdx.x) / nct;   // the host launches rows * C CTAs
-    if (t == 0) {   // this CTA's chunk of the row (and of r)
+    if (t == 0 && row < rows) {   // this CTA's chunk of the row (and of r)
         const int64_t v0 = static_cast<int64_t>(rank) * NV * kClusterBlock;
         const int64_t left = cols / E - v0;
         const int64_t n = (left < NV * kClusterBlock ? left : NV * kClusterBlock) * VB;

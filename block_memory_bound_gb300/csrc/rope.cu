@@ -63,19 +63,18 @@ rope_tiled_kernel(const void* x, void* y, int heads, const void* x2, void* y2, i
     const int tpc = kRopeBlock / per_pos;                      // positions per CTA
     const int tk = static_cast<int>(threadIdx.x) / per_pos;
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-    if (threadIdx.x == 0) {   // this CTA's positions of both tensors, and their table rows
+    if (threadIdx.x == 0 && block * tpc < tokens) {   // this CTA's positions and table rows
         const int64_t p0 = block * tpc;
         const int64_t np = tokens - p0 < tpc ? tokens - p0 : tpc;
         const int64_t rb = static_cast<int64_t>(2 * ES) * half;
         prefetch_l2(static_cast<const char*>(x) + p0 * heads * rb, np * heads * rb);
-        prefetch_l2(static_cast<const char*>(x2) + p0 * heads2 * rb, np * heads2 * rb);
-        if (np > 0) {   // table rows s0 .. s0 + ns - 1, up to the end of the sequence
-            const uint32_t p32 = static_cast<uint32_t>(p0);
-            const uint32_t s0 = p32 - fast_div(p32, seq) * seq.d;
-            const int64_t ns = np < seq.d - s0 ? np : seq.d - s0;
-            prefetch_l2(sin_t + static_cast<int64_t>(s0) * half, ns * half * 4);
-            prefetch_l2(cos_t + static_cast<int64_t>(s0) * half, ns * half * 4);
-        }
+        if (heads2 > 0) prefetch_l2(static_cast<const char*>(x2) + p0 * heads2 * rb, np * heads2 * rb);
+        // table rows s0 .. s0 + ns - 1, up to the end of the sequence
+        const uint32_t p32 = static_cast<uint32_t>(p0);
+        const uint32_t s0 = p32 - fast_div(p32, seq) * seq.d;
+        const int64_t ns = np < seq.d - s0 ? np : seq.d - s0;
+        prefetch_l2(sin_t + static_cast<int64_t>(s0) * half, ns * half * 4);
+        prefetch_l2(cos_t + static_cast<int64_t>(s0) * half, ns * half * 4);
     }
     griddep_wait();
     griddep_launch_dependents();

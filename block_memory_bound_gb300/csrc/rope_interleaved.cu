@@ -39,7 +39,8 @@ rope_interleaved_kernel(const void* x, const float* __restrict__ sin_t,
     const int tpc = kRopeBlock / per_pos;
     const int tk = static_cast<int>(threadIdx.x) / per_pos;
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-    if (threadIdx.x == 0) {   // this CTA's tokens of x (the table rows depend on positions)
+    if (threadIdx.x == 0 && block * tpc < tokens) {   // this CTA's tokens of x (the table
+                                                       // rows depend on the positions)
         const int64_t t0 = block * tpc;
         const int64_t nt = tokens - t0 < tpc ? tokens - t0 : tpc;
         const int64_t rb = static_cast<int64_t>(dim) * ES * heads;
