@@ -126,17 +126,16 @@ rmsnorm_rows_kernel(const void* x, const void* r, void* h, const void* __restric
         const int64_t n = (rows - row0 < Sh::kRowsPerCta ? rows - row0 : Sh::kRowsPerCta) * cols * ES;
         prefetch_l2(static_cast<const char*>(x) + row0 * cols * ES, n);
         if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + row0 * cols * ES, n);
-        // When the whole input is small next to L2 (at most 32 MB), also the rows of the
-        // CTA one resident wave later, so that a second wave finds its rows in L2 (4096 x
-        // 3000 bf16: 9.47 -> 8.97 us; with the residual add, 4096 x 2048: 12.0 -> 11.4 us).
-        if (rows * cols * ES * (ADD ? 2 : 1) <= (int64_t{32} << 20)) {
-            const int64_t wave =
-                static_cast<int64_t>(rows_min_blocks(VB, G, ADD ? 2 * NV : NV)) * sm_id_count();
+        // Without the residual add, and when x is small next to L2 (at most 32 MB), also the
+        // rows of the CTA one resident wave later, so that a second wave finds its rows in
+        // L2 (bf16 4096 x 3000: 9.47 -> 9.08 us, 8192 x 2048: 11.8 -> 11.2 us; the add path
+        // measured no gain).
+        if (!ADD && rows * cols * ES <= (int64_t{32} << 20)) {
+            const int64_t wave = static_cast<int64_t>(rows_min_blocks(VB, G, NV)) * sm_id_count();
             const int64_t r1 = (block + wave) * Sh::kRowsPerCta;
             if (r1 < rows) {
                 const int64_t n1 = (rows - r1 < Sh::kRowsPerCta ? rows - r1 : Sh::kRowsPerCta) * cols * ES;
                 prefetch_l2(static_cast<const char*>(x) + r1 * cols * ES, n1);
-                if constexpr (ADD) prefetch_l2(static_cast<const char*>(r) + r1 * cols * ES, n1);
             }
         }
     }
