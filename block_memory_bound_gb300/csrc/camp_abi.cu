@@ -1025,18 +1025,33 @@ void ln_staged_plan_fields(const LnCall& c, int cluster, int stages, int64_t chu
 }
 
 // Rows of more than kLnStagedFrom 16-byte vectors, and rows of more than kLnStagedFewFrom
-// vectors when there are at most kLnFewRows of them, take the staged kernel, with the
-// RMSNorm staged kernel's cluster size (CTA chunks of about 1024 vectors) and 2 buffers:
-// LayerNorm also holds gamma and beta, and a third buffer costs more occupancy than it
-// hides. Measured on GB300 (bf16, L2-cold, graphs of back-to-back launches, each CTA's
-// first inputs prefetched into L2 before the dependent-launch wait), fraction of the
-// measured HBM peak, register kernel against staged: 4096 x 16384 0.89 / 0.75, 2048 x
-// 24576 0.77 / 0.65, 2048 x 32768 0.78 / 0.72, but 1024 x 32768 0.63 / 0.68 (a few waves
-// of 512-thread CTAs); 1024 x 65536 (8192 vectors) 0.57 / 0.64. Past 8192 vectors only the
-// staged kernel holds the row (256 x 131072: 0.54).
+// vectors when there are at most kLnFewRows of them, take the staged kernel with the
+// smallest power-of-two cluster whose CTA chunks hold at most kLnStagedChunk vectors (8 a
+// thread) and 2 buffers. Measured on GB300 (bf16, L2-cold, graphs of back-to-back
+// launches, each CTA's first inputs prefetched into L2 before the dependent-launch wait),
+// fraction of the measured HBM peak, register kernel against staged: 4096 x 16384 0.89 /
+// 0.75, 2048 x 24576 0.77 / 0.65, 2048 x 32768 0.78 / 0.72, but 1024 x 32768 0.63 / 0.67 (a
+// few waves of 512-thread CTAs); 1024 x 65536 (8192 vectors) 0.57 / 0.64. Past 8192 vectors
+// only the staged kernel holds the row. Chunk size, with gamma and beta read through L1
+// (shared memory then holds only the ring): 2048-vector chunks against 1024 at 1024 x
+// 65536 0.64 / 0.58, 2048 x 65536 0.69 / 0.65, 256 x 131072 0.59 / 0.47, 512 x 131072
+// 0.65 / 0.53, 64 x 262144 0.46 (16 CTAs of 2048, the most that fit) where gamma and beta
+// in shared memory gave 0.64, 0.65, 0.54, 0.56 and 0.37 at their best cluster; a third
+// buffer costs more occupancy than it hides (1024 x 65536: 0.44).
 constexpr int64_t kLnStagedFrom = 4096;
 constexpr int64_t kLnStagedFewFrom = 2048;
 constexpr int64_t kLnFewRows = 1024;
+constexpr int64_t kLnStagedChunk = 2048;
+
+bool ln_choose_staged(int64_t nvec, int* cluster, int64_t* chunk) {
+    for (int cl = 1; cl <= 16; cl *= 2) {
+        if (ceil_div(nvec, cl) <= kLnStagedChunk && ln_staged_fits(nvec, cl, 2, chunk)) {
+            *cluster = cl;
+            return true;
+        }
+    }
+    return false;
+}
 
 camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p) {
     if (forced && forced->kernel != CAMP_KERNEL_LAYERNORM_ROWS &&
@@ -1069,11 +1084,10 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
     } else {
         if (widest == 16 && (nvec16 > kLnStagedFrom ||
                              (nvec16 > kLnStagedFewFrom && rc.a.rows <= kLnFewRows))) {
-            int cl = 0, st = 0;
+            int cl = 0;
             int64_t chunk = 0;
-            if (rms_choose_staged(rc, nvec16, &cl, &st, &chunk) &&
-                ln_staged_fits(nvec16, cl, (st = 2), &chunk)) {
-                ln_staged_plan_fields(c, cl, st, chunk, p);
+            if (ln_choose_staged(nvec16, &cl, &chunk)) {
+                ln_staged_plan_fields(c, cl, 2, chunk, p);
                 return CAMP_SUCCESS;
             }
         }

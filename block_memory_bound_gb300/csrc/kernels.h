@@ -185,10 +185,10 @@ cudaError_t layernorm_rows_launch(DType t, int vec_bytes, int group, int per_thr
                                   const LayernormArgs& a, int64_t grid, cudaStream_t s);
 
 // Staged LayerNorm (layernorm_staged.cu): the staged RMSNorm kernel's persistent clusters,
-// with gamma and beta chunks held in shared memory and each row buffer carrying the row's
-// first 16 bytes (the shift) ahead of the CTA's chunk.
+// each row buffer carrying the row's first 16 bytes (the shift) ahead of the CTA's chunk;
+// gamma and beta are read through L1.
 inline int64_t ln_staged_smem_bytes(int64_t chunk_vecs, int stages) {
-    return 2 * chunk_vecs * 16 + stages * (16 + chunk_vecs * 16);
+    return stages * (16 + chunk_vecs * 16);
 }
 cudaError_t layernorm_staged_launch(DType t, int cluster, int stages, const LayernormArgs& a,
                                     cudaStream_t s);

@@ -7,7 +7,9 @@
 //
 // Mapping: the staged RMSNorm kernel's (rmsnorm_staged.cu). Persistent clusters of C CTAs;
 // CTA rank k owns a contiguous chunk of 16-byte vectors of every row of its cluster and
-// holds its chunks of gamma and beta in shared memory. A ring of `stages` row buffers is
+// reads its chunks of gamma and beta through L1 in the output pass (the same chunk every
+// row, so they stay cached; holding them in shared memory cost a third of the CTAs an SM
+// could run). A ring of `stages` row buffers is
 // filled by bulk asynchronous copies: each copies the CTA's chunk plus the row's first 16
 // bytes (every CTA needs the shift K). Per row, each CTA takes the statistics of its own
 // chunk in two passes over its registers, in shifted coordinates: m_k = sum(x - K) / n_k and
@@ -87,7 +89,7 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
     // Dynamic shared memory: gamma chunk, beta chunk, then `stages` buffers of (the row's
     // first 16 bytes, the CTA's chunk of the row).
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long full[kStagedMaxStages + 1];   // + gamma/beta
+    __shared__ __align__(8) unsigned long long full[kStagedMaxStages];
     __shared__ __align__(8) unsigned long long bar_x[2];   // this row's (m_k, M2_k) pairs
     __shared__ float part_a[2][kWarps], part_b[2][kWarps];
     __shared__ float slot_m[2][16], slot_v[2][16];
@@ -106,19 +108,16 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
     const uint32_t my_bytes = static_cast<uint32_t>(my_vecs) * 16u;
     const int64_t pitch = cols * ES;
     const int64_t stage_bytes = 16 + static_cast<int64_t>(chunk_vecs) * 16;
-    unsigned char* gbuf = smem;
-    unsigned char* bbuf = smem + static_cast<int64_t>(chunk_vecs) * 16;
-    unsigned char* ring = smem + 2 * static_cast<int64_t>(chunk_vecs) * 16;
-    const uint32_t wbar = smem_u32(&full[kStagedMaxStages]);
+    unsigned char* ring = smem;
 
     if (t == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(smem_u32(&full[s]), 1);
-        mbar_init(wbar, 1);
         mbar_init(smem_u32(&bar_x[0]), 1);
         mbar_init(smem_u32(&bar_x[1]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         timed_out = 0;
-        // The chunks that the first bulk loads below will read (after griddep_wait).
+        // The chunks that the first bulk loads below, and the first output pass, will read
+        // (after griddep_wait).
         prefetch_l2(static_cast<const char*>(gamma) + v0 * 16, my_bytes);
         prefetch_l2(static_cast<const char*>(beta) + v0 * 16, my_bytes);
         for (int s = 0; s < stages; ++s) {
@@ -145,11 +144,6 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
         if (my_bytes > 0) bulk_load(dst + 16, xb + row * pitch + v0 * 16, my_bytes, bar);
     };
     if (t == 0) {
-        if (my_bytes > 0) {
-            mbar_arrive_expect_tx(wbar, 2 * my_bytes);
-            bulk_load(smem_u32(gbuf), static_cast<const char*>(gamma) + v0 * 16, my_bytes, wbar);
-            bulk_load(smem_u32(bbuf), static_cast<const char*>(beta) + v0 * 16, my_bytes, wbar);
-        }
         for (int s = 0; s < stages; ++s) {
             const int64_t row = cid + s * ncl;
             if (row < rows) issue(s, row);
@@ -165,7 +159,6 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
         const int64_t lq = nvec - static_cast<int64_t>(lane) * chunk_vecs;
         if (lane < nct && lq > 0) n_lane = static_cast<float>((lq < chunk_vecs ? lq : chunk_vecs) * E);
     }
-    bool w_ready = false;
     int64_t fail_iter = -1;
     int64_t i = 0;
     for (int64_t row = cid; row < rows; row += ncl, ++i) {
@@ -238,20 +231,18 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
         const float rstd = rsqrtf(var + eps);
         const f32x2 m2v = f2_make(mu, mu);
 
-        if (ok && my_bytes > 0 && !w_ready) {
-            if (!mbar_wait_bounded(wbar, 0)) timed_out = 1;
-            w_ready = true;
-        }
         if (ok) {
             const f32x2 r2 = f2_make(rstd, rstd);
             char* yr = static_cast<char*>(y) + row * pitch + v0 * 16;
+            const char* gb = static_cast<const char*>(gamma) + v0 * 16;
+            const char* bb = static_cast<const char*>(beta) + v0 * 16;
 #pragma unroll
             for (int k = 0; k < NVT; ++k) {
                 const int vi = t + k * kStagedBlock;
                 if (vi < my_vecs)
                     st_out<16>(yr + static_cast<int64_t>(vi) * 16,
-                               affine16<C>(v[k], ld_smem16(gbuf + vi * 16),
-                                           ld_smem16(bbuf + vi * 16), k2, m2v, r2));
+                               affine16<C>(v[k], ld_shared_ro<16>(gb + vi * 16),
+                                           ld_shared_ro<16>(bb + vi * 16), k2, m2v, r2));
             }
         }
     }
@@ -259,10 +250,8 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
     __syncthreads();
     if (timed_out && t == 0) {
         atomicOr(&g_ln_device_error, kDeviceErrorWaitTimeout);
-        // Copies that may still be in flight into this CTA's shared memory: gamma and beta,
-        // and those issued for iterations fail_iter .. fail_iter + stages - 1. Wait for each,
-        // at most a second.
-        if (my_bytes > 0) mbar_wait_bounded(wbar, 0);
+        // Copies that may still be in flight into this CTA's shared memory: those issued for
+        // iterations fail_iter .. fail_iter + stages - 1. Wait for each, at most a second.
         const int64_t f = fail_iter < 0 ? i : fail_iter;
         for (int64_t j = f; j < f + stages; ++j) {
             if (cid + j * ncl < rows)

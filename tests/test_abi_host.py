@@ -571,22 +571,22 @@ def test_layernorm_keeps_the_smaller_group_past_1024_vectors(lib):
         assert (q.kernel, q.group, q.per_thread) == (camp.KERNEL_RMSNORM_ROWS,) + rms
 
 
-def test_layernorm_stages_rows_past_4096_vectors(lib):
-    # past 4096 vectors both operators stage the row in shared memory with the same cluster
-    # size; LayerNorm keeps 2 buffers (it also holds gamma and beta, and each buffer carries
-    # the row's first 16 bytes), and with at most 1024 rows it stages from 2048 vectors
-    for rows, cols, dtype in ((5, 65536, "bf16"), (7, 32768, "f32"), (64, 262144, "bf16"),
-                              (3, 40000, "bf16")):
-        q = camp.camp_rmsnorm_plan(X, W, Y, rows, cols, dtype)
-        p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
-        assert q.kernel == camp.KERNEL_RMSNORM_STAGED
-        assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
-        assert (p.vec_bytes, p.group, p.cluster, p.block, p.per_thread) == \
-            (q.vec_bytes, q.group, q.cluster, q.block, 2)
-    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 32768, "bf16")   # 4096 vectors, few rows
-    assert (p.kernel, p.cluster, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_STAGED, 4, 1024, 2)
-    p = camp.camp_layernorm_plan(X, W, BETA, Y, 1024, 24576, "bf16")   # 3072 vectors, few rows
-    assert (p.kernel, p.cluster, p.per_thread) == (camp.KERNEL_LAYERNORM_STAGED, 4, 2)
+@pytest.mark.parametrize("rows,cols,dtype,cluster,chunk", [
+    (5, 65536, "bf16", 4, 2048), (7, 32768, "f32", 4, 2048), (64, 262144, "bf16", 16, 2048),
+    (3, 40000, "bf16", 4, 1250), (2, 131080, "bf16", 16, 1025),
+    (4, 32768, "bf16", 2, 2048),        # 4096 vectors, few rows
+    (1024, 24576, "bf16", 2, 1536),     # 3072 vectors, few rows
+])
+def test_layernorm_stages_rows_past_4096_vectors(lib, rows, cols, dtype, cluster, chunk):
+    # past 4096 vectors (2048 with at most 1024 rows) LayerNorm stages the row in shared
+    # memory with the smallest cluster whose CTA chunks hold at most 2048 vectors, 2 buffers
+    # (each carries the row's first 16 bytes; gamma and beta are read through L1)
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
+    assert (p.kernel, p.vec_bytes, p.cluster, p.group, p.block, p.per_thread) == \
+        (camp.KERNEL_LAYERNORM_STAGED, 16, cluster, chunk, 256, 2)
+
+
+def test_layernorm_staged_and_rows_thresholds(lib):
     p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 16384, "bf16")   # 2048 vectors: rows
     assert (p.kernel, p.group, p.per_thread) == (camp.KERNEL_LAYERNORM_ROWS, 512, 4)
     for rows, cols, nv in ((1025, 24576, 6), (2048, 24576, 6), (2048, 32768, 8)):   # rows
