@@ -7,9 +7,9 @@
 #include "common.cuh"
 #include "kernels.h"
 
-// Each translation unit that uses these keeps its own device error word (device variables
-// do not link across translation units in this build) and reports it through a host function
-// that camp_device_errors combines.
+// Each translation unit that uses these keeps its own device error word (without relocatable
+// device code, device variables do not link across translation units) and reports it
+// through a host function that camp_device_errors combines.
 
 namespace camp {
 namespace staged {

@@ -52,7 +52,7 @@ typedef enum {
     CAMP_ERR_INVALID_ARG = 1,      /* a null pointer, a bad size, eps, alignment or overlap */
     CAMP_ERR_UNSUPPORTED_DTYPE = 2,
     CAMP_ERR_RUNTIME = 3,          /* a CUDA call failed; see camp_last_cuda_error() */
-    CAMP_ERR_NOT_SUPPORTED = 5     /* a valid request that this build cannot run */
+    CAMP_ERR_NOT_SUPPORTED = 5     /* a valid request that no compiled kernel can run */
 } camp_status_t;
 
 /* Storage types. Arithmetic is fp32 for all three: bf16 is the upper half of an fp32,
