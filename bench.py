@@ -549,6 +549,7 @@ LARGE_CASES = [
     ("rmsnorm bf16 [1024,65536] (staged in shared memory)", "rms", (1024, 65536, False, 1e-5)),
     ("rmsnorm bf16 [256,131072] (staged in shared memory)", "rms", (256, 131072, False, 1e-5)),
     ("add_rmsnorm bf16 [512,131072] (staged in shared memory)", "add", (512, 131072)),
+    ("add_rmsnorm bf16 [2048,65536] (staged in shared memory)", "add", (2048, 65536)),
     ("layernorm bf16 [8192,4096]", "ln", (8192, 4096)),
     ("layernorm fp16 [8192,4096] (the TileLang tutorial's example 2)", "ln", (8192, 4096, "f16")),
     ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),

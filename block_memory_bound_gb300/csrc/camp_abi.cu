@@ -320,11 +320,24 @@ void rms_staged_plan_fields(const RmsCall& c, int cluster, int stages, int64_t c
 // fast (2048 x 32768: 0.87 / 0.88) and keep those rows.
 constexpr int64_t kStagedFrom = 4096;
 
+// With the residual add (x and r both staged) the measured best split differs (bf16,
+// graph-timed, two passes agreeing, fraction of the measured peak against the plain rule's
+// 8 CTAs of about 1024 vectors): up to 6144 vectors 4 CTAs with 3 buffers (2048 and 4096
+// rows of 40000 columns: 0.94 / 0.95 against 0.85 / 0.85); at 6144..8192 vectors 16 CTAs
+// with 3 buffers from 1024 rows on (1024 and 2048 rows of 65536: 0.94 / 0.95 against 0.86 /
+// 0.88) and 4 CTAs below (512 rows: 0.95 against 0.89).
+constexpr int64_t kStagedAddFew = 6144;
+constexpr int64_t kStagedAddManyRows = 1024;
+
 bool rms_choose_staged(const RmsCall& c, int64_t nvec, int* cluster, int* stages,
                        int64_t* chunk) {
-    int cl = 1;
-    while (cl < 16 && ceil_div(nvec, cl) > 1024) cl *= 2;
-    const int st = cl == 16 ? 2 : 3;
+    int cl = 1, st = 3;
+    if (c.add && nvec <= 8192) {
+        cl = (nvec <= kStagedAddFew || c.a.rows < kStagedAddManyRows) ? 4 : 16;
+    } else {
+        while (cl < 16 && ceil_div(nvec, cl) > 1024) cl *= 2;
+        st = cl == 16 ? 2 : 3;
+    }
     if (!rms_staged_fits(c, nvec, cl, st, chunk)) return false;
     *cluster = cl;
     *stages = st;

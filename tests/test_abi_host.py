@@ -376,8 +376,15 @@ def test_add_rmsnorm_exact_aliases_are_accepted(lib):
 @pytest.mark.parametrize("rows,cols,expect", [
     (4096, 2048, (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 1)),
     (16384, 8192, (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 1)),
-    # past 4096 vectors a row the add path stages x and r in shared memory
-    (64, 40000, (camp.KERNEL_RMSNORM_STAGED, 16, 625, 3, 8)),
+    # past 4096 vectors a row the add path stages x and r in shared memory: 4 CTAs of 3
+    # buffers up to 6144 vectors, and up to 8192 with fewer than 1024 rows; 16 CTAs of 3
+    # buffers at 6144..8192 vectors from 1024 rows on; past 8192 the plain rule
+    (64, 40000, (camp.KERNEL_RMSNORM_STAGED, 16, 1250, 3, 4)),
+    (4096, 40000, (camp.KERNEL_RMSNORM_STAGED, 16, 1250, 3, 4)),
+    (512, 65536, (camp.KERNEL_RMSNORM_STAGED, 16, 2048, 3, 4)),
+    (1024, 65536, (camp.KERNEL_RMSNORM_STAGED, 16, 512, 3, 16)),
+    (1024, 50000, (camp.KERNEL_RMSNORM_STAGED, 16, 391, 3, 16)),
+    (512, 131072, (camp.KERNEL_RMSNORM_STAGED, 16, 1024, 2, 16)),
 ])
 def test_add_rmsnorm_plans(lib, rows, cols, expect):
     p = camp.camp_add_rmsnorm_plan(X, R_, W, H_, Y, rows, cols, "bf16")
