@@ -607,6 +607,35 @@ bool rope_plan_latency(const RopeCall& c, camp_plan_t* p) {
     return best > 0;
 }
 
+// Between the decode sizes and a grid of kRopeFillCtas CTAs, the bandwidth choice leaves
+// most SMs idle: there the planner takes the tiled variant whose grid is the smallest one
+// of at least kRopeFillCtas CTAs (then the widest access, then the fewest heads per
+// thread). Measured on GB300 (bf16, graphs of back-to-back launches, every tiled variant
+// of Q, and of Q+K, at 256..8192 positions of 8 and 32 heads of 64 and 128): it changes the
+// plan of 7 of those 36 shapes, each 5-24% faster (256 x 8 x 64: 1.25 us against 1.61,
+// 512 x 8 x 64: 1.30 against 1.69, 1024 x 8 x 64: 1.62 against 1.75) and none slower;
+// reaching for 152 CTAs or more instead made 4 shapes 15-21% slower.
+constexpr int64_t kRopeFillCtas = 128;
+
+bool rope_plan_fill(const RopeCall& c, camp_plan_t* p) {
+    const int es = camp::elem_bytes(c.t);
+    int64_t best = 0;
+    for (int vb : {16, 8, 4}) {
+        if (vb < 2 * es || !rope_vec_ok(c, vb)) continue;
+        for (int hpt : {1, 2, 4, 8}) {
+            if (!camp::rope_compiled(c.t, vb, hpt) || rope_positions_per_cta(c, vb, hpt) == 0)
+                continue;
+            const int64_t g = rope_grid(c, CAMP_KERNEL_ROPE, vb, hpt);
+            if (g >= kRopeFillCtas && (best == 0 || g < best)) {   // ties keep the first seen
+                best = g;
+                p->vec_bytes = vb;
+                p->group = hpt;
+            }
+        }
+    }
+    return best > 0;
+}
+
 void rope_plan(const RopeCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
     p->cluster = 1;
@@ -627,6 +656,8 @@ void rope_plan(const RopeCall& c, camp_plan_t* p) {
     if (rope_positions_per_cta(c, p->vec_bytes, p->group) > 0) {
         p->kernel = CAMP_KERNEL_ROPE;
         p->grid = rope_grid(c, CAMP_KERNEL_ROPE, p->vec_bytes, p->group);
+        if (p->grid < kRopeFillCtas && rope_plan_fill(c, p))
+            p->grid = rope_grid(c, CAMP_KERNEL_ROPE, p->vec_bytes, p->group);
     } else if (c.a.heads2 == 0) {
         p->kernel = CAMP_KERNEL_ROPE_FLAT;
         p->grid = rope_grid(c, CAMP_KERNEL_ROPE_FLAT, p->vec_bytes, p->group);

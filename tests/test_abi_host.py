@@ -190,7 +190,13 @@ def test_rmsnorm_plan_misaligned_pointer_uses_element_accesses(lib):
     (1, 8, 32, 64, "bf16", (camp.KERNEL_ROPE, 8, 1, 8)),        # 256 threads a position
     (1, 64, 8, 128, "bf16", (camp.KERNEL_ROPE, 4, 1, 64)),
     (1, 152, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 1, 152)),
-    (1, 153, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 2, 77)),   # past the SMs
+    # past the SMs, while the bandwidth choice would leave fewer than 128 CTAs: the variant
+    # with the smallest grid of at least 128 CTAs
+    (1, 153, 32, 128, "bf16", (camp.KERNEL_ROPE, 16, 1, 153)),
+    (1, 256, 8, 64, "bf16", (camp.KERNEL_ROPE, 4, 1, 128)),
+    (1, 512, 8, 64, "bf16", (camp.KERNEL_ROPE, 8, 1, 128)),
+    (1, 1024, 8, 64, "bf16", (camp.KERNEL_ROPE, 16, 1, 128)),
+    (1, 512, 32, 64, "bf16", (camp.KERNEL_ROPE, 16, 2, 128)),     # already 128 CTAs
     # a position needs more than one CTA: the flat kernel
     (1, 4, 1024, 256, "bf16", (camp.KERNEL_ROPE_FLAT, 16, 2, 128)),
 ])
@@ -304,7 +310,7 @@ def test_rope_qk_empty_and_single_tensor_calls_need_no_cuda(lib):
     # Q 32 + K 8 heads of 64, 2 heads per thread: (16 + 4) x 4 = 80 threads a position,
     # 3 positions per CTA
     (1, 4096, 32, 8, 64, (camp.KERNEL_ROPE, 16, 2, 1366)),
-    (2, 128, 14, 2, 128, (camp.KERNEL_ROPE, 16, 2, 64)),
+    (2, 128, 14, 2, 128, (camp.KERNEL_ROPE, 16, 1, 128)),    # 64 CTAs with 2 heads: fill to 128
     (1, 65536, 32, 8, 128, (camp.KERNEL_ROPE, 16, 4, 21846)),
     (1, 16, 3, 1, 64, (camp.KERNEL_ROPE, 4, 1, 4)),         # decode size: 64 threads a position
     (1, 8, 32, 8, 64, (camp.KERNEL_ROPE, 16, 1, 8)),         # 160 threads: the widest of 3 ties
