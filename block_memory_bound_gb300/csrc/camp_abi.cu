@@ -915,6 +915,26 @@ camp_status_t rope_il_plan(const RopeIlCall& c, const camp_plan_t* forced, camp_
         if (p->vec_bytes == 0) return CAMP_ERR_NOT_SUPPORTED;   // pointers not pair-aligned
         p->group = c.a.heads % 4 == 0 ? 4 : c.a.heads % 2 == 0 ? 2 : 1;
         while (p->group < 8 && rope_il_tpc(c, p->vec_bytes, p->group) == 0) p->group *= 2;
+        // The rotate-half planner's fill rule: fewer than kRopeFillCtas CTAs leave most SMs
+        // idle, so take the variant with the smallest grid of at least that many.
+        const int64_t t0 = rope_il_tpc(c, p->vec_bytes, p->group);
+        if (t0 > 0 && ceil_div(c.a.tokens, t0) < kRopeFillCtas) {
+            int64_t best = 0;
+            for (int vb : {16, 8, 4}) {
+                if (!rope_il_vec_ok(c, vb)) continue;
+                for (int hpt : {1, 2, 4, 8}) {
+                    const int64_t tpc = camp::rope_interleaved_compiled(c.t, vb, hpt)
+                                            ? rope_il_tpc(c, vb, hpt) : 0;
+                    if (tpc == 0) continue;
+                    const int64_t g = ceil_div(c.a.tokens, tpc);
+                    if (g >= kRopeFillCtas && (best == 0 || g < best)) {
+                        best = g;
+                        p->vec_bytes = vb;
+                        p->group = hpt;
+                    }
+                }
+            }
+        }
     }
     if (!camp::rope_interleaved_compiled(c.t, p->vec_bytes, p->group)) return CAMP_ERR_NOT_SUPPORTED;
     const int64_t tpc = rope_il_tpc(c, p->vec_bytes, p->group);
@@ -1016,6 +1036,26 @@ camp_status_t kv_cat_plan(const KvCatCall& c, const camp_plan_t* forced, camp_pl
         }
         p->group = c.a.heads % 2 == 0 ? 2 : 1;
         while (p->group < 8 && kv_cat_tpc(c, p->vec_bytes, p->group) == 0) p->group *= 2;
+        // The rotate-half planner's fill rule (fewer than kRopeFillCtas CTAs: the variant
+        // with the smallest grid of at least that many).
+        const int64_t t0 = kv_cat_tpc(c, p->vec_bytes, p->group);
+        if (t0 > 0 && ceil_div(c.rows, t0) < kRopeFillCtas) {
+            int64_t best = 0;
+            for (int vb : {16, 8, 4, 2}) {
+                if (!kv_cat_vec_ok(c, vb)) continue;
+                for (int hpt : {1, 2, 4, 8}) {
+                    const int64_t tpc =
+                        camp::kv_cat_compiled(c.t, vb, hpt) ? kv_cat_tpc(c, vb, hpt) : 0;
+                    if (tpc == 0) continue;
+                    const int64_t g = ceil_div(c.rows, tpc);
+                    if (g >= kRopeFillCtas && (best == 0 || g < best)) {
+                        best = g;
+                        p->vec_bytes = vb;
+                        p->group = hpt;
+                    }
+                }
+            }
+        }
     }
     if (!camp::kv_cat_compiled(c.t, p->vec_bytes, p->group)) return CAMP_ERR_NOT_SUPPORTED;
     const int64_t tpc = kv_cat_tpc(c, p->vec_bytes, p->group);

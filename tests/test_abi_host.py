@@ -501,9 +501,13 @@ def test_rope_interleaved_plans(lib):
     p = camp.camp_rope_interleaved_plan(*ILP, 65536, 32, 128, 131072, "bf16")
     assert (p.kernel, p.vec_bytes, p.group, p.grid) == (camp.KERNEL_ROPE_INTERLEAVED, 16, 4, 32768)
     p = camp.camp_rope_interleaved_plan(*ILP, 1000, 5, 6, 16, "bf16")     # odd head count
-    assert (p.vec_bytes, p.group, p.grid) == (4, 1, 59)
-    p = camp.camp_rope_interleaved_plan(*ILP, 1000, 6, 64, 16, "bf16")    # even, not 4k
-    assert p.group == 2
+    assert (p.vec_bytes, p.group, p.grid) == (4, 1, 59)   # no variant reaches 128 CTAs
+    p = camp.camp_rope_interleaved_plan(*ILP, 4000, 6, 64, 16, "bf16")    # even, not 4k
+    assert (p.vec_bytes, p.group, p.grid) == (16, 2, 400)
+    # fewer than 128 CTAs: the smallest grid of at least 128 (1000 x 6 x 64: 2 heads a
+    # thread would give 100 CTAs)
+    p = camp.camp_rope_interleaved_plan(*ILP, 1000, 6, 64, 16, "bf16")
+    assert (p.vec_bytes, p.group, p.grid) == (16, 1, 200)
     p = camp.camp_rope_interleaved_plan(*ILP, 1000, 64, 128, 16, "bf16")  # 4 heads: 256 threads
     assert p.group == 4
     p = camp.camp_rope_interleaved_plan(*ILP, 1000, 128, 128, 16, "bf16")  # 4 heads: 512 threads
@@ -747,6 +751,10 @@ def test_kv_cat_plans(lib):
     assert (p.vec_bytes, p.group, p.grid) == (16, 2, 2 * 4096 // 4)   # 64 threads a row
     p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 3, 4, 5, 6, 2, "bf16")     # odd heads, D/2 = 3
     assert (p.vec_bytes, p.group, p.grid) == (2, 1, 1)
+    # fewer than 128 CTAs (256 rows: 16 with the bandwidth choice): the variant with the
+    # smallest grid of at least 128
+    p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 255, 1, 8, 64, 4, "bf16")
+    assert (p.vec_bytes, p.group, p.grid) == (4, 1, 128)
     p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 3, 4, 64, 256, 2, "bf16")  # 64 heads of 256
     assert (p.vec_bytes, p.group) == (16, 4)                             # 16 x 16 threads
     p = camp.camp_kv_cat_repeat_plan(*CAT, 1, 3, 4, 128, 256, 2, "bf16")
