@@ -188,8 +188,17 @@ struct RowsCandidate {
 // group. Measured on GB300 (bf16, graphs of back-to-back launches): 1 x 8192 512 x 2
 // 1.97 us against 256 x 4 2.22 us, 1 x 3000 512 x 1 1.70 against 128 x 3 1.94, 8 x 8192
 // 512 x 2 2.05 against 2.21, 64 x 8192 2.07 against 2.32; 1 x 2048 256 x 1 1.52.
+// Rows of RMSNorm up to kRowsFewRows rows take the 2..4-accesses band with groups of up to
+// 512 threads, and the residual-add path takes 2 accesses a thread in groups of up to 512
+// at every row count: a sweep of every rows variant at 256..8192 rows of 2048, 3000 and
+// 8192 bf16 columns (36 shapes, both paths) changed 15 plans, each 0.5-21% faster (512 x
+// 8192: 512 x 2 3.62 us against 256 x 4 4.41; with the add, 256 x 8192 3.56 against 4.53,
+// 1024 x 3000 4.45 against 4.97) and none slower. With few rows a launch is short of
+// threads in flight, and the add path holds twice the data a thread.
+constexpr int64_t kRowsFewRows = 2048;
+
 bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm,
-                 bool latency) {
+                 bool latency, bool add = false, int64_t rows = 0) {
     const int64_t sa = a.ctas < camp::kSmCount ? a.ctas : camp::kSmCount;
     const int64_t sb = b.ctas < camp::kSmCount ? b.ctas : camp::kSmCount;
     if (sa != sb) return sa > sb;
@@ -200,8 +209,13 @@ bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm,
         if (a.idle != b.idle) return a.idle < b.idle;
         return a.group < b.group;
     }
-    const bool ma = a.per_thread >= 2 && a.per_thread <= 4 && a.group <= 256;
-    const bool mb = b.per_thread >= 2 && b.per_thread <= 4 && b.group <= 256;
+    auto in_band = [&](const RowsCandidate& k) {
+        if (!layernorm && add) return k.per_thread == 2 && k.group <= 512;
+        const int gmax = (!layernorm && rows <= kRowsFewRows) ? 512 : 256;
+        return k.per_thread >= 2 && k.per_thread <= 4 && k.group <= gmax;
+    };
+    const bool ma = in_band(a);
+    const bool mb = in_band(b);
     if (ma != mb) return ma;
     if (a.idle != b.idle) return a.idle < b.idle;
     if (a.one_wave != b.one_wave) return a.one_wave;
@@ -249,7 +263,8 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread,
                       : camp::rows_min_blocks(vb, g, c.add ? 2 * k.per_thread : k.per_thread);
         k.one_wave = k.ctas <= static_cast<int64_t>(camp::kSmCount) * per_sm;
         k.many_waves = k.ctas >= 2 * static_cast<int64_t>(camp::kSmCount) * per_sm;
-        if (!found || rows_better(k, best, layernorm, c.a.rows <= camp::kSmCount)) best = k;
+        if (!found || rows_better(k, best, layernorm, c.a.rows <= camp::kSmCount, c.add, c.a.rows))
+            best = k;
         found = true;
     }
     if (!found) return false;

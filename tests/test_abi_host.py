@@ -138,7 +138,10 @@ def test_rope_empty_is_success_without_cuda(lib):
     (1, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 2, 512, 1)),
     (8, 3000, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 1, 512, 8)),
     (152, 2048, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 1, 256, 152)),
-    (153, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 153)),   # past the SMs
+    # past the SMs, up to 2048 rows: 2..4 accesses in groups of up to 512 threads
+    (153, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 2, 512, 153)),
+    (2048, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 512, 2, 512, 2048)),
+    (4096, 8192, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 256, 4096)),
     (1, 8, "bf16", (camp.KERNEL_RMSNORM_ROWS, 16, 32, 1, 256, 1)),
     (64, 3001, "bf16", (camp.KERNEL_RMSNORM_ROWS, 2, 256, 16, 256, 64)),
     # wider rows: one CTA of up to 1024 threads while it holds the row (8192 vectors);
@@ -380,8 +383,10 @@ def test_add_rmsnorm_exact_aliases_are_accepted(lib):
 
 
 @pytest.mark.parametrize("rows,cols,expect", [
+    # the add path: 2 accesses a thread in groups of up to 512 threads
     (4096, 2048, (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 1)),
-    (16384, 8192, (camp.KERNEL_RMSNORM_ROWS, 16, 256, 4, 1)),
+    (16384, 8192, (camp.KERNEL_RMSNORM_ROWS, 16, 512, 2, 1)),
+    (1024, 3000, (camp.KERNEL_RMSNORM_ROWS, 16, 256, 2, 1)),
     # past 4096 vectors a row the add path stages x and r in shared memory: 4 CTAs of 3
     # buffers up to 6144 vectors, and up to 8192 with fewer than 1024 rows; 16 CTAs of 3
     # buffers at 6144..8192 vectors from 1024 rows on; past 8192 the plain rule
