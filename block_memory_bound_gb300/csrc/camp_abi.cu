@@ -153,6 +153,7 @@ struct RowsCandidate {
     int64_t ctas, idle;
     bool one_wave;     // every CTA resident at once (CTAs <= SMs x CTAs per SM)
     bool many_waves;   // at least 2 waves of CTAs
+    bool add16;        // residual-add path on 16-byte vectors (may take 1024-thread groups)
 };
 
 // Is candidate a preferred over b? Measured on GB300 (L2-cold, back-to-back launches):
@@ -197,6 +198,17 @@ struct RowsCandidate {
 // threads in flight, and the add path holds twice the data a thread. The same band for
 // LayerNorm (18 bf16 and 6 fp16 shapes at 256..8192 rows of 2048..8192 columns): 3 plans
 // changed, 7-12% faster (512 x 8192: 512 x 2 4.75 us against 256 x 4 5.40), none slower.
+// The residual-add path on 16-byte vectors lifts the 512-thread cap to 1024 wherever a
+// 1024-thread group gives every thread at least 2 accesses, that is past 1024 vectors a row
+// (the band's 2 accesses, otherwise at most 4; at decode sizes the fewest accesses): each
+// thread holds x and r, and halving a thread's work pays more than the wider barrier costs.
+// Measured at 1..8192 rows of 1536, 2048, 3072 and 4096 vectors (bf16 and fp32, 64 shapes):
+// the 1024-thread group is 0.1-32% faster in 55 of them (152 x 12288 fp32: 1024 x 3 6.29 us
+// against 512 x 6 8.32; 512 x 32768 bf16: 1024 x 4 25.9 against 29.2; 2048 x 16384 bf16:
+// 1024 x 2 40.3 against 41.2), at most 5% slower in the others (fp32 at 3072 vectors and
+// 512..4096 rows, 1536 vectors at 1..8 rows). Plain RMSNorm keeps 512: there the
+// 1024-thread group loses at 768 rows and more (2048 x 32768 bf16: 1024 x 4 51.0 us against
+// 512 x 8 43.3).
 constexpr int64_t kRowsFewRows = 2048;
 
 bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm,
@@ -204,15 +216,17 @@ bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm,
     const int64_t sa = a.ctas < camp::kSmCount ? a.ctas : camp::kSmCount;
     const int64_t sb = b.ctas < camp::kSmCount ? b.ctas : camp::kSmCount;
     if (sa != sb) return sa > sb;
+    const int add_gmax = a.add16 ? 1024 : 512;
     if (latency) {
-        const bool la = a.group <= 512, lb = b.group <= 512;
+        const bool la = a.group <= 512 || (a.group <= add_gmax && a.per_thread >= 2);
+        const bool lb = b.group <= 512 || (b.group <= add_gmax && b.per_thread >= 2);
         if (la != lb) return la;
         if (a.per_thread != b.per_thread) return a.per_thread < b.per_thread;
         if (a.idle != b.idle) return a.idle < b.idle;
         return a.group < b.group;
     }
     auto in_band = [&](const RowsCandidate& k) {
-        if (!layernorm && add) return k.per_thread == 2 && k.group <= 512;
+        if (!layernorm && add) return k.per_thread == 2 && k.group <= add_gmax;
         const int gmax = rows <= kRowsFewRows ? 512 : 256;
         return k.per_thread >= 2 && k.per_thread <= 4 && k.group <= gmax;
     };
@@ -224,8 +238,8 @@ bool rows_better(const RowsCandidate& a, const RowsCandidate& b, bool layernorm,
     if (ma && layernorm && a.many_waves && b.many_waves) return a.per_thread > b.per_thread;
     if (ma) return a.per_thread < b.per_thread;
     if (!layernorm) {
-        const bool na = a.per_thread <= 4 && a.group <= 512;
-        const bool nb = b.per_thread <= 4 && b.group <= 512;
+        const bool na = a.per_thread <= 4 && a.group <= add_gmax;
+        const bool nb = b.per_thread <= 4 && b.group <= add_gmax;
         if (na != nb) return na;
     }
     return a.group < b.group;
@@ -265,6 +279,7 @@ bool rms_choose_rows(const RmsCall& c, int vb, int* group, int* per_thread,
                       : camp::rows_min_blocks(vb, g, c.add ? 2 * k.per_thread : k.per_thread);
         k.one_wave = k.ctas <= static_cast<int64_t>(camp::kSmCount) * per_sm;
         k.many_waves = k.ctas >= 2 * static_cast<int64_t>(camp::kSmCount) * per_sm;
+        k.add16 = c.add && vec && !layernorm;
         if (!found || rows_better(k, best, layernorm, c.a.rows <= camp::kSmCount, c.add, c.a.rows))
             best = k;
         found = true;

@@ -383,10 +383,18 @@ def test_add_rmsnorm_exact_aliases_are_accepted(lib):
 
 
 @pytest.mark.parametrize("rows,cols,expect", [
-    # the add path: 2 accesses a thread in groups of up to 512 threads
+    # the add path: 2 accesses a thread in groups of up to 512 threads, and past 1024
+    # vectors a row 1024-thread groups (2 accesses, else at most 4; fewest at decode sizes)
     (4096, 2048, (camp.KERNEL_RMSNORM_ROWS, 16, 128, 2, 1)),
     (16384, 8192, (camp.KERNEL_RMSNORM_ROWS, 16, 512, 2, 1)),
     (1024, 3000, (camp.KERNEL_RMSNORM_ROWS, 16, 256, 2, 1)),
+    (8, 8192, (camp.KERNEL_RMSNORM_ROWS, 16, 512, 2, 1)),
+    (512, 12288, (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 2, 1)),
+    (4096, 16384, (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 2, 1)),
+    (1, 16384, (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 2, 1)),
+    (2048, 24576, (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 3, 1)),
+    (152, 32768, (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 4, 1)),
+    (8192, 32768, (camp.KERNEL_RMSNORM_ROWS, 16, 1024, 4, 1)),
     # past 4096 vectors a row the add path stages x and r in shared memory: 4 CTAs of 3
     # buffers up to 6144 vectors, and up to 8192 with fewer than 1024 rows; 16 CTAs of 3
     # buffers at 6144..8192 vectors from 1024 rows on; past 8192 the plain rule

@@ -117,6 +117,14 @@ def test_every_variant(dtype):
         run_case(4, 8192, dtype, seed=vb, plan=plan)
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows,cols", [(777, 12288), (153, 16384), (9, 24576), (1, 32768)])
+def test_default_plans_past_1024_vectors(rows, cols, dtype):
+    # 1024-thread groups on the 16-bit types (2, 2, 3 and 4 accesses a thread), the
+    # staged kernel for fp32 at 24576 columns and more
+    run_case(rows, cols, dtype, seed=rows + cols)
+
+
 def test_config_bf16_4096x2048():
     run_case(4096, 2048, "bf16", seed=0)
 
