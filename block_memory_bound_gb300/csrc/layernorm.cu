@@ -13,7 +13,12 @@
 //      (K, mu) and never rounded to one fp32 number: every deviation is formed as
 //      d = (x - K) - mu, whose rounding errors are relative to the spread of the row, not
 //      to |mean| (an fp32 mean alone is off by up to ulp(mean) / 2);
-//   2. var = sum(d^2) / n from the registers;
+//   2. var = sum(d^2) / n from the registers; in 16-bit storage (where the kernel is bound
+//      by instruction issue) pass 1 also sums (x - K)^2, and when mu^2 <= 4 (that sum / n -
+//      mu^2), i.e. K lies within two standard deviations of the mean, that difference is
+//      the variance and pass 2 is skipped: its cancellation then costs at most a few times
+//      the summation error of the two-pass value, far below a 16-bit output's rounding;
+//      a row whose shift lies further out (or whose difference is negative) takes pass 2;
 //   3. y = fma(d * rsqrt(var + eps), gamma, beta), rounded once.
 #include "common.cuh"
 #include "kernels.h"
@@ -41,6 +46,43 @@ __device__ __forceinline__ float group_sum(float v, float (&scratch)[LnShape<G>:
         v = sum_partials<LnShape<G>::kWarpsPerRow>(scratch[g]);
     }
     return v;
+}
+
+// Sums of a and b over the row group with one barrier (G > 32), as group_sum.
+template <int G>
+__device__ __forceinline__ void group_sum2(float& a, float& b,
+                                           float (&sa)[LnShape<G>::kRowsPerCta][LnShape<G>::kWarpsPerRow],
+                                           float (&sb)[LnShape<G>::kRowsPerCta][LnShape<G>::kWarpsPerRow],
+                                           int g, int t) {
+    a = warp_sum(a);
+    b = warp_sum(b);
+    if constexpr (LnShape<G>::kWarpsPerRow > 1) {
+        if ((threadIdx.x & 31) == 0) {
+            sa[g][t / 32] = a;
+            sb[g][t / 32] = b;
+        }
+        __syncthreads();
+        a = sum_partials<LnShape<G>::kWarpsPerRow>(sa[g]);
+        b = sum_partials<LnShape<G>::kWarpsPerRow>(sb[g]);
+    }
+}
+
+// Pass 1 of the one-pass path (packed pairs): this thread's sums of (x - K) and (x - K)^2.
+template <typename C, int G, int NV, int VB>
+__device__ __forceinline__ void shifted_moments(const Raw<VB> (&v)[NV], float shift, int live,
+                                                float& s1, float& s2) {
+    const f32x2 k2 = f2_make(shift, shift);
+    f32x2 a = f2_make(0.0f, 0.0f), q = f2_make(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        if (k * G < live)
+            C::each_pair(v[k], [&](int, f32x2 p) {
+                const f32x2 d = f2_sub(p, k2);
+                a = f2_add(a, d);
+                q = f2_fma(d, d, q);
+            });
+    s1 = f2_lo(a) + f2_hi(a);
+    s2 = f2_lo(q) + f2_hi(q);
 }
 
 // Pass 1: this thread's sum of (x - K) over its live accesses.
@@ -123,8 +165,12 @@ layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
     constexpr int E = C::kElems;
     constexpr int ES = Storage<S>::kBytes;
 
+    // The one-pass statistics (pass 2 only where the shift is far from the mean): 16-bit
+    // storage in packed pairs.
+    constexpr bool kOnePass = ES == 2 && E >= 2;
     __shared__ float part_mean[Sh::kRowsPerCta][Sh::kWarpsPerRow];
     __shared__ float part_var[Sh::kRowsPerCta][Sh::kWarpsPerRow];
+    __shared__ float part_sq[kOnePass ? Sh::kRowsPerCta : 1][Sh::kWarpsPerRow];
 
     const int64_t block = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
     if (threadIdx.x == 0 && block * Sh::kRowsPerCta < rows) {   // this CTA's rows of x
@@ -157,8 +203,28 @@ layernorm_rows_kernel(const void* x, const void* __restrict__ gamma,
     }
 
     const float n = static_cast<float>(cols);
-    const float mu = group_sum<G>(shifted_sum<C, G>(v, shift, live), part_mean, g, t) / n;
-    const float var = group_sum<G>(squared_deviations<C, G>(v, shift, mu, live), part_var, g, t) / n;
+    float mu, var;
+    if constexpr (kOnePass) {
+        float s1, s2;
+        shifted_moments<C, G>(v, shift, live, s1, s2);
+        group_sum2<G>(s1, s2, part_mean, part_sq, g, t);
+        mu = s1 / n;
+        var = s2 / n - mu * mu;
+        // Every lane of a group holds the same bits, so the choice is uniform per group; with
+        // several warps a row it is made CTA-wide, since the reduction has a barrier.
+        const bool two_pass = !(mu * mu <= 4.0f * var);
+        bool any;
+        if constexpr (Sh::kWarpsPerRow > 1) any = __syncthreads_or(two_pass) != 0;
+        else any = two_pass;
+        if (any) {
+            const float d2 = group_sum<G>(
+                two_pass ? squared_deviations<C, G>(v, shift, mu, live) : 0.0f, part_var, g, t);
+            if (two_pass) var = d2 / n;
+        }
+    } else {
+        mu = group_sum<G>(shifted_sum<C, G>(v, shift, live), part_mean, g, t) / n;
+        var = group_sum<G>(squared_deviations<C, G>(v, shift, mu, live), part_var, g, t) / n;
+    }
     const float rstd = rsqrtf(var + eps);
 
     if (!active) return;

@@ -69,15 +69,21 @@ def check(got: torch.Tensor, x_cpu, g_cpu, b_cpu, eps32: float, plan: camp.Plan,
         k = per_thread * (16 // es) + 5 + 8 + plan.cluster
     else:
         k = plan.per_thread * (plan.vec_bytes // es) + 5 + plan.group // 32
+    # The rows kernel in 16-bit storage with packed accesses takes the variance in one pass,
+    # sum((x - K)^2) / n - mu^2, whenever mu^2 <= 4 of that value; it then cancels at most
+    # about 5 var against its inputs, so its error is at most about 14 times the summation
+    # error, moving rstd by 7 k u relatively and y by 7 k u |xhat| |gamma|.
+    one_pass = (plan.kernel != camp.KERNEL_LAYERNORM_STAGED and es == 2
+                and plan.vec_bytes >= 2 * es)
     g, b = _decode(g_cpu), _decode(b_cpu)
     step = max(1, (1 << 22) // cols)
     for r0 in range(0, rows, step):
         r1 = min(rows, r0 + step)
         _check_rows(_decode(got[r0:r1]), _decode(x_cpu[r0:r1]), g, b, eps32, k, r0,
-                    dtype, what)
+                    dtype, what, one_pass)
 
 
-def _check_rows(y, x, g, b, eps32, k, r0, dtype, what):
+def _check_rows(y, x, g, b, eps32, k, r0, dtype, what, one_pass=False):
     ref, _ = oracle.layernorm_f64(x, g, b, eps32)
     dev = x - x[:, :1]
     var = ((x - x.mean(axis=1, keepdims=True)) ** 2).mean(axis=1, keepdims=True)
@@ -85,6 +91,8 @@ def _check_rows(y, x, g, b, eps32, k, r0, dtype, what):
     c = np.abs(dev).mean(axis=1, keepdims=True) / sig
     xhat = (x - x.mean(axis=1, keepdims=True)) / sig
     bound = U32 * ((k + 4) * np.abs(g) * (c + np.abs(xhat) * (1 + c)) + np.abs(ref))
+    if one_pass:
+        bound = bound + U32 * 8 * (k + 4) * np.abs(g) * np.abs(xhat)
     if dtype != "f32":
         bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(y)), dtype)
     err = np.abs(y - ref)
