@@ -79,6 +79,18 @@ WORKLOAD = ("llama3.2-1b prefill 4096 tokens: rmsnorm x[4096,2048] + rope of Q[1
 
 FALLBACK_HBM_GBS = 6800.0
 
+# How the timed region keeps HBM cold; one statement for both arms so their configs match.
+L2_POLICY = ("inputs larger than L2: rotating input sets of more than 4 x L2 in total, "
+             "and an L2 flush (a write larger than L2) between timed repeats")
+# Both arms print this config: N independent replicas of the workload (one per rank).
+STEP_CONFIG = {"workload": WORKLOAD, "parallelism": "replicas", "step_bytes": STEP_BYTES,
+               "l2": L2_POLICY}
+
+# Where the per-kernel, large-shape, sweep and calibration figures are written (the JSON
+# line on stdout stays short).
+DETAIL_PATH = os.path.join("gpurun_out", "bench_detail.json")
+LINE_LIMIT = 2048   # bytes of the final stdout line
+
 
 # ------------------------------------------------------------------ helpers
 
@@ -401,7 +413,7 @@ def run_reference(args) -> None:
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "parallelism": "replicas"},
+        "config": dict(STEP_CONFIG),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -745,18 +757,23 @@ def oracle_case(kind: str, tensors: tuple, shp: tuple, budget_bytes: int = 64 <<
             "kind": "oracle", "sample": f"{what}, median of {runs}"}
 
 
+# Most input sets one large-shape or sweep case rotates over: every case of at least
+# 4 x L2 / MAX_SETS bytes (about 0.5 MB) is timed L2-cold.
+MAX_SETS = 1024
+
+
 def large_configs(peak: float, reps: int, cases=None, cpu: bool = False) -> list[dict]:
     """Single-operator timings, timed like the step: a CUDA graph of N back-to-back launches
-    rotating over R input sets (R x bytes > 4 x L2 where R <= 8 allows it, so every launch
-    reads from HBM), one event pair per graph replay; the median over `reps` replays of
-    the replay time / N."""
+    rotating over R input sets (R x bytes > 4 x L2 for every case of more than 4 x L2 /
+    MAX_SETS bytes, so every launch reads from HBM), one event pair per graph replay; the
+    median over `reps` replays of the replay time / N."""
     out = []
     l2 = getattr(torch.cuda.get_device_properties(torch.cuda.current_device()),
                  "L2_cache_size", 0) or 129 * 2**20
     for name, kind, shp in (LARGE_CASES if cases is None else cases):
         first = _large_case(kind, shp, 0)
         nbytes = first[1]
-        R = max(1, min(8, math.ceil(4 * l2 / nbytes)))
+        R = max(1, min(MAX_SETS, math.ceil(4 * l2 / nbytes)))
         sets = [first] + [_large_case(kind, shp, i) for i in range(1, R)]
         N = R * max(1, round(16 / R))
         stream = torch.cuda.current_stream().cuda_stream
@@ -887,13 +904,118 @@ def run_case(case: str, launches: int) -> None:
     print(json.dumps({"case": case, "kernel": plan, "launches": launches}), flush=True)
 
 
+# ------------------------------------------------------------------ the JSON line
+
+def build_line(*, value: float, world: int, steps: int, warmup: int, ms_per_step: float,
+               reps: int, M: int, kernels: list[dict], roofline: dict, cpu: dict | None,
+               e2e: dict, clocks: dict, peak: float, detail_path: str | None) -> dict:
+    """The one JSON line rank 0 prints last: the headline metric and the keys the
+    benchmark contract names, and nothing bulky (the per-shape tables go to the detail
+    file)."""
+    r3 = lambda v: None if v is None else round(float(v), 3)
+    short_k = [{"name": k["name"], "kernel": k["kernel"], "us": r3(k["us"]),
+                "GB/s": r3(k["GB/s"]), "frac": r3(k["frac"])} for k in kernels]
+    line = {
+        "metric": METRIC, "value": r3(value), "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(STEP_CONFIG),
+        "timing": {"repeats": reps, "stat": "median over repeats of the K-step region",
+                   "graph_steps": M, "pct_of_peak": r3(100.0 * value / world / peak)},
+        "roofline": {k: (r3(v) if isinstance(v, float) else v) for k, v in roofline.items()},
+        "kernels": short_k,
+        "cpu_baseline": None if cpu is None else {
+            "value": r3(cpu["value"]), "unit": cpu["unit"], "cores": cpu["cores"],
+            "kind": cpu["kind"], "sample": cpu["sample"]},
+        "e2e": {"value": r3(e2e["value"]), "unit": e2e["unit"],
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "serial": r3(e2e["serial"]["value"])},
+        "gpu_launches": len(kernels) * steps * reps,
+        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                   "reasons": clocks.get("reasons", []), "samples": clocks.get("samples", 0)},
+    }
+    if detail_path:
+        line["detail"] = detail_path
+    return line
+
+
+def line_text(line: dict) -> str:
+    """The line as printed; raises if it is not under LINE_LIMIT bytes."""
+    text = json.dumps(line, separators=(",", ":"))
+    if len(text.encode()) > LINE_LIMIT:
+        raise ValueError(f"the JSON line is {len(text)} bytes, over {LINE_LIMIT}")
+    return text
+
+
+def write_detail(path: str, detail: dict) -> str | None:
+    try:
+        os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+        with open(path, "w") as f:
+            json.dump(detail, f, indent=1)
+        return path
+    except OSError as e:
+        log(f"bench: could not write {path}: {e}")
+        return None
+
+
+# ------------------------------------------------------------------ the timed region
+
+def make_flush(l2: int) -> torch.Tensor:
+    """A buffer of twice the L2 size; writing it evicts whatever a region left in L2."""
+    return torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+
+
+def time_regions(graphs: dict, tail: dict | None, blocks: list, reps: int,
+                 flush: torch.Tensor) -> tuple[list[float], dict[str, list[float]]]:
+    """`reps` repeats of the K-step region. Before each, L2 is flushed (outside the
+    events); each repeat records a start event, then per block one graph per operator with
+    an event after each. Returns per repeat the region's seconds and per operator its
+    summed graph seconds."""
+    M = blocks[0][0]
+    rec = []
+    for _ in range(reps):
+        flush.fill_(1.0)
+        start = torch.cuda.Event(enable_timing=True)
+        start.record()
+        marks = []
+        for count, _ in blocks:
+            gs = graphs if count == M else tail
+            row = []
+            for kind in KERNELS:
+                gs[kind].replay()
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record()
+                row.append(ev)
+            marks.append(row)
+        rec.append((start, marks))
+    torch.cuda.synchronize()
+    region, per = [], {kind: [] for kind in KERNELS}
+    for start, marks in rec:
+        region.append(start.elapsed_time(marks[-1][-1]) * 1e-3)
+        acc = {kind: 0.0 for kind in KERNELS}
+        prev = start
+        for row in marks:
+            for kind, ev in zip(KERNELS, row):
+                acc[kind] += prev.elapsed_time(ev) * 1e-3
+                prev = ev
+        for kind in KERNELS:
+            per[kind].append(acc[kind])
+    return region, per
+
+
 # ------------------------------------------------------------------ main
 
 def main() -> None:
     ap = argparse.ArgumentParser(description="RMSNorm + RoPE hot-path benchmark")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--steps", type=int, default=640)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--repeats", type=int, default=21,
+                    help="least number of timed repeats of the K-step region (median reported)")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the region until about this much GPU time (clock samples)")
     ap.add_argument("--impl", choices=("camp", "reference"), default="camp")
     ap.add_argument("--graph-steps", type=int, default=0,
                     help="steps per captured graph (0: a whole number of input rotations near 64)")
@@ -901,6 +1023,8 @@ def main() -> None:
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--large-reps", type=int, default=50)
+    ap.add_argument("--detail", default=DETAIL_PATH,
+                    help="file for the per-kernel, large-shape and sweep figures")
     ap.add_argument("--no-large", action="store_true", help="skip the large-shape timings")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", default=None,
@@ -921,6 +1045,8 @@ def main() -> None:
         ap.error("--warmup must be at least 3")
     if args.steps < 1:
         ap.error("--steps must be at least 1")
+    if args.repeats < 1:
+        ap.error("--repeats must be at least 1")
 
     if args.impl == "reference":
         run_reference(args)
@@ -942,6 +1068,7 @@ def main() -> None:
     l2 = getattr(props, "L2_cache_size", 0) or 129 * 2**20
     R = max(2, math.ceil(4 * l2 / STEP_BYTES))
     sets = [InputSet(seed=rank * 1000 + i, device="cuda") for i in range(R)]
+    flush = make_flush(l2)
     torch.cuda.synchronize()
     plans = {
         "rmsnorm": plan_name("rmsnorm", camp.camp_rmsnorm_plan(
@@ -964,9 +1091,12 @@ def main() -> None:
     graphs = {kind: capture_kernel(sets, kind, 0, M) for kind in KERNELS}
     tail = ({kind: capture_kernel(sets, kind, n_full * M, rest) for kind in KERNELS}
             if rest else None)
-    for kind in KERNELS:                   # uploads the graphs; untimed
-        graphs[kind].replay()
-    torch.cuda.synchronize()
+    # Upload the graphs and size the repeats (untimed): at least --repeats, and enough for
+    # about --min-seconds of GPU time so that the clock sampler sees the load.
+    probe, _ = time_regions(graphs, tail, blocks, 3, flush)
+    t_rep = statistics.median(probe) + 2 * l2 / (peak * 1e9)
+    reps = max(args.repeats, min(100000, math.ceil(args.min_seconds / max(t_rep, 1e-7))))
+    reps = int(ranks_max([float(reps)], dist)[0])
 
     gpu_id = str(local)
     try:
@@ -977,39 +1107,24 @@ def main() -> None:
     sampler.start()
     time.sleep(0.5)
 
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in KERNELS] for _ in blocks]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t_host0 = time.time()
-    start = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for b, (count, _) in enumerate(blocks):
-        gs = graphs if count == M else tail
-        for ki, kind in enumerate(KERNELS):
-            gs[kind].replay()
-            marks[b][ki].record()
+    region, per = time_regions(graphs, tail, blocks, reps, flush)
     torch.cuda.synchronize()
     t_host1 = time.time()
     if dist is not None:
         dist.barrier()
     sampler.stop()
-    end = marks[-1][-1]
-    elapsed = start.elapsed_time(end) * 1e-3
     clocks = sampler.summary(t_host0, t_host1)
 
-    elapsed = ranks_max([elapsed], dist)[0]
-
-    # Per-kernel time: the intervals between consecutive marks, summed over the region.
-    per_kernel = {kind: 0.0 for kind in KERNELS}
-    prev = start
-    for b in range(len(blocks)):
-        for ki, kind in enumerate(KERNELS):
-            per_kernel[kind] += prev.elapsed_time(marks[b][ki]) * 1e-3
-            prev = marks[b][ki]
-    per_kernel = {kind: t / args.steps for kind, t in per_kernel.items()}
-    kernel_timing = (f"per kernel: summed time of its {M}-launch graphs over the timed "
-                     f"region / K")
+    # The median repeat, then the slowest rank.
+    elapsed = statistics.median(region)
+    per_kernel = {kind: statistics.median(per[kind]) / args.steps for kind in KERNELS}
+    maxed = ranks_max([elapsed] + [per_kernel[k] for k in KERNELS], dist)
+    elapsed = maxed[0]
+    per_kernel = dict(zip(KERNELS, maxed[1:]))
 
     value = job_value(STEP_BYTES, args.steps, world, elapsed)
     kernels = []
@@ -1032,57 +1147,59 @@ def main() -> None:
     dom = max(kernels, key=lambda k: k["us"])
     roofline = {"bound": "hbm", "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
                 "frac": dom["GB/s"] / peak, "traffic": recorded_traffic(dom["kernel"]),
-                "kernel": dom["kernel"], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6800 GB/s"}
+                "kernel": dom["kernel"],
+                "peak_source": "of measured (hbm_gbs)" if peak_kind == "measured"
+                else "of fallback (6800 GB/s)"}
 
     # End to end through the C ABI with host buffers (pinned), copies inside the timing.
     e2e = end_to_end(sets, args.e2e_steps, world, dist)
 
     calibration = copy_calibration(sets, M, 50, peak)
+    del sets, graphs, tail, flush
+    torch.cuda.empty_cache()
 
     large = sweep = None
     if rank == 0 and not args.no_large:
-        cpu_cases = rank == 0 and world == 1 and not args.no_cpu
+        cpu_cases = world == 1 and not args.no_cpu
         large = large_configs(peak, args.large_reps, cpu=cpu_cases)
         sweep = large_configs(peak, args.large_reps, sweep_cases(), cpu=cpu_cases)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(_host_step_inputs(sets[0]), args.cpu_seconds)
+        s0 = InputSet(0, "cuda")
+        cpu = cpu_baseline(_host_step_inputs(s0), args.cpu_seconds)
+        del s0
 
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank != 0:
         return
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "step_bytes": STEP_BYTES,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": f"inputs larger than L2: {R} rotating input sets, "
-                         f"{R * STEP_BYTES / 1e6:.0f} MB > 4 x {l2 / 2**20:.0f} MiB L2",
-                   "timing": f"blocks of {M} steps, one CUDA graph per operator per block; "
-                             f"{kernel_timing}",
-                   "pct_of_peak": 100.0 * value / world / peak},
-        "roofline": roofline,
-        "kernels": kernels,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": len(KERNELS) * args.steps,
+    detail = {
+        "metric": METRIC, "value": value, "unit": UNIT, "steps": args.steps,
+        "repeats": reps, "region_seconds": region,
+        "input_sets": R, "l2_bytes": l2,
+        "timing": (f"{reps} repeats of the {args.steps}-step region, L2 flushed between "
+                   f"repeats; per repeat, blocks of {M} steps, one CUDA graph per operator per "
+                   f"block, an event after each graph; per kernel: its summed graph time in "
+                   f"the median repeat / K"),
+        "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks,
         "calibration": {"plain_copy_same_bytes": calibration,
                         "note": "device-to-device copies of each operator's bytes in the same "
                                 "graph and rotation harness (outside the timed region): the "
                                 "launch, ramp and drain cost any kernel of this size pays"},
+        "large_configs": large, "sweep": sweep,
     }
-    if large is not None:
-        line["large_configs"] = large
-    if sweep is not None:
-        line["sweep"] = sweep
-    print(json.dumps(line), flush=True)
+    path = write_detail(args.detail, detail) if args.detail else None
+    for group in (large or []) + (sweep or []):
+        log(f"  {group['config']:<70s} {group['kernel']:<44s} {group['us']:9.2f} us "
+            f"{group['GB/s']:8.1f} GB/s {group['frac']:.3f} cold={group['l2_cold']}")
+    line = build_line(value=value, world=world, steps=args.steps, warmup=args.warmup,
+                      ms_per_step=elapsed / args.steps * 1e3, reps=reps, M=M, kernels=kernels,
+                      roofline=roofline, cpu=cpu, e2e=e2e, clocks=clocks, peak=peak,
+                      detail_path=path)
+    print(line_text(line), flush=True)
 
 
 if __name__ == "__main__":
