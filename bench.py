@@ -10,16 +10,17 @@ the weight and the tables included).
 
 Timing. Inputs are drawn on the device before timing. Each step uses one of R input sets
 (R * step bytes > 4 x L2), so nothing a step reads is still in L2 from its last use. The
-timed region runs exactly K steps as blocks of M steps: per block, one CUDA graph of M
-back-to-back RMSNorm launches (input sets 0, 1, ... mod R), then one of M Q+K RoPE
-launches (the two operators of a step are independent, so a block runs all of its steps'
-work). A CUDA event after each graph gives every kernel's time over
-the whole timed region without timing events between individual launches (an event pair
-around a 5 us kernel adds several microseconds). Start and end events bracket the region
-on the launching stream, with a barrier and a device synchronize on both sides.
-``value`` is the step bytes x K x ranks / the slowest rank's time; a kernel's average
-launch duration is its summed graph time / K. nvidia-smi samples the SM clock and the
-throttle reasons during the timed region.
+timed region runs exactly K steps as blocks of up to 1024 steps: per block, one CUDA graph
+with an event node, the block's M back-to-back RMSNorm launches (input sets 0, 1, ... mod
+R), an event node, its M Q+K RoPE launches and a last event node (the two operators of a
+step are independent, so a block runs all of its steps' work). The event nodes give every
+kernel's time without events between individual launches (an event pair around a 5 us
+kernel adds several microseconds). The region is timed again and again, with L2 flushed
+by a read of twice its size before each repeat, for at least --repeats repeats and about --min-seconds of GPU time,
+with a barrier and a device synchronize before and after; ``value`` is the step bytes x K x
+ranks / the slowest rank's median region time, and a kernel's launch duration its summed
+time in the median repeat / K. nvidia-smi samples the SM clock and the throttle reasons
+during the repeats.
 
 ``e2e`` is the same metric through the C ABI with host buffers: every step copies its
 inputs (one packed slab) from pinned host memory, runs the two kernels and copies the
@@ -81,7 +82,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 # How the timed region keeps HBM cold; one statement for both arms so their configs match.
 L2_POLICY = ("inputs larger than L2: rotating input sets of more than 4 x L2 in total, "
-             "and an L2 flush (a write larger than L2) between timed repeats")
+             "and between timed repeats a read of a buffer of 2 x L2, which evicts what the "
+             "last repeat left in L2")
 # Both arms print this config: N independent replicas of the workload (one per rank).
 STEP_CONFIG = {"workload": WORKLOAD, "parallelism": "replicas", "step_bytes": STEP_BYTES,
                "l2": L2_POLICY}
@@ -268,18 +270,6 @@ def launch(kind: str, s: InputSet, stream: int) -> None:
 def launch_step(s: InputSet, stream: int) -> None:
     for kind in KERNELS:
         launch(kind, s, stream)
-
-
-def capture_kernel(sets, kind: str, first: int, count: int):
-    """A CUDA graph of `count` back-to-back launches of one operator on input sets
-    first, first+1, ... (mod R)."""
-    g = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream()
-    with torch.cuda.graph(g, stream=cap):
-        h = torch.cuda.current_stream().cuda_stream
-        for i in range(count):
-            launch(kind, sets[(first + i) % len(sets)], h)
-    return g
 
 
 def copy_calibration(sets, M: int, blocks: int, peak: float) -> dict:
@@ -963,45 +953,95 @@ def write_detail(path: str, detail: dict) -> str | None:
 # ------------------------------------------------------------------ the timed region
 
 def make_flush(l2: int) -> torch.Tensor:
-    """A buffer of twice the L2 size; writing it evicts whatever a region left in L2."""
-    return torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    """A buffer of twice the L2 size; reading it (flush_l2) evicts whatever a region left in
+    L2. A read, not a write: a write would leave L2 full of dirty lines, whose write-back
+    would then land inside the next timed region (about 126 MB of extra traffic, 8% of a
+    20-step region)."""
+    return torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
 
 
-def time_regions(graphs: dict, tail: dict | None, blocks: list, reps: int,
-                 flush: torch.Tensor) -> tuple[list[float], dict[str, list[float]]]:
-    """`reps` repeats of the K-step region. Before each, L2 is flushed (outside the
-    events); each repeat records a start event, then per block one graph per operator with
-    an event after each. Returns per repeat the region's seconds and per operator its
-    summed graph seconds."""
-    M = blocks[0][0]
-    rec = []
-    for _ in range(reps):
-        flush.fill_(1.0)
-        start = torch.cuda.Event(enable_timing=True)
-        start.record()
-        marks = []
-        for count, _ in blocks:
-            gs = graphs if count == M else tail
-            row = []
-            for kind in KERNELS:
-                gs[kind].replay()
-                ev = torch.cuda.Event(enable_timing=True)
-                ev.record()
-                row.append(ev)
-            marks.append(row)
-        rec.append((start, marks))
-    torch.cuda.synchronize()
+def flush_l2(buf: torch.Tensor) -> None:
+    torch.sum(buf)
+
+
+def timing_event() -> torch.cuda.Event:
+    """A timing event that, recorded during graph capture, becomes an event node of the
+    graph (torch's `external` events); a plain timing event where torch lacks them."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
+def external_events_supported() -> bool:
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+class RegionBlock:
+    """`count` consecutive steps (first, first + 1, ... on input sets mod R) as one CUDA
+    graph: an event node, the steps' RMSNorm launches back to back, an event node, their
+    Q+K RoPE launches, an event node. The two operators of a step are independent, so a
+    block runs all of its steps' work; consecutive launches of an operator overlap through
+    programmatic dependent launch. Without graph event nodes (older torch), the events are
+    recorded between per-operator graphs instead."""
+
+    def __init__(self, sets, first: int, count: int, in_graph: bool):
+        self.in_graph = in_graph
+        self.ev = [timing_event() for _ in range(len(KERNELS) + 1)]
+        self.graphs = []
+        cap = torch.cuda.Stream()
+        parts = [KERNELS] if in_graph else [(k,) for k in KERNELS]
+        for part in parts:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                h = torch.cuda.current_stream().cuda_stream
+                if in_graph:
+                    self.ev[0].record()
+                for ki, kind in enumerate(part):
+                    for i in range(count):
+                        launch(kind, sets[(first + i) % len(sets)], h)
+                    if in_graph:
+                        self.ev[ki + 1].record()
+            self.graphs.append(g)
+
+    def replay(self) -> None:
+        if self.in_graph:
+            self.graphs[0].replay()
+            return
+        self.ev[0].record()
+        for ki, g in enumerate(self.graphs):
+            g.replay()
+            self.ev[ki + 1].record()
+
+    def times(self) -> list[float]:
+        """Seconds of each operator's part in the last replay (after a synchronize)."""
+        return [self.ev[i].elapsed_time(self.ev[i + 1]) * 1e-3 for i in range(len(KERNELS))]
+
+
+def time_regions(blocks: list, reps: int, flush: torch.Tensor
+                 ) -> tuple[list[float], dict[str, list[float]]]:
+    """`reps` repeats of the K-step region (its blocks in order). Before each repeat L2 is
+    flushed by a read, outside the events; after it the device is synchronized and the
+    events read.
+    Returns per repeat the region's seconds (first block's first event to the last block's
+    last) and per operator the summed seconds of its parts."""
     region, per = [], {kind: [] for kind in KERNELS}
-    for start, marks in rec:
-        region.append(start.elapsed_time(marks[-1][-1]) * 1e-3)
-        acc = {kind: 0.0 for kind in KERNELS}
-        prev = start
-        for row in marks:
-            for kind, ev in zip(KERNELS, row):
-                acc[kind] += prev.elapsed_time(ev) * 1e-3
-                prev = ev
-        for kind in KERNELS:
-            per[kind].append(acc[kind])
+    for _ in range(reps):
+        flush_l2(flush)
+        for blk in blocks:
+            blk.replay()
+        torch.cuda.synchronize()
+        region.append(blocks[0].ev[0].elapsed_time(blocks[-1].ev[-1]) * 1e-3)
+        acc = [0.0] * len(KERNELS)
+        for blk in blocks:
+            for i, t in enumerate(blk.times()):
+                acc[i] += t
+        for kind, t in zip(KERNELS, acc):
+            per[kind].append(t)
     return region, per
 
 
@@ -1018,7 +1058,7 @@ def main() -> None:
                     help="repeat the region until about this much GPU time (clock samples)")
     ap.add_argument("--impl", choices=("camp", "reference"), default="camp")
     ap.add_argument("--graph-steps", type=int, default=0,
-                    help="steps per captured graph (0: a whole number of input rotations near 64)")
+                    help="steps per captured graph (0: up to 1024)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
@@ -1084,16 +1124,13 @@ def main() -> None:
         launch_step(sets[i % R], stream)
     torch.cuda.synchronize()
 
-    M = args.graph_steps or R * max(1, round(64 / R))
-    M = min(M, args.steps)
-    n_full, rest = divmod(args.steps, M)
-    blocks = [(M, 0)] * n_full + ([(rest, n_full * M)] if rest else [])
-    graphs = {kind: capture_kernel(sets, kind, 0, M) for kind in KERNELS}
-    tail = ({kind: capture_kernel(sets, kind, n_full * M, rest) for kind in KERNELS}
-            if rest else None)
+    M = min(args.graph_steps or 1024, args.steps)
+    in_graph = external_events_supported()
+    blocks = [RegionBlock(sets, s0, min(M, args.steps - s0), in_graph)
+              for s0 in range(0, args.steps, M)]
     # Upload the graphs and size the repeats (untimed): at least --repeats, and enough for
     # about --min-seconds of GPU time so that the clock sampler sees the load.
-    probe, _ = time_regions(graphs, tail, blocks, 3, flush)
+    probe, _ = time_regions(blocks, 3, flush)
     t_rep = statistics.median(probe) + 2 * l2 / (peak * 1e9)
     reps = max(args.repeats, min(100000, math.ceil(args.min_seconds / max(t_rep, 1e-7))))
     reps = int(ranks_max([float(reps)], dist)[0])
@@ -1111,7 +1148,7 @@ def main() -> None:
         dist.barrier()
     torch.cuda.synchronize()
     t_host0 = time.time()
-    region, per = time_regions(graphs, tail, blocks, reps, flush)
+    region, per = time_regions(blocks, reps, flush)
     torch.cuda.synchronize()
     t_host1 = time.time()
     if dist is not None:
@@ -1154,8 +1191,8 @@ def main() -> None:
     # End to end through the C ABI with host buffers (pinned), copies inside the timing.
     e2e = end_to_end(sets, args.e2e_steps, world, dist)
 
-    calibration = copy_calibration(sets, M, 50, peak)
-    del sets, graphs, tail, flush
+    calibration = copy_calibration(sets, min(M, 64), 50, peak)
+    del sets, blocks, flush
     torch.cuda.empty_cache()
 
     large = sweep = None
@@ -1179,10 +1216,13 @@ def main() -> None:
         "metric": METRIC, "value": value, "unit": UNIT, "steps": args.steps,
         "repeats": reps, "region_seconds": region,
         "input_sets": R, "l2_bytes": l2,
-        "timing": (f"{reps} repeats of the {args.steps}-step region, L2 flushed between "
-                   f"repeats; per repeat, blocks of {M} steps, one CUDA graph per operator per "
-                   f"block, an event after each graph; per kernel: its summed graph time in "
-                   f"the median repeat / K"),
+        "timing": (f"{reps} repeats of the {args.steps}-step region, L2 flushed by a read "
+                   f"before each; "
+                   f"blocks of up to {M} steps, each "
+                   + ("one CUDA graph with event nodes before, between and after the "
+                      "operators' launch runs" if in_graph else
+                      "one CUDA graph per operator with events between them")
+                   + "; per kernel: its summed time in the median repeat / K"),
         "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks,
         "calibration": {"plain_copy_same_bytes": calibration,
