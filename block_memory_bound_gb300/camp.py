@@ -43,6 +43,7 @@ KERNEL_LAYERNORM_ROWS = 9
 KERNEL_KV_CAT = 10
 KERNEL_RMSNORM_STAGED = 11
 KERNEL_LAYERNORM_STAGED = 12
+KERNEL_LAYERNORM_WIDE = 13
 
 DEVICE_ERROR_WAIT_TIMEOUT = 1
 
@@ -58,7 +59,7 @@ EXPORTS = (
     "camp_rope_tables",
     "camp_layernorm", "camp_layernorm_plan", "camp_layernorm_with_plan",
     "camp_kv_cat_repeat", "camp_kv_cat_repeat_plan", "camp_kv_cat_repeat_with_plan",
-    "camp_device_errors",
+    "camp_device_errors", "camp_layernorm_wait_probe",
 )
 
 
@@ -83,6 +84,7 @@ class Plan(ctypes.Structure):
         ("block", ctypes.c_int32),
         ("cluster", ctypes.c_int32),
         ("grid", ctypes.c_int64),
+        ("rows_per_step", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -119,6 +121,9 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_last_cuda_error.restype = c_int
         lib.camp_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), c_int]
         lib.camp_device_errors.restype = c_int
+        lib.camp_layernorm_wait_probe.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int,
+                                                  ctypes.c_uint64, vp]
+        lib.camp_layernorm_wait_probe.restype = c_int
         lib.camp_rmsnorm_plan.argtypes = [vp, vp, vp, i64, i64, c_int, pplan]
         lib.camp_rmsnorm_plan.restype = c_int
         lib.camp_rope_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, pplan]
@@ -335,6 +340,15 @@ def camp_layernorm(x, gamma, beta, y, rows: int, cols: int, eps: float, dtype, s
     _check("camp_layernorm", load().camp_layernorm(
         _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), int(rows), int(cols), float(eps),
         _dtype(dtype), _stream(stream)))
+
+
+def camp_layernorm_wait_probe(x, gamma, beta, y, rows: int, cols: int, eps: float, dtype,
+                              wait_ns: int, stream=None) -> None:
+    """The staged LayerNorm with every wait bounded by `wait_ns` and each CTA's first row
+    copy left unissued (a diagnostic of the bounded waits; see include/camp.h)."""
+    _check("camp_layernorm_wait_probe", load().camp_layernorm_wait_probe(
+        _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), int(rows), int(cols), float(eps),
+        _dtype(dtype), int(wait_ns), _stream(stream)))
 
 
 def camp_layernorm_plan(x, gamma, beta, y, rows: int, cols: int, dtype) -> Plan:

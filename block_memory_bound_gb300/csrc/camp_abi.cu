@@ -1116,21 +1116,27 @@ camp_status_t ln_validate(const void* x, const void* gamma, const void* beta, co
     return CAMP_SUCCESS;
 }
 
-// Staged LayerNorm: chunk vectors per CTA and whether the ring fits shared memory.
-bool ln_staged_fits(int64_t nvec, int cluster, int stages, int64_t* chunk) {
+// Staged LayerNorm: chunk vectors per CTA and whether gamma, beta and the ring fit shared
+// memory, for `rps` rows a step (chunks of at most 8 vectors a thread with one row a step,
+// 4 with two).
+bool ln_staged_fits(int64_t nvec, int cluster, int stages, int rps, int64_t* chunk) {
     if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1)) != 0) return false;
-    if (stages < 2 || stages > camp::kStagedMaxStages) return false;
+    if (rps < 1 || rps > camp::kLnStagedMaxRowsPerStep) return false;
+    if (stages < rps || stages < 2 || stages > camp::kStagedMaxStages) return false;
     *chunk = ceil_div(nvec, cluster);
-    return *chunk <= static_cast<int64_t>(camp::kStagedMaxVecsPerThread) * camp::kStagedBlock &&
+    const int64_t max_chunk =
+        static_cast<int64_t>(camp::kStagedMaxVecsPerThread / rps) * camp::kStagedBlock;
+    return *chunk <= max_chunk &&
            camp::ln_staged_smem_bytes(*chunk, stages) <= camp::kStagedSmemMax;
 }
 
-void ln_staged_plan_fields(const LnCall& c, int cluster, int stages, int64_t chunk,
+void ln_staged_plan_fields(const LnCall& c, int cluster, int stages, int rps, int64_t chunk,
                            camp_plan_t* p) {
     p->kernel = CAMP_KERNEL_LAYERNORM_STAGED;
     p->vec_bytes = 16;
     p->group = static_cast<int32_t>(chunk);
     p->per_thread = stages;
+    p->rows_per_step = rps;
     p->block = camp::kStagedBlock;
     p->cluster = cluster;
     const int64_t per_sm = camp::kSmSmemBytes / (camp::ln_staged_smem_bytes(chunk, stages) + 1024);
@@ -1141,37 +1147,63 @@ void ln_staged_plan_fields(const LnCall& c, int cluster, int stages, int64_t chu
 }
 
 // Rows of more than kLnStagedFrom 16-byte vectors, and rows of more than kLnStagedFewFrom
-// vectors when there are at most kLnFewRows of them, take the staged kernel with the
-// smallest power-of-two cluster whose CTA chunks hold at most kLnStagedChunk vectors (8 a
-// thread) and 2 buffers. Measured on GB300 (bf16, L2-cold, graphs of back-to-back
-// launches, each CTA's first inputs prefetched into L2 before the dependent-launch wait),
-// fraction of the measured HBM peak, register kernel against staged: 4096 x 16384 0.89 /
-// 0.75, 2048 x 24576 0.77 / 0.65, 2048 x 32768 0.78 / 0.72, but 1024 x 32768 0.63 / 0.67 (a
-// few waves of 512-thread CTAs); 1024 x 65536 (8192 vectors) 0.57 / 0.64. Past 8192 vectors
-// only the staged kernel holds the row. Chunk size, with gamma and beta read through L1
-// (shared memory then holds only the ring): 2048-vector chunks against 1024 at 1024 x
-// 65536 0.64 / 0.58, 2048 x 65536 0.69 / 0.65, 256 x 131072 0.59 / 0.47, 512 x 131072
-// 0.65 / 0.53, 64 x 262144 0.46 (16 CTAs of 2048, the most that fit) where gamma and beta
-// in shared memory gave 0.64, 0.65, 0.54, 0.56 and 0.37 at their best cluster; a third
-// buffer costs more occupancy than it hides (1024 x 65536: 0.44).
+// vectors when there are at most kLnFewRows of them, take the staged kernel. In fp32 storage,
+// where a cluster of at most kLnPairsMaxCluster CTAs gives chunks of at most kLnStagedChunk2
+// vectors (4 a thread), it takes two rows a step with 2 buffers; otherwise (and always in
+// 16-bit storage) one row a step, 2 buffers, and the smallest power-of-two cluster whose
+// chunks hold at most kLnStagedChunk vectors (8 a thread). Measured on GB300 (L2-cold, graphs
+// of back-to-back launches, of the measured HBM peak), fp32, two rows a step against the
+// one-row rule: 1024 x 32768 0.745 / 0.661, 2048 x 32768 0.794 / 0.729, 512 x 32768 0.682 /
+// 0.646, 1024 x 16384 0.754 / 0.709; with a cluster of 16 it loses (256 x 65536: 0.621 /
+// 0.645), and in 16-bit storage it loses everywhere measured (bf16 1024 x 65536: 0.58 /
+// 0.63 at its best cluster). The one-row rule with 2048-vector chunks is the measured best
+// of every cluster and buffer count at bf16 1024 x 65536 (0.63), 2048 x 65536 (0.70),
+// 256 x 131072 (0.59), 512 x 131072 (0.64), 64 x 262144 (0.50), 1024 x 32768 (0.63), 2048
+// x 32768 (0.77), 2048 x 16384 (0.83), fp16 1024 x 65536 (0.65) or within 0.02 of it.
 constexpr int64_t kLnStagedFrom = 4096;
 constexpr int64_t kLnStagedFewFrom = 2048;
 constexpr int64_t kLnFewRows = 1024;
 constexpr int64_t kLnStagedChunk = 2048;
+constexpr int64_t kLnStagedChunk2 = 1024;
+constexpr int kLnPairsMaxCluster = 8;
 
-bool ln_choose_staged(int64_t nvec, int* cluster, int64_t* chunk) {
-    for (int cl = 1; cl <= 16; cl *= 2) {
-        if (ceil_div(nvec, cl) <= kLnStagedChunk && ln_staged_fits(nvec, cl, 2, chunk)) {
+bool ln_choose_staged(int64_t nvec, int es, int* cluster, int* stages, int* rps,
+                      int64_t* chunk) {
+    for (int cl = 1; cl <= kLnPairsMaxCluster && es == 4; cl *= 2) {
+        if (ceil_div(nvec, cl) <= kLnStagedChunk2 && ln_staged_fits(nvec, cl, 2, 2, chunk)) {
             *cluster = cl;
+            *stages = 2;
+            *rps = 2;
+            return true;
+        }
+    }
+    for (int cl = 1; cl <= 16; cl *= 2) {
+        if (ceil_div(nvec, cl) <= kLnStagedChunk && ln_staged_fits(nvec, cl, 2, 1, chunk)) {
+            *cluster = cl;
+            *stages = 2;
+            *rps = 1;
             return true;
         }
     }
     return false;
 }
 
+// The wide kernel: one CTA of kWideBlock threads per row (at most kMaxGrid CTAs, each then
+// taking every grid-th row).
+void ln_wide_plan_fields(const LnCall& c, int vec_bytes, camp_plan_t* p) {
+    p->kernel = CAMP_KERNEL_LAYERNORM_WIDE;
+    p->vec_bytes = vec_bytes;
+    p->group = camp::kWideBlock;
+    p->per_thread = 0;
+    p->block = camp::kWideBlock;
+    p->cluster = 1;
+    p->grid = c.rc.a.rows < kMaxGrid ? c.rc.a.rows : kMaxGrid;
+}
+
 camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p) {
     if (forced && forced->kernel != CAMP_KERNEL_LAYERNORM_ROWS &&
-        forced->kernel != CAMP_KERNEL_LAYERNORM_STAGED)
+        forced->kernel != CAMP_KERNEL_LAYERNORM_STAGED &&
+        forced->kernel != CAMP_KERNEL_LAYERNORM_WIDE)
         return CAMP_ERR_NOT_SUPPORTED;
     const RmsCall& rc = c.rc;
     const int es = camp::elem_bytes(rc.t);
@@ -1180,11 +1212,20 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
     p->kernel = CAMP_KERNEL_LAYERNORM_ROWS;
     p->cluster = 1;
     const int64_t nvec16 = rc.a.cols * es / 16;
+    if (forced && forced->kernel == CAMP_KERNEL_LAYERNORM_WIDE) {
+        const int vb = forced->vec_bytes;
+        if ((vb != 16 && vb != es) || vb > widest || !camp::layernorm_wide_compiled(rc.t, vb))
+            return CAMP_ERR_NOT_SUPPORTED;
+        ln_wide_plan_fields(c, vb, p);
+        return CAMP_SUCCESS;
+    }
     if (forced && forced->kernel == CAMP_KERNEL_LAYERNORM_STAGED) {
         int64_t chunk = 0;
-        if (widest != 16 || !ln_staged_fits(nvec16, forced->cluster, forced->per_thread, &chunk))
+        const int rps = forced->rows_per_step == 0 ? 1 : forced->rows_per_step;
+        if (widest != 16 ||
+            !ln_staged_fits(nvec16, forced->cluster, forced->per_thread, rps, &chunk))
             return CAMP_ERR_NOT_SUPPORTED;
-        ln_staged_plan_fields(c, forced->cluster, forced->per_thread, chunk, p);
+        ln_staged_plan_fields(c, forced->cluster, forced->per_thread, rps, chunk, p);
         return CAMP_SUCCESS;
     }
     if (forced) {
@@ -1200,16 +1241,19 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
     } else {
         if (widest == 16 && (nvec16 > kLnStagedFrom ||
                              (nvec16 > kLnStagedFewFrom && rc.a.rows <= kLnFewRows))) {
-            int cl = 0;
+            int cl = 0, st = 0, rps = 0;
             int64_t chunk = 0;
-            if (ln_choose_staged(nvec16, &cl, &chunk)) {
-                ln_staged_plan_fields(c, cl, 2, chunk, p);
+            if (ln_choose_staged(nvec16, es, &cl, &st, &rps, &chunk)) {
+                ln_staged_plan_fields(c, cl, st, rps, chunk, p);
                 return CAMP_SUCCESS;
             }
         }
         p->vec_bytes = widest;
         int g = 0, nv = 0;
-        if (!rms_choose_rows(rc, widest, &g, &nv, true)) return CAMP_ERR_NOT_SUPPORTED;
+        if (!rms_choose_rows(rc, widest, &g, &nv, true)) {
+            ln_wide_plan_fields(c, widest, p);   // no register or staged kernel holds the row
+            return CAMP_SUCCESS;
+        }
         p->group = g;
         p->per_thread = nv;
     }
@@ -1502,8 +1546,12 @@ CAMP_API camp_status_t camp_layernorm_with_plan(const void* x, const void* gamma
     if (st != CAMP_SUCCESS) return st;
     const camp::LayernormArgs a{x, gamma, c.beta, y, rows, cols, eps};
     if (p.kernel == CAMP_KERNEL_LAYERNORM_STAGED)
-        return runtime_status(camp::layernorm_staged_launch(c.rc.t, p.cluster, p.per_thread, a,
+        return runtime_status(camp::layernorm_staged_launch(c.rc.t, p.cluster, p.per_thread,
+                                                            p.rows_per_step, a,
                                                             static_cast<cudaStream_t>(stream)));
+    if (p.kernel == CAMP_KERNEL_LAYERNORM_WIDE)
+        return runtime_status(camp::layernorm_wide_launch(c.rc.t, p.vec_bytes, a, p.grid,
+                                                          static_cast<cudaStream_t>(stream)));
     return runtime_status(camp::layernorm_rows_launch(c.rc.t, p.vec_bytes, p.group,
                                                       p.per_thread, a, p.grid,
                                                       static_cast<cudaStream_t>(stream)));
@@ -1513,6 +1561,27 @@ CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const vo
                                       void* y, int64_t rows, int64_t cols, float eps,
                                       camp_dtype_t dtype, void* stream) {
     return camp_layernorm_with_plan(x, gamma, beta, y, rows, cols, eps, dtype, nullptr, stream);
+}
+
+CAMP_API camp_status_t camp_layernorm_wait_probe(const void* x, const void* gamma,
+                                                 const void* beta, void* y, int64_t rows,
+                                                 int64_t cols, float eps, camp_dtype_t dtype,
+                                                 uint64_t wait_ns, void* stream) {
+    LnCall c;
+    bool empty = false;
+    camp_status_t st = ln_validate(x, gamma, beta, y, rows, cols, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (!eps_ok(eps) || wait_ns < 1000 || wait_ns > 1000000000ull) return CAMP_ERR_INVALID_ARG;
+    if (empty) return CAMP_SUCCESS;
+    camp_plan_t p;
+    st = ln_plan(c, nullptr, &p);
+    if (st != CAMP_SUCCESS) return st;
+    if (p.kernel != CAMP_KERNEL_LAYERNORM_STAGED) return CAMP_ERR_NOT_SUPPORTED;
+    const camp::LayernormArgs a{x, gamma, c.beta, y, rows, cols, eps};
+    return runtime_status(camp::layernorm_staged_launch(c.rc.t, p.cluster, p.per_thread,
+                                                        p.rows_per_step, a,
+                                                        static_cast<cudaStream_t>(stream),
+                                                        wait_ns, 1));
 }
 
 CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* cos, void* y,

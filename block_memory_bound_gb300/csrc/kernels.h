@@ -186,12 +186,34 @@ cudaError_t layernorm_rows_launch(DType t, int vec_bytes, int group, int per_thr
 
 // Staged LayerNorm (layernorm_staged.cu): the staged RMSNorm kernel's persistent clusters,
 // each row buffer carrying the row's first 16 bytes (the shift) ahead of the CTA's chunk;
-// gamma and beta are read through L1.
-inline int64_t ln_staged_smem_bytes(int64_t chunk_vecs, int stages) {
-    return stages * (16 + chunk_vecs * 16);
+// the CTA's chunks of gamma and beta are staged in shared memory too where that leaves
+// three CTAs an SM (ln_staged_gamma_in_smem), else read through L1. A step takes
+// `rows_per_step` (1 or 2) rows at once: one pair of block reductions and one cluster
+// exchange for all of them. Chunks of at most kStagedMaxVecsPerThread * kStagedBlock
+// vectors with one row a step, half that with two; `stages` >= rows_per_step buffers.
+inline int64_t ln_staged_smem_bytes(int64_t chunk_vecs, int stages, bool gamma_in_smem) {
+    return stages * (16 + chunk_vecs * 16) + (gamma_in_smem ? chunk_vecs * 32 : 0);
 }
-cudaError_t layernorm_staged_launch(DType t, int cluster, int stages, const LayernormArgs& a,
-                                    cudaStream_t s);
+constexpr int64_t kLnGammaSmemMax = 75 * 1024;   // 3 CTAs an SM, with the static part
+inline bool ln_staged_gamma_in_smem(int64_t chunk_vecs, int stages) {
+    return chunk_vecs <= 4 * 256 && ln_staged_smem_bytes(chunk_vecs, stages, true) <= kLnGammaSmemMax;
+}
+inline int64_t ln_staged_smem_bytes(int64_t chunk_vecs, int stages) {
+    return ln_staged_smem_bytes(chunk_vecs, stages, ln_staged_gamma_in_smem(chunk_vecs, stages));
+}
+constexpr int kLnStagedMaxRowsPerStep = 2;
+// `wait_ns` bounds every mbarrier wait (kLnWaitNs in normal calls); `probe` != 0 leaves
+// every CTA's first row copy unissued (a diagnostic of the bounded waits, see camp.h).
+constexpr unsigned long long kLnWaitNs = 1000000000ull;
+cudaError_t layernorm_staged_launch(DType t, int cluster, int stages, int rows_per_step,
+                                    const LayernormArgs& a, cudaStream_t s,
+                                    unsigned long long wait_ns = kLnWaitNs, int probe = 0);
+
+// Wide LayerNorm (layernorm_wide.cu): rows no other LayerNorm kernel holds, any width; one
+// CTA of kWideBlock threads per row, block-stride sweeps over x (16-byte or element accesses).
+bool layernorm_wide_compiled(DType t, int vec_bytes);
+cudaError_t layernorm_wide_launch(DType t, int vec_bytes, const LayernormArgs& a, int64_t grid,
+                                  cudaStream_t s);
 
 // ------------------------------------------------------------------ interleaved RoPE
 // x [tokens, heads, dim], pairs (2i, 2i+1); table row positions[token] of [max_pos, dim/2].

@@ -47,12 +47,32 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase of `bar` with this parity to complete; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// As mbar_test, but the thread may be suspended in hardware for up to `hint_ns` while the
+// phase is incomplete (it resumes as soon as the phase completes): a waiting warp then
+// takes no issue slots from the warps that have work.
+__device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity,
+                                                  uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 20000;   // per try; the bound below is the real limit
+
+// Wait for the phase of `bar` with this parity to complete; false after `limit_ns`
+// nanoseconds (kWaitLimitNs in normal calls).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    while (!mbar_test(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+    while (!mbar_test_suspend(bar, parity, kSuspendHintNs)) {
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

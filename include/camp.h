@@ -300,6 +300,26 @@ CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const vo
 #define CAMP_DEVICE_ERROR_WAIT_TIMEOUT 1u
 CAMP_API camp_status_t camp_device_errors(uint32_t* flags, int clear);
 
+/*
+ * Diagnostic of the bounded waits (the pages have no counterpart; it exists so that the
+ * failure path of the staged kernels can be exercised without faulting anything). Runs the
+ * staged LayerNorm kernel on these arguments with every mbarrier wait bounded by `wait_ns`
+ * nanoseconds instead of one second, and with the bulk copy of each CTA's first row left
+ * unissued (its barrier still expects the bytes), so every CTA's first wait runs out. Each
+ * CTA then sets CAMP_DEVICE_ERROR_WAIT_TIMEOUT in the device error word, stores nothing into
+ * y, keeps exchanging its (zero) partials so that no peer waits for it, waits (bounded
+ * again) for the copies it did issue, and returns: y is left untouched and the next call
+ * runs normally. Arguments, validation and errors as camp_layernorm; in addition
+ * CAMP_ERR_INVALID_ARG if wait_ns is outside [1000, 1000000000], and
+ * CAMP_ERR_NOT_SUPPORTED unless these arguments take the staged kernel (16-byte-aligned
+ * pointers and rows of more than 4096 16-byte vectors, or 2048 with at most 1024 rows).
+ * Each CTA spends about two times wait_ns.
+ */
+CAMP_API camp_status_t camp_layernorm_wait_probe(const void* x, const void* gamma,
+                                                 const void* beta, void* y, int64_t rows,
+                                                 int64_t cols, float eps, camp_dtype_t dtype,
+                                                 uint64_t wait_ns, void* stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 CAMP_API const char* camp_status_string(camp_status_t status);
 
@@ -329,7 +349,9 @@ typedef enum {
     CAMP_KERNEL_KV_CAT = 10,        /* camp_kv_cat_repeat: tiled like CAMP_KERNEL_ROPE */
     CAMP_KERNEL_RMSNORM_STAGED = 11, /* persistent clusters, rows staged in shared memory by
                                         bulk asynchronous copies, `per_thread` buffers deep */
-    CAMP_KERNEL_LAYERNORM_STAGED = 12 /* camp_layernorm: the same, for the widest rows */
+    CAMP_KERNEL_LAYERNORM_STAGED = 12, /* camp_layernorm: the same, for the widest rows */
+    CAMP_KERNEL_LAYERNORM_WIDE = 13 /* camp_layernorm: one CTA per row, block-stride sweeps
+                                       over x, for rows no other kernel holds (any width) */
 } camp_kernel_t;
 
 typedef struct {
@@ -343,6 +365,8 @@ typedef struct {
     int32_t block;         /* threads per CTA */
     int32_t cluster;       /* CTAs per cluster (RMSNorm cluster kernel: 2..16), else 1 */
     int64_t grid;          /* CTAs launched */
+    int32_t rows_per_step; /* staged LayerNorm: rows one step takes (1 or 2; 0 on input means
+                              1); other kernels: 0 */
 } camp_plan_t;
 
 /*

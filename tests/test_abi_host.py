@@ -601,19 +601,24 @@ def test_layernorm_keeps_the_smaller_group_past_1024_vectors(lib):
         assert (q.kernel, q.group, q.per_thread) == (camp.KERNEL_RMSNORM_ROWS,) + rms
 
 
-@pytest.mark.parametrize("rows,cols,dtype,cluster,chunk", [
-    (5, 65536, "bf16", 4, 2048), (7, 32768, "f32", 4, 2048), (64, 262144, "bf16", 16, 2048),
-    (3, 40000, "bf16", 4, 1250), (2, 131080, "bf16", 16, 1025),
-    (4, 32768, "bf16", 2, 2048),        # 4096 vectors, few rows
-    (1024, 24576, "bf16", 2, 1536),     # 3072 vectors, few rows
+@pytest.mark.parametrize("rows,cols,dtype,cluster,chunk,rps", [
+    (5, 65536, "bf16", 4, 2048, 1), (64, 262144, "bf16", 16, 2048, 1),
+    (3, 40000, "bf16", 4, 1250, 1), (2, 131080, "bf16", 16, 1025, 1),
+    (4, 32768, "bf16", 2, 2048, 1),        # 4096 vectors, few rows
+    (1024, 24576, "bf16", 2, 1536, 1),     # 3072 vectors, few rows
+    (1024, 65536, "f16", 4, 2048, 1),
+    (7, 32768, "f32", 8, 1024, 2),         # fp32: two rows a step with chunks of 1024
+    (1024, 16384, "f32", 4, 1024, 2),
+    (256, 65536, "f32", 8, 2048, 1),       # ... but not with a cluster of 16
 ])
-def test_layernorm_stages_rows_past_4096_vectors(lib, rows, cols, dtype, cluster, chunk):
+def test_layernorm_stages_rows_past_4096_vectors(lib, rows, cols, dtype, cluster, chunk, rps):
     # past 4096 vectors (2048 with at most 1024 rows) LayerNorm stages the row in shared
-    # memory with the smallest cluster whose CTA chunks hold at most 2048 vectors, 2 buffers
-    # (each carries the row's first 16 bytes; gamma and beta are read through L1)
+    # memory, 2 buffers (each carries the row's first 16 bytes): in fp32 two rows a step with
+    # chunks of at most 1024 vectors where a cluster of at most 8 gives them, otherwise one
+    # row a step with the smallest cluster whose CTA chunks hold at most 2048 vectors
     p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
-    assert (p.kernel, p.vec_bytes, p.cluster, p.group, p.block, p.per_thread) == \
-        (camp.KERNEL_LAYERNORM_STAGED, 16, cluster, chunk, 256, 2)
+    assert (p.kernel, p.vec_bytes, p.cluster, p.group, p.block, p.per_thread,
+            p.rows_per_step) == (camp.KERNEL_LAYERNORM_STAGED, 16, cluster, chunk, 256, 2, rps)
 
 
 def test_layernorm_staged_and_rows_thresholds(lib):
@@ -663,14 +668,28 @@ def test_layernorm_one_wave_test_uses_its_own_occupancy(lib):
     assert (q.group, q.per_thread, q.grid) == (64, 4, 1024)
 
 
-def test_layernorm_rows_that_do_not_fit_are_refused(lib):
+def test_layernorm_rows_past_the_staged_kernel_take_the_wide_kernel(lib):
     # the staged kernel holds up to 16 x 2048 sixteen-byte vectors (262144 bf16 / 131072
-    # fp32 elements); the element path holds 1024 x 16 elements
-    for cols, dtype, b in ((262152, "bf16", BETA), (131076, "f32", BETA), (16385, "bf16", BETA + 2)):
-        with pytest.raises(camp.CampError):
-            camp.camp_layernorm_plan(X, W, b, Y, 4, cols, dtype)
-    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 65544, "bf16")   # staged now
+    # fp32 elements) and the element path of the rows kernel 1024 x 16 elements; wider rows
+    # take the wide kernel (one CTA of 1024 threads per row), any width
+    for cols, dtype, b, vb in ((262152, "bf16", BETA, 16), (131076, "f32", BETA, 16),
+                               (16385, "bf16", BETA + 2, 2), (300001, "bf16", BETA, 2),
+                               (524296, "f16", BETA, 16), (10**7 + 3, "f32", BETA, 4)):
+        p = camp.camp_layernorm_plan(X, W, b, Y, 5, cols, dtype)
+        assert (p.kernel, p.vec_bytes, p.block, p.grid) == \
+            (camp.KERNEL_LAYERNORM_WIDE, vb, 1024, 5), (cols, dtype)
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 65544, "bf16")   # staged
     assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
+
+
+def test_layernorm_forced_wide_plans_that_do_not_fit_are_refused(lib):
+    # the wide kernel takes 16-byte or element accesses, never wider than the pointers allow
+    # (only refusals here: an accepted plan would launch)
+    for vb, b in ((16, BETA + 2), (8, BETA), (4, BETA)):
+        plan = camp.Plan(kernel=camp.KERNEL_LAYERNORM_WIDE, vec_bytes=vb)
+        st = lib.camp_layernorm_with_plan(X, W, b, Y, 2, 4096, ctypes.c_float(1e-5), camp.BF16,
+                                          ctypes.byref(plan), None)
+        assert st == camp.ERR_NOT_SUPPORTED, (vb, b)
 
 
 def test_layernorm_misaligned_beta_uses_element_accesses(lib):

@@ -1,0 +1,66 @@
+"""The failure path of the staged kernels' bounded waits, exercised without faulting
+anything: camp_layernorm_wait_probe runs the staged LayerNorm with every mbarrier wait
+bounded by a short limit and each CTA's first row copy left unissued, so every CTA's first
+wait runs out. The kernel must return (the call completes), set the timeout bit in the
+device error word, store nothing, and leave the library usable: the bit reads back once and
+clears, and the next normal call is clean and correct."""
+
+from __future__ import annotations
+
+import pytest
+import torch
+
+from block_memory_bound_gb300 import camp
+
+import test_layernorm_gpu as ln_tests
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    camp.load()
+    torch.cuda.set_device(0)
+    camp.camp_device_errors(clear=True)
+
+
+@pytest.mark.parametrize("dtype,rows,cols", [("bf16", 6, 65536), ("f32", 5, 40000),
+                                             ("f16", 40, 131072)])
+def test_a_wait_that_runs_out_sets_the_bit_and_stores_nothing(dtype, rows, cols):
+    x = torch.randn(rows, cols, device="cuda").to(ln_tests.inputs.STORAGE[dtype])
+    g = torch.ones(cols, device="cuda", dtype=x.dtype)
+    b = torch.zeros(cols, device="cuda", dtype=x.dtype)
+    assert camp.camp_layernorm_plan(x, g, b, x, rows, cols, dtype).kernel == \
+        camp.KERNEL_LAYERNORM_STAGED
+    yflat, buf = ln_tests._guarded(rows * cols, x.dtype)
+    bits = torch.int16 if buf.element_size() == 2 else torch.int32   # the canary is a NaN
+    before = buf.view(bits).clone()
+    assert camp.camp_device_errors(clear=True) == 0
+    camp.camp_layernorm_wait_probe(x, g, b, yflat, rows, cols, 1e-5, dtype, wait_ns=200_000)
+    torch.cuda.synchronize()
+    assert camp.camp_device_errors() & camp.DEVICE_ERROR_WAIT_TIMEOUT
+    assert torch.equal(buf.view(bits), before), "a CTA whose wait ran out stored output"
+    # the bit reads back until cleared, then stays clear
+    assert camp.camp_device_errors(clear=True) & camp.DEVICE_ERROR_WAIT_TIMEOUT
+    assert camp.camp_device_errors() == 0
+    # the next normal call is clean and correct
+    ln_tests.run_case(rows, cols, dtype, seed=rows)
+    assert camp.camp_device_errors() == 0
+
+
+def test_probe_argument_checks():
+    x = torch.zeros(4, 65536, device="cuda", dtype=torch.bfloat16)
+    g = torch.ones(65536, device="cuda", dtype=torch.bfloat16)
+    y = torch.empty_like(x)
+    for ns in (0, 999, 1_000_000_001):
+        with pytest.raises(camp.CampError) as ei:
+            camp.camp_layernorm_wait_probe(x, g, g, y, 4, 65536, 1e-5, "bf16", wait_ns=ns)
+        assert ei.value.status == camp.ERR_INVALID_ARG
+    small = torch.zeros(4, 2048, device="cuda", dtype=torch.bfloat16)   # the rows kernel
+    with pytest.raises(camp.CampError) as ei:
+        camp.camp_layernorm_wait_probe(small, g, g, torch.empty_like(small), 4, 2048, 1e-5,
+                                       "bf16", wait_ns=100_000)
+    assert ei.value.status == camp.ERR_NOT_SUPPORTED
+    assert camp.camp_device_errors() == 0
