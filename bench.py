@@ -109,31 +109,44 @@ def load_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest() -> str:
-    """Digest of the device code (every kernel source and header; camp_abi.cu, host-only
-    planning and argument checks, is left out: it cannot change what a kernel variant
-    moves)."""
+# The device sources each recorded kernel is built from (profiles/traffic.json): a
+# recorded DRAM figure is reported only while these files are unchanged.
+KERNEL_SOURCES = {
+    "rope_tiled": ("rope.cu", "common.cuh", "kernels.h"),
+    "rmsnorm_rows": ("rmsnorm.cu", "rmsnorm_kernels.cuh", "common.cuh", "kernels.h"),
+}
+
+
+def source_digest(names=None) -> str:
+    """Digest of device code: the named files of csrc/, or every kernel source and header
+    (camp_abi.cu, host-only planning and argument checks, left out: it cannot change what a
+    kernel variant moves)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_memory_bound_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and name != "camp_abi.cu":
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    files = sorted(names) if names else sorted(
+        n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")) and n != "camp_abi.cu")
+    for name in files:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
 def recorded_traffic(kernel_name: str):
-    """DRAM bytes per launch from the committed ncu summary, if it is for these sources."""
+    """DRAM bytes per launch from the committed ncu summary, if its kernel's sources are
+    the ones it was recorded from."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("source_sha256") != source_digest():
-        return None
     entry = rec.get("kernels", {}).get(kernel_name)
-    return None if entry is None else entry.get("dram_bytes_per_launch")
+    if entry is None:
+        return None
+    family = kernel_name.split("<")[0]
+    if entry.get("source_sha256") != source_digest(KERNEL_SOURCES.get(family)):
+        return None
+    return entry.get("dram_bytes_per_launch")
 
 
 def plan_name(kind: str, p: camp.Plan, dt: str = "bf16") -> str:
