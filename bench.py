@@ -12,10 +12,11 @@ Timing. Inputs are drawn on the device before timing. Each step uses one of R in
 (R * step bytes > 4 x L2), so nothing a step reads is still in L2 from its last use. The
 timed region runs exactly K steps as blocks of up to 1024 steps: per block, one CUDA graph
 with an event node, the block's M back-to-back RMSNorm launches (input sets 0, 1, ... mod
-R), an event node, its M Q+K RoPE launches and a last event node (the two operators of a
-step are independent, so a block runs all of its steps' work). The event nodes give every
-kernel's time without events between individual launches (an event pair around a 5 us
-kernel adds several microseconds). The region is timed again and again, with L2 flushed
+R), its M Q+K RoPE launches and a last event node (the two operators of a step are
+independent, so a block runs all of its steps' work); the event between the two runs sits
+on a side branch of the graph, so that it adds no dependency between the kernels. The event
+nodes give every kernel's time without events between individual launches (an event pair
+around a 5 us kernel adds several microseconds). The region is timed again and again, with L2 flushed
 by a read of twice its size before each repeat, for at least --repeats repeats and about --min-seconds of GPU time,
 with a barrier and a device synchronize before and after; ``value`` is the step bytes x K x
 ranks / the slowest rank's median region time, and a kernel's launch duration its summed
@@ -996,29 +997,46 @@ def external_events_supported() -> bool:
 
 class RegionBlock:
     """`count` consecutive steps (first, first + 1, ... on input sets mod R) as one CUDA
-    graph: an event node, the steps' RMSNorm launches back to back, an event node, their
-    Q+K RoPE launches, an event node. The two operators of a step are independent, so a
-    block runs all of its steps' work; consecutive launches of an operator overlap through
-    programmatic dependent launch. Without graph event nodes (older torch), the events are
-    recorded between per-operator graphs instead."""
+    graph: an event node, the steps' RMSNorm launches back to back, then their Q+K RoPE
+    launches, and an event node at the end. The two operators of a step are independent,
+    so a block runs all of its steps' work; consecutive launches overlap through
+    programmatic dependent launch, the first RoPE launch after the last RMSNorm one
+    included: the event that splits the two runs is recorded on a side branch of the graph
+    (forked after the last RMSNorm launch, joined before the end), so it times that point
+    without adding a dependency between the kernels. Without graph event nodes (older
+    torch), the events are recorded between per-operator graphs instead."""
 
     def __init__(self, sets, first: int, count: int, in_graph: bool):
         self.in_graph = in_graph
         self.ev = [timing_event() for _ in range(len(KERNELS) + 1)]
         self.graphs = []
         cap = torch.cuda.Stream()
+        # created before capture: the side stream and the fork/join events of each split
+        sides = [(torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event())
+                 for _ in KERNELS[1:]]
         parts = [KERNELS] if in_graph else [(k,) for k in KERNELS]
         for part in parts:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
-                h = torch.cuda.current_stream().cuda_stream
+                main = torch.cuda.current_stream()
+                h = main.cuda_stream
                 if in_graph:
                     self.ev[0].record()
                 for ki, kind in enumerate(part):
                     for i in range(count):
                         launch(kind, sets[(first + i) % len(sets)], h)
-                    if in_graph:
-                        self.ev[ki + 1].record()
+                    if in_graph and ki + 1 < len(part):
+                        side, fork, join = sides[ki]
+                        fork.record(main)
+                        side.wait_event(fork)
+                        with torch.cuda.stream(side):
+                            self.ev[ki + 1].record()
+                        join.record(side)
+                if in_graph:
+                    for _, _, join in sides:
+                        main.wait_event(join)
+                if in_graph:
+                    self.ev[len(part)].record()
             self.graphs.append(g)
 
     def replay(self) -> None:
@@ -1232,8 +1250,8 @@ def main() -> None:
         "timing": (f"{reps} repeats of the {args.steps}-step region, L2 flushed by a read "
                    f"before each; "
                    f"blocks of up to {M} steps, each "
-                   + ("one CUDA graph with event nodes before, between and after the "
-                      "operators' launch runs" if in_graph else
+                   + ("one CUDA graph with event nodes before and after the operators' "
+                      "launch runs and one on a side branch between them" if in_graph else
                       "one CUDA graph per operator with events between them")
                    + "; per kernel: its summed time in the median repeat / K"),
         "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
