@@ -27,13 +27,15 @@ def _device():
 
 
 @pytest.mark.parametrize("dtype,rows,cols", [("bf16", 6, 65536), ("f32", 5, 40000),
-                                             ("f16", 40, 131072)])
+                                             ("f16", 40, 131072),
+                                             ("f32", 7, 32768)])   # two rows a step
 def test_a_wait_that_runs_out_sets_the_bit_and_stores_nothing(dtype, rows, cols):
     x = torch.randn(rows, cols, device="cuda").to(ln_tests.inputs.STORAGE[dtype])
     g = torch.ones(cols, device="cuda", dtype=x.dtype)
     b = torch.zeros(cols, device="cuda", dtype=x.dtype)
-    assert camp.camp_layernorm_plan(x, g, b, x, rows, cols, dtype).kernel == \
-        camp.KERNEL_LAYERNORM_STAGED
+    p = camp.camp_layernorm_plan(x, g, b, x, rows, cols, dtype)
+    assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
+    assert p.rows_per_step == (2 if (dtype, cols) == ("f32", 32768) else 1)
     yflat, buf = ln_tests._guarded(rows * cols, x.dtype)
     bits = torch.int16 if buf.element_size() == 2 else torch.int32   # the canary is a NaN
     before = buf.view(bits).clone()
