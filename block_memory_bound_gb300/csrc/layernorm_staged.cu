@@ -163,8 +163,8 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
     griddep_launch_dependents();
 
     const char* xb = static_cast<const char*>(x);
-    auto issue = [&](int64_t j) {   // one thread: the head of row j and this CTA's chunk
-        const int s = static_cast<int>(j % stages);
+    // One thread: the head of row j and this CTA's chunk, into ring slot s (j mod stages).
+    auto issue = [&](int64_t j, int s) {
         const int64_t row = cid + j * ncl;
         const uint32_t bar = smem_u32(&full[s]);
         const uint32_t dst = smem_u32(ring + s * stage_bytes);
@@ -181,7 +181,7 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
             bulk_load(smem_u32(bsm), static_cast<const char*>(beta) + v0 * 16, my_bytes,
                       smem_u32(&gb_bar));
         }
-        for (int64_t j = 0; j < stages && j < my_rows; ++j) issue(j);
+        for (int j = 0; j < stages && j < my_rows; ++j) issue(j, j);
     }
     bool gb_ready = !GBS || my_bytes == 0;
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
@@ -198,15 +198,33 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
     int64_t nz = 0;   // second-pass exchanges so far (the same count in every CTA)
     int64_t fail_step = -1;
     int64_t i = 0;
+    // Ring slot and phase parity of the step's first row (row j0 uses slot j0 mod stages,
+    // phase (j0 / stages) mod 2), advanced without dividing.
+    int slot0 = 0;
+    uint32_t par0 = 0;
     for (int64_t j0 = 0; j0 < my_rows; j0 += RP, ++i) {
         const int set = static_cast<int>(i & 1);
+        int slot[RP];
+        uint32_t par[RP];
+#pragma unroll
+        for (int u = 0; u < RP; ++u) {
+            slot[u] = slot0 + u;
+            par[u] = par0;
+            if (slot[u] >= stages) {
+                slot[u] -= stages;
+                par[u] ^= 1u;
+            }
+        }
+        slot0 += RP;
+        if (slot0 >= stages) {
+            slot0 -= stages;
+            par0 ^= 1u;
+        }
         if (fail_step < 0) {
 #pragma unroll
             for (int u = 0; u < RP; ++u) {
-                const int64_t j = j0 + u;
-                if (j < my_rows &&
-                    !mbar_wait_bounded(smem_u32(&full[j % stages]),
-                                       static_cast<uint32_t>((j / stages) & 1), wait_ns))
+                if (j0 + u < my_rows &&
+                    !mbar_wait_bounded(smem_u32(&full[slot[u]]), par[u], wait_ns))
                     timed_out = 1;
             }
         }
@@ -219,9 +237,8 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
         Raw<16> v[RP][NVT];
 #pragma unroll
         for (int u = 0; u < RP; ++u) {
-            const int64_t j = j0 + u;
-            const unsigned char* buf = ring + (j % stages) * stage_bytes;
-            const bool on = ok && j < my_rows;
+            const unsigned char* buf = ring + slot[u] * stage_bytes;
+            const bool on = ok && j0 + u < my_rows;
             shift[u] = 0.0f;
             if (on) C::each(ld_smem16(buf), [&](int e, float f) { if (e == 0) shift[u] = f; });
 #pragma unroll
@@ -264,8 +281,8 @@ layernorm_staged_kernel(const void* x, const void* __restrict__ gamma,
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
             for (int u = 0; u < RP; ++u) {
-                const int64_t j = j0 + u + stages;
-                if (j < my_rows) issue(j);
+                const int64_t j = j0 + u + stages;   // the same slot as row j0 + u
+                if (j < my_rows) issue(j, slot[u]);
             }
         }
         // Two-pass form (fp32 storage): m_k = sum(x - K) / n_k, then M2_k = sum(((x - K) -
