@@ -815,10 +815,24 @@ def large_configs(peak: float, reps: int, cases=None, cpu: bool = False) -> list
 
 # ------------------------------------------------------------------ profiling cases
 
-def run_case(case: str, launches: int) -> None:
+def parse_plan(text: str | None):
+    """An explicit plan from `field=value,...` (the camp_plan_t fields), or None."""
+    if not text:
+        return None
+    p = camp.Plan()
+    for item in text.split(","):
+        key, _, val = item.partition("=")
+        if key not in dict(camp.Plan._fields_):
+            raise SystemExit(f"unknown plan field {key!r}")
+        setattr(p, key, int(val))
+    return p
+
+
+def run_case(case: str, launches: int, plan_text: str | None = None) -> None:
     """Launch one operator `launches` times at one shape (inputs drawn on the device),
     for profilers; prints the plan and the launch count. `case` is kind:AxBx..[:dtype]
-    (dtype bf16 when left out)."""
+    (dtype bf16 when left out); `plan_text` (rmsnorm and layernorm only) forces a plan."""
+    forced = parse_plan(plan_text)
     kind, _, rest = case.partition(":")
     shape, _, dt = rest.partition(":")
     dt = dt or "bf16"
@@ -832,9 +846,12 @@ def run_case(case: str, launches: int) -> None:
         rows, cols = dims
         x, w = inputs.rmsnorm_inputs(rows, cols, dt, seed=0, device="cuda")
         y = torch.empty_like(x)
-        plan = plan_name("rmsnorm", camp.camp_rmsnorm_plan(x, w, y, rows, cols, dt), dt)
+        plan = plan_name("rmsnorm", forced or camp.camp_rmsnorm_plan(x, w, y, rows, cols, dt), dt)
         for _ in range(launches):
-            camp.camp_rmsnorm(x, w, y, rows, cols, EPS, code, stream)
+            if forced is None:
+                camp.camp_rmsnorm(x, w, y, rows, cols, EPS, code, stream)
+            else:
+                camp.camp_rmsnorm_with_plan(x, w, y, rows, cols, EPS, code, forced, stream)
     elif kind == "add":
         rows, cols = dims
         x, w = inputs.rmsnorm_inputs(rows, cols, dt, seed=0, device="cuda")
@@ -848,9 +865,12 @@ def run_case(case: str, launches: int) -> None:
         rows, cols = dims
         x, w, bt = inputs.layernorm_inputs(rows, cols, dt, seed=0, device="cuda")
         y = torch.empty_like(x)
-        plan = plan_name("layernorm", camp.camp_layernorm_plan(x, w, bt, y, rows, cols, dt), dt)
+        plan = plan_name("layernorm", forced or camp.camp_layernorm_plan(x, w, bt, y, rows, cols, dt), dt)
         for _ in range(launches):
-            camp.camp_layernorm(x, w, bt, y, rows, cols, EPS, code, stream)
+            if forced is None:
+                camp.camp_layernorm(x, w, bt, y, rows, cols, EPS, code, stream)
+            else:
+                camp.camp_layernorm_with_plan(x, w, bt, y, rows, cols, EPS, code, forced, stream)
     elif kind == "rope_il":
         T, H, D = dims
         mp = 2 * T
@@ -1108,9 +1128,12 @@ def main() -> None:
                          "(B x P x S x Hk x D x n_rep); a third field picks the storage "
                          "type, e.g. layernorm:8192x4096:f16 (bf16 when left out)")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--plan", default=None,
+                    help="with --case rmsnorm or layernorm: an explicit plan as camp_plan_t "
+                         "fields, e.g. kernel=12,cluster=16,per_thread=2,rows_per_step=1")
     args = ap.parse_args()
     if args.case:
-        run_case(args.case, args.launches)
+        run_case(args.case, args.launches, args.plan)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
