@@ -151,10 +151,14 @@ def recorded_traffic(kernel_name: str):
 
 
 def plan_name(kind: str, p: camp.Plan, dt: str = "bf16") -> str:
+    if p.kernel in (camp.KERNEL_RMSNORM_SPREAD, camp.KERNEL_LAYERNORM_SPREAD):
+        return f"{kind}_spread<{dt},cluster{p.cluster},chunk{p.group}vec,stages{p.per_thread}>"
     if kind == "layernorm":
         if p.kernel == camp.KERNEL_LAYERNORM_STAGED:
             return (f"layernorm_staged<{dt},cluster{p.cluster},chunk{p.group}vec,"
                     f"stages{p.per_thread}>")
+        if p.kernel == camp.KERNEL_LAYERNORM_WIDE:
+            return f"layernorm_wide<{dt},vec{p.vec_bytes}>"
         return f"layernorm_rows<{dt},vec{p.vec_bytes},group{p.group},nv{p.per_thread}>"
     if kind == "rmsnorm":
         if p.kernel == camp.KERNEL_RMSNORM_STAGED:
@@ -570,8 +574,18 @@ LARGE_CASES = [
     ("layernorm fp16 [8192,4096] (the TileLang tutorial's example 2)", "ln", (8192, 4096, "f16")),
     ("layernorm bf16 [65536,2048]", "ln", (65536, 2048)),
     ("layernorm bf16 [16384,8192]", "ln", (16384, 8192)),
-    ("layernorm bf16 [1024,65536] (staged in shared memory)", "ln", (1024, 65536)),
-    ("layernorm bf16 [256,131072] (staged in shared memory)", "ln", (256, 131072)),
+    ("layernorm bf16 [1024,65536] (a cluster per row, chunks in shared memory)", "ln",
+     (1024, 65536)),
+    ("layernorm bf16 [256,131072] (a cluster per row, chunks in shared memory)", "ln",
+     (256, 131072)),
+    ("layernorm fp32 [1024,32768] (staged in shared memory, two rows a step)", "ln",
+     (1024, 32768, "f32")),
+    ("rmsnorm bf16 [1024,262152] (a cluster per row, chunks in shared memory)", "rms",
+     (1024, 262152, False, 1e-5)),
+    ("layernorm bf16 [1024,262152] (a cluster per row, chunks in shared memory)", "ln",
+     (1024, 262152)),
+    ("layernorm bf16 [512,140000] (ragged staged chunks: a cluster per row)", "ln",
+     (512, 140000)),
     ("rope bf16 [1,65536,32,128]", "rope", (65536, 32, 128)),
     ("rope fp16 [1,4096,32,128] (the TileLang tutorial's exercise E13)", "rope",
      (4096, 32, 128, "f16")),

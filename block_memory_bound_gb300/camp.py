@@ -44,6 +44,8 @@ KERNEL_KV_CAT = 10
 KERNEL_RMSNORM_STAGED = 11
 KERNEL_LAYERNORM_STAGED = 12
 KERNEL_LAYERNORM_WIDE = 13
+KERNEL_RMSNORM_SPREAD = 14
+KERNEL_LAYERNORM_SPREAD = 15
 
 DEVICE_ERROR_WAIT_TIMEOUT = 1
 
@@ -121,7 +123,7 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_last_cuda_error.restype = c_int
         lib.camp_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), c_int]
         lib.camp_device_errors.restype = c_int
-        lib.camp_layernorm_wait_probe.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int,
+        lib.camp_layernorm_wait_probe.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int, pplan,
                                                   ctypes.c_uint64, vp]
         lib.camp_layernorm_wait_probe.restype = c_int
         lib.camp_rmsnorm_plan.argtypes = [vp, vp, vp, i64, i64, c_int, pplan]
@@ -343,12 +345,14 @@ def camp_layernorm(x, gamma, beta, y, rows: int, cols: int, eps: float, dtype, s
 
 
 def camp_layernorm_wait_probe(x, gamma, beta, y, rows: int, cols: int, eps: float, dtype,
-                              wait_ns: int, stream=None) -> None:
-    """The staged LayerNorm with every wait bounded by `wait_ns` and each CTA's first row
-    copy left unissued (a diagnostic of the bounded waits; see include/camp.h)."""
+                              wait_ns: int, plan: Plan | None = None, stream=None) -> None:
+    """The staged LayerNorm (or the staged or spread kernel of `plan`) with every wait
+    bounded by `wait_ns` and each CTA's first row copy left unissued (a diagnostic of the
+    bounded waits; see include/camp.h)."""
     _check("camp_layernorm_wait_probe", load().camp_layernorm_wait_probe(
         _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), int(rows), int(cols), float(eps),
-        _dtype(dtype), int(wait_ns), _stream(stream)))
+        _dtype(dtype), None if plan is None else ctypes.byref(plan), int(wait_ns),
+        _stream(stream)))
 
 
 def camp_layernorm_plan(x, gamma, beta, y, rows: int, cols: int, dtype) -> Plan:

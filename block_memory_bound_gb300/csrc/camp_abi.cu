@@ -376,6 +376,57 @@ bool rms_choose_staged(const RmsCall& c, int64_t nvec, int* cluster, int* stages
     return true;
 }
 
+// Rows past the staged kernel (more than 16 x 2048 16-byte vectors) that still fit a
+// cluster's shared memory take the spread kernel: one buffer a CTA and the smallest
+// power-of-two cluster whose chunks hold at most spread_chunk_max vectors, else 16 CTAs
+// (rows of up to about 1.7 M bf16 columns). The limit is the chunk at which shared memory
+// (228 KB an SM, 1 KB of it reserved a CTA, and under 1 KB of static arrays) still holds
+// as many CTAs an SM as the registers allow: 3 (73 KB chunks), or 2 for fp32 LayerNorm
+// (109 KB). The plan's grid counts no more resident CTAs than that.
+constexpr int64_t spread_chunk_max(int per_sm) { return per_sm >= 3 ? 4700 : 7000; }
+
+bool spread_fits(int64_t nvec, int cluster, int stages, int64_t* chunk) {
+    if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1)) != 0) return false;
+    if (stages < 1 || stages > camp::kSpreadMaxStages) return false;
+    *chunk = ceil_div(nvec, cluster);
+    return camp::spread_smem_bytes(*chunk, stages) <= camp::kStagedSmemMax;
+}
+
+bool spread_choose(int64_t nvec, int64_t rows, int per_sm, int* cluster, int* stages,
+                   int64_t* chunk) {
+    for (int cl = 1; cl <= 16; cl *= 2) {
+        if ((ceil_div(nvec, cl) <= spread_chunk_max(per_sm) || cl == 16) &&
+            spread_fits(nvec, cl, 1, chunk)) {
+            // So few rows that their CTAs would leave half the SMs idle: split each row
+            // further (GB300, bf16: 5 x 40000 0.03 -> 0.05, fp32 3 x 131080 0.11 -> 0.14;
+            // splitting while the rows' CTAs fill fewer than all resident slots lost at
+            // 32 x 131072, 0.36 -> 0.25, and 100 x 100000, 0.51 -> 0.44).
+            while (cl < 16 && rows * cl < camp::kSmCount / 2) cl *= 2;
+            spread_fits(nvec, cl, 1, chunk);
+            *cluster = cl;
+            *stages = 1;
+            return true;
+        }
+    }
+    return false;
+}
+
+void spread_plan_fields(int64_t rows, int kernel, int per_sm_regs, int cluster, int stages,
+                        int64_t chunk, camp_plan_t* p) {
+    p->kernel = kernel;
+    p->vec_bytes = 16;
+    p->group = static_cast<int32_t>(chunk);
+    p->per_thread = stages;
+    p->block = camp::kSpreadBlock;
+    p->cluster = cluster;
+    int64_t per_sm = camp::kSmSmemBytes / (camp::spread_smem_bytes(chunk, stages) + 2048);
+    if (per_sm > per_sm_regs) per_sm = per_sm_regs;
+    int64_t clusters = (camp::kSmCount * (per_sm < 1 ? 1 : per_sm)) / cluster;
+    if (clusters < 1) clusters = 1;
+    if (clusters > rows) clusters = rows;
+    p->grid = clusters * cluster;
+}
+
 void rms_plan(const RmsCall& c, camp_plan_t* p) {
     *p = camp_plan_t{};
     p->vec_bytes = rms_vec_bytes(c);
@@ -386,6 +437,11 @@ void rms_plan(const RmsCall& c, camp_plan_t* p) {
     const int64_t cluster_from = c.add ? kClusterFrom / 2 : kClusterFrom;
     if (p->vec_bytes == 16 && nvec > kStagedFrom && rms_choose_staged(c, nvec, &cl, &st, &chunk)) {
         rms_staged_plan_fields(c, cl, st, chunk, p);
+    } else if (p->vec_bytes == 16 && !c.add && nvec > kStagedFrom &&
+               spread_choose(nvec, c.a.rows, camp::spread_ctas_per_sm(false, camp::elem_bytes(c.t)),
+                             &cl, &st, &chunk)) {
+        spread_plan_fields(c.a.rows, CAMP_KERNEL_RMSNORM_SPREAD,
+                           camp::spread_ctas_per_sm(false, camp::elem_bytes(c.t)), cl, st, chunk, p);
     } else if (p->vec_bytes == 16 && nvec > cluster_from && rms_choose_cluster(c, nvec, &cl, &nv)) {
         p->kernel = CAMP_KERNEL_RMSNORM_CLUSTER;
         p->group = cl * camp::kClusterBlock;
@@ -445,6 +501,15 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
         rms_staged_plan_fields(c, in.cluster, in.per_thread, chunk, p);
         return CAMP_SUCCESS;
     }
+    if (in.kernel == CAMP_KERNEL_RMSNORM_SPREAD) {
+        int64_t chunk = 0;
+        if (vb != 16 || c.add || !spread_fits(nvec, in.cluster, in.per_thread, &chunk))
+            return CAMP_ERR_NOT_SUPPORTED;
+        spread_plan_fields(c.a.rows, CAMP_KERNEL_RMSNORM_SPREAD,
+                           camp::spread_ctas_per_sm(false, camp::elem_bytes(c.t)), in.cluster,
+                           in.per_thread, chunk, p);
+        return CAMP_SUCCESS;
+    }
     if (in.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
         if (!camp::rmsnorm_wide_compiled(c.t, vb)) return CAMP_ERR_NOT_SUPPORTED;
         p->group = camp::kWideBlock;
@@ -467,6 +532,8 @@ camp_status_t rms_launch(const RmsCall& c, const camp_plan_t& p, cudaStream_t s)
         e = camp::rmsnorm_wide_launch(c.add, c.t, p.vec_bytes, c.a, p.grid, s);
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_STAGED) {
         e = camp::rmsnorm_staged_launch(c.add, c.t, p.cluster, p.per_thread, c.a, s);
+    } else if (p.kernel == CAMP_KERNEL_RMSNORM_SPREAD) {
+        e = camp::rmsnorm_spread_launch(c.t, p.cluster, p.per_thread, c.a, s);
     }
     return runtime_status(e);
 }
@@ -1188,6 +1255,28 @@ bool ln_choose_staged(int64_t nvec, int es, int* cluster, int* stages, int* rps,
     return false;
 }
 
+// The share of the staged kernel's per-thread vector slots a chunk fills: its launcher gives
+// each thread 1, 2, 4 or 8 vectors, the fewest that hold the chunk. Below kLnStagedMinFill
+// the spread kernel takes the row, if its own chunks hold at least kLnSpreadMinChunk
+// vectors (its per-row cost of two cluster exchanges and three sweeps over shared memory
+// pays off only over long chunks). Measured on GB300 (L2-cold, graphs of back-to-back
+// launches, of the measured HBM peak), staged against spread: bf16 512 x 140000 (chunks
+// of 1094 vectors, 8 a thread: 0.53 full) 0.45 / 0.62, 256 x 200000 (0.76) 0.54 / 0.60,
+// 2048 x 36000 (0.55) 0.58 / 0.70, 4096 x 36864 (0.56) 0.65 / 0.78, 1024 x 65544 (0.50)
+// 0.53 / 0.69, fp32 512 x 70000 (0.53) 0.54 / 0.61, 1024 x 40000 (0.61) 0.71 / 0.73; with
+// short spread chunks the staged kernel wins (bf16 1024 x 24576: 1536 of 2048 slots
+// against one CTA of 3072, 0.62 / 0.55; 1024 x 20480 0.58 / 0.51), and at full chunks it
+// mostly does (512 x 131072 0.69 / 0.65, 1024 x 32768 0.67 / 0.61, fp16 1024 x 65536 0.68 /
+// 0.67, fp32 1024 x 32768 0.85 / 0.72; bf16 1024 x 65536 0.66 / 0.72 is the exception).
+constexpr double kLnStagedMinFill = 0.8;
+constexpr int64_t kLnSpreadMinChunk = 4096;
+
+double ln_staged_fill(int64_t chunk) {
+    const int64_t need = ceil_div(chunk, camp::kStagedBlock);
+    const int64_t nvt = need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
+    return static_cast<double>(chunk) / static_cast<double>(nvt * camp::kStagedBlock);
+}
+
 // The wide kernel: one CTA of kWideBlock threads per row (at most kMaxGrid CTAs, each then
 // taking every grid-th row).
 void ln_wide_plan_fields(const LnCall& c, int vec_bytes, camp_plan_t* p) {
@@ -1200,10 +1289,29 @@ void ln_wide_plan_fields(const LnCall& c, int vec_bytes, camp_plan_t* p) {
     p->grid = c.rc.a.rows < kMaxGrid ? c.rc.a.rows : kMaxGrid;
 }
 
+// The staged kernel's plan for these arguments, whichever kernel camp_layernorm takes:
+// 16-byte pitches and pointers, rows past kLnStagedFrom vectors (kLnStagedFewFrom with at
+// most kLnFewRows rows) that a cluster of 16 holds. False if the staged kernel cannot.
+bool ln_staged_plan_for(const LnCall& c, camp_plan_t* p) {
+    const RmsCall& rc = c.rc;
+    const int es = camp::elem_bytes(rc.t);
+    if (rms_vec_bytes(rc) != 16 || !aligned(c.beta, 16)) return false;
+    const int64_t nvec16 = rc.a.cols * es / 16;
+    if (!(nvec16 > kLnStagedFrom || (nvec16 > kLnStagedFewFrom && rc.a.rows <= kLnFewRows)))
+        return false;
+    int cl = 0, st = 0, rps = 0;
+    int64_t chunk = 0;
+    if (!ln_choose_staged(nvec16, es, &cl, &st, &rps, &chunk)) return false;
+    *p = camp_plan_t{};
+    ln_staged_plan_fields(c, cl, st, rps, chunk, p);
+    return true;
+}
+
 camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p) {
     if (forced && forced->kernel != CAMP_KERNEL_LAYERNORM_ROWS &&
         forced->kernel != CAMP_KERNEL_LAYERNORM_STAGED &&
-        forced->kernel != CAMP_KERNEL_LAYERNORM_WIDE)
+        forced->kernel != CAMP_KERNEL_LAYERNORM_WIDE &&
+        forced->kernel != CAMP_KERNEL_LAYERNORM_SPREAD)
         return CAMP_ERR_NOT_SUPPORTED;
     const RmsCall& rc = c.rc;
     const int es = camp::elem_bytes(rc.t);
@@ -1212,6 +1320,15 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
     p->kernel = CAMP_KERNEL_LAYERNORM_ROWS;
     p->cluster = 1;
     const int64_t nvec16 = rc.a.cols * es / 16;
+    const int ln_per_sm = camp::spread_ctas_per_sm(true, es);
+    if (forced && forced->kernel == CAMP_KERNEL_LAYERNORM_SPREAD) {
+        int64_t chunk = 0;
+        if (widest != 16 || !spread_fits(nvec16, forced->cluster, forced->per_thread, &chunk))
+            return CAMP_ERR_NOT_SUPPORTED;
+        spread_plan_fields(rc.a.rows, CAMP_KERNEL_LAYERNORM_SPREAD, ln_per_sm, forced->cluster,
+                           forced->per_thread, chunk, p);
+        return CAMP_SUCCESS;
+    }
     if (forced && forced->kernel == CAMP_KERNEL_LAYERNORM_WIDE) {
         const int vb = forced->vec_bytes;
         if ((vb != 16 && vb != es) || vb > widest || !camp::layernorm_wide_compiled(rc.t, vb))
@@ -1243,8 +1360,27 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
                              (nvec16 > kLnStagedFewFrom && rc.a.rows <= kLnFewRows))) {
             int cl = 0, st = 0, rps = 0;
             int64_t chunk = 0;
+            if (es == 2 && spread_choose(nvec16, rc.a.rows, ln_per_sm, &cl, &st, &chunk)) {
+                spread_plan_fields(rc.a.rows, CAMP_KERNEL_LAYERNORM_SPREAD, ln_per_sm, cl, st,
+                                   chunk, p);
+                return CAMP_SUCCESS;
+            }
             if (ln_choose_staged(nvec16, es, &cl, &st, &rps, &chunk)) {
+                int scl = 0, sst = 0;
+                int64_t schunk = 0;
+                if (ln_staged_fill(chunk) < kLnStagedMinFill &&
+                    spread_choose(nvec16, rc.a.rows, ln_per_sm, &scl, &sst, &schunk) &&
+                    schunk >= kLnSpreadMinChunk) {
+                    spread_plan_fields(rc.a.rows, CAMP_KERNEL_LAYERNORM_SPREAD, ln_per_sm, scl, sst, schunk,
+                                       p);
+                    return CAMP_SUCCESS;
+                }
                 ln_staged_plan_fields(c, cl, st, rps, chunk, p);
+                return CAMP_SUCCESS;
+            }
+            if (spread_choose(nvec16, rc.a.rows, ln_per_sm, &cl, &st, &chunk)) {   // past the staged kernel
+                spread_plan_fields(rc.a.rows, CAMP_KERNEL_LAYERNORM_SPREAD, ln_per_sm, cl, st,
+                                   chunk, p);
                 return CAMP_SUCCESS;
             }
         }
@@ -1281,10 +1417,11 @@ CAMP_API int camp_last_cuda_error(void) { return g_last_cuda_error; }
 
 CAMP_API camp_status_t camp_device_errors(uint32_t* flags, int clear) {
     if (flags == nullptr) return CAMP_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, d = 0;
     camp_status_t st = runtime_status(camp::read_device_errors(&a, clear != 0));
     if (st == CAMP_SUCCESS) st = runtime_status(camp::read_layernorm_device_errors(&b, clear != 0));
-    *flags = st == CAMP_SUCCESS ? (a | b) : 0u;
+    if (st == CAMP_SUCCESS) st = runtime_status(camp::read_spread_device_errors(&d, clear != 0));
+    *flags = st == CAMP_SUCCESS ? (a | b | d) : 0u;
     return st;
 }
 
@@ -1552,6 +1689,9 @@ CAMP_API camp_status_t camp_layernorm_with_plan(const void* x, const void* gamma
     if (p.kernel == CAMP_KERNEL_LAYERNORM_WIDE)
         return runtime_status(camp::layernorm_wide_launch(c.rc.t, p.vec_bytes, a, p.grid,
                                                           static_cast<cudaStream_t>(stream)));
+    if (p.kernel == CAMP_KERNEL_LAYERNORM_SPREAD)
+        return runtime_status(camp::layernorm_spread_launch(c.rc.t, p.cluster, p.per_thread, a,
+                                                            static_cast<cudaStream_t>(stream)));
     return runtime_status(camp::layernorm_rows_launch(c.rc.t, p.vec_bytes, p.group,
                                                       p.per_thread, a, p.grid,
                                                       static_cast<cudaStream_t>(stream)));
@@ -1566,7 +1706,8 @@ CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const vo
 CAMP_API camp_status_t camp_layernorm_wait_probe(const void* x, const void* gamma,
                                                  const void* beta, void* y, int64_t rows,
                                                  int64_t cols, float eps, camp_dtype_t dtype,
-                                                 uint64_t wait_ns, void* stream) {
+                                                 const camp_plan_t* plan, uint64_t wait_ns,
+                                                 void* stream) {
     LnCall c;
     bool empty = false;
     camp_status_t st = ln_validate(x, gamma, beta, y, rows, cols, dtype, &c, &empty);
@@ -1574,14 +1715,22 @@ CAMP_API camp_status_t camp_layernorm_wait_probe(const void* x, const void* gamm
     if (!eps_ok(eps) || wait_ns < 1000 || wait_ns > 1000000000ull) return CAMP_ERR_INVALID_ARG;
     if (empty) return CAMP_SUCCESS;
     camp_plan_t p;
-    st = ln_plan(c, nullptr, &p);
-    if (st != CAMP_SUCCESS) return st;
-    if (p.kernel != CAMP_KERNEL_LAYERNORM_STAGED) return CAMP_ERR_NOT_SUPPORTED;
+    if (plan != nullptr) {
+        if (plan->kernel != CAMP_KERNEL_LAYERNORM_STAGED &&
+            plan->kernel != CAMP_KERNEL_LAYERNORM_SPREAD)
+            return CAMP_ERR_NOT_SUPPORTED;
+        st = ln_plan(c, plan, &p);
+        if (st != CAMP_SUCCESS) return st;
+    } else if (!ln_staged_plan_for(c, &p)) {
+        return CAMP_ERR_NOT_SUPPORTED;
+    }
     const camp::LayernormArgs a{x, gamma, c.beta, y, rows, cols, eps};
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.kernel == CAMP_KERNEL_LAYERNORM_SPREAD)
+        return runtime_status(
+            camp::layernorm_spread_launch(c.rc.t, p.cluster, p.per_thread, a, s, wait_ns, 1));
     return runtime_status(camp::layernorm_staged_launch(c.rc.t, p.cluster, p.per_thread,
-                                                        p.rows_per_step, a,
-                                                        static_cast<cudaStream_t>(stream),
-                                                        wait_ns, 1));
+                                                        p.rows_per_step, a, s, wait_ns, 1));
 }
 
 CAMP_API camp_status_t camp_rope(const void* x, const float* sin, const float* cos, void* y,

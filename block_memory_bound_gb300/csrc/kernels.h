@@ -129,11 +129,36 @@ inline int64_t staged_smem_bytes(bool add, int64_t chunk_vecs, int stages) {
 cudaError_t rmsnorm_staged_launch(bool add, DType t, int cluster, int stages,
                                   const RmsnormArgs& a, cudaStream_t s);
 
+// Rows past the staged kernels' registers (spread.cu): clusters of `cluster` (1..16) CTAs of
+// kSpreadBlock threads; each CTA keeps its whole chunk of ceil(nvec / cluster) 16-byte
+// vectors of a row in shared memory (`stages` buffers of it, 1..kSpreadMaxStages), so x is
+// read from HBM once. RMSNorm without the residual add, and LayerNorm; 16-byte accesses.
+constexpr int kSpreadBlock = 512;
+constexpr int kSpreadMaxStages = 3;
+// CTAs an SM the launch bounds guarantee by registers (fp32 LayerNorm keeps more live than
+// 40 registers hold without spilling); the plan's grid estimate counts no more resident
+// CTAs than this.
+constexpr int spread_ctas_per_sm(bool layernorm, int elem_bytes) {
+    return layernorm && elem_bytes == 4 ? 2 : 3;
+}
+inline int64_t spread_smem_bytes(int64_t chunk_vecs, int stages) {
+    return stages * (16 + chunk_vecs * 16);
+}
+cudaError_t rmsnorm_spread_launch(DType t, int cluster, int stages, const RmsnormArgs& a,
+                                  cudaStream_t s);
+struct LayernormArgs;
+// `wait_ns` bounds every mbarrier wait (one second in normal calls); `probe` != 0 leaves each
+// CTA's first row copy unissued (the wait diagnostic), as for layernorm_staged_launch.
+cudaError_t layernorm_spread_launch(DType t, int cluster, int stages, const LayernormArgs& a,
+                                    cudaStream_t s, unsigned long long wait_ns = 1000000000ull,
+                                    int probe = 0);
+
 // The library's device error words (one per translation unit with bounded waits): kernels
 // whose bounded waits ran out set bits in them; camp_device_errors reports their union.
 constexpr unsigned int kDeviceErrorWaitTimeout = 1u;
 cudaError_t read_device_errors(unsigned int* flags, bool clear);            // staged RMSNorm
 cudaError_t read_layernorm_device_errors(unsigned int* flags, bool clear);  // staged LayerNorm
+cudaError_t read_spread_device_errors(unsigned int* flags, bool clear);     // spread kernels
 
 // The add-path tables live in their own translation unit (compiled in parallel).
 namespace add_path {

@@ -282,9 +282,13 @@ CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos,
  * more than 4096 16-byte vectors (32768 bf16/f16 / 16384 fp32 columns), or of more than
  * 2048 when there are at most 1024 rows (all pointers and the row pitch 16-byte aligned),
  * are staged in shared memory by persistent clusters of CTAs instead (up to 16 x 2048
- * vectors: 262144 bf16/f16 / 131072 fp32 columns). Wider rows, and rows past 16384 columns
- * on the element path, return CAMP_ERR_NOT_SUPPORTED. Errors otherwise as for
- * camp_rmsnorm.
+ * vectors: 262144 bf16/f16 / 131072 fp32 columns). Wider rows (and staged rows whose
+ * chunks would leave a fifth or more of the threads' vector slots empty) are spread over a
+ * cluster of up to 16 CTAs, each holding its whole chunk in shared memory (up to about
+ * 1.7 M bf16 columns); rows wider still, and rows past 16384 columns on the element path,
+ * take one CTA per row (any width). In 16-bit storage any of these kernels may take the
+ * variance as sum((x - K)^2) / n - mu^2 (one pass) for a row where mu^2 <= 4 times that
+ * value. Errors as for camp_rmsnorm.
  */
 CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const void* beta,
                                       void* y, int64_t rows, int64_t cols, float eps,
@@ -299,26 +303,6 @@ CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const vo
  */
 #define CAMP_DEVICE_ERROR_WAIT_TIMEOUT 1u
 CAMP_API camp_status_t camp_device_errors(uint32_t* flags, int clear);
-
-/*
- * Diagnostic of the bounded waits (the pages have no counterpart; it exists so that the
- * failure path of the staged kernels can be exercised without faulting anything). Runs the
- * staged LayerNorm kernel on these arguments with every mbarrier wait bounded by `wait_ns`
- * nanoseconds instead of one second, and with the bulk copy of each CTA's first row left
- * unissued (its barrier still expects the bytes), so every CTA's first wait runs out. Each
- * CTA then sets CAMP_DEVICE_ERROR_WAIT_TIMEOUT in the device error word, stores nothing into
- * y, keeps exchanging its (zero) partials so that no peer waits for it, waits (bounded
- * again) for the copies it did issue, and returns: y is left untouched and the next call
- * runs normally. Arguments, validation and errors as camp_layernorm; in addition
- * CAMP_ERR_INVALID_ARG if wait_ns is outside [1000, 1000000000], and
- * CAMP_ERR_NOT_SUPPORTED unless these arguments take the staged kernel (16-byte-aligned
- * pointers and rows of more than 4096 16-byte vectors, or 2048 with at most 1024 rows).
- * Each CTA spends about two times wait_ns.
- */
-CAMP_API camp_status_t camp_layernorm_wait_probe(const void* x, const void* gamma,
-                                                 const void* beta, void* y, int64_t rows,
-                                                 int64_t cols, float eps, camp_dtype_t dtype,
-                                                 uint64_t wait_ns, void* stream);
 
 /* A static, human-readable name for a status code (never NULL). */
 CAMP_API const char* camp_status_string(camp_status_t status);
@@ -350,8 +334,12 @@ typedef enum {
     CAMP_KERNEL_RMSNORM_STAGED = 11, /* persistent clusters, rows staged in shared memory by
                                         bulk asynchronous copies, `per_thread` buffers deep */
     CAMP_KERNEL_LAYERNORM_STAGED = 12, /* camp_layernorm: the same, for the widest rows */
-    CAMP_KERNEL_LAYERNORM_WIDE = 13 /* camp_layernorm: one CTA per row, block-stride sweeps
-                                       over x, for rows no other kernel holds (any width) */
+    CAMP_KERNEL_LAYERNORM_WIDE = 13, /* camp_layernorm: one CTA per row, block-stride sweeps
+                                        over x, for rows no other kernel holds (any width) */
+    CAMP_KERNEL_RMSNORM_SPREAD = 14, /* camp_rmsnorm: a cluster of CTAs per row, each holding
+                                        its whole chunk in shared memory (rows past the
+                                        staged kernel) */
+    CAMP_KERNEL_LAYERNORM_SPREAD = 15 /* camp_layernorm: the same */
 } camp_kernel_t;
 
 typedef struct {
@@ -364,7 +352,11 @@ typedef struct {
                               shared-memory buffers per CTA). RoPE: unused (0) */
     int32_t block;         /* threads per CTA */
     int32_t cluster;       /* CTAs per cluster (RMSNorm cluster kernel: 2..16), else 1 */
-    int64_t grid;          /* CTAs launched */
+    int64_t grid;          /* CTAs launched. Staged and spread kernels (persistent
+                              clusters): the planner's estimate from shared memory and
+                              registers per SM; the launch takes the clusters the device
+                              holds at once (cudaOccupancyMaxActiveClusters), at most one a
+                              row */
     int32_t rows_per_step; /* staged LayerNorm: rows one step takes (1 or 2; 0 on input means
                               1); other kernels: 0 */
 } camp_plan_t;
@@ -482,6 +474,30 @@ CAMP_API camp_status_t camp_layernorm_with_plan(const void* x, const void* gamma
                                                 const void* beta, void* y, int64_t rows,
                                                 int64_t cols, float eps, camp_dtype_t dtype,
                                                 const camp_plan_t* plan, void* stream);
+
+/*
+ * Diagnostic of the bounded waits (the pages have no counterpart; it exists so that the
+ * failure path of the staged and spread kernels can be exercised without faulting
+ * anything). Runs the staged LayerNorm kernel (plan == NULL: the staged plan for these
+ * arguments, whichever kernel camp_layernorm would take) or the kernel of `plan` (staged
+ * or spread, checked as camp_layernorm_with_plan checks it) on these arguments, with every
+ * mbarrier wait bounded by `wait_ns` nanoseconds instead of one second and with the bulk
+ * copy of each CTA's first row left unissued (its barrier still expects the bytes), so
+ * every CTA's first wait runs out. Each CTA then sets CAMP_DEVICE_ERROR_WAIT_TIMEOUT in the
+ * device error word, stores nothing into y, keeps exchanging its (zero) partials so that
+ * no peer waits for it, waits (bounded again) for the copies it did issue, and returns: y
+ * is left untouched and the next call runs normally. Arguments, validation and errors as
+ * camp_layernorm; in addition CAMP_ERR_INVALID_ARG if wait_ns is outside
+ * [1000, 1000000000], and CAMP_ERR_NOT_SUPPORTED for a plan of another kernel or one that
+ * does not hold the row, or, with plan == NULL, unless the staged kernel holds the row
+ * (16-byte-aligned pointers and rows of more than 4096 16-byte vectors, or 2048 with at
+ * most 1024 rows, up to 16 x 2048). Each CTA spends about two times wait_ns.
+ */
+CAMP_API camp_status_t camp_layernorm_wait_probe(const void* x, const void* gamma,
+                                                 const void* beta, void* y, int64_t rows,
+                                                 int64_t cols, float eps, camp_dtype_t dtype,
+                                                 const camp_plan_t* plan, uint64_t wait_ns,
+                                                 void* stream);
 
 #ifdef __cplusplus
 }

@@ -158,9 +158,17 @@ def test_rope_empty_is_success_without_cuda(lib):
     (256, 131072, "bf16", (camp.KERNEL_RMSNORM_STAGED, 16, 1024, 2, 256, 608, 16)),
     (2, 262144, "bf16", (camp.KERNEL_RMSNORM_STAGED, 16, 2048, 2, 256, 32, 16)),
     (7, 32768, "f32", (camp.KERNEL_RMSNORM_STAGED, 16, 1024, 3, 256, 56, 8)),
-    # past 16 x 2048 vectors: two sweeps over the row in one CTA
-    (3, 131080, "f32", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 3, 1)),
-    (2, 262152, "bf16", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 2, 1)),
+    # past 16 x 2048 vectors: a cluster of CTAs of 512 threads per row, each CTA's chunk
+    # held in shared memory, one buffer, the smallest cluster whose chunks hold at most 4700
+    # vectors (else 16), doubled while the rows' CTAs number under 76; grid = the clusters
+    # that fit (3 CTAs an SM at most), at most one per row, x the cluster
+    (3, 131080, "f32", (camp.KERNEL_RMSNORM_SPREAD, 16, 2049, 1, 512, 48, 16)),   # 8 x 3 < 76
+    (2, 262152, "bf16", (camp.KERNEL_RMSNORM_SPREAD, 16, 2049, 1, 512, 32, 16)),
+    (512, 300000, "bf16", (camp.KERNEL_RMSNORM_SPREAD, 16, 4688, 1, 512, 456, 8)),
+    (64, 524296, "bf16", (camp.KERNEL_RMSNORM_SPREAD, 16, 4097, 1, 512, 448, 16)),
+    (40, 1600000, "bf16", (camp.KERNEL_RMSNORM_SPREAD, 16, 12500, 1, 512, 144, 16)),
+    # past what a cluster's shared memory holds, or element accesses: two sweeps in one CTA
+    (3, 2000000, "bf16", (camp.KERNEL_RMSNORM_WIDE, 16, 1024, 0, 1024, 3, 1)),
     (5, 16385, "f32", (camp.KERNEL_RMSNORM_WIDE, 4, 1024, 0, 1024, 5, 1)),
 ])
 def test_rmsnorm_plans(lib, rows, cols, dtype, expect):
@@ -602,23 +610,61 @@ def test_layernorm_keeps_the_smaller_group_past_1024_vectors(lib):
 
 
 @pytest.mark.parametrize("rows,cols,dtype,cluster,chunk,rps", [
-    (5, 65536, "bf16", 4, 2048, 1), (64, 262144, "bf16", 16, 2048, 1),
-    (3, 40000, "bf16", 4, 1250, 1), (2, 131080, "bf16", 16, 1025, 1),
-    (4, 32768, "bf16", 2, 2048, 1),        # 4096 vectors, few rows
-    (1024, 24576, "bf16", 2, 1536, 1),     # 3072 vectors, few rows
-    (1024, 65536, "f16", 4, 2048, 1),
-    (7, 32768, "f32", 8, 1024, 2),         # fp32: two rows a step with chunks of 1024
+    (7, 32768, "f32", 8, 1024, 2),         # two rows a step with chunks of 1024
     (1024, 16384, "f32", 4, 1024, 2),
+    (4, 32768, "f32", 8, 1024, 2),
     (256, 65536, "f32", 8, 2048, 1),       # ... but not with a cluster of 16
+    (1024, 12288, "f32", 4, 768, 2),       # 0.75 full, but one spread CTA would hold 3072
+    (4, 32776, "f32", 8, 1025, 1),         # 0.50 full, but 4 rows split spread chunks to 513
 ])
-def test_layernorm_stages_rows_past_4096_vectors(lib, rows, cols, dtype, cluster, chunk, rps):
-    # past 4096 vectors (2048 with at most 1024 rows) LayerNorm stages the row in shared
-    # memory, 2 buffers (each carries the row's first 16 bytes): in fp32 two rows a step with
-    # chunks of at most 1024 vectors where a cluster of at most 8 gives them, otherwise one
-    # row a step with the smallest cluster whose CTA chunks hold at most 2048 vectors
+def test_fp32_layernorm_stages_rows_past_4096_vectors(lib, rows, cols, dtype, cluster, chunk,
+                                                      rps):
+    # fp32 rows past 4096 vectors (2048 with at most 1024 rows) are staged in shared memory,
+    # 2 buffers (each carries the row's first 16 bytes): two rows a step with chunks of at
+    # most 1024 vectors where a cluster of at most 8 gives them, otherwise one row a step
+    # with the smallest cluster whose CTA chunks hold at most 2048 vectors
     p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
     assert (p.kernel, p.vec_bytes, p.cluster, p.group, p.block, p.per_thread,
             p.rows_per_step) == (camp.KERNEL_LAYERNORM_STAGED, 16, cluster, chunk, 256, 2, rps)
+
+
+@pytest.mark.parametrize("rows,cols,dtype,cluster,chunk,grid", [
+    (64, 262144, "bf16", 8, 4096, 456),    # 3 CTAs an SM: 57 clusters of 8
+    (1024, 65536, "f16", 2, 4096, 456),
+    (1024, 30720, "bf16", 1, 3840, 456),   # few rows, 3840 vectors
+    (1024, 24576, "bf16", 1, 3072, 456),
+    (512, 140000, "bf16", 4, 4375, 456),
+    (256, 200000, "bf16", 8, 3125, 456),   # 4 CTAs would hold 6250
+    (5, 65536, "bf16", 16, 512, 80),       # 5 rows x 2 CTAs: split to 16 a row
+    (4, 32768, "bf16", 16, 256, 64),
+])
+def test_16bit_layernorm_spreads_rows_past_4096_vectors(lib, rows, cols, dtype, cluster,
+                                                        chunk, grid):
+    # in 16-bit storage the same rows take the spread kernel: one buffer, the smallest
+    # cluster whose chunks hold at most 4700 vectors, doubled while the rows' CTAs number
+    # under 76; grid = 3 CTAs an SM at most, one cluster a row at most
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, dtype)
+    assert (p.kernel, p.vec_bytes, p.cluster, p.group, p.block, p.per_thread, p.grid) == \
+        (camp.KERNEL_LAYERNORM_SPREAD, 16, cluster, chunk, 512, 1, grid)
+
+
+@pytest.mark.parametrize("rows,cols,staged_chunk,cluster,chunk,grid", [
+    (512, 70000, 1094, 4, 4375, 304),      # 1094 vectors in 8 x 256 slots: 0.53 full
+    (1024, 40000, 1250, 2, 5000, 304),     # 0.61 full
+    (512, 32776, 1025, 2, 4097, 304),      # 0.50 full
+])
+def test_fp32_layernorm_ragged_staged_chunks_take_the_spread_kernel(lib, rows, cols,
+                                                                    staged_chunk, cluster,
+                                                                    chunk, grid):
+    # where the staged kernel's chunk fills under 0.8 of its threads' 1, 2, 4 or 8 vector
+    # slots, the spread kernel takes the row: one buffer, the smallest cluster whose chunks
+    # hold at most 7000 vectors (2 CTAs an SM in fp32), if they hold at least 4096
+    need = -(-staged_chunk // 256)
+    slots = 256 * next(n for n in (1, 2, 4, 8) if n >= need)
+    assert staged_chunk / slots < 0.8
+    p = camp.camp_layernorm_plan(X, W, BETA, Y, rows, cols, "f32")
+    assert (p.kernel, p.vec_bytes, p.cluster, p.group, p.block, p.per_thread, p.grid) == \
+        (camp.KERNEL_LAYERNORM_SPREAD, 16, cluster, chunk, 512, 1, grid)
 
 
 def test_layernorm_staged_and_rows_thresholds(lib):
@@ -668,18 +714,26 @@ def test_layernorm_one_wave_test_uses_its_own_occupancy(lib):
     assert (q.group, q.per_thread, q.grid) == (64, 4, 1024)
 
 
-def test_layernorm_rows_past_the_staged_kernel_take_the_wide_kernel(lib):
+def test_layernorm_rows_past_the_staged_kernel(lib):
     # the staged kernel holds up to 16 x 2048 sixteen-byte vectors (262144 bf16 / 131072
     # fp32 elements) and the element path of the rows kernel 1024 x 16 elements; wider rows
-    # take the wide kernel (one CTA of 1024 threads per row), any width
-    for cols, dtype, b, vb in ((262152, "bf16", BETA, 16), (131076, "f32", BETA, 16),
-                               (16385, "bf16", BETA + 2, 2), (300001, "bf16", BETA, 2),
-                               (524296, "f16", BETA, 16), (10**7 + 3, "f32", BETA, 4)):
+    # with 16-byte pitches take the spread kernel (16 CTAs of 512 threads, each CTA's chunk in
+    # shared memory) while a chunk fits, everything else the wide kernel (one CTA of 1024
+    # threads per row), any width
+    for cols, dtype, b, kernel, vb, block in (
+            (262152, "bf16", BETA, camp.KERNEL_LAYERNORM_SPREAD, 16, 512),
+            (131076, "f32", BETA, camp.KERNEL_LAYERNORM_SPREAD, 16, 512),
+            (524296, "f16", BETA, camp.KERNEL_LAYERNORM_SPREAD, 16, 512),
+            (16385, "bf16", BETA + 2, camp.KERNEL_LAYERNORM_WIDE, 2, 1024),
+            (300001, "bf16", BETA, camp.KERNEL_LAYERNORM_WIDE, 2, 1024),
+            (2000000, "bf16", BETA, camp.KERNEL_LAYERNORM_WIDE, 16, 1024),
+            (10**7 + 3, "f32", BETA, camp.KERNEL_LAYERNORM_WIDE, 4, 1024)):
         p = camp.camp_layernorm_plan(X, W, b, Y, 5, cols, dtype)
-        assert (p.kernel, p.vec_bytes, p.block, p.grid) == \
-            (camp.KERNEL_LAYERNORM_WIDE, vb, 1024, 5), (cols, dtype)
-    p = camp.camp_layernorm_plan(X, W, BETA, Y, 4, 65544, "bf16")   # staged
-    assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
+        assert (p.kernel, p.vec_bytes, p.block) == (kernel, vb, block), (cols, dtype)
+        if kernel == camp.KERNEL_LAYERNORM_WIDE:
+            assert (p.grid, p.cluster) == (5, 1)
+        else:   # one buffer; 5 rows of 8 CTAs are split to 16 CTAs a row
+            assert (p.per_thread, p.cluster, p.grid) == (1, 16, 80)
 
 
 def test_layernorm_forced_wide_plans_that_do_not_fit_are_refused(lib):
@@ -901,3 +955,23 @@ def test_f16_dtype_names(lib):
     import torch
     for name in ("f16", "fp16", "float16", torch.float16, camp.F16):
         assert camp._dtype(name) == camp.F16 == 0
+
+
+def test_wait_probe_refusals_launch_nothing(lib):
+    # argument checks and plan refusals return before any launch (no device needed)
+    plan_t = camp.Plan
+    f = lib.camp_layernorm_wait_probe
+    eps = ctypes.c_float(1e-5)
+    for ns in (0, 999, 1_000_000_001):
+        assert f(X, W, BETA, Y, 4, 65536, eps, camp.BF16, None, ns, None) == camp.ERR_INVALID_ARG
+    # the rows kernel's width: no staged plan
+    assert f(X, W, BETA, Y, 4, 2048, eps, camp.BF16, None, 100_000, None) == \
+        camp.ERR_NOT_SUPPORTED
+    for plan in (plan_t(kernel=camp.KERNEL_LAYERNORM_ROWS, vec_bytes=16, group=512, per_thread=8),
+                 plan_t(kernel=camp.KERNEL_LAYERNORM_WIDE, vec_bytes=16),
+                 plan_t(kernel=camp.KERNEL_LAYERNORM_STAGED, vec_bytes=16, cluster=1, per_thread=2),
+                 plan_t(kernel=camp.KERNEL_LAYERNORM_SPREAD, vec_bytes=16, cluster=3, per_thread=1),
+                 plan_t(kernel=camp.KERNEL_RMSNORM_SPREAD, vec_bytes=16, cluster=2, per_thread=1)):
+        assert f(X, W, BETA, Y, 4, 65536, eps, camp.BF16, ctypes.byref(plan), 100_000, None) == \
+            camp.ERR_NOT_SUPPORTED, plan
+    assert f(X, W, BETA, Y, 0, 65536, eps, camp.BF16, None, 100_000, None) == camp.SUCCESS

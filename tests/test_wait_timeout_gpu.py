@@ -1,7 +1,7 @@
-"""The failure path of the staged kernels' bounded waits, exercised without faulting
-anything: camp_layernorm_wait_probe runs the staged LayerNorm with every mbarrier wait
-bounded by a short limit and each CTA's first row copy left unissued, so every CTA's first
-wait runs out. The kernel must return (the call completes), set the timeout bit in the
+"""The failure path of the staged and spread kernels' bounded waits, exercised without
+faulting anything: camp_layernorm_wait_probe runs the staged or spread LayerNorm with every
+mbarrier wait bounded by a short limit and each CTA's first row copy left unissued, so every
+CTA's first wait runs out. The kernel must return (the call completes), set the timeout bit in the
 device error word, store nothing, and leave the library usable: the bit reads back once and
 clears, and the next normal call is clean and correct."""
 
@@ -26,21 +26,37 @@ def _device():
     camp.camp_device_errors(clear=True)
 
 
-@pytest.mark.parametrize("dtype,rows,cols", [("bf16", 6, 65536), ("f32", 5, 40000),
-                                             ("f16", 40, 131072),
-                                             ("f32", 7, 32768)])   # two rows a step
-def test_a_wait_that_runs_out_sets_the_bit_and_stores_nothing(dtype, rows, cols):
+def staged(cluster, rows_per_step=1):
+    return camp.Plan(kernel=camp.KERNEL_LAYERNORM_STAGED, vec_bytes=16, cluster=cluster,
+                     per_thread=2, rows_per_step=rows_per_step)
+
+
+def spread(cluster, stages=1):
+    return camp.Plan(kernel=camp.KERNEL_LAYERNORM_SPREAD, vec_bytes=16, cluster=cluster,
+                     per_thread=stages)
+
+
+@pytest.mark.parametrize("dtype,rows,cols,plan", [
+    ("bf16", 6, 65536, None),            # the staged plan for these arguments
+    ("bf16", 6, 65536, staged(4)),
+    ("f32", 5, 65536, staged(8)),
+    ("f16", 40, 131072, staged(8)),
+    ("f32", 7, 32768, staged(8, 2)),     # two rows a step
+    ("bf16", 6, 65536, spread(2)),
+    ("f16", 40, 131072, spread(4)),
+    ("f32", 5, 300000, spread(16)),      # the second pass and its exchange on every row
+    ("bf16", 400, 40000, spread(1, 2)),  # 2-3 rows a CTA: the second buffer's copy lands
+])
+def test_a_wait_that_runs_out_sets_the_bit_and_stores_nothing(dtype, rows, cols, plan):
     x = torch.randn(rows, cols, device="cuda").to(ln_tests.inputs.STORAGE[dtype])
     g = torch.ones(cols, device="cuda", dtype=x.dtype)
     b = torch.zeros(cols, device="cuda", dtype=x.dtype)
-    p = camp.camp_layernorm_plan(x, g, b, x, rows, cols, dtype)
-    assert p.kernel == camp.KERNEL_LAYERNORM_STAGED
-    assert p.rows_per_step == (2 if (dtype, cols) == ("f32", 32768) else 1)
     yflat, buf = ln_tests._guarded(rows * cols, x.dtype)
     bits = torch.int16 if buf.element_size() == 2 else torch.int32   # the canary is a NaN
     before = buf.view(bits).clone()
     assert camp.camp_device_errors(clear=True) == 0
-    camp.camp_layernorm_wait_probe(x, g, b, yflat, rows, cols, 1e-5, dtype, wait_ns=200_000)
+    camp.camp_layernorm_wait_probe(x, g, b, yflat, rows, cols, 1e-5, dtype, wait_ns=200_000,
+                                   plan=plan)
     torch.cuda.synchronize()
     assert camp.camp_device_errors() & camp.DEVICE_ERROR_WAIT_TIMEOUT
     assert torch.equal(buf.view(bits), before), "a CTA whose wait ran out stored output"
@@ -65,4 +81,13 @@ def test_probe_argument_checks():
         camp.camp_layernorm_wait_probe(small, g, g, torch.empty_like(small), 4, 2048, 1e-5,
                                        "bf16", wait_ns=100_000)
     assert ei.value.status == camp.ERR_NOT_SUPPORTED
+    for plan in (camp.Plan(kernel=camp.KERNEL_LAYERNORM_ROWS, vec_bytes=16, group=512,
+                           per_thread=8),          # a kernel without bounded waits
+                 camp.Plan(kernel=camp.KERNEL_LAYERNORM_WIDE, vec_bytes=16),
+                 staged(1),                        # 8192 vectors do not fit one CTA
+                 spread(3)):                       # not a power of two
+        with pytest.raises(camp.CampError) as ei:
+            camp.camp_layernorm_wait_probe(x, g, g, y, 4, 65536, 1e-5, "bf16", wait_ns=100_000,
+                                           plan=plan)
+        assert ei.value.status == camp.ERR_NOT_SUPPORTED
     assert camp.camp_device_errors() == 0
