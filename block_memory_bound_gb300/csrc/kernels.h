@@ -135,6 +135,7 @@ cudaError_t rmsnorm_staged_launch(bool add, DType t, int cluster, int stages,
 // read from HBM once. RMSNorm without the residual add, and LayerNorm; 16-byte accesses.
 constexpr int kSpreadBlock = 512;
 constexpr int kSpreadMaxStages = 3;
+constexpr int kSpreadHeadBytes = 16 * (kSpreadBlock / 32);   // a row head copy a copy group
 // CTAs an SM the launch bounds guarantee by registers (fp32 LayerNorm keeps more live than
 // 40 registers hold without spilling); the plan's grid estimate counts no more resident
 // CTAs than this.
@@ -142,7 +143,7 @@ constexpr int spread_ctas_per_sm(bool layernorm, int elem_bytes) {
     return layernorm && elem_bytes == 4 ? 2 : 3;
 }
 inline int64_t spread_smem_bytes(int64_t chunk_vecs, int stages) {
-    return stages * (16 + chunk_vecs * 16);
+    return stages * (kSpreadHeadBytes + chunk_vecs * 16);
 }
 cudaError_t rmsnorm_spread_launch(DType t, int cluster, int stages, const RmsnormArgs& a,
                                   cudaStream_t s);

@@ -12,9 +12,11 @@
 // half that with two, so x is still read from HBM once for rows of up to about 1.7 M bf16
 // columns. (LayerNorm rows that the staged kernel would hold in ragged chunks, filling
 // little of its threads' vector slots, come here too.) Per row:
-//   1. the CTA's chunk lands in a ring buffer by one bulk asynchronous copy (with the row's
-//      first 16 bytes, for the LayerNorm shift);
-//   2. every thread sums over its vectors of the buffer (vectors t, t + 512, ...), in kAcc
+//   1. each copy group (a warp, or the whole CTA for 16-bit LayerNorm) owns a contiguous
+//      segment of the CTA's chunk, which lands in a ring buffer by the group's own bulk
+//      asynchronous copy on its own mbarrier (with a copy of the row's first 16 bytes, for
+//      the LayerNorm shift);
+//   2. every thread sums over its vectors of the segment (one every group-size vectors), in kAcc
 //      independent packed accumulators: sum(x^2) for RMSNorm; sum(x - K) and, in 16-bit
 //      storage, sum((x - K)^2) for LayerNorm; one block reduction;
 //   3. the CTA's sums go to every CTA of the cluster by st.async (counted on the receiver's
@@ -23,9 +25,10 @@
 //   4. LayerNorm rows whose shift lies more than two standard deviations from the mean
 //      (the rows kernel's rule; every row in fp32 storage) take a second pass over the
 //      buffer, sum(((x - K) - mu)^2), with one more reduction and exchange;
-//   5. the output pass re-reads the buffer and writes y with 16-byte stores (the weight, or
-//      gamma and beta, read through L1, two vectors ahead of their stores);
-//   6. once every thread has read the buffer it is refilled with the row `stages` rows on.
+//   5. the output pass re-reads the segment and writes y with 16-byte stores (the weight,
+//      or gamma and beta, read through L1, two vectors ahead of their stores);
+//   6. as soon as its threads have read the segment, the group refills it with the row
+//      `stages` rows on: a group's next copy waits for its own output, not for the CTA's.
 //
 // Waits: every mbarrier wait gives up after `wait_ns` nanoseconds (one second in normal
 // calls); a CTA whose wait ran out sets a bit in this file's device error word
@@ -47,6 +50,17 @@ __device__ unsigned int g_spread_device_error = 0;
 
 constexpr int kWarps = kSpreadBlock / 32;
 constexpr int kAcc = 4;   // independent packed accumulators a thread
+// The copy groups of a CTA: each group of kSpreadBlock / groups threads owns a contiguous
+// segment of the chunk, fills it with its own bulk copy on its own barrier and refills it as
+// soon as its own threads have written it out. A warp a group in general; the whole CTA for
+// 16-bit LayerNorm, whose 40 registers a thread do not hold the per-warp bookkeeping
+// without spilling. Measured on GB300 (graphs of back-to-back launches, L2-cold, of the
+// measured HBM peak), a group a warp against one a CTA: RMSNorm bf16 1024 x 262152 0.88 ->
+// 0.90, 256 x 300000 0.84 -> 0.85, fp32 128 x 262144 0.81 -> 0.86, LayerNorm fp32 128 x
+// 262144 0.55 -> 0.60; 16-bit LayerNorm lost (bf16 1024 x 262152 0.69 -> 0.64).
+__host__ __device__ constexpr int spread_copy_groups(bool layernorm, int elem_bytes) {
+    return layernorm && elem_bytes == 2 ? 1 : kSpreadBlock / 32;
+}
 
 // Several CTAs an SM by registers (40 a thread, 64 for fp32 LayerNorm), so that one CTA's
 // row can compute while another's lands even with a single buffer each.
@@ -60,14 +74,17 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     constexpr int E = C::kElems;
     constexpr int ES = Storage<S>::kBytes;
     constexpr bool kOnePass = ES == 2;   // LayerNorm: one-pass statistics where they hold
+    constexpr int kGroups = spread_copy_groups(LN, ES);
+    constexpr int GS = kSpreadBlock / kGroups;   // threads a copy group
 
-    // Dynamic shared memory: `stages` buffers of (the row's first 16 bytes, the chunk).
+    // Dynamic shared memory: `stages` buffers, each kSpreadHeadBytes of row heads (a copy of
+    // the row's first 16 bytes a group, for the LayerNorm shift) and then the chunk.
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long full[kSpreadMaxStages];
+    __shared__ __align__(8) unsigned long long full[kSpreadMaxStages][kGroups];
     __shared__ __align__(8) unsigned long long bar_x[2], bar_z[2];
     __shared__ float part_a[2][kWarps], part_b[2][kWarps];
     // The second pass's partials: written after this row's exchange, which not every warp
-    // has finished reading part_a from; rewritten only after a later row's opening barrier.
+    // has finished reading part_a from; rewritten only after a later row's first barrier.
     __shared__ float part_c[kWarps];
     __shared__ float slot_a[2][16], slot_b[2][16], slot_z[2][16];
     __shared__ int timed_out;
@@ -78,17 +95,29 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     const int64_t ncl = gridDim.x / nct;
     const int64_t cid = blockIdx.x / nct;
     const int t = threadIdx.x;
+    const int wid = t >> 5;
+    const int lane = t & 31;
+    static_assert(GS == 32 || GS == kSpreadBlock, "a copy group is a warp or the CTA");
+    const int g = kGroups == 1 ? 0 : wid;    // this thread's copy group ...
+    const int gt = kGroups == 1 ? t : lane;  // ... and its index in it
     const int64_t nvec = cols / E;
     const int64_t v0 = static_cast<int64_t>(rank) * chunk_vecs;
     const int64_t left = nvec - v0;
     const int my_vecs = left <= 0 ? 0 : (left < chunk_vecs ? static_cast<int>(left) : chunk_vecs);
     const uint32_t my_bytes = static_cast<uint32_t>(my_vecs) * 16u;
+    // The group's segment of the chunk: vectors [g_lo, g_lo + g_len).
+    const int seg = (my_vecs + kGroups - 1) / kGroups;
+    const int g_lo = g * seg < my_vecs ? g * seg : my_vecs;
+    const int g_len = my_vecs - g_lo < seg ? my_vecs - g_lo : seg;
     const int64_t pitch = cols * ES;
-    const int64_t stage_bytes = 16 + static_cast<int64_t>(chunk_vecs) * 16;
-    const int64_t my_rows = cid < rows ? (rows - cid + ncl - 1) / ncl : 0;
+    const uint32_t stage_bytes = kSpreadHeadBytes + static_cast<uint32_t>(chunk_vecs) * 16u;
+    // A row here holds at least 16 x 2048 16-byte vectors (512 KB), so a cluster's row count
+    // fits 32 bits with room to spare.
+    const int my_rows = cid < rows ? static_cast<int>((rows - cid + ncl - 1) / ncl) : 0;
 
     if (t == 0) {
-        for (int s = 0; s < stages; ++s) mbar_init(smem_u32(&full[s]), 1);
+        for (int s = 0; s < stages; ++s)
+            for (int q = 0; q < kGroups; ++q) mbar_init(smem_u32(&full[s][q]), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bar_x[s]), 1);
             mbar_init(smem_u32(&bar_z[s]), 1);
@@ -110,38 +139,53 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     griddep_launch_dependents();
 
     const char* xb = static_cast<const char*>(x);
-    auto issue = [&](int64_t j, int s) {   // one thread: row j into ring slot s
-        const int64_t row = cid + j * ncl;
-        const uint32_t bar = smem_u32(&full[s]);
-        const uint32_t dst = smem_u32(smem + s * stage_bytes);
-        mbar_arrive_expect_tx(bar, 16u + my_bytes);
+    // The group's first thread: its segment of row j (and, for LayerNorm, the row's first
+    // 16 bytes) into ring slot s, counted on the group's own barrier.
+    auto issue = [&](int j, int s) {
+        const char* src = xb + (cid + static_cast<int64_t>(j) * ncl) * pitch;
+        const uint32_t bar = smem_u32(&full[s][g]);
+        const uint32_t base = smem_u32(smem) + static_cast<uint32_t>(s) * stage_bytes;
+        const uint32_t g_bytes = static_cast<uint32_t>(g_len) * 16u;
+        mbar_arrive_expect_tx(bar, (LN ? 16u : 0u) + g_bytes);
         if (probe && j == 0) return;   // diagnostic: this copy is never issued
-        bulk_load(dst, xb + row * pitch, 16u, bar);
-        if (my_bytes > 0) bulk_load(dst + 16, xb + row * pitch + v0 * 16, my_bytes, bar);
+        if constexpr (LN) bulk_load(base + g * 16, src, 16u, bar);
+        if (g_bytes > 0) bulk_load(base + kSpreadHeadBytes + g_lo * 16, src + (v0 + g_lo) * 16, g_bytes, bar);
     };
-    if (t == 0) {
+    if (gt == 0) {
         for (int j = 0; j < stages && j < my_rows; ++j) issue(j, j);
     }
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
+    // Shared-memory loads of the ring: for the one-group CTA plain loads through pointers
+    // into smem, which the compiler can schedule; for warp groups loads at 32-bit shared
+    // addresses, since their extra bookkeeping would otherwise spill fp32 RMSNorm out of 40
+    // registers.
+    const uint32_t smem_at = smem_u32(smem);
     const float n = static_cast<float>(cols);
-    const char* wb = static_cast<const char*>(w) + v0 * 16;
-    const char* bb = LN ? static_cast<const char*>(beta) + v0 * 16 : nullptr;
-    int64_t nz = 0;   // second-pass exchanges so far (the same count in every CTA)
-    int64_t fail = -1;
+    const char* wb = static_cast<const char*>(w) + (v0 + g_lo) * 16;
+    const char* bb = LN ? static_cast<const char*>(beta) + (v0 + g_lo) * 16 : nullptr;
+    int nz = 0;       // second-pass exchanges so far (the same count in every CTA)
+    int fail = -1;
     int s = 0;        // ring slot of row j (j mod stages) ...
     uint32_t par = 0; // ... and its phase parity, advanced by counters
-    for (int64_t j = 0; j < my_rows; ++j) {
+    for (int j = 0; j < my_rows; ++j) {
         const int set = static_cast<int>(j & 1);
-        if (fail < 0 && !mbar_wait_bounded(smem_u32(&full[s]), par, wait_ns)) timed_out = 1;
-        __syncthreads();
-        if (fail < 0 && timed_out) fail = j;   // the same in every thread
-        const bool ok = fail < 0;
-        const unsigned char* buf = smem + s * stage_bytes;
+        // 1. The group's segment of the row has landed (each group waits for its own copy).
+        if (fail < 0 && !mbar_wait_bounded(smem_u32(&full[s][g]), par, wait_ns)) timed_out = 1;
+        const uint32_t slot = static_cast<uint32_t>(s) * stage_bytes;
+        const unsigned char* segp = smem + slot + kSpreadHeadBytes + g_lo * 16;
+        const uint32_t sega = smem_at + slot + kSpreadHeadBytes + g_lo * 16;
+        auto ldv = [&](int v) -> Raw<16> {   // vector v of the group's segment
+            if constexpr (kGroups == 1) return ld_smem16(segp + v * 16);
+            else return ld_smem16_at(sega + v * 16);
+        };
 
-        // 2. This thread's sums over its vectors of the buffer.
+        // 2. This thread's sums over its vectors of the segment.
         float shift = 0.0f;
-        if (LN && ok) C::each(ld_smem16(buf), [&](int e, float f) { if (e == 0) shift = f; });
+        if (LN && fail < 0) {
+            const Raw<16> h = kGroups == 1 ? ld_smem16(smem + slot) : ld_smem16_at(smem_at + slot + g * 16);
+            C::each(h, [&](int e, float f) { if (e == 0) shift = f; });
+        }
         const f32x2 k2 = f2_make(shift, shift);
         f32x2 acc1[kAcc], acc2[kAcc];
 #pragma unroll
@@ -149,13 +193,13 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
             acc1[a] = f2_make(0.0f, 0.0f);
             acc2[a] = f2_make(0.0f, 0.0f);
         }
-        if (ok) {
-            for (int vi = t; vi < my_vecs; vi += kAcc * kSpreadBlock) {
+        if (fail < 0) {
+            for (int vi = gt; vi < g_len; vi += kAcc * GS) {
 #pragma unroll
                 for (int a = 0; a < kAcc; ++a) {
-                    const int vj = vi + a * kSpreadBlock;
-                    if (vj < my_vecs) {
-                        C::each_pair(ld_smem16(buf + 16 + vj * 16), [&](int, f32x2 p) {
+                    const int vj = vi + a * GS;
+                    if (vj < g_len) {
+                        C::each_pair(ldv(vj), [&](int, f32x2 p) {
                             if constexpr (!LN) {
                                 acc1[a] = f2_fma(p, p, acc1[a]);
                             } else {
@@ -176,11 +220,13 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
         }
         s1 = warp_sum(s1);
         if constexpr (LN && kOnePass) s2 = warp_sum(s2);
-        if ((t & 31) == 0) {
-            part_a[set][t / 32] = s1;
-            part_b[set][t / 32] = s2;
+        if (lane == 0) {
+            part_a[set][wid] = s1;
+            part_b[set][wid] = s2;
         }
         __syncthreads();
+        if (fail < 0 && timed_out) fail = j;   // the same in every thread
+        const bool ok = fail < 0;
 
         // 3. The exchange: this CTA's sums to every CTA of the cluster.
         if (t == 0) mbar_arrive_expect_tx(smem_u32(&bar_x[set]), static_cast<uint32_t>(nct) * 8u);
@@ -216,12 +262,12 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
 #pragma unroll
                 for (int a = 0; a < kAcc; ++a) acc[a] = f2_make(0.0f, 0.0f);
                 if (ok) {
-                    for (int vi = t; vi < my_vecs; vi += kAcc * kSpreadBlock) {
+                    for (int vi = gt; vi < g_len; vi += kAcc * GS) {
 #pragma unroll
                         for (int a = 0; a < kAcc; ++a) {
-                            const int vj = vi + a * kSpreadBlock;
-                            if (vj < my_vecs)
-                                C::each_pair(ld_smem16(buf + 16 + vj * 16), [&](int, f32x2 p) {
+                            const int vj = vi + a * GS;
+                            if (vj < g_len)
+                                C::each_pair(ldv(vj), [&](int, f32x2 p) {
                                     const f32x2 d = f2_sub(f2_sub(p, k2), m2);
                                     acc[a] = f2_fma(d, d, acc[a]);
                                 });
@@ -232,9 +278,9 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
 #pragma unroll
                 for (int a = 0; a < kAcc; ++a) s3 += f2_lo(acc[a]) + f2_hi(acc[a]);
                 s3 = warp_sum(s3);
-                if ((t & 31) == 0) part_c[t / 32] = s3;
+                if (lane == 0) part_c[wid] = s3;
                 __syncthreads();
-                const int zs = static_cast<int>(nz & 1);
+                const int zs = nz & 1;
                 if (t == 0)
                     mbar_arrive_expect_tx(smem_u32(&bar_z[zs]), static_cast<uint32_t>(nct) * 4u);
                 if (t < nct) {
@@ -253,14 +299,16 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
             scale = rsqrtf(var + eps);
         }
 
-        // 5. The output pass, from the buffer.
+        // 5. The output pass over the group's segment, two vectors an iteration (both
+        //    weights loaded ahead of the first store).
         if (ok) {
-            char* yr = static_cast<char*>(y) + (cid + j * ncl) * pitch + v0 * 16;
+            char* yr = static_cast<char*>(y) + (cid + static_cast<int64_t>(j) * ncl) * pitch +
+                       (v0 + g_lo) * 16;
             const f32x2 r2 = f2_make(scale, scale);
             const f32x2 m2 = f2_make(mu, mu);
-            for (int vi = t; vi < my_vecs; vi += 2 * kSpreadBlock) {
-                const int vj = vi + kSpreadBlock;
-                const bool two = vj < my_vecs;
+            for (int vi = gt; vi < g_len; vi += 2 * GS) {
+                const int vj = vi + GS;
+                const bool two = vj < g_len;
                 const Raw<16> w0 = ld_shared_ro<16>(wb + vi * 16);
                 const Raw<16> w1 = two ? ld_shared_ro<16>(wb + vj * 16) : raw_zero<16>();
                 Raw<16> b0 = raw_zero<16>(), b1 = raw_zero<16>();
@@ -269,7 +317,7 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
                     if (two) b1 = ld_shared_ro<16>(bb + vj * 16);
                 }
                 auto out = [&](int v, const Raw<16>& wv, const Raw<16>& bv) {
-                    const Raw<16> xv = ld_smem16(buf + 16 + v * 16);
+                    const Raw<16> xv = ldv(v);
                     f32x2 wp[C::kPairs], bp[C::kPairs];
                     C::each_pair(wv, [&](int p, f32x2 q) { wp[p] = q; });
                     if constexpr (LN) C::each_pair(bv, [&](int p, f32x2 q) { bp[p] = q; });
@@ -285,10 +333,11 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
             }
         }
 
-        // 6. Every thread has read the buffer: refill it with the row `stages` rows on.
-        __syncthreads();
-        if (ok && t == 0 && j + stages < my_rows) {
-            // Order this CTA's generic-proxy reads of the buffer before the async-proxy
+        // 6. Every thread of the group has read its segment: refill it with the row `stages`
+        //    rows on, without waiting for the other groups.
+        if constexpr (kGroups == 1) __syncthreads(); else __syncwarp();
+        if (ok && gt == 0 && j + stages < my_rows) {
+            // Order the group's generic-proxy reads of the segment before the async-proxy
             // write that refills it.
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(j + stages, s);
@@ -300,14 +349,16 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     }
 
     __syncthreads();
-    if (timed_out && t == 0) {
-        atomicOr(&g_spread_device_error, kDeviceErrorWaitTimeout);
-        // Copies that may still be in flight into this CTA's shared memory: the rows from
-        // the failed one up to `stages` rows on. Wait for each, bounded.
-        const int64_t f = fail < 0 ? my_rows : fail;
-        for (int64_t jj = f; jj < f + stages && jj < my_rows; ++jj)
-            mbar_wait_bounded(smem_u32(&full[jj % stages]), static_cast<uint32_t>((jj / stages) & 1),
-                              wait_ns);
+    if (timed_out) {
+        if (t == 0) atomicOr(&g_spread_device_error, kDeviceErrorWaitTimeout);
+        // Copies that may still be in flight into this group's segment: the rows from the
+        // failed one up to `stages` rows on. Wait for each, bounded.
+        if (gt == 0) {
+            const int f = fail < 0 ? my_rows : fail;
+            for (int jj = f; jj < f + stages && jj < my_rows; ++jj)
+                mbar_wait_bounded(smem_u32(&full[jj % stages][g]),
+                                  static_cast<uint32_t>((jj / stages) & 1), wait_ns);
+        }
     }
 }
 

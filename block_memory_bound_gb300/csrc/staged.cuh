@@ -112,5 +112,17 @@ __device__ __forceinline__ Raw<16> ld_smem16(const unsigned char* p) {
     return r;
 }
 
+// The same from a 32-bit shared-memory address (a shared::cta window offset, as smem_u32
+// gives), which takes one register where a generic pointer takes two; ordered as a volatile
+// access (the compiler keeps it where it is written).
+__device__ __forceinline__ Raw<16> ld_smem16_at(uint32_t addr) {
+    Raw<16> r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+                 : "r"(addr)
+                 : "memory");
+    return r;
+}
+
 }  // namespace staged
 }  // namespace camp
