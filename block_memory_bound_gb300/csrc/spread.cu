@@ -10,15 +10,15 @@
 // spreads each row over a cluster of C CTAs (up to 16) and keeps each CTA's whole chunk in
 // shared memory instead: a chunk of up to about 13,000 vectors (200 KB) with one buffer,
 // half that with two, so x is still read from HBM once for rows of up to about 1.7 M bf16
-// columns. (LayerNorm rows that the staged kernel would hold in ragged chunks, filling
-// little of its threads' vector slots, come here too.) Per row:
+// columns. (16-bit LayerNorm rows past the register kernel, and fp32 LayerNorm rows that
+// the staged kernel would hold in ragged chunks, come here too.) Per row:
 //   1. each copy group (a warp, or the whole CTA for 16-bit LayerNorm) owns a contiguous
 //      segment of the CTA's chunk, which lands in a ring buffer by the group's own bulk
 //      asynchronous copy on its own mbarrier (with a copy of the row's first 16 bytes, for
 //      the LayerNorm shift);
-//   2. every thread sums over its vectors of the segment (one every group-size vectors), in kAcc
-//      independent packed accumulators: sum(x^2) for RMSNorm; sum(x - K) and, in 16-bit
-//      storage, sum((x - K)^2) for LayerNorm; one block reduction;
+//   2. every thread sums over its vectors of the segment (one every group-size vectors),
+//      in kAcc independent packed accumulators: sum(x^2) for RMSNorm; sum(x - K) and, in
+//      16-bit storage, sum((x - K)^2) for LayerNorm; one block reduction;
 //   3. the CTA's sums go to every CTA of the cluster by st.async (counted on the receiver's
 //      mbarrier; two slot sets alternating by row) and every CTA adds the C of them in rank
 //      order (the same bits everywhere);
@@ -37,6 +37,8 @@
 // copies it still has in flight. With `probe` set (a diagnostic of that path) each CTA's
 // first row copy is armed on its barrier but never issued, so every CTA's first wait runs
 // out.
+#include <climits>
+
 #include <cooperative_groups.h>
 
 #include "staged.cuh"
@@ -111,8 +113,7 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     const int g_len = my_vecs - g_lo < seg ? my_vecs - g_lo : seg;
     const int64_t pitch = cols * ES;
     const uint32_t stage_bytes = kSpreadHeadBytes + static_cast<uint32_t>(chunk_vecs) * 16u;
-    // A row here holds at least 16 x 2048 16-byte vectors (512 KB), so a cluster's row count
-    // fits 32 bits with room to spare.
+    // The launcher refuses grids that would give a cluster more than INT_MAX rows.
     const int my_rows = cid < rows ? static_cast<int>((rows - cid + ncl - 1) / ncl) : 0;
 
     if (t == 0) {
@@ -149,7 +150,8 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
         mbar_arrive_expect_tx(bar, (LN ? 16u : 0u) + g_bytes);
         if (probe && j == 0) return;   // diagnostic: this copy is never issued
         if constexpr (LN) bulk_load(base + g * 16, src, 16u, bar);
-        if (g_bytes > 0) bulk_load(base + kSpreadHeadBytes + g_lo * 16, src + (v0 + g_lo) * 16, g_bytes, bar);
+        if (g_bytes > 0)
+            bulk_load(base + kSpreadHeadBytes + g_lo * 16, src + (v0 + g_lo) * 16, g_bytes, bar);
     };
     if (gt == 0) {
         for (int j = 0; j < stages && j < my_rows; ++j) issue(j, j);
@@ -183,7 +185,8 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
         // 2. This thread's sums over its vectors of the segment.
         float shift = 0.0f;
         if (LN && fail < 0) {
-            const Raw<16> h = kGroups == 1 ? ld_smem16(smem + slot) : ld_smem16_at(smem_at + slot + g * 16);
+            const Raw<16> h =
+                kGroups == 1 ? ld_smem16(smem + slot) : ld_smem16_at(smem_at + slot + g * 16);
             C::each(h, [&](int e, float f) { if (e == 0) shift = f; });
         }
         const f32x2 k2 = f2_make(shift, shift);
@@ -397,6 +400,7 @@ cudaError_t launch_spread(const void* x, const void* w, const void* beta, void* 
     if (e != cudaSuccess) return e;
     if (active < 1) return cudaErrorInvalidConfiguration;
     const int64_t ncl = rows < active ? rows : active;
+    if ((rows + ncl - 1) / ncl > INT_MAX) return cudaErrorInvalidValue;   // 32-bit row counters
     cfg.gridDim = dim3(static_cast<unsigned>(ncl * cluster));
     return cudaLaunchKernelEx(&cfg, kernel, x, w, beta, y, rows, cols, eps, chunk, stages,
                               wait_ns, probe);
