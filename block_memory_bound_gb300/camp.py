@@ -61,7 +61,7 @@ EXPORTS = (
     "camp_rope_tables",
     "camp_layernorm", "camp_layernorm_plan", "camp_layernorm_with_plan",
     "camp_kv_cat_repeat", "camp_kv_cat_repeat_plan", "camp_kv_cat_repeat_with_plan",
-    "camp_device_errors", "camp_layernorm_wait_probe",
+    "camp_device_errors", "camp_layernorm_wait_probe", "camp_rmsnorm_wait_probe",
 )
 
 
@@ -126,6 +126,9 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
         lib.camp_layernorm_wait_probe.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int, pplan,
                                                   ctypes.c_uint64, vp]
         lib.camp_layernorm_wait_probe.restype = c_int
+        lib.camp_rmsnorm_wait_probe.argtypes = [vp, vp, vp, i64, i64, f32, c_int, pplan,
+                                                ctypes.c_uint64, vp]
+        lib.camp_rmsnorm_wait_probe.restype = c_int
         lib.camp_rmsnorm_plan.argtypes = [vp, vp, vp, i64, i64, c_int, pplan]
         lib.camp_rmsnorm_plan.restype = c_int
         lib.camp_rope_plan.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, c_int, pplan]
@@ -353,6 +356,16 @@ def camp_layernorm_wait_probe(x, gamma, beta, y, rows: int, cols: int, eps: floa
         _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), int(rows), int(cols), float(eps),
         _dtype(dtype), None if plan is None else ctypes.byref(plan), int(wait_ns),
         _stream(stream)))
+
+
+def camp_rmsnorm_wait_probe(x, w, y, rows: int, cols: int, eps: float, dtype, wait_ns: int,
+                            plan: Plan | None = None, stream=None) -> None:
+    """The staged RMSNorm (or the staged or spread kernel of `plan`) with every wait bounded
+    by `wait_ns` and each CTA's first row copy left unissued (a diagnostic of the bounded
+    waits; see include/camp.h)."""
+    _check("camp_rmsnorm_wait_probe", load().camp_rmsnorm_wait_probe(
+        _ptr(x), _ptr(w), _ptr(y), int(rows), int(cols), float(eps), _dtype(dtype),
+        None if plan is None else ctypes.byref(plan), int(wait_ns), _stream(stream)))
 
 
 def camp_layernorm_plan(x, gamma, beta, y, rows: int, cols: int, dtype) -> Plan:

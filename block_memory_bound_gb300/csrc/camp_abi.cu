@@ -1703,6 +1703,43 @@ CAMP_API camp_status_t camp_layernorm(const void* x, const void* gamma, const vo
     return camp_layernorm_with_plan(x, gamma, beta, y, rows, cols, eps, dtype, nullptr, stream);
 }
 
+CAMP_API camp_status_t camp_rmsnorm_wait_probe(const void* x, const void* w, void* y,
+                                               int64_t rows, int64_t cols, float eps,
+                                               camp_dtype_t dtype, const camp_plan_t* plan,
+                                               uint64_t wait_ns, void* stream) {
+    RmsCall c;
+    bool empty = false;
+    camp_status_t st = rms_validate(x, w, y, rows, cols, dtype, &c, &empty);
+    if (st != CAMP_SUCCESS) return st;
+    if (!eps_ok(eps) || wait_ns < 1000 || wait_ns > 1000000000ull) return CAMP_ERR_INVALID_ARG;
+    if (empty) return CAMP_SUCCESS;
+    c.a.eps = eps;
+    camp_plan_t p;
+    if (plan != nullptr) {
+        if (plan->kernel != CAMP_KERNEL_RMSNORM_STAGED &&
+            plan->kernel != CAMP_KERNEL_RMSNORM_SPREAD)
+            return CAMP_ERR_NOT_SUPPORTED;
+        st = rms_accept_plan(c, *plan, &p);
+        if (st != CAMP_SUCCESS) return st;
+    } else {
+        // The staged kernel's plan for these arguments, whichever kernel camp_rmsnorm takes.
+        const int64_t nvec = cols * camp::elem_bytes(c.t) / 16;
+        int cl = 0, stg = 0;
+        int64_t chunk = 0;
+        if (rms_vec_bytes(c) != 16 || nvec <= kStagedFrom ||
+            !rms_choose_staged(c, nvec, &cl, &stg, &chunk))
+            return CAMP_ERR_NOT_SUPPORTED;
+        p = camp_plan_t{};
+        rms_staged_plan_fields(c, cl, stg, chunk, &p);
+    }
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.kernel == CAMP_KERNEL_RMSNORM_SPREAD)
+        return runtime_status(
+            camp::rmsnorm_spread_launch(c.t, p.cluster, p.per_thread, c.a, s, wait_ns, 1));
+    return runtime_status(
+        camp::rmsnorm_staged_launch(false, c.t, p.cluster, p.per_thread, c.a, s, wait_ns, 1));
+}
+
 CAMP_API camp_status_t camp_layernorm_wait_probe(const void* x, const void* gamma,
                                                  const void* beta, void* y, int64_t rows,
                                                  int64_t cols, float eps, camp_dtype_t dtype,

@@ -126,8 +126,10 @@ constexpr int64_t kSmSmemBytes = 228 * 1024;     // shared memory per SM
 inline int64_t staged_smem_bytes(bool add, int64_t chunk_vecs, int stages) {
     return chunk_vecs * 16 * (1 + (add ? 2 : 1) * stages);   // w, then the row buffers
 }
+// `wait_ns` and `probe` as for layernorm_staged_launch (the probe: plain RMSNorm only).
 cudaError_t rmsnorm_staged_launch(bool add, DType t, int cluster, int stages,
-                                  const RmsnormArgs& a, cudaStream_t s);
+                                  const RmsnormArgs& a, cudaStream_t s,
+                                  unsigned long long wait_ns = 1000000000ull, int probe = 0);
 
 // Rows past the staged kernels' registers (spread.cu): clusters of `cluster` (1..16) CTAs of
 // kSpreadBlock threads; each CTA keeps its whole chunk of ceil(nvec / cluster) 16-byte
@@ -146,7 +148,8 @@ inline int64_t spread_smem_bytes(int64_t chunk_vecs, int stages) {
     return stages * (kSpreadHeadBytes + chunk_vecs * 16);
 }
 cudaError_t rmsnorm_spread_launch(DType t, int cluster, int stages, const RmsnormArgs& a,
-                                  cudaStream_t s);
+                                  cudaStream_t s, unsigned long long wait_ns = 1000000000ull,
+                                  int probe = 0);
 struct LayernormArgs;
 // `wait_ns` bounds every mbarrier wait (one second in normal calls); `probe` != 0 leaves each
 // CTA's first row copy unissued (the wait diagnostic), as for layernorm_staged_launch.

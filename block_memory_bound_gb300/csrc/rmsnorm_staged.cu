@@ -65,17 +65,21 @@ __device__ __forceinline__ Raw<16> scale16(const Raw<16>& xv, const Raw<16>& wv,
     return C::map_pair(xv, [&](int p, f32x2 xp) { return f2_mul(f2_mul(xp, r2), wp[p]); });
 }
 
-template <typename S, bool ADD, int NVT>
+// PROBE: the wait diagnostic's variant (plain RMSNorm only): every mbarrier wait bounded by
+// `wait_ns` instead of one second, and each CTA's first row copy armed on its barrier but
+// never issued, so every CTA's first wait runs out. The normal variants ignore `wait_ns`.
+template <typename S, bool ADD, int NVT, bool PROBE>
 __global__ void __launch_bounds__(kStagedBlock, 1)
 rmsnorm_staged_kernel(const void* x, const void* r, void* h, const void* __restrict__ w,
                       void* y, int64_t rows, int64_t cols, float eps, int chunk_vecs,
-                      int stages) {
+                      int stages, unsigned long long wait_ns) {
     namespace cg = cooperative_groups;
     using C = Codec<S, 16>;
     constexpr int E = C::kElems;
     constexpr int ES = Storage<S>::kBytes;
     constexpr int kWarps = kStagedBlock / 32;
     constexpr int NB = ADD ? 2 : 1;   // staged tensors per row: x (and r)
+    const unsigned long long limit = PROBE ? wait_ns : kWaitLimitNs;
 
     // Dynamic shared memory: this CTA's chunk of w, then `stages` row buffers.
     extern __shared__ __align__(128) unsigned char smem[];
@@ -133,6 +137,7 @@ rmsnorm_staged_kernel(const void* x, const void* r, void* h, const void* __restr
         const uint32_t bar = smem_u32(&full[s]);
         const uint32_t dst = smem_u32(ring + s * stage_bytes);
         mbar_arrive_expect_tx(bar, my_bytes * NB);
+        if (PROBE && row == cid) return;   // diagnostic: the first row's copy is never issued
         bulk_load(dst, xb + row * pitch, my_bytes, bar);
         if constexpr (ADD) bulk_load(dst + chunk_vecs * 16, rb + row * pitch, my_bytes, bar);
     };
@@ -154,7 +159,7 @@ rmsnorm_staged_kernel(const void* x, const void* r, void* h, const void* __restr
         const int set = static_cast<int>(i & 1);
         const unsigned char* buf = ring + s * stage_bytes;
         if (fail_iter < 0 && my_bytes > 0 &&
-            !mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>((i / stages) & 1)))
+            !mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>((i / stages) & 1), limit))
             timed_out = 1;
         __syncthreads();
         if (fail_iter < 0 && timed_out) fail_iter = i;   // the same in every thread
@@ -207,7 +212,7 @@ rmsnorm_staged_kernel(const void* x, const void* r, void* h, const void* __restr
         }
         // Every CTA waits for all partials of every row, even after a failure: a peer's
         // stores must have landed before this CTA's shared memory is released.
-        if (!mbar_wait_bounded(smem_u32(&sum_bar[set]), static_cast<uint32_t>((i >> 1) & 1)))
+        if (!mbar_wait_bounded(smem_u32(&sum_bar[set]), static_cast<uint32_t>((i >> 1) & 1), limit))
             timed_out = 1;
         float tot = 0.0f;
         for (int q = 0; q < nct; ++q) tot += slot[set][q];   // rank order in every CTA
@@ -215,7 +220,7 @@ rmsnorm_staged_kernel(const void* x, const void* r, void* h, const void* __restr
 
         // Pass 2: y = x * rinv * w from the registers and the staged w.
         if (ok && my_bytes > 0 && !w_ready) {
-            if (!mbar_wait_bounded(wbar, 0)) timed_out = 1;
+            if (!mbar_wait_bounded(wbar, 0, limit)) timed_out = 1;
             w_ready = true;
         }
         if (ok) {
@@ -234,21 +239,21 @@ rmsnorm_staged_kernel(const void* x, const void* r, void* h, const void* __restr
     if (timed_out && t == 0) {
         atomicOr(&g_device_error, kDeviceErrorWaitTimeout);
         // Copies that may still be in flight into this CTA's shared memory: w, and those
-        // issued for iterations fail_iter .. fail_iter + stages - 1. Wait for each, at most
-        // a second.
-        if (my_bytes > 0) mbar_wait_bounded(wbar, 0);
+        // issued for iterations fail_iter .. fail_iter + stages - 1. Wait for each, bounded.
+        if (my_bytes > 0) mbar_wait_bounded(wbar, 0, limit);
         const int64_t f = fail_iter < 0 ? i : fail_iter;
         for (int64_t j = f; j < f + stages; ++j) {
             if (my_bytes > 0 && cid + j * ncl < rows)
-                mbar_wait_bounded(smem_u32(&full[j % stages]), static_cast<uint32_t>((j / stages) & 1));
+                mbar_wait_bounded(smem_u32(&full[j % stages]),
+                                  static_cast<uint32_t>((j / stages) & 1), limit);
         }
     }
 }
 
-template <typename S, bool ADD, int NVT>
-cudaError_t launch_staged(const RmsnormArgs& a, int cluster, int stages, int chunk_vecs,
-                          cudaStream_t s) {
-    auto kernel = rmsnorm_staged_kernel<S, ADD, NVT>;
+template <typename S, bool ADD, int NVT, bool PROBE>
+cudaError_t launch_staged_kernel(const RmsnormArgs& a, int cluster, int stages, int chunk_vecs,
+                                 unsigned long long wait_ns, cudaStream_t s) {
+    auto kernel = rmsnorm_staged_kernel<S, ADD, NVT, PROBE>;
     const size_t smem = static_cast<size_t>(staged_smem_bytes(ADD, chunk_vecs, stages));
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -280,36 +285,51 @@ cudaError_t launch_staged(const RmsnormArgs& a, int cluster, int stages, int chu
     const int64_t ncl = a.rows < active ? a.rows : active;
     cfg.gridDim = dim3(static_cast<unsigned>(ncl * cluster));
     return cudaLaunchKernelEx(&cfg, kernel, a.x, a.r, a.h, a.w, a.y, a.rows, a.cols, a.eps,
-                              chunk_vecs, stages);
+                              chunk_vecs, stages, wait_ns);
+}
+
+template <typename S, bool ADD, int NVT>
+cudaError_t launch_staged(const RmsnormArgs& a, int cluster, int stages, int chunk_vecs,
+                          unsigned long long wait_ns, int probe, cudaStream_t s) {
+    if constexpr (!ADD) {
+        if (probe)
+            return launch_staged_kernel<S, false, NVT, true>(a, cluster, stages, chunk_vecs,
+                                                             wait_ns, s);
+    }
+    if (probe) return cudaErrorInvalidValue;   // the probe has no add-path variant
+    return launch_staged_kernel<S, ADD, NVT, false>(a, cluster, stages, chunk_vecs, wait_ns, s);
 }
 
 template <typename S, bool ADD>
-cudaError_t launch_staged_nvt(const RmsnormArgs& a, int cluster, int stages, cudaStream_t s) {
+cudaError_t launch_staged_nvt(const RmsnormArgs& a, int cluster, int stages,
+                              unsigned long long wait_ns, int probe, cudaStream_t s) {
     constexpr int E = 16 / Storage<S>::kBytes;
     const int64_t nvec = a.cols / E;
     const int chunk = static_cast<int>((nvec + cluster - 1) / cluster);
     const int need = (chunk + kStagedBlock - 1) / kStagedBlock;
-    if (need <= 1) return launch_staged<S, ADD, 1>(a, cluster, stages, chunk, s);
-    if (need <= 2) return launch_staged<S, ADD, 2>(a, cluster, stages, chunk, s);
-    if (need <= 4) return launch_staged<S, ADD, 4>(a, cluster, stages, chunk, s);
-    if (need <= kStagedMaxVecsPerThread) return launch_staged<S, ADD, 8>(a, cluster, stages, chunk, s);
+    if (need <= 1) return launch_staged<S, ADD, 1>(a, cluster, stages, chunk, wait_ns, probe, s);
+    if (need <= 2) return launch_staged<S, ADD, 2>(a, cluster, stages, chunk, wait_ns, probe, s);
+    if (need <= 4) return launch_staged<S, ADD, 4>(a, cluster, stages, chunk, wait_ns, probe, s);
+    if (need <= kStagedMaxVecsPerThread)
+        return launch_staged<S, ADD, 8>(a, cluster, stages, chunk, wait_ns, probe, s);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t rmsnorm_staged_launch(bool add, DType t, int cluster, int stages,
-                                  const RmsnormArgs& a, cudaStream_t s) {
+                                  const RmsnormArgs& a, cudaStream_t s,
+                                  unsigned long long wait_ns, int probe) {
     if (cluster < 1 || cluster > 16 || stages < 2 || stages > kStagedMaxStages)
         return cudaErrorInvalidValue;
     if (t == DType::BF16)
-        return add ? launch_staged_nvt<bf16_t, true>(a, cluster, stages, s)
-                   : launch_staged_nvt<bf16_t, false>(a, cluster, stages, s);
+        return add ? launch_staged_nvt<bf16_t, true>(a, cluster, stages, wait_ns, probe, s)
+                   : launch_staged_nvt<bf16_t, false>(a, cluster, stages, wait_ns, probe, s);
     if (t == DType::F16)
-        return add ? launch_staged_nvt<f16_t, true>(a, cluster, stages, s)
-                   : launch_staged_nvt<f16_t, false>(a, cluster, stages, s);
-    return add ? launch_staged_nvt<f32_t, true>(a, cluster, stages, s)
-               : launch_staged_nvt<f32_t, false>(a, cluster, stages, s);
+        return add ? launch_staged_nvt<f16_t, true>(a, cluster, stages, wait_ns, probe, s)
+                   : launch_staged_nvt<f16_t, false>(a, cluster, stages, wait_ns, probe, s);
+    return add ? launch_staged_nvt<f32_t, true>(a, cluster, stages, wait_ns, probe, s)
+               : launch_staged_nvt<f32_t, false>(a, cluster, stages, wait_ns, probe, s);
 }
 
 cudaError_t read_device_errors(unsigned int* flags, bool clear) {

@@ -426,11 +426,11 @@ cudaError_t spread_dtype(DType t, const void* x, const void* w, const void* beta
 }  // namespace
 
 cudaError_t rmsnorm_spread_launch(DType t, int cluster, int stages, const RmsnormArgs& a,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, unsigned long long wait_ns, int probe) {
     if (cluster < 1 || cluster > 16 || stages < 1 || stages > kSpreadMaxStages)
         return cudaErrorInvalidValue;
     return spread_dtype<false>(t, a.x, a.w, nullptr, a.y, a.rows, a.cols, a.eps, cluster, stages,
-                               kWaitLimitNs, 0, s);
+                               wait_ns, probe, s);
 }
 
 cudaError_t layernorm_spread_launch(DType t, int cluster, int stages, const LayernormArgs& a,

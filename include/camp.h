@@ -476,6 +476,23 @@ CAMP_API camp_status_t camp_layernorm_with_plan(const void* x, const void* gamma
                                                 const camp_plan_t* plan, void* stream);
 
 /*
+ * The same diagnostic for RMSNorm without the residual add (the pages have no counterpart):
+ * the staged RMSNorm kernel (plan == NULL: the staged plan for these arguments, whichever
+ * kernel camp_rmsnorm would take) or the kernel of `plan` (staged or spread, checked as
+ * camp_rmsnorm_with_plan checks it), with every mbarrier wait bounded by `wait_ns` and each
+ * CTA's first row copy left unissued; the outcome is as for camp_layernorm_wait_probe below
+ * (the timeout bit set, y untouched, the next call normal). Arguments, validation and errors
+ * as camp_rmsnorm; in addition CAMP_ERR_INVALID_ARG if wait_ns is outside
+ * [1000, 1000000000], and CAMP_ERR_NOT_SUPPORTED for a plan of another kernel or one that
+ * does not hold the row, or, with plan == NULL, unless the staged kernel holds the row
+ * (16-byte-aligned pointers and rows of more than 4096 16-byte vectors, up to 16 x 2048).
+ */
+CAMP_API camp_status_t camp_rmsnorm_wait_probe(const void* x, const void* w, void* y,
+                                               int64_t rows, int64_t cols, float eps,
+                                               camp_dtype_t dtype, const camp_plan_t* plan,
+                                               uint64_t wait_ns, void* stream);
+
+/*
  * Diagnostic of the bounded waits (the pages have no counterpart; it exists so that the
  * failure path of the staged and spread kernels can be exercised without faulting
  * anything). Runs the staged LayerNorm kernel (plan == NULL: the staged plan for these

@@ -975,3 +975,22 @@ def test_wait_probe_refusals_launch_nothing(lib):
         assert f(X, W, BETA, Y, 4, 65536, eps, camp.BF16, ctypes.byref(plan), 100_000, None) == \
             camp.ERR_NOT_SUPPORTED, plan
     assert f(X, W, BETA, Y, 0, 65536, eps, camp.BF16, None, 100_000, None) == camp.SUCCESS
+
+
+def test_rmsnorm_wait_probe_refusals_launch_nothing(lib):
+    plan_t = camp.Plan
+    f = lib.camp_rmsnorm_wait_probe
+    eps = ctypes.c_float(1e-5)
+    for ns in (0, 999, 1_000_000_001):
+        assert f(X, W, Y, 4, 65536, eps, camp.BF16, None, ns, None) == camp.ERR_INVALID_ARG
+    # 2048 vectors: the rows kernel's width, no staged plan
+    assert f(X, W, Y, 4, 16384, eps, camp.BF16, None, 100_000, None) == camp.ERR_NOT_SUPPORTED
+    for plan in (plan_t(kernel=camp.KERNEL_RMSNORM_ROWS, vec_bytes=16, group=512, per_thread=8),
+                 plan_t(kernel=camp.KERNEL_RMSNORM_WIDE, vec_bytes=16),
+                 plan_t(kernel=camp.KERNEL_RMSNORM_CLUSTER, vec_bytes=16, cluster=8, per_thread=8),
+                 plan_t(kernel=camp.KERNEL_RMSNORM_STAGED, vec_bytes=16, cluster=1, per_thread=2),
+                 plan_t(kernel=camp.KERNEL_RMSNORM_SPREAD, vec_bytes=16, cluster=3, per_thread=1),
+                 plan_t(kernel=camp.KERNEL_LAYERNORM_SPREAD, vec_bytes=16, cluster=2, per_thread=1)):
+        assert f(X, W, Y, 4, 65536, eps, camp.BF16, ctypes.byref(plan), 100_000, None) == \
+            camp.ERR_NOT_SUPPORTED, plan
+    assert f(X, W, Y, 0, 65536, eps, camp.BF16, None, 100_000, None) == camp.SUCCESS

@@ -91,3 +91,46 @@ def test_probe_argument_checks():
                                            plan=plan)
         assert ei.value.status == camp.ERR_NOT_SUPPORTED
     assert camp.camp_device_errors() == 0
+
+
+# ------------------------------------------------------------------ RMSNorm
+
+import test_rmsnorm_gpu as rms_tests   # noqa: E402  (the RMSNorm run-and-compare helper)
+
+
+def rms_staged(cluster, stages):
+    return camp.Plan(kernel=camp.KERNEL_RMSNORM_STAGED, vec_bytes=16, cluster=cluster,
+                     per_thread=stages)
+
+
+def rms_spread(cluster, stages=1):
+    return camp.Plan(kernel=camp.KERNEL_RMSNORM_SPREAD, vec_bytes=16, cluster=cluster,
+                     per_thread=stages)
+
+
+@pytest.mark.parametrize("dtype,rows,cols,plan", [
+    ("bf16", 6, 65536, None),              # the staged plan for these arguments
+    ("f32", 5, 65536, rms_staged(16, 2)),
+    ("f16", 40, 131072, rms_staged(16, 3)),
+    ("bf16", 700, 65536, rms_staged(8, 3)),  # a dozen rows a cluster after the failed one
+    ("bf16", 6, 300000, rms_spread(8)),      # a copy group a warp
+    ("f32", 5, 262144, rms_spread(16)),
+    ("bf16", 400, 140000, rms_spread(4, 2)),  # two buffers, about ten rows a cluster
+])
+def test_an_rmsnorm_wait_that_runs_out_sets_the_bit_and_stores_nothing(dtype, rows, cols,
+                                                                        plan):
+    x = torch.randn(rows, cols, device="cuda").to(ln_tests.inputs.STORAGE[dtype])
+    w = torch.ones(cols, device="cuda", dtype=x.dtype)
+    yflat, buf = ln_tests._guarded(rows * cols, x.dtype)
+    bits = torch.int16 if buf.element_size() == 2 else torch.int32   # the canary is a NaN
+    before = buf.view(bits).clone()
+    assert camp.camp_device_errors(clear=True) == 0
+    camp.camp_rmsnorm_wait_probe(x, w, yflat, rows, cols, 1e-5, dtype, wait_ns=200_000,
+                                 plan=plan)
+    torch.cuda.synchronize()
+    assert camp.camp_device_errors() & camp.DEVICE_ERROR_WAIT_TIMEOUT
+    assert torch.equal(buf.view(bits), before), "a CTA whose wait ran out stored output"
+    assert camp.camp_device_errors(clear=True) & camp.DEVICE_ERROR_WAIT_TIMEOUT
+    assert camp.camp_device_errors() == 0
+    rms_tests.run_case(rows, cols, dtype, seed=rows)   # the next normal call
+    assert camp.camp_device_errors() == 0
