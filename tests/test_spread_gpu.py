@@ -100,6 +100,27 @@ def test_default_plan_past_the_staged_kernel(cols, dtype):
     ln_tests.run_case(3, cols, dtype, seed=cols % 17)
 
 
+@pytest.mark.parametrize("kind,rows,cols,dtype,plan", [
+    # more rows than one round of the resident clusters, not a whole number of rounds: the
+    # last round's rows on a part of the clusters
+    ("ln", 256, 131072, "bf16", None),       # 4-CTA clusters, 28 rows in the last round
+    ("rms", 60, 300000, "bf16", None),       # 8-CTA clusters, 9 rows in the last round
+    ("ln", 300, 140000, "f32", None),        # two CTAs an SM
+    ("rms", 200, 140000, "f16", None),
+    ("ln", 403, 140000, "bf16", "4x2"),      # two buffers
+    ("rms", 501, 65536, "bf16", "2x1"),
+])
+def test_rows_past_a_round_of_clusters(kind, rows, cols, dtype, plan):
+    p = None
+    if plan is not None:
+        cl, st = map(int, plan.split("x"))
+        p = ln_plan(cl, st) if kind == "ln" else rms_plan(cl, st)
+    if kind == "ln":
+        ln_tests.run_case(rows, cols, dtype, seed=rows % 11, plan=p)
+    else:
+        rms_tests.run_case(rows, cols, dtype, seed=rows % 11, plan=p)
+
+
 def test_forced_plans_that_do_not_fit_are_refused():
     x = torch.zeros(2, 4096, dtype=torch.bfloat16, device="cuda")
     w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
