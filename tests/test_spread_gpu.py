@@ -42,7 +42,7 @@ def ln_plan(cluster, stages):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("cluster", [1, 2, 4, 16])
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("stages", [1, 2, 3])
 def test_every_variant(dtype, cluster, stages):
     # chunks that are not a multiple of the 512 threads, the last rank's chunk short
@@ -75,6 +75,24 @@ def test_layernorm_rows_far_from_their_shift(dtype):
     for stages in (1, 2):
         ln_tests.run_case(rows, cols, dtype, seed=stages, plan=ln_plan(8, stages),
                           x_cpu=ln_tests._mixed_rows(rows, cols, dtype, stages))
+
+
+@pytest.mark.parametrize("plan", [None, (8, 1), (16, 2)])
+def test_rmsnorm_stress_rows(plan):
+    # the stress distribution (1% of rows x1e3, 1% x1e-4) on rows past the staged kernel:
+    # fp32 sums over a row spread across the cluster's CTAs
+    p = None if plan is None else rms_plan(*plan)
+    rms_tests.run_case(200, 262152, "bf16", eps=1e-6, seed=4, stress=True, plan=p)
+
+
+def test_rmsnorm_constant_rows_match_closed_form_within_tolerance():
+    # x_j = c: y_j = w_j * sign(c) / sqrt(1 + eps/c^2), and a zero row gives 0 (eps > 0)
+    cols = 262152
+    vals = torch.tensor([1.0, -2.0, 0.01, 300.0, 0.0], dtype=torch.float32)
+    x_cpu = vals[:, None].expand(5, cols).contiguous().to(torch.bfloat16)
+    _, w_cpu = rms_tests.inputs.rmsnorm_inputs(1, cols, "bf16", seed=3)
+    y = rms_tests.run_case(5, cols, "bf16", x_cpu=x_cpu, w_cpu=w_cpu)
+    assert bool((y[4] == 0).all())
 
 
 def test_in_place():
