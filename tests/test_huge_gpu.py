@@ -100,6 +100,33 @@ def test_layernorm_past_2_32_elements():
     del x, y
 
 
+@pytest.mark.parametrize("cols,kinds", [
+    (65536, (camp.KERNEL_RMSNORM_STAGED, camp.KERNEL_LAYERNORM_SPREAD)),   # rows in shared memory
+    (262152, (camp.KERNEL_RMSNORM_SPREAD, camp.KERNEL_LAYERNORM_SPREAD)),  # a cluster per row
+])
+def test_wide_rows_past_2_32_elements(cols, kinds):
+    rows = BIG // cols + 3
+    x = _randn_bf16((rows, cols), 6)
+    g = (1 + 0.1 * torch.randn(cols, device="cuda")).to(torch.bfloat16)
+    b = torch.randn(cols, device="cuda").to(torch.bfloat16)
+    y = torch.empty_like(x)
+    idx = torch.tensor(_sample_rows(rows, cols), device="cuda")
+    assert camp.camp_rmsnorm_plan(x, g, y, rows, cols, "bf16").kernel == kinds[0]
+    camp.camp_rmsnorm(x, g, y, rows, cols, 1e-5, "bf16")
+    torch.cuda.synchronize()
+    want = oracle.rmsnorm(inputs.to_numpy(x[idx]), inputs.to_numpy(g), float(np.float32(1e-5)),
+                          "bf16")
+    assert_bf16_close(inputs.to_numpy(y[idx]), want, f"rmsnorm {rows}x{cols}")
+    plan = camp.camp_layernorm_plan(x, g, b, y, rows, cols, "bf16")
+    assert plan.kernel == kinds[1]
+    camp.camp_layernorm(x, g, b, y, rows, cols, 1e-5, "bf16")
+    torch.cuda.synchronize()
+    ln_tests.check(y[idx].cpu(), x[idx].cpu(), g.cpu(), b.cpu(), float(np.float32(1e-5)), plan,
+                   f"layernorm {rows}x{cols}")
+    assert camp.camp_device_errors() == 0
+    del x, y
+
+
 def test_rope_qk_past_2_32_elements():
     S, Hq, Hk, D = (BIG // (40 * 64)) + 33, 32, 8, 64   # Q + K: 4.3 G elements
     q = _randn_bf16((1, S, Hq, D), 5)
