@@ -1256,18 +1256,15 @@ bool ln_choose_staged(int64_t nvec, int es, int* cluster, int* stages, int* rps,
 }
 
 // The share of the staged kernel's per-thread vector slots a chunk fills: its launcher gives
-// each thread 1, 2, 4 or 8 vectors, the fewest that hold the chunk. Below kLnStagedMinFill
-// the spread kernel takes the row, if its own chunks hold at least kLnSpreadMinChunk
-// vectors (its per-row cost of two cluster exchanges and three sweeps over shared memory
-// pays off only over long chunks). Measured on GB300 (L2-cold, graphs of back-to-back
-// launches, of the measured HBM peak), staged against spread: bf16 512 x 140000 (chunks
-// of 1094 vectors, 8 a thread: 0.53 full) 0.45 / 0.62, 256 x 200000 (0.76) 0.54 / 0.60,
-// 2048 x 36000 (0.55) 0.58 / 0.70, 4096 x 36864 (0.56) 0.65 / 0.78, 1024 x 65544 (0.50)
-// 0.53 / 0.69, fp32 512 x 70000 (0.53) 0.54 / 0.61, 1024 x 40000 (0.61) 0.71 / 0.73; with
-// short spread chunks the staged kernel wins (bf16 1024 x 24576: 1536 of 2048 slots
-// against one CTA of 3072, 0.62 / 0.55; 1024 x 20480 0.58 / 0.51), and at full chunks it
-// mostly does (512 x 131072 0.69 / 0.65, 1024 x 32768 0.67 / 0.61, fp16 1024 x 65536 0.68 /
-// 0.67, fp32 1024 x 32768 0.85 / 0.72; bf16 1024 x 65536 0.66 / 0.72 is the exception).
+// each thread 1, 2, 4 or 8 vectors, the fewest that hold the chunk. In fp32 storage (16-bit
+// rows take the spread kernel in any case, see ln_plan), below kLnStagedMinFill the spread
+// kernel takes the row, if its own chunks hold at least kLnSpreadMinChunk vectors (its
+// per-row cost of two cluster exchanges and three sweeps over shared memory pays off only
+// over long chunks). Measured on GB300 (L2-cold, graphs of back-to-back launches, of the
+// measured HBM peak), fp32, staged against spread: 512 x 70000 (chunks of 1094 vectors, 8 a
+// thread: 0.53 full) 0.54 / 0.60, 1024 x 40000 (0.61) 0.71 / 0.73; with a short spread chunk
+// the staged kernel keeps the row (1024 x 12288: 768 of 1024 slots against one CTA of 3072,
+// 0.70 / 0.53), and at full chunks it wins (1024 x 32768 0.85 / 0.72).
 constexpr double kLnStagedMinFill = 0.8;
 constexpr int64_t kLnSpreadMinChunk = 4096;
 
@@ -1360,6 +1357,12 @@ camp_status_t ln_plan(const LnCall& c, const camp_plan_t* forced, camp_plan_t* p
                              (nvec16 > kLnStagedFewFrom && rc.a.rows <= kLnFewRows))) {
             int cl = 0, st = 0, rps = 0;
             int64_t chunk = 0;
+            // 16-bit storage: the spread kernel, three CTAs an SM with whole chunks in shared
+            // memory. Against the staged kernel (GB300, graphs of back-to-back launches,
+            // L2-cold, of the measured HBM peak) it was as fast within 0.01 or faster at 20
+            // of 22 shapes: bf16 1024 x 65536 0.75 / 0.66, 2048 x 65536 0.80 / 0.71, 4096 x
+            // 36864 0.80 / 0.65, 512 x 140000 0.67 / 0.46, fp16 1024 x 65536 0.72 / 0.68;
+            // slower only at 16 and 64 rows of 262144 (0.33 / 0.35, 0.49 / 0.51).
             if (es == 2 && spread_choose(nvec16, rc.a.rows, ln_per_sm, &cl, &st, &chunk)) {
                 spread_plan_fields(rc.a.rows, CAMP_KERNEL_LAYERNORM_SPREAD, ln_per_sm, cl, st,
                                    chunk, p);
