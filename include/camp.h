@@ -281,12 +281,13 @@ CAMP_API camp_status_t camp_rope_tables(float* sin, float* cos, int64_t max_pos,
  * y = fma(d * rsqrt(var + eps), gamma, beta), rounded once to the storage type. Rows of
  * more than 4096 16-byte vectors (32768 bf16/f16 / 16384 fp32 columns), or of more than
  * 2048 when there are at most 1024 rows (all pointers and the row pitch 16-byte aligned),
- * are staged in shared memory by persistent clusters of CTAs instead (up to 16 x 2048
- * vectors: 262144 bf16/f16 / 131072 fp32 columns). Wider rows (and staged rows whose
- * chunks would leave a fifth or more of the threads' vector slots empty) are spread over a
- * cluster of up to 16 CTAs, each holding its whole chunk in shared memory (up to about
- * 1.7 M bf16 columns); rows wider still, and rows past 16384 columns on the element path,
- * take one CTA per row (any width). In 16-bit storage any of these kernels may take the
+ * leave the registers: in 16-bit storage they are spread over a cluster of up to 16 CTAs,
+ * each holding its whole chunk of the row in shared memory (up to about 1.7 M columns); in
+ * fp32 they are staged in shared memory by persistent clusters of CTAs (up to 16 x 2048
+ * vectors: 131072 columns), and spread like 16-bit rows where the staged chunks would
+ * leave a fifth or more of the threads' vector slots empty, or past the staged kernel.
+ * Rows wider still, and rows past 16384 columns on the element path, take one CTA per row
+ * (any width). In 16-bit storage any of these kernels may take the
  * variance as sum((x - K)^2) / n - mu^2 (one pass) for a row where mu^2 <= 4 times that
  * value. Errors as for camp_rmsnorm.
  */
