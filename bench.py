@@ -582,6 +582,8 @@ LARGE_CASES = [
      (1024, 32768, "f32")),
     ("rmsnorm bf16 [1024,262152] (a cluster per row, chunks in shared memory)", "rms",
      (1024, 262152, False, 1e-5)),
+    ("add_rmsnorm bf16 [256,300000] (a cluster per row, x and r in shared memory)", "add",
+     (256, 300000)),
     ("layernorm bf16 [1024,262152] (a cluster per row, chunks in shared memory)", "ln",
      (1024, 262152)),
     ("layernorm bf16 [512,140000] (ragged staged chunks: a cluster per row)", "ln",

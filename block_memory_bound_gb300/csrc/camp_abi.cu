@@ -382,27 +382,28 @@ bool rms_choose_staged(const RmsCall& c, int64_t nvec, int* cluster, int* stages
 // (rows of up to about 1.7 M bf16 columns). The limit is the chunk at which shared memory
 // (228 KB an SM, 1 KB of it reserved a CTA, and under 1 KB of static arrays) still holds
 // as many CTAs an SM as the registers allow: 3 (73 KB chunks), or 2 for fp32 LayerNorm
-// (109 KB). The plan's grid counts no more resident CTAs than that.
+// (109 KB). The plan's grid counts no more resident CTAs than that. On RMSNorm's residual-
+// add path (`staged` = 2: x and r in shared memory) the limit is halved.
 constexpr int64_t spread_chunk_max(int per_sm) { return per_sm >= 3 ? 4700 : 7000; }
 
-bool spread_fits(int64_t nvec, int cluster, int stages, int64_t* chunk) {
+bool spread_fits(int64_t nvec, int cluster, int stages, int64_t* chunk, int staged = 1) {
     if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1)) != 0) return false;
     if (stages < 1 || stages > camp::kSpreadMaxStages) return false;
     *chunk = ceil_div(nvec, cluster);
-    return camp::spread_smem_bytes(*chunk, stages) <= camp::kStagedSmemMax;
+    return camp::spread_smem_bytes(*chunk, stages, staged) <= camp::kStagedSmemMax;
 }
 
 bool spread_choose(int64_t nvec, int64_t rows, int per_sm, int* cluster, int* stages,
-                   int64_t* chunk) {
+                   int64_t* chunk, int staged = 1) {
     for (int cl = 1; cl <= 16; cl *= 2) {
-        if ((ceil_div(nvec, cl) <= spread_chunk_max(per_sm) || cl == 16) &&
-            spread_fits(nvec, cl, 1, chunk)) {
+        if ((ceil_div(nvec, cl) <= spread_chunk_max(per_sm) / staged || cl == 16) &&
+            spread_fits(nvec, cl, 1, chunk, staged)) {
             // So few rows that their CTAs would leave half the SMs idle: split each row
             // further (GB300, bf16: 5 x 40000 0.03 -> 0.05, fp32 3 x 131080 0.11 -> 0.14;
             // splitting while the rows' CTAs fill fewer than all resident slots lost at
             // 32 x 131072, 0.36 -> 0.25, and 100 x 100000, 0.51 -> 0.44).
             while (cl < 16 && rows * cl < camp::kSmCount / 2) cl *= 2;
-            spread_fits(nvec, cl, 1, chunk);
+            spread_fits(nvec, cl, 1, chunk, staged);
             *cluster = cl;
             *stages = 1;
             return true;
@@ -412,19 +413,24 @@ bool spread_choose(int64_t nvec, int64_t rows, int per_sm, int* cluster, int* st
 }
 
 void spread_plan_fields(int64_t rows, int kernel, int per_sm_regs, int cluster, int stages,
-                        int64_t chunk, camp_plan_t* p) {
+                        int64_t chunk, camp_plan_t* p, int staged = 1) {
     p->kernel = kernel;
     p->vec_bytes = 16;
     p->group = static_cast<int32_t>(chunk);
     p->per_thread = stages;
     p->block = camp::kSpreadBlock;
     p->cluster = cluster;
-    int64_t per_sm = camp::kSmSmemBytes / (camp::spread_smem_bytes(chunk, stages) + 2048);
+    int64_t per_sm = camp::kSmSmemBytes / (camp::spread_smem_bytes(chunk, stages, staged) + 2048);
     if (per_sm > per_sm_regs) per_sm = per_sm_regs;
     int64_t clusters = (camp::kSmCount * (per_sm < 1 ? 1 : per_sm)) / cluster;
     if (clusters < 1) clusters = 1;
     if (clusters > rows) clusters = rows;
     p->grid = clusters * cluster;
+}
+
+// CTAs an SM the spread kernel's registers allow for this call (fewer with the residual add).
+int rms_spread_per_sm(const RmsCall& c) {
+    return camp::spread_ctas_per_sm(false, camp::elem_bytes(c.t), c.add);
 }
 
 void rms_plan(const RmsCall& c, camp_plan_t* p) {
@@ -437,11 +443,11 @@ void rms_plan(const RmsCall& c, camp_plan_t* p) {
     const int64_t cluster_from = c.add ? kClusterFrom / 2 : kClusterFrom;
     if (p->vec_bytes == 16 && nvec > kStagedFrom && rms_choose_staged(c, nvec, &cl, &st, &chunk)) {
         rms_staged_plan_fields(c, cl, st, chunk, p);
-    } else if (p->vec_bytes == 16 && !c.add && nvec > kStagedFrom &&
-               spread_choose(nvec, c.a.rows, camp::spread_ctas_per_sm(false, camp::elem_bytes(c.t)),
-                             &cl, &st, &chunk)) {
-        spread_plan_fields(c.a.rows, CAMP_KERNEL_RMSNORM_SPREAD,
-                           camp::spread_ctas_per_sm(false, camp::elem_bytes(c.t)), cl, st, chunk, p);
+    } else if (p->vec_bytes == 16 && nvec > kStagedFrom &&
+               spread_choose(nvec, c.a.rows, rms_spread_per_sm(c), &cl, &st, &chunk,
+                             c.add ? 2 : 1)) {
+        spread_plan_fields(c.a.rows, CAMP_KERNEL_RMSNORM_SPREAD, rms_spread_per_sm(c), cl, st,
+                           chunk, p, c.add ? 2 : 1);
     } else if (p->vec_bytes == 16 && nvec > cluster_from && rms_choose_cluster(c, nvec, &cl, &nv)) {
         p->kernel = CAMP_KERNEL_RMSNORM_CLUSTER;
         p->group = cl * camp::kClusterBlock;
@@ -503,11 +509,10 @@ camp_status_t rms_accept_plan(const RmsCall& c, const camp_plan_t& in, camp_plan
     }
     if (in.kernel == CAMP_KERNEL_RMSNORM_SPREAD) {
         int64_t chunk = 0;
-        if (vb != 16 || c.add || !spread_fits(nvec, in.cluster, in.per_thread, &chunk))
+        if (vb != 16 || !spread_fits(nvec, in.cluster, in.per_thread, &chunk, c.add ? 2 : 1))
             return CAMP_ERR_NOT_SUPPORTED;
-        spread_plan_fields(c.a.rows, CAMP_KERNEL_RMSNORM_SPREAD,
-                           camp::spread_ctas_per_sm(false, camp::elem_bytes(c.t)), in.cluster,
-                           in.per_thread, chunk, p);
+        spread_plan_fields(c.a.rows, CAMP_KERNEL_RMSNORM_SPREAD, rms_spread_per_sm(c),
+                           in.cluster, in.per_thread, chunk, p, c.add ? 2 : 1);
         return CAMP_SUCCESS;
     }
     if (in.kernel == CAMP_KERNEL_RMSNORM_WIDE) {
@@ -533,7 +538,7 @@ camp_status_t rms_launch(const RmsCall& c, const camp_plan_t& p, cudaStream_t s)
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_STAGED) {
         e = camp::rmsnorm_staged_launch(c.add, c.t, p.cluster, p.per_thread, c.a, s);
     } else if (p.kernel == CAMP_KERNEL_RMSNORM_SPREAD) {
-        e = camp::rmsnorm_spread_launch(c.t, p.cluster, p.per_thread, c.a, s);
+        e = camp::rmsnorm_spread_launch(c.add, c.t, p.cluster, p.per_thread, c.a, s);
     }
     return runtime_status(e);
 }
@@ -1738,7 +1743,7 @@ CAMP_API camp_status_t camp_rmsnorm_wait_probe(const void* x, const void* w, voi
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.kernel == CAMP_KERNEL_RMSNORM_SPREAD)
         return runtime_status(
-            camp::rmsnorm_spread_launch(c.t, p.cluster, p.per_thread, c.a, s, wait_ns, 1));
+            camp::rmsnorm_spread_launch(false, c.t, p.cluster, p.per_thread, c.a, s, wait_ns, 1));
     return runtime_status(
         camp::rmsnorm_staged_launch(false, c.t, p.cluster, p.per_thread, c.a, s, wait_ns, 1));
 }

@@ -141,15 +141,16 @@ constexpr int kSpreadHeadBytes = 16 * (kSpreadBlock / 32);   // a row head copy 
 // CTAs an SM the launch bounds guarantee by registers (fp32 LayerNorm keeps more live than
 // 40 registers hold without spilling); the plan's grid estimate counts no more resident
 // CTAs than this.
-constexpr int spread_ctas_per_sm(bool layernorm, int elem_bytes) {
-    return layernorm && elem_bytes == 4 ? 2 : 3;
+constexpr int spread_ctas_per_sm(bool layernorm, int elem_bytes, bool add = false) {
+    return (layernorm && elem_bytes == 4) || add ? 2 : 3;
 }
-inline int64_t spread_smem_bytes(int64_t chunk_vecs, int stages) {
-    return stages * (kSpreadHeadBytes + chunk_vecs * 16);
+// `staged`: tensors staged a row, 1 (x), or 2 (x and r) on RMSNorm's residual-add path.
+inline int64_t spread_smem_bytes(int64_t chunk_vecs, int stages, int staged = 1) {
+    return stages * (kSpreadHeadBytes + staged * chunk_vecs * 16);
 }
-cudaError_t rmsnorm_spread_launch(DType t, int cluster, int stages, const RmsnormArgs& a,
-                                  cudaStream_t s, unsigned long long wait_ns = 1000000000ull,
-                                  int probe = 0);
+cudaError_t rmsnorm_spread_launch(bool add, DType t, int cluster, int stages,
+                                  const RmsnormArgs& a, cudaStream_t s,
+                                  unsigned long long wait_ns = 1000000000ull, int probe = 0);
 struct LayernormArgs;
 // `wait_ns` bounds every mbarrier wait (one second in normal calls); `probe` != 0 leaves each
 // CTA's first row copy unissued (the wait diagnostic), as for layernorm_staged_launch.

@@ -65,16 +65,22 @@ __host__ __device__ constexpr int spread_copy_groups(bool layernorm, int elem_by
 
 // Several CTAs an SM by registers (40 a thread, 64 for fp32 LayerNorm), so that one CTA's
 // row can compute while another's lands even with a single buffer each.
-template <typename S, bool LN>
-__global__ void __launch_bounds__(kSpreadBlock, spread_ctas_per_sm(LN, Storage<S>::kBytes))
-norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __restrict__ beta,
-                   void* y, int64_t rows, int64_t cols, float eps, int chunk_vecs,
-                   int stages, unsigned long long wait_ns, int probe) {
+// ADD (RMSNorm only): h = x + r, rounded once to the storage type, is stored and normalized,
+// as camp_add_rmsnorm defines it; x and r are both staged, and h is formed again from them
+// for the output sweep (the same rounding, so the same bits) instead of being re-read.
+template <typename S, bool LN, bool ADD>
+__global__ void __launch_bounds__(kSpreadBlock, spread_ctas_per_sm(LN, Storage<S>::kBytes, ADD))
+norm_spread_kernel(const void* x, const void* r, void* h, const void* __restrict__ w,
+                   const void* __restrict__ beta, void* y, int64_t rows, int64_t cols,
+                   float eps, int chunk_vecs, int stages, unsigned long long wait_ns,
+                   int probe) {
     namespace cg = cooperative_groups;
     using C = Codec<S, 16>;
     constexpr int E = C::kElems;
     constexpr int ES = Storage<S>::kBytes;
     constexpr bool kOnePass = ES == 2;   // LayerNorm: one-pass statistics where they hold
+    static_assert(!(LN && ADD), "the residual add is an RMSNorm path");
+    constexpr int NB = ADD ? 2 : 1;   // staged tensors: x (and r)
     constexpr int kGroups = spread_copy_groups(LN, ES);
     constexpr int GS = kSpreadBlock / kGroups;   // threads a copy group
     // Independent packed accumulators a thread: two for 16-bit LayerNorm (two sums a pair
@@ -83,7 +89,8 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     constexpr int kAcc = (LN && ES == 2) ? 2 : 4;
 
     // Dynamic shared memory: `stages` buffers, each kSpreadHeadBytes of row heads (a copy of
-    // the row's first 16 bytes a group, for the LayerNorm shift) and then the chunk.
+    // the row's first 16 bytes a group, for the LayerNorm shift) and then the chunk (of x,
+    // then of r on the add path).
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[kSpreadMaxStages][kGroups];
     __shared__ __align__(8) unsigned long long bar_x[2], bar_z[2];
@@ -115,7 +122,9 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     const int g_lo = g * seg < my_vecs ? g * seg : my_vecs;
     const int g_len = my_vecs - g_lo < seg ? my_vecs - g_lo : seg;
     const int64_t pitch = cols * ES;
-    const uint32_t stage_bytes = kSpreadHeadBytes + static_cast<uint32_t>(chunk_vecs) * 16u;
+    const uint32_t stage_bytes =
+        kSpreadHeadBytes + static_cast<uint32_t>(NB) * static_cast<uint32_t>(chunk_vecs) * 16u;
+    const uint32_t r_off = static_cast<uint32_t>(chunk_vecs) * 16u;   // r's chunk after x's
     // The launcher refuses grids that would give a cluster more than INT_MAX rows.
     const int my_rows = cid < rows ? static_cast<int>((rows - cid + ncl - 1) / ncl) : 0;
 
@@ -131,8 +140,12 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
         // The inputs the first bulk loads and output pass will read (after griddep_wait).
         prefetch_l2(static_cast<const char*>(w) + v0 * 16, my_bytes);
         if constexpr (LN) prefetch_l2(static_cast<const char*>(beta) + v0 * 16, my_bytes);
-        for (int s = 0; s < stages && s < my_rows; ++s)
+        for (int s = 0; s < stages && s < my_rows; ++s) {
             prefetch_l2(static_cast<const char*>(x) + (cid + s * ncl) * pitch + v0 * 16, my_bytes);
+            if constexpr (ADD)
+                prefetch_l2(static_cast<const char*>(r) + (cid + s * ncl) * pitch + v0 * 16,
+                            my_bytes);
+        }
     }
     // Every CTA of the cluster has started and initialized its barriers before any CTA
     // stores into a peer's shared memory (split cluster barrier).
@@ -143,18 +156,23 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     griddep_launch_dependents();
 
     const char* xb = static_cast<const char*>(x);
-    // The group's first thread: its segment of row j (and, for LayerNorm, the row's first
-    // 16 bytes) into ring slot s, counted on the group's own barrier.
+    const char* rb = ADD ? static_cast<const char*>(r) : nullptr;
+    // The group's first thread: its segment of row j (of x, and of r on the add path; for
+    // LayerNorm also the row's first 16 bytes) into ring slot s, counted on the group's own
+    // barrier.
     auto issue = [&](int j, int s) {
-        const char* src = xb + (cid + static_cast<int64_t>(j) * ncl) * pitch;
+        const int64_t off = (cid + static_cast<int64_t>(j) * ncl) * pitch;
         const uint32_t bar = smem_u32(&full[s][g]);
         const uint32_t base = smem_u32(smem) + static_cast<uint32_t>(s) * stage_bytes;
         const uint32_t g_bytes = static_cast<uint32_t>(g_len) * 16u;
-        mbar_arrive_expect_tx(bar, (LN ? 16u : 0u) + g_bytes);
+        mbar_arrive_expect_tx(bar, (LN ? 16u : 0u) + NB * g_bytes);
         if (probe && j == 0) return;   // diagnostic: this copy is never issued
-        if constexpr (LN) bulk_load(base + g * 16, src, 16u, bar);
-        if (g_bytes > 0)
-            bulk_load(base + kSpreadHeadBytes + g_lo * 16, src + (v0 + g_lo) * 16, g_bytes, bar);
+        if constexpr (LN) bulk_load(base + g * 16, xb + off, 16u, bar);
+        if (g_bytes > 0) {
+            const uint32_t dst = base + kSpreadHeadBytes + g_lo * 16;
+            bulk_load(dst, xb + off + (v0 + g_lo) * 16, g_bytes, bar);
+            if constexpr (ADD) bulk_load(dst + r_off, rb + off + (v0 + g_lo) * 16, g_bytes, bar);
+        }
     };
     if (gt == 0) {
         for (int j = 0; j < stages && j < my_rows; ++j) issue(j, j);
@@ -180,10 +198,18 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
         const uint32_t slot = static_cast<uint32_t>(s) * stage_bytes;
         const unsigned char* segp = smem + slot + kSpreadHeadBytes + g_lo * 16;
         const uint32_t sega = smem_at + slot + kSpreadHeadBytes + g_lo * 16;
-        auto ldv = [&](int v) -> Raw<16> {   // vector v of the group's segment
-            if constexpr (kGroups == 1) return ld_smem16(segp + v * 16);
-            else return ld_smem16_at(sega + v * 16);
+        auto ld1 = [&](int v, uint32_t o) -> Raw<16> {   // vector v of a staged segment
+            if constexpr (kGroups == 1) return ld_smem16(segp + o + v * 16);
+            else return ld_smem16_at(sega + o + v * 16);
         };
+        // Vector v of the row the operator normalizes: x, or h = x + r on the add path.
+        auto ldv = [&](int v) -> Raw<16> {
+            if constexpr (ADD) return C::add(ld1(v, 0), ld1(v, r_off));
+            else return ld1(v, 0);
+        };
+        char* hr = ADD ? static_cast<char*>(h) + (cid + static_cast<int64_t>(j) * ncl) * pitch +
+                             (v0 + g_lo) * 16
+                       : nullptr;
 
         // 2. This thread's sums over its vectors of the segment.
         float shift = 0.0f;
@@ -205,7 +231,9 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
                 for (int a = 0; a < kAcc; ++a) {
                     const int vj = vi + a * GS;
                     if (vj < g_len) {
-                        C::each_pair(ldv(vj), [&](int, f32x2 p) {
+                        const Raw<16> v = ldv(vj);
+                        if constexpr (ADD) st_out<16>(hr + static_cast<int64_t>(vj) * 16, v);
+                        C::each_pair(v, [&](int, f32x2 p) {
                             if constexpr (!LN) {
                                 acc1[a] = f2_fma(p, p, acc1[a]);
                             } else {
@@ -368,15 +396,15 @@ norm_spread_kernel(const void* x, const void* __restrict__ w, const void* __rest
     }
 }
 
-template <typename S, bool LN>
-cudaError_t launch_spread(const void* x, const void* w, const void* beta, void* y, int64_t rows,
-                          int64_t cols, float eps, int cluster, int stages,
-                          unsigned long long wait_ns, int probe, cudaStream_t s) {
-    auto kernel = norm_spread_kernel<S, LN>;
+template <typename S, bool LN, bool ADD>
+cudaError_t launch_spread(const void* x, const void* r, void* h, const void* w, const void* beta,
+                          void* y, int64_t rows, int64_t cols, float eps, int cluster,
+                          int stages, unsigned long long wait_ns, int probe, cudaStream_t s) {
+    auto kernel = norm_spread_kernel<S, LN, ADD>;
     constexpr int E = 16 / Storage<S>::kBytes;
     const int64_t nvec = cols / E;
     const int chunk = static_cast<int>((nvec + cluster - 1) / cluster);
-    const size_t smem = static_cast<size_t>(spread_smem_bytes(chunk, stages));
+    const size_t smem = static_cast<size_t>(spread_smem_bytes(chunk, stages, ADD ? 2 : 1));
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -405,43 +433,48 @@ cudaError_t launch_spread(const void* x, const void* w, const void* beta, void* 
     const int64_t ncl = rows < active ? rows : active;
     if ((rows + ncl - 1) / ncl > INT_MAX) return cudaErrorInvalidValue;   // 32-bit row counters
     cfg.gridDim = dim3(static_cast<unsigned>(ncl * cluster));
-    return cudaLaunchKernelEx(&cfg, kernel, x, w, beta, y, rows, cols, eps, chunk, stages,
+    return cudaLaunchKernelEx(&cfg, kernel, x, r, h, w, beta, y, rows, cols, eps, chunk, stages,
                               wait_ns, probe);
 }
 
-template <bool LN>
-cudaError_t spread_dtype(DType t, const void* x, const void* w, const void* beta, void* y,
-                         int64_t rows, int64_t cols, float eps, int cluster, int stages,
-                         unsigned long long wait_ns, int probe, cudaStream_t s) {
+template <bool LN, bool ADD>
+cudaError_t spread_dtype(DType t, const void* x, const void* r, void* h, const void* w,
+                         const void* beta, void* y, int64_t rows, int64_t cols, float eps,
+                         int cluster, int stages, unsigned long long wait_ns, int probe,
+                         cudaStream_t s) {
     switch (t) {
         case DType::BF16:
-            return launch_spread<bf16_t, LN>(x, w, beta, y, rows, cols, eps, cluster, stages,
-                                             wait_ns, probe, s);
+            return launch_spread<bf16_t, LN, ADD>(x, r, h, w, beta, y, rows, cols, eps, cluster,
+                                                  stages, wait_ns, probe, s);
         case DType::F16:
-            return launch_spread<f16_t, LN>(x, w, beta, y, rows, cols, eps, cluster, stages,
-                                            wait_ns, probe, s);
+            return launch_spread<f16_t, LN, ADD>(x, r, h, w, beta, y, rows, cols, eps, cluster,
+                                                 stages, wait_ns, probe, s);
         default:
-            return launch_spread<f32_t, LN>(x, w, beta, y, rows, cols, eps, cluster, stages,
-                                            wait_ns, probe, s);
+            return launch_spread<f32_t, LN, ADD>(x, r, h, w, beta, y, rows, cols, eps, cluster,
+                                                 stages, wait_ns, probe, s);
     }
 }
 
 }  // namespace
 
-cudaError_t rmsnorm_spread_launch(DType t, int cluster, int stages, const RmsnormArgs& a,
-                                  cudaStream_t s, unsigned long long wait_ns, int probe) {
+cudaError_t rmsnorm_spread_launch(bool add, DType t, int cluster, int stages,
+                                  const RmsnormArgs& a, cudaStream_t s,
+                                  unsigned long long wait_ns, int probe) {
     if (cluster < 1 || cluster > 16 || stages < 1 || stages > kSpreadMaxStages)
         return cudaErrorInvalidValue;
-    return spread_dtype<false>(t, a.x, a.w, nullptr, a.y, a.rows, a.cols, a.eps, cluster, stages,
-                               wait_ns, probe, s);
+    if (add)
+        return spread_dtype<false, true>(t, a.x, a.r, a.h, a.w, nullptr, a.y, a.rows, a.cols,
+                                         a.eps, cluster, stages, wait_ns, probe, s);
+    return spread_dtype<false, false>(t, a.x, nullptr, nullptr, a.w, nullptr, a.y, a.rows,
+                                      a.cols, a.eps, cluster, stages, wait_ns, probe, s);
 }
 
 cudaError_t layernorm_spread_launch(DType t, int cluster, int stages, const LayernormArgs& a,
                                     cudaStream_t s, unsigned long long wait_ns, int probe) {
     if (cluster < 1 || cluster > 16 || stages < 1 || stages > kSpreadMaxStages)
         return cudaErrorInvalidValue;
-    return spread_dtype<true>(t, a.x, a.gamma, a.beta, a.y, a.rows, a.cols, a.eps, cluster,
-                              stages, wait_ns, probe, s);
+    return spread_dtype<true, false>(t, a.x, nullptr, nullptr, a.gamma, a.beta, a.y, a.rows,
+                                     a.cols, a.eps, cluster, stages, wait_ns, probe, s);
 }
 
 cudaError_t read_spread_device_errors(unsigned int* flags, bool clear) {

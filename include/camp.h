@@ -337,9 +337,9 @@ typedef enum {
     CAMP_KERNEL_LAYERNORM_STAGED = 12, /* camp_layernorm: the same, for the widest rows */
     CAMP_KERNEL_LAYERNORM_WIDE = 13, /* camp_layernorm: one CTA per row, block-stride sweeps
                                         over x, for rows no other kernel holds (any width) */
-    CAMP_KERNEL_RMSNORM_SPREAD = 14, /* camp_rmsnorm: a cluster of CTAs per row, each holding
-                                        its whole chunk in shared memory (rows past the
-                                        staged kernel) */
+    CAMP_KERNEL_RMSNORM_SPREAD = 14, /* camp_rmsnorm and camp_add_rmsnorm: a cluster of CTAs
+                                        per row, each holding its whole chunk (of x, and of
+                                        r) in shared memory (rows past the staged kernel) */
     CAMP_KERNEL_LAYERNORM_SPREAD = 15 /* camp_layernorm: the same */
 } camp_kernel_t;
 

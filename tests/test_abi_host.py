@@ -994,3 +994,17 @@ def test_rmsnorm_wait_probe_refusals_launch_nothing(lib):
         assert f(X, W, Y, 4, 65536, eps, camp.BF16, ctypes.byref(plan), 100_000, None) == \
             camp.ERR_NOT_SUPPORTED, plan
     assert f(X, W, Y, 0, 65536, eps, camp.BF16, None, 100_000, None) == camp.SUCCESS
+
+
+@pytest.mark.parametrize("rows,cols,dtype,cluster,chunk,grid", [
+    (256, 300000, "bf16", 16, 2344, 304),   # x and r staged: chunks of at most 3500 vectors
+    (1024, 262152, "bf16", 16, 2049, 304),  # two CTAs an SM with the add
+    (64, 524296, "bf16", 16, 4097, 144),    # 2 x 64 KB a CTA: one an SM
+    (3, 131080, "f32", 16, 2049, 48),
+])
+def test_add_rmsnorm_rows_past_the_staged_kernel_take_the_spread_kernel(lib, rows, cols, dtype,
+                                                                        cluster, chunk, grid):
+    R, H = 0x7F3000000000, 0x7F4000000000
+    p = camp.camp_add_rmsnorm_plan(X, R, W, H, Y, rows, cols, dtype)
+    assert (p.kernel, p.vec_bytes, p.cluster, p.group, p.per_thread, p.block, p.grid) == \
+        (camp.KERNEL_RMSNORM_SPREAD, 16, cluster, chunk, 1, 512, grid)

@@ -14,6 +14,7 @@ import torch
 from block_memory_bound_gb300 import camp
 from parity import DTYPES, ES
 
+import test_add_rmsnorm_gpu as add_tests
 import test_layernorm_gpu as ln_tests
 import test_rmsnorm_gpu as rms_tests
 
@@ -137,6 +138,30 @@ def test_rows_past_a_round_of_clusters(kind, rows, cols, dtype, plan):
         ln_tests.run_case(rows, cols, dtype, seed=rows % 11, plan=p)
     else:
         rms_tests.run_case(rows, cols, dtype, seed=rows % 11, plan=p)
+
+
+# ------------------------------------------------------------------ the residual add
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("stages", [1, 2])
+def test_add_every_variant(dtype, cluster, stages):
+    # x and r staged, h stored from the statistics sweep and formed again for the output
+    e = 16 // ES[dtype]
+    add_tests.run_case(7, (cluster * 1300 - 7) * e, dtype, seed=cluster + stages,
+                       plan=rms_plan(cluster, stages))
+
+
+@pytest.mark.parametrize("alias", ["h=r,y=x", "h=x,y=r"])
+def test_add_in_place(alias):
+    add_tests.run_case(21, 16 * 2100 * 8, "bf16", seed=5, plan=rms_plan(16, 2), alias=alias)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows,cols", [(3, 262152), (300, 280000)])
+def test_add_default_plan_past_the_staged_kernel(rows, cols, dtype):
+    # the planner's spread plan for the add path (its choice is pinned by the host tests)
+    add_tests.run_case(rows, cols, dtype, seed=cols % 7)
 
 
 def test_forced_plans_that_do_not_fit_are_refused():
