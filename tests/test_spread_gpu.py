@@ -78,12 +78,14 @@ def test_layernorm_rows_far_from_their_shift(dtype):
                           x_cpu=ln_tests._mixed_rows(rows, cols, dtype, stages))
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("plan", [None, (8, 1), (16, 2)])
-def test_rmsnorm_stress_rows(plan):
-    # the stress distribution (1% of rows x1e3, 1% x1e-4) on rows past the staged kernel:
-    # fp32 sums over a row spread across the cluster's CTAs
+def test_rmsnorm_stress_rows(plan, dtype):
+    # the stress distribution (1% of rows x1e3, 1% x1e-4; in fp16 partly subnormal) on rows
+    # past the staged kernel: fp32 sums over a row spread across the cluster's CTAs
     p = None if plan is None else rms_plan(*plan)
-    rms_tests.run_case(200, 262152, "bf16", eps=1e-6, seed=4, stress=True, plan=p)
+    cols = 262152 if ES[dtype] == 2 else 131076
+    rms_tests.run_case(200, cols, dtype, eps=1e-6, seed=4, stress=True, plan=p)
 
 
 def test_rmsnorm_constant_rows_match_closed_form_within_tolerance():
